@@ -1,0 +1,147 @@
+"""Sequential CPU oracle for the batched small dense solvers (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline / reference arm
+of ``bench.py`` may import this package. The CUDA library never links, loads or calls
+it, and it imports nothing from the CUDA side.
+
+The arithmetic lives in ``oracle.cpp`` (plain sequential C++, one system at a time, in
+the dtype of the inputs). This module only builds that file with g++ and marshals
+NumPy arrays: every function copies its inputs and returns new arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+ROW_MAJOR = 0
+COL_MAJOR = 1
+
+
+def compile_library(src: str, out: str) -> str:
+    """g++ -O2 without FMA contraction or fast-math; writes ``out`` atomically."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-pthread", "-o", tmp, src]
+    subprocess.check_call(cmd)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.cpp into _build/liboracle.so if it is missing or stale."""
+    stale = (not os.path.exists(_SO)) or os.path.getmtime(_SO) < os.path.getmtime(_SRC)
+    if force or stale:
+        compile_library(_SRC, _SO)
+    return _SO
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the default one, or a variant)."""
+
+    def __init__(self, so_path: str):
+        lib = ctypes.CDLL(so_path)
+        i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+        for name in ("oracle_getrf_getrs_f32", "oracle_getrf_getrs_f64"):
+            getattr(lib, name).argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, vp, i32]
+            getattr(lib, name).restype = i32
+        for name in ("oracle_potrf_potrs_f32", "oracle_potrf_potrs_f64"):
+            getattr(lib, name).argtypes = [i32, i32, i32, i64, vp, vp, vp, i32]
+            getattr(lib, name).restype = i32
+        for name in ("oracle_bdsv_f32", "oracle_bdsv_f64"):
+            getattr(lib, name).argtypes = [i32, i32, i64, vp, vp, vp, i32]
+            getattr(lib, name).restype = i32
+        self.lib = lib
+
+    def getrf_getrs(self, A, B, layout: int = ROW_MAJOR, nthreads: int = 1):
+        """LU with partial pivoting + solve, one system at a time.
+
+        A: (batch, n, n) and B: raw storage in ``layout`` order (see gen.workloads).
+        Returns (LU, X, ipiv, info, tie_step) with LU/X in the inputs' storage order.
+        """
+        A = np.ascontiguousarray(A).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).copy()
+        batch, n = A.shape[0], A.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        ipiv = np.zeros((batch, n), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_getrs_" + _suffix(A.dtype))
+        rc = fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
+                nthreads)
+        if rc != 0:
+            raise ValueError("oracle getrf_getrs rejected its arguments")
+        return A, B, ipiv, info, tie
+
+    def potrf_potrs(self, A, B, layout: int = COL_MAJOR, nthreads: int = 1):
+        """Cholesky (lower fill) + solve, one system at a time. Returns (L, X, info)."""
+        A = np.ascontiguousarray(A).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).copy()
+        batch, n = A.shape[0], A.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_potrf_potrs_" + _suffix(A.dtype))
+        rc = fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(info), nthreads)
+        if rc != 0:
+            raise ValueError("oracle potrf_potrs rejected its arguments")
+        return A, B, info
+
+    def bdsv(self, strips, xpad, nthreads: int = 1):
+        """Block-tridiagonal block-Cholesky solve.
+
+        strips: (batch, nbr, bs, 3*bs) [L|D|R]; xpad: (batch, (nbr+2)*bs).
+        Returns (factored strips, padded solution, info).
+        """
+        S = np.ascontiguousarray(strips).copy()
+        X = np.ascontiguousarray(xpad, dtype=S.dtype).copy()
+        batch, nbr, bs = S.shape[0], S.shape[1], S.shape[2]
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_bdsv_" + _suffix(S.dtype))
+        rc = fn(nbr, bs, batch, _ptr(S), _ptr(X), _ptr(info), nthreads)
+        if rc != 0:
+            raise ValueError("oracle bdsv rejected its arguments")
+        return S, X, info
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def getrf_getrs(A, B, layout: int = ROW_MAJOR, nthreads: int = 1):
+    return default().getrf_getrs(A, B, layout, nthreads)
+
+
+def potrf_potrs(A, B, layout: int = COL_MAJOR, nthreads: int = 1):
+    return default().potrf_potrs(A, B, layout, nthreads)
+
+
+def bdsv(strips, xpad, nthreads: int = 1):
+    return default().bdsv(strips, xpad, nthreads)
+
+
+def _suffix(dtype) -> str:
+    dt = np.dtype(dtype)
+    if dt == np.float32:
+        return "f32"
+    if dt == np.float64:
+        return "f64"
+    raise TypeError(f"oracle supports float32/float64, not {dt}")
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)

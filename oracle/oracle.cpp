@@ -1,0 +1,374 @@
+// Sequential CPU oracle for the batched small dense solvers.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or calls this
+// file: only the test suite, the smoke check and the benchmark's CPU-baseline leg do.
+// It shares no source, header, table or helper with the CUDA library.
+//
+// Every routine solves one system at a time, in the arithmetic type of its inputs
+// (float or double), with the textbook operation order written out below. The batch
+// loops only hand whole systems to worker threads; the arithmetic of a system never
+// depends on the thread count.
+//
+// Arithmetic convention shared by every routine (where the pages leave rounding open):
+//   * a Schur/substitution update  a <- a - l*u  is one fused multiply-add (one rounding),
+//     i.e. std::fma(-l, u, a);
+//   * a scaling by a pivot p multiplies by the correctly rounded reciprocal r = 1/p;
+//   * nothing else is fused (the file is compiled with -ffp-contract=off).
+//
+// Sources (web pages):
+//   [TDLS]  TDLS API, "solver_static.hpp File Reference" (CooperativeLUppSolverStatic),
+//           Detailed Description: factorization, factored format, departures from MAGMA.
+//   [GLASS] GLASS API reference, "Block-tridiagonal Ops", sections "Direct solve
+//           (glass::bdsv)" and "Block-tridiagonal matrix-vector product".
+//   [RUDA]  RUDA docs, "ruSOLVER: small-matrix kernel optimisation", section on the
+//           unchanged numerical and failure contract.
+//   [cuSolverDx] cuSolverDx docs, "Cholesky Factorization" (POTRF).
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+template <typename T> struct Limits;
+template <> struct Limits<float> {
+  static float floor_() { return FLT_MIN; }
+};
+template <> struct Limits<double> {
+  static double floor_() { return DBL_MIN; }
+};
+
+// Element (r, c) of an n x m matrix stored row-major (layout 0) or column-major (1).
+inline int64_t at(int layout, int rows, int cols, int r, int c) {
+  return layout == 0 ? (int64_t)r * cols + c : (int64_t)c * rows + r;
+}
+
+// ---------------------------------------------------------------------------------
+// LU with partial pivoting, right-looking, in LAPACK's unblocked order ([TDLS]:
+// "the right-looking LU with partial pivoting of MAGMA's register-blocked small-system
+// kernel ... same operations, same order and, with relative_pivot_threshold = 1, same
+// pivot choice"), applied to A itself (P A = L U) whatever the storage order.
+//
+// Step k:
+//   1. pivot search over rows k..n-1 of column k: the first row of largest magnitude
+//      in the current row order (lowest-row tie rule, [RUDA]);
+//   2. ipiv[k] = p + 1 (1-based LAPACK swap sequence);
+//   3. a pivot with !(|pivot| >= smallest normal) is singular ([TDLS] singular_floor
+//      default); the first such step sets info = k + 1 and the sweep goes on with a
+//      pivot reciprocal of 1 ([TDLS]: "a pivot reciprocal of 1 keeps it finite");
+//   4. rows k and p are interchanged in A (whole rows, L part included) and in B;
+//   5. multipliers l_ik = a_ik * (1/a_kk) for i > k, stored in place of a_ik;
+//   6. rank-1 Schur update a_ij -= l_ik a_kj (i, j > k), and the forward solve
+//      b_i -= l_ik b_k folded into the same step ([TDLS]: "L y = P b folded into the
+//      factorization").
+// Then U x = y by back substitution, column by column from the last:
+//   x_k = y_k * (1/u_kk);  y_i -= u_ik x_k for i < k.
+// A system with info != 0 returns X = 0 ([RUDA] failed outputs zeroed); its factor
+// holds whatever the sweep produced.
+//
+// tie_step (optional) receives the first step whose two largest candidates lie within
+// 1e-6 relative of each other (a near tie, where a different rounding may legitimately
+// pick the other row), or -1.
+// ---------------------------------------------------------------------------------
+template <typename T>
+void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int32_t* info,
+                     int32_t* tie_step) {
+  const T floor_v = Limits<T>::floor_();
+  int32_t inf = 0;
+  int32_t tie = -1;
+  auto a = [&](int r, int c) -> T& { return A[at(layout, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
+
+  for (int k = 0; k < n; ++k) {
+    int p = k;
+    T best = std::fabs(a(k, k));
+    for (int i = k + 1; i < n; ++i) {
+      T v = std::fabs(a(i, k));
+      if (v > best) {
+        best = v;
+        p = i;
+      }
+    }
+    if (tie < 0 && best > T(0)) {
+      T second = T(-1);
+      for (int i = k; i < n; ++i) {
+        if (i == p) continue;
+        T v = std::fabs(a(i, k));
+        if (v > second) second = v;
+      }
+      if (second >= T(0) && (double)best - (double)second <= 1e-6 * (double)best) tie = k;
+    }
+    ipiv[k] = p + 1;
+    const bool ok = best >= floor_v;
+    if (!ok && inf == 0) inf = k + 1;
+    if (p != k) {
+      for (int c = 0; c < n; ++c) {
+        T t = a(k, c);
+        a(k, c) = a(p, c);
+        a(p, c) = t;
+      }
+      for (int c = 0; c < nrhs; ++c) {
+        T t = b(k, c);
+        b(k, c) = b(p, c);
+        b(p, c) = t;
+      }
+    }
+    const T r = ok ? T(1) / a(k, k) : T(1);
+    for (int i = k + 1; i < n; ++i) a(i, k) = a(i, k) * r;
+    for (int i = k + 1; i < n; ++i) {
+      const T l = a(i, k);
+      for (int j = k + 1; j < n; ++j) a(i, j) = std::fma(-l, a(k, j), a(i, j));
+      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));
+    }
+  }
+  for (int k = n - 1; k >= 0; --k) {
+    const T piv = a(k, k);
+    const T r = (std::fabs(piv) >= floor_v) ? T(1) / piv : T(1);
+    for (int c = 0; c < nrhs; ++c) {
+      const T x = b(k, c) * r;
+      b(k, c) = x;
+      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-a(i, k), x, b(i, c));
+    }
+  }
+  if (inf != 0) {
+    for (int r0 = 0; r0 < n; ++r0)
+      for (int c = 0; c < nrhs; ++c) b(r0, c) = T(0);
+  }
+  *info = inf;
+  if (tie_step) *tie_step = tie;
+}
+
+// ---------------------------------------------------------------------------------
+// Cholesky, lower fill, right-looking ([cuSolverDx] POTRF: only the lower triangle is
+// read and replaced by L, the upper part is untouched; info = the smallest leading
+// minor that is not positive definite). Column k:
+//   d = a_kk (already updated); !(d > 0) -> info = k + 1 and the remaining columns
+//   are left as they are; l_kk = sqrt(d); l_ik = a_ik * (1/l_kk) for i > k;
+//   a_ij -= l_ik l_jk for k < j <= i.
+// potrs: L y = b (column by column, y_k = b_k * (1/l_kk), b_i -= l_ik y_k for i > k),
+// then L^T x = y (from the last: x_k = y_k * (1/l_kk), y_i -= l_ki x_k for i < k).
+// A failed system returns X = 0.
+// ---------------------------------------------------------------------------------
+template <typename T>
+void potrf_potrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* info) {
+  int32_t inf = 0;
+  auto a = [&](int r, int c) -> T& { return A[at(layout, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
+  for (int k = 0; k < n; ++k) {
+    const T d = a(k, k);
+    if (!(d > T(0))) {
+      inf = k + 1;
+      break;
+    }
+    const T l = std::sqrt(d);
+    a(k, k) = l;
+    const T r = T(1) / l;
+    for (int i = k + 1; i < n; ++i) a(i, k) = a(i, k) * r;
+    for (int j = k + 1; j < n; ++j) {
+      const T ljk = a(j, k);
+      for (int i = j; i < n; ++i) a(i, j) = std::fma(-a(i, k), ljk, a(i, j));
+    }
+  }
+  if (inf != 0) {
+    for (int r0 = 0; r0 < n; ++r0)
+      for (int c = 0; c < nrhs; ++c) b(r0, c) = T(0);
+    *info = inf;
+    return;
+  }
+  for (int c = 0; c < nrhs; ++c) {
+    for (int k = 0; k < n; ++k) {
+      const T y = b(k, c) * (T(1) / a(k, k));
+      b(k, c) = y;
+      for (int i = k + 1; i < n; ++i) b(i, c) = std::fma(-a(i, k), y, b(i, c));
+    }
+    for (int k = n - 1; k >= 0; --k) {
+      const T x = b(k, c) * (T(1) / a(k, k));
+      b(k, c) = x;
+      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-a(k, i), x, b(i, c));
+    }
+  }
+  *info = 0;
+}
+
+// ---------------------------------------------------------------------------------
+// Block-tridiagonal SPD solve by the block-Cholesky (block-Thomas) sweep ([GLASS]
+// bdsv_factor / bdsv_solve / bdsv).
+// Layout ([GLASS]): block-row br is a bs x (3 bs) row-major strip [L | D | R] at
+// strips + br*3*bs*bs; slot (y, x) of sub-block s lives at strip[y*3bs + s*bs + x].
+// The vector is padded: (nbr + 2)*bs entries, block-row br at (br + 1)*bs.
+// Factor: F_0 = chol(D_0); for k > 0: E_k = L_k F_{k-1}^{-T}, F_k = chol(D_k - E_k E_k^T).
+//   MAIN <- F_k (lower triangle; the upper triangle keeps D_k), LEFT <- E_k, RIGHT is
+//   neither read nor written.
+// Solve: y_k = F_k^{-1}(b_k - E_k y_{k-1}), then x_k = F_k^{-T}(y_k - E_{k+1}^T x_{k+1}).
+// info = global index br*bs + j + 1 of the first failing diagonal of the sweep (the
+// dense Cholesky factor of the assembled matrix fails at the same index). GLASS only
+// raises a flag and runs the sweep on; this oracle stops at the first failure, the
+// strips beyond it are then unspecified and the solution is returned as zeros.
+// ---------------------------------------------------------------------------------
+template <typename T>
+void bdsv_one(int nbr, int bs, T* strips, T* xpad, int32_t* info) {
+  const int w = 3 * bs;
+  auto blk = [&](int br, int slot, int y, int x) -> T& {
+    return strips[(int64_t)br * bs * w + (int64_t)y * w + slot * bs + x];
+  };
+  const int LEFT = 0, MAIN = 1;
+  int32_t inf = 0;
+  std::vector<T> S((size_t)bs * bs), E((size_t)bs * bs);
+  for (int k = 0; k < nbr && inf == 0; ++k) {
+    // S = D_k (lower triangle), minus E_k E_k^T for k > 0.
+    for (int i = 0; i < bs; ++i)
+      for (int j = 0; j <= i; ++j) S[i * bs + j] = blk(k, MAIN, i, j);
+    if (k > 0) {
+      // E_k = L_k F_{k-1}^{-T}: row a solves e_a F^T = l_a, i.e. for j = 0..bs-1
+      // e_aj = (l_aj - sum_{m<j} e_am f_jm) * (1/f_jj).
+      for (int ar = 0; ar < bs; ++ar) {
+        for (int j = 0; j < bs; ++j) {
+          T s = blk(k, LEFT, ar, j);
+          for (int m = 0; m < j; ++m) s = std::fma(-E[ar * bs + m], blk(k - 1, MAIN, j, m), s);
+          E[ar * bs + j] = s * (T(1) / blk(k - 1, MAIN, j, j));
+        }
+      }
+      for (int i = 0; i < bs; ++i)
+        for (int j = 0; j <= i; ++j) {
+          T s = S[i * bs + j];
+          for (int m = 0; m < bs; ++m) s = std::fma(-E[i * bs + m], E[j * bs + m], s);
+          S[i * bs + j] = s;
+        }
+      for (int i = 0; i < bs; ++i)
+        for (int j = 0; j < bs; ++j) blk(k, LEFT, i, j) = E[i * bs + j];
+    }
+    // F_k = chol(S), right-looking as in potrf_potrs_one.
+    for (int c = 0; c < bs; ++c) {
+      const T d = S[c * bs + c];
+      if (!(d > T(0))) {
+        inf = k * bs + c + 1;
+        break;
+      }
+      const T l = std::sqrt(d);
+      S[c * bs + c] = l;
+      const T r = T(1) / l;
+      for (int i = c + 1; i < bs; ++i) S[i * bs + c] = S[i * bs + c] * r;
+      for (int j = c + 1; j < bs; ++j) {
+        const T ljc = S[j * bs + c];
+        for (int i = j; i < bs; ++i) S[i * bs + j] = std::fma(-S[i * bs + c], ljc, S[i * bs + j]);
+      }
+    }
+    for (int i = 0; i < bs; ++i)
+      for (int j = 0; j <= i; ++j) blk(k, MAIN, i, j) = S[i * bs + j];
+  }
+  T* x = xpad + bs;  // interior: block-row br at x + br*bs
+  if (inf != 0) {
+    for (int i = 0; i < nbr * bs; ++i) x[i] = T(0);
+    *info = inf;
+    return;
+  }
+  std::vector<T> z(bs);
+  // Forward sweep: z = b_k - E_k y_{k-1}; y_k = F_k^{-1} z.
+  for (int k = 0; k < nbr; ++k) {
+    for (int i = 0; i < bs; ++i) z[i] = x[k * bs + i];
+    if (k > 0)
+      for (int i = 0; i < bs; ++i)
+        for (int m = 0; m < bs; ++m) z[i] = std::fma(-blk(k, LEFT, i, m), x[(k - 1) * bs + m], z[i]);
+    for (int j = 0; j < bs; ++j) {
+      T s = z[j];
+      for (int m = 0; m < j; ++m) s = std::fma(-blk(k, MAIN, j, m), x[k * bs + m], s);
+      x[k * bs + j] = s * (T(1) / blk(k, MAIN, j, j));
+    }
+  }
+  // Backward sweep: w = y_k - E_{k+1}^T x_{k+1}; x_k = F_k^{-T} w.
+  for (int k = nbr - 1; k >= 0; --k) {
+    for (int i = 0; i < bs; ++i) z[i] = x[k * bs + i];
+    if (k < nbr - 1)
+      for (int m = 0; m < bs; ++m)
+        for (int i = 0; i < bs; ++i) z[m] = std::fma(-blk(k + 1, LEFT, i, m), x[(k + 1) * bs + i], z[m]);
+    for (int j = bs - 1; j >= 0; --j) {
+      T s = z[j];
+      for (int m = j + 1; m < bs; ++m) s = std::fma(-blk(k, MAIN, m, j), x[k * bs + m], s);
+      x[k * bs + j] = s * (T(1) / blk(k, MAIN, j, j));
+    }
+  }
+  *info = 0;
+}
+
+// Hands contiguous ranges of systems to nthreads workers (1 = the calling thread).
+template <typename F>
+void for_systems(int64_t batch, int nthreads, F&& f) {
+  if (nthreads <= 1 || batch < 2) {
+    for (int64_t s = 0; s < batch; ++s) f(s);
+    return;
+  }
+  if ((int64_t)nthreads > batch) nthreads = (int)batch;
+  std::vector<std::thread> pool;
+  pool.reserve(nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    const int64_t lo = batch * t / nthreads, hi = batch * (t + 1) / nthreads;
+    pool.emplace_back([lo, hi, &f] {
+      for (int64_t s = lo; s < hi; ++s) f(s);
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+template <typename T>
+int getrf_getrs_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
+                        int32_t* info, int32_t* tie_step, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0) return 1;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    getrf_getrs_one<T>(layout, n, nrhs, A + s * n * n, B + s * n * nrhs, ipiv + s * n, info + s,
+                       tie_step ? tie_step + s : nullptr);
+  });
+  return 0;
+}
+
+template <typename T>
+int potrf_potrs_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B, int32_t* info,
+                        int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0) return 1;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    potrf_potrs_one<T>(layout, n, nrhs, A + s * n * n, B + s * n * nrhs, info + s);
+  });
+  return 0;
+}
+
+template <typename T>
+int bdsv_batched(int nbr, int bs, int64_t batch, T* strips, T* xpad, int32_t* info, int nthreads) {
+  if (nbr < 1 || bs < 1 || batch < 0) return 1;
+  const int64_t sstride = (int64_t)nbr * bs * 3 * bs, vstride = (int64_t)(nbr + 2) * bs;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    bdsv_one<T>(nbr, bs, strips + s * sstride, xpad + s * vstride, info + s);
+  });
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_getrf_getrs_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
+                           int32_t* ipiv, int32_t* info, int32_t* tie_step, int nthreads) {
+  return getrf_getrs_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, nthreads);
+}
+int oracle_getrf_getrs_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
+                           int32_t* ipiv, int32_t* info, int32_t* tie_step, int nthreads) {
+  return getrf_getrs_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, nthreads);
+}
+int oracle_potrf_potrs_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
+                           int32_t* info, int nthreads) {
+  return potrf_potrs_batched<float>(layout, n, nrhs, batch, A, B, info, nthreads);
+}
+int oracle_potrf_potrs_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
+                           int32_t* info, int nthreads) {
+  return potrf_potrs_batched<double>(layout, n, nrhs, batch, A, B, info, nthreads);
+}
+int oracle_bdsv_f32(int nbr, int bs, int64_t batch, float* strips, float* xpad, int32_t* info,
+                    int nthreads) {
+  return bdsv_batched<float>(nbr, bs, batch, strips, xpad, info, nthreads);
+}
+int oracle_bdsv_f64(int nbr, int bs, int64_t batch, double* strips, double* xpad, int32_t* info,
+                    int nthreads) {
+  return bdsv_batched<double>(nbr, bs, batch, strips, xpad, info, nthreads);
+}
+
+}  // extern "C"

@@ -1,0 +1,453 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each pin takes an ``oracle.Oracle`` instance, so that the same checks run on the real
+oracle (test_oracle_pins.py) and on deliberately broken copies of it
+(test_oracle_mutations.py, which shows that every planted mistake trips a pin).
+A pin raises AssertionError on failure. None of them calls the CUDA library.
+
+What each pin rests on:
+  * closed forms of 2x2 / 3x3 systems worked by hand (exact binary values);
+  * Cramer's rule with determinants by permutation expansion in exact rational
+    arithmetic, on n <= 4 (brute force);
+  * reconstructions P A = L U and A = L L^T;
+  * LAPACK (through SciPy) as a library special case: same pivot sequence as dgetrf on
+    inputs without near ties, same first failing minor as dpotrf;
+  * the info contract on constructed singular / indefinite inputs;
+  * the block-tridiagonal solve against dense Cholesky of the assembled matrix.
+"""
+from __future__ import annotations
+
+import itertools
+from fractions import Fraction
+
+import numpy as np
+import scipy.linalg as sla
+
+from gen.workloads import COL_MAJOR, ROW_MAJOR, assemble_bdsv_dense, from_storage, to_storage
+from tests.numerics import backward_error, eps_of, forward_error, lapack_perm, unpack_lu
+
+
+# ----------------------------------------------------------------------------- helpers
+def _lu(orc, A_logical, B_logical, layout=ROW_MAJOR):
+    A = to_storage(np.asarray(A_logical), layout)
+    B = to_storage(np.asarray(B_logical, A.dtype), layout)
+    LU, X, ipiv, info, tie = orc.getrf_getrs(A, B, layout)
+    return from_storage(LU, layout), from_storage(X, layout), ipiv, info, tie
+
+
+def _chol(orc, A_logical, B_logical, layout=COL_MAJOR):
+    A = to_storage(np.asarray(A_logical), layout)
+    B = to_storage(np.asarray(B_logical, A.dtype), layout)
+    L, X, info = orc.potrf_potrs(A, B, layout)
+    return from_storage(L, layout), from_storage(X, layout), info
+
+
+def _det_exact(M):
+    n = len(M)
+    total = Fraction(0)
+    for perm in itertools.permutations(range(n)):
+        inv = sum(1 for i in range(n) for j in range(i + 1, n) if perm[i] > perm[j])
+        term = Fraction(1)
+        for i in range(n):
+            term *= M[i][perm[i]]
+        total += -term if inv % 2 else term
+    return total
+
+
+def _cramer_exact(A, b):
+    n = A.shape[0]
+    M = [[Fraction(float(A[i, j])) for j in range(n)] for i in range(n)]
+    bb = [Fraction(float(v)) for v in b]
+    d = _det_exact(M)
+    if d == 0:
+        return None, d
+    xs = []
+    for j in range(n):
+        Mj = [row[:] for row in M]
+        for i in range(n):
+            Mj[i][j] = bb[i]
+        xs.append(_det_exact(Mj) / d)
+    return xs, d
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------------------- LU pins
+def pin_lu_3x3_hand_worked(orc):
+    """Hand-worked 3x3 with a pivot tie at step 2 (lowest-row rule keeps the row).
+
+    A = [[2,1,1],[4,-6,0],[-2,7,2]], b = [5,-2,9]. Step 1 pivots on row 2 (|4|);
+    the Schur complement's first column is [4, 4]: a tie, the row in place wins.
+    Exact: ipiv = [2,2,3], U = [[4,-6,0],[0,4,1],[0,0,1]], L = [[1],[.5,1],[-.5,1,1]],
+    x = [1,1,2]."""
+    for dt in (np.float64, np.float32):
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            A = np.array([[[2, 1, 1], [4, -6, 0], [-2, 7, 2]]], dt)
+            b = np.array([[[5], [-2], [9]]], dt)
+            LU, X, ipiv, info, _ = _lu(orc, A, b, layout)
+            assert info[0] == 0
+            assert list(ipiv[0]) == [2, 2, 3], ipiv
+            exp = np.array([[4, -6, 0], [0.5, 4, 1], [-0.5, 1, 1]], dt)
+            assert np.array_equal(LU[0], exp), LU[0]
+            assert np.array_equal(X[0, :, 0], np.array([1, 1, 2], dt)), X
+
+
+def pin_lu_2x2_closed_form(orc):
+    """2x2: the pivot is the larger of |a11|, |a21|; x by Cramer's rule."""
+    rng = _rng(11)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for _ in range(50):
+            A = rng.uniform(-1, 1, (2, 2)).astype(dt)
+            b = rng.uniform(-1, 1, (2, 1)).astype(dt)
+            det = float(A[0, 0]) * float(A[1, 1]) - float(A[0, 1]) * float(A[1, 0])
+            if abs(det) < 0.1:
+                continue
+            LU, X, ipiv, info, _ = _lu(orc, A[None], b[None])
+            swap = abs(A[1, 0]) > abs(A[0, 0])
+            assert list(ipiv[0]) == ([2, 2] if swap else [1, 2])
+            a = A.astype(np.float64)
+            if swap:
+                a = a[::-1]
+                bb = b.astype(np.float64)[::-1]
+            else:
+                bb = b.astype(np.float64)
+            l21 = a[1, 0] / a[0, 0]
+            u22 = a[1, 1] - l21 * a[0, 1]
+            exp = np.array([[a[0, 0], a[0, 1]], [l21, u22]])
+            assert np.allclose(LU[0], exp, rtol=8 * eps, atol=8 * eps), (LU[0], exp)
+            x1 = (float(b[0, 0]) * float(A[1, 1]) - float(A[0, 1]) * float(b[1, 0])) / det
+            x2 = (float(A[0, 0]) * float(b[1, 0]) - float(b[0, 0]) * float(A[1, 0])) / det
+            kappa = np.linalg.cond(a)
+            tol = 16 * kappa * eps
+            assert np.allclose(X[0, :, 0], [x1, x2], rtol=tol, atol=tol), (X[0, :, 0], x1, x2)
+            del bb
+
+
+def pin_lu_cramer_bruteforce(orc):
+    """n <= 4: the oracle's x against the exact rational solution (Cramer, Leibniz
+    determinants), and prod(diag U) * (-1)^swaps against the exact determinant."""
+    rng = _rng(12)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for n in (1, 2, 3, 4):
+            for _ in range(12):
+                A = rng.integers(-9, 10, (n, n)).astype(dt)
+                b = rng.integers(-9, 10, (n, 1)).astype(dt)
+                xs, d = _cramer_exact(A, b[:, 0])
+                if d == 0:
+                    continue
+                LU, X, ipiv, info, _ = _lu(orc, A[None], b[None])
+                assert info[0] == 0
+                kappa = np.linalg.cond(A.astype(np.float64))
+                xe = np.array([float(v) for v in xs])
+                err = np.abs(X[0, :, 0].astype(np.float64) - xe).max() / max(np.abs(xe).max(), 1e-300)
+                assert err <= 8 * n * kappa * eps, (n, err, kappa)
+                swaps = sum(1 for k in range(n) if ipiv[0, k] != k + 1)
+                detu = float(np.prod(np.diag(LU[0]).astype(np.float64))) * (-1) ** swaps
+                assert abs(detu - float(d)) <= 8 * n * eps * max(abs(float(d)), 1.0) * kappa, (detu, d)
+
+
+def pin_lu_reconstruction(orc):
+    """P A = L U to within a small multiple of n eps ||A|| (both dtypes, both layouts)."""
+    rng = _rng(13)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for n in (1, 3, 8, 16, 33):
+            A = rng.standard_normal((6, n, n)).astype(dt)
+            B = rng.standard_normal((6, n, 2)).astype(dt)
+            for layout in (ROW_MAJOR, COL_MAJOR):
+                LU, X, ipiv, info, _ = _lu(orc, A, B, layout)
+                for s in range(A.shape[0]):
+                    L, U = unpack_lu(LU[s])
+                    P = lapack_perm(ipiv[s])
+                    res = np.abs(A[s].astype(np.float64)[P] - L @ U).max()
+                    assert res <= 4 * n * eps * np.abs(A[s]).max(), (n, res)
+
+
+def pin_lu_matches_lapack(orc):
+    """Against LAPACK dgetrf/sgetrf (SciPy): identical pivot sequence on inputs without
+    near ties, factors and solutions to rounding."""
+    rng = _rng(14)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for n in (2, 5, 16, 32, 64):
+            A = rng.standard_normal((5, n, n)).astype(dt)
+            B = rng.standard_normal((5, n, 3)).astype(dt)
+            LU, X, ipiv, info, tie = _lu(orc, A, B)
+            for s in range(A.shape[0]):
+                lu, piv = sla.lu_factor(A[s])
+                if tie[s] < 0:
+                    assert np.array_equal(piv + 1, ipiv[s]), (piv + 1, ipiv[s])
+                    assert np.allclose(LU[s], lu, rtol=0, atol=64 * n * eps * np.abs(lu).max())
+                be = backward_error(A[s][None], X[s][None], B[s][None])[0]
+                assert be <= 8 * n * eps, be
+
+
+def pin_lu_info_contract(orc):
+    """info = first singular pivot (1-based); X = 0; ipiv still reported.
+
+    * column j zeroed: the column stays exactly zero, the tie among zeros keeps the row
+      in place: info = j + 1, ipiv[j] = j + 1;
+    * [[1,2],[2,4]]: pivot 2, then 4 - 0.5*... = 0 exactly: info = 2;
+    * 1x1 subnormal pivot is singular, the smallest normal is not (singular floor)."""
+    rng = _rng(15)
+    for dt in (np.float64, np.float32):
+        n = 8
+        for j in range(n):
+            A = rng.uniform(-1, 1, (1, n, n)).astype(dt)
+            A[0, :, j] = 0
+            b = rng.uniform(-1, 1, (1, n, 1)).astype(dt)
+            LU, X, ipiv, info, _ = _lu(orc, A, b)
+            assert info[0] == j + 1, (j, info)
+            assert ipiv[0, j] == j + 1
+            assert np.all(X == 0)
+        LU, X, ipiv, info, _ = _lu(orc, np.array([[[1, 2], [2, 4]]], dt), np.ones((1, 2, 1), dt))
+        assert info[0] == 2 and list(ipiv[0]) == [2, 2] and np.all(X == 0)
+        tiny = np.finfo(dt).smallest_subnormal
+        _, X, _, info, _ = _lu(orc, np.array([[[tiny]]], dt), np.ones((1, 1, 1), dt))
+        assert info[0] == 1 and X[0, 0, 0] == 0
+        _, X, _, info, _ = _lu(orc, np.array([[[np.finfo(dt).tiny]]], dt), np.ones((1, 1, 1), dt))
+        assert info[0] == 0 and X[0, 0, 0] == dt(1) / np.finfo(dt).tiny
+        # only the first failing pivot is reported
+        A = np.zeros((1, 3, 3), dt)
+        A[0, 2, 2] = 1
+        _, _, ipiv, info, _ = _lu(orc, A, np.ones((1, 3, 1), dt))
+        assert info[0] == 1 and list(ipiv[0]) == [1, 2, 3]
+
+
+def pin_lu_layout_invariance(orc):
+    """Row- and column-major storage of the same A give the same pivots, info and,
+    the arithmetic being identical, bitwise identical factors and solutions."""
+    rng = _rng(16)
+    for dt in (np.float64, np.float32):
+        A = rng.standard_normal((10, 12, 12)).astype(dt)
+        B = rng.standard_normal((10, 12, 3)).astype(dt)
+        r = _lu(orc, A, B, ROW_MAJOR)
+        c = _lu(orc, A, B, COL_MAJOR)
+        for a, b in zip(r, c):
+            assert np.array_equal(a, b)
+
+
+def pin_lu_near_tie_flag(orc):
+    """The near-tie record: two top candidates within 1e-6 relative at step 0."""
+    A = np.array([[[1.0, 2.0], [1.0 + 1e-9, 3.0]]])
+    _, _, _, _, tie = _lu(orc, A, np.ones((1, 2, 1)))
+    assert tie[0] == 0
+    A = np.array([[[1.0, 2.0], [0.5, 3.0]]])
+    _, _, _, _, tie = _lu(orc, A, np.ones((1, 2, 1)))
+    assert tie[0] == -1
+
+
+# ----------------------------------------------------------------------- Cholesky pins
+def pin_chol_hand_worked(orc):
+    """A = L L^T with L = [[2,0,0],[1,3,0],[-1,2,4]]: A = [[4,2,-2],[2,10,5],[-2,5,21]];
+    with b = A [1,1,1]^T = [4,17,24] the solution is [1,1,1]."""
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for layout in (COL_MAJOR, ROW_MAJOR):
+            A = np.array([[[4, 2, -2], [2, 10, 5], [-2, 5, 21]]], dt)
+            b = np.array([[[4], [17], [24]]], dt)
+            L, X, info = _chol(orc, A, b, layout)
+            assert info[0] == 0
+            Lexp = np.array([[2, 0, 0], [1, 3, 0], [-1, 2, 4]], np.float64)
+            assert np.allclose(np.tril(L[0]), Lexp, rtol=0, atol=8 * eps * 4)
+            assert np.allclose(X[0, :, 0], [1, 1, 1], rtol=0, atol=64 * eps)
+
+
+def pin_chol_2x2_closed_form(orc):
+    """l11 = sqrt(a11), l21 = a21 / l11, l22 = sqrt(a22 - l21^2)."""
+    rng = _rng(21)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for _ in range(40):
+            G = rng.standard_normal((2, 2))
+            A = (G @ G.T + 0.5 * np.eye(2)).astype(dt)
+            L, X, info = _chol(orc, A[None], np.ones((1, 2, 1), dt))
+            a = A.astype(np.float64)
+            l11 = np.sqrt(a[0, 0])
+            l21 = a[1, 0] / l11
+            l22 = np.sqrt(a[1, 1] - l21 * l21)
+            assert info[0] == 0
+            assert np.allclose([L[0, 0, 0], L[0, 1, 0], L[0, 1, 1]], [l11, l21, l22],
+                               rtol=16 * eps * np.linalg.cond(a), atol=0)
+
+
+def pin_chol_reconstruction_and_lapack(orc):
+    """A = L L^T; L against LAPACK dpotrf; x against the exact rational solution for
+    n <= 4 integer SPD matrices; only the lower triangle is written."""
+    rng = _rng(22)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for n in (1, 4, 9, 32):
+            G = rng.standard_normal((4, n, n))
+            A = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dt)
+            B = rng.standard_normal((4, n, 2)).astype(dt)
+            for layout in (COL_MAJOR, ROW_MAJOR):
+                L, X, info = _chol(orc, A, B, layout)
+                assert np.all(info == 0)
+                for s in range(4):
+                    Ls = np.tril(L[s]).astype(np.float64)
+                    assert np.abs(Ls @ Ls.T - A[s]).max() <= 4 * n * eps * np.abs(A[s]).max()
+                    ref = sla.cholesky(A[s].astype(np.float64), lower=True)
+                    assert np.allclose(Ls, ref, rtol=0, atol=32 * n * eps * np.abs(ref).max())
+                    # the strictly upper triangle is untouched
+                    iu = np.triu_indices(n, 1)
+                    assert np.array_equal(L[s][iu], A[s][iu])
+                be = backward_error(A, X, B)
+                assert np.all(be <= 8 * n * eps), be
+        for n in (2, 3, 4):
+            for _ in range(6):
+                G = rng.integers(-3, 4, (n, n))
+                A = (G @ G.T + np.eye(n, dtype=int)).astype(dt)
+                b = rng.integers(-5, 6, (n, 1)).astype(dt)
+                xs, d = _cramer_exact(A, b[:, 0])
+                _, X, info = _chol(orc, A[None], b[None])
+                xe = np.array([float(v) for v in xs])
+                kappa = np.linalg.cond(A.astype(np.float64))
+                err = np.abs(X[0, :, 0] - xe).max() / max(np.abs(xe).max(), 1e-300)
+                assert err <= 16 * n * kappa * eps, (err, kappa)
+
+
+def pin_chol_info_contract(orc):
+    """info = smallest leading minor that is not positive definite; X = 0.
+
+    * A[k][k] = -1 on an SPD matrix (minors 1..k untouched, the (k+1)-th Schur value
+      is <= -1): info = k + 1;
+    * agreement with LAPACK dpotrf's info on random indefinite matrices;
+    * a zero or NaN diagonal fails (!(d > 0))."""
+    rng = _rng(23)
+    for dt in (np.float64, np.float32):
+        n = 12
+        for k in range(n):
+            G = rng.standard_normal((n, n))
+            A = (G @ G.T + n * np.eye(n)).astype(dt)
+            A[k, k] = -1
+            _, X, info = _chol(orc, A[None], np.ones((1, n, 1), dt))
+            assert info[0] == k + 1 and np.all(X == 0)
+        for _ in range(20):
+            S = rng.standard_normal((n, n))
+            A = ((S + S.T) / 2 + rng.uniform(-1, 4) * np.eye(n)).astype(dt)
+            _, _, info = _chol(orc, A[None], np.ones((1, n, 1), dt))
+            potrf = sla.lapack.dpotrf if dt == np.float64 else sla.lapack.spotrf
+            _, linfo = potrf(A, lower=1)
+            assert info[0] == linfo, (info[0], linfo)
+        A = np.diag([1.0, 0.0, 1.0]).astype(dt)
+        assert _chol(orc, A[None], np.ones((1, 3, 1), dt))[2][0] == 2
+        A = np.diag([1.0, 1.0, np.nan]).astype(dt)
+        assert _chol(orc, A[None], np.ones((1, 3, 1), dt))[2][0] == 3
+
+
+# --------------------------------------------------------------------------- bdsv pins
+def _random_bdsv(rng, batch, nbr, bs, dt=np.float64):
+    strips = np.zeros((batch, nbr, bs, 3 * bs), dt)
+    C = rng.uniform(-0.5, 0.5, (batch, max(nbr - 1, 0), bs, bs)) / bs
+    M = rng.standard_normal((batch, nbr, bs, bs)) / np.sqrt(bs)
+    strips[:, :, :, bs:2 * bs] = M @ np.swapaxes(M, 2, 3) + 3.0 * np.eye(bs)
+    if nbr > 1:
+        strips[:, :nbr - 1, :, 2 * bs:] = C
+        strips[:, 1:, :, :bs] = np.swapaxes(C, 2, 3)
+    xpad = np.zeros((batch, (nbr + 2) * bs), dt)
+    xpad[:, bs:(nbr + 1) * bs] = rng.standard_normal((batch, nbr * bs))
+    return strips, xpad
+
+
+def pin_bdsv_dense_equivalence(orc):
+    """bdsv equals the dense solve of the assembled matrix (backward error), its MAIN
+    blocks are the diagonal blocks of the dense Cholesky factor and its LEFT blocks the
+    sub-diagonal ones; RIGHT slots, the upper triangles of MAIN and the pads are left as
+    they were."""
+    rng = _rng(31)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for nbr, bs in ((1, 4), (2, 3), (5, 8), (32, 8)):
+            strips, xpad = _random_bdsv(rng, 3, nbr, bs, dt)
+            S, X, info = orc.bdsv(strips, xpad)
+            assert np.all(info == 0)
+            Ad = assemble_bdsv_dense(strips).astype(np.float64)
+            N = nbr * bs
+            b = xpad[:, bs:bs + N]
+            x = X[:, bs:bs + N]
+            be = backward_error(Ad, x[:, :, None], b[:, :, None])
+            assert np.all(be <= 8 * N * eps), be
+            for s in range(3):
+                Lf = np.linalg.cholesky(Ad[s])
+                for k in range(nbr):
+                    r0 = k * bs
+                    F = np.tril(S[s, k, :, bs:2 * bs])
+                    assert np.allclose(F, Lf[r0:r0 + bs, r0:r0 + bs], rtol=0, atol=64 * N * eps)
+                    iu = np.triu_indices(bs, 1)
+                    assert np.array_equal(S[s, k, :, bs:2 * bs][iu], strips[s, k, :, bs:2 * bs][iu])
+                    if k > 0:
+                        assert np.allclose(S[s, k, :, :bs], Lf[r0:r0 + bs, r0 - bs:r0], rtol=0,
+                                           atol=64 * N * eps)
+                assert np.array_equal(S[s, :, :, 2 * bs:], strips[s, :, :, 2 * bs:])
+                assert np.all(X[s, :bs] == 0) and np.all(X[s, bs + N:] == 0)
+
+
+def pin_bdsv_single_block_is_potrf(orc):
+    """NBR = 1 reduces to Cholesky factor + solve of D_0 (LAPACK dpotrf/dpotrs)."""
+    rng = _rng(32)
+    strips, xpad = _random_bdsv(rng, 4, 1, 6)
+    S, X, info = orc.bdsv(strips, xpad)
+    for s in range(4):
+        D = strips[s, 0, :, 6:12]
+        c = sla.cho_factor(D, lower=True)
+        x = sla.cho_solve(c, xpad[s, 6:12])
+        assert np.allclose(np.tril(S[s, 0, :, 6:12]), np.tril(c[0]), rtol=0, atol=1e-13)
+        assert np.allclose(X[s, 6:12], x, rtol=1e-12, atol=1e-14)
+
+
+def pin_bdsv_scalar_tridiagonal(orc):
+    """BS = 1, NBR = 2: [[d0, c], [c, d1]] gives f0 = sqrt(d0), e1 = c / f0,
+    f1 = sqrt(d1 - e1^2) (the scalar block-Thomas recurrence)."""
+    strips = np.zeros((1, 2, 1, 3))
+    d0, d1, c = 4.0, 5.0, 2.0
+    strips[0, 0, 0, 1], strips[0, 0, 0, 2] = d0, c
+    strips[0, 1, 0, 0], strips[0, 1, 0, 1] = c, d1
+    xpad = np.array([[0.0, 8.0, 9.0, 0.0]])
+    S, X, info = orc.bdsv(strips, xpad)
+    f0 = 2.0
+    e1 = 1.0
+    f1 = 2.0
+    assert S[0, 0, 0, 1] == f0 and S[0, 1, 0, 0] == e1 and S[0, 1, 0, 1] == f1
+    # [[4,2],[2,5]] x = [8,9] -> x = [(40-18)/16, (36-16)/16] = [1.375, 1.25]
+    assert np.allclose(X[0], [0.0, 1.375, 1.25, 0.0], rtol=0, atol=1e-15)
+
+
+def pin_bdsv_info(orc):
+    """A non-positive-definite knot: info = global index br*bs + j + 1, the same minor
+    at which LAPACK dpotrf fails on the assembled dense matrix; X = 0."""
+    rng = _rng(33)
+    nbr, bs = 6, 4
+    for knot in (0, 3, 5):
+        for j in (0, 2):
+            strips, xpad = _random_bdsv(rng, 1, nbr, bs)
+            strips[0, knot, j, bs + j] = -1.0
+            S, X, info = orc.bdsv(strips, xpad)
+            _, linfo = sla.lapack.dpotrf(assemble_bdsv_dense(strips)[0], lower=1)
+            assert info[0] == linfo == knot * bs + j + 1, (info[0], linfo)
+            assert np.all(X == 0)
+
+
+LU_PINS = [pin_lu_3x3_hand_worked, pin_lu_2x2_closed_form, pin_lu_cramer_bruteforce,
+           pin_lu_reconstruction, pin_lu_matches_lapack, pin_lu_info_contract,
+           pin_lu_layout_invariance, pin_lu_near_tie_flag]
+CHOL_PINS = [pin_chol_hand_worked, pin_chol_2x2_closed_form,
+             pin_chol_reconstruction_and_lapack, pin_chol_info_contract]
+BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,
+             pin_bdsv_scalar_tridiagonal, pin_bdsv_info]
+ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS
+
+
+def failing_pins(orc, pins=ALL_PINS):
+    """Names of the pins that fail (or raise) on this oracle."""
+    bad = []
+    for p in pins:
+        try:
+            p(orc)
+        except Exception:  # noqa: BLE001 - any failure counts as a tripped pin
+            bad.append(p.__name__)
+    return bad

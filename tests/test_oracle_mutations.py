@@ -1,0 +1,92 @@
+"""Planted mistakes in the oracle must trip a pin.
+
+Each case below edits one line of a copy of oracle.cpp (a dropped term, a wrong sign,
+a transposed operand or index, an off-by-one), builds the copy with the same flags as
+the real oracle, and checks that at least one pin of tests/pins.py fails on it. The
+real oracle passes every pin (test_oracle_pins.py), so the pins are shown to tell a
+correct oracle from a plausibly broken one. Runs on the CPU only.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from tests import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.cpp")
+
+MUTATIONS = [
+    ("lu_tie_rule_last_max", "      if (v > best) {", "      if (v >= best) {"),
+    ("lu_search_skips_last_row",
+     "    for (int i = k + 1; i < n; ++i) {\n      T v = std::fabs(a(i, k));\n      if (v > best)",
+     "    for (int i = k + 1; i < n - 1; ++i) {\n      T v = std::fabs(a(i, k));\n      if (v > best)"),
+    ("lu_rhs_not_swapped",
+     "        T t = b(k, c);\n        b(k, c) = b(p, c);\n        b(p, c) = t;", ""),
+    ("lu_L_part_not_swapped",
+     "      for (int c = 0; c < n; ++c) {\n        T t = a(k, c);",
+     "      for (int c = k; c < n; ++c) {\n        T t = a(k, c);"),
+    ("lu_schur_sign", "a(i, j) = std::fma(-l, a(k, j), a(i, j));",
+     "a(i, j) = std::fma(l, a(k, j), a(i, j));"),
+    ("lu_schur_transposed_operand", "a(i, j) = std::fma(-l, a(k, j), a(i, j));",
+     "a(i, j) = std::fma(-l, a(j, k), a(i, j));"),
+    ("lu_forward_solve_dropped", "b(i, c) = std::fma(-l, b(k, c), b(i, c));", ";"),
+    ("lu_back_subst_transposed", "b(i, c) = std::fma(-a(i, k), x, b(i, c));",
+     "b(i, c) = std::fma(-a(k, i), x, b(i, c));"),
+    ("lu_floor_is_zero", "const bool ok = best >= floor_v;", "const bool ok = best > T(0);"),
+    ("lu_info_off_by_one", "if (!ok && inf == 0) inf = k + 1;", "if (!ok && inf == 0) inf = k;"),
+    ("lu_info_last_not_first", "if (!ok && inf == 0) inf = k + 1;", "if (!ok) inf = k + 1;"),
+    ("lu_failed_x_not_zeroed",
+     "      for (int c = 0; c < nrhs; ++c) b(r0, c) = T(0);\n  }\n  *info = inf;\n  if (tie_step)",
+     "      ;\n  }\n  *info = inf;\n  if (tie_step)"),
+    ("chol_sqrt_dropped", "const T l = std::sqrt(d);\n    a(k, k) = l;",
+     "const T l = d;\n    a(k, k) = l;"),
+    ("chol_update_writes_upper",
+     "for (int i = j; i < n; ++i) a(i, j) = std::fma(-a(i, k), ljk, a(i, j));",
+     "for (int i = j; i < n; ++i) a(j, i) = std::fma(-a(i, k), ljk, a(j, i));"),
+    ("chol_back_solve_not_transposed", "b(i, c) = std::fma(-a(k, i), x, b(i, c));",
+     "b(i, c) = std::fma(-a(i, k), x, b(i, c));"),
+    ("chol_info_off_by_one", "      inf = k + 1;\n      break;", "      inf = k;\n      break;"),
+    ("chol_zero_pivot_accepted", "if (!(d > T(0))) {\n      inf = k + 1;",
+     "if (!(d >= T(0))) {\n      inf = k + 1;"),
+    ("bdsv_trsm_uses_F_not_FT", "s = std::fma(-E[ar * bs + m], blk(k - 1, MAIN, j, m), s);",
+     "s = std::fma(-E[ar * bs + m], blk(k - 1, MAIN, m, j), s);"),
+    ("bdsv_syrk_transposed", "s = std::fma(-E[i * bs + m], E[j * bs + m], s);",
+     "s = std::fma(-E[i * bs + m], E[m * bs + j], s);"),
+    ("bdsv_forward_coupling_dropped",
+     "z[i] = std::fma(-blk(k, LEFT, i, m), x[(k - 1) * bs + m], z[i]);", ";"),
+    ("bdsv_backward_uses_E_not_ET",
+     "z[m] = std::fma(-blk(k + 1, LEFT, i, m), x[(k + 1) * bs + i], z[m]);",
+     "z[m] = std::fma(-blk(k + 1, LEFT, m, i), x[(k + 1) * bs + i], z[m]);"),
+    ("bdsv_backward_trsv_not_transposed",
+     "s = std::fma(-blk(k, MAIN, m, j), x[k * bs + m], s);",
+     "s = std::fma(-blk(k, MAIN, j, m), x[k * bs + m], s);"),
+    ("bdsv_info_local_index", "inf = k * bs + c + 1;", "inf = c + 1;"),
+]
+
+
+def _build_variant(tmpdir, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation {name}: pattern must occur exactly once"
+    path = os.path.join(tmpdir, f"{name}.cpp")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    return oracle.compile_library(path, os.path.join(tmpdir, f"lib{name}.so"))
+
+
+@pytest.fixture(scope="module")
+def variants():
+    with tempfile.TemporaryDirectory() as d:
+        with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+            futs = {m[0]: ex.submit(_build_variant, d, *m) for m in MUTATIONS}
+            libs = {k: f.result() for k, f in futs.items()}
+        yield libs
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTATIONS])
+def test_planted_mistake_trips_a_pin(variants, name):
+    orc = oracle.Oracle(variants[name])
+    assert pins.failing_pins(orc), f"no pin caught the planted mistake {name}"
