@@ -1,0 +1,139 @@
+"""Batched small dense linear solvers for GB300 (sm_103a): Python binding.
+
+This module only marshals arguments: it reads shapes, dtypes, device pointers and the
+CUDA stream from torch tensors and calls the C ABI of ``libbsolve.so`` (declared in
+``include/bsolve.h``) under the same names. Every step of every solve runs in the CUDA
+kernels of that library; there is no CPU or PyTorch fallback. If the library has not
+been built, importing works but every call raises.
+
+Storage convention (raw storage tensors, as the C ABI sees memory):
+  * A: (batch, n, n); row-major holds A itself, column-major holds A^T in memory;
+  * B: (batch, n, nrhs) row-major, (batch, nrhs, n) column-major;
+  * bdsv strips: (batch, nbr, bs, 3*bs), padded vector: (batch, (nbr + 2)*bs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libbsolve.so")
+
+BS_OK, BS_ERR_INVALID_ARG, BS_ERR_UNSUPPORTED, BS_ERR_CUDA = 0, 1, 2, 3
+BS_FP32, BS_FP64 = 0, 1
+BS_ROW_MAJOR, BS_COL_MAJOR = 0, 1
+BS_LOWER, BS_UPPER = 0, 1
+ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
+
+EXPORTED = (
+    "bs_getrf_getrs_batched", "bs_potrf_potrs_batched", "bs_bdsv_batched",
+    "bs_status_string", "bs_last_cuda_error", "bs_getrf_getrs_supported",
+    "bs_potrf_potrs_supported", "bs_bdsv_supported", "bs_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class BsolveError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}"
+                         + (f" (cuda error {lib().bs_last_cuda_error()})" if status == BS_ERR_CUDA
+                            else ""))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libbsolve.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with dense_linear_solvers_gb300._build.build() "
+                    "(or __graft_entry__.build()); there is no fallback path")
+            L = ctypes.CDLL(LIB_PATH)
+            i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+            L.bs_getrf_getrs_batched.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp]
+            L.bs_getrf_getrs_batched.restype = i32
+            L.bs_potrf_potrs_batched.argtypes = [i32, i32, i32, i32, i32, i64, vp, vp, vp, vp]
+            L.bs_potrf_potrs_batched.restype = i32
+            L.bs_bdsv_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp]
+            L.bs_bdsv_batched.restype = i32
+            L.bs_status_string.argtypes = [i32]
+            L.bs_status_string.restype = ctypes.c_char_p
+            L.bs_last_cuda_error.argtypes = []
+            L.bs_last_cuda_error.restype = i32
+            L.bs_getrf_getrs_supported.argtypes = [i32, i32, i32, i32]
+            L.bs_getrf_getrs_supported.restype = i32
+            L.bs_potrf_potrs_supported.argtypes = [i32, i32, i32, i32, i32]
+            L.bs_potrf_potrs_supported.restype = i32
+            L.bs_bdsv_supported.argtypes = [i32, i32, i32]
+            L.bs_bdsv_supported.restype = i32
+            L.bs_version.argtypes = []
+            L.bs_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().bs_status_string(int(status)).decode()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return BS_FP32
+    if t.dtype == torch.float64:
+        return BS_FP64
+    raise TypeError(f"unsupported dtype {t.dtype}: float32 or float64")
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError("bsolve operands are device tensors (torch CUDA tensors)")
+    if not t.is_contiguous():
+        raise ValueError("bsolve operands must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != BS_OK:
+        raise BsolveError(status, what)
+
+
+def bs_getrf_getrs_batched(A, B, ipiv, info, layout: int = ROW_MAJOR, stream=None) -> None:
+    """LU with partial pivoting + solve of A[s] X = B[s], in place (see bsolve.h)."""
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    st = lib().bs_getrf_getrs_batched(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
+                                      _ptr(ipiv), _ptr(info), _stream(stream))
+    _check(st, "bs_getrf_getrs_batched")
+
+
+def bs_potrf_potrs_batched(A, B, info, layout: int = COL_MAJOR, fill: int = BS_LOWER,
+                           stream=None) -> None:
+    """Cholesky + solve of SPD systems, in place (see bsolve.h)."""
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    st = lib().bs_potrf_potrs_batched(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
+                                      _ptr(B), _ptr(info), _stream(stream))
+    _check(st, "bs_potrf_potrs_batched")
+
+
+def bs_bdsv_batched(strips, x_padded, info, stream=None) -> None:
+    """Block-tridiagonal block-Cholesky solve, in place (see bsolve.h)."""
+    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    st = lib().bs_bdsv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
+                               _ptr(info), _stream(stream))
+    _check(st, "bs_bdsv_batched")

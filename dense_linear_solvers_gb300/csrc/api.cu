@@ -1,0 +1,136 @@
+// C ABI of libbsolve.so: argument checks and dispatch to the kernel launchers.
+// See include/bsolve.h for the contract of every entry point.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "bsolve.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxLuN = 64;
+constexpr int kMaxRegN = 32;
+constexpr int kMaxNrhs = 8;
+constexpr int kMaxBdsvBs = 8;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bs_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return BS_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return BS_ERR_CUDA;
+}
+
+bool lu_supported(bs_dtype dtype, bs_layout layout, int n, int nrhs) {
+  return (dtype == BS_FP32 || dtype == BS_FP64) &&
+         (layout == BS_ROW_MAJOR || layout == BS_COL_MAJOR) && n >= 1 && n <= kMaxLuN &&
+         nrhs >= 1 && nrhs <= kMaxNrhs;
+}
+
+bool chol_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs) {
+  return (dtype == BS_FP32 || dtype == BS_FP64) &&
+         (layout == BS_ROW_MAJOR || layout == BS_COL_MAJOR) && fill == BS_LOWER && n >= 1 &&
+         n <= kMaxLuN && nrhs >= 1 && nrhs <= kMaxNrhs;
+}
+
+bool bdsv_supported(bs_dtype dtype, int nbr, int bs) {
+  return (dtype == BS_FP32 || dtype == BS_FP64) && nbr >= 1 && bs >= 1 && bs <= kMaxBdsvBs;
+}
+
+}  // namespace
+
+extern "C" {
+
+bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                 int64_t batch, void* A, void* B, int32_t* ipiv,
+                                 int32_t* info, void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_reg<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                           static_cast<float*>(B), ipiv, info, s)
+            : bsolve::launch_lu_reg<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                            static_cast<double*>(B), ipiv, info, s);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_smem<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                            static_cast<float*>(B), ipiv, info, s)
+            : bsolve::launch_lu_smem<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                             static_cast<double*>(B), ipiv, info, s);
+  }
+  return from_cuda(e);
+}
+
+bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                 int nrhs, int64_t batch, void* A, void* B, int32_t* info,
+                                 void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_chol_smem<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                            static_cast<float*>(B), info, s)
+          : bsolve::launch_chol_smem<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                             static_cast<double*>(B), info, s);
+  return from_cuda(e);
+}
+
+bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+                          void* strips, void* x_padded, int32_t* info, void* stream) {
+  if (num_block_rows < 0 || block_size < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!bdsv_supported(dtype, num_block_rows, block_size)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!strips || !x_padded || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(strips) || !aligned16(x_padded) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_bdsv<float>(num_block_rows, block_size, batch,
+                                       static_cast<float*>(strips),
+                                       static_cast<float*>(x_padded), info, s)
+          : bsolve::launch_bdsv<double>(num_block_rows, block_size, batch,
+                                        static_cast<double*>(strips),
+                                        static_cast<double*>(x_padded), info, s);
+  return from_cuda(e);
+}
+
+const char* bs_status_string(bs_status status) {
+  switch (status) {
+    case BS_OK: return "BS_OK";
+    case BS_ERR_INVALID_ARG: return "BS_ERR_INVALID_ARG";
+    case BS_ERR_UNSUPPORTED: return "BS_ERR_UNSUPPORTED";
+    case BS_ERR_CUDA: return "BS_ERR_CUDA";
+    default: return "BS_UNKNOWN_STATUS";
+  }
+}
+
+int bs_last_cuda_error(void) { return g_last_cuda_error; }
+
+int bs_getrf_getrs_supported(bs_dtype dtype, bs_layout layout, int n, int nrhs) {
+  return lu_supported(dtype, layout, n, nrhs) ? 1 : 0;
+}
+
+int bs_potrf_potrs_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs) {
+  return chol_supported(dtype, layout, fill, n, nrhs) ? 1 : 0;
+}
+
+int bs_bdsv_supported(bs_dtype dtype, int num_block_rows, int block_size) {
+  return bdsv_supported(dtype, num_block_rows, block_size) ? 1 : 0;
+}
+
+int bs_version(void) { return 100; }
+
+}  // extern "C"

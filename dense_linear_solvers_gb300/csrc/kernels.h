@@ -1,0 +1,33 @@
+// Host-side launchers of the CUDA kernels (internal to libbsolve.so).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bsolve {
+
+// LU + solve, rows in registers, 1 <= n <= 32, 1 <= nrhs <= 8.
+template <typename T>
+cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                          int32_t* ipiv, int32_t* info, cudaStream_t stream);
+
+// LU + solve, one warp per system in shared memory, 1 <= n <= 64, 1 <= nrhs <= 8.
+template <typename T>
+cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                           int32_t* ipiv, int32_t* info, cudaStream_t stream);
+
+// Lower Cholesky + solve, one warp per system in shared memory, 1 <= n <= 64.
+template <typename T>
+cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                             int32_t* info, cudaStream_t stream);
+
+// Block-tridiagonal block-Cholesky sweep, one thread per system, 1 <= bs <= 8.
+template <typename T>
+cudaError_t launch_bdsv(int nbr, int bs, int64_t batch, T* strips, T* xpad, int32_t* info,
+                        cudaStream_t stream);
+
+// Shared memory one system needs in the shared-memory kernels.
+size_t lu_smem_bytes(int n, int nrhs, int elem_size);
+size_t chol_smem_bytes(int n, int nrhs, int elem_size);
+
+}  // namespace bsolve

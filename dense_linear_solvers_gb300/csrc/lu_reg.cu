@@ -1,0 +1,26 @@
+// Dispatch of the register-resident LU kernel (n <= 32) by layout; the kernel and its
+// tiers live in lu_reg.cuh, instantiated per dtype and layout in lu_reg_*.cu.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsolve {
+namespace lu_reg_detail {
+template <typename T, int LAYOUT>
+cudaError_t launch_layout(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
+                          int32_t* info, cudaStream_t stream);
+}  // namespace lu_reg_detail
+
+template <typename T>
+cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                          int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if (layout == kRowMajor)
+    return lu_reg_detail::launch_layout<T, kRowMajor>(n, nrhs, batch, A, B, ipiv, info, stream);
+  return lu_reg_detail::launch_layout<T, kColMajor>(n, nrhs, batch, A, B, ipiv, info, stream);
+}
+
+template cudaError_t launch_lu_reg<float>(int, int, int, int64_t, float*, float*, int32_t*,
+                                          int32_t*, cudaStream_t);
+template cudaError_t launch_lu_reg<double>(int, int, int, int64_t, double*, double*, int32_t*,
+                                           int32_t*, cudaStream_t);
+
+}  // namespace bsolve

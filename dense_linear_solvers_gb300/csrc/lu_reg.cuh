@@ -1,0 +1,277 @@
+// LU with partial pivoting + solve for n <= 32, rows held in registers.
+//
+// One system per group of G = NT lanes (NT = the order tier, a power of two); 32/NT
+// systems share a warp. Lane t holds physical row t of A and of B in registers for the
+// whole solve, as in the TDLS CooperativeLUpp solver (TDLS API, "solver_static.hpp File
+// Reference", Detailed Description): rows never move between lanes ("logical" row
+// interchanges, MAGMA's rowid); each lane tracks the current position of its row.
+//
+// Step k (fully unrolled, every operand index static):
+//   1. pivot search: integer magnitude keys (see common.cuh), group max by xor
+//      shuffles, then the lowest current position among the lanes holding the max
+//      (lowest-row tie rule; a rare exact tie takes a second reduction);
+//   2. positions k and p exchange (a bookkeeping swap, no data moves); the pivot lane
+//      records the LAPACK swap entry ipiv[k] = position(p) + 1;
+//   3. the pivot lane publishes its row (columns >= k and the right-hand sides) in a
+//      shared-memory buffer, double-buffered by step parity so that one __syncwarp per
+//      step orders writes and reads;
+//   4. every row still below the pivot scales its column-k entry by the pivot
+//      reciprocal and applies the rank-1 update to its row of A and B (the forward solve
+//      L y = P b folded into the factorization).
+// Back substitution keeps x_i in the register of the lane that owns position i and
+// publishes it through shared memory, one __syncwarp per step.
+// Each row is written once, at its final position: the stored factor is in LAPACK
+// order (row k = position k).
+//
+// Arithmetic (identical, operation by operation, to the CPU oracle): r = 1/pivot
+// correctly rounded (r = 1 for a singular pivot), l = a_ik * r, every update one fused
+// multiply-add, x_k = y_k * r_k.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsolve {
+namespace lu_reg_detail {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <typename T, int N>
+__device__ __forceinline__ void load_vec(const T* __restrict__ p, T (&r)[N]) {
+  if constexpr ((N * sizeof(T)) % 16 == 0) {
+    constexpr int V = 16 / sizeof(T);
+#pragma unroll
+    for (int j = 0; j < N; j += V) {
+      if constexpr (sizeof(T) == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p + j));
+        r[j] = v.x; r[j + 1] = v.y; r[j + 2] = v.z; r[j + 3] = v.w;
+      } else {
+        const double2 v = __ldg(reinterpret_cast<const double2*>(p + j));
+        r[j] = v.x; r[j + 1] = v.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) r[j] = p[j];
+  }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vec(T* __restrict__ p, const T (&r)[N]) {
+  if constexpr ((N * sizeof(T)) % 16 == 0) {
+    constexpr int V = 16 / sizeof(T);
+#pragma unroll
+    for (int j = 0; j < N; j += V) {
+      if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4*>(p + j) = make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+      } else {
+        *reinterpret_cast<double2*>(p + j) = make_double2(r[j], r[j + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) p[j] = r[j];
+  }
+}
+
+// FULL: n == NT and nrhs == RT (every guard compiles away).
+template <typename T, int NT, int RT, int LAYOUT, bool FULL>
+__global__ void __launch_bounds__(kThreads)
+lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict__ B,
+              int32_t* __restrict__ ipiv, int32_t* __restrict__ info) {
+  using Key = typename Traits<T>::Key;
+  constexpr int G = NT;
+  constexpr int GPW = 32 / G;                 // groups (systems) per warp
+  constexpr int W = NT + RT;                  // published row: A part, then B part
+  constexpr int WP = (W * sizeof(T) + 15) / 16 * 16 / sizeof(T);
+  constexpr unsigned GMASK = (G == 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
+
+  __shared__ __align__(16) T prow[kWarps][GPW][2][WP];
+  __shared__ __align__(16) T xbuf[kWarps][GPW][2][RT];
+
+  const int n = FULL ? NT : n_;
+  const int nrhs = FULL ? RT : nrhs_;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane / G;
+  const int t = lane % G;
+  const int64_t s = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * GPW + g;
+  const bool valid = s < batch;
+  const bool row_ok = valid && (FULL || t < n);
+
+  T a[NT];
+  T b[RT];
+  const int64_t sA = s * n * n;
+  const int64_t sB = s * n * nrhs;
+  if (row_ok) {
+    if (LAYOUT == kRowMajor) {
+      if (FULL) {
+        load_vec<T, NT>(A + sA + static_cast<int64_t>(t) * NT, a);
+        load_vec<T, RT>(B + sB + static_cast<int64_t>(t) * RT, b);
+      } else {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) a[j] = (j < n) ? A[sA + t * n + j] : T(0);
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[c] = (c < nrhs) ? B[sB + t * nrhs + c] : T(0);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) a[j] = (FULL || j < n) ? A[sA + j * n + t] : T(0);
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = (FULL || c < nrhs) ? B[sB + c * n + t] : T(0);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) a[j] = T(0);
+#pragma unroll
+    for (int c = 0; c < RT; ++c) b[c] = T(0);
+  }
+
+  int pos = t;          // current position of this lane's row
+  int my_ipiv = 0;      // LAPACK entry of the step that chose this row
+  T my_r = T(1);        // reciprocal of this row's pivot
+  int inf = 0;
+
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    if (!FULL && k >= n) break;
+    const bool cand = row_ok && pos >= k;
+    const Key key = cand ? pivot_key<T>(a[k], pos == k) : Key(0);
+    Key mk = key;
+#pragma unroll
+    for (int off = G / 2; off >= 1; off >>= 1) {
+      const Key o = shfl_xor_key(mk, off, G);
+      mk = o > mk ? o : mk;
+    }
+    const bool hold = cand && key == mk;
+    const unsigned bal = (__ballot_sync(0xFFFFFFFFu, hold) >> (g * G)) & GMASK;
+    int plane;
+    if (__any_sync(0xFFFFFFFFu, __popc(bal) > 1)) {
+      // exact tie: the lowest current position among the lanes holding the max
+      int tp = hold ? pos : 0x7FFFFFFF;
+#pragma unroll
+      for (int off = G / 2; off >= 1; off >>= 1) {
+        const int o = __shfl_xor_sync(0xFFFFFFFFu, tp, off, G);
+        tp = o < tp ? o : tp;
+      }
+      const unsigned b2 =
+          (__ballot_sync(0xFFFFFFFFu, hold && pos == tp) >> (g * G)) & GMASK;
+      plane = __ffs(b2) - 1;
+    } else {
+      plane = __ffs(bal) - 1;
+    }
+    if (plane < 0) plane = 0;  // only in groups past the end of the batch
+    const int pos_p = __shfl_sync(0xFFFFFFFFu, pos, plane, G);
+    const bool ok = pivot_ok<T>(mk);
+    if (!ok && inf == 0) inf = k + 1;
+    const bool is_p = (t == plane);
+    if (is_p) my_ipiv = pos_p + 1;
+    if (pos == k) pos = pos_p;
+    if (is_p) pos = k;
+
+    T* pr = prow[warp][g][k & 1];
+    if (is_p) {
+#pragma unroll
+      for (int j = k; j < NT; ++j) pr[j] = a[j];
+#pragma unroll
+      for (int c = 0; c < RT; ++c) pr[NT + c] = b[c];
+    }
+    __syncwarp();
+    const T piv = pr[k];
+    const T r = ok ? T(1) / piv : T(1);
+    if (is_p) my_r = r;
+    if (row_ok && pos > k) {
+      const T l = a[k] * r;
+      a[k] = l;
+#pragma unroll
+      for (int j = k + 1; j < NT; ++j) a[j] = fma_rn<T>(-l, pr[j], a[j]);
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-l, pr[NT + c], b[c]);
+    }
+  }
+
+  // U x = y, from the last position.
+#pragma unroll
+  for (int i = NT - 1; i >= 0; --i) {
+    if (!FULL && i >= n) continue;
+    T* xb = xbuf[warp][g][i & 1];
+    if (row_ok && pos == i) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) {
+        b[c] = b[c] * my_r;
+        xb[c] = b[c];
+      }
+    }
+    __syncwarp();
+    if (row_ok && pos < i) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-a[i], xb[c], b[c]);
+    }
+  }
+
+  if (row_ok) {
+    if (inf != 0) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = T(0);
+    }
+    if (LAYOUT == kRowMajor) {
+      if (FULL) {
+        store_vec<T, NT>(A + sA + static_cast<int64_t>(pos) * NT, a);
+        store_vec<T, RT>(B + sB + static_cast<int64_t>(pos) * RT, b);
+      } else {
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+          if (j < n) A[sA + pos * n + j] = a[j];
+#pragma unroll
+        for (int c = 0; c < RT; ++c)
+          if (c < nrhs) B[sB + pos * nrhs + c] = b[c];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+        if (FULL || j < n) A[sA + j * n + pos] = a[j];
+#pragma unroll
+      for (int c = 0; c < RT; ++c)
+        if (FULL || c < nrhs) B[sB + c * n + pos] = b[c];
+    }
+    ipiv[s * n + pos] = my_ipiv;
+    if (t == 0) info[s] = inf;
+  }
+}
+
+template <typename T, int NT, int RT, int LAYOUT>
+cudaError_t launch_tier(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
+                        int32_t* info, cudaStream_t stream) {
+  constexpr int per_block = kWarps * (32 / NT);
+  const int64_t blocks = (batch + per_block - 1) / per_block;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  if (n == NT && nrhs == RT)
+    lu_reg_kernel<T, NT, RT, LAYOUT, true>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv, info);
+  else
+    lu_reg_kernel<T, NT, RT, LAYOUT, false>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv, info);
+  return cudaGetLastError();
+}
+
+template <typename T, int NT, int LAYOUT>
+cudaError_t launch_rhs(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv, int32_t* info,
+                       cudaStream_t stream) {
+  if (nrhs <= 1) return launch_tier<T, NT, 1, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+  if (nrhs <= 2) return launch_tier<T, NT, 2, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+  if (nrhs <= 4) return launch_tier<T, NT, 4, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+  return launch_tier<T, NT, 8, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+}
+
+template <typename T, int LAYOUT>
+cudaError_t launch_layout(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
+                          int32_t* info, cudaStream_t stream) {
+  if (n <= 4) return launch_rhs<T, 4, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+  if (n <= 8) return launch_rhs<T, 8, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+  if (n <= 16) return launch_rhs<T, 16, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+  return launch_rhs<T, 32, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+}
+
+}  // namespace lu_reg_detail
+}  // namespace bsolve

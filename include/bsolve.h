@@ -1,0 +1,150 @@
+/*
+ * bsolve.h -- C ABI of libbsolve.so: batched solution of many independent small dense
+ * linear systems A x = b on one GPU (sm_103a).
+ *
+ * Every entry point solves `batch` independent systems in one asynchronous launch on
+ * the caller's CUDA stream. All matrix and vector pointers are DEVICE pointers owned by
+ * the caller; the library allocates no memory, keeps no state between calls and never
+ * synchronizes the host. Results are valid once the stream has reached the launch;
+ * the per-system `info` array is read back by the caller when it needs it.
+ *
+ * Batched storage: system s of a batched operand starts at element s * (elements per
+ * system); there is no padding between systems. Offsets are 64-bit.
+ *
+ * Errors are reported synchronously, before anything is launched:
+ *   BS_ERR_INVALID_ARG  null pointer, negative size, or a base address not 16-byte aligned;
+ *   BS_ERR_UNSUPPORTED  a shape, dtype, layout or fill with no kernel instance (there is
+ *                       no CPU fallback: the caller chooses another path);
+ *   BS_ERR_CUDA         the launch itself failed (bs_last_cuda_error() gives the code).
+ * batch == 0 returns BS_OK and launches nothing. Numerical failure of a system (a
+ * singular pivot, a minor that is not positive definite) is not an error of the call:
+ * it is reported in that system's info entry.
+ */
+#ifndef BSOLVE_H
+#define BSOLVE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BS_API __attribute__((visibility("default")))
+#else
+#define BS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BS_OK = 0,
+  BS_ERR_INVALID_ARG = 1,
+  BS_ERR_UNSUPPORTED = 2,
+  BS_ERR_CUDA = 3
+} bs_status;
+
+typedef enum { BS_FP32 = 0, BS_FP64 = 1 } bs_dtype;
+
+/* Element (r, c) of an n x m operand lives at r*m + c (row-major) or c*n + r
+ * (column-major) within its system. */
+typedef enum { BS_ROW_MAJOR = 0, BS_COL_MAJOR = 1 } bs_layout;
+
+typedef enum { BS_LOWER = 0, BS_UPPER = 1 } bs_fill;
+
+/*
+ * LU factorization with partial pivoting and solve (getrf + getrs), in place.
+ *
+ * Source: TDLS API, "solver_static.hpp File Reference" (CooperativeLUppSolverStatic),
+ * Detailed Description -- right-looking LU with partial pivoting, one system per thread
+ * group, rows held in registers, L y = P b folded into the factorization, then U x = y;
+ * RUDA docs, "ruSOLVER: small-matrix kernel optimisation" -- lowest-row tie rule,
+ * status 0 / first failing pivot, failed outputs zeroed.
+ *
+ *   A     batch x n x n, in `layout`. On return: L\U of P A in LAPACK format -- row k
+ *         holds the unit-lower multipliers of L left of the diagonal and row k of U from
+ *         the diagonal on; the diagonal holds the pivots themselves.
+ *   B     batch x n x nrhs, same layout as A. On return: X. Systems with info != 0
+ *         return X = 0.
+ *   ipiv  batch x n int32. ipiv[s*n + k] = 1-based row interchanged with row k at step k
+ *         (the LAPACK swap sequence).
+ *   info  batch int32. 0 = success; k > 0 = the first step k-1 whose pivot is singular,
+ *         i.e. !(|pivot| >= smallest normal number of the dtype) (zero, subnormal or
+ *         NaN). The sweep runs to the end with a pivot reciprocal of 1; the factor of
+ *         such a system is then unspecified.
+ * Pivot choice: the row of largest magnitude in the pivot column, lowest current row
+ * on ties. The factorization is of A itself (P A = L U) in both layouts.
+ * Supported: dtype FP32/FP64, both layouts, 1 <= n <= 64, 1 <= nrhs <= 8.
+ * stream: a cudaStream_t (0 = the legacy default stream).
+ */
+BS_API bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                 int64_t batch, void* A, void* B, int32_t* ipiv,
+                                 int32_t* info, void* stream);
+
+/*
+ * Cholesky factorization and solve (potrf + potrs) of symmetric positive definite
+ * systems, in place.
+ *
+ * Source: cuSolverDx docs, "Cholesky Factorization" (POTRF) -- only the `fill` triangle
+ * is read and replaced by the Cholesky factor, the other triangle is untouched; info
+ * reports the smallest leading minor that is not positive definite; RUDA docs,
+ * "ruSOLVER: small-matrix kernel optimisation" -- failed outputs zeroed.
+ *
+ *   A     batch x n x n in `layout`; with BS_LOWER only the lower triangle (diagonal
+ *         included) is read and replaced by L (A = L L^T); the strict upper triangle is
+ *         neither read nor written.
+ *   B     batch x n x nrhs, same layout as A. On return: X (zero where info != 0).
+ *   info  batch int32. 0 = success; k > 0 = the leading minor of order k is not positive
+ *         definite (the k-th diagonal of the factorization is not > 0, NaN included).
+ *         The factor from column k-1 on is then unspecified.
+ * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER, 1 <= n <= 64, 1 <= nrhs <= 8.
+ * BS_UPPER returns BS_ERR_UNSUPPORTED.
+ */
+BS_API bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                 int nrhs, int64_t batch, void* A, void* B, int32_t* info,
+                                 void* stream);
+
+/*
+ * Block-tridiagonal symmetric positive definite solve by the block-Cholesky
+ * (block-Thomas) sweep (bdsv = bdsv_factor + bdsv_solve), in place.
+ *
+ * Source: GLASS API reference, "Block-tridiagonal Ops", sections "Block-tridiagonal
+ * matrix-vector product" (strip and padded-vector layouts) and "Direct solve
+ * (glass::bdsv)" (the factorization and the two sweeps).
+ *
+ *   strips    batch x num_block_rows x block_size x (3*block_size): block-row br of a
+ *             system is a row-major strip [L | D | R]; entry (y, x) of slot s (LEFT 0,
+ *             MAIN 1, RIGHT 2) at strip[y*3*bs + s*bs + x]. D is read through its lower
+ *             triangle, L_br for br >= 1; L_0 and every RIGHT slot are never read.
+ *             On return: MAIN <- F_k lower triangle (its strict upper triangle keeps D_k),
+ *             LEFT <- E_k for k >= 1; RIGHT slots untouched.
+ *             F_0 = chol(D_0); E_k = L_k F_{k-1}^{-T}; F_k = chol(D_k - E_k E_k^T).
+ *   x_padded  batch x (num_block_rows + 2)*block_size: block-row br at (br+1)*block_size.
+ *             On entry the interior holds b, on return x; the two pad blocks are neither
+ *             read nor written.
+ *   info      batch int32. 0 = success; k > 0 = global index br*bs + j + 1 of the first
+ *             diagonal of the sweep that is not > 0 (the dense Cholesky factor of the
+ *             assembled matrix fails at the same minor). x is then zero and the strips
+ *             from that knot on are unspecified.
+ * Supported: dtype FP32/FP64, 1 <= block_size <= 8, num_block_rows >= 1.
+ */
+BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+                          void* strips, void* x_padded, int32_t* info, void* stream);
+
+/* Human-readable name of a status code (a static string). */
+BS_API const char* bs_status_string(bs_status status);
+
+/* The CUDA error code of the last BS_ERR_CUDA returned on this host thread (0 if none). */
+BS_API int bs_last_cuda_error(void);
+
+/* 1 if the call with these arguments has a kernel instance, else 0 (no launch). */
+BS_API int bs_getrf_getrs_supported(bs_dtype dtype, bs_layout layout, int n, int nrhs);
+BS_API int bs_potrf_potrs_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs);
+BS_API int bs_bdsv_supported(bs_dtype dtype, int num_block_rows, int block_size);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+BS_API int bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSOLVE_H */

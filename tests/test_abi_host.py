@@ -1,0 +1,107 @@
+"""The C ABI on the host: the library loads, exports every symbol bsolve.h declares,
+and rejects bad arguments before launching anything (no GPU needed: none of these calls
+reaches the CUDA runtime)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_linear_solvers_gb300 as bs
+from dense_linear_solvers_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "bsolve.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return bs.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"BS_API\s+[\w\s\*]+?\b(bs_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for must in ("bs_getrf_getrs_batched", "bs_potrf_potrs_batched", "bs_bdsv_batched",
+                 "bs_status_string"):
+        assert must in names
+    assert set(names) == set(bs.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        ctypes.cast(getattr(lib, name), ctypes.c_void_p)
+
+
+def test_status_strings(lib):
+    assert bs.status_string(bs.BS_OK) == "BS_OK"
+    assert bs.status_string(bs.BS_ERR_UNSUPPORTED) == "BS_ERR_UNSUPPORTED"
+    assert bs.status_string(99) == "BS_UNKNOWN_STATUS"
+    assert lib.bs_version() >= 100
+    assert lib.bs_last_cuda_error() == 0
+
+
+def test_supported_queries(lib):
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP32, bs.BS_ROW_MAJOR, 16, 4) == 1
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, 64, 8) == 1
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 65, 1) == 0
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 8, 9) == 0
+    assert lib.bs_getrf_getrs_supported(2, bs.BS_ROW_MAJOR, 8, 1) == 0
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_LOWER, 32, 1) == 1
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_UPPER, 32, 1) == 0
+    assert lib.bs_bdsv_supported(bs.BS_FP64, 32, 8) == 1
+    assert lib.bs_bdsv_supported(bs.BS_FP64, 32, 9) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below returns early
+
+
+def test_lu_argument_errors(lib):
+    f = lib.bs_getrf_getrs_batched
+    assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, None) == bs.BS_OK  # empty batch
+    assert f(bs.BS_FP32, 0, 16, 4, -1, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, -3, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 65, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 0, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 9, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(7, 0, 16, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 5, 16, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 4, 5, None, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, FAKE, FAKE, None, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, FAKE + 4, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP64, 1, 16, 4, 5, FAKE, FAKE + 8, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+
+
+def test_chol_argument_errors(lib):
+    f = lib.bs_potrf_potrs_batched
+    assert f(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 1, 1, 32, 1, 5, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED  # upper
+    assert f(bs.BS_FP64, 1, 0, 32, 1, 5, FAKE, None, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP64, 1, 0, 32, 1, 5, FAKE, FAKE, FAKE + 2, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP64, 1, 0, 32, -1, 5, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+
+
+def test_bdsv_argument_errors(lib):
+    f = lib.bs_bdsv_batched
+    assert f(bs.BS_FP64, 32, 8, 0, None, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 32, 9, 4, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP64, 0, 8, 4, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP64, -1, 8, 4, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP64, 32, 8, 4, FAKE, None, FAKE, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP64, 32, 8, 4, FAKE, FAKE + 8, FAKE, None) == bs.BS_ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    A = torch.zeros((2, 4, 4))
+    B = torch.zeros((2, 4, 1))
+    ipiv = torch.zeros((2, 4), dtype=torch.int32)
+    info = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        bs.bs_getrf_getrs_batched(A, B, ipiv, info)
