@@ -1,0 +1,441 @@
+"""Throughput of the batched small dense solvers on GB300: one JSON line.
+
+The headline workload is LU with partial pivoting + solve, FP32, n = 16, nrhs = 4,
+batch 65536, row-major (A, B iid N(0,1)). One step = one call of the C ABI over the
+whole batch: load, pivot search, interchange, multipliers, Schur update with the
+folded forward solve, back substitution and the single store of every output.
+
+Timing: W warm-up steps, then exactly K timed steps. Before every step the inputs are
+restored from a pristine device copy and L2 is flushed by writing a 256 MiB buffer;
+both happen outside the CUDA events, which bracket the solver launch alone on the
+launching stream. ``value`` = systems per second over all ranks (weak scaling: every
+rank solves its own batch). ``e2e`` times the same call with pinned host buffers, the
+host-to-device copy of A and B and the device-to-host copy of every output inside the
+timed region. ``cpu_baseline`` is the CPU oracle on this host's cores.
+
+``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from dense_linear_solvers_gb300 import costs  # noqa: E402
+from gen import workloads as W  # noqa: E402
+
+METRIC = "systems/sec per (n, dtype, nrhs); achieved HBM GB/s and % of roofline, 1 GB300"
+HEADLINE = "lu_f32_n16"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = {
+    "lu_f32_n16": ["lu_reg.cuh", "common.cuh"],
+    "lu_f64_n8": ["lu_reg.cuh", "common.cuh"],
+    "lu_f64_n64": ["smem_solvers.cu", "common.cuh"],
+    "chol_f64_n32": ["smem_solvers.cu", "common.cuh"],
+    "bdsv_f64_32x8": ["bdsv.cu", "common.cuh"],
+}
+KERNEL_NAMES = {
+    "lu_f32_n16": "lu_reg_kernel", "lu_f64_n8": "lu_reg_kernel", "lu_f64_n64": "lu_smem_kernel",
+    "chol_f64_n32": "chol_smem_kernel", "bdsv_f64_32x8": "bdsv_kernel",
+}
+REASONS = ["clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+           "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+def dtype_tag(dt) -> str:
+    return {np.dtype(np.float32): "f32", np.dtype(np.float64): "f64"}[np.dtype(dt)]
+
+
+def kernel_source_sha(name: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[name]:
+        with open(os.path.join(ROOT, "dense_linear_solvers_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+def ncu_traffic(name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    kernel source that is built now."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(name)
+    if not rec or rec.get("kernel_source_sha") != kernel_source_sha(name):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def workload_text(w) -> str:
+    return f"{w.name}: {w.text}"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              + ",".join(REASONS))
+
+    def __init__(self, out_path: str | None):
+        self.proc = None
+        self.path = out_path or os.path.join("/tmp", f"bsolve_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, device_index: int) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9 or parts[0] != str(device_index):
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(REASONS, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name.split(".")[-1])
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class Problem:
+    """Device buffers of one workload, a pristine copy and the solver call."""
+
+    def __init__(self, name: str, batch: int | None, device):
+        import torch
+        import dense_linear_solvers_gb300 as bs
+        self.bs, self.torch = bs, torch
+        self.d = W.make(name, batch)
+        self.w = self.d["workload"]
+        self.batch = self.d["batch"]
+        self.device = device
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        if self.w.op == "bdsv":
+            self.inputs = [t(self.d["strips"]), t(self.d["x"])]
+        else:
+            self.inputs = [t(self.d["A"]), t(self.d["B"])]
+        self.work = [x.clone() for x in self.inputs]
+        n = self.w.n
+        self.info = torch.zeros(self.batch, dtype=torch.int32, device=device)
+        self.ipiv = (torch.zeros((self.batch, n), dtype=torch.int32, device=device)
+                     if self.w.op == "getrf_getrs" else None)
+        elem = np.dtype(self.w.dtype).itemsize
+        self.bytes_per_sys, self.flops_per_sys = costs.per_system(
+            self.w.op, n, self.w.nrhs, elem, self.w.nbr)
+
+    def call(self, bufs=None, stream=None):
+        bs = self.bs
+        a, b = bufs if bufs is not None else self.work
+        if self.w.op == "getrf_getrs":
+            bs.bs_getrf_getrs_batched(a, b, self.ipiv, self.info, self.w.layout, stream)
+        elif self.w.op == "potrf_potrs":
+            bs.bs_potrf_potrs_batched(a, b, self.info, self.w.layout, bs.BS_LOWER, stream)
+        else:
+            bs.bs_bdsv_batched(a, b, self.info, stream)
+
+    def restore(self):
+        for dst, src in zip(self.work, self.inputs):
+            dst.copy_(src)
+
+
+def time_device(prob: Problem, steps: int, warmup: int, flush, min_warm_s: float = 0.0):
+    torch = prob.torch
+    stream = torch.cuda.current_stream()
+    t0 = time.time()
+    i = 0
+    while i < warmup or time.time() - t0 < min_warm_s:
+        prob.restore()
+        flush.fill_(1.0)
+        prob.call(stream=stream)
+        i += 1
+    torch.cuda.synchronize()
+    times = []
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for k in range(steps):
+        prob.restore()
+        flush.fill_(1.0)
+        evs[k][0].record(stream)
+        prob.call(stream=stream)
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
+    return times
+
+
+def time_e2e(prob: Problem, steps: int, warmup: int):
+    """Pinned host inputs -> device, the C-ABI call, every output -> pinned host."""
+    torch = prob.torch
+    stream = torch.cuda.current_stream()
+    host_in = [x.cpu().pin_memory() for x in prob.inputs]
+    outs = [x for x in (prob.work[0], prob.work[1], prob.ipiv, prob.info) if x is not None]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    def one():
+        for dst, src in zip(prob.work, host_in):
+            dst.copy_(src, non_blocking=True)
+        prob.call(stream=stream)
+        for dst, src in zip(host_out, outs):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times, h2d, d2h
+
+
+def roofline(prob: Problem, ms: float, peaks: dict, name: str) -> dict:
+    elem = np.dtype(prob.w.dtype).itemsize
+    bytes_launch = prob.bytes_per_sys * prob.batch
+    flops_launch = prob.flops_per_sys * prob.batch
+    hbm = peaks.get("hbm_gbs")
+    hbm_src = "measured" if hbm else "fallback"
+    hbm = hbm or costs.HBM_FALLBACK_GBS
+    alu = costs.alu_peak_tflops(elem)
+    t_hbm = bytes_launch / (hbm * 1e9)
+    t_alu = flops_launch / (alu * 1e12)
+    traffic = ncu_traffic(name)
+    if t_hbm >= t_alu:
+        ach = bytes_launch / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "traffic": traffic,
+                "peak_source": f"{hbm_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": bytes_launch}
+    ach = flops_launch / (ms * 1e-3) / 1e12
+    return {"bound": "alu", "achieved": round(ach, 4), "peak": round(alu, 4), "unit": "TFLOP/s",
+            "frac": round(ach / alu, 4), "traffic": traffic,
+            "peak_source": (f"{'FP64' if elem == 8 else 'FP32'} FMA: 152 SMs x "
+                            f"{costs.FP64_FMA_PER_CLK_PER_SM if elem == 8 else costs.FP32_FMA_PER_CLK_PER_SM}"
+                            " FMA/clk x 2 flops x 2070 MHz"),
+            "algorithmic_flops_per_launch": flops_launch,
+            "achieved_gbs": round(bytes_launch / (ms * 1e-3) / 1e9, 1)}
+
+
+def cpu_baseline(name: str, batch: int | None, seconds: float) -> dict:
+    import oracle
+    d = W.make(name, batch)
+    w = d["workload"]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    reps, t0 = 0, time.time()
+    while True:
+        if w.op == "getrf_getrs":
+            oracle.getrf_getrs(d["A"], d["B"], w.layout, nthreads=cores)
+        elif w.op == "potrf_potrs":
+            oracle.potrf_potrs(d["A"], d["B"], w.layout, nthreads=cores)
+        else:
+            oracle.bdsv(d["strips"], d["x"], nthreads=cores)
+        reps += 1
+        el = time.time() - t0
+        if el >= seconds:
+            break
+    return {"value": round(reps * d["batch"] / el, 1), "unit": "systems/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{reps} passes over the {d['batch']}-system batch of {name} "
+                      f"({el:.1f} s wall, oracle built with g++ -O2, systems split over "
+                      f"{cores} threads)"}
+
+
+def run_native(args) -> None:
+    import torch
+    import torch.distributed as dist
+    import dense_linear_solvers_gb300 as bs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    bs.lib()
+    peaks = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    prob = Problem(args.workload, None, dev)
+    sampler = ClockSampler(os.path.join(args.out, "clocks_bench.csv") if args.out else None)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    times = time_device(prob, args.steps, args.warmup, flush, min_warm_s=args.warm_seconds)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop(local)
+    ms = statistics.fmean(times)
+    e2e_times, h2d, d2h = time_e2e(prob, max(3, min(args.steps, 20)), 2)
+    e2e_ms = statistics.fmean(e2e_times)
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    total = prob.batch * world
+    w = prob.w
+    line = {
+        "metric": METRIC,
+        "value": round(total / (ms * 1e-3), 1),
+        "unit": "systems/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype_tag(w.dtype),
+        "data": "synthetic (seeded NumPy draws with the workload's distributions)",
+        "config": {
+            "workload": workload_text(w), "op": w.op, "n": w.n, "nrhs": w.nrhs,
+            "batch_per_gpu": prob.batch, "layout": "row-major" if w.layout == 0 else "column-major",
+            "l2": "flushed before every step (256 MiB write); inputs restored from a pristine "
+                  "device copy; both outside the CUDA events around the solver launch",
+            "ms_per_step_min": round(min(times), 5),
+            "ms_per_step_median": round(statistics.median(times), 5),
+            "parallelism": f"batch shard x{world} (independent systems, no collective)",
+        },
+        "roofline": roofline(prob, ms, peaks, args.workload),
+        "e2e": {"value": round(total / (e2e_ms * 1e-3), 1), "unit": "systems/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    line["cpu_baseline"] = cpu_baseline(args.workload, None, args.cpu_seconds)
+    if not args.headline_only:
+        extra = {}
+        for name in W.WORKLOADS:
+            if name == args.workload:
+                continue
+            p = Problem(name, None, dev)
+            tt = time_device(p, min(args.steps, 10), 2, flush)
+            m = statistics.fmean(tt)
+            extra[name] = {"systems_per_s": round(p.batch / (m * 1e-3), 1), "ms_per_step": round(m, 4),
+                           "batch": p.batch, "roofline": roofline(p, m, peaks, name)}
+            del p
+        extra[args.workload] = {"systems_per_s": line["value"] / world, "ms_per_step": line["ms_per_step"],
+                                "batch": prob.batch, "roofline": line["roofline"]}
+        line["workloads"] = extra
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    d = W.make(args.workload, None)
+    w = d["workload"]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+    def one():
+        if w.op == "getrf_getrs":
+            oracle.getrf_getrs(d["A"], d["B"], w.layout, nthreads=cores)
+        elif w.op == "potrf_potrs":
+            oracle.potrf_potrs(d["A"], d["B"], w.layout, nthreads=cores)
+        else:
+            oracle.bdsv(d["strips"], d["x"], nthreads=cores)
+
+    for _ in range(args.warmup):
+        one()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        times.append((time.perf_counter() - t0) * 1e3)
+    ms = statistics.fmean(times)
+    value = round(d["batch"] / (ms * 1e-3), 1)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "systems/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_tag(w.dtype),
+        "data": "synthetic (seeded NumPy draws with the workload's distributions)",
+        "config": {"workload": workload_text(w), "op": w.op, "n": w.n, "nrhs": w.nrhs,
+                   "batch_per_gpu": d["batch"],
+                   "layout": "row-major" if w.layout == 0 else "column-major"},
+        "cpu_baseline": {"value": value, "unit": "systems/s", "cores": cores, "kind": "oracle",
+                         "sample": f"the whole {d['batch']}-system batch per step on {cores} "
+                                   f"host threads (sequential C++ oracle, g++ -O2)"},
+        "e2e": {"value": value, "unit": "systems/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default=HEADLINE)
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the per-workload table of the other four workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--warm-seconds", type=float, default=1.0,
+                    help="keep warming up for at least this long (lets the clock sampler "
+                         "see the GPU under this load)")
+    ap.add_argument("--out", default=None, help="folder for the clock samples")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "native":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -167,7 +167,13 @@ def bdsv_backward_error(strips, b_pad, x_pad):
     window over the padded vector), normalized as the dense backward error."""
     batch, nbr, bs_ = strips.shape[0], strips.shape[1], strips.shape[2]
     from tests.numerics import residual_dd
-    Ablk = strips.reshape(batch * nbr, bs_, 3 * bs_).astype(np.float64)
+    strips = np.array(strips, np.float64)
+    strips[:, 0, :, :bs_] = 0.0            # L_0 and R_{nbr-1} are not part of the matrix
+    strips[:, nbr - 1, :, 2 * bs_:] = 0.0
+    x_pad = np.array(x_pad, np.float64)
+    x_pad[:, :bs_] = 0.0                   # the matvec window reads zero pads
+    x_pad[:, (nbr + 1) * bs_:] = 0.0
+    Ablk = strips.reshape(batch * nbr, bs_, 3 * bs_)
     win = np.stack([x_pad[:, br * bs_: br * bs_ + 3 * bs_] for br in range(nbr)], axis=1)
     Xw = win.reshape(batch * nbr, 3 * bs_, 1).astype(np.float64)
     Bb = b_pad[:, bs_:(nbr + 1) * bs_].reshape(batch * nbr, bs_, 1).astype(np.float64)
