@@ -41,13 +41,13 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {
     "lu_f32_n16": ["lu_reg.cuh", "common.cuh"],
     "lu_f64_n8": ["lu_reg.cuh", "common.cuh"],
-    "lu_f64_n64": ["smem_solvers.cu", "common.cuh"],
-    "chol_f64_n32": ["smem_solvers.cu", "common.cuh"],
+    "lu_f64_n64": ["lu_cta.cu", "common.cuh"],
+    "chol_f64_n32": ["chol_sys.cu", "common.cuh"],
     "bdsv_f64_32x8": ["bdsv.cu", "common.cuh"],
 }
 KERNEL_NAMES = {
-    "lu_f32_n16": "lu_reg_kernel", "lu_f64_n8": "lu_reg_kernel", "lu_f64_n64": "lu_smem_kernel",
-    "chol_f64_n32": "chol_smem_kernel", "bdsv_f64_32x8": "bdsv_kernel",
+    "lu_f32_n16": "lu_reg_kernel", "lu_f64_n8": "lu_reg_kernel", "lu_f64_n64": "lu_cta_kernel",
+    "chol_f64_n32": "chol_sys_kernel", "bdsv_f64_32x8": "bdsv_kernel",
 }
 REASONS = ["clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
            "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
@@ -297,7 +297,7 @@ def run_native(args) -> None:
     peaks = measured_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    prob = Problem(args.workload, None, dev)
+    prob = Problem(args.workload, args.batch, dev)
     sampler = ClockSampler(os.path.join(args.out, "clocks_bench.csv") if args.out else None)
     sampler.start()
     if world > 1:
@@ -349,7 +349,7 @@ def run_native(args) -> None:
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
-    line["cpu_baseline"] = cpu_baseline(args.workload, None, args.cpu_seconds)
+    line["cpu_baseline"] = cpu_baseline(args.workload, args.batch, args.cpu_seconds)
     if not args.headline_only:
         extra = {}
         for name in W.WORKLOADS:
@@ -375,7 +375,7 @@ def run_reference(args) -> None:
         return
     import oracle
     oracle.build()
-    d = W.make(args.workload, None)
+    d = W.make(args.workload, args.batch)
     w = d["workload"]
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
@@ -421,6 +421,8 @@ def main(argv=None) -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default=HEADLINE)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (profiling runs on a smaller case)")
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the per-workload table of the other four workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

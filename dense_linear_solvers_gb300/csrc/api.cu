@@ -79,12 +79,20 @@ bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill,
   if (!A || !B || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e =
-      dtype == BS_FP32
-          ? bsolve::launch_chol_smem<float>(layout, n, nrhs, batch, static_cast<float*>(A),
-                                            static_cast<float*>(B), info, s)
-          : bsolve::launch_chol_smem<double>(layout, n, nrhs, batch, static_cast<double*>(A),
-                                             static_cast<double*>(B), info, s);
+  cudaError_t e;
+  if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_sys<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                             static_cast<float*>(B), info, s)
+            : bsolve::launch_chol_sys<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                              static_cast<double*>(B), info, s);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_smem<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                              static_cast<float*>(B), info, s)
+            : bsolve::launch_chol_smem<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                               static_cast<double*>(B), info, s);
+  }
   return from_cuda(e);
 }
 

@@ -1,0 +1,216 @@
+// Lower Cholesky + solve for n <= 32: sixteen systems per block, computed in lockstep
+// with one system per lane.
+//
+// On a part whose FP64 pipe runs at 1/64 of the FP32 lane rate and charges a warp
+// instruction whatever its active lanes, the per-column scalar chain of Cholesky (a
+// square root and a reciprocal, several FP64 instructions each) is ruinous when a warp
+// works on one system: it costs as much as a whole column's update. Here every warp
+// instruction works on the same element of sixteen systems (lane l -> system l % 16,
+// half-warp l / 16 -> one of two element slots), so the scalar chain of sixteen systems
+// costs one instruction sequence, and the trailing update runs as many elements per
+// instruction as there are lanes, with no idle lanes however small the trailing
+// triangle gets.
+//
+// Each system lives in shared memory as a packed lower triangle (row i at i(i+1)/2)
+// followed by its right-hand sides (row i at tri + i*nrhs). The per-system stride is an
+// odd number of elements, so the sixteen lanes that touch the same element of sixteen
+// systems hit sixteen different banks.
+//
+// The factorization is right-looking (cuSolverDx docs, "Cholesky Factorization": only
+// the lower triangle is read and replaced by L; info = the smallest leading minor that
+// is not positive definite), with the forward solve folded into it; then L^T x = y.
+// The arithmetic is the CPU oracle's, operation by operation. A system whose minor
+// fails keeps computing (no branch depends on the data) and returns X = 0.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsolve {
+namespace {
+
+constexpr int kSys = 16;      // systems per block
+constexpr int kWarps = 4;     // warps per block
+constexpr int kSlots = kWarps * 2;
+constexpr int kMaxN = 32;
+
+__host__ __device__ inline int tri(int i) { return i * (i + 1) / 2; }
+
+__host__ __device__ inline int sys_stride(int n, int nrhs) { return (tri(n) + n * nrhs) | 1; }
+
+template <typename T>
+__device__ __forceinline__ T rcp_rn(T x);
+template <>
+__device__ __forceinline__ float rcp_rn<float>(float x) { return __frcp_rn(x); }
+template <>
+__device__ __forceinline__ double rcp_rn<double>(double x) { return __drcp_rn(x); }
+
+template <typename T>
+__device__ __forceinline__ T sqrt_rn(T x);
+template <>
+__device__ __forceinline__ float sqrt_rn<float>(float x) { return __fsqrt_rn(x); }
+template <>
+__device__ __forceinline__ double sqrt_rn<double>(double x) { return __dsqrt_rn(x); }
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
+                T* __restrict__ B, int32_t* __restrict__ info) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int D = sys_stride(n, nrhs);
+  const int TRI = tri(n);
+  T* const M = reinterpret_cast<T*>(smem_raw);     // kSys systems, stride D
+  T* const rr = M + kSys * D;                       // [kSys][kMaxN] reciprocals
+  int* const sinfo = reinterpret_cast<int*>(rr + kSys * kMaxN);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int s = lane & (kSys - 1);                  // system of this lane
+  const int slot = warp * 2 + (lane >> 4);          // element slot of this lane
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kSys;
+  T* const Ms = M + s * D;                          // this lane's system
+  T* const Ys = Ms + TRI;                           // its right-hand sides, [i][c]
+
+  // load: warp w copies systems w, w+4, ...; lanes walk the rows of a column
+  for (int q = warp; q < kSys; q += kWarps) {
+    const int64_t sys = s0 + q;
+    T* const Mq = M + q * D;
+    if (sys < batch) {
+      const T* As = A + sys * n * n;
+      const T* Bs = B + sys * n * nrhs;
+      for (int j = 0; j < n; ++j)
+        for (int i = j + lane; i < n; i += 32)
+          Mq[tri(i) + j] = layout == kColMajor ? As[j * n + i] : As[i * n + j];
+      for (int c = 0; c < nrhs; ++c)
+        for (int i = lane; i < n; i += 32)
+          Mq[TRI + i * nrhs + c] = layout == kColMajor ? Bs[c * n + i] : Bs[i * nrhs + c];
+    } else {
+      // a system past the end of the batch: an identity keeps its lanes finite
+      for (int e = lane; e < D; e += 32) Mq[e] = T(0);
+      for (int i = lane; i < n; i += 32) Mq[tri(i) + i] = T(1);
+    }
+    if (lane == 0) sinfo[q] = 0;
+  }
+  __syncthreads();
+
+  for (int k = 0; k < n; ++k) {
+    // A: pivot square root and reciprocal, one lane per system
+    if (tid < kSys) {
+      const T d = Ms[tri(k) + k];
+      if (!(d > T(0)) && sinfo[s] == 0) sinfo[s] = k + 1;
+      const T l = sqrt_rn<T>(d);
+      Ms[tri(k) + k] = l;
+      rr[s * kMaxN + k] = rcp_rn<T>(l);
+    }
+    __syncthreads();
+    // B: scale column k below the diagonal, and y_k
+    {
+      const int m = n - 1 - k;
+      const T r = rr[s * kMaxN + k];
+      for (int e = slot; e < m + nrhs; e += kSlots) {
+        if (e < m) {
+          const int i = k + 1 + e;
+          Ms[tri(i) + k] = Ms[tri(i) + k] * r;
+        } else {
+          const int c = e - m;
+          Ys[k * nrhs + c] = Ys[k * nrhs + c] * r;
+        }
+      }
+    }
+    __syncthreads();
+    // C: trailing lower triangle (row by row: row i holds columns k+1..i), then the
+    //    forward solve of rows k+1..n-1
+    {
+      const int m = n - 1 - k;
+      const int T_k = m * (m + 1) / 2;
+      int i = k + 1, j = k + 1 + slot;
+      while (i < n && j > i) {
+        j -= i - k;
+        ++i;
+      }
+      int e = slot;
+      for (; e < T_k; e += kSlots) {
+        const int ti = tri(i);
+        Ms[ti + j] = fma_rn<T>(-Ms[ti + k], Ms[tri(j) + k], Ms[ti + j]);
+        j += kSlots;
+        while (i < n && j > i) {
+          j -= i - k;
+          ++i;
+        }
+      }
+      for (e -= T_k; e < m * nrhs; e += kSlots) {
+        const int ii = k + 1 + e / nrhs, c = e - (e / nrhs) * nrhs;
+        Ys[ii * nrhs + c] = fma_rn<T>(-Ms[tri(ii) + k], Ys[k * nrhs + c], Ys[ii * nrhs + c]);
+      }
+    }
+    __syncthreads();
+  }
+
+  // L^T x = y, from the last row
+  for (int k = n - 1; k >= 0; --k) {
+    const T r = rr[s * kMaxN + k];
+    for (int c = slot; c < nrhs; c += kSlots) Ys[k * nrhs + c] = Ys[k * nrhs + c] * r;
+    __syncthreads();
+    const int tk = tri(k);
+    for (int e = slot; e < k * nrhs; e += kSlots) {
+      const int i = e / nrhs, c = e - i * nrhs;
+      Ys[i * nrhs + c] = fma_rn<T>(-Ms[tk + i], Ys[k * nrhs + c], Ys[i * nrhs + c]);
+    }
+    __syncthreads();
+  }
+
+  // store: the lower triangle, X (zero for a failed system), info
+  for (int q = warp; q < kSys; q += kWarps) {
+    const int64_t sys = s0 + q;
+    if (sys >= batch) continue;
+    const T* const Mq = M + q * D;
+    T* As = A + sys * n * n;
+    T* Bs = B + sys * n * nrhs;
+    const bool failed = sinfo[q] != 0;
+    for (int j = 0; j < n; ++j)
+      for (int i = j + lane; i < n; i += 32) {
+        const T v = Mq[tri(i) + j];
+        if (layout == kColMajor)
+          As[j * n + i] = v;
+        else
+          As[i * n + j] = v;
+      }
+    for (int c = 0; c < nrhs; ++c)
+      for (int i = lane; i < n; i += 32) {
+        const T v = failed ? T(0) : Mq[TRI + i * nrhs + c];
+        if (layout == kColMajor)
+          Bs[c * n + i] = v;
+        else
+          Bs[i * nrhs + c] = v;
+      }
+    if (lane == 0) info[sys] = sinfo[q];
+  }
+}
+
+}  // namespace
+
+size_t chol_sys_bytes(int n, int nrhs, int elem_size) {
+  return static_cast<size_t>(kSys) * sys_stride(n, nrhs) * elem_size +
+         static_cast<size_t>(kSys) * kMaxN * elem_size + kSys * sizeof(int);
+}
+
+template <typename T>
+cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                            int32_t* info, cudaStream_t stream) {
+  if (n > kMaxN) return cudaErrorInvalidValue;
+  const int64_t blocks = (batch + kSys - 1) / kSys;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const size_t bytes = chol_sys_bytes(n, nrhs, sizeof(T));
+  cudaError_t e = cudaFuncSetAttribute(chol_sys_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  chol_sys_kernel<T><<<static_cast<unsigned>(blocks), kWarps * 32, bytes, stream>>>(
+      n, nrhs, layout, batch, A, B, info);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_chol_sys<float>(int, int, int, int64_t, float*, float*, int32_t*,
+                                            cudaStream_t);
+template cudaError_t launch_chol_sys<double>(int, int, int, int64_t, double*, double*,
+                                             int32_t*, cudaStream_t);
+
+}  // namespace bsolve

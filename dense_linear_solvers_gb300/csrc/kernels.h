@@ -21,13 +21,19 @@ template <typename T>
 cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                              int32_t* info, cudaStream_t stream);
 
+// Lower Cholesky + solve, sixteen systems per block in lockstep, 1 <= n <= 32.
+template <typename T>
+cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                            int32_t* info, cudaStream_t stream);
+
 // Block-tridiagonal block-Cholesky sweep, one thread per system, 1 <= bs <= 8.
 template <typename T>
 cudaError_t launch_bdsv(int nbr, int bs, int64_t batch, T* strips, T* xpad, int32_t* info,
                         cudaStream_t stream);
 
 // Shared memory one system needs in the shared-memory kernels.
-size_t lu_smem_bytes(int n, int nrhs, int elem_size);
+size_t lu_cta_bytes(int n, int nrhs, int elem_size);
 size_t chol_smem_bytes(int n, int nrhs, int elem_size);
+size_t chol_sys_bytes(int n, int nrhs, int elem_size);
 
 }  // namespace bsolve

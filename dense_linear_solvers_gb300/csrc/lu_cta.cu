@@ -1,0 +1,223 @@
+// LU with partial pivoting + solve for 32 < n <= 64: one system per block of four warps,
+// the system resident in shared memory.
+//
+// The system is one n x P row-major tile M = [A | B] (P = n + nrhs rounded up to an
+// odd number of elements: a walk down a column touches distinct banks). The right-
+// looking factorization follows LAPACK's order with physical row interchanges (TDLS
+// API, "solver_static.hpp File Reference", Detailed Description: physical and logical
+// interchanges choose the same pivots and run the same operations):
+//   phase 1 (warp 0): pivot search over column k with integer magnitude keys and the
+//     lowest-row tie rule, interchange of rows k and p, the correctly rounded pivot
+//     reciprocal, the multipliers of column k;
+//   phase 2 (all warps): the rank-1 update of rows k+1.., columns k+1.. of [A | B]
+//     (the forward solve L y = P b folded in), spread element by element over the
+//     block's 128 lanes so that lanes stay busy however small the trailing block gets.
+// On this part a warp FP64 instruction is charged whatever its active lanes, so the
+// lane count that does useful FP64 work is what sets the speed; four warps per system
+// also give the SM enough warps to cover each system's serial pivot phase.
+// Back substitution runs by blocks of four rows: warp 0 solves the 4 x 4 diagonal block,
+// then all warps apply its four columns to every row above, each element taking the four
+// updates in decreasing column order -- the oracle's order, so the arithmetic is the
+// CPU oracle's, operation by operation.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsolve {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kBlk = 4;  // rows per back-substitution block
+
+__host__ __device__ inline int odd_pitch(int w) { return w | 1; }
+
+template <typename T>
+__device__ __forceinline__ T rcp_rn(T x);
+template <>
+__device__ __forceinline__ float rcp_rn<float>(float x) { return __frcp_rn(x); }
+template <>
+__device__ __forceinline__ double rcp_rn<double>(double x) { return __drcp_rn(x); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
+              T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info) {
+  using Key = typename Traits<T>::Key;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t s = blockIdx.x;
+  if (s >= batch) return;
+  const int W = n + nrhs;
+  const int P = odd_pitch(W);
+  T* const M = reinterpret_cast<T*>(smem_raw);
+  T* const rcp = M + n * P;
+  int* const piv = reinterpret_cast<int*>(rcp + n);
+  __shared__ int s_info;
+
+  A += s * n * n;
+  B += s * n * nrhs;
+  if (layout == kRowMajor) {
+    for (int e = tid; e < n * n; e += kThreads) {
+      const int i = e / n, j = e - i * n;
+      M[i * P + j] = A[e];
+    }
+    for (int e = tid; e < n * nrhs; e += kThreads) {
+      const int i = e / nrhs, c = e - i * nrhs;
+      M[i * P + n + c] = B[e];
+    }
+  } else {
+    for (int e = tid; e < n * n; e += kThreads) {
+      const int j = e / n, i = e - j * n;
+      M[i * P + j] = A[e];
+    }
+    for (int e = tid; e < n * nrhs; e += kThreads) {
+      const int c = e / n, i = e - c * n;
+      M[i * P + n + c] = B[e];
+    }
+  }
+  if (tid == 0) s_info = 0;
+  __syncthreads();
+
+  for (int k = 0; k < n; ++k) {
+    if (warp == 0) {
+      // pivot search over rows k..n-1 of column k; a lane keeps its first maximum
+      Key best = 0;
+      int bi = 0x7FFFFFFF;
+      for (int i = k + lane; i < n; i += 32) {
+        const Key key = pivot_key<T>(M[i * P + k], i == k);
+        if (key > best) {
+          best = key;
+          bi = i;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const Key ob = shfl_xor_key(best, off, 32);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+        if (ob > best || (ob == best && oi < bi)) {
+          best = ob;
+          bi = oi;
+        }
+      }
+      const int p = bi;
+      const bool ok = pivot_ok<T>(best);
+      if (lane == 0) {
+        piv[k] = p + 1;
+        if (!ok && s_info == 0) s_info = k + 1;
+      }
+      if (p != k) {
+        for (int j = lane; j < W; j += 32) {
+          const T t = M[k * P + j];
+          M[k * P + j] = M[p * P + j];
+          M[p * P + j] = t;
+        }
+      }
+      __syncwarp();
+      const T r = ok ? rcp_rn<T>(M[k * P + k]) : T(1);
+      if (lane == 0) rcp[k] = r;
+      for (int i = k + 1 + lane; i < n; i += 32) M[i * P + k] = M[i * P + k] * r;
+    }
+    __syncthreads();
+    // rank-1 update of rows k+1..n-1, columns k+1..W-1, walked column by column
+    const int m = n - k - 1;
+    const int w = W - k - 1;
+    if (m > 0) {
+      const int total = m * w;
+      const int dq = kThreads / m, dr = kThreads - dq * m;
+      int ii = tid % m, jj = tid / m;
+      for (int e = tid; e < total; e += kThreads) {
+        const int i = k + 1 + ii, j = k + 1 + jj;
+        M[i * P + j] = fma_rn<T>(-M[i * P + k], M[k * P + j], M[i * P + j]);
+        ii += dr;
+        jj += dq;
+        if (ii >= m) {
+          ii -= m;
+          ++jj;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // U x = y by blocks of kBlk rows, from the last block
+  const int nblk = (n + kBlk - 1) / kBlk;
+  for (int cb = nblk - 1; cb >= 0; --cb) {
+    const int lo = cb * kBlk, hi = min(n, lo + kBlk);
+    if (warp == 0) {
+      for (int i = hi - 1; i >= lo; --i) {
+        const T r = rcp[i];
+        for (int c = lane; c < nrhs; c += 32) M[i * P + n + c] = M[i * P + n + c] * r;
+        __syncwarp();
+        const int cnt = (i - lo) * nrhs;
+        for (int e = lane; e < cnt; e += 32) {
+          const int c = e / (i - lo), i2 = lo + (e - c * (i - lo));
+          M[i2 * P + n + c] = fma_rn<T>(-M[i2 * P + i], M[i * P + n + c], M[i2 * P + n + c]);
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    // the block's columns applied to every row above it, decreasing column order
+    const int cnt = lo * nrhs;
+    for (int e = tid; e < cnt; e += kThreads) {
+      const int c = e / lo, i2 = e - c * lo;
+      T y = M[i2 * P + n + c];
+      for (int i = hi - 1; i >= lo; --i) y = fma_rn<T>(-M[i2 * P + i], M[i * P + n + c], y);
+      M[i2 * P + n + c] = y;
+    }
+    __syncthreads();
+  }
+
+  const bool zero_x = s_info != 0;
+  if (layout == kRowMajor) {
+    for (int e = tid; e < n * n; e += kThreads) {
+      const int i = e / n, j = e - i * n;
+      A[e] = M[i * P + j];
+    }
+    for (int e = tid; e < n * nrhs; e += kThreads) {
+      const int i = e / nrhs, c = e - i * nrhs;
+      B[e] = zero_x ? T(0) : M[i * P + n + c];
+    }
+  } else {
+    for (int e = tid; e < n * n; e += kThreads) {
+      const int j = e / n, i = e - j * n;
+      A[e] = M[i * P + j];
+    }
+    for (int e = tid; e < n * nrhs; e += kThreads) {
+      const int c = e / n, i = e - c * n;
+      B[e] = zero_x ? T(0) : M[i * P + n + c];
+    }
+  }
+  for (int k = tid; k < n; k += kThreads) ipiv[s * n + k] = piv[k];
+  if (tid == 0) info[s] = s_info;
+}
+
+}  // namespace
+
+size_t lu_cta_bytes(int n, int nrhs, int elem_size) {
+  const int P = odd_pitch(n + nrhs);
+  return static_cast<size_t>(n) * P * elem_size + static_cast<size_t>(n) * elem_size +
+         static_cast<size_t>(n) * sizeof(int);
+}
+
+template <typename T>
+cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                           int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const size_t bytes = lu_cta_bytes(n, nrhs, sizeof(T));
+  cudaError_t e = cudaFuncSetAttribute(lu_cta_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  lu_cta_kernel<T><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
+      n, nrhs, layout, batch, A, B, ipiv, info);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_lu_smem<float>(int, int, int, int64_t, float*, float*, int32_t*,
+                                           int32_t*, cudaStream_t);
+template cudaError_t launch_lu_smem<double>(int, int, int, int64_t, double*, double*, int32_t*,
+                                            int32_t*, cudaStream_t);
+
+}  // namespace bsolve

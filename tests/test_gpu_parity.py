@@ -180,8 +180,12 @@ def test_empty_batch_launches_nothing():
     B = torch.zeros((0, 16, 4), device=dev)
     bs.bs_getrf_getrs_batched(A, B, torch.zeros((0, 16), dtype=torch.int32, device=dev),
                               torch.zeros(0, dtype=torch.int32, device=dev))
-    bs.bs_potrf_potrs_batched(A.double(), B.double(), torch.zeros(0, dtype=torch.int32, device=dev),
+    Bc = torch.zeros((0, 4, 16), dtype=torch.float64, device=dev)  # column-major storage
+    bs.bs_potrf_potrs_batched(A.double(), Bc, torch.zeros(0, dtype=torch.int32, device=dev),
                               COL_MAJOR)
+    S = torch.zeros((0, 32, 8, 24), dtype=torch.float64, device=dev)
+    X = torch.zeros((0, 34 * 8), dtype=torch.float64, device=dev)
+    bs.bs_bdsv_batched(S, X, torch.zeros(0, dtype=torch.int32, device=dev))
     torch.cuda.synchronize()
 
 
