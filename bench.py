@@ -281,16 +281,52 @@ def cpu_baseline(name: str, batch: int | None, seconds: float) -> dict:
                       f"{cores} threads)"}
 
 
+class Ranks:
+    """Rank bookkeeping of a torchrun launch (one process per GPU, RANK / LOCAL_RANK /
+    WORLD_SIZE / MASTER_* from the environment). The systems are independent, so ranks
+    exchange nothing but a barrier and the max over ranks of their timings."""
+
+    def __init__(self, backend: str):
+        import torch.distributed as dist
+        self.dist = dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.backend = backend
+        if self.world > 1:
+            dist.init_process_group(backend)
+
+    def barrier(self) -> None:
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, values, device=None) -> list:
+        """Element-wise max over ranks of a list of floats (every rank gets it)."""
+        if self.world == 1:
+            return [float(v) for v in values]
+        import torch
+        t = torch.tensor([float(v) for v in values], dtype=torch.float64,
+                         device=device if device is not None else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return [float(v) for v in t.cpu()]
+
+    def close(self) -> None:
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+def whole_job_rate(batch_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Systems per second over all ranks: every rank solves its own batch in a step, and
+    a step lasts as long as the slowest rank's."""
+    return batch_per_rank * world / (ms_per_step * 1e-3)
+
+
 def run_native(args) -> None:
     import torch
-    import torch.distributed as dist
     import dense_linear_solvers_gb300 as bs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
+    ranks = Ranks("nccl")
+    world, rank, local = ranks.world, ranks.rank, ranks.local
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     bs.lib()
@@ -300,30 +336,23 @@ def run_native(args) -> None:
     prob = Problem(args.workload, args.batch, dev)
     sampler = ClockSampler(os.path.join(args.out, "clocks_bench.csv") if args.out else None)
     sampler.start()
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     torch.cuda.synchronize()
     times = time_device(prob, args.steps, args.warmup, flush, min_warm_s=args.warm_seconds)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     clocks = sampler.stop(local)
     ms = statistics.fmean(times)
     e2e_times, h2d, d2h = time_e2e(prob, max(3, min(args.steps, 20)), 2)
     e2e_ms = statistics.fmean(e2e_times)
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = ranks.max([ms, e2e_ms], device=dev)
     if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
+        ranks.close()
         return
-    total = prob.batch * world
     w = prob.w
     line = {
         "metric": METRIC,
-        "value": round(total / (ms * 1e-3), 1),
+        "value": round(whole_job_rate(prob.batch, world, ms), 1),
         "unit": "systems/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -344,7 +373,7 @@ def run_native(args) -> None:
             "parallelism": f"batch shard x{world} (independent systems, no collective)",
         },
         "roofline": roofline(prob, ms, peaks, args.workload),
-        "e2e": {"value": round(total / (e2e_ms * 1e-3), 1), "unit": "systems/s",
+        "e2e": {"value": round(whole_job_rate(prob.batch, world, e2e_ms), 1), "unit": "systems/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -365,8 +394,7 @@ def run_native(args) -> None:
                                 "batch": prob.batch, "roofline": line["roofline"]}
         line["workloads"] = extra
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    ranks.close()
 
 
 def run_reference(args) -> None:

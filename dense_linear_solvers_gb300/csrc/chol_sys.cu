@@ -28,7 +28,7 @@ namespace bsolve {
 namespace {
 
 constexpr int kSys = 16;      // systems per block
-constexpr int kWarps = 4;     // warps per block
+constexpr int kWarps = 8;     // warps per block
 constexpr int kSlots = kWarps * 2;
 constexpr int kMaxN = 32;
 
@@ -69,7 +69,8 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   T* const Ms = M + s * D;                          // this lane's system
   T* const Ys = Ms + TRI;                           // its right-hand sides, [i][c]
 
-  // load: warp w copies systems w, w+4, ...; lanes walk the rows of a column
+  // load: warp w copies systems w, w+kWarps, ...; lanes walk the rows of a column, with
+  // asynchronous element copies so that every load of the block is in flight at once
   for (int q = warp; q < kSys; q += kWarps) {
     const int64_t sys = s0 + q;
     T* const Mq = M + q * D;
@@ -78,17 +79,20 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       const T* Bs = B + sys * n * nrhs;
       for (int j = 0; j < n; ++j)
         for (int i = j + lane; i < n; i += 32)
-          Mq[tri(i) + j] = layout == kColMajor ? As[j * n + i] : As[i * n + j];
+          cp_async_elem<T>(Mq + tri(i) + j, layout == kColMajor ? As + j * n + i : As + i * n + j);
       for (int c = 0; c < nrhs; ++c)
         for (int i = lane; i < n; i += 32)
-          Mq[TRI + i * nrhs + c] = layout == kColMajor ? Bs[c * n + i] : Bs[i * nrhs + c];
+          cp_async_elem<T>(Mq + TRI + i * nrhs + c,
+                           layout == kColMajor ? Bs + c * n + i : Bs + i * nrhs + c);
     } else {
       // a system past the end of the batch: an identity keeps its lanes finite
       for (int e = lane; e < D; e += 32) Mq[e] = T(0);
+      __syncwarp();
       for (int i = lane; i < n; i += 32) Mq[tri(i) + i] = T(1);
     }
     if (lane == 0) sinfo[q] = 0;
   }
+  cp_async_wait_all();
   __syncthreads();
 
   for (int k = 0; k < n; ++k) {

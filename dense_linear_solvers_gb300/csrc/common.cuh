@@ -66,6 +66,29 @@ __device__ __forceinline__ double fma_rn<double>(double a, double b, double c) {
   return __fma_rn(a, b, c);
 }
 
+// Asynchronous global -> shared copies of one element (cp.async, 4 or 8 bytes; both
+// addresses aligned to the element size). Every copy a thread issues is in flight at
+// once; cp_async_wait_all() waits for the thread's own copies.
+template <typename T>
+__device__ __forceinline__ void cp_async_elem(T* smem_dst, const T* gmem_src) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+  if constexpr (sizeof(T) == 8)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem_src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+// Waits until at most N of the thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
 // Shuffle of a 64-bit integer key as two 32-bit halves.
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m,
                                                            int width) {

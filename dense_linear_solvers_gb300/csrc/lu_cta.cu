@@ -57,26 +57,28 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
 
   A += s * n * n;
   B += s * n * nrhs;
+  // asynchronous element copies: every load of the system is in flight at once
   if (layout == kRowMajor) {
     for (int e = tid; e < n * n; e += kThreads) {
       const int i = e / n, j = e - i * n;
-      M[i * P + j] = A[e];
+      cp_async_elem<T>(M + i * P + j, A + e);
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int i = e / nrhs, c = e - i * nrhs;
-      M[i * P + n + c] = B[e];
+      cp_async_elem<T>(M + i * P + n + c, B + e);
     }
   } else {
     for (int e = tid; e < n * n; e += kThreads) {
       const int j = e / n, i = e - j * n;
-      M[i * P + j] = A[e];
+      cp_async_elem<T>(M + i * P + j, A + e);
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int c = e / n, i = e - c * n;
-      M[i * P + n + c] = B[e];
+      cp_async_elem<T>(M + i * P + n + c, B + e);
     }
   }
   if (tid == 0) s_info = 0;
+  cp_async_wait_all();
   __syncthreads();
 
   for (int k = 0; k < n; ++k) {

@@ -7,9 +7,10 @@
 // interchanges, MAGMA's rowid); each lane tracks the current position of its row.
 //
 // Step k (fully unrolled, every operand index static):
-//   1. pivot search: integer magnitude keys (see common.cuh), group max by xor
-//      shuffles, then the lowest current position among the lanes holding the max
-//      (lowest-row tie rule; a rare exact tie takes a second reduction);
+//   1. pivot search: integer magnitude keys (see common.cuh), the group max by one
+//      full-warp redux.sync per group (FP32) or xor shuffles (FP64), then the lowest
+//      current position among the lanes holding the max (lowest-row tie rule; a rare
+//      exact tie takes a second reduction);
 //   2. positions k and p exchange (a bookkeeping swap, no data moves); the pivot lane
 //      records the LAPACK swap entry ipiv[k] = position(p) + 1;
 //   3. the pivot lane publishes its row (columns >= k and the right-hand sides) in a
@@ -138,11 +139,23 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     if (!FULL && k >= n) break;
     const bool cand = row_ok && pos >= k;
     const Key key = cand ? pivot_key<T>(a[k], pos == k) : Key(0);
-    Key mk = key;
+    Key mk;
+    if constexpr (sizeof(Key) == 4 && GPW <= 4) {
+      // one full-warp redux.sync per group (non-members contribute 0, below every key):
+      // shorter latency than a shuffle butterfly, and cheaper than a partial-mask redux
+      mk = 0;
 #pragma unroll
-    for (int off = G / 2; off >= 1; off >>= 1) {
-      const Key o = shfl_xor_key(mk, off, G);
-      mk = o > mk ? o : mk;
+      for (int q = 0; q < GPW; ++q) {
+        const Key m = __reduce_max_sync(0xFFFFFFFFu, g == q ? key : Key(0));
+        mk = (g == q) ? m : mk;
+      }
+    } else {
+      mk = key;
+#pragma unroll
+      for (int off = G / 2; off >= 1; off >>= 1) {
+        const Key o = shfl_xor_key(mk, off, G);
+        mk = o > mk ? o : mk;
+      }
     }
     const bool hold = cand && key == mk;
     const unsigned bal = (__ballot_sync(0xFFFFFFFFu, hold) >> (g * G)) & GMASK;
