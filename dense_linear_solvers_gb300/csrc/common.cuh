@@ -55,6 +55,19 @@ __device__ __forceinline__ bool pivot_ok(typename Traits<T>::Key k) {
   return k != Tr::kKeyMax && k >= Tr::kFloorBits + 1;
 }
 
+// The pivot value of a regular pivot from its key (magnitude bits + 1) and sign bit.
+template <typename T>
+__device__ __forceinline__ T pivot_from_key(typename Traits<T>::Key k, unsigned sign);
+template <>
+__device__ __forceinline__ float pivot_from_key<float>(uint32_t k, unsigned sign) {
+  return __uint_as_float((k - 1u) | (sign << 31));
+}
+template <>
+__device__ __forceinline__ double pivot_from_key<double>(unsigned long long k, unsigned sign) {
+  return __longlong_as_double(static_cast<long long>((k - 1ull) |
+                                                     (static_cast<unsigned long long>(sign) << 63)));
+}
+
 template <typename T>
 __device__ __forceinline__ T fma_rn(T a, T b, T c);
 template <>

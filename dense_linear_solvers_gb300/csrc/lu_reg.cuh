@@ -35,7 +35,7 @@
 namespace bsolve {
 namespace lu_reg_detail {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 
 template <typename T, int N>
@@ -157,6 +157,7 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
         mk = o > mk ? o : mk;
       }
     }
+    const unsigned sbal = __ballot_sync(0xFFFFFFFFu, signbit(a[k]));
     const bool hold = cand && key == mk;
     const unsigned bal = (__ballot_sync(0xFFFFFFFFu, hold) >> (g * G)) & GMASK;
     int plane;
@@ -183,20 +184,25 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     if (pos == k) pos = pos_p;
     if (is_p) pos = k;
 
+    // The pivot is known without waiting for the published row: its magnitude is the
+    // max key less one, its sign the pivot lane's bit of the sign ballot. The reciprocal
+    // and the multipliers thus overlap the shared-memory round trip of the pivot row.
+    const T piv = pivot_from_key<T>(mk, (sbal >> (g * G + plane)) & 1u);
+    const T r = ok ? T(1) / piv : T(1);
+    if (is_p) my_r = r;
+    const bool upd = row_ok && pos > k;
+    const T l = a[k] * r;
+    if (upd) a[k] = l;
+
     T* pr = prow[warp][g][k & 1];
     if (is_p) {
 #pragma unroll
-      for (int j = k; j < NT; ++j) pr[j] = a[j];
+      for (int j = k + 1; j < NT; ++j) pr[j] = a[j];
 #pragma unroll
       for (int c = 0; c < RT; ++c) pr[NT + c] = b[c];
     }
     __syncwarp();
-    const T piv = pr[k];
-    const T r = ok ? T(1) / piv : T(1);
-    if (is_p) my_r = r;
-    if (row_ok && pos > k) {
-      const T l = a[k] * r;
-      a[k] = l;
+    if (upd) {
 #pragma unroll
       for (int j = k + 1; j < NT; ++j) a[j] = fma_rn<T>(-l, pr[j], a[j]);
 #pragma unroll
