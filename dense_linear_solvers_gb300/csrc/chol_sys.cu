@@ -58,7 +58,7 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   const int D = sys_stride(n, nrhs);
   const int TRI = tri(n);
   T* const M = reinterpret_cast<T*>(smem_raw);     // kSys systems, stride D
-  T* const rr = M + kSys * D;                       // [kSys][kMaxN] reciprocals
+  T* const rr = M + kSys * D;                       // [kMaxN][kSys] reciprocals
   int* const sinfo = reinterpret_cast<int*>(rr + kSys * kMaxN);
 
   const int tid = threadIdx.x;
@@ -96,19 +96,19 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   __syncthreads();
 
   for (int k = 0; k < n; ++k) {
-    // A: pivot square root and reciprocal, one lane per system
+    // A: the pivot square root and reciprocal of column k, one lane per system
     if (tid < kSys) {
       const T d = Ms[tri(k) + k];
       if (!(d > T(0)) && sinfo[s] == 0) sinfo[s] = k + 1;
       const T l = sqrt_rn<T>(d);
       Ms[tri(k) + k] = l;
-      rr[s * kMaxN + k] = rcp_rn<T>(l);
+      rr[k * kSys + s] = rcp_rn<T>(l);
     }
     __syncthreads();
     // B: scale column k below the diagonal, and y_k
     {
       const int m = n - 1 - k;
-      const T r = rr[s * kMaxN + k];
+      const T r = rr[k * kSys + s];
       for (int e = slot; e < m + nrhs; e += kSlots) {
         if (e < m) {
           const int i = k + 1 + e;
@@ -148,15 +148,18 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     __syncthreads();
   }
 
-  // L^T x = y, from the last row
-  for (int k = n - 1; k >= 0; --k) {
-    const T r = rr[s * kMaxN + k];
-    for (int c = slot; c < nrhs; c += kSlots) Ys[k * nrhs + c] = Ys[k * nrhs + c] * r;
-    __syncthreads();
+  // L^T x = y, from the last row. x_k = y_k * r_k is taken by whichever thread gives
+  // y_k its last update (in step k+1), so each step needs a single barrier.
+  for (int c = slot; c < nrhs; c += kSlots) Ys[(n - 1) * nrhs + c] *= rr[(n - 1) * kSys + s];
+  __syncthreads();
+  for (int k = n - 1; k >= 1; --k) {
     const int tk = tri(k);
+    const T rkm1 = rr[(k - 1) * kSys + s];
     for (int e = slot; e < k * nrhs; e += kSlots) {
       const int i = e / nrhs, c = e - i * nrhs;
-      Ys[i * nrhs + c] = fma_rn<T>(-Ms[tk + i], Ys[k * nrhs + c], Ys[i * nrhs + c]);
+      T y = fma_rn<T>(-Ms[tk + i], Ys[k * nrhs + c], Ys[i * nrhs + c]);
+      if (i == k - 1) y = y * rkm1;
+      Ys[i * nrhs + c] = y;
     }
     __syncthreads();
   }
