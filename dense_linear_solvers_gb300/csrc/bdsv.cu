@@ -92,8 +92,8 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
         failed = true;
         inf = k * BS + c + 1;
       }
-      const T l = sqrt(d);
-      const T r = T(1) / l;
+      const T l = sqrt_rn<T>(d);
+      const T r = rcp_rn<T>(l);
       Sm[Tr::at(c, c)] = l;
       Fr[c] = r;
 #pragma unroll
@@ -154,7 +154,7 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
       T acc = w[j];
 #pragma unroll
       for (int m = j + 1; m < BS; ++m) acc = fma_rn<T>(-F[Tr::at(m, j)], xk[m], acc);
-      xk[j] = acc * (T(1) / F[Tr::at(j, j)]);
+      xk[j] = acc * rcp_rn<T>(F[Tr::at(j, j)]);
     }
 #pragma unroll
     for (int j = 0; j < BS; ++j) {

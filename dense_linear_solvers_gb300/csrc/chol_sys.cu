@@ -37,20 +37,6 @@ __host__ __device__ inline int tri(int i) { return i * (i + 1) / 2; }
 __host__ __device__ inline int sys_stride(int n, int nrhs) { return (tri(n) + n * nrhs) | 1; }
 
 template <typename T>
-__device__ __forceinline__ T rcp_rn(T x);
-template <>
-__device__ __forceinline__ float rcp_rn<float>(float x) { return __frcp_rn(x); }
-template <>
-__device__ __forceinline__ double rcp_rn<double>(double x) { return __drcp_rn(x); }
-
-template <typename T>
-__device__ __forceinline__ T sqrt_rn(T x);
-template <>
-__device__ __forceinline__ float sqrt_rn<float>(float x) { return __fsqrt_rn(x); }
-template <>
-__device__ __forceinline__ double sqrt_rn<double>(double x) { return __dsqrt_rn(x); }
-
-template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
                 T* __restrict__ B, int32_t* __restrict__ info) {

@@ -102,6 +102,22 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
+// Correctly rounded reciprocal and square root (IEEE round to nearest, the same results
+// as 1/x and sqrt(x) on the host, with shorter instruction sequences than a division).
+template <typename T>
+__device__ __forceinline__ T rcp_rn(T x);
+template <>
+__device__ __forceinline__ float rcp_rn<float>(float x) { return __frcp_rn(x); }
+template <>
+__device__ __forceinline__ double rcp_rn<double>(double x) { return __drcp_rn(x); }
+
+template <typename T>
+__device__ __forceinline__ T sqrt_rn(T x);
+template <>
+__device__ __forceinline__ float sqrt_rn<float>(float x) { return __fsqrt_rn(x); }
+template <>
+__device__ __forceinline__ double sqrt_rn<double>(double x) { return __dsqrt_rn(x); }
+
 // Shuffle of a 64-bit integer key as two 32-bit halves.
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m,
                                                            int width) {

@@ -32,13 +32,6 @@ constexpr int kBlk = 4;  // rows per back-substitution block
 __host__ __device__ inline int odd_pitch(int w) { return w | 1; }
 
 template <typename T>
-__device__ __forceinline__ T rcp_rn(T x);
-template <>
-__device__ __forceinline__ float rcp_rn<float>(float x) { return __frcp_rn(x); }
-template <>
-__device__ __forceinline__ double rcp_rn<double>(double x) { return __drcp_rn(x); }
-
-template <typename T>
 __global__ void __launch_bounds__(kThreads)
 lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
               T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info) {

@@ -7,15 +7,17 @@
 // interchanges, MAGMA's rowid); each lane tracks the current position of its row.
 //
 // Step k (fully unrolled, every operand index static):
-//   1. pivot search: integer magnitude keys (see common.cuh), the group max by one
+//   1. pivot search: live keys (the magnitude bits with the top bit set while the row is
+//      still below the step, one OR per row; see LiveKey), the group max by one
 //      full-warp redux.sync per group (FP32) or xor shuffles (FP64), then the lowest
 //      current position among the lanes holding the max (lowest-row tie rule; a rare
-//      exact tie takes a second reduction);
+//      exact tie takes a second reduction, a rare NaN candidate a rewrite of the keys);
 //   2. positions k and p exchange (a bookkeeping swap, no data moves); the pivot lane
 //      records the LAPACK swap entry ipiv[k] = position(p) + 1;
-//   3. the pivot lane publishes its row (columns >= k and the right-hand sides) in a
-//      shared-memory buffer, double-buffered by step parity so that one __syncwarp per
-//      step orders writes and reads;
+//   3. the pivot lane publishes its row (columns > k, from the 16-byte chunk holding
+//      k+1, and the right-hand sides) with 16-byte stores in a shared-memory buffer,
+//      double-buffered by step parity so that one __syncwarp per step orders writes and
+//      reads;
 //   4. every row still below the pivot scales its column-k entry by the pivot
 //      reciprocal and applies the rank-1 update to its row of A and B (the forward solve
 //      L y = P b folded into the factorization).
@@ -76,6 +78,62 @@ __device__ __forceinline__ void store_vec(T* __restrict__ p, const T (&r)[N]) {
   }
 }
 
+// Live pivot keys: the magnitude bits with the top bit set for a row still below the
+// step and not yet a pivot row (0 otherwise). One OR per row orders |x| exactly, puts
+// every live row above every dead or phantom one, and leaves the dead ones out of the tie
+// rule. A live NaN has a key above inf's.
+template <typename T> struct LiveKey;
+template <> struct LiveKey<float> {
+  using Key = uint32_t;
+  static constexpr Key kAlive = 0x80000000u;
+  static constexpr Key kNanAbove = 0xFF800000u;   // live key of inf
+  static constexpr Key kRegular = 0x80800000u;    // live key of the smallest normal
+  static constexpr Key kMax = 0xFFFFFFFFu;        // a NaN at the step's own position
+  __device__ __forceinline__ static float value(Key k, unsigned sign) {
+    return __uint_as_float((k & 0x7FFFFFFFu) | (sign << 31));
+  }
+};
+template <> struct LiveKey<double> {
+  using Key = unsigned long long;
+  static constexpr Key kAlive = 0x8000000000000000ull;
+  static constexpr Key kNanAbove = 0xFFF0000000000000ull;
+  static constexpr Key kRegular = 0x8010000000000000ull;
+  static constexpr Key kMax = 0xFFFFFFFFFFFFFFFFull;
+  __device__ __forceinline__ static double value(Key k, unsigned sign) {
+    return __longlong_as_double(static_cast<long long>(
+        (k & 0x7FFFFFFFFFFFFFFFull) | (static_cast<unsigned long long>(sign) << 63)));
+  }
+};
+
+// One 16-byte chunk of a register row to or from shared memory (j a multiple of 16/size).
+template <typename T, int N>
+__device__ __forceinline__ void st_chunk(T* p, const T (&r)[N], int j) {
+  if constexpr (sizeof(T) == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+  else
+    *reinterpret_cast<double2*>(p) = make_double2(r[j], r[j + 1]);
+}
+template <typename T, int N>
+__device__ __forceinline__ void ld_chunk(const T* p, T (&r)[N], int j) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    r[j] = v.x; r[j + 1] = v.y; r[j + 2] = v.z; r[j + 3] = v.w;
+  } else {
+    const double2 v = *reinterpret_cast<const double2*>(p);
+    r[j] = v.x; r[j + 1] = v.y;
+  }
+}
+template <typename T, int N>
+__device__ __forceinline__ void load_vec_shared(const T* p, T (&r)[N]) {
+  if constexpr ((N * sizeof(T)) % 16 == 0) {
+#pragma unroll
+    for (int j = 0; j < N; j += 16 / sizeof(T)) ld_chunk<T, N>(p + j, r, j);
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) r[j] = p[j];
+  }
+}
+
 // FULL: n == NT and nrhs == RT (every guard compiles away).
 template <typename T, int NT, int RT, int LAYOUT, bool FULL>
 __global__ void __launch_bounds__(kThreads)
@@ -129,20 +187,20 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     for (int c = 0; c < RT; ++c) b[c] = T(0);
   }
 
+  using LK = LiveKey<T>;
+  Key alive = row_ok ? LK::kAlive : Key(0);   // live: below the step, not yet a pivot row
   int pos = t;          // current position of this lane's row
   int my_ipiv = 0;      // LAPACK entry of the step that chose this row
   T my_r = T(1);        // reciprocal of this row's pivot
   int inf = 0;
+  constexpr int V = 16 / sizeof(T);
 
-#pragma unroll
-  for (int k = 0; k < NT; ++k) {
-    if (!FULL && k >= n) break;
-    const bool cand = row_ok && pos >= k;
-    const Key key = cand ? pivot_key<T>(a[k], pos == k) : Key(0);
+  // the group maximum of a key: one full-warp redux.sync per group for FP32 (non-members
+  // contribute 0, below every key; shorter latency than a shuffle butterfly and cheaper
+  // than a partial-mask redux), xor shuffles for FP64
+  auto group_max = [&](Key key) {
     Key mk;
     if constexpr (sizeof(Key) == 4 && GPW <= 4) {
-      // one full-warp redux.sync per group (non-members contribute 0, below every key):
-      // shorter latency than a shuffle butterfly, and cheaper than a partial-mask redux
       mk = 0;
 #pragma unroll
       for (int q = 0; q < GPW; ++q) {
@@ -157,8 +215,22 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
         mk = o > mk ? o : mk;
       }
     }
+    return mk;
+  };
+
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    if (!FULL && k >= n) break;
+    Key key = Traits<T>::mag_bits(a[k]) | alive;
+    Key mk = group_max(key);
+    if (__any_sync(0xFFFFFFFFu, mk > LK::kNanAbove)) {
+      // a NaN among some group's candidates (rare): the contract's keys, a NaN at the
+      // step's own position wins, a NaN elsewhere ties with zero
+      if (key > LK::kNanAbove) key = (pos == k) ? LK::kMax : LK::kAlive;
+      mk = group_max(key);
+    }
     const unsigned sbal = __ballot_sync(0xFFFFFFFFu, signbit(a[k]));
-    const bool hold = cand && key == mk;
+    const bool hold = key == mk;
     const unsigned bal = (__ballot_sync(0xFFFFFFFFu, hold) >> (g * G)) & GMASK;
     int plane;
     if (__any_sync(0xFFFFFFFFu, __popc(bal) > 1)) {
@@ -177,36 +249,47 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     }
     if (plane < 0) plane = 0;  // only in groups past the end of the batch
     const int pos_p = __shfl_sync(0xFFFFFFFFu, pos, plane, G);
-    const bool ok = pivot_ok<T>(mk);
+    const bool ok = mk >= LK::kRegular && mk != LK::kMax;
     if (!ok && inf == 0) inf = k + 1;
     const bool is_p = (t == plane);
-    if (is_p) my_ipiv = pos_p + 1;
     if (pos == k) pos = pos_p;
-    if (is_p) pos = k;
+    if (is_p) {
+      my_ipiv = pos_p + 1;
+      pos = k;
+      alive = 0;
+    }
 
-    // The pivot is known without waiting for the published row: its magnitude is the
-    // max key less one, its sign the pivot lane's bit of the sign ballot. The reciprocal
-    // and the multipliers thus overlap the shared-memory round trip of the pivot row.
-    const T piv = pivot_from_key<T>(mk, (sbal >> (g * G + plane)) & 1u);
+    // The pivot is known without waiting for the published row: its magnitude is in the
+    // max key, its sign the pivot lane's bit of the sign ballot. The reciprocal and the
+    // multipliers thus overlap the shared-memory round trip of the pivot row.
+    const T piv = LK::value(mk, (sbal >> (g * G + plane)) & 1u);
     const T r = ok ? T(1) / piv : T(1);
     if (is_p) my_r = r;
-    const bool upd = row_ok && pos > k;
+    const bool upd = alive != 0;
     const T l = a[k] * r;
     if (upd) a[k] = l;
 
+    // the pivot row's columns > k (from the 16-byte chunk holding k+1) and its B part
     T* pr = prow[warp][g][k & 1];
+    const int c1 = (k + 1) & ~(V - 1);
     if (is_p) {
 #pragma unroll
-      for (int j = k + 1; j < NT; ++j) pr[j] = a[j];
-#pragma unroll
-      for (int c = 0; c < RT; ++c) pr[NT + c] = b[c];
+      for (int j = 0; j < NT; j += V)
+        if (j >= c1) st_chunk<T>(pr + j, a, j);
+      store_vec<T, RT>(pr + NT, b);
     }
     __syncwarp();
     if (upd) {
+      T u[NT];
 #pragma unroll
-      for (int j = k + 1; j < NT; ++j) a[j] = fma_rn<T>(-l, pr[j], a[j]);
+      for (int j = 0; j < NT; j += V)
+        if (j >= c1) ld_chunk<T>(pr + j, u, j);
+      T ub[RT];
+      load_vec_shared<T, RT>(pr + NT, ub);
 #pragma unroll
-      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-l, pr[NT + c], b[c]);
+      for (int j = k + 1; j < NT; ++j) a[j] = fma_rn<T>(-l, u[j], a[j]);
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-l, ub[c], b[c]);
     }
   }
 

@@ -86,8 +86,8 @@ chol_smem_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       inf = k + 1;
       break;
     }
-    const T l = sqrt(d);
-    const T r = T(1) / l;
+    const T l = sqrt_rn<T>(d);
+    const T r = rcp_rn<T>(l);
     __syncwarp();
     if (lane == 0) {
       M[k * P + k] = l;
