@@ -62,6 +62,20 @@ class Oracle:
         for name in ("oracle_bdsv_f32", "oracle_bdsv_f64"):
             getattr(lib, name).argtypes = [i32, i32, i64, vp, vp, vp, i32]
             getattr(lib, name).restype = i32
+        sig = {
+            "getrf": [i32, i32, i64, vp, vp, vp, vp, i32],
+            "getrs": [i32, i32, i32, i64, vp, vp, vp, i32],
+            "potrf": [i32, i32, i64, vp, vp, i32],
+            "potrs": [i32, i32, i32, i64, vp, vp, i32],
+            "bdsv_factor": [i32, i32, i64, vp, vp, i32],
+            "bdsv_solve": [i32, i32, i64, vp, vp, i32],
+            "bdmv": [i32, i32, i64, vp, vp, vp, i32],
+        }
+        for op, args in sig.items():
+            for sfx in ("f32", "f64"):
+                fn = getattr(lib, f"oracle_{op}_{sfx}")
+                fn.argtypes = args
+                fn.restype = i32
         self.lib = lib
 
     def getrf_getrs(self, A, B, layout: int = ROW_MAJOR, nthreads: int = 1):
@@ -113,6 +127,85 @@ class Oracle:
             raise ValueError("oracle bdsv rejected its arguments")
         return S, X, info
 
+    # --- factor once, solve per right-hand side -------------------------------------
+    def getrf(self, A, layout: int = ROW_MAJOR, nthreads: int = 1):
+        """LU with partial pivoting only. Returns (LU, ipiv, info, tie_step)."""
+        A = np.ascontiguousarray(A).copy()
+        batch, n = A.shape[0], A.shape[1]
+        ipiv = np.zeros((batch, n), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_" + _suffix(A.dtype))
+        if fn(layout, n, batch, _ptr(A), _ptr(ipiv), _ptr(info), _ptr(tie), nthreads) != 0:
+            raise ValueError("oracle getrf rejected its arguments")
+        return A, ipiv, info, tie
+
+    def getrs(self, LU, ipiv, B, layout: int = ROW_MAJOR, nthreads: int = 1):
+        """Solve with a stored LU factor and swap sequence. Returns X."""
+        LU = np.ascontiguousarray(LU)
+        ipiv = np.ascontiguousarray(ipiv, dtype=np.int32)
+        B = np.ascontiguousarray(B, dtype=LU.dtype).copy()
+        batch, n = LU.shape[0], LU.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        fn = getattr(self.lib, "oracle_getrs_" + _suffix(LU.dtype))
+        if fn(layout, n, nrhs, batch, _ptr(LU), _ptr(ipiv), _ptr(B), nthreads) != 0:
+            raise ValueError("oracle getrs rejected its arguments")
+        return B
+
+    def potrf(self, A, layout: int = COL_MAJOR, nthreads: int = 1):
+        """Cholesky (lower fill) only. Returns (L, info)."""
+        A = np.ascontiguousarray(A).copy()
+        batch, n = A.shape[0], A.shape[1]
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_potrf_" + _suffix(A.dtype))
+        if fn(layout, n, batch, _ptr(A), _ptr(info), nthreads) != 0:
+            raise ValueError("oracle potrf rejected its arguments")
+        return A, info
+
+    def potrs(self, L, B, layout: int = COL_MAJOR, nthreads: int = 1):
+        """Solve with a stored lower Cholesky factor. Returns X."""
+        L = np.ascontiguousarray(L)
+        B = np.ascontiguousarray(B, dtype=L.dtype).copy()
+        batch, n = L.shape[0], L.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        fn = getattr(self.lib, "oracle_potrs_" + _suffix(L.dtype))
+        if fn(layout, n, nrhs, batch, _ptr(L), _ptr(B), nthreads) != 0:
+            raise ValueError("oracle potrs rejected its arguments")
+        return B
+
+    def bdsv_factor(self, strips, nthreads: int = 1):
+        """Block-Cholesky factor sweep in place. Returns (factored strips, info)."""
+        S = np.ascontiguousarray(strips).copy()
+        batch, nbr, bs = S.shape[0], S.shape[1], S.shape[2]
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_bdsv_factor_" + _suffix(S.dtype))
+        if fn(nbr, bs, batch, _ptr(S), _ptr(info), nthreads) != 0:
+            raise ValueError("oracle bdsv_factor rejected its arguments")
+        return S, info
+
+    def bdsv_solve(self, strips, xpad, nthreads: int = 1):
+        """Forward/backward block substitution with factored strips. Returns the padded x."""
+        S = np.ascontiguousarray(strips)
+        X = np.ascontiguousarray(xpad, dtype=S.dtype).copy()
+        batch, nbr, bs = S.shape[0], S.shape[1], S.shape[2]
+        fn = getattr(self.lib, "oracle_bdsv_solve_" + _suffix(S.dtype))
+        if fn(nbr, bs, batch, _ptr(S), _ptr(X), nthreads) != 0:
+            raise ValueError("oracle bdsv_solve rejected its arguments")
+        return X
+
+    def bdmv(self, strips, xpad, ypad=None, nthreads: int = 1):
+        """Block-tridiagonal matvec y = A x on padded vectors (y's pads kept from ypad, or
+        zero). Returns the padded y."""
+        S = np.ascontiguousarray(strips)
+        X = np.ascontiguousarray(xpad, dtype=S.dtype)
+        Y = (np.zeros_like(X) if ypad is None
+             else np.ascontiguousarray(ypad, dtype=S.dtype).copy())
+        batch, nbr, bs = S.shape[0], S.shape[1], S.shape[2]
+        fn = getattr(self.lib, "oracle_bdmv_" + _suffix(S.dtype))
+        if fn(nbr, bs, batch, _ptr(S), _ptr(X), _ptr(Y), nthreads) != 0:
+            raise ValueError("oracle bdmv rejected its arguments")
+        return Y
+
 
 def default() -> Oracle:
     global _default
@@ -132,6 +225,34 @@ def potrf_potrs(A, B, layout: int = COL_MAJOR, nthreads: int = 1):
 
 def bdsv(strips, xpad, nthreads: int = 1):
     return default().bdsv(strips, xpad, nthreads)
+
+
+def getrf(A, layout: int = ROW_MAJOR, nthreads: int = 1):
+    return default().getrf(A, layout, nthreads)
+
+
+def getrs(LU, ipiv, B, layout: int = ROW_MAJOR, nthreads: int = 1):
+    return default().getrs(LU, ipiv, B, layout, nthreads)
+
+
+def potrf(A, layout: int = COL_MAJOR, nthreads: int = 1):
+    return default().potrf(A, layout, nthreads)
+
+
+def potrs(L, B, layout: int = COL_MAJOR, nthreads: int = 1):
+    return default().potrs(L, B, layout, nthreads)
+
+
+def bdsv_factor(strips, nthreads: int = 1):
+    return default().bdsv_factor(strips, nthreads)
+
+
+def bdsv_solve(strips, xpad, nthreads: int = 1):
+    return default().bdsv_solve(strips, xpad, nthreads)
+
+
+def bdmv(strips, xpad, ypad=None, nthreads: int = 1):
+    return default().bdmv(strips, xpad, ypad, nthreads)
 
 
 def _suffix(dtype) -> str:

@@ -141,6 +141,46 @@ void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int
 }
 
 // ---------------------------------------------------------------------------------
+// getrs: solve with a stored factor ([TDLS] separate substitution; [GLASS] "factor once,
+// call this per right-hand side"). LU holds L\U as left by getrf_getrs_one (nrhs = 0 gives
+// getrf), ipiv the 1-based swap sequence. B <- X:
+//   1. the interchanges in step order: rows k and ipiv[k]-1 of B for k = 0..n-1;
+//   2. L y = P b with unit L, column by column: b_i -= l_ik b_k for i > k (each b_i takes
+//      its updates in increasing k, as in the fused sweep);
+//   3. U x = y as in getrf_getrs_one, a pivot reciprocal of 1 for a singular u_kk.
+// No info: a factor whose info != 0 gives an unspecified (finite or not) X.
+// ---------------------------------------------------------------------------------
+template <typename T>
+void getrs_one(int layout, int n, int nrhs, const T* LU, const int32_t* ipiv, T* B) {
+  const T floor_v = Limits<T>::floor_();
+  auto a = [&](int r, int c) -> T { return LU[at(layout, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
+  for (int k = 0; k < n; ++k) {
+    const int p = ipiv[k] - 1;
+    if (p != k)
+      for (int c = 0; c < nrhs; ++c) {
+        T t = b(k, c);
+        b(k, c) = b(p, c);
+        b(p, c) = t;
+      }
+  }
+  for (int k = 0; k < n; ++k)
+    for (int i = k + 1; i < n; ++i) {
+      const T l = a(i, k);
+      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));
+    }
+  for (int k = n - 1; k >= 0; --k) {
+    const T piv = a(k, k);
+    const T r = (std::fabs(piv) >= floor_v) ? T(1) / piv : T(1);
+    for (int c = 0; c < nrhs; ++c) {
+      const T x = b(k, c) * r;
+      b(k, c) = x;
+      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-a(i, k), x, b(i, c));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
 // Cholesky, lower fill, right-looking ([cuSolverDx] POTRF: only the lower triangle is
 // read and replaced by L, the upper part is untouched; info = the smallest leading
 // minor that is not positive definite). Column k:
@@ -192,6 +232,27 @@ void potrf_potrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* info) {
   *info = 0;
 }
 
+// potrs with a stored lower factor L (potrf_potrs_one with nrhs = 0 gives potrf): the
+// solve half of potrf_potrs_one, with the same operation order. No info: a failed factor
+// gives an unspecified X.
+template <typename T>
+void potrs_one(int layout, int n, int nrhs, const T* L, T* B) {
+  auto a = [&](int r, int c) -> T { return L[at(layout, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
+  for (int c = 0; c < nrhs; ++c) {
+    for (int k = 0; k < n; ++k) {
+      const T y = b(k, c) * (T(1) / a(k, k));
+      b(k, c) = y;
+      for (int i = k + 1; i < n; ++i) b(i, c) = std::fma(-a(i, k), y, b(i, c));
+    }
+    for (int k = n - 1; k >= 0; --k) {
+      const T x = b(k, c) * (T(1) / a(k, k));
+      b(k, c) = x;
+      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-a(k, i), x, b(i, c));
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // Block-tridiagonal SPD solve by the block-Cholesky (block-Thomas) sweep ([GLASS]
 // bdsv_factor / bdsv_solve / bdsv).
@@ -207,11 +268,18 @@ void potrf_potrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* info) {
 // raises a flag and runs the sweep on; this oracle stops at the first failure, the
 // strips beyond it are then unspecified and the solution is returned as zeros.
 // ---------------------------------------------------------------------------------
-template <typename T>
-void bdsv_one(int nbr, int bs, T* strips, T* xpad, int32_t* info) {
+// Offset of slot (y, x) of sub-block `slot` (0 = LEFT, 1 = MAIN, 2 = RIGHT) of block-row br.
+inline int64_t strip_at(int bs, int br, int slot, int y, int x) {
   const int w = 3 * bs;
+  return (int64_t)br * bs * w + (int64_t)y * w + slot * bs + x;
+}
+
+// bdsv_factor: the factor sweep, in place on the strips; returns info (0 or the global
+// index of the first failing diagonal, where the sweep stops).
+template <typename T>
+int32_t bdsv_factor_one(int nbr, int bs, T* strips) {
   auto blk = [&](int br, int slot, int y, int x) -> T& {
-    return strips[(int64_t)br * bs * w + (int64_t)y * w + slot * bs + x];
+    return strips[strip_at(bs, br, slot, y, x)];
   };
   const int LEFT = 0, MAIN = 1;
   int32_t inf = 0;
@@ -258,12 +326,16 @@ void bdsv_one(int nbr, int bs, T* strips, T* xpad, int32_t* info) {
     for (int i = 0; i < bs; ++i)
       for (int j = 0; j <= i; ++j) blk(k, MAIN, i, j) = S[i * bs + j];
   }
+  return inf;
+}
+
+// bdsv_solve: forward then backward block substitution on the interior of the padded
+// vector, with strips factored by bdsv_factor_one (read only).
+template <typename T>
+void bdsv_solve_one(int nbr, int bs, const T* strips, T* xpad) {
+  auto blk = [&](int br, int slot, int y, int x) -> T { return strips[strip_at(bs, br, slot, y, x)]; };
+  const int LEFT = 0, MAIN = 1;
   T* x = xpad + bs;  // interior: block-row br at x + br*bs
-  if (inf != 0) {
-    for (int i = 0; i < nbr * bs; ++i) x[i] = T(0);
-    *info = inf;
-    return;
-  }
   std::vector<T> z(bs);
   // Forward sweep: z = b_k - E_k y_{k-1}; y_k = F_k^{-1} z.
   for (int k = 0; k < nbr; ++k) {
@@ -289,7 +361,41 @@ void bdsv_one(int nbr, int bs, T* strips, T* xpad, int32_t* info) {
       x[k * bs + j] = s * (T(1) / blk(k, MAIN, j, j));
     }
   }
+}
+
+// bdsv = bdsv_factor then bdsv_solve; a failed factor returns the interior as zeros.
+template <typename T>
+void bdsv_one(int nbr, int bs, T* strips, T* xpad, int32_t* info) {
+  const int32_t inf = bdsv_factor_one(nbr, bs, strips);
+  if (inf != 0) {
+    for (int i = 0; i < nbr * bs; ++i) xpad[bs + i] = T(0);
+    *info = inf;
+    return;
+  }
+  bdsv_solve_one(nbr, bs, strips, xpad);
   *info = 0;
+}
+
+// ---------------------------------------------------------------------------------
+// bdmv ([GLASS] "Block-tridiagonal matrix-vector product"): y = A x with A given by the
+// strips [L | D | R] (all three blocks as stored) and padded vectors. Block-row br reads
+// the window x[br*bs, br*bs + 3bs) (previous / current / next block) and writes
+// y[(br+1)*bs + row]; the pad blocks of y are left as they are. The pages fix no
+// summation order (only that the result does not depend on the thread count): here each
+// entry is one dot product over its strip row in increasing column order, one fused
+// multiply-add per term, starting from zero.
+// ---------------------------------------------------------------------------------
+template <typename T>
+void bdmv_one(int nbr, int bs, const T* strips, const T* xpad, T* ypad) {
+  const int w = 3 * bs;
+  for (int br = 0; br < nbr; ++br)
+    for (int row = 0; row < bs; ++row) {
+      const T* srow = strips + strip_at(bs, br, 0, row, 0);
+      const T* xw = xpad + (int64_t)br * bs;
+      T acc = T(0);
+      for (int c = 0; c < w; ++c) acc = std::fma(srow[c], xw[c], acc);
+      ypad[(int64_t)(br + 1) * bs + row] = acc;
+    }
 }
 
 // Hands contiguous ranges of systems to nthreads workers (1 = the calling thread).
@@ -342,6 +448,76 @@ int bdsv_batched(int nbr, int bs, int64_t batch, T* strips, T* xpad, int32_t* in
   return 0;
 }
 
+template <typename T>
+int getrf_batched(int layout, int n, int64_t batch, T* A, int32_t* ipiv, int32_t* info,
+                  int32_t* tie_step, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || batch < 0) return 1;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    getrf_getrs_one<T>(layout, n, 0, A + s * n * n, nullptr, ipiv + s * n, info + s,
+                       tie_step ? tie_step + s : nullptr);
+  });
+  return 0;
+}
+
+template <typename T>
+int getrs_batched(int layout, int n, int nrhs, int64_t batch, const T* LU, const int32_t* ipiv,
+                  T* B, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0) return 1;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    getrs_one<T>(layout, n, nrhs, LU + s * n * n, ipiv + s * n, B + s * n * nrhs);
+  });
+  return 0;
+}
+
+template <typename T>
+int potrf_batched(int layout, int n, int64_t batch, T* A, int32_t* info, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || batch < 0) return 1;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    potrf_potrs_one<T>(layout, n, 0, A + s * n * n, nullptr, info + s);
+  });
+  return 0;
+}
+
+template <typename T>
+int potrs_batched(int layout, int n, int nrhs, int64_t batch, const T* L, T* B, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0) return 1;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    potrs_one<T>(layout, n, nrhs, L + s * n * n, B + s * n * nrhs);
+  });
+  return 0;
+}
+
+template <typename T>
+int bdsv_factor_batched(int nbr, int bs, int64_t batch, T* strips, int32_t* info, int nthreads) {
+  if (nbr < 1 || bs < 1 || batch < 0) return 1;
+  const int64_t sstride = (int64_t)nbr * bs * 3 * bs;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    info[s] = bdsv_factor_one<T>(nbr, bs, strips + s * sstride);
+  });
+  return 0;
+}
+
+template <typename T>
+int bdsv_solve_batched(int nbr, int bs, int64_t batch, const T* strips, T* xpad, int nthreads) {
+  if (nbr < 1 || bs < 1 || batch < 0) return 1;
+  const int64_t sstride = (int64_t)nbr * bs * 3 * bs, vstride = (int64_t)(nbr + 2) * bs;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    bdsv_solve_one<T>(nbr, bs, strips + s * sstride, xpad + s * vstride);
+  });
+  return 0;
+}
+
+template <typename T>
+int bdmv_batched(int nbr, int bs, int64_t batch, const T* strips, const T* xpad, T* ypad,
+                 int nthreads) {
+  if (nbr < 1 || bs < 1 || batch < 0) return 1;
+  const int64_t sstride = (int64_t)nbr * bs * 3 * bs, vstride = (int64_t)(nbr + 2) * bs;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    bdmv_one<T>(nbr, bs, strips + s * sstride, xpad + s * vstride, ypad + s * vstride);
+  });
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -369,6 +545,61 @@ int oracle_bdsv_f32(int nbr, int bs, int64_t batch, float* strips, float* xpad, 
 int oracle_bdsv_f64(int nbr, int bs, int64_t batch, double* strips, double* xpad, int32_t* info,
                     int nthreads) {
   return bdsv_batched<double>(nbr, bs, batch, strips, xpad, info, nthreads);
+}
+
+int oracle_getrf_f32(int layout, int n, int64_t batch, float* A, int32_t* ipiv, int32_t* info,
+                     int32_t* tie_step, int nthreads) {
+  return getrf_batched<float>(layout, n, batch, A, ipiv, info, tie_step, nthreads);
+}
+int oracle_getrs_f32(int layout, int n, int nrhs, int64_t batch, const float* LU,
+                     const int32_t* ipiv, float* B, int nthreads) {
+  return getrs_batched<float>(layout, n, nrhs, batch, LU, ipiv, B, nthreads);
+}
+int oracle_potrf_f32(int layout, int n, int64_t batch, float* A, int32_t* info, int nthreads) {
+  return potrf_batched<float>(layout, n, batch, A, info, nthreads);
+}
+int oracle_potrs_f32(int layout, int n, int nrhs, int64_t batch, const float* L, float* B,
+                     int nthreads) {
+  return potrs_batched<float>(layout, n, nrhs, batch, L, B, nthreads);
+}
+int oracle_bdsv_factor_f32(int nbr, int bs, int64_t batch, float* strips, int32_t* info,
+                           int nthreads) {
+  return bdsv_factor_batched<float>(nbr, bs, batch, strips, info, nthreads);
+}
+int oracle_bdsv_solve_f32(int nbr, int bs, int64_t batch, const float* strips, float* xpad,
+                          int nthreads) {
+  return bdsv_solve_batched<float>(nbr, bs, batch, strips, xpad, nthreads);
+}
+int oracle_bdmv_f32(int nbr, int bs, int64_t batch, const float* strips, const float* xpad,
+                    float* ypad, int nthreads) {
+  return bdmv_batched<float>(nbr, bs, batch, strips, xpad, ypad, nthreads);
+}
+int oracle_getrf_f64(int layout, int n, int64_t batch, double* A, int32_t* ipiv, int32_t* info,
+                     int32_t* tie_step, int nthreads) {
+  return getrf_batched<double>(layout, n, batch, A, ipiv, info, tie_step, nthreads);
+}
+int oracle_getrs_f64(int layout, int n, int nrhs, int64_t batch, const double* LU,
+                     const int32_t* ipiv, double* B, int nthreads) {
+  return getrs_batched<double>(layout, n, nrhs, batch, LU, ipiv, B, nthreads);
+}
+int oracle_potrf_f64(int layout, int n, int64_t batch, double* A, int32_t* info, int nthreads) {
+  return potrf_batched<double>(layout, n, batch, A, info, nthreads);
+}
+int oracle_potrs_f64(int layout, int n, int nrhs, int64_t batch, const double* L, double* B,
+                     int nthreads) {
+  return potrs_batched<double>(layout, n, nrhs, batch, L, B, nthreads);
+}
+int oracle_bdsv_factor_f64(int nbr, int bs, int64_t batch, double* strips, int32_t* info,
+                           int nthreads) {
+  return bdsv_factor_batched<double>(nbr, bs, batch, strips, info, nthreads);
+}
+int oracle_bdsv_solve_f64(int nbr, int bs, int64_t batch, const double* strips, double* xpad,
+                          int nthreads) {
+  return bdsv_solve_batched<double>(nbr, bs, batch, strips, xpad, nthreads);
+}
+int oracle_bdmv_f64(int nbr, int bs, int64_t batch, const double* strips, const double* xpad,
+                    double* ypad, int nthreads) {
+  return bdmv_batched<double>(nbr, bs, batch, strips, xpad, ypad, nthreads);
 }
 
 }  // extern "C"

@@ -13,7 +13,11 @@ What each pin rests on:
   * LAPACK (through SciPy) as a library special case: same pivot sequence as dgetrf on
     inputs without near ties, same first failing minor as dpotrf;
   * the info contract on constructed singular / indefinite inputs;
-  * the block-tridiagonal solve against dense Cholesky of the assembled matrix.
+  * the block-tridiagonal solve against dense Cholesky of the assembled matrix;
+  * the factor/solve split against the fused routines (same operations, same order),
+    a swap-only solve, Cramer's rule and a diagonal factor worked by hand;
+  * the block-tridiagonal matvec against integer arithmetic (exact) and the assembled
+    dense product.
 """
 from __future__ import annotations
 
@@ -432,6 +436,188 @@ def pin_bdsv_info(orc):
             assert np.all(X == 0)
 
 
+# ----------------------------------------------------- factor once, solve per right-hand side
+def pin_getrs_composition(orc):
+    """getrf then getrs reproduces the fused getrf+getrs bit for bit (the interchanges
+    applied in step order, then each b_i's updates in increasing k, are the fused
+    sweep's operations in the fused sweep's order); getrf alone leaves the same
+    factor, pivots and info, singular systems included."""
+    rng = _rng(41)
+    for dt in (np.float32, np.float64):
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            for n, nrhs in ((1, 1), (3, 2), (8, 1), (16, 4), (33, 3)):
+                A = rng.standard_normal((6, n, n)).astype(dt)
+                A[1, :, n // 2] = 0        # singular: info > 0
+                B = rng.standard_normal((6, n, nrhs)).astype(dt)
+                As, Bs = to_storage(A, layout), to_storage(B, layout)
+                LU, X, ipiv, info, tie = orc.getrf_getrs(As, Bs, layout)
+                LU2, ipiv2, info2, tie2 = orc.getrf(As, layout)
+                assert np.array_equal(LU, LU2) and np.array_equal(ipiv, ipiv2)
+                assert np.array_equal(info, info2) and np.array_equal(tie, tie2)
+                X2 = orc.getrs(LU2, ipiv2, Bs, layout)
+                ok = info == 0
+                assert np.array_equal(X[ok], X2[ok])
+
+
+def pin_getrs_permutation_only(orc):
+    """With L = U = I the solve is the swap sequence alone: row k of B exchanged with row
+    ipiv[k]-1 for k = 0..n-1, in that order (exact)."""
+    rng = _rng(42)
+    n, nrhs = 6, 3
+    LU = np.broadcast_to(np.eye(n), (5, n, n)).copy()
+    ipiv = np.stack([rng.integers(k, n, size=5) for k in range(n)], axis=1).astype(np.int32) + 1
+    B = rng.standard_normal((5, n, nrhs))
+    X = orc.getrs(LU, ipiv, B, ROW_MAJOR)
+    for s in range(5):
+        want = B[s].copy()
+        for k in range(n):
+            p = ipiv[s, k] - 1
+            want[[k, p]] = want[[p, k]]
+        assert np.array_equal(X[s], want)
+
+
+def pin_getrs_cramer(orc):
+    """getrf + getrs on n <= 4 agrees with Cramer's rule in exact rational arithmetic
+    (determinants by permutation expansion) to a few ulps, for every right-hand side."""
+    rng = _rng(43)
+    for n in (2, 3, 4):
+        A = rng.uniform(-1, 1, (4, n, n))
+        B = rng.uniform(-1, 1, (4, n, 2))
+        LU, ipiv, info, _ = orc.getrf(A, ROW_MAJOR)
+        X = orc.getrs(LU, ipiv, B, ROW_MAJOR)
+        for s in range(4):
+            for c in range(2):
+                xs, d = _cramer_exact(A[s], B[s, :, c])
+                assert xs is not None
+                want = np.array([float(v) for v in xs])
+                assert np.allclose(X[s, :, c], want, rtol=1e-12, atol=1e-13), (X[s, :, c], want)
+
+
+def pin_potrs_composition(orc):
+    """potrf then potrs reproduces the fused potrf+potrs bit for bit; potrf alone leaves
+    the same factor and info."""
+    rng = _rng(44)
+    for dt in (np.float32, np.float64):
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            for n, nrhs in ((1, 1), (4, 2), (32, 1), (40, 3)):
+                G = rng.standard_normal((5, n, n))
+                A = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dt)
+                A[2, n - 1, n - 1] = -1.0
+                B = rng.standard_normal((5, n, nrhs)).astype(dt)
+                As, Bs = to_storage(A, layout), to_storage(B, layout)
+                L, X, info = orc.potrf_potrs(As, Bs, layout)
+                L2, info2 = orc.potrf(As, layout)
+                assert np.array_equal(L, L2) and np.array_equal(info, info2)
+                X2 = orc.potrs(L2, Bs, layout)
+                ok = info == 0
+                assert np.array_equal(X[ok], X2[ok])
+
+
+def pin_potrs_diagonal(orc):
+    """L = diag(d): x_i = (b_i * (1/d_i)) * (1/d_i), each product rounded once."""
+    d = np.array([[2.0, 0.5, 3.0, 7.0]])
+    L = np.zeros((1, 4, 4))
+    L[0][np.diag_indices(4)] = d[0]
+    b = np.array([[[1.0], [3.0], [5.0], [11.0]]])
+    X = orc.potrs(L, b, ROW_MAJOR)
+    r = 1.0 / d[0]
+    assert np.array_equal(X[0, :, 0], (b[0, :, 0] * r) * r)
+
+
+def pin_potrs_dense(orc):
+    """potrs with a factor from LAPACK dpotrf solves L L^T x = b to the backward-error
+    bound (upper triangle of the factor storage ignored)."""
+    rng = _rng(45)
+    n = 12
+    G = rng.standard_normal((3, n, n))
+    A = G @ np.swapaxes(G, 1, 2) + n * np.eye(n)
+    B = rng.standard_normal((3, n, 2))
+    L = np.stack([np.linalg.cholesky(A[s]) for s in range(3)])
+    L = L + np.triu(np.full((n, n), 9.0), 1)   # garbage above the diagonal
+    X = orc.potrs(to_storage(L, COL_MAJOR), to_storage(B, COL_MAJOR), COL_MAJOR)
+    X = from_storage(X, COL_MAJOR)
+    be = backward_error(A, X, B)
+    assert np.all(be <= 8 * n * eps_of(np.float64)), be
+
+
+def pin_bdsv_split(orc):
+    """bdsv_factor then bdsv_solve reproduces the fused bdsv bit for bit; one factor
+    serves several right-hand sides (factor once, solve per right-hand side)."""
+    rng = _rng(46)
+    for dt in (np.float64, np.float32):
+        for nbr, bs in ((1, 3), (4, 5), (32, 8)):
+            strips, xpad = _random_bdsv(rng, 3, nbr, bs, dt)
+            _, xpad2 = _random_bdsv(rng, 3, nbr, bs, dt)
+            S, X, info = orc.bdsv(strips, xpad)
+            S2, info2 = orc.bdsv_factor(strips)
+            assert np.array_equal(S, S2) and np.array_equal(info, info2)
+            assert np.array_equal(orc.bdsv_solve(S2, xpad), X)
+            _, Xb, _ = orc.bdsv(strips, xpad2)
+            assert np.array_equal(orc.bdsv_solve(S2, xpad2), Xb)
+
+
+# --------------------------------------------------------------------------- bdmv pins
+def pin_bdmv_exact_integers(orc):
+    """Small integers make every product and partial sum exact, so y must equal the
+    window definition evaluated in integers: y[(br+1)bs + r] = sum over the strip row of
+    strip[br][r][c] * x[br*bs + c]; the pad blocks of y keep their input values."""
+    rng = _rng(47)
+    for nbr, bs in ((1, 2), (3, 4), (5, 8)):
+        strips = rng.integers(-9, 10, (2, nbr, bs, 3 * bs)).astype(np.float64)
+        xpad = rng.integers(-9, 10, (2, (nbr + 2) * bs)).astype(np.float64)
+        xpad[:, :bs] = 0
+        xpad[:, (nbr + 1) * bs:] = 0
+        ypad = np.full_like(xpad, 7.0)
+        Y = orc.bdmv(strips, xpad, ypad)
+        for s in range(2):
+            Si = strips[s].astype(np.int64)
+            xi = xpad[s].astype(np.int64)
+            for br in range(nbr):
+                for r in range(bs):
+                    want = int(sum(int(Si[br, r, c]) * int(xi[br * bs + c]) for c in range(3 * bs)))
+                    assert Y[s, (br + 1) * bs + r] == want
+            assert np.all(Y[s, :bs] == 7.0) and np.all(Y[s, (nbr + 1) * bs:] == 7.0)
+
+
+def pin_bdmv_dense(orc):
+    """y agrees with the assembled dense matrix times x (NumPy, float64) within the dot
+    product rounding bound gamma_{3bs} |A| |x|; the edge blocks L_0 / R_{nbr-1} multiply
+    the zero pads."""
+    rng = _rng(48)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for nbr, bs in ((1, 4), (6, 3), (32, 8)):
+            strips, xpad = _random_bdsv(rng, 3, nbr, bs, dt)
+            strips[:, 0, :, :bs] = rng.standard_normal((3, bs, bs))     # multiplies the pad
+            strips[:, -1, :, 2 * bs:] = rng.standard_normal((3, bs, bs))
+            Y = orc.bdmv(strips, xpad)
+            S64 = strips.astype(np.float64)
+            S64[:, 0, :, :bs] = 0
+            S64[:, -1, :, 2 * bs:] = 0
+            Ad = assemble_bdsv_dense(S64)
+            N = nbr * bs
+            x = xpad[:, bs:bs + N].astype(np.float64)
+            want = np.einsum("sij,sj->si", Ad, x)
+            bound = 3 * bs * eps * np.einsum("sij,sj->si", np.abs(Ad), np.abs(x)) * 1.01
+            assert np.all(np.abs(Y[:, bs:bs + N] - want) <= bound + 1e-300)
+
+
+def pin_bdmv_inverts_bdsv(orc):
+    """bdmv applied to the bdsv solution gives back b to the backward-error bound (the
+    two routines read the same strips with the same layout)."""
+    rng = _rng(49)
+    nbr, bs = 8, 6
+    strips, xpad = _random_bdsv(rng, 3, nbr, bs)
+    _, X, info = orc.bdsv(strips, xpad)
+    assert np.all(info == 0)
+    Y = orc.bdmv(strips, X)
+    N = nbr * bs
+    b = xpad[:, bs:bs + N]
+    Ad = assemble_bdsv_dense(strips)
+    scale = np.abs(Ad).sum(axis=2).max(axis=1) * np.abs(X).max(axis=1) + np.abs(b).max(axis=1)
+    assert np.all(np.abs(Y[:, bs:bs + N] - b).max(axis=1) <= 8 * N * eps_of(np.float64) * scale)
+
+
 LU_PINS = [pin_lu_3x3_hand_worked, pin_lu_2x2_closed_form, pin_lu_cramer_bruteforce,
            pin_lu_reconstruction, pin_lu_matches_lapack, pin_lu_info_contract,
            pin_lu_layout_invariance, pin_lu_near_tie_flag]
@@ -439,7 +625,10 @@ CHOL_PINS = [pin_chol_hand_worked, pin_chol_2x2_closed_form,
              pin_chol_reconstruction_and_lapack, pin_chol_info_contract]
 BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,
              pin_bdsv_scalar_tridiagonal, pin_bdsv_info]
-ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS
+SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
+              pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
+BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
+ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS
 
 
 def failing_pins(orc, pins=ALL_PINS):

@@ -25,7 +25,8 @@ MUTATIONS = [
      "    for (int i = k + 1; i < n; ++i) {\n      T v = std::fabs(a(i, k));\n      if (v > best)",
      "    for (int i = k + 1; i < n - 1; ++i) {\n      T v = std::fabs(a(i, k));\n      if (v > best)"),
     ("lu_rhs_not_swapped",
-     "        T t = b(k, c);\n        b(k, c) = b(p, c);\n        b(p, c) = t;", ""),
+     "        T t = b(k, c);\n        b(k, c) = b(p, c);\n        b(p, c) = t;\n      }\n    }\n    const T r",
+     "      }\n    }\n    const T r"),
     ("lu_L_part_not_swapped",
      "      for (int c = 0; c < n; ++c) {\n        T t = a(k, c);",
      "      for (int c = k; c < n; ++c) {\n        T t = a(k, c);"),
@@ -33,9 +34,12 @@ MUTATIONS = [
      "a(i, j) = std::fma(l, a(k, j), a(i, j));"),
     ("lu_schur_transposed_operand", "a(i, j) = std::fma(-l, a(k, j), a(i, j));",
      "a(i, j) = std::fma(-l, a(j, k), a(i, j));"),
-    ("lu_forward_solve_dropped", "b(i, c) = std::fma(-l, b(k, c), b(i, c));", ";"),
-    ("lu_back_subst_transposed", "b(i, c) = std::fma(-a(i, k), x, b(i, c));",
-     "b(i, c) = std::fma(-a(k, i), x, b(i, c));"),
+    ("lu_forward_solve_dropped",
+     "      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));\n    }\n  }\n  for (int k = n - 1",
+     "    }\n  }\n  for (int k = n - 1"),
+    ("lu_back_subst_transposed",
+     "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n  if (inf != 0) {",
+     "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n  if (inf != 0) {"),
     ("lu_floor_is_zero", "const bool ok = best >= floor_v;", "const bool ok = best > T(0);"),
     ("lu_info_off_by_one", "if (!ok && inf == 0) inf = k + 1;", "if (!ok && inf == 0) inf = k;"),
     ("lu_info_last_not_first", "if (!ok && inf == 0) inf = k + 1;", "if (!ok) inf = k + 1;"),
@@ -47,8 +51,9 @@ MUTATIONS = [
     ("chol_update_writes_upper",
      "for (int i = j; i < n; ++i) a(i, j) = std::fma(-a(i, k), ljk, a(i, j));",
      "for (int i = j; i < n; ++i) a(j, i) = std::fma(-a(i, k), ljk, a(j, i));"),
-    ("chol_back_solve_not_transposed", "b(i, c) = std::fma(-a(k, i), x, b(i, c));",
-     "b(i, c) = std::fma(-a(i, k), x, b(i, c));"),
+    ("chol_back_solve_not_transposed",
+     "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n  *info = 0;",
+     "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n  *info = 0;"),
     ("chol_info_off_by_one", "      inf = k + 1;\n      break;", "      inf = k;\n      break;"),
     ("chol_zero_pivot_accepted", "if (!(d > T(0))) {\n      inf = k + 1;",
      "if (!(d >= T(0))) {\n      inf = k + 1;"),
@@ -65,6 +70,31 @@ MUTATIONS = [
      "s = std::fma(-blk(k, MAIN, m, j), x[k * bs + m], s);",
      "s = std::fma(-blk(k, MAIN, j, m), x[k * bs + m], s);"),
     ("bdsv_info_local_index", "inf = k * bs + c + 1;", "inf = c + 1;"),
+    ("getrs_swaps_skipped", "    if (p != k)\n      for (int c = 0; c < nrhs; ++c) {",
+     "    if (false)\n      for (int c = 0; c < nrhs; ++c) {"),
+    ("getrs_swaps_reverse_order",
+     "  for (int k = 0; k < n; ++k) {\n    const int p = ipiv[k] - 1;",
+     "  for (int k = n - 1; k >= 0; --k) {\n    const int p = ipiv[k] - 1;"),
+    ("getrs_forward_transposed",
+     "      const T l = a(i, k);\n      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));\n    }\n  for",
+     "      const T l = a(k, i);\n      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));\n    }\n  for"),
+    ("getrs_back_subst_transposed",
+     "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n}",
+     "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n}"),
+    ("potrs_forward_unscaled",
+     "B[at(layout, n, nrhs, r, c)]; };\n  for (int c = 0; c < nrhs; ++c) {\n    for (int k = 0; k < n; ++k) {\n      const T y = b(k, c) * (T(1) / a(k, k));",
+     "B[at(layout, n, nrhs, r, c)]; };\n  for (int c = 0; c < nrhs; ++c) {\n    for (int k = 0; k < n; ++k) {\n      const T y = b(k, c);"),
+    ("potrs_back_solve_not_transposed",
+     "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n}",
+     "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n}"),
+    ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
+     "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
+    ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
+     "ypad[(int64_t)br * bs + row] = acc;"),
+    ("bdmv_right_block_dropped", "for (int c = 0; c < w; ++c) acc = std::fma(srow[c], xw[c], acc);",
+     "for (int c = 0; c < 2 * bs; ++c) acc = std::fma(srow[c], xw[c], acc);"),
+    ("bdmv_blocks_transposed", "acc = std::fma(srow[c], xw[c], acc);",
+     "acc = std::fma(strips[strip_at(bs, br, c / bs, c % bs, row)], xw[c], acc);"),
 ]
 
 
