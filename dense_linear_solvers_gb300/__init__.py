@@ -28,6 +28,8 @@ ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
 
 EXPORTED = (
     "bs_getrf_getrs_batched", "bs_potrf_potrs_batched", "bs_bdsv_batched",
+    "bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched", "bs_potrs_batched",
+    "bs_bdsv_factor_batched", "bs_bdsv_solve_batched", "bs_bdmv_batched",
     "bs_status_string", "bs_last_cuda_error", "bs_getrf_getrs_supported",
     "bs_potrf_potrs_supported", "bs_bdsv_supported", "bs_version",
 )
@@ -61,6 +63,17 @@ def lib() -> ctypes.CDLL:
             L.bs_potrf_potrs_batched.restype = i32
             L.bs_bdsv_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp]
             L.bs_bdsv_batched.restype = i32
+            L.bs_getrf_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp]
+            L.bs_getrs_batched.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp]
+            L.bs_potrf_batched.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp]
+            L.bs_potrs_batched.argtypes = [i32, i32, i32, i32, i32, i64, vp, vp, vp]
+            L.bs_bdsv_factor_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp]
+            L.bs_bdsv_solve_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp]
+            L.bs_bdmv_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp]
+            for name in ("bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched",
+                         "bs_potrs_batched", "bs_bdsv_factor_batched", "bs_bdsv_solve_batched",
+                         "bs_bdmv_batched"):
+                getattr(L, name).restype = i32
             L.bs_status_string.argtypes = [i32]
             L.bs_status_string.restype = ctypes.c_char_p
             L.bs_last_cuda_error.argtypes = []
@@ -137,3 +150,63 @@ def bs_bdsv_batched(strips, x_padded, info, stream=None) -> None:
     st = lib().bs_bdsv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
                                _ptr(info), _stream(stream))
     _check(st, "bs_bdsv_batched")
+
+
+# --------------------------------------------- factor once, solve per right-hand side
+def bs_getrf_batched(A, ipiv, info, layout: int = ROW_MAJOR, stream=None) -> None:
+    """LU with partial pivoting alone, in place: A <- L\\U, ipiv, info (see bsolve.h)."""
+    batch, n = A.shape[0], A.shape[1]
+    st = lib().bs_getrf_batched(_dtype_code(A), layout, n, batch, _ptr(A), _ptr(ipiv), _ptr(info),
+                                _stream(stream))
+    _check(st, "bs_getrf_batched")
+
+
+def bs_getrs_batched(LU, ipiv, B, layout: int = ROW_MAJOR, stream=None) -> None:
+    """Solve with a getrf factor: B <- X (see bsolve.h)."""
+    batch, n = LU.shape[0], LU.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    st = lib().bs_getrs_batched(_dtype_code(LU), layout, n, nrhs, batch, _ptr(LU), _ptr(ipiv),
+                                _ptr(B), _stream(stream))
+    _check(st, "bs_getrs_batched")
+
+
+def bs_potrf_batched(A, info, layout: int = COL_MAJOR, fill: int = BS_LOWER, stream=None) -> None:
+    """Cholesky alone, in place: the lower triangle of A <- L, info (see bsolve.h)."""
+    batch, n = A.shape[0], A.shape[1]
+    st = lib().bs_potrf_batched(_dtype_code(A), layout, fill, n, batch, _ptr(A), _ptr(info),
+                                _stream(stream))
+    _check(st, "bs_potrf_batched")
+
+
+def bs_potrs_batched(L, B, layout: int = COL_MAJOR, fill: int = BS_LOWER, stream=None) -> None:
+    """Solve with a potrf factor: B <- X (see bsolve.h)."""
+    batch, n = L.shape[0], L.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    st = lib().bs_potrs_batched(_dtype_code(L), layout, fill, n, nrhs, batch, _ptr(L), _ptr(B),
+                                _stream(stream))
+    _check(st, "bs_potrs_batched")
+
+
+def bs_bdsv_factor_batched(strips, info, stream=None) -> None:
+    """Block-Cholesky factor sweep alone, in place on the strips (see bsolve.h)."""
+    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    st = lib().bs_bdsv_factor_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips),
+                                      _ptr(info), _stream(stream))
+    _check(st, "bs_bdsv_factor_batched")
+
+
+def bs_bdsv_solve_batched(strips, x_padded, stream=None) -> None:
+    """Forward/backward block substitution with factored strips, in place on x (see
+    bsolve.h)."""
+    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    st = lib().bs_bdsv_solve_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips),
+                                     _ptr(x_padded), _stream(stream))
+    _check(st, "bs_bdsv_solve_batched")
+
+
+def bs_bdmv_batched(strips, x_padded, y_padded, stream=None) -> None:
+    """Block-tridiagonal matvec: the interior of y_padded <- A x (see bsolve.h)."""
+    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    st = lib().bs_bdmv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
+                               _ptr(y_padded), _stream(stream))
+    _check(st, "bs_bdmv_batched")

@@ -17,6 +17,12 @@ constexpr int kMaxBdsvBs = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
 bs_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return BS_OK;
   g_last_cuda_error = static_cast<int>(e);
@@ -112,6 +118,170 @@ bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_size, in
           : bsolve::launch_bdsv<double>(num_block_rows, block_size, batch,
                                         static_cast<double*>(strips),
                                         static_cast<double*>(x_padded), info, s);
+  return from_cuda(e);
+}
+
+bs_status bs_getrf_batched(bs_dtype dtype, bs_layout layout, int n, int64_t batch, void* A,
+                           int32_t* ipiv, int32_t* info, void* stream) {
+  if (n < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, 1)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !ipiv || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(ipiv) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_reg<float>(layout, n, 0, batch, static_cast<float*>(A), nullptr,
+                                           ipiv, info, s)
+            : bsolve::launch_lu_reg<double>(layout, n, 0, batch, static_cast<double*>(A),
+                                            nullptr, ipiv, info, s);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_smem<float>(layout, n, 0, batch, static_cast<float*>(A), nullptr,
+                                            ipiv, info, s)
+            : bsolve::launch_lu_smem<double>(layout, n, 0, batch, static_cast<double*>(A),
+                                             nullptr, ipiv, info, s);
+  }
+  return from_cuda(e);
+}
+
+bs_status bs_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs, int64_t batch,
+                           const void* LU, const int32_t* ipiv, void* B, void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!LU || !ipiv || !B) return BS_ERR_INVALID_ARG;
+  if (!aligned16(LU) || !aligned16(ipiv) || !aligned16(B)) return BS_ERR_INVALID_ARG;
+  const size_t es = dtype == BS_FP32 ? 4 : 8;
+  const size_t bbytes = static_cast<size_t>(batch) * n * nrhs * es;
+  if (overlap(B, bbytes, LU, static_cast<size_t>(batch) * n * n * es) ||
+      overlap(B, bbytes, ipiv, static_cast<size_t>(batch) * n * sizeof(int32_t)))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_getrs<float>(layout, n, nrhs, batch, static_cast<const float*>(LU),
+                                        ipiv, static_cast<float*>(B), s)
+          : bsolve::launch_getrs<double>(layout, n, nrhs, batch, static_cast<const double*>(LU),
+                                         ipiv, static_cast<double*>(B), s);
+  return from_cuda(e);
+}
+
+bs_status bs_potrf_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int64_t batch,
+                           void* A, int32_t* info, void* stream) {
+  if (n < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, 1)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_sys<float>(layout, n, 0, batch, static_cast<float*>(A), nullptr,
+                                             info, s)
+            : bsolve::launch_chol_sys<double>(layout, n, 0, batch, static_cast<double*>(A),
+                                              nullptr, info, s);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_smem<float>(layout, n, 0, batch, static_cast<float*>(A),
+                                              nullptr, info, s)
+            : bsolve::launch_chol_smem<double>(layout, n, 0, batch, static_cast<double*>(A),
+                                               nullptr, info, s);
+  }
+  return from_cuda(e);
+}
+
+bs_status bs_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs,
+                           int64_t batch, const void* L, void* B, void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!L || !B) return BS_ERR_INVALID_ARG;
+  if (!aligned16(L) || !aligned16(B)) return BS_ERR_INVALID_ARG;
+  const size_t es = dtype == BS_FP32 ? 4 : 8;
+  if (overlap(B, static_cast<size_t>(batch) * n * nrhs * es, L,
+              static_cast<size_t>(batch) * n * n * es))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_potrs<float>(layout, n, nrhs, batch, static_cast<const float*>(L),
+                                        static_cast<float*>(B), s)
+          : bsolve::launch_potrs<double>(layout, n, nrhs, batch, static_cast<const double*>(L),
+                                         static_cast<double*>(B), s);
+  return from_cuda(e);
+}
+
+bs_status bs_bdsv_factor_batched(bs_dtype dtype, int num_block_rows, int block_size,
+                                 int64_t batch, void* strips, int32_t* info, void* stream) {
+  if (num_block_rows < 0 || block_size < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!bdsv_supported(dtype, num_block_rows, block_size)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!strips || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(strips) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_bdsv_factor<float>(num_block_rows, block_size, batch,
+                                              static_cast<float*>(strips), info, s)
+          : bsolve::launch_bdsv_factor<double>(num_block_rows, block_size, batch,
+                                               static_cast<double*>(strips), info, s);
+  return from_cuda(e);
+}
+
+bs_status bs_bdsv_solve_batched(bs_dtype dtype, int num_block_rows, int block_size,
+                                int64_t batch, const void* strips, void* x_padded,
+                                void* stream) {
+  if (num_block_rows < 0 || block_size < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!bdsv_supported(dtype, num_block_rows, block_size)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!strips || !x_padded) return BS_ERR_INVALID_ARG;
+  if (!aligned16(strips) || !aligned16(x_padded)) return BS_ERR_INVALID_ARG;
+  const size_t es = dtype == BS_FP32 ? 4 : 8;
+  const size_t sbytes = static_cast<size_t>(batch) * num_block_rows * block_size * 3 *
+                        block_size * es;
+  const size_t vbytes = static_cast<size_t>(batch) * (num_block_rows + 2) * block_size * es;
+  if (overlap(x_padded, vbytes, strips, sbytes)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_bdsv_solve<float>(num_block_rows, block_size, batch,
+                                             static_cast<const float*>(strips),
+                                             static_cast<float*>(x_padded), s)
+          : bsolve::launch_bdsv_solve<double>(num_block_rows, block_size, batch,
+                                              static_cast<const double*>(strips),
+                                              static_cast<double*>(x_padded), s);
+  return from_cuda(e);
+}
+
+bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+                          const void* strips, const void* x_padded, void* y_padded,
+                          void* stream) {
+  if (num_block_rows < 0 || block_size < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!bdsv_supported(dtype, num_block_rows, block_size)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!strips || !x_padded || !y_padded) return BS_ERR_INVALID_ARG;
+  if (!aligned16(strips) || !aligned16(x_padded) || !aligned16(y_padded))
+    return BS_ERR_INVALID_ARG;
+  const size_t es = dtype == BS_FP32 ? 4 : 8;
+  const size_t sbytes = static_cast<size_t>(batch) * num_block_rows * block_size * 3 *
+                        block_size * es;
+  const size_t vbytes = static_cast<size_t>(batch) * (num_block_rows + 2) * block_size * es;
+  if (overlap(y_padded, vbytes, strips, sbytes) || overlap(y_padded, vbytes, x_padded, vbytes))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_bdmv<float>(num_block_rows, block_size, batch,
+                                       static_cast<const float*>(strips),
+                                       static_cast<const float*>(x_padded),
+                                       static_cast<float*>(y_padded), s)
+          : bsolve::launch_bdmv<double>(num_block_rows, block_size, batch,
+                                        static_cast<const double*>(strips),
+                                        static_cast<const double*>(x_padded),
+                                        static_cast<double*>(y_padded), s);
   return from_cuda(e);
 }
 

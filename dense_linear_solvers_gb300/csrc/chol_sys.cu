@@ -138,7 +138,7 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   // y_k its last update (in step k+1), so each step needs a single barrier.
   for (int c = slot; c < nrhs; c += kSlots) Ys[(n - 1) * nrhs + c] *= rr[(n - 1) * kSys + s];
   __syncthreads();
-  for (int k = n - 1; k >= 1; --k) {
+  for (int k = nrhs > 0 ? n - 1 : 0; k >= 1; --k) {   // nothing to do without B
     const int tk = tri(k);
     const T rkm1 = rr[(k - 1) * kSys + s];
     for (int e = slot; e < k * nrhs; e += kSlots) {

@@ -6,7 +6,8 @@
 
 namespace bsolve {
 
-// LU + solve, rows in registers, 1 <= n <= 32, 1 <= nrhs <= 8.
+// LU + solve, rows in registers, 1 <= n <= 32, 0 <= nrhs <= 8 (0: factor only). The
+// LU and Cholesky launchers below take nrhs = 0 the same way.
 template <typename T>
 cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                           int32_t* ipiv, int32_t* info, cudaStream_t stream);
@@ -15,6 +16,15 @@ cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B
 template <typename T>
 cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                            int32_t* ipiv, int32_t* info, cudaStream_t stream);
+
+// Solve with a stored factor: getrs (L\U and the 1-based swap sequence of getrf) and
+// potrs (lower Cholesky factor), 1 <= n <= 64, 1 <= nrhs <= 8.
+template <typename T>
+cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU,
+                         const int32_t* ipiv, T* B, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
+                         cudaStream_t stream);
 
 // Lower Cholesky + solve, one warp per system in shared memory, 1 <= n <= 64.
 template <typename T>
@@ -29,6 +39,19 @@ cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T*
 // Block-tridiagonal block-Cholesky sweep, one thread per system, 1 <= bs <= 8.
 template <typename T>
 cudaError_t launch_bdsv(int nbr, int bs, int64_t batch, T* strips, T* xpad, int32_t* info,
+                        cudaStream_t stream);
+
+// The factor sweep alone, and the substitutions alone on factored strips.
+template <typename T>
+cudaError_t launch_bdsv_factor(int nbr, int bs, int64_t batch, T* strips, int32_t* info,
+                               cudaStream_t stream);
+template <typename T>
+cudaError_t launch_bdsv_solve(int nbr, int bs, int64_t batch, const T* strips, T* xpad,
+                              cudaStream_t stream);
+
+// Block-tridiagonal matrix-vector product on padded vectors, 1 <= bs <= 8.
+template <typename T>
+cudaError_t launch_bdmv(int nbr, int bs, int64_t batch, const T* strips, const T* xpad, T* ypad,
                         cudaStream_t stream);
 
 // Shared memory one system needs in the shared-memory kernels.

@@ -135,8 +135,8 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     __syncthreads();
   }
 
-  // U x = y by blocks of kBlk rows, from the last block
-  const int nblk = (n + kBlk - 1) / kBlk;
+  // U x = y by blocks of kBlk rows, from the last block (nothing to do without B)
+  const int nblk = nrhs > 0 ? (n + kBlk - 1) / kBlk : 0;
   for (int cb = nblk - 1; cb >= 0; --cb) {
     const int lo = cb * kBlk, hi = min(n, lo + kBlk);
     if (warp == 0) {

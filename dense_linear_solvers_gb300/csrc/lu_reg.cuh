@@ -134,7 +134,7 @@ __device__ __forceinline__ void load_vec_shared(const T* p, T (&r)[N]) {
   }
 }
 
-// FULL: n == NT and nrhs == RT (every guard compiles away).
+// FULL: n == NT and nrhs == RT (every guard compiles away). RT = 0: factor only (getrf).
 template <typename T, int NT, int RT, int LAYOUT, bool FULL>
 __global__ void __launch_bounds__(kThreads)
 lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict__ B,
@@ -142,12 +142,14 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
   using Key = typename Traits<T>::Key;
   constexpr int G = NT;
   constexpr int GPW = 32 / G;                 // groups (systems) per warp
+  constexpr bool kSolve = RT > 0;
+  constexpr int RB = kSolve ? RT : 1;         // register / buffer size of the B part
   constexpr int W = NT + RT;                  // published row: A part, then B part
   constexpr int WP = (W * sizeof(T) + 15) / 16 * 16 / sizeof(T);
   constexpr unsigned GMASK = (G == 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
 
   __shared__ __align__(16) T prow[kWarps][GPW][2][WP];
-  __shared__ __align__(16) T xbuf[kWarps][GPW][2][RT];
+  __shared__ __align__(16) T xbuf[kWarps][GPW][2][RB];
 
   const int n = FULL ? NT : n_;
   const int nrhs = FULL ? RT : nrhs_;
@@ -160,31 +162,33 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
   const bool row_ok = valid && (FULL || t < n);
 
   T a[NT];
-  T b[RT];
+  T b[RB];
   const int64_t sA = s * n * n;
   const int64_t sB = s * n * nrhs;
   if (row_ok) {
     if (LAYOUT == kRowMajor) {
       if (FULL) {
         load_vec<T, NT>(A + sA + static_cast<int64_t>(t) * NT, a);
-        load_vec<T, RT>(B + sB + static_cast<int64_t>(t) * RT, b);
+        if constexpr (kSolve) load_vec<T, RT>(B + sB + static_cast<int64_t>(t) * RT, b);
       } else {
 #pragma unroll
         for (int j = 0; j < NT; ++j) a[j] = (j < n) ? A[sA + t * n + j] : T(0);
 #pragma unroll
         for (int c = 0; c < RT; ++c) b[c] = (c < nrhs) ? B[sB + t * nrhs + c] : T(0);
+        if constexpr (!kSolve) b[0] = T(0);
       }
     } else {
 #pragma unroll
       for (int j = 0; j < NT; ++j) a[j] = (FULL || j < n) ? A[sA + j * n + t] : T(0);
 #pragma unroll
       for (int c = 0; c < RT; ++c) b[c] = (FULL || c < nrhs) ? B[sB + c * n + t] : T(0);
+      if constexpr (!kSolve) b[0] = T(0);
     }
   } else {
 #pragma unroll
     for (int j = 0; j < NT; ++j) a[j] = T(0);
 #pragma unroll
-    for (int c = 0; c < RT; ++c) b[c] = T(0);
+    for (int c = 0; c < RB; ++c) b[c] = T(0);
   }
 
   using LK = LiveKey<T>;
@@ -276,7 +280,7 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
 #pragma unroll
       for (int j = 0; j < NT; j += V)
         if (j >= c1) st_chunk<T>(pr + j, a, j);
-      store_vec<T, RT>(pr + NT, b);
+      if constexpr (kSolve) store_vec<T, RT>(pr + NT, b);
     }
     __syncwarp();
     if (upd) {
@@ -284,8 +288,8 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
 #pragma unroll
       for (int j = 0; j < NT; j += V)
         if (j >= c1) ld_chunk<T>(pr + j, u, j);
-      T ub[RT];
-      load_vec_shared<T, RT>(pr + NT, ub);
+      T ub[RB];
+      if constexpr (kSolve) load_vec_shared<T, RT>(pr + NT, ub);
 #pragma unroll
       for (int j = k + 1; j < NT; ++j) a[j] = fma_rn<T>(-l, u[j], a[j]);
 #pragma unroll
@@ -296,6 +300,7 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
   // U x = y, from the last position.
 #pragma unroll
   for (int i = NT - 1; i >= 0; --i) {
+    if constexpr (!kSolve) break;
     if (!FULL && i >= n) continue;
     T* xb = xbuf[warp][g][i & 1];
     if (row_ok && pos == i) {
@@ -320,7 +325,7 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     if (LAYOUT == kRowMajor) {
       if (FULL) {
         store_vec<T, NT>(A + sA + static_cast<int64_t>(pos) * NT, a);
-        store_vec<T, RT>(B + sB + static_cast<int64_t>(pos) * RT, b);
+        if constexpr (kSolve) store_vec<T, RT>(B + sB + static_cast<int64_t>(pos) * RT, b);
       } else {
 #pragma unroll
         for (int j = 0; j < NT; ++j)
@@ -360,6 +365,7 @@ cudaError_t launch_tier(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipi
 template <typename T, int NT, int LAYOUT>
 cudaError_t launch_rhs(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv, int32_t* info,
                        cudaStream_t stream) {
+  if (nrhs == 0) return launch_tier<T, NT, 0, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
   if (nrhs <= 1) return launch_tier<T, NT, 1, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
   if (nrhs <= 2) return launch_tier<T, NT, 2, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
   if (nrhs <= 4) return launch_tier<T, NT, 4, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);

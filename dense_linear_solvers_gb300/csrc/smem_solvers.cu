@@ -123,7 +123,7 @@ chol_smem_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     __syncwarp();
   }
   __syncwarp();
-  if (inf == 0) {
+  if (inf == 0 && nrhs > 0) {
     // L^T x = y
     for (int k = n - 1; k >= 0; --k) {
       const T r = rcp[k];

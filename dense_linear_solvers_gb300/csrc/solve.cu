@@ -1,0 +1,342 @@
+// Solves with a stored factor: getrs (L\U from getrf and its swap sequence) and potrs
+// (the lower Cholesky factor from potrf). "Factor once, call this per right-hand side"
+// (GLASS API reference, "Block-tridiagonal Ops", bdsv_solve; TDLS API,
+// "solver_static.hpp File Reference", separate substitution).
+//
+// n <= 32: one system per group of G = NT lanes (32/NT systems per warp), lane t owns
+// position t: its right-hand-side row in registers, and in registers the factor entries
+// its row needs. For LU that is row t of L\U (the forward sweep reads l_tk, k < t, the
+// backward sweep u_tk, k > t). For Cholesky the forward sweep needs row t of L and the
+// backward sweep (with L^T) column t, so lane t holds the symmetric fill of the lower
+// triangle: v[j] = L[max(t,j)][min(t,j)] (row t left of the diagonal, column t right of
+// it). Each step k then broadcasts one value per right-hand side from lane k by a
+// shuffle, and every lane applies it from registers: no shared memory, no barrier.
+// 32 < n <= 64: one warp per system, the factor in shared memory with an odd pitch, lane
+// t owning positions t and t+32.
+//
+// getrs: lane t loads the right-hand-side row that the swap sequence brings to position
+// t (the swaps undone from the last: pos = t, then for k = n-1..0 pos <- tau_k(pos)); an
+// ipiv entry outside 1..n swaps nothing, so no access leaves the system.
+// The arithmetic is the CPU oracle's, operation by operation: b_i -= l_ik y_k for i > k
+// in increasing k (Cholesky: y_k = b_k * (1/l_kk) first), then x_k = y_k * r_k and
+// b_i -= m_ik x_k for i < k in decreasing k; r_k = 1/u_kk (1 for a pivot below the
+// smallest normal) for LU, 1/l_kk for Cholesky; every update one fused multiply-add.
+#include <cfloat>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsolve {
+namespace {
+
+enum SolveKind : int { kSolveLu = 0, kSolveChol = 1 };
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+
+template <typename T> struct Floor;   // smallest normal number: a smaller |pivot| is singular
+template <> struct Floor<float> {
+  __device__ __forceinline__ static float v() { return FLT_MIN; }
+};
+template <> struct Floor<double> {
+  __device__ __forceinline__ static double v() { return DBL_MIN; }
+};
+
+template <typename T, int KIND>
+__device__ __forceinline__ T diag_rcp(T d) {
+  if (KIND == kSolveLu) return (fabs(d) >= Floor<T>::v()) ? T(1) / d : T(1);
+  return T(1) / d;
+}
+
+// Element (r, c) of an n x m matrix in the given storage order.
+__device__ __forceinline__ int64_t idx(int layout, int rows, int cols, int r, int c) {
+  return layout == kRowMajor ? static_cast<int64_t>(r) * cols + c
+                             : static_cast<int64_t>(c) * rows + r;
+}
+
+// ------------------------------------------------------------------ n <= 32, registers
+template <typename T, int NT, int RT, int KIND>
+__global__ void __launch_bounds__(kThreads)
+solve_reg_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restrict__ M,
+                 const int32_t* __restrict__ ipiv, T* __restrict__ B) {
+  constexpr int G = NT;
+  constexpr int GPW = 32 / G;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane / G;
+  const int t = lane % G;
+  const int64_t s = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * GPW + g;
+  const bool valid = s < batch;
+  const bool row_ok = valid && t < n;
+  const T* Ms = M + s * n * n;
+  T* Bs = B + s * n * nrhs;
+
+  T v[NT];
+  T rt = T(1);
+  int src = t;   // the right-hand-side row that lands at position t
+  if (KIND == kSolveLu) {
+    // undo the swaps from the last; lane k of the group holds ipiv[k]
+    const int ip = row_ok ? __ldg(ipiv + s * n + t) - 1 : 0;
+#pragma unroll
+    for (int k = NT - 1; k >= 0; --k) {
+      int p = __shfl_sync(0xFFFFFFFFu, ip, k, G);
+      if (p < 0 || p >= n) p = k;   // an entry out of range swaps nothing
+      if (k < n) {
+        if (src == k) src = p;
+        else if (src == p) src = k;
+      }
+    }
+  }
+  if (row_ok) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      if (j < n) {
+        const int r = (KIND == kSolveLu || j <= t) ? t : j;
+        const int c = (KIND == kSolveLu || j <= t) ? j : t;
+        v[j] = __ldg(Ms + idx(layout, n, n, r, c));
+      } else {
+        v[j] = T(0);
+      }
+    }
+    rt = diag_rcp<T, KIND>(__ldg(Ms + idx(layout, n, n, t, t)));
+  } else {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) v[j] = T(0);
+  }
+  T b[RT];
+#pragma unroll
+  for (int c = 0; c < RT; ++c) b[c] = (row_ok && c < nrhs) ? Bs[idx(layout, n, nrhs, src, c)] : T(0);
+
+  // forward: L y = P b (unit L) or L y = b
+#pragma unroll
+  for (int k = 0; k < NT; ++k) {
+    if (k >= n) break;
+    if (KIND == kSolveChol && t == k) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = b[c] * rt;
+    }
+    T y[RT];
+#pragma unroll
+    for (int c = 0; c < RT; ++c) y[c] = __shfl_sync(0xFFFFFFFFu, b[c], k, G);
+    if (row_ok && t > k) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-v[k], y[c], b[c]);
+    }
+  }
+  // backward: U x = y or L^T x = y
+#pragma unroll
+  for (int k = NT - 1; k >= 0; --k) {
+    if (k >= n) continue;
+    if (t == k) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = b[c] * rt;
+    }
+    T x[RT];
+#pragma unroll
+    for (int c = 0; c < RT; ++c) x[c] = __shfl_sync(0xFFFFFFFFu, b[c], k, G);
+    if (row_ok && t < k) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-v[k], x[c], b[c]);
+    }
+  }
+  if (row_ok) {
+#pragma unroll
+    for (int c = 0; c < RT; ++c)
+      if (c < nrhs) Bs[idx(layout, n, nrhs, t, c)] = b[c];
+  }
+}
+
+template <typename T, int NT, int KIND>
+cudaError_t launch_reg_rhs(int layout, int n, int nrhs, int64_t batch, const T* M,
+                           const int32_t* ipiv, T* B, cudaStream_t stream) {
+  constexpr int per_block = kWarps * (32 / NT);
+  const int64_t blocks = (batch + per_block - 1) / per_block;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const unsigned nb = static_cast<unsigned>(blocks);
+  if (nrhs <= 1)
+    solve_reg_kernel<T, NT, 1, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+  else if (nrhs <= 2)
+    solve_reg_kernel<T, NT, 2, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+  else if (nrhs <= 4)
+    solve_reg_kernel<T, NT, 4, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+  else
+    solve_reg_kernel<T, NT, 8, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------- 32 < n <= 64, shared memory, a warp
+constexpr int kSmemWarps = 2;
+
+__host__ __device__ inline int odd_pitch(int n) { return n | 1; }
+
+template <typename T, int RT, int KIND>
+__global__ void __launch_bounds__(kSmemWarps * 32)
+solve_smem_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restrict__ M,
+                  const int32_t* __restrict__ ipiv, T* __restrict__ B) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int P = odd_pitch(n);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t s = static_cast<int64_t>(blockIdx.x) * kSmemWarps + warp;
+  if (s >= batch) return;   // whole warp: no block barrier below
+  T* const F = reinterpret_cast<T*>(smem_raw) + static_cast<int64_t>(warp) * n * P;
+  const T* Ms = M + s * n * n;
+  T* Bs = B + s * n * nrhs;
+
+  // the factor (LU: all of it; Cholesky: the lower triangle only)
+  for (int e = lane; e < n * n; e += 32) {
+    int r, c;
+    if (layout == kRowMajor) {
+      r = e / n;
+      c = e - r * n;
+    } else {
+      c = e / n;
+      r = e - c * n;
+    }
+    if (KIND == kSolveLu || c <= r) cp_async_elem<T>(F + r * P + c, Ms + e);
+  }
+  cp_async_wait_all();
+  __syncwarp();
+
+  int src[2] = {lane, lane + 32};
+  if (KIND == kSolveLu) {
+    const int ip0 = lane < n ? __ldg(ipiv + s * n + lane) - 1 : 0;
+    const int ip1 = lane + 32 < n ? __ldg(ipiv + s * n + lane + 32) - 1 : 0;
+    for (int k = n - 1; k >= 0; --k) {
+      int p = __shfl_sync(0xFFFFFFFFu, k < 32 ? ip0 : ip1, k & 31);
+      if (p < 0 || p >= n) p = k;   // an entry out of range swaps nothing
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (src[q] == k) src[q] = p;
+        else if (src[q] == p) src[q] = k;
+      }
+    }
+  }
+  T b[2][RT];
+  T rq[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int i = lane + 32 * q;
+    const bool ok = i < n;
+    rq[q] = ok ? diag_rcp<T, KIND>(F[i * P + i]) : T(1);
+#pragma unroll
+    for (int c = 0; c < RT; ++c) b[q][c] = (ok && c < nrhs) ? Bs[idx(layout, n, nrhs, src[q], c)] : T(0);
+  }
+
+  for (int k = 0; k < n; ++k) {
+    const int kq = k >> 5, kl = k & 31;
+    if (KIND == kSolveChol && lane == kl) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) {
+        if (kq == 0) b[0][c] = b[0][c] * rq[0];
+        else b[1][c] = b[1][c] * rq[1];
+      }
+    }
+    T y[RT];
+#pragma unroll
+    for (int c = 0; c < RT; ++c) y[c] = __shfl_sync(0xFFFFFFFFu, kq == 0 ? b[0][c] : b[1][c], kl);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = lane + 32 * q;
+      if (i > k && i < n) {
+        const T l = F[i * P + k];
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-l, y[c], b[q][c]);
+      }
+    }
+  }
+  for (int k = n - 1; k >= 0; --k) {
+    const int kq = k >> 5, kl = k & 31;
+    if (lane == kl) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) {
+        if (kq == 0) b[0][c] = b[0][c] * rq[0];
+        else b[1][c] = b[1][c] * rq[1];
+      }
+    }
+    T x[RT];
+#pragma unroll
+    for (int c = 0; c < RT; ++c) x[c] = __shfl_sync(0xFFFFFFFFu, kq == 0 ? b[0][c] : b[1][c], kl);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = lane + 32 * q;
+      if (i < k) {
+        const T u = KIND == kSolveLu ? F[i * P + k] : F[k * P + i];
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-u, x[c], b[q][c]);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int i = lane + 32 * q;
+    if (i < n) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c)
+        if (c < nrhs) Bs[idx(layout, n, nrhs, i, c)] = b[q][c];
+    }
+  }
+}
+
+template <typename T, int KIND>
+cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
+                        const int32_t* ipiv, T* B, cudaStream_t stream) {
+  const int64_t blocks = (batch + kSmemWarps - 1) / kSmemWarps;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const size_t bytes = static_cast<size_t>(kSmemWarps) * n * odd_pitch(n) * sizeof(T);
+  const unsigned nb = static_cast<unsigned>(blocks);
+  cudaError_t e = cudaSuccess;
+#define BSOLVE_SOLVE_SMEM(RTV)                                                              \
+  e = cudaFuncSetAttribute(solve_smem_kernel<T, RTV, KIND>,                                 \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)); \
+  if (e != cudaSuccess) return e;                                                           \
+  solve_smem_kernel<T, RTV, KIND><<<nb, kSmemWarps * 32, bytes, stream>>>(n, nrhs, layout,  \
+                                                                          batch, M, ipiv, B);
+  if (nrhs <= 1) {
+    BSOLVE_SOLVE_SMEM(1)
+  } else if (nrhs <= 2) {
+    BSOLVE_SOLVE_SMEM(2)
+  } else if (nrhs <= 4) {
+    BSOLVE_SOLVE_SMEM(4)
+  } else {
+    BSOLVE_SOLVE_SMEM(8)
+  }
+#undef BSOLVE_SOLVE_SMEM
+  return cudaGetLastError();
+}
+
+template <typename T, int KIND>
+cudaError_t launch_kind(int layout, int n, int nrhs, int64_t batch, const T* M,
+                        const int32_t* ipiv, T* B, cudaStream_t stream) {
+  if (n <= 4) return launch_reg_rhs<T, 4, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 8) return launch_reg_rhs<T, 8, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 16) return launch_reg_rhs<T, 16, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 32) return launch_reg_rhs<T, 32, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 64) return launch_smem<T, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU,
+                         const int32_t* ipiv, T* B, cudaStream_t stream) {
+  return launch_kind<T, kSolveLu>(layout, n, nrhs, batch, LU, ipiv, B, stream);
+}
+
+template <typename T>
+cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
+                         cudaStream_t stream) {
+  return launch_kind<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, stream);
+}
+
+template cudaError_t launch_getrs<float>(int, int, int, int64_t, const float*, const int32_t*,
+                                         float*, cudaStream_t);
+template cudaError_t launch_getrs<double>(int, int, int, int64_t, const double*, const int32_t*,
+                                          double*, cudaStream_t);
+template cudaError_t launch_potrs<float>(int, int, int, int64_t, const float*, float*,
+                                         cudaStream_t);
+template cudaError_t launch_potrs<double>(int, int, int, int64_t, const double*, double*,
+                                          cudaStream_t);
+
+}  // namespace bsolve

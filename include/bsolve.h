@@ -129,6 +129,68 @@ BS_API bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fil
 BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
                           void* strips, void* x_padded, int32_t* info, void* stream);
 
+/*
+ * Factor once, solve per right-hand side: the two halves of the fused calls above.
+ *
+ * Source: GLASS API reference, "Block-tridiagonal Ops", "Direct solve (glass::bdsv)"
+ * (bdsv_factor, bdsv_solve: "reusable: factor once, call this per right-hand side");
+ * TDLS API, "solver_static.hpp File Reference", Detailed Description (the substitution as
+ * a step of its own after the factorization).
+ *
+ * The factor calls leave A (or the strips), ipiv and info exactly as the fused call does;
+ * the solve calls, given that factor, leave exactly the fused call's X wherever info == 0
+ * (same operations in the same order). The solve calls take no info: with a factor whose
+ * info != 0 their X is unspecified (the fused calls return zeros there).
+ *
+ * bs_getrf_batched:  A (batch x n x n, `layout`) <- L\U, ipiv, info as bs_getrf_getrs_batched.
+ * bs_getrs_batched:  LU, ipiv from bs_getrf_batched (read only; an ipiv entry outside 1..n
+ *                    swaps nothing); B (batch x n x nrhs, same layout) <- X. B must not
+ *                    overlap LU or ipiv.
+ * bs_potrf_batched:  A <- L (lower triangle; the strict upper triangle neither read nor
+ *                    written), info as bs_potrf_potrs_batched.
+ * bs_potrs_batched:  L from bs_potrf_batched (read only, lower triangle only); B <- X.
+ * bs_bdsv_factor_batched: strips <- F_k (MAIN, lower), E_k (LEFT); info as bs_bdsv_batched.
+ * bs_bdsv_solve_batched:  strips from bs_bdsv_factor_batched (read only); interior of
+ *                    x_padded: b on entry, x on return (pads neither read nor written).
+ * Supported: as the fused calls (getrf/potrf: 1 <= n <= 64; getrs/potrs: 1 <= n <= 64,
+ * 1 <= nrhs <= 8; bdsv: 1 <= block_size <= 8), FP32/FP64, both layouts, fill BS_LOWER.
+ */
+BS_API bs_status bs_getrf_batched(bs_dtype dtype, bs_layout layout, int n, int64_t batch, void* A,
+                                  int32_t* ipiv, int32_t* info, void* stream);
+BS_API bs_status bs_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs, int64_t batch,
+                                  const void* LU, const int32_t* ipiv, void* B, void* stream);
+BS_API bs_status bs_potrf_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                  int64_t batch, void* A, int32_t* info, void* stream);
+BS_API bs_status bs_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs,
+                                  int64_t batch, const void* L, void* B, void* stream);
+BS_API bs_status bs_bdsv_factor_batched(bs_dtype dtype, int num_block_rows, int block_size,
+                                        int64_t batch, void* strips, int32_t* info, void* stream);
+BS_API bs_status bs_bdsv_solve_batched(bs_dtype dtype, int num_block_rows, int block_size,
+                                       int64_t batch, const void* strips, void* x_padded,
+                                       void* stream);
+
+/*
+ * Block-tridiagonal matrix-vector product y = A x (glass::bdmv).
+ *
+ * Source: GLASS API reference, "Block-tridiagonal Ops", section "Block-tridiagonal
+ * matrix-vector product (glass::bdmv)" -- strips [L | D | R], padded vectors, block-row br
+ * reads the window x_padded[br*bs, br*bs + 3*bs) and writes y_padded[(br+1)*bs + row].
+ *
+ *   strips    as bs_bdsv_batched, read only; all three blocks are read as stored (the
+ *             caller keeps the pad blocks of x_padded zero, so that L_0 and R_{nbr-1}
+ *             multiply zeros).
+ *   x_padded  batch x (num_block_rows + 2)*block_size, read only.
+ *   y_padded  same shape; the interior receives A x, the two pad blocks are not written.
+ *             Must not overlap strips or x_padded (BS_ERR_INVALID_ARG when it does).
+ * Each entry is one dot product over its strip row in increasing column order, one fused
+ * multiply-add per term, from zero (the pages fix no order; the result does not depend on
+ * the launch configuration).
+ * Supported: dtype FP32/FP64, 1 <= block_size <= 8, num_block_rows >= 1.
+ */
+BS_API bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+                                 const void* strips, const void* x_padded, void* y_padded,
+                                 void* stream);
+
 /* Human-readable name of a status code (a static string). */
 BS_API const char* bs_status_string(bs_status status);
 

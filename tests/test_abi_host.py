@@ -97,6 +97,46 @@ def test_bdsv_argument_errors(lib):
     assert f(bs.BS_FP64, 32, 8, 4, FAKE, FAKE + 8, FAKE, None) == bs.BS_ERR_INVALID_ARG
 
 
+def test_split_argument_errors(lib):
+    """The factor and solve halves check their arguments like the fused calls, and the
+    solve calls refuse an output that overlaps a read-only input."""
+    A, B, P, I = FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000
+    f = lib.bs_getrf_batched
+    assert f(bs.BS_FP32, 0, 16, 0, None, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP32, 0, 65, 5, A, P, I, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, -1, 5, A, P, I, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 5, A, None, I, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 5, A + 4, P, I, None) == bs.BS_ERR_INVALID_ARG
+    f = lib.bs_getrs_batched
+    assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP32, 0, 16, 9, 5, A, P, B, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, P, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, P, A + 16, None) == bs.BS_ERR_INVALID_ARG  # B over LU
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, P, P, None) == bs.BS_ERR_INVALID_ARG       # B over ipiv
+    f = lib.bs_potrf_batched
+    assert f(bs.BS_FP64, 1, 0, 32, 0, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 1, 1, 32, 5, A, I, None) == bs.BS_ERR_UNSUPPORTED  # upper fill
+    assert f(bs.BS_FP64, 1, 0, 32, 5, A, None, None) == bs.BS_ERR_INVALID_ARG
+    f = lib.bs_potrs_batched
+    assert f(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 1, 0, 32, 1, 5, A, A, None) == bs.BS_ERR_INVALID_ARG       # B over L
+    assert f(bs.BS_FP64, 1, 0, 32, 0, 5, A, B, None) == bs.BS_ERR_UNSUPPORTED
+    f = lib.bs_bdsv_factor_batched
+    assert f(bs.BS_FP64, 32, 8, 0, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 32, 9, 4, A, I, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP64, 32, 8, 4, A, None, None) == bs.BS_ERR_INVALID_ARG
+    f = lib.bs_bdsv_solve_batched
+    assert f(bs.BS_FP64, 32, 8, 0, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 32, 8, 4, A, A + 64, None) == bs.BS_ERR_INVALID_ARG        # x over strips
+    assert f(bs.BS_FP64, 32, 8, 4, A, B + 8, None) == bs.BS_ERR_INVALID_ARG         # misaligned
+    f = lib.bs_bdmv_batched
+    assert f(bs.BS_FP64, 32, 8, 0, None, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 32, 0, 4, A, B, P, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, B + 16, None) == bs.BS_ERR_INVALID_ARG     # y over x
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, A, None) == bs.BS_ERR_INVALID_ARG          # y over strips
+
+
 def test_binding_refuses_host_tensors():
     import torch
     A = torch.zeros((2, 4, 4))
