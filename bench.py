@@ -174,6 +174,75 @@ class Problem:
             dst.copy_(src)
 
 
+# The factor / solve halves and the block-tridiagonal matvec, each measured on the inputs of
+# the workload it serves (the solves on a factor made once before timing).
+NEXT_ROWS = {
+    "getrf_f32_n16": ("lu_f32_n16", "getrf"),
+    "getrs_f32_n16": ("lu_f32_n16", "getrs"),
+    "potrf_f64_n32": ("chol_f64_n32", "potrf"),
+    "potrs_f64_n32": ("chol_f64_n32", "potrs"),
+    "bdsv_factor_f64_32x8": ("bdsv_f64_32x8", "bdsv_factor"),
+    "bdsv_solve_f64_32x8": ("bdsv_f64_32x8", "bdsv_solve"),
+    "bdmv_f64_32x8": ("bdsv_f64_32x8", "bdmv"),
+}
+KERNEL_SOURCES.update({
+    "getrf_f32_n16": ["lu_reg.cuh", "common.cuh"], "getrs_f32_n16": ["solve.cu", "common.cuh"],
+    "potrf_f64_n32": ["chol_sys.cu", "common.cuh"], "potrs_f64_n32": ["solve.cu", "common.cuh"],
+    "bdsv_factor_f64_32x8": ["bdsv.cu", "common.cuh"],
+    "bdsv_solve_f64_32x8": ["bdsv.cu", "common.cuh"], "bdmv_f64_32x8": ["bdmv.cu", "common.cuh"],
+})
+
+
+class SplitProblem(Problem):
+    """One of NEXT_ROWS: the inputs of its base workload, the operation alone."""
+
+    def __init__(self, name: str, device):
+        import torch
+        base, op = NEXT_ROWS[name]
+        super().__init__(base, None, device)
+        self.op = op
+        bs, w = self.bs, self.w
+        a, b = self.inputs
+        if op == "getrs":
+            LU = a.clone()
+            bs.bs_getrf_batched(LU, self.ipiv, self.info, w.layout)
+            self.inputs, self.fixed = [b], (LU, self.ipiv)
+        elif op == "potrs":
+            L = a.clone()
+            bs.bs_potrf_batched(L, self.info, w.layout)
+            self.inputs, self.fixed = [b], (L,)
+        elif op == "bdsv_solve":
+            S = a.clone()
+            bs.bs_bdsv_factor_batched(S, self.info)
+            self.inputs, self.fixed = [b], (S,)
+        elif op == "bdmv":
+            self.y = torch.zeros_like(b)
+            self.inputs, self.fixed = [], (a, b)
+        else:   # the factor calls mutate A only
+            self.inputs = [a]
+        torch.cuda.synchronize()
+        self.work = [x.clone() for x in self.inputs]
+        elem = np.dtype(w.dtype).itemsize
+        self.bytes_per_sys, self.flops_per_sys = costs.per_system(op, w.n, w.nrhs, elem, w.nbr)
+
+    def call(self, bufs=None, stream=None):
+        bs, w, op = self.bs, self.w, self.op
+        if op == "getrf":
+            bs.bs_getrf_batched(self.work[0], self.ipiv, self.info, w.layout, stream)
+        elif op == "getrs":
+            bs.bs_getrs_batched(self.fixed[0], self.fixed[1], self.work[0], w.layout, stream)
+        elif op == "potrf":
+            bs.bs_potrf_batched(self.work[0], self.info, w.layout, bs.BS_LOWER, stream)
+        elif op == "potrs":
+            bs.bs_potrs_batched(self.fixed[0], self.work[0], w.layout, bs.BS_LOWER, stream)
+        elif op == "bdsv_factor":
+            bs.bs_bdsv_factor_batched(self.work[0], self.info, stream)
+        elif op == "bdsv_solve":
+            bs.bs_bdsv_solve_batched(self.fixed[0], self.work[0], stream)
+        else:
+            bs.bs_bdmv_batched(self.fixed[0], self.fixed[1], self.y, stream)
+
+
 def time_device(prob: Problem, steps: int, warmup: int, flush, min_warm_s: float = 0.0):
     torch = prob.torch
     stream = torch.cuda.current_stream()
@@ -393,6 +462,16 @@ def run_native(args) -> None:
         extra[args.workload] = {"systems_per_s": line["value"] / world, "ms_per_step": line["ms_per_step"],
                                 "batch": prob.batch, "roofline": line["roofline"]}
         line["workloads"] = extra
+        nxt = {}
+        for name in NEXT_ROWS:
+            p = SplitProblem(name, dev)
+            tt = time_device(p, min(args.steps, 10), 3, flush)
+            m = statistics.fmean(tt)
+            nxt[name] = {"op": p.op, "on": p.w.name, "systems_per_s": round(p.batch / (m * 1e-3), 1),
+                         "ms_per_step": round(m, 4), "batch": p.batch,
+                         "roofline": roofline(p, m, peaks, name)}
+            del p
+        line["next_rows"] = nxt
     print(json.dumps(line), flush=True)
     ranks.close()
 

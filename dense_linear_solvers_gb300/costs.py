@@ -63,12 +63,66 @@ def bdsv_flops(nbr: int, bs: int) -> int:
     return potrf * nbr + (trsm + syrk) * (nbr - 1) + gemv * 2 * (nbr - 1) + trsv * 2 * nbr
 
 
+# --- the factor / solve halves and the block-tridiagonal matvec -------------------------
+def getrf_only(n: int, elem: int):
+    return 2 * n * n * elem + 4 * n + 4, n * (n - 1) // 2 + (n - 1) * n * (2 * n - 1) // 3
+
+
+def getrs_only(n: int, nrhs: int, elem: int):
+    # reads L\U and ipiv, reads and writes B
+    return n * n * elem + 4 * n + 2 * n * nrhs * elem, nrhs * (2 * n * n - n)
+
+
+def potrf_only(n: int, elem: int):
+    return 2 * (n * (n + 1) // 2) * elem + 4, n + n * (n - 1) // 2 + (n - 1) * n * (n + 1) // 3
+
+
+def potrs_only(n: int, nrhs: int, elem: int):
+    return (n * (n + 1) // 2) * elem + 2 * n * nrhs * elem, 2 * n * n * nrhs
+
+
+def bdsv_factor_only(nbr: int, bs: int, elem: int):
+    d_lower = nbr * bs * (bs + 1) // 2
+    left = (nbr - 1) * bs * bs
+    potrf = bs + bs * (bs - 1) // 2 + (bs - 1) * bs * (bs + 1) // 3
+    flops = potrf * nbr + (bs ** 3 + bs * bs * (bs + 1)) * (nbr - 1)
+    return 2 * (d_lower + left) * elem + 4, flops
+
+
+def bdsv_solve_only(nbr: int, bs: int, elem: int):
+    d_lower = nbr * bs * (bs + 1) // 2
+    left = (nbr - 1) * bs * bs
+    vec = nbr * bs
+    return (d_lower + left) * elem + 2 * vec * elem, 2 * bs * bs * 2 * (nbr - 1) + bs * bs * 2 * nbr
+
+
+def bdmv_bytes_flops(nbr: int, bs: int, elem: int):
+    # every strip entry and the padded x in, the interior of y out
+    strips = nbr * bs * 3 * bs
+    return (strips + (nbr + 2) * bs + nbr * bs) * elem, 2 * strips
+
+
 def per_system(op: str, n: int, nrhs: int, elem: int, nbr: int = 0):
-    """(bytes, flops) of one system of a workload."""
+    """(bytes, flops) of one system of a workload (n is the block size for the
+    block-tridiagonal operations)."""
     if op == "getrf_getrs":
         return getrf_getrs_bytes(n, nrhs, elem), getrf_getrs_flops(n, nrhs)
     if op == "potrf_potrs":
         return potrf_potrs_bytes(n, nrhs, elem), potrf_potrs_flops(n, nrhs)
     if op == "bdsv":
         return bdsv_bytes(nbr, n, elem), bdsv_flops(nbr, n)
+    if op == "getrf":
+        return getrf_only(n, elem)
+    if op == "getrs":
+        return getrs_only(n, nrhs, elem)
+    if op == "potrf":
+        return potrf_only(n, elem)
+    if op == "potrs":
+        return potrs_only(n, nrhs, elem)
+    if op == "bdsv_factor":
+        return bdsv_factor_only(nbr, n, elem)
+    if op == "bdsv_solve":
+        return bdsv_solve_only(nbr, n, elem)
+    if op == "bdmv":
+        return bdmv_bytes_flops(nbr, n, elem)
     raise KeyError(op)
