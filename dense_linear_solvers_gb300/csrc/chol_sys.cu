@@ -28,7 +28,7 @@ namespace bsolve {
 namespace {
 
 constexpr int kSys = 16;      // systems per block
-constexpr int kWarps = 8;     // warps per block
+constexpr int kWarps = 16;    // warps per block (3 blocks per SM by shared memory: 48 warps)
 constexpr int kSlots = kWarps * 2;
 constexpr int kMaxN = 32;
 
@@ -82,8 +82,11 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   __syncthreads();
 
   for (int k = 0; k < n; ++k) {
-    // A: the pivot square root and reciprocal of column k, one lane per system
-    if (tid < kSys) {
+    // A: the pivot square root and reciprocal of column k, one lane per system, on lanes
+    //    0..15 of a warp that rotates with the column and the block: warp w runs on SM
+    //    sub-partition w % 4, so a fixed warp would put every block's chain on one FP64 pipe
+    const int cw = (static_cast<int>(blockIdx.x) + k) & (kWarps - 1);
+    if (warp == cw && lane < kSys) {
       const T d = Ms[tri(k) + k];
       if (!(d > T(0)) && sinfo[s] == 0) sinfo[s] = k + 1;
       const T l = sqrt_rn<T>(d);

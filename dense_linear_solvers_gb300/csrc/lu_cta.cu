@@ -6,7 +6,7 @@
 // looking factorization follows LAPACK's order with physical row interchanges (TDLS
 // API, "solver_static.hpp File Reference", Detailed Description: physical and logical
 // interchanges choose the same pivots and run the same operations):
-//   phase 1 (warp 0): pivot search over column k with integer magnitude keys and the
+//   phase 1 (one warp): pivot search over column k with integer magnitude keys and the
 //     lowest-row tie rule, interchange of rows k and p, the correctly rounded pivot
 //     reciprocal, the multipliers of column k;
 //   phase 2 (all warps): the rank-1 update of rows k+1.., columns k+1.. of [A | B]
@@ -14,8 +14,10 @@
 //     block's 128 lanes so that lanes stay busy however small the trailing block gets.
 // On this part a warp FP64 instruction is charged whatever its active lanes, so the
 // lane count that does useful FP64 work is what sets the speed; four warps per system
-// also give the SM enough warps to cover each system's serial pivot phase.
-// Back substitution runs by blocks of four rows: warp 0 solves the 4 x 4 diagonal block,
+// also give the SM enough warps to cover each system's serial pivot phase. The serial
+// warp rotates with the step and the block, so the serial work of the blocks on an SM is
+// spread over its four sub-partitions.
+// Back substitution runs by blocks of four rows: one warp solves the 4 x 4 diagonal block,
 // then all warps apply its four columns to every row above, each element taking the four
 // updates in decreasing column order -- the oracle's order, so the arithmetic is the
 // CPU oracle's, operation by operation.
@@ -75,7 +77,10 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   __syncthreads();
 
   for (int k = 0; k < n; ++k) {
-    if (warp == 0) {
+    // the serial part of step k runs on a warp that rotates with the step and the block:
+    // warp w runs on SM sub-partition w % 4, and a fixed warp would put every block's
+    // serial work on one sub-partition
+    if (warp == ((static_cast<int>(blockIdx.x) + k) & (kWarps - 1))) {
       // pivot search over rows k..n-1 of column k; a lane keeps its first maximum
       Key best = 0;
       int bi = 0x7FFFFFFF;
@@ -139,7 +144,7 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   const int nblk = nrhs > 0 ? (n + kBlk - 1) / kBlk : 0;
   for (int cb = nblk - 1; cb >= 0; --cb) {
     const int lo = cb * kBlk, hi = min(n, lo + kBlk);
-    if (warp == 0) {
+    if (warp == ((static_cast<int>(blockIdx.x) + cb) & (kWarps - 1))) {
       for (int i = hi - 1; i >= lo; --i) {
         const T r = rcp[i];
         for (int c = lane; c < nrhs; c += 32) M[i * P + n + c] = M[i * P + n + c] * r;
