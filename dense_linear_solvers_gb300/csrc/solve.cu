@@ -3,9 +3,9 @@
 // (GLASS API reference, "Block-tridiagonal Ops", bdsv_solve; TDLS API,
 // "solver_static.hpp File Reference", separate substitution).
 //
-// n <= 32: one system per group of G = NT lanes (32/NT systems per warp), lane t owns
-// position t: its right-hand-side row in registers, and in registers the factor entries
-// its row needs. For LU that is row t of L\U (the forward sweep reads l_tk, k < t, the
+// n <= 32: one system per group of G = NT / R lanes (32/G systems per warp), lane t owns
+// positions t + qG (q < R): their right-hand-side rows in registers, and in registers the
+// factor entries those rows need. For LU that is row t of L\U (the forward sweep reads l_tk, k < t, the
 // backward sweep u_tk, k > t). For Cholesky the forward sweep needs row t of L and the
 // backward sweep (with L^T) column t, so lane t holds the symmetric fill of the lower
 // triangle: v[j] = L[max(t,j)][min(t,j)] (row t left of the diagonal, column t right of
@@ -22,6 +22,7 @@
 // b_i -= m_ik x_k for i < k in decreasing k; r_k = 1/u_kk (1 for a pivot below the
 // smallest normal) for LU, 1/l_kk for Cholesky; every update one fused multiply-add.
 #include <cfloat>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -30,6 +31,12 @@ namespace bsolve {
 namespace {
 
 enum SolveKind : int { kSolveLu = 0, kSolveChol = 1 };
+
+// Positions per lane for the order tiers 8, 16 and 32. Two positions per lane halve the
+// shuffles per system and let a step skip, at compile time, a slot whose rows are all
+// past (FP32 n=16 getrs: 35.5 -> 31.4 us; FP64 n=32 potrs: 1.97 -> 1.33 ms; four per lane
+// gained nothing more).
+constexpr int kRows8 = 2, kRows16 = 2, kRows32 = 2;
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
@@ -55,113 +62,195 @@ __device__ __forceinline__ int64_t idx(int layout, int rows, int cols, int r, in
 }
 
 // ------------------------------------------------------------------ n <= 32, registers
-template <typename T, int NT, int RT, int KIND>
+// R positions per lane: lane t of a group of G = NT / R lanes owns positions t + q G.
+template <typename T, int N>
+__device__ __forceinline__ void ldg_row(const T* __restrict__ p, T (&r)[N]) {
+  if constexpr ((N * sizeof(T)) % 16 == 0) {
+#pragma unroll
+    for (int j = 0; j < N; j += 16 / sizeof(T)) {
+      if constexpr (std::is_integral<T>::value) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(p + j));
+        r[j] = v.x; r[j + 1] = v.y; r[j + 2] = v.z; r[j + 3] = v.w;
+      } else if constexpr (sizeof(T) == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p + j));
+        r[j] = v.x; r[j + 1] = v.y; r[j + 2] = v.z; r[j + 3] = v.w;
+      } else {
+        const double2 v = __ldg(reinterpret_cast<const double2*>(p + j));
+        r[j] = v.x; r[j + 1] = v.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) r[j] = __ldg(p + j);
+  }
+}
+
+template <typename T, int NT, int R, int RT, int KIND, bool FULL>
 __global__ void __launch_bounds__(kThreads)
-solve_reg_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restrict__ M,
+solve_reg_kernel(int n_, int nrhs_, int layout, int64_t batch, const T* __restrict__ M,
                  const int32_t* __restrict__ ipiv, T* __restrict__ B) {
-  constexpr int G = NT;
+  constexpr int G = NT / R;
   constexpr int GPW = 32 / G;
+  const int n = FULL ? NT : n_;
+  const int nrhs = FULL ? RT : nrhs_;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane / G;
   const int t = lane % G;
   const int64_t s = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * GPW + g;
   const bool valid = s < batch;
-  const bool row_ok = valid && t < n;
   const T* Ms = M + s * n * n;
   T* Bs = B + s * n * nrhs;
 
-  T v[NT];
-  T rt = T(1);
-  int src = t;   // the right-hand-side row that lands at position t
-  if (KIND == kSolveLu) {
-    // undo the swaps from the last; lane k of the group holds ipiv[k]
-    const int ip = row_ok ? __ldg(ipiv + s * n + t) - 1 : 0;
+  bool ok[R];
+  int src[R];   // the right-hand-side row that lands at position t + qG
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    ok[q] = valid && (FULL || t + q * G < n);
+    src[q] = t + q * G;
+  }
+  if (KIND == kSolveLu && valid) {
+    // the swaps undone from the last, on the group's copy of the swap sequence
+    int iv[NT];
+    if (FULL && (NT % 4) == 0) {
+      ldg_row<int, NT>(ipiv + s * n, iv);
+    } else {
+#pragma unroll
+      for (int k = 0; k < NT; ++k) iv[k] = k < n ? __ldg(ipiv + s * n + k) : k + 1;
+    }
 #pragma unroll
     for (int k = NT - 1; k >= 0; --k) {
-      int p = __shfl_sync(0xFFFFFFFFu, ip, k, G);
+      int p = iv[k] - 1;
       if (p < 0 || p >= n) p = k;   // an entry out of range swaps nothing
-      if (k < n) {
-        if (src == k) src = p;
-        else if (src == p) src = k;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        if (src[q] == k) src[q] = p;
+        else if (src[q] == p) src[q] = k;
       }
     }
   }
-  if (row_ok) {
+  T v[R][NT];
+  T rt[R];
+  T b[R][RT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      if (j < n) {
-        const int r = (KIND == kSolveLu || j <= t) ? t : j;
-        const int c = (KIND == kSolveLu || j <= t) ? j : t;
-        v[j] = __ldg(Ms + idx(layout, n, n, r, c));
+  for (int q = 0; q < R; ++q) {
+    const int pq = t + q * G;
+    rt[q] = T(1);
+    if (ok[q]) {
+      if (KIND == kSolveLu && FULL && layout == kRowMajor) {
+        ldg_row<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
       } else {
-        v[j] = T(0);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if (FULL || j < n) {
+            const int r = (KIND == kSolveLu || j <= pq) ? pq : j;
+            const int c = (KIND == kSolveLu || j <= pq) ? j : pq;
+            v[q][j] = __ldg(Ms + idx(layout, n, n, r, c));
+          } else {
+            v[q][j] = T(0);
+          }
+        }
       }
+      rt[q] = diag_rcp<T, KIND>(__ldg(Ms + idx(layout, n, n, pq, pq)));
+      if (FULL && layout == kRowMajor) {
+        ldg_row<T, RT>(Bs + static_cast<int64_t>(src[q]) * RT, b[q]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[q][c] = (c < nrhs) ? Bs[idx(layout, n, nrhs, src[q], c)] : T(0);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) v[q][j] = T(0);
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[q][c] = T(0);
     }
-    rt = diag_rcp<T, KIND>(__ldg(Ms + idx(layout, n, n, t, t)));
-  } else {
-#pragma unroll
-    for (int j = 0; j < NT; ++j) v[j] = T(0);
   }
-  T b[RT];
-#pragma unroll
-  for (int c = 0; c < RT; ++c) b[c] = (row_ok && c < nrhs) ? Bs[idx(layout, n, nrhs, src, c)] : T(0);
 
-  // forward: L y = P b (unit L) or L y = b
+  // forward: L y = P b (unit L) or L y = b. Slot q holds positions qG..qG+G-1: it has
+  // rows below k unless qG + G - 1 <= k (known at compile time).
 #pragma unroll
   for (int k = 0; k < NT; ++k) {
-    if (k >= n) break;
-    if (KIND == kSolveChol && t == k) {
+    if (!FULL && k >= n) break;
+    const int kq = k / G, kl = k % G;
+    if (KIND == kSolveChol && t == kl) {
 #pragma unroll
-      for (int c = 0; c < RT; ++c) b[c] = b[c] * rt;
+      for (int c = 0; c < RT; ++c) b[kq][c] = b[kq][c] * rt[kq];
     }
     T y[RT];
 #pragma unroll
-    for (int c = 0; c < RT; ++c) y[c] = __shfl_sync(0xFFFFFFFFu, b[c], k, G);
-    if (row_ok && t > k) {
+    for (int c = 0; c < RT; ++c) y[c] = __shfl_sync(0xFFFFFFFFu, b[kq][c], kl, G);
 #pragma unroll
-      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-v[k], y[c], b[c]);
+    for (int q = 0; q < R; ++q) {
+      if (q * G + G - 1 <= k) continue;
+      if (ok[q] && t + q * G > k) {
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-v[q][k], y[c], b[q][c]);
+      }
     }
   }
-  // backward: U x = y or L^T x = y
+  // backward: U x = y or L^T x = y. Slot q has rows above k unless qG >= k.
 #pragma unroll
   for (int k = NT - 1; k >= 0; --k) {
-    if (k >= n) continue;
-    if (t == k) {
+    if (!FULL && k >= n) continue;
+    const int kq = k / G, kl = k % G;
+    if (t == kl) {
 #pragma unroll
-      for (int c = 0; c < RT; ++c) b[c] = b[c] * rt;
+      for (int c = 0; c < RT; ++c) b[kq][c] = b[kq][c] * rt[kq];
     }
     T x[RT];
 #pragma unroll
-    for (int c = 0; c < RT; ++c) x[c] = __shfl_sync(0xFFFFFFFFu, b[c], k, G);
-    if (row_ok && t < k) {
+    for (int c = 0; c < RT; ++c) x[c] = __shfl_sync(0xFFFFFFFFu, b[kq][c], kl, G);
 #pragma unroll
-      for (int c = 0; c < RT; ++c) b[c] = fma_rn<T>(-v[k], x[c], b[c]);
+    for (int q = 0; q < R; ++q) {
+      if (q * G >= k) continue;
+      if (ok[q] && t + q * G < k) {
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-v[q][k], x[c], b[q][c]);
+      }
     }
   }
-  if (row_ok) {
 #pragma unroll
-    for (int c = 0; c < RT; ++c)
-      if (c < nrhs) Bs[idx(layout, n, nrhs, t, c)] = b[c];
+  for (int q = 0; q < R; ++q) {
+    if (!ok[q]) continue;
+    const int pq = t + q * G;
+    if (FULL && layout == kRowMajor && (RT * sizeof(T)) % 16 == 0) {
+      T* dst = Bs + static_cast<int64_t>(pq) * RT;
+#pragma unroll
+      for (int c = 0; c < RT; c += 16 / sizeof(T)) {
+        if constexpr (sizeof(T) == 4)
+          *reinterpret_cast<float4*>(dst + c) = make_float4(b[q][c], b[q][c + 1], b[q][c + 2], b[q][c + 3]);
+        else
+          *reinterpret_cast<double2*>(dst + c) = make_double2(b[q][c], b[q][c + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < RT; ++c)
+        if (c < nrhs) Bs[idx(layout, n, nrhs, pq, c)] = b[q][c];
+    }
   }
 }
 
-template <typename T, int NT, int KIND>
-cudaError_t launch_reg_rhs(int layout, int n, int nrhs, int64_t batch, const T* M,
-                           const int32_t* ipiv, T* B, cudaStream_t stream) {
-  constexpr int per_block = kWarps * (32 / NT);
+template <typename T, int NT, int R, int RT, int KIND>
+cudaError_t launch_reg_tier(int layout, int n, int nrhs, int64_t batch, const T* M,
+                            const int32_t* ipiv, T* B, cudaStream_t stream) {
+  constexpr int per_block = kWarps * (32 / (NT / R));
   const int64_t blocks = (batch + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const unsigned nb = static_cast<unsigned>(blocks);
-  if (nrhs <= 1)
-    solve_reg_kernel<T, NT, 1, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
-  else if (nrhs <= 2)
-    solve_reg_kernel<T, NT, 2, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
-  else if (nrhs <= 4)
-    solve_reg_kernel<T, NT, 4, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+  if (n == NT && nrhs == RT)
+    solve_reg_kernel<T, NT, R, RT, KIND, true><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
   else
-    solve_reg_kernel<T, NT, 8, KIND><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+    solve_reg_kernel<T, NT, R, RT, KIND, false><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
   return cudaGetLastError();
+}
+
+template <typename T, int NT, int R, int KIND>
+cudaError_t launch_reg_rhs(int layout, int n, int nrhs, int64_t batch, const T* M,
+                           const int32_t* ipiv, T* B, cudaStream_t stream) {
+  if (nrhs <= 1) return launch_reg_tier<T, NT, R, 1, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (nrhs <= 2) return launch_reg_tier<T, NT, R, 2, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (nrhs <= 4) return launch_reg_tier<T, NT, R, 4, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  return launch_reg_tier<T, NT, R, 8, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
 }
 
 // ------------------------------------------------- 32 < n <= 64, shared memory, a warp
@@ -308,10 +397,10 @@ cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
 template <typename T, int KIND>
 cudaError_t launch_kind(int layout, int n, int nrhs, int64_t batch, const T* M,
                         const int32_t* ipiv, T* B, cudaStream_t stream) {
-  if (n <= 4) return launch_reg_rhs<T, 4, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 8) return launch_reg_rhs<T, 8, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 16) return launch_reg_rhs<T, 16, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 32) return launch_reg_rhs<T, 32, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 4) return launch_reg_rhs<T, 4, 1, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 8) return launch_reg_rhs<T, 8, kRows8, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 16) return launch_reg_rhs<T, 16, kRows16, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+  if (n <= 32) return launch_reg_rhs<T, 32, kRows32, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
   if (n <= 64) return launch_smem<T, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
   return cudaErrorInvalidValue;
 }
