@@ -4,13 +4,14 @@
 // "solver_static.hpp File Reference", separate substitution).
 //
 // n <= 32: one system per group of G = NT / R lanes (32/G systems per warp), lane t owns
-// positions t + qG (q < R): their right-hand-side rows in registers, and in registers the
-// factor entries those rows need. For LU that is row t of L\U (the forward sweep reads l_tk, k < t, the
-// backward sweep u_tk, k > t). For Cholesky the forward sweep needs row t of L and the
-// backward sweep (with L^T) column t, so lane t holds the symmetric fill of the lower
-// triangle: v[j] = L[max(t,j)][min(t,j)] (row t left of the diagonal, column t right of
-// it). Each step k then broadcasts one value per right-hand side from lane k by a
-// shuffle, and every lane applies it from registers: no shared memory, no barrier.
+// positions p = t + qG (q < R): their right-hand-side rows in registers, and in registers
+// the factor entries those rows need. For LU that is row p of L\U (the forward sweep
+// reads l_pk, k < p, the backward sweep u_pk, k > p). For Cholesky the forward sweep
+// needs row p of L and the backward sweep (with L^T) column p, so the lane holds the
+// symmetric fill of the lower triangle: v[j] = L[max(p,j)][min(p,j)] (row p left of the
+// diagonal, column p right of it). Each step k broadcasts one value per right-hand side
+// from the owner of position k by a shuffle, and every lane applies it from registers:
+// no shared memory, no barrier.
 // 32 < n <= 64: one warp per system, the factor in shared memory with an odd pitch, lane
 // t owning positions t and t+32.
 //
