@@ -26,6 +26,8 @@ _default = None
 
 ROW_MAJOR = 0
 COL_MAJOR = 1
+LOWER = 0
+UPPER = 1
 
 
 def compile_library(src: str, out: str) -> str:
@@ -57,7 +59,7 @@ class Oracle:
             getattr(lib, name).argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, vp, i32]
             getattr(lib, name).restype = i32
         for name in ("oracle_potrf_potrs_f32", "oracle_potrf_potrs_f64"):
-            getattr(lib, name).argtypes = [i32, i32, i32, i64, vp, vp, vp, i32]
+            getattr(lib, name).argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, i32]
             getattr(lib, name).restype = i32
         for name in ("oracle_bdsv_f32", "oracle_bdsv_f64"):
             getattr(lib, name).argtypes = [i32, i32, i64, vp, vp, vp, i32]
@@ -65,8 +67,8 @@ class Oracle:
         sig = {
             "getrf": [i32, i32, i64, vp, vp, vp, vp, i32],
             "getrs": [i32, i32, i32, i64, vp, vp, vp, i32],
-            "potrf": [i32, i32, i64, vp, vp, i32],
-            "potrs": [i32, i32, i32, i64, vp, vp, i32],
+            "potrf": [i32, i32, i32, i64, vp, vp, i32],
+            "potrs": [i32, i32, i32, i32, i64, vp, vp, i32],
             "bdsv_factor": [i32, i32, i64, vp, vp, i32],
             "bdsv_solve": [i32, i32, i64, vp, vp, i32],
             "bdmv": [i32, i32, i64, vp, vp, vp, i32],
@@ -98,15 +100,16 @@ class Oracle:
             raise ValueError("oracle getrf_getrs rejected its arguments")
         return A, B, ipiv, info, tie
 
-    def potrf_potrs(self, A, B, layout: int = COL_MAJOR, nthreads: int = 1):
-        """Cholesky (lower fill) + solve, one system at a time. Returns (L, X, info)."""
+    def potrf_potrs(self, A, B, layout: int = COL_MAJOR, nthreads: int = 1, fill: int = LOWER):
+        """Cholesky + solve, one system at a time (fill LOWER: A = L L^T in the lower
+        triangle; UPPER: A = U^T U in the upper one). Returns (factor, X, info)."""
         A = np.ascontiguousarray(A).copy()
         B = np.ascontiguousarray(B, dtype=A.dtype).copy()
         batch, n = A.shape[0], A.shape[1]
         nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
         info = np.zeros(batch, np.int32)
         fn = getattr(self.lib, "oracle_potrf_potrs_" + _suffix(A.dtype))
-        rc = fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(info), nthreads)
+        rc = fn(layout, fill, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(info), nthreads)
         if rc != 0:
             raise ValueError("oracle potrf_potrs rejected its arguments")
         return A, B, info
@@ -152,24 +155,24 @@ class Oracle:
             raise ValueError("oracle getrs rejected its arguments")
         return B
 
-    def potrf(self, A, layout: int = COL_MAJOR, nthreads: int = 1):
-        """Cholesky (lower fill) only. Returns (L, info)."""
+    def potrf(self, A, layout: int = COL_MAJOR, nthreads: int = 1, fill: int = LOWER):
+        """Cholesky only (fill as potrf_potrs). Returns (factor, info)."""
         A = np.ascontiguousarray(A).copy()
         batch, n = A.shape[0], A.shape[1]
         info = np.zeros(batch, np.int32)
         fn = getattr(self.lib, "oracle_potrf_" + _suffix(A.dtype))
-        if fn(layout, n, batch, _ptr(A), _ptr(info), nthreads) != 0:
+        if fn(layout, fill, n, batch, _ptr(A), _ptr(info), nthreads) != 0:
             raise ValueError("oracle potrf rejected its arguments")
         return A, info
 
-    def potrs(self, L, B, layout: int = COL_MAJOR, nthreads: int = 1):
-        """Solve with a stored lower Cholesky factor. Returns X."""
+    def potrs(self, L, B, layout: int = COL_MAJOR, nthreads: int = 1, fill: int = LOWER):
+        """Solve with a stored Cholesky factor (fill as potrf_potrs). Returns X."""
         L = np.ascontiguousarray(L)
         B = np.ascontiguousarray(B, dtype=L.dtype).copy()
         batch, n = L.shape[0], L.shape[1]
         nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
         fn = getattr(self.lib, "oracle_potrs_" + _suffix(L.dtype))
-        if fn(layout, n, nrhs, batch, _ptr(L), _ptr(B), nthreads) != 0:
+        if fn(layout, fill, n, nrhs, batch, _ptr(L), _ptr(B), nthreads) != 0:
             raise ValueError("oracle potrs rejected its arguments")
         return B
 
@@ -219,8 +222,8 @@ def getrf_getrs(A, B, layout: int = ROW_MAJOR, nthreads: int = 1):
     return default().getrf_getrs(A, B, layout, nthreads)
 
 
-def potrf_potrs(A, B, layout: int = COL_MAJOR, nthreads: int = 1):
-    return default().potrf_potrs(A, B, layout, nthreads)
+def potrf_potrs(A, B, layout: int = COL_MAJOR, nthreads: int = 1, fill: int = LOWER):
+    return default().potrf_potrs(A, B, layout, nthreads, fill)
 
 
 def bdsv(strips, xpad, nthreads: int = 1):
@@ -235,12 +238,12 @@ def getrs(LU, ipiv, B, layout: int = ROW_MAJOR, nthreads: int = 1):
     return default().getrs(LU, ipiv, B, layout, nthreads)
 
 
-def potrf(A, layout: int = COL_MAJOR, nthreads: int = 1):
-    return default().potrf(A, layout, nthreads)
+def potrf(A, layout: int = COL_MAJOR, nthreads: int = 1, fill: int = LOWER):
+    return default().potrf(A, layout, nthreads, fill)
 
 
-def potrs(L, B, layout: int = COL_MAJOR, nthreads: int = 1):
-    return default().potrs(L, B, layout, nthreads)
+def potrs(L, B, layout: int = COL_MAJOR, nthreads: int = 1, fill: int = LOWER):
+    return default().potrs(L, B, layout, nthreads, fill)
 
 
 def bdsv_factor(strips, nthreads: int = 1):

@@ -190,12 +190,17 @@ void getrs_one(int layout, int n, int nrhs, const T* LU, const int32_t* ipiv, T*
 // potrs: L y = b (column by column, y_k = b_k * (1/l_kk), b_i -= l_ik y_k for i > k),
 // then L^T x = y (from the last: x_k = y_k * (1/l_kk), y_i -= l_ki x_k for i < k).
 // A failed system returns X = 0.
+// Upper fill ([cuSolverDx]: A = U^T U, only the upper triangle processed and replaced by
+// U, the lower part untouched): U is L^T for the lower factor of the mirrored matrix, and
+// the upper algorithm's operations are the lower algorithm's on mirrored entries. A in
+// layout X with upper fill is therefore read as the lower fill of A in the other layout
+// (a_layout = 1 - X), while B keeps its own layout.
 // ---------------------------------------------------------------------------------
 template <typename T>
-void potrf_potrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* info) {
+void potrf_potrs_one(int a_layout, int b_layout, int n, int nrhs, T* A, T* B, int32_t* info) {
   int32_t inf = 0;
-  auto a = [&](int r, int c) -> T& { return A[at(layout, n, n, r, c)]; };
-  auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
+  auto a = [&](int r, int c) -> T& { return A[at(a_layout, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(b_layout, n, nrhs, r, c)]; };
   for (int k = 0; k < n; ++k) {
     const T d = a(k, k);
     if (!(d > T(0))) {
@@ -236,9 +241,9 @@ void potrf_potrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* info) {
 // solve half of potrf_potrs_one, with the same operation order. No info: a failed factor
 // gives an unspecified X.
 template <typename T>
-void potrs_one(int layout, int n, int nrhs, const T* L, T* B) {
-  auto a = [&](int r, int c) -> T { return L[at(layout, n, n, r, c)]; };
-  auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
+void potrs_one(int a_layout, int b_layout, int n, int nrhs, const T* L, T* B) {
+  auto a = [&](int r, int c) -> T { return L[at(a_layout, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(b_layout, n, nrhs, r, c)]; };
   for (int c = 0; c < nrhs; ++c) {
     for (int k = 0; k < n; ++k) {
       const T y = b(k, c) * (T(1) / a(k, k));
@@ -429,11 +434,13 @@ int getrf_getrs_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B, 
 }
 
 template <typename T>
-int potrf_potrs_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B, int32_t* info,
-                        int nthreads) {
-  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0) return 1;
+int potrf_potrs_batched(int layout, int fill, int n, int nrhs, int64_t batch, T* A, T* B,
+                        int32_t* info, int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 || batch < 0)
+    return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
   for_systems(batch, nthreads, [&](int64_t s) {
-    potrf_potrs_one<T>(layout, n, nrhs, A + s * n * n, B + s * n * nrhs, info + s);
+    potrf_potrs_one<T>(a_layout, layout, n, nrhs, A + s * n * n, B + s * n * nrhs, info + s);
   });
   return 0;
 }
@@ -470,19 +477,23 @@ int getrs_batched(int layout, int n, int nrhs, int64_t batch, const T* LU, const
 }
 
 template <typename T>
-int potrf_batched(int layout, int n, int64_t batch, T* A, int32_t* info, int nthreads) {
-  if ((layout != 0 && layout != 1) || n < 1 || batch < 0) return 1;
+int potrf_batched(int layout, int fill, int n, int64_t batch, T* A, int32_t* info, int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || batch < 0) return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
   for_systems(batch, nthreads, [&](int64_t s) {
-    potrf_potrs_one<T>(layout, n, 0, A + s * n * n, nullptr, info + s);
+    potrf_potrs_one<T>(a_layout, layout, n, 0, A + s * n * n, nullptr, info + s);
   });
   return 0;
 }
 
 template <typename T>
-int potrs_batched(int layout, int n, int nrhs, int64_t batch, const T* L, T* B, int nthreads) {
-  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0) return 1;
+int potrs_batched(int layout, int fill, int n, int nrhs, int64_t batch, const T* L, T* B,
+                  int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 || batch < 0)
+    return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
   for_systems(batch, nthreads, [&](int64_t s) {
-    potrs_one<T>(layout, n, nrhs, L + s * n * n, B + s * n * nrhs);
+    potrs_one<T>(a_layout, layout, n, nrhs, L + s * n * n, B + s * n * nrhs);
   });
   return 0;
 }
@@ -530,13 +541,13 @@ int oracle_getrf_getrs_f64(int layout, int n, int nrhs, int64_t batch, double* A
                            int32_t* ipiv, int32_t* info, int32_t* tie_step, int nthreads) {
   return getrf_getrs_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, nthreads);
 }
-int oracle_potrf_potrs_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
+int oracle_potrf_potrs_f32(int layout, int fill, int n, int nrhs, int64_t batch, float* A, float* B,
                            int32_t* info, int nthreads) {
-  return potrf_potrs_batched<float>(layout, n, nrhs, batch, A, B, info, nthreads);
+  return potrf_potrs_batched<float>(layout, fill, n, nrhs, batch, A, B, info, nthreads);
 }
-int oracle_potrf_potrs_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
+int oracle_potrf_potrs_f64(int layout, int fill, int n, int nrhs, int64_t batch, double* A, double* B,
                            int32_t* info, int nthreads) {
-  return potrf_potrs_batched<double>(layout, n, nrhs, batch, A, B, info, nthreads);
+  return potrf_potrs_batched<double>(layout, fill, n, nrhs, batch, A, B, info, nthreads);
 }
 int oracle_bdsv_f32(int nbr, int bs, int64_t batch, float* strips, float* xpad, int32_t* info,
                     int nthreads) {
@@ -555,12 +566,13 @@ int oracle_getrs_f32(int layout, int n, int nrhs, int64_t batch, const float* LU
                      const int32_t* ipiv, float* B, int nthreads) {
   return getrs_batched<float>(layout, n, nrhs, batch, LU, ipiv, B, nthreads);
 }
-int oracle_potrf_f32(int layout, int n, int64_t batch, float* A, int32_t* info, int nthreads) {
-  return potrf_batched<float>(layout, n, batch, A, info, nthreads);
-}
-int oracle_potrs_f32(int layout, int n, int nrhs, int64_t batch, const float* L, float* B,
+int oracle_potrf_f32(int layout, int fill, int n, int64_t batch, float* A, int32_t* info,
                      int nthreads) {
-  return potrs_batched<float>(layout, n, nrhs, batch, L, B, nthreads);
+  return potrf_batched<float>(layout, fill, n, batch, A, info, nthreads);
+}
+int oracle_potrs_f32(int layout, int fill, int n, int nrhs, int64_t batch, const float* L, float* B,
+                     int nthreads) {
+  return potrs_batched<float>(layout, fill, n, nrhs, batch, L, B, nthreads);
 }
 int oracle_bdsv_factor_f32(int nbr, int bs, int64_t batch, float* strips, int32_t* info,
                            int nthreads) {
@@ -582,12 +594,13 @@ int oracle_getrs_f64(int layout, int n, int nrhs, int64_t batch, const double* L
                      const int32_t* ipiv, double* B, int nthreads) {
   return getrs_batched<double>(layout, n, nrhs, batch, LU, ipiv, B, nthreads);
 }
-int oracle_potrf_f64(int layout, int n, int64_t batch, double* A, int32_t* info, int nthreads) {
-  return potrf_batched<double>(layout, n, batch, A, info, nthreads);
-}
-int oracle_potrs_f64(int layout, int n, int nrhs, int64_t batch, const double* L, double* B,
+int oracle_potrf_f64(int layout, int fill, int n, int64_t batch, double* A, int32_t* info,
                      int nthreads) {
-  return potrs_batched<double>(layout, n, nrhs, batch, L, B, nthreads);
+  return potrf_batched<double>(layout, fill, n, batch, A, info, nthreads);
+}
+int oracle_potrs_f64(int layout, int fill, int n, int nrhs, int64_t batch, const double* L, double* B,
+                     int nthreads) {
+  return potrs_batched<double>(layout, fill, n, nrhs, batch, L, B, nthreads);
 }
 int oracle_bdsv_factor_f64(int nbr, int bs, int64_t batch, double* strips, int32_t* info,
                            int nthreads) {

@@ -344,6 +344,51 @@ def pin_chol_info_contract(orc):
         assert _chol(orc, A[None], np.ones((1, 3, 1), dt))[2][0] == 3
 
 
+def pin_chol_upper_fill(orc):
+    """Upper fill (cuSolverDx POTRF: A = U^T U, only the upper triangle processed and
+    replaced by U, the lower part untouched): the 2x2 closed form u11 = sqrt(a11),
+    u12 = a12/u11, u22 = sqrt(a22 - u12^2); U^T U = A to rounding; U equals the
+    transpose of the lower factor of the same matrix (the Cholesky factor is unique);
+    NaN in the lower triangle is never read; a planted indefinite minor gives the same
+    info as lower fill; the solve meets the backward-error bound."""
+    A2 = np.array([[[4.0, 2.0], [np.nan, 5.0]]])          # upper fill, row-major
+    U, X, info = orc.potrf_potrs(A2, np.array([[[8.0], [9.0]]]), ROW_MAJOR, fill=1)
+    assert info[0] == 0 and U[0, 0, 0] == 2.0 and U[0, 0, 1] == 1.0 and U[0, 1, 1] == 2.0
+    assert np.isnan(U[0, 1, 0])
+    assert np.allclose(X[0, :, 0], [1.375, 1.25], rtol=0, atol=1e-15)
+    rng = _rng(28)
+    for dt in (np.float64, np.float32):
+        eps = eps_of(dt)
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            for n in (1, 5, 17, 40):
+                G = rng.standard_normal((4, n, n))
+                Al = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dt)
+                if n > 2:
+                    Al[2, n // 2, n // 2] = -1.0
+                B = rng.standard_normal((4, n, 2)).astype(dt)
+                Au = Al.copy()
+                Al_ = Al.copy()
+                il, iu = np.tril_indices(n, -1), np.triu_indices(n, 1)
+                Au[:, il[0], il[1]] = np.nan
+                Al_[:, iu[0], iu[1]] = np.nan
+                Uu, Xu, infu = orc.potrf_potrs(to_storage(Au, layout), to_storage(B, layout), layout, fill=1)
+                Ll, Xl, infl = orc.potrf_potrs(to_storage(Al_, layout), to_storage(B, layout), layout, fill=0)
+                Uu, Ll = from_storage(Uu, layout), from_storage(Ll, layout)
+                Xu, Xl = from_storage(Xu, layout), from_storage(Xl, layout)
+                assert np.array_equal(infu, infl)
+                assert np.all(np.isnan(Uu[:, il[0], il[1]]))
+                ok = infu == 0
+                assert np.array_equal(np.triu(np.nan_to_num(Uu[ok])),
+                                      np.swapaxes(np.tril(np.nan_to_num(Ll[ok])), 1, 2))
+                assert np.array_equal(Xu[ok], Xl[ok])
+                Ut = np.triu(np.nan_to_num(Uu[ok])).astype(np.float64)
+                Asym = np.triu(Al[ok]) + np.swapaxes(np.triu(Al[ok], 1), 1, 2)
+                rec = np.swapaxes(Ut, 1, 2) @ Ut
+                assert np.allclose(rec, Asym, rtol=0, atol=16 * n * eps * np.abs(Asym).max())
+                be = backward_error(Asym, Xu[ok], B[ok])
+                assert np.all(be <= 8 * n * eps)
+
+
 # --------------------------------------------------------------------------- bdsv pins
 def _random_bdsv(rng, batch, nbr, bs, dt=np.float64):
     strips = np.zeros((batch, nbr, bs, 3 * bs), dt)
@@ -622,7 +667,7 @@ LU_PINS = [pin_lu_3x3_hand_worked, pin_lu_2x2_closed_form, pin_lu_cramer_brutefo
            pin_lu_reconstruction, pin_lu_matches_lapack, pin_lu_info_contract,
            pin_lu_layout_invariance, pin_lu_near_tie_flag]
 CHOL_PINS = [pin_chol_hand_worked, pin_chol_2x2_closed_form,
-             pin_chol_reconstruction_and_lapack, pin_chol_info_contract]
+             pin_chol_reconstruction_and_lapack, pin_chol_info_contract, pin_chol_upper_fill]
 BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,
              pin_bdsv_scalar_tridiagonal, pin_bdsv_info]
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,

@@ -82,11 +82,17 @@ MUTATIONS = [
      "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n}",
      "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n}"),
     ("potrs_forward_unscaled",
-     "B[at(layout, n, nrhs, r, c)]; };\n  for (int c = 0; c < nrhs; ++c) {\n    for (int k = 0; k < n; ++k) {\n      const T y = b(k, c) * (T(1) / a(k, k));",
-     "B[at(layout, n, nrhs, r, c)]; };\n  for (int c = 0; c < nrhs; ++c) {\n    for (int k = 0; k < n; ++k) {\n      const T y = b(k, c);"),
+     "B[at(b_layout, n, nrhs, r, c)]; };\n  for (int c = 0; c < nrhs; ++c) {\n    for (int k = 0; k < n; ++k) {\n      const T y = b(k, c) * (T(1) / a(k, k));",
+     "B[at(b_layout, n, nrhs, r, c)]; };\n  for (int c = 0; c < nrhs; ++c) {\n    for (int k = 0; k < n; ++k) {\n      const T y = b(k, c);"),
     ("potrs_back_solve_not_transposed",
      "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n}",
      "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n}"),
+    ("chol_upper_fill_reads_lower",
+     "  const int a_layout = fill == 0 ? layout : 1 - layout;\n  for_systems(batch, nthreads, [&](int64_t s) {\n    potrf_potrs_one<T>(a_layout, layout, n, nrhs,",
+     "  const int a_layout = layout;\n  for_systems(batch, nthreads, [&](int64_t s) {\n    potrf_potrs_one<T>(a_layout, layout, n, nrhs,"),
+    ("chol_upper_fill_b_transposed",
+     "    potrf_potrs_one<T>(a_layout, layout, n, nrhs,",
+     "    potrf_potrs_one<T>(a_layout, a_layout, n, nrhs,"),
     ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
      "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
     ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
