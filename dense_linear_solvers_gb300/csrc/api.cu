@@ -12,7 +12,8 @@ thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxLuN = 64;
 constexpr int kMaxRegN = 32;
-constexpr int kMaxNrhs = 8;
+constexpr int kMaxNrhs = 8;          // right-hand sides a fused kernel holds
+constexpr int kMaxNrhsAny = 65536;   // beyond kMaxNrhs: factor, then a chunked solve
 constexpr int kMaxBdsvBs = 8;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -32,13 +33,22 @@ bs_status from_cuda(cudaError_t e) {
 bool lu_supported(bs_dtype dtype, bs_layout layout, int n, int nrhs) {
   return (dtype == BS_FP32 || dtype == BS_FP64) &&
          (layout == BS_ROW_MAJOR || layout == BS_COL_MAJOR) && n >= 1 && n <= kMaxLuN &&
-         nrhs >= 1 && nrhs <= kMaxNrhs;
+         nrhs >= 1 && nrhs <= kMaxNrhsAny;
 }
 
 bool chol_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs) {
   return (dtype == BS_FP32 || dtype == BS_FP64) &&
-         (layout == BS_ROW_MAJOR || layout == BS_COL_MAJOR) && fill == BS_LOWER && n >= 1 &&
-         n <= kMaxLuN && nrhs >= 1 && nrhs <= kMaxNrhs;
+         (layout == BS_ROW_MAJOR || layout == BS_COL_MAJOR) &&
+         (fill == BS_LOWER || fill == BS_UPPER) && n >= 1 &&
+         n <= kMaxLuN && nrhs >= 1 && nrhs <= kMaxNrhsAny;
+}
+
+// Packed storage-order code of the Cholesky kernels: bit 0 for A (or the factor), bit 1 for
+// B. Upper fill in one order is the lower fill of the mirrored matrix, i.e. A read in the
+// other order (cuSolverDx docs, "Cholesky Factorization": A = U^T U with U = L^T).
+int chol_layouts(bs_layout layout, bs_fill fill) {
+  const int a = fill == BS_LOWER ? static_cast<int>(layout) : 1 - static_cast<int>(layout);
+  return a | (static_cast<int>(layout) << 1);
 }
 
 bool bdsv_supported(bs_dtype dtype, int nbr, int bs) {
@@ -60,7 +70,19 @@ bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nr
     return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (n <= kMaxRegN) {
+  if (nrhs > kMaxNrhs) {
+    // more right-hand sides than a fused kernel holds: the factor, then the solve (which
+    // zeroes X where info != 0); the same operations in the same order as the fused sweep
+    const bs_status st = bs_getrf_batched(dtype, layout, n, batch, A, ipiv, info, stream);
+    if (st != BS_OK) return st;
+    e = dtype == BS_FP32
+            ? bsolve::launch_getrs<float>(layout | (layout << 1), n, nrhs, batch,
+                                          static_cast<const float*>(A), ipiv,
+                                          static_cast<float*>(B), info, s)
+            : bsolve::launch_getrs<double>(layout | (layout << 1), n, nrhs, batch,
+                                           static_cast<const double*>(A), ipiv,
+                                           static_cast<double*>(B), info, s);
+  } else if (n <= kMaxRegN) {
     e = dtype == BS_FP32
             ? bsolve::launch_lu_reg<float>(layout, n, nrhs, batch, static_cast<float*>(A),
                                            static_cast<float*>(B), ipiv, info, s)
@@ -86,18 +108,33 @@ bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill,
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (n <= kMaxRegN) {
+  if (nrhs > kMaxNrhs) {
+    // the factor, then the solve that zeroes X where info != 0 (see the LU call)
+    const bs_status st = bs_potrf_batched(dtype, layout, fill, n, batch, A, info, stream);
+    if (st != BS_OK) return st;
     e = dtype == BS_FP32
-            ? bsolve::launch_chol_sys<float>(layout, n, nrhs, batch, static_cast<float*>(A),
-                                             static_cast<float*>(B), info, s)
-            : bsolve::launch_chol_sys<double>(layout, n, nrhs, batch, static_cast<double*>(A),
-                                              static_cast<double*>(B), info, s);
+            ? bsolve::launch_potrs<float>(chol_layouts(layout, fill), n, nrhs, batch,
+                                          static_cast<const float*>(A), static_cast<float*>(B),
+                                          info, s)
+            : bsolve::launch_potrs<double>(chol_layouts(layout, fill), n, nrhs, batch,
+                                           static_cast<const double*>(A),
+                                           static_cast<double*>(B), info, s);
+  } else if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_sys<float>(chol_layouts(layout, fill), n, nrhs, batch,
+                                             static_cast<float*>(A), static_cast<float*>(B),
+                                             info, s)
+            : bsolve::launch_chol_sys<double>(chol_layouts(layout, fill), n, nrhs, batch,
+                                              static_cast<double*>(A), static_cast<double*>(B),
+                                              info, s);
   } else {
     e = dtype == BS_FP32
-            ? bsolve::launch_chol_smem<float>(layout, n, nrhs, batch, static_cast<float*>(A),
-                                              static_cast<float*>(B), info, s)
-            : bsolve::launch_chol_smem<double>(layout, n, nrhs, batch, static_cast<double*>(A),
-                                               static_cast<double*>(B), info, s);
+            ? bsolve::launch_chol_smem<float>(chol_layouts(layout, fill), n, nrhs, batch,
+                                              static_cast<float*>(A), static_cast<float*>(B),
+                                              info, s)
+            : bsolve::launch_chol_smem<double>(chol_layouts(layout, fill), n, nrhs, batch,
+                                               static_cast<double*>(A), static_cast<double*>(B),
+                                               info, s);
   }
   return from_cuda(e);
 }
@@ -161,10 +198,12 @@ bs_status bs_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == BS_FP32
-          ? bsolve::launch_getrs<float>(layout, n, nrhs, batch, static_cast<const float*>(LU),
-                                        ipiv, static_cast<float*>(B), s)
-          : bsolve::launch_getrs<double>(layout, n, nrhs, batch, static_cast<const double*>(LU),
-                                         ipiv, static_cast<double*>(B), s);
+          ? bsolve::launch_getrs<float>(layout | (layout << 1), n, nrhs, batch,
+                                        static_cast<const float*>(LU), ipiv,
+                                        static_cast<float*>(B), nullptr, s)
+          : bsolve::launch_getrs<double>(layout | (layout << 1), n, nrhs, batch,
+                                         static_cast<const double*>(LU), ipiv,
+                                         static_cast<double*>(B), nullptr, s);
   return from_cuda(e);
 }
 
@@ -179,16 +218,16 @@ bs_status bs_potrf_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n
   cudaError_t e;
   if (n <= kMaxRegN) {
     e = dtype == BS_FP32
-            ? bsolve::launch_chol_sys<float>(layout, n, 0, batch, static_cast<float*>(A), nullptr,
-                                             info, s)
-            : bsolve::launch_chol_sys<double>(layout, n, 0, batch, static_cast<double*>(A),
-                                              nullptr, info, s);
+            ? bsolve::launch_chol_sys<float>(chol_layouts(layout, fill), n, 0, batch,
+                                             static_cast<float*>(A), nullptr, info, s)
+            : bsolve::launch_chol_sys<double>(chol_layouts(layout, fill), n, 0, batch,
+                                              static_cast<double*>(A), nullptr, info, s);
   } else {
     e = dtype == BS_FP32
-            ? bsolve::launch_chol_smem<float>(layout, n, 0, batch, static_cast<float*>(A),
-                                              nullptr, info, s)
-            : bsolve::launch_chol_smem<double>(layout, n, 0, batch, static_cast<double*>(A),
-                                               nullptr, info, s);
+            ? bsolve::launch_chol_smem<float>(chol_layouts(layout, fill), n, 0, batch,
+                                              static_cast<float*>(A), nullptr, info, s)
+            : bsolve::launch_chol_smem<double>(chol_layouts(layout, fill), n, 0, batch,
+                                               static_cast<double*>(A), nullptr, info, s);
   }
   return from_cuda(e);
 }
@@ -207,10 +246,12 @@ bs_status bs_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == BS_FP32
-          ? bsolve::launch_potrs<float>(layout, n, nrhs, batch, static_cast<const float*>(L),
-                                        static_cast<float*>(B), s)
-          : bsolve::launch_potrs<double>(layout, n, nrhs, batch, static_cast<const double*>(L),
-                                         static_cast<double*>(B), s);
+          ? bsolve::launch_potrs<float>(chol_layouts(layout, fill), n, nrhs, batch,
+                                        static_cast<const float*>(L), static_cast<float*>(B),
+                                        nullptr, s)
+          : bsolve::launch_potrs<double>(chol_layouts(layout, fill), n, nrhs, batch,
+                                         static_cast<const double*>(L), static_cast<double*>(B),
+                                         nullptr, s);
   return from_cuda(e);
 }
 

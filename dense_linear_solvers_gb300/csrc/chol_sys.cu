@@ -38,9 +38,10 @@ __host__ __device__ inline int sys_stride(int n, int nrhs) { return (tri(n) + n 
 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
-chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
+chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
                 T* __restrict__ B, int32_t* __restrict__ info) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int alay = layouts & 1, blay = layouts >> 1;   // storage orders of A and of B
   const int D = sys_stride(n, nrhs);
   const int TRI = tri(n);
   T* const M = reinterpret_cast<T*>(smem_raw);     // kSys systems, stride D
@@ -65,11 +66,11 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       const T* Bs = B + sys * n * nrhs;
       for (int j = 0; j < n; ++j)
         for (int i = j + lane; i < n; i += 32)
-          cp_async_elem<T>(Mq + tri(i) + j, layout == kColMajor ? As + j * n + i : As + i * n + j);
+          cp_async_elem<T>(Mq + tri(i) + j, alay == kColMajor ? As + j * n + i : As + i * n + j);
       for (int c = 0; c < nrhs; ++c)
         for (int i = lane; i < n; i += 32)
           cp_async_elem<T>(Mq + TRI + i * nrhs + c,
-                           layout == kColMajor ? Bs + c * n + i : Bs + i * nrhs + c);
+                           blay == kColMajor ? Bs + c * n + i : Bs + i * nrhs + c);
     } else {
       // a system past the end of the batch: an identity keeps its lanes finite
       for (int e = lane; e < D; e += 32) Mq[e] = T(0);
@@ -164,7 +165,7 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     for (int j = 0; j < n; ++j)
       for (int i = j + lane; i < n; i += 32) {
         const T v = Mq[tri(i) + j];
-        if (layout == kColMajor)
+        if (alay == kColMajor)
           As[j * n + i] = v;
         else
           As[i * n + j] = v;
@@ -172,7 +173,7 @@ chol_sys_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     for (int c = 0; c < nrhs; ++c)
       for (int i = lane; i < n; i += 32) {
         const T v = failed ? T(0) : Mq[TRI + i * nrhs + c];
-        if (layout == kColMajor)
+        if (blay == kColMajor)
           Bs[c * n + i] = v;
         else
           Bs[i * nrhs + c] = v;

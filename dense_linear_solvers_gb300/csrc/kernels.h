@@ -18,14 +18,19 @@ cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* 
                            int32_t* ipiv, int32_t* info, cudaStream_t stream);
 
 // Solve with a stored factor: getrs (L\U and the 1-based swap sequence of getrf) and
-// potrs (lower Cholesky factor), 1 <= n <= 64, 1 <= nrhs <= 8.
+// potrs (Cholesky factor), 1 <= n <= 64.
+// Any nrhs >= 1 (a register tier's worth at a time). zinfo (may be null): X = 0 where
+// zinfo[s] != 0.
 template <typename T>
 cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU,
-                         const int32_t* ipiv, T* B, cudaStream_t stream);
+                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream);
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
-                         cudaStream_t stream);
+                         const int32_t* zinfo, cudaStream_t stream);
 
+// The Cholesky launchers (chol_smem, chol_sys, potrs) take a packed storage-order code:
+// bit 0 for A (or the factor), bit 1 for B; upper fill is passed as the lower fill of A in
+// the other order.
 // Lower Cholesky + solve, one warp per system in shared memory, 1 <= n <= 64.
 template <typename T>
 cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,

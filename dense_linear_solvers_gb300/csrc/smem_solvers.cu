@@ -20,22 +20,26 @@ namespace {
 
 __host__ __device__ inline int odd_pitch(int w) { return w | 1; }
 
+// layouts: bit 0 the storage order of A, bit 1 that of B.
 template <typename T>
 __device__ __forceinline__ void load_system(const T* __restrict__ A, const T* __restrict__ B,
-                                            T* M, int n, int nrhs, int P, int layout,
+                                            T* M, int n, int nrhs, int P, int layouts,
                                             bool lower_only, int lane) {
-  if (layout == kRowMajor) {
+  if ((layouts & 1) == kRowMajor) {
     for (int i = 0; i < n; ++i) {
       const int jend = lower_only ? i + 1 : n;
       for (int j = lane; j < jend; j += 32) M[i * P + j] = A[i * n + j];
     }
+  } else {
+    for (int j = 0; j < n; ++j)
+      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) M[i * P + j] = A[j * n + i];
+  }
+  if ((layouts >> 1) == kRowMajor) {
     for (int e = lane; e < n * nrhs; e += 32) {
       const int i = e / nrhs, c = e - i * nrhs;
       M[i * P + n + c] = B[e];
     }
   } else {
-    for (int j = 0; j < n; ++j)
-      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) M[i * P + j] = A[j * n + i];
     for (int c = 0; c < nrhs; ++c)
       for (int i = lane; i < n; i += 32) M[i * P + n + c] = B[c * n + i];
   }
@@ -43,20 +47,23 @@ __device__ __forceinline__ void load_system(const T* __restrict__ A, const T* __
 
 template <typename T>
 __device__ __forceinline__ void store_system(T* __restrict__ A, T* __restrict__ B, const T* M,
-                                             int n, int nrhs, int P, int layout,
+                                             int n, int nrhs, int P, int layouts,
                                              bool lower_only, bool zero_x, int lane) {
-  if (layout == kRowMajor) {
+  if ((layouts & 1) == kRowMajor) {
     for (int i = 0; i < n; ++i) {
       const int jend = lower_only ? i + 1 : n;
       for (int j = lane; j < jend; j += 32) A[i * n + j] = M[i * P + j];
     }
+  } else {
+    for (int j = 0; j < n; ++j)
+      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) A[j * n + i] = M[i * P + j];
+  }
+  if ((layouts >> 1) == kRowMajor) {
     for (int e = lane; e < n * nrhs; e += 32) {
       const int i = e / nrhs, c = e - i * nrhs;
       B[e] = zero_x ? T(0) : M[i * P + n + c];
     }
   } else {
-    for (int j = 0; j < n; ++j)
-      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) A[j * n + i] = M[i * P + j];
     for (int c = 0; c < nrhs; ++c)
       for (int i = lane; i < n; i += 32) B[c * n + i] = zero_x ? T(0) : M[i * P + n + c];
   }
@@ -64,7 +71,7 @@ __device__ __forceinline__ void store_system(T* __restrict__ A, T* __restrict__ 
 
 template <typename T>
 __global__ void __launch_bounds__(32)
-chol_smem_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
+chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
                  T* __restrict__ B, int32_t* __restrict__ info) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x;
@@ -76,7 +83,7 @@ chol_smem_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
 
   A += s * n * n;
   B += s * n * nrhs;
-  load_system<T>(A, B, M, n, nrhs, P, layout, true, lane);
+  load_system<T>(A, B, M, n, nrhs, P, layouts, true, lane);
   __syncwarp();
 
   int inf = 0;
@@ -136,7 +143,7 @@ chol_smem_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       __syncwarp();
     }
   }
-  store_system<T>(A, B, M, n, nrhs, P, layout, true, inf != 0, lane);
+  store_system<T>(A, B, M, n, nrhs, P, layouts, true, inf != 0, lane);
   if (lane == 0) info[s] = inf;
 }
 

@@ -88,8 +88,9 @@ __device__ __forceinline__ void ldg_row(const T* __restrict__ p, T (&r)[N]) {
 
 template <typename T, int NT, int R, int RT, int KIND, bool FULL>
 __global__ void __launch_bounds__(kThreads)
-solve_reg_kernel(int n_, int nrhs_, int layout, int64_t batch, const T* __restrict__ M,
-                 const int32_t* __restrict__ ipiv, T* __restrict__ B) {
+solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restrict__ M,
+                 const int32_t* __restrict__ ipiv, T* __restrict__ B,
+                 const int32_t* __restrict__ zinfo) {
   constexpr int G = NT / R;
   constexpr int GPW = 32 / G;
   const int n = FULL ? NT : n_;
@@ -132,13 +133,12 @@ solve_reg_kernel(int n_, int nrhs_, int layout, int64_t batch, const T* __restri
   }
   T v[R][NT];
   T rt[R];
-  T b[R][RT];
 #pragma unroll
   for (int q = 0; q < R; ++q) {
     const int pq = t + q * G;
     rt[q] = T(1);
     if (ok[q]) {
-      if (KIND == kSolveLu && FULL && layout == kRowMajor) {
+      if (KIND == kSolveLu && FULL && (layouts & 1) == kRowMajor) {
         ldg_row<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
       } else {
 #pragma unroll
@@ -146,22 +146,35 @@ solve_reg_kernel(int n_, int nrhs_, int layout, int64_t batch, const T* __restri
           if (FULL || j < n) {
             const int r = (KIND == kSolveLu || j <= pq) ? pq : j;
             const int c = (KIND == kSolveLu || j <= pq) ? j : pq;
-            v[q][j] = __ldg(Ms + idx(layout, n, n, r, c));
+            v[q][j] = __ldg(Ms + idx(layouts & 1, n, n, r, c));
           } else {
             v[q][j] = T(0);
           }
         }
       }
-      rt[q] = diag_rcp<T, KIND>(__ldg(Ms + idx(layout, n, n, pq, pq)));
-      if (FULL && layout == kRowMajor) {
-        ldg_row<T, RT>(Bs + static_cast<int64_t>(src[q]) * RT, b[q]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < RT; ++c) b[q][c] = (c < nrhs) ? Bs[idx(layout, n, nrhs, src[q], c)] : T(0);
-      }
+      rt[q] = diag_rcp<T, KIND>(__ldg(Ms + idx(layouts & 1, n, n, pq, pq)));
     } else {
 #pragma unroll
       for (int j = 0; j < NT; ++j) v[q][j] = T(0);
+    }
+  }
+  // a failed factor of the fused call with more right-hand sides than a tier: X = 0
+  const bool zero_x = zinfo != nullptr && valid && __ldg(zinfo + s) != 0;
+
+  // the right-hand sides RT columns at a time (one pass when nrhs <= RT)
+  for (int c0 = 0; c0 < nrhs; c0 += RT) {
+  T b[R][RT];
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    if (ok[q]) {
+      if (FULL && (layouts >> 1) == kRowMajor) {
+        ldg_row<T, RT>(Bs + static_cast<int64_t>(src[q]) * RT, b[q]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < RT; ++c)
+          b[q][c] = (c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, src[q], c0 + c)] : T(0);
+      }
+    } else {
 #pragma unroll
       for (int c = 0; c < RT; ++c) b[q][c] = T(0);
     }
@@ -214,44 +227,49 @@ solve_reg_kernel(int n_, int nrhs_, int layout, int64_t batch, const T* __restri
   for (int q = 0; q < R; ++q) {
     if (!ok[q]) continue;
     const int pq = t + q * G;
-    if (FULL && layout == kRowMajor && (RT * sizeof(T)) % 16 == 0) {
+    if (FULL && (layouts >> 1) == kRowMajor && (RT * sizeof(T)) % 16 == 0) {
       T* dst = Bs + static_cast<int64_t>(pq) * RT;
 #pragma unroll
       for (int c = 0; c < RT; c += 16 / sizeof(T)) {
         if constexpr (sizeof(T) == 4)
-          *reinterpret_cast<float4*>(dst + c) = make_float4(b[q][c], b[q][c + 1], b[q][c + 2], b[q][c + 3]);
+          *reinterpret_cast<float4*>(dst + c) =
+              zero_x ? make_float4(0.f, 0.f, 0.f, 0.f)
+                     : make_float4(b[q][c], b[q][c + 1], b[q][c + 2], b[q][c + 3]);
         else
-          *reinterpret_cast<double2*>(dst + c) = make_double2(b[q][c], b[q][c + 1]);
+          *reinterpret_cast<double2*>(dst + c) =
+              zero_x ? make_double2(0.0, 0.0) : make_double2(b[q][c], b[q][c + 1]);
       }
     } else {
 #pragma unroll
       for (int c = 0; c < RT; ++c)
-        if (c < nrhs) Bs[idx(layout, n, nrhs, pq, c)] = b[q][c];
+        if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, pq, c0 + c)] = zero_x ? T(0) : b[q][c];
     }
   }
+  }   // right-hand-side chunk
 }
 
 template <typename T, int NT, int R, int RT, int KIND>
 cudaError_t launch_reg_tier(int layout, int n, int nrhs, int64_t batch, const T* M,
-                            const int32_t* ipiv, T* B, cudaStream_t stream) {
+                            const int32_t* ipiv, T* B, const int32_t* zinfo,
+                            cudaStream_t stream) {
   constexpr int per_block = kWarps * (32 / (NT / R));
   const int64_t blocks = (batch + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const unsigned nb = static_cast<unsigned>(blocks);
   if (n == NT && nrhs == RT)
-    solve_reg_kernel<T, NT, R, RT, KIND, true><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+    solve_reg_kernel<T, NT, R, RT, KIND, true><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo);
   else
-    solve_reg_kernel<T, NT, R, RT, KIND, false><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B);
+    solve_reg_kernel<T, NT, R, RT, KIND, false><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo);
   return cudaGetLastError();
 }
 
 template <typename T, int NT, int R, int KIND>
 cudaError_t launch_reg_rhs(int layout, int n, int nrhs, int64_t batch, const T* M,
-                           const int32_t* ipiv, T* B, cudaStream_t stream) {
-  if (nrhs <= 1) return launch_reg_tier<T, NT, R, 1, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (nrhs <= 2) return launch_reg_tier<T, NT, R, 2, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (nrhs <= 4) return launch_reg_tier<T, NT, R, 4, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  return launch_reg_tier<T, NT, R, 8, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+                           const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
+  if (nrhs <= 1) return launch_reg_tier<T, NT, R, 1, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (nrhs <= 2) return launch_reg_tier<T, NT, R, 2, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (nrhs <= 4) return launch_reg_tier<T, NT, R, 4, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  return launch_reg_tier<T, NT, R, 8, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
 }
 
 // ------------------------------------------------- 32 < n <= 64, shared memory, a warp
@@ -261,8 +279,9 @@ __host__ __device__ inline int odd_pitch(int n) { return n | 1; }
 
 template <typename T, int RT, int KIND>
 __global__ void __launch_bounds__(kSmemWarps * 32)
-solve_smem_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restrict__ M,
-                  const int32_t* __restrict__ ipiv, T* __restrict__ B) {
+solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restrict__ M,
+                  const int32_t* __restrict__ ipiv, T* __restrict__ B,
+                  const int32_t* __restrict__ zinfo) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int P = odd_pitch(n);
   const int lane = threadIdx.x & 31;
@@ -276,7 +295,7 @@ solve_smem_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restric
   // the factor (LU: all of it; Cholesky: the lower triangle only)
   for (int e = lane; e < n * n; e += 32) {
     int r, c;
-    if (layout == kRowMajor) {
+    if ((layouts & 1) == kRowMajor) {
       r = e / n;
       c = e - r * n;
     } else {
@@ -302,15 +321,23 @@ solve_smem_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restric
       }
     }
   }
-  T b[2][RT];
   T rq[2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const int i = lane + 32 * q;
-    const bool ok = i < n;
-    rq[q] = ok ? diag_rcp<T, KIND>(F[i * P + i]) : T(1);
+    rq[q] = i < n ? diag_rcp<T, KIND>(F[i * P + i]) : T(1);
+  }
+  const bool zero_x = zinfo != nullptr && __ldg(zinfo + s) != 0;
+
+  // the right-hand sides RT columns at a time
+  for (int c0 = 0; c0 < nrhs; c0 += RT) {
+  T b[2][RT];
 #pragma unroll
-    for (int c = 0; c < RT; ++c) b[q][c] = (ok && c < nrhs) ? Bs[idx(layout, n, nrhs, src[q], c)] : T(0);
+  for (int q = 0; q < 2; ++q) {
+    const bool ok = lane + 32 * q < n;
+#pragma unroll
+    for (int c = 0; c < RT; ++c)
+      b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, src[q], c0 + c)] : T(0);
   }
 
   for (int k = 0; k < n; ++k) {
@@ -363,14 +390,15 @@ solve_smem_kernel(int n, int nrhs, int layout, int64_t batch, const T* __restric
     if (i < n) {
 #pragma unroll
       for (int c = 0; c < RT; ++c)
-        if (c < nrhs) Bs[idx(layout, n, nrhs, i, c)] = b[q][c];
+        if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, i, c0 + c)] = zero_x ? T(0) : b[q][c];
     }
   }
+  }   // right-hand-side chunk
 }
 
 template <typename T, int KIND>
 cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
-                        const int32_t* ipiv, T* B, cudaStream_t stream) {
+                        const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
   const int64_t blocks = (batch + kSmemWarps - 1) / kSmemWarps;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = static_cast<size_t>(kSmemWarps) * n * odd_pitch(n) * sizeof(T);
@@ -381,7 +409,7 @@ cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)); \
   if (e != cudaSuccess) return e;                                                           \
   solve_smem_kernel<T, RTV, KIND><<<nb, kSmemWarps * 32, bytes, stream>>>(n, nrhs, layout,  \
-                                                                          batch, M, ipiv, B);
+                                                                          batch, M, ipiv, B, zinfo);
   if (nrhs <= 1) {
     BSOLVE_SOLVE_SMEM(1)
   } else if (nrhs <= 2) {
@@ -397,36 +425,41 @@ cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
 
 template <typename T, int KIND>
 cudaError_t launch_kind(int layout, int n, int nrhs, int64_t batch, const T* M,
-                        const int32_t* ipiv, T* B, cudaStream_t stream) {
-  if (n <= 4) return launch_reg_rhs<T, 4, 1, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 8) return launch_reg_rhs<T, 8, kRows8, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 16) return launch_reg_rhs<T, 16, kRows16, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 32) return launch_reg_rhs<T, 32, kRows32, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
-  if (n <= 64) return launch_smem<T, KIND>(layout, n, nrhs, batch, M, ipiv, B, stream);
+                        const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
+  if (n <= 4) return launch_reg_rhs<T, 4, 1, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (n <= 8) return launch_reg_rhs<T, 8, kRows8, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (n <= 16) return launch_reg_rhs<T, 16, kRows16, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (n <= 32) return launch_reg_rhs<T, 32, kRows32, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (n <= 64) return launch_smem<T, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+// `layout` of the launchers below is the packed code: bit 0 the storage order of the
+// factor, bit 1 that of B (getrs: both the same; potrs with upper fill: the factor read as
+// the lower triangle of the other order). zinfo (may be null): the factor's info, and X is
+// written as zeros where it is not 0 (the fused calls' contract, when they run as a factor
+// and a solve for more right-hand sides than a register tier holds).
 template <typename T>
 cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU,
-                         const int32_t* ipiv, T* B, cudaStream_t stream) {
-  return launch_kind<T, kSolveLu>(layout, n, nrhs, batch, LU, ipiv, B, stream);
+                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
+  return launch_kind<T, kSolveLu>(layout, n, nrhs, batch, LU, ipiv, B, zinfo, stream);
 }
 
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
-                         cudaStream_t stream) {
-  return launch_kind<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, stream);
+                         const int32_t* zinfo, cudaStream_t stream) {
+  return launch_kind<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, zinfo, stream);
 }
 
 template cudaError_t launch_getrs<float>(int, int, int, int64_t, const float*, const int32_t*,
-                                         float*, cudaStream_t);
+                                         float*, const int32_t*, cudaStream_t);
 template cudaError_t launch_getrs<double>(int, int, int, int64_t, const double*, const int32_t*,
-                                          double*, cudaStream_t);
+                                          double*, const int32_t*, cudaStream_t);
 template cudaError_t launch_potrs<float>(int, int, int, int64_t, const float*, float*,
-                                         cudaStream_t);
+                                         const int32_t*, cudaStream_t);
 template cudaError_t launch_potrs<double>(int, int, int, int64_t, const double*, double*,
-                                          cudaStream_t);
+                                          const int32_t*, cudaStream_t);
 
 }  // namespace bsolve

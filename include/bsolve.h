@@ -2,7 +2,8 @@
  * bsolve.h -- C ABI of libbsolve.so: batched solution of many independent small dense
  * linear systems A x = b on one GPU (sm_103a).
  *
- * Every entry point solves `batch` independent systems in one asynchronous launch on
+ * Every entry point solves `batch` independent systems in one asynchronous launch (two
+ * for a fused call with more than 8 right-hand sides: the factor, then the solve) on
  * the caller's CUDA stream. All matrix and vector pointers are DEVICE pointers owned by
  * the caller; the library allocates no memory, keeps no state between calls and never
  * synchronizes the host. Results are valid once the stream has reached the launch;
@@ -72,7 +73,9 @@ typedef enum { BS_LOWER = 0, BS_UPPER = 1 } bs_fill;
  *         such a system is then unspecified.
  * Pivot choice: the row of largest magnitude in the pivot column, lowest current row
  * on ties. The factorization is of A itself (P A = L U) in both layouts.
- * Supported: dtype FP32/FP64, both layouts, 1 <= n <= 64, 1 <= nrhs <= 8.
+ * Supported: dtype FP32/FP64, both layouts, 1 <= n <= 64, 1 <= nrhs <= 65536 (above 8 the
+ * call runs as bs_getrf_batched then the solve of bs_getrs_batched, X zeroed where
+ * info != 0: the same operations in the same order, so the same bits).
  * stream: a cudaStream_t (0 = the legacy default stream).
  */
 BS_API bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs,
@@ -89,14 +92,17 @@ BS_API bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n,
  * "ruSOLVER: small-matrix kernel optimisation" -- failed outputs zeroed.
  *
  *   A     batch x n x n in `layout`; with BS_LOWER only the lower triangle (diagonal
- *         included) is read and replaced by L (A = L L^T); the strict upper triangle is
- *         neither read nor written.
+ *         included) is read and replaced by L (A = L L^T), the strict upper triangle is
+ *         neither read nor written; with BS_UPPER only the upper triangle is read and
+ *         replaced by U (A = U^T U, U = L^T: the same operations on mirrored entries),
+ *         the strict lower triangle is neither read nor written.
  *   B     batch x n x nrhs, same layout as A. On return: X (zero where info != 0).
  *   info  batch int32. 0 = success; k > 0 = the leading minor of order k is not positive
  *         definite (the k-th diagonal of the factorization is not > 0, NaN included).
  *         The factor from column k-1 on is then unspecified.
- * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER, 1 <= n <= 64, 1 <= nrhs <= 8.
- * BS_UPPER returns BS_ERR_UNSUPPORTED.
+ * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER or BS_UPPER, 1 <= n <= 64,
+ * 1 <= nrhs <= 65536 (above 8: bs_potrf_batched then the solve of bs_potrs_batched, X
+ * zeroed where info != 0).
  */
 BS_API bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
                                  int nrhs, int64_t batch, void* A, void* B, int32_t* info,
@@ -146,14 +152,16 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  * bs_getrs_batched:  LU, ipiv from bs_getrf_batched (read only; an ipiv entry outside 1..n
  *                    swaps nothing); B (batch x n x nrhs, same layout) <- X. B must not
  *                    overlap LU or ipiv.
- * bs_potrf_batched:  A <- L (lower triangle; the strict upper triangle neither read nor
- *                    written), info as bs_potrf_potrs_batched.
- * bs_potrs_batched:  L from bs_potrf_batched (read only, lower triangle only); B <- X.
+ * bs_potrf_batched:  A <- L or U in the `fill` triangle (the other triangle neither read
+ *                    nor written), info as bs_potrf_potrs_batched.
+ * bs_potrs_batched:  the factor from bs_potrf_batched with the same fill (read only, its
+ *                    triangle only); B <- X.
  * bs_bdsv_factor_batched: strips <- F_k (MAIN, lower), E_k (LEFT); info as bs_bdsv_batched.
  * bs_bdsv_solve_batched:  strips from bs_bdsv_factor_batched (read only); interior of
  *                    x_padded: b on entry, x on return (pads neither read nor written).
  * Supported: as the fused calls (getrf/potrf: 1 <= n <= 64; getrs/potrs: 1 <= n <= 64,
- * 1 <= nrhs <= 8; bdsv: 1 <= block_size <= 8), FP32/FP64, both layouts, fill BS_LOWER.
+ * 1 <= nrhs <= 65536, taken 8 columns at a time; bdsv: 1 <= block_size <= 8), FP32/FP64,
+ * both layouts, both fills.
  */
 BS_API bs_status bs_getrf_batched(bs_dtype dtype, bs_layout layout, int n, int64_t batch, void* A,
                                   int32_t* ipiv, int32_t* info, void* stream);

@@ -51,10 +51,12 @@ def test_supported_queries(lib):
     assert lib.bs_getrf_getrs_supported(bs.BS_FP32, bs.BS_ROW_MAJOR, 16, 4) == 1
     assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, 64, 8) == 1
     assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 65, 1) == 0
-    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 8, 9) == 0
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 8, 9) == 1
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 8, 65537) == 0
     assert lib.bs_getrf_getrs_supported(2, bs.BS_ROW_MAJOR, 8, 1) == 0
     assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_LOWER, 32, 1) == 1
-    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_UPPER, 32, 1) == 0
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_UPPER, 32, 1) == 1
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, 2, 32, 1) == 0
     assert lib.bs_bdsv_supported(bs.BS_FP64, 32, 8) == 1
     assert lib.bs_bdsv_supported(bs.BS_FP64, 32, 9) == 0
 
@@ -69,7 +71,7 @@ def test_lu_argument_errors(lib):
     assert f(bs.BS_FP32, 0, -3, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 65, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 0, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
-    assert f(bs.BS_FP32, 0, 16, 9, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 65537, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(7, 0, 16, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 5, 16, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 4, 5, None, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
@@ -81,7 +83,7 @@ def test_lu_argument_errors(lib):
 def test_chol_argument_errors(lib):
     f = lib.bs_potrf_potrs_batched
     assert f(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None, None) == bs.BS_OK
-    assert f(bs.BS_FP64, 1, 1, 32, 1, 5, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED  # upper
+    assert f(bs.BS_FP64, 1, 2, 32, 1, 5, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED  # bad fill
     assert f(bs.BS_FP64, 1, 0, 32, 1, 5, FAKE, None, FAKE, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP64, 1, 0, 32, 1, 5, FAKE, FAKE, FAKE + 2, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP64, 1, 0, 32, -1, 5, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
@@ -109,13 +111,13 @@ def test_split_argument_errors(lib):
     assert f(bs.BS_FP32, 0, 16, 5, A + 4, P, I, None) == bs.BS_ERR_INVALID_ARG
     f = lib.bs_getrs_batched
     assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None) == bs.BS_OK
-    assert f(bs.BS_FP32, 0, 16, 9, 5, A, P, B, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 65537, 5, A, P, B, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, P, None, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, P, A + 16, None) == bs.BS_ERR_INVALID_ARG  # B over LU
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, P, P, None) == bs.BS_ERR_INVALID_ARG       # B over ipiv
     f = lib.bs_potrf_batched
     assert f(bs.BS_FP64, 1, 0, 32, 0, None, None, None) == bs.BS_OK
-    assert f(bs.BS_FP64, 1, 1, 32, 5, A, I, None) == bs.BS_ERR_UNSUPPORTED  # upper fill
+    assert f(bs.BS_FP64, 1, 3, 32, 5, A, I, None) == bs.BS_ERR_UNSUPPORTED  # bad fill
     assert f(bs.BS_FP64, 1, 0, 32, 5, A, None, None) == bs.BS_ERR_INVALID_ARG
     f = lib.bs_potrs_batched
     assert f(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None) == bs.BS_OK

@@ -275,3 +275,86 @@ def test_bdmv_every_block_size(dtype):
             yg = gpu_bdmv(strips, xpad, y0)
             yo = oracle.bdmv(strips, xpad, y0)
             assert np.array_equal(yg, yo), (bsz, nbr)
+
+
+# ------------------------------------------------------------------ Cholesky, upper fill
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_cholesky_upper_fill_every_order(dtype, layout):
+    """Upper fill (A = U^T U): the fused call, potrf and potrs leave the oracle's U, info
+    and X bit for bit; the strict lower triangle (NaN here) is neither read nor written."""
+    rng = np.random.default_rng(909 + layout)
+    for n in range(1, 65):
+        nrhs = int(rng.integers(1, 9))
+        G = rng.standard_normal((23, n, n))
+        Al = G @ np.swapaxes(G, 1, 2) + n * np.eye(n)
+        if n > 2:
+            Al[4, n // 2, n // 2] = -1.0
+        il = np.tril_indices(n, -1)
+        Al[:, il[0], il[1]] = np.nan
+        A = to_storage(Al.astype(dtype), layout)
+        B = to_storage(rng.standard_normal((23, n, nrhs)).astype(dtype), layout)
+        Uo, Xo, info_o = oracle.potrf_potrs(A, B, layout, nthreads=NT, fill=oracle.UPPER)
+        tA, tB = _dev(A), _dev(B)
+        info = torch.full((23,), SENT, dtype=torch.int32, device="cuda")
+        bs.bs_potrf_potrs_batched(tA, tB, info, layout, bs.BS_UPPER)
+        Ug, Xg, infg = _host(tA), _host(tB), _host(info)
+        assert np.array_equal(infg, info_o)
+        ok = info_o == 0
+        assert np.array_equal(Ug[ok], Uo[ok], equal_nan=True)
+        assert np.array_equal(Xg, Xo)                    # failed systems: zeros on both
+        # the halves
+        tA2 = _dev(A)
+        info2 = torch.full((23,), SENT, dtype=torch.int32, device="cuda")
+        bs.bs_potrf_batched(tA2, info2, layout, bs.BS_UPPER)
+        assert np.array_equal(_host(info2), info_o)
+        assert np.array_equal(_host(tA2)[ok], Uo[ok], equal_nan=True)
+        tB2 = _dev(B)
+        bs.bs_potrs_batched(_dev(Uo), tB2, layout, bs.BS_UPPER)
+        Xs = _host(tB2)
+        Xso = oracle.potrs(Uo, B, layout, fill=oracle.UPPER)
+        assert np.array_equal(Xs[ok], Xso[ok])
+        assert np.array_equal(Xs[ok], Xo[ok])
+
+
+# ------------------------------------------------------------------ more right-hand sides
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_many_right_hand_sides(dtype, layout):
+    """nrhs > 8: the fused calls run as factor + chunked solve and still leave the oracle's
+    fused results bit for bit (X zero where info != 0); getrs/potrs take the right-hand
+    sides eight at a time."""
+    rng = np.random.default_rng(1010 + layout)
+    for n, nrhs in ((1, 9), (5, 13), (16, 40), (31, 17), (33, 9), (64, 24)):
+        Al = rng.standard_normal((29, n, n)).astype(dtype)
+        if n > 1:
+            Al[3, :, n - 1] = 0
+        A = to_storage(Al, layout)
+        B = to_storage(rng.standard_normal((29, n, nrhs)).astype(dtype), layout)
+        LUo, Xo, ipo, info_o, tie = oracle.getrf_getrs(A, B, layout, nthreads=NT)
+        LUg, Xg, ipg, infg = parity.gpu_lu(A, B, layout)
+        clean = tie < 0
+        assert np.array_equal(infg[clean], info_o[clean])
+        assert np.array_equal(LUg[clean], LUo[clean]) and np.array_equal(Xg[clean], Xo[clean])
+        assert np.all(Xg[infg != 0] == 0)
+        Xs = gpu_getrs(LUo, ipo, B, layout)
+        ok = info_o == 0
+        assert np.array_equal(Xs[ok], oracle.getrs(LUo, ipo, B, layout)[ok])
+        # Cholesky, both fills
+        G = rng.standard_normal((29, n, n))
+        S = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dtype)
+        if n > 2:
+            S[5, 1, 1] = -1.0
+        As = to_storage(S, layout)
+        for fill in (bs.BS_LOWER, bs.BS_UPPER):
+            Lo, Xco, inf_co = oracle.potrf_potrs(As, B, layout, nthreads=NT, fill=fill)
+            tA, tB = _dev(As), _dev(B)
+            info = torch.full((29,), SENT, dtype=torch.int32, device="cuda")
+            bs.bs_potrf_potrs_batched(tA, tB, info, layout, fill)
+            okc = inf_co == 0
+            assert np.array_equal(_host(info), inf_co)
+            assert np.array_equal(_host(tA)[okc], Lo[okc])
+            assert np.array_equal(_host(tB), Xco)
+            tB2 = _dev(B)
+            bs.bs_potrs_batched(_dev(Lo), tB2, layout, fill)
+            assert np.array_equal(_host(tB2)[okc], Xco[okc])
