@@ -10,7 +10,7 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
-constexpr int kMaxLuN = 64;
+constexpr int kMaxLuN = 128;
 constexpr int kMaxRegN = 32;
 constexpr int kMaxNrhs = 8;          // right-hand sides a fused kernel holds
 constexpr int kMaxNrhsAny = 65536;   // beyond kMaxNrhs: factor, then a chunked solve

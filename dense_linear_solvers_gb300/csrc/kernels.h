@@ -12,13 +12,13 @@ template <typename T>
 cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                           int32_t* ipiv, int32_t* info, cudaStream_t stream);
 
-// LU + solve, one warp per system in shared memory, 1 <= n <= 64, 1 <= nrhs <= 8.
+// LU + solve, one block of four warps per system in shared memory, 1 <= n <= 128, 0 <= nrhs <= 8.
 template <typename T>
 cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                            int32_t* ipiv, int32_t* info, cudaStream_t stream);
 
 // Solve with a stored factor: getrs (L\U and the 1-based swap sequence of getrf) and
-// potrs (Cholesky factor), 1 <= n <= 64.
+// potrs (Cholesky factor), 1 <= n <= 128.
 // Any nrhs >= 1 (a register tier's worth at a time). zinfo (may be null): X = 0 where
 // zinfo[s] != 0.
 template <typename T>
@@ -31,7 +31,7 @@ cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L,
 // The Cholesky launchers (chol_smem, chol_sys, potrs) take a packed storage-order code:
 // bit 0 for A (or the factor), bit 1 for B; upper fill is passed as the lower fill of A in
 // the other order.
-// Lower Cholesky + solve, one warp per system in shared memory, 1 <= n <= 64.
+// Lower Cholesky + solve, one warp per system in shared memory, 1 <= n <= 128.
 template <typename T>
 cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                              int32_t* info, cudaStream_t stream);

@@ -1,4 +1,4 @@
-// LU with partial pivoting + solve for 32 < n <= 64: one system per block of four warps,
+// LU with partial pivoting + solve for 32 < n <= 128: one system per block of four warps,
 // the system resident in shared memory.
 //
 // The system is one n x P row-major tile M = [A | B] (P = n + nrhs rounded up to an

@@ -1,4 +1,4 @@
-// Lower Cholesky for 32 < n <= 64, one warp per system, with the system resident in
+// Lower Cholesky for 32 < n <= 128, one warp per system, with the system resident in
 // shared memory (n <= 32 runs the lockstep kernel of chol_sys.cu).
 //
 // The system is held as one n x P row-major tile M = [A | B] (P = n + nrhs rounded up to

@@ -12,8 +12,8 @@
 // diagonal, column p right of it). Each step k broadcasts one value per right-hand side
 // from the owner of position k by a shuffle, and every lane applies it from registers:
 // no shared memory, no barrier.
-// 32 < n <= 64: one warp per system, the factor in shared memory with an odd pitch, lane
-// t owning positions t and t+32.
+// 32 < n <= 128: one warp per system, the factor in shared memory with an odd pitch, lane
+// t owning positions t, t+32, ...
 //
 // getrs: lane t loads the right-hand-side row that the swap sequence brings to position
 // t (the swaps undone from the last: pos = t, then for k = n-1..0 pos <- tau_k(pos)); an
@@ -272,13 +272,20 @@ cudaError_t launch_reg_rhs(int layout, int n, int nrhs, int64_t batch, const T* 
   return launch_reg_tier<T, NT, R, 8, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
 }
 
-// ------------------------------------------------- 32 < n <= 64, shared memory, a warp
-constexpr int kSmemWarps = 2;
-
+// ---------------------------------------- 32 < n <= 128, shared memory, one warp a system
 __host__ __device__ inline int odd_pitch(int n) { return n | 1; }
 
-template <typename T, int RT, int KIND>
-__global__ void __launch_bounds__(kSmemWarps * 32)
+// Q positions per lane (lane t owns t, t+32, ...): Q = 2 for n <= 64, 4 for n <= 128.
+template <typename T, int Q>
+__device__ __forceinline__ T pick(const T (&v)[Q], int q) {
+  T r = v[0];
+#pragma unroll
+  for (int i = 1; i < Q; ++i) r = (q == i) ? v[i] : r;
+  return r;
+}
+
+template <typename T, int RT, int KIND, int Q, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
 solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restrict__ M,
                   const int32_t* __restrict__ ipiv, T* __restrict__ B,
                   const int32_t* __restrict__ zinfo) {
@@ -286,7 +293,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
   const int P = odd_pitch(n);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int64_t s = static_cast<int64_t>(blockIdx.x) * kSmemWarps + warp;
+  const int64_t s = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
   if (s >= batch) return;   // whole warp: no block barrier below
   T* const F = reinterpret_cast<T*>(smem_raw) + static_cast<int64_t>(warp) * n * P;
   const T* Ms = M + s * n * n;
@@ -307,23 +314,27 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
   cp_async_wait_all();
   __syncwarp();
 
-  int src[2] = {lane, lane + 32};
+  int src[Q];
+#pragma unroll
+  for (int q = 0; q < Q; ++q) src[q] = lane + 32 * q;
   if (KIND == kSolveLu) {
-    const int ip0 = lane < n ? __ldg(ipiv + s * n + lane) - 1 : 0;
-    const int ip1 = lane + 32 < n ? __ldg(ipiv + s * n + lane + 32) - 1 : 0;
+    int ip[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+      ip[q] = lane + 32 * q < n ? __ldg(ipiv + s * n + lane + 32 * q) - 1 : 0;
     for (int k = n - 1; k >= 0; --k) {
-      int p = __shfl_sync(0xFFFFFFFFu, k < 32 ? ip0 : ip1, k & 31);
+      int p = __shfl_sync(0xFFFFFFFFu, pick<int, Q>(ip, k >> 5), k & 31);
       if (p < 0 || p >= n) p = k;   // an entry out of range swaps nothing
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < Q; ++q) {
         if (src[q] == k) src[q] = p;
         else if (src[q] == p) src[q] = k;
       }
     }
   }
-  T rq[2];
+  T rq[Q];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
+  for (int q = 0; q < Q; ++q) {
     const int i = lane + 32 * q;
     rq[q] = i < n ? diag_rcp<T, KIND>(F[i * P + i]) : T(1);
   }
@@ -331,96 +342,110 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
 
   // the right-hand sides RT columns at a time
   for (int c0 = 0; c0 < nrhs; c0 += RT) {
-  T b[2][RT];
+    T b[Q][RT];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const bool ok = lane + 32 * q < n;
-#pragma unroll
-    for (int c = 0; c < RT; ++c)
-      b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, src[q], c0 + c)] : T(0);
-  }
-
-  for (int k = 0; k < n; ++k) {
-    const int kq = k >> 5, kl = k & 31;
-    if (KIND == kSolveChol && lane == kl) {
-#pragma unroll
-      for (int c = 0; c < RT; ++c) {
-        if (kq == 0) b[0][c] = b[0][c] * rq[0];
-        else b[1][c] = b[1][c] * rq[1];
-      }
-    }
-    T y[RT];
-#pragma unroll
-    for (int c = 0; c < RT; ++c) y[c] = __shfl_sync(0xFFFFFFFFu, kq == 0 ? b[0][c] : b[1][c], kl);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int i = lane + 32 * q;
-      if (i > k && i < n) {
-        const T l = F[i * P + k];
-#pragma unroll
-        for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-l, y[c], b[q][c]);
-      }
-    }
-  }
-  for (int k = n - 1; k >= 0; --k) {
-    const int kq = k >> 5, kl = k & 31;
-    if (lane == kl) {
-#pragma unroll
-      for (int c = 0; c < RT; ++c) {
-        if (kq == 0) b[0][c] = b[0][c] * rq[0];
-        else b[1][c] = b[1][c] * rq[1];
-      }
-    }
-    T x[RT];
-#pragma unroll
-    for (int c = 0; c < RT; ++c) x[c] = __shfl_sync(0xFFFFFFFFu, kq == 0 ? b[0][c] : b[1][c], kl);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int i = lane + 32 * q;
-      if (i < k) {
-        const T u = KIND == kSolveLu ? F[i * P + k] : F[k * P + i];
-#pragma unroll
-        for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-u, x[c], b[q][c]);
-      }
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int i = lane + 32 * q;
-    if (i < n) {
+    for (int q = 0; q < Q; ++q) {
+      const bool ok = lane + 32 * q < n;
 #pragma unroll
       for (int c = 0; c < RT; ++c)
-        if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, i, c0 + c)] = zero_x ? T(0) : b[q][c];
+        b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, src[q], c0 + c)] : T(0);
+    }
+    for (int k = 0; k < n; ++k) {
+      const int kq = k >> 5, kl = k & 31;
+      if (KIND == kSolveChol && lane == kl) {
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+          if (q == kq)
+#pragma unroll
+            for (int c = 0; c < RT; ++c) b[q][c] = b[q][c] * rq[q];
+      }
+      T y[RT];
+#pragma unroll
+      for (int c = 0; c < RT; ++c) {
+        T own = b[0][c];
+#pragma unroll
+        for (int q = 1; q < Q; ++q) own = (kq == q) ? b[q][c] : own;
+        y[c] = __shfl_sync(0xFFFFFFFFu, own, kl);
+      }
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const int i = lane + 32 * q;
+        if (i > k && i < n) {
+          const T l = F[i * P + k];
+#pragma unroll
+          for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-l, y[c], b[q][c]);
+        }
+      }
+    }
+    for (int k = n - 1; k >= 0; --k) {
+      const int kq = k >> 5, kl = k & 31;
+      if (lane == kl) {
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+          if (q == kq)
+#pragma unroll
+            for (int c = 0; c < RT; ++c) b[q][c] = b[q][c] * rq[q];
+      }
+      T x[RT];
+#pragma unroll
+      for (int c = 0; c < RT; ++c) {
+        T own = b[0][c];
+#pragma unroll
+        for (int q = 1; q < Q; ++q) own = (kq == q) ? b[q][c] : own;
+        x[c] = __shfl_sync(0xFFFFFFFFu, own, kl);
+      }
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const int i = lane + 32 * q;
+        if (i < k) {
+          const T u = KIND == kSolveLu ? F[i * P + k] : F[k * P + i];
+#pragma unroll
+          for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-u, x[c], b[q][c]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const int i = lane + 32 * q;
+      if (i < n) {
+#pragma unroll
+        for (int c = 0; c < RT; ++c)
+          if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, i, c0 + c)] = zero_x ? T(0) : b[q][c];
+      }
     }
   }
-  }   // right-hand-side chunk
+}
+
+template <typename T, int RT, int KIND, int Q, int WARPS>
+cudaError_t launch_smem_q(int layout, int n, int nrhs, int64_t batch, const T* M,
+                          const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
+  const int64_t blocks = (batch + WARPS - 1) / WARPS;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const size_t bytes = static_cast<size_t>(WARPS) * n * odd_pitch(n) * sizeof(T);
+  cudaError_t e = cudaFuncSetAttribute(solve_smem_kernel<T, RT, KIND, Q, WARPS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  solve_smem_kernel<T, RT, KIND, Q, WARPS><<<static_cast<unsigned>(blocks), WARPS * 32, bytes,
+                                             stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo);
+  return cudaGetLastError();
+}
+
+template <typename T, int KIND, int Q, int WARPS>
+cudaError_t launch_smem_rhs(int layout, int n, int nrhs, int64_t batch, const T* M,
+                            const int32_t* ipiv, T* B, const int32_t* zinfo,
+                            cudaStream_t stream) {
+  if (nrhs <= 1) return launch_smem_q<T, 1, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (nrhs <= 2) return launch_smem_q<T, 2, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (nrhs <= 4) return launch_smem_q<T, 4, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  return launch_smem_q<T, 8, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
 }
 
 template <typename T, int KIND>
 cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
-  const int64_t blocks = (batch + kSmemWarps - 1) / kSmemWarps;
-  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  const size_t bytes = static_cast<size_t>(kSmemWarps) * n * odd_pitch(n) * sizeof(T);
-  const unsigned nb = static_cast<unsigned>(blocks);
-  cudaError_t e = cudaSuccess;
-#define BSOLVE_SOLVE_SMEM(RTV)                                                              \
-  e = cudaFuncSetAttribute(solve_smem_kernel<T, RTV, KIND>,                                 \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)); \
-  if (e != cudaSuccess) return e;                                                           \
-  solve_smem_kernel<T, RTV, KIND><<<nb, kSmemWarps * 32, bytes, stream>>>(n, nrhs, layout,  \
-                                                                          batch, M, ipiv, B, zinfo);
-  if (nrhs <= 1) {
-    BSOLVE_SOLVE_SMEM(1)
-  } else if (nrhs <= 2) {
-    BSOLVE_SOLVE_SMEM(2)
-  } else if (nrhs <= 4) {
-    BSOLVE_SOLVE_SMEM(4)
-  } else {
-    BSOLVE_SOLVE_SMEM(8)
-  }
-#undef BSOLVE_SOLVE_SMEM
-  return cudaGetLastError();
+  if (n <= 64) return launch_smem_rhs<T, KIND, 2, 2>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  return launch_smem_rhs<T, KIND, 4, 1>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
 }
 
 template <typename T, int KIND>
@@ -430,7 +455,7 @@ cudaError_t launch_kind(int layout, int n, int nrhs, int64_t batch, const T* M,
   if (n <= 8) return launch_reg_rhs<T, 8, kRows8, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
   if (n <= 16) return launch_reg_rhs<T, 16, kRows16, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
   if (n <= 32) return launch_reg_rhs<T, 32, kRows32, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
-  if (n <= 64) return launch_smem<T, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+  if (n <= 128) return launch_smem<T, KIND>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -73,7 +73,7 @@ typedef enum { BS_LOWER = 0, BS_UPPER = 1 } bs_fill;
  *         such a system is then unspecified.
  * Pivot choice: the row of largest magnitude in the pivot column, lowest current row
  * on ties. The factorization is of A itself (P A = L U) in both layouts.
- * Supported: dtype FP32/FP64, both layouts, 1 <= n <= 64, 1 <= nrhs <= 65536 (above 8 the
+ * Supported: dtype FP32/FP64, both layouts, 1 <= n <= 128, 1 <= nrhs <= 65536 (above 8 the
  * call runs as bs_getrf_batched then the solve of bs_getrs_batched, X zeroed where
  * info != 0: the same operations in the same order, so the same bits).
  * stream: a cudaStream_t (0 = the legacy default stream).
@@ -100,7 +100,7 @@ BS_API bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n,
  *   info  batch int32. 0 = success; k > 0 = the leading minor of order k is not positive
  *         definite (the k-th diagonal of the factorization is not > 0, NaN included).
  *         The factor from column k-1 on is then unspecified.
- * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER or BS_UPPER, 1 <= n <= 64,
+ * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER or BS_UPPER, 1 <= n <= 128,
  * 1 <= nrhs <= 65536 (above 8: bs_potrf_batched then the solve of bs_potrs_batched, X
  * zeroed where info != 0).
  */
@@ -159,7 +159,7 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  * bs_bdsv_factor_batched: strips <- F_k (MAIN, lower), E_k (LEFT); info as bs_bdsv_batched.
  * bs_bdsv_solve_batched:  strips from bs_bdsv_factor_batched (read only); interior of
  *                    x_padded: b on entry, x on return (pads neither read nor written).
- * Supported: as the fused calls (getrf/potrf: 1 <= n <= 64; getrs/potrs: 1 <= n <= 64,
+ * Supported: as the fused calls (getrf/potrf: 1 <= n <= 128; getrs/potrs: 1 <= n <= 128,
  * 1 <= nrhs <= 65536, taken 8 columns at a time; bdsv: 1 <= block_size <= 8), FP32/FP64,
  * both layouts, both fills.
  */

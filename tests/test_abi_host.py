@@ -50,7 +50,7 @@ def test_status_strings(lib):
 def test_supported_queries(lib):
     assert lib.bs_getrf_getrs_supported(bs.BS_FP32, bs.BS_ROW_MAJOR, 16, 4) == 1
     assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, 64, 8) == 1
-    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 65, 1) == 0
+    assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 129, 1) == 0
     assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 8, 9) == 1
     assert lib.bs_getrf_getrs_supported(bs.BS_FP64, bs.BS_ROW_MAJOR, 8, 65537) == 0
     assert lib.bs_getrf_getrs_supported(2, bs.BS_ROW_MAJOR, 8, 1) == 0
@@ -69,7 +69,7 @@ def test_lu_argument_errors(lib):
     assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, None) == bs.BS_OK  # empty batch
     assert f(bs.BS_FP32, 0, 16, 4, -1, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, -3, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_INVALID_ARG
-    assert f(bs.BS_FP32, 0, 65, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 129, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 0, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 65537, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
     assert f(7, 0, 16, 4, 5, FAKE, FAKE, FAKE, FAKE, None) == bs.BS_ERR_UNSUPPORTED
@@ -105,7 +105,7 @@ def test_split_argument_errors(lib):
     A, B, P, I = FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000
     f = lib.bs_getrf_batched
     assert f(bs.BS_FP32, 0, 16, 0, None, None, None, None) == bs.BS_OK
-    assert f(bs.BS_FP32, 0, 65, 5, A, P, I, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 129, 5, A, P, I, None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, -1, 5, A, P, I, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 5, A, None, I, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 5, A + 4, P, I, None) == bs.BS_ERR_INVALID_ARG

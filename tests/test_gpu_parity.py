@@ -191,9 +191,9 @@ def test_empty_batch_launches_nothing():
 
 def test_unsupported_shape_is_an_error():
     dev = torch.device("cuda")
-    A = torch.zeros((2, 65, 65), device=dev)
-    B = torch.zeros((2, 65, 1), device=dev)
+    A = torch.zeros((2, 129, 129), device=dev)
+    B = torch.zeros((2, 129, 1), device=dev)
     with pytest.raises(bs.BsolveError) as e:
-        bs.bs_getrf_getrs_batched(A, B, torch.zeros((2, 65), dtype=torch.int32, device=dev),
+        bs.bs_getrf_getrs_batched(A, B, torch.zeros((2, 129), dtype=torch.int32, device=dev),
                                   torch.zeros(2, dtype=torch.int32, device=dev))
     assert e.value.status == bs.BS_ERR_UNSUPPORTED

@@ -358,3 +358,41 @@ def test_many_right_hand_sides(dtype, layout):
             tB2 = _dev(B)
             bs.bs_potrs_batched(_dev(Lo), tB2, layout, fill)
             assert np.array_equal(_host(tB2)[okc], Xco[okc])
+
+
+# ------------------------------------------------------------------ orders 65..128
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_orders_up_to_128(dtype, layout):
+    """One system per CTA up to n = 128: the fused calls, the factor calls and the solves
+    against the oracle, LU with a singular system, Cholesky (both fills) with an indefinite
+    one."""
+    rng = np.random.default_rng(1111 + layout)
+    for n, nrhs in ((65, 3), (80, 8), (97, 1), (127, 12), (128, 5)):
+        batch = 9
+        Al = rng.standard_normal((batch, n, n)).astype(dtype)
+        Al[2, :, n // 3] = 0
+        A = to_storage(Al, layout)
+        B = to_storage(rng.standard_normal((batch, n, nrhs)).astype(dtype), layout)
+        LUo, Xo, ipo, info_o, tie = oracle.getrf_getrs(A, B, layout, nthreads=NT)
+        LUg, Xg, ipg, infg = parity.gpu_lu(A, B, layout)
+        clean = tie < 0
+        assert np.array_equal(infg[clean], info_o[clean])
+        assert np.array_equal(LUg[clean], LUo[clean]) and np.array_equal(Xg[clean], Xo[clean])
+        assert np.all(Xg[infg != 0] == 0)
+        _lu_case(A, B, layout)
+        G = rng.standard_normal((batch, n, n))
+        S = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dtype)
+        S[4, n // 2, n // 2] = -1.0
+        As = to_storage(S, layout)
+        for fill in (bs.BS_LOWER, bs.BS_UPPER):
+            Lo, Xco, inf_co = oracle.potrf_potrs(As, B, layout, nthreads=NT, fill=fill)
+            tA, tB = _dev(As), _dev(B)
+            info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+            bs.bs_potrf_potrs_batched(tA, tB, info, layout, fill)
+            okc = inf_co == 0
+            assert np.array_equal(_host(info), inf_co)
+            assert np.array_equal(_host(tA)[okc], Lo[okc]) and np.array_equal(_host(tB), Xco)
+            tB2 = _dev(B)
+            bs.bs_potrs_batched(_dev(Lo), tB2, layout, fill)
+            assert np.array_equal(_host(tB2)[okc], Xco[okc])
