@@ -73,6 +73,8 @@ class Oracle:
             "bdsv_solve": [i32, i32, i64, vp, vp, i32],
             "bdmv": [i32, i32, i64, vp, vp, vp, i32],
         }
+        sig["getrf_getrs_ex"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32, i32]
+        sig["potrf_potrs_ex"] = [i32, i32, i32, i32, i64, vp, vp, vp, i32, i32]
         for op, args in sig.items():
             for sfx in ("f32", "f64"):
                 fn = getattr(lib, f"oracle_{op}_{sfx}")
@@ -209,6 +211,37 @@ class Oracle:
             raise ValueError("oracle bdmv rejected its arguments")
         return Y
 
+    # --- contract variants ------------------------------------------------------------
+    def getrf_getrs_ex(self, A, B, layout: int = ROW_MAJOR, tau: float = 1.0, ruda: int = 0,
+                       nthreads: int = 1):
+        """LU + solve with TDLS threshold pivoting (tau) and/or the RUDA status contract.
+        Returns (LU, X, ipiv, info, tie_step)."""
+        A = np.ascontiguousarray(A).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).copy()
+        batch, n = A.shape[0], A.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        ipiv = np.zeros((batch, n), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_getrs_ex_" + _suffix(A.dtype))
+        if fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
+              float(tau), int(ruda), nthreads) != 0:
+            raise ValueError("oracle getrf_getrs_ex rejected its arguments")
+        return A, B, ipiv, info, tie
+
+    def potrf_potrs_ex(self, A, B, layout: int = COL_MAJOR, fill: int = LOWER, ruda: int = 0,
+                       nthreads: int = 1):
+        """Cholesky + solve under the RUDA status contract. Returns (factor, X, info)."""
+        A = np.ascontiguousarray(A).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).copy()
+        batch, n = A.shape[0], A.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_potrf_potrs_ex_" + _suffix(A.dtype))
+        if fn(layout, fill, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(info), int(ruda), nthreads) != 0:
+            raise ValueError("oracle potrf_potrs_ex rejected its arguments")
+        return A, B, info
+
 
 def default() -> Oracle:
     global _default
@@ -256,6 +289,16 @@ def bdsv_solve(strips, xpad, nthreads: int = 1):
 
 def bdmv(strips, xpad, ypad=None, nthreads: int = 1):
     return default().bdmv(strips, xpad, ypad, nthreads)
+
+
+def getrf_getrs_ex(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, ruda: int = 0,
+                   nthreads: int = 1):
+    return default().getrf_getrs_ex(A, B, layout, tau, ruda, nthreads)
+
+
+def potrf_potrs_ex(A, B, layout: int = COL_MAJOR, fill: int = LOWER, ruda: int = 0,
+                   nthreads: int = 1):
+    return default().potrf_potrs_ex(A, B, layout, fill, ruda, nthreads)
 
 
 def _suffix(dtype) -> str:

@@ -72,15 +72,49 @@ inline int64_t at(int layout, int rows, int cols, int r, int c) {
 // 1e-6 relative of each other (a near tie, where a different rounding may legitimately
 // pick the other row), or -1.
 // ---------------------------------------------------------------------------------
+// ---------------------------------------------------------------------------------
+// Contract variants (the option sets of the _ex calls).
+//
+// [TDLS] threshold pivoting, Config.relative_pivot_threshold = tau in (0, 1]: "1 keeps
+// the choice of MAGMA and LAPACK, a smaller value keeps the row in place more often".
+// Reading: with m the magnitude the partial-pivoting search of step k finds (its first
+// maximum, the NaN rules of getrf_getrs_one), the row in place stays the pivot when
+// |a_kk| >= tau * m, the product rounded in T; otherwise the first maximum is taken.
+// tau = 1 is getrf_getrs_one exactly.
+//
+// [RUDA] status contract ("unchanged numerical and failure contract"): 0 success; k > 0
+// the first failing pivot (Cholesky: leading minor); -1 a non-finite input (A or B);
+// -2 (Cholesky) an input matrix that is not symmetric; -3 a non-finite intermediate
+// result (read here: an entry of the factor or of X that is not finite at the end of a
+// sweep that met no failing pivot). A failed system returns its factor and X as zeros
+// and, for LU, every pivot entry as -1. Checks run in the order -1, -2, the sweep, -3.
+// ---------------------------------------------------------------------------------
 template <typename T>
-void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int32_t* info,
-                     int32_t* tie_step) {
+bool all_finite(const T* p, int64_t count) {
+  for (int64_t i = 0; i < count; ++i)
+    if (!std::isfinite(p[i])) return false;
+  return true;
+}
+
+template <typename T>
+void getrf_getrs_ex_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int32_t* info,
+                        int32_t* tie_step, T tau, int ruda) {
   const T floor_v = Limits<T>::floor_();
+  auto fail_ruda = [&](int32_t code) {
+    for (int i = 0; i < n * n; ++i) A[i] = T(0);
+    for (int i = 0; i < n * nrhs; ++i) B[i] = T(0);
+    for (int k = 0; k < n; ++k) ipiv[k] = -1;
+    *info = code;
+  };
+  if (ruda && !(all_finite(A, (int64_t)n * n) && all_finite(B, (int64_t)n * nrhs))) {
+    fail_ruda(-1);
+    if (tie_step) *tie_step = -1;
+    return;
+  }
   int32_t inf = 0;
   int32_t tie = -1;
   auto a = [&](int r, int c) -> T& { return A[at(layout, n, n, r, c)]; };
   auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
-
   for (int k = 0; k < n; ++k) {
     int p = k;
     T best = std::fabs(a(k, k));
@@ -100,8 +134,15 @@ void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int
       }
       if (second >= T(0) && (double)best - (double)second <= 1e-6 * (double)best) tie = k;
     }
+    const T akk = std::fabs(a(k, k));
+    if (p != k && tau < T(1)) {
+      const T bar = tau * best;
+      if (tie < 0 && std::fabs((double)akk - (double)bar) <= 1e-6 * (double)best) tie = k;
+      if (akk >= bar) p = k;   // the row in place is kept
+    }
+    const T mag = (p == k) ? akk : best;
     ipiv[k] = p + 1;
-    const bool ok = best >= floor_v;
+    const bool ok = mag >= floor_v;
     if (!ok && inf == 0) inf = k + 1;
     if (p != k) {
       for (int c = 0; c < n; ++c) {
@@ -132,12 +173,24 @@ void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int
       for (int i = 0; i < k; ++i) b(i, c) = std::fma(-a(i, k), x, b(i, c));
     }
   }
+  if (tie_step) *tie_step = tie;
+  if (ruda && inf == 0 && !(all_finite(A, (int64_t)n * n) && all_finite(B, (int64_t)n * nrhs)))
+    inf = -3;
   if (inf != 0) {
-    for (int r0 = 0; r0 < n; ++r0)
-      for (int c = 0; c < nrhs; ++c) b(r0, c) = T(0);
+    if (ruda) {
+      fail_ruda(inf);
+      return;
+    }
+    for (int i = 0; i < n * nrhs; ++i) B[i] = T(0);
   }
   *info = inf;
-  if (tie_step) *tie_step = tie;
+}
+
+template <typename T>
+void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int32_t* info,
+                     int32_t* tie_step) {
+  // partial pivoting (tau = 1) under the default contract: the steps listed above
+  getrf_getrs_ex_one<T>(layout, n, nrhs, A, B, ipiv, info, tie_step, T(1), 0);
 }
 
 // ---------------------------------------------------------------------------------
@@ -403,6 +456,44 @@ void bdmv_one(int nbr, int bs, const T* strips, const T* xpad, T* ypad) {
     }
 }
 
+template <typename T>
+void potrf_potrs_ex_one(int a_layout, int b_layout, int n, int nrhs, T* A, T* B, int32_t* info,
+                        int ruda) {
+  auto a = [&](int r, int c) -> T& { return A[at(a_layout, n, n, r, c)]; };
+  auto fail_ruda = [&](int32_t code) {
+    for (int r = 0; r < n; ++r)
+      for (int c = 0; c <= r; ++c) a(r, c) = T(0);   // the factor's triangle
+    for (int i = 0; i < n * nrhs; ++i) B[i] = T(0);
+    *info = code;
+  };
+  if (ruda) {
+    if (!(all_finite(A, (int64_t)n * n) && all_finite(B, (int64_t)n * nrhs))) {
+      fail_ruda(-1);
+      return;
+    }
+    for (int r = 0; r < n; ++r)
+      for (int c = 0; c < r; ++c)
+        if (!(a(r, c) == a(c, r))) {
+          fail_ruda(-2);
+          return;
+        }
+  }
+  potrf_potrs_one<T>(a_layout, b_layout, n, nrhs, A, B, info);
+  if (!ruda) return;
+  int32_t inf = *info;
+  if (inf == 0) {
+    bool fin = all_finite(B, (int64_t)n * nrhs);
+    for (int r = 0; r < n && fin; ++r)
+      for (int c = 0; c <= r; ++c)
+        if (!std::isfinite(a(r, c))) {
+          fin = false;
+          break;
+        }
+    if (!fin) inf = -3;
+  }
+  if (inf != 0) fail_ruda(inf);
+}
+
 // Hands contiguous ranges of systems to nthreads workers (1 = the calling thread).
 template <typename F>
 void for_systems(int64_t batch, int nthreads, F&& f) {
@@ -529,6 +620,34 @@ int bdmv_batched(int nbr, int bs, int64_t batch, const T* strips, const T* xpad,
   return 0;
 }
 
+template <typename T>
+int getrf_getrs_ex_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
+                           int32_t* info, int32_t* tie_step, double tau, int ruda,
+                           int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || !(tau > 0.0) ||
+      !(tau <= 1.0))
+    return 1;
+  const T t = static_cast<T>(tau);
+  for_systems(batch, nthreads, [&](int64_t s) {
+    getrf_getrs_ex_one<T>(layout, n, nrhs, A + s * n * n, B + s * n * nrhs, ipiv + s * n,
+                          info + s, tie_step ? tie_step + s : nullptr, t, ruda);
+  });
+  return 0;
+}
+
+template <typename T>
+int potrf_potrs_ex_batched(int layout, int fill, int n, int nrhs, int64_t batch, T* A, T* B,
+                           int32_t* info, int ruda, int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 || batch < 0)
+    return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
+  for_systems(batch, nthreads, [&](int64_t s) {
+    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, A + s * n * n, B + s * n * nrhs, info + s,
+                          ruda);
+  });
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -613,6 +732,26 @@ int oracle_bdsv_solve_f64(int nbr, int bs, int64_t batch, const double* strips, 
 int oracle_bdmv_f64(int nbr, int bs, int64_t batch, const double* strips, const double* xpad,
                     double* ypad, int nthreads) {
   return bdmv_batched<double>(nbr, bs, batch, strips, xpad, ypad, nthreads);
+}
+int oracle_getrf_getrs_ex_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
+                              int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
+                              int ruda, int nthreads) {
+  return getrf_getrs_ex_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau, ruda,
+                                     nthreads);
+}
+int oracle_potrf_potrs_ex_f32(int layout, int fill, int n, int nrhs, int64_t batch, float* A,
+                              float* B, int32_t* info, int ruda, int nthreads) {
+  return potrf_potrs_ex_batched<float>(layout, fill, n, nrhs, batch, A, B, info, ruda, nthreads);
+}
+int oracle_getrf_getrs_ex_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
+                              int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
+                              int ruda, int nthreads) {
+  return getrf_getrs_ex_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau, ruda,
+                                     nthreads);
+}
+int oracle_potrf_potrs_ex_f64(int layout, int fill, int n, int nrhs, int64_t batch, double* A,
+                              double* B, int32_t* info, int ruda, int nthreads) {
+  return potrf_potrs_ex_batched<double>(layout, fill, n, nrhs, batch, A, B, info, ruda, nthreads);
 }
 
 }  // extern "C"

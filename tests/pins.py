@@ -389,6 +389,100 @@ def pin_chol_upper_fill(orc):
                 assert np.all(be <= 8 * n * eps)
 
 
+# ----------------------------------------------------------------- contract variants
+def pin_threshold_pivoting(orc):
+    """TDLS threshold pivoting (relative_pivot_threshold tau): tau = 1 is partial pivoting
+    bit for bit; the hand-worked 2x2 [[0.6, 1], [1, 1]] keeps its first row for tau = 0.5
+    (0.6 >= 0.5 * 1) and swaps for tau = 0.7; on random matrices every multiplier obeys
+    |l_ik| <= 1/tau (the growth bound threshold pivoting exists for) and P A = L U holds to
+    rounding."""
+    rng = _rng(51)
+    for dt in (np.float32, np.float64):
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            A = rng.standard_normal((6, 9, 9)).astype(dt)
+            A[2, :, 4] = 0
+            B = rng.standard_normal((6, 9, 2)).astype(dt)
+            As, Bs = to_storage(A, layout), to_storage(B, layout)
+            r1 = orc.getrf_getrs(As, Bs, layout)
+            r2 = orc.getrf_getrs_ex(As, Bs, layout, tau=1.0)
+            assert all(np.array_equal(x, y) for x, y in zip(r1, r2))
+    A2 = np.array([[[0.6, 1.0], [1.0, 1.0]]])
+    b2 = np.array([[[1.0], [2.0]]])
+    LU, X, ipiv, info, _ = orc.getrf_getrs_ex(A2, b2, ROW_MAJOR, tau=0.5)
+    assert list(ipiv[0]) == [1, 2] and LU[0, 0, 0] == 0.6 and info[0] == 0
+    assert np.allclose(X[0, :, 0], np.linalg.solve(A2[0], b2[0, :, 0]), rtol=1e-14)
+    LU, X, ipiv, info, _ = orc.getrf_getrs_ex(A2, b2, ROW_MAJOR, tau=0.7)
+    assert list(ipiv[0]) == [2, 2] and LU[0, 0, 0] == 1.0
+    # the kept pivot is judged by its own magnitude: 0.9 * FLT_MIN (subnormal) stays in
+    # place against FLT_MIN with tau = 0.5, and is singular (info = 1)
+    fmin = np.finfo(np.float32).tiny
+    A3 = np.array([[[0.9 * fmin, 1.0], [fmin, 1.0]]], np.float32)
+    LU, X, ipiv, info, _ = orc.getrf_getrs_ex(A3, np.ones((1, 2, 1), np.float32), ROW_MAJOR, tau=0.5)
+    assert ipiv[0, 0] == 1 and info[0] == 1
+    for tau in (0.1, 0.5, 0.9):
+        A = rng.standard_normal((20, 12, 12))
+        B = rng.standard_normal((20, 12, 1))
+        LU, X, ipiv, info, tie = orc.getrf_getrs_ex(A, B, ROW_MAJOR, tau=tau)
+        for s in range(20):
+            L, U = unpack_lu(LU[s])
+            assert np.abs(L).max() <= (1.0 / tau) * (1 + 1e-12)
+            PA = A[s][lapack_perm(ipiv[s])]
+            growth = max(np.abs(U).max() / np.abs(A[s]).max(), 1.0)
+            err = np.abs(PA - L @ U).max() / np.abs(A[s]).max()
+            assert err <= 64 * 12 * eps_of(np.float64) * growth, (tau, s, err)
+
+
+def pin_ruda_status_lu(orc):
+    """RUDA status contract on constructed inputs: a NaN in A or an inf in B gives -1; a
+    zero column j gives j + 1; a finite input whose solution overflows (FP32 diag(1e-30, 1),
+    b = (1e10, 1): x_0 = 1e40) gives -3; each failed system returns zeros and ipiv = -1;
+    a system that succeeds is the default contract's bit for bit."""
+    n = 4
+    rng = _rng(52)
+    A = rng.standard_normal((5, n, n)).astype(np.float32) + 3 * np.eye(n, dtype=np.float32)
+    B = rng.standard_normal((5, n, 1)).astype(np.float32)
+    A[0, 1, 2] = np.nan
+    B[1, 3, 0] = np.inf
+    A[2, :, 1] = 0
+    A[3] = np.diag([1e-30, 1.0, 1.0, 1.0]).astype(np.float32)
+    B[3, :, 0] = [1e10, 1.0, 1.0, 1.0]
+    LU, X, ipiv, info, _ = orc.getrf_getrs_ex(A, B, ROW_MAJOR, ruda=1)
+    assert list(info) == [-1, -1, 2, -3, 0], info
+    for s in range(4):
+        assert np.all(LU[s] == 0) and np.all(X[s] == 0) and np.all(ipiv[s] == -1)
+    d = orc.getrf_getrs(A[4:], B[4:], ROW_MAJOR)
+    assert np.array_equal(LU[4], d[0][0]) and np.array_equal(X[4], d[1][0])
+    assert np.array_equal(ipiv[4], d[2][0])
+
+
+def pin_ruda_status_chol(orc):
+    """RUDA status contract for Cholesky: NaN in A or inf in B -> -1; one off-diagonal pair
+    differing in its last bit -> -2 (the symmetry check is exact); A[k][k] = -1 -> k + 1; FP32
+    diag(1e-30, ...) with b = 1e30 overflows y -> -3; failures return the factor's
+    triangle and X as zeros; a success is the default contract's bit for bit."""
+    n = 5
+    rng = _rng(53)
+    G = rng.standard_normal((5, n, n))
+    A = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(np.float32)
+    B = rng.standard_normal((5, n, 2)).astype(np.float32)
+    A = np.concatenate([A, A[4:]])       # system 5: a copy of the good one with inf in B
+    B = np.concatenate([B, B[4:]])
+    B[5, 2, 1] = np.inf
+    A[0, 3, 3] = np.nan
+    A[1, 1, 3] = np.nextafter(A[1, 1, 3], np.float32(np.inf))
+    A[2, 2, 2] = -1.0
+    A[3] = np.diag([1e-30] * n).astype(np.float32)
+    B[3] = 1e30
+    for fill in (0, 1):
+        L, X, info = orc.potrf_potrs_ex(A, B, ROW_MAJOR, fill=fill, ruda=1)
+        assert list(info) == [-1, -2, 3, -3, 0, -1], (fill, info)
+        tri = np.tril_indices(n) if fill == 0 else np.triu_indices(n)
+        for s in (0, 1, 2, 3, 5):
+            assert np.all(L[s][tri] == 0) and np.all(X[s] == 0)
+        d = orc.potrf_potrs(A[4:5], B[4:5], ROW_MAJOR, fill=fill)
+        assert np.array_equal(L[4], d[0][0]) and np.array_equal(X[4], d[1][0])
+
+
 # --------------------------------------------------------------------------- bdsv pins
 def _random_bdsv(rng, batch, nbr, bs, dt=np.float64):
     strips = np.zeros((batch, nbr, bs, 3 * bs), dt)
@@ -673,7 +767,8 @@ BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
               pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
 BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
-ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS
+VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol]
+ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS
 
 
 def failing_pins(orc, pins=ALL_PINS):

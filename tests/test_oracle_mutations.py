@@ -38,14 +38,14 @@ MUTATIONS = [
      "      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));\n    }\n  }\n  for (int k = n - 1",
      "    }\n  }\n  for (int k = n - 1"),
     ("lu_back_subst_transposed",
-     "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n  if (inf != 0) {",
-     "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n  if (inf != 0) {"),
-    ("lu_floor_is_zero", "const bool ok = best >= floor_v;", "const bool ok = best > T(0);"),
+     "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n  if (tie_step) *tie_step = tie;",
+     "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n  if (tie_step) *tie_step = tie;"),
+    ("lu_floor_is_zero", "const bool ok = mag >= floor_v;", "const bool ok = mag > T(0);"),
     ("lu_info_off_by_one", "if (!ok && inf == 0) inf = k + 1;", "if (!ok && inf == 0) inf = k;"),
     ("lu_info_last_not_first", "if (!ok && inf == 0) inf = k + 1;", "if (!ok) inf = k + 1;"),
     ("lu_failed_x_not_zeroed",
-     "      for (int c = 0; c < nrhs; ++c) b(r0, c) = T(0);\n  }\n  *info = inf;\n  if (tie_step)",
-     "      ;\n  }\n  *info = inf;\n  if (tie_step)"),
+     "    for (int i = 0; i < n * nrhs; ++i) B[i] = T(0);\n  }\n  *info = inf;",
+     "  }\n  *info = inf;"),
     ("chol_sqrt_dropped", "const T l = std::sqrt(d);\n    a(k, k) = l;",
      "const T l = d;\n    a(k, k) = l;"),
     ("chol_update_writes_upper",
@@ -93,6 +93,18 @@ MUTATIONS = [
     ("chol_upper_fill_b_transposed",
      "    potrf_potrs_one<T>(a_layout, layout, n, nrhs,",
      "    potrf_potrs_one<T>(a_layout, a_layout, n, nrhs,"),
+    ("threshold_comparison_flipped", "if (akk >= bar) p = k;   // the row in place is kept",
+     "if (akk <= bar) p = k;   // the row in place is kept"),
+    ("threshold_pivot_magnitude_of_max", "const T mag = (p == k) ? akk : best;",
+     "const T mag = best;"),
+    ("ruda_pivots_not_minus_one", "    for (int k = 0; k < n; ++k) ipiv[k] = -1;\n", ""),
+    ("ruda_overflow_not_reported", "    inf = -3;\n  if (inf != 0) {\n    if (ruda) {",
+     "    inf = 0;\n  if (inf != 0) {\n    if (ruda) {"),
+    ("ruda_symmetry_check_trivial", "        if (!(a(r, c) == a(c, r))) {",
+     "        if (!(a(r, c) == a(r, c))) {"),
+    ("ruda_chol_input_check_skips_b",
+     "    if (!(all_finite(A, (int64_t)n * n) && all_finite(B, (int64_t)n * nrhs))) {\n      fail_ruda(-1);\n      return;\n    }\n    for (int r = 0;",
+     "    if (!(all_finite(A, (int64_t)n * n))) {\n      fail_ruda(-1);\n      return;\n    }\n    for (int r = 0;"),
     ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
      "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
     ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
