@@ -24,12 +24,19 @@ BS_OK, BS_ERR_INVALID_ARG, BS_ERR_UNSUPPORTED, BS_ERR_CUDA = 0, 1, 2, 3
 BS_FP32, BS_FP64 = 0, 1
 BS_ROW_MAJOR, BS_COL_MAJOR = 0, 1
 BS_LOWER, BS_UPPER = 0, 1
+BS_CONTRACT_DEFAULT, BS_CONTRACT_RUDA = 0, 1
+
+
+class Options(ctypes.Structure):
+    """bs_options: TDLS pivot threshold and the status contract (see bsolve.h)."""
+    _fields_ = [("pivot_threshold", ctypes.c_double), ("status_contract", ctypes.c_int)]
 ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
 
 EXPORTED = (
     "bs_getrf_getrs_batched", "bs_potrf_potrs_batched", "bs_bdsv_batched",
     "bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched", "bs_potrs_batched",
     "bs_bdsv_factor_batched", "bs_bdsv_solve_batched", "bs_bdmv_batched",
+    "bs_getrf_getrs_batched_ex", "bs_potrf_potrs_batched_ex",
     "bs_status_string", "bs_last_cuda_error", "bs_getrf_getrs_supported",
     "bs_potrf_potrs_supported", "bs_bdsv_supported", "bs_version",
 )
@@ -70,6 +77,12 @@ def lib() -> ctypes.CDLL:
             L.bs_bdsv_factor_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp]
             L.bs_bdsv_solve_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp]
             L.bs_bdmv_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp]
+            L.bs_getrf_getrs_batched_ex.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp,
+                                                    ctypes.POINTER(Options), vp]
+            L.bs_potrf_potrs_batched_ex.argtypes = [i32, i32, i32, i32, i32, i64, vp, vp, vp,
+                                                    ctypes.POINTER(Options), vp]
+            L.bs_getrf_getrs_batched_ex.restype = i32
+            L.bs_potrf_potrs_batched_ex.restype = i32
             for name in ("bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched",
                          "bs_potrs_batched", "bs_bdsv_factor_batched", "bs_bdsv_solve_batched",
                          "bs_bdmv_batched"):
@@ -210,3 +223,28 @@ def bs_bdmv_batched(strips, x_padded, y_padded, stream=None) -> None:
     st = lib().bs_bdmv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
                                _ptr(y_padded), _stream(stream))
     _check(st, "bs_bdmv_batched")
+
+
+# --------------------------------------------------------------- contract variants
+def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
+                              pivot_threshold: float = 1.0,
+                              status_contract: int = BS_CONTRACT_DEFAULT, stream=None) -> None:
+    """LU + solve with TDLS threshold pivoting and/or the RUDA status contract."""
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    opts = Options(float(pivot_threshold), int(status_contract))
+    st = lib().bs_getrf_getrs_batched_ex(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
+                                         _ptr(ipiv), _ptr(info), ctypes.byref(opts),
+                                         _stream(stream))
+    _check(st, "bs_getrf_getrs_batched_ex")
+
+
+def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = BS_LOWER,
+                              status_contract: int = BS_CONTRACT_DEFAULT, stream=None) -> None:
+    """Cholesky + solve under the RUDA status contract."""
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    opts = Options(1.0, int(status_contract))
+    st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
+                                         _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
+    _check(st, "bs_potrf_potrs_batched_ex")

@@ -326,6 +326,58 @@ bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_size, in
   return from_cuda(e);
 }
 
+bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                    int64_t batch, void* A, void* B, int32_t* ipiv,
+                                    int32_t* info, const bs_options* opts, void* stream) {
+  const double tau = opts ? opts->pivot_threshold : 1.0;
+  const int contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
+  if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
+  if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
+  if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT)
+    return bs_getrf_getrs_batched(dtype, layout, n, nrhs, batch, A, B, ipiv, info, stream);
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int ruda = contract == BS_CONTRACT_RUDA;
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_lu_smem_ex<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                             static_cast<float*>(B), ipiv, info, tau, ruda, s)
+          : bsolve::launch_lu_smem_ex<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                              static_cast<double*>(B), ipiv, info, tau, ruda, s);
+  return from_cuda(e);
+}
+
+bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                    int nrhs, int64_t batch, void* A, void* B, int32_t* info,
+                                    const bs_options* opts, void* stream) {
+  const double tau = opts ? opts->pivot_threshold : 1.0;
+  const int contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
+  if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
+  if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
+  if (contract == BS_CONTRACT_DEFAULT)   // the threshold has no meaning without pivoting
+    return bs_potrf_potrs_batched(dtype, layout, fill, n, nrhs, batch, A, B, info, stream);
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_chol_smem_ex<float>(chol_layouts(layout, fill), n, nrhs, batch,
+                                               static_cast<float*>(A), static_cast<float*>(B),
+                                               info, 1, s)
+          : bsolve::launch_chol_smem_ex<double>(chol_layouts(layout, fill), n, nrhs, batch,
+                                                static_cast<double*>(A),
+                                                static_cast<double*>(B), info, 1, s);
+  return from_cuda(e);
+}
+
 const char* bs_status_string(bs_status status) {
   switch (status) {
     case BS_OK: return "BS_OK";

@@ -17,6 +17,13 @@ template <typename T>
 cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                            int32_t* ipiv, int32_t* info, cudaStream_t stream);
 
+// The same with the options of the _ex calls: TDLS threshold tau in (0, 1], RUDA status
+// contract (ruda != 0); any 1 <= n <= 128.
+template <typename T>
+cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                              int32_t* ipiv, int32_t* info, double tau, int ruda,
+                              cudaStream_t stream);
+
 // Solve with a stored factor: getrs (L\U and the 1-based swap sequence of getrf) and
 // potrs (Cholesky factor), 1 <= n <= 128.
 // Any nrhs >= 1 (a register tier's worth at a time). zinfo (may be null): X = 0 where
@@ -35,6 +42,12 @@ cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L,
 template <typename T>
 cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                              int32_t* info, cudaStream_t stream);
+
+// The same under the RUDA status contract (ruda != 0): -1 non-finite input, -2 input
+// not symmetric (the whole matrix is read), -3 non-finite result; failures zeroed.
+template <typename T>
+cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                                int32_t* info, int ruda, cudaStream_t stream);
 
 // Lower Cholesky + solve, sixteen systems per block in lockstep, 1 <= n <= 32.
 template <typename T>

@@ -17,6 +17,10 @@
 // also give the SM enough warps to cover each system's serial pivot phase. The serial
 // warp rotates with the step and the block, so the serial work of the blocks on an SM is
 // spread over its four sub-partitions.
+// Options of the _ex calls (run here for every n): TDLS threshold pivoting (the row in
+// place stays when |a_kk| >= tau * m, m the magnitude the search found) and the RUDA
+// status contract (-1 for a non-finite input before the sweep, -3 for a non-finite factor
+// or solution after it, failed systems returned as zeros with pivots -1).
 // Back substitution runs by blocks of four rows: one warp solves the 4 x 4 diagonal block,
 // then all warps apply its four columns to every row above, each element taking the four
 // updates in decreasing column order -- the oracle's order, so the arithmetic is the
@@ -36,7 +40,8 @@ __host__ __device__ inline int odd_pitch(int w) { return w | 1; }
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
-              T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info) {
+              T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info,
+              T tau, int ruda) {
   using Key = typename Traits<T>::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x;
@@ -76,6 +81,22 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   cp_async_wait_all();
   __syncthreads();
 
+  // RUDA status contract: a non-finite input fails the system with -1 before the sweep
+  if (ruda) {
+    int bad = 0;
+    for (int e = tid; e < n * W; e += kThreads) {
+      const int i = e / W, j = e - i * W;
+      bad |= !isfinite(M[i * P + j]);
+    }
+    if (__syncthreads_or(bad)) {
+      for (int e = tid; e < n * n; e += kThreads) A[e] = T(0);
+      for (int e = tid; e < n * nrhs; e += kThreads) B[e] = T(0);
+      for (int k = tid; k < n; k += kThreads) ipiv[s * n + k] = -1;
+      if (tid == 0) info[s] = -1;
+      return;
+    }
+  }
+
   for (int k = 0; k < n; ++k) {
     // the serial part of step k runs on a warp that rotates with the step and the block:
     // warp w runs on SM sub-partition w % 4, and a fixed warp would put every block's
@@ -100,8 +121,18 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
           bi = oi;
         }
       }
-      const int p = bi;
-      const bool ok = pivot_ok<T>(best);
+      int p = bi;
+      Key pkey = best;
+      if (p != k && tau < T(1)) {
+        // threshold pivoting: the row in place stays when |a_kk| >= tau * m, m the
+        // magnitude the search found (not a NaN: a NaN in place would have won)
+        const T akk = M[k * P + k];
+        if (fabs(akk) >= tau * pivot_from_key<T>(best, 0u)) {
+          p = k;
+          pkey = pivot_key<T>(akk, true);
+        }
+      }
+      const bool ok = pivot_ok<T>(pkey);
       if (lane == 0) {
         piv[k] = p + 1;
         if (!ok && s_info == 0) s_info = k + 1;
@@ -169,11 +200,25 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     __syncthreads();
   }
 
-  const bool zero_x = s_info != 0;
+  // RUDA status contract: a non-finite factor or solution after a sweep without a failing
+  // pivot is -3; a failed system returns zeros and pivots -1
+  int status = s_info;
+  if (ruda) {
+    int bad = 0;
+    if (status == 0) {
+      for (int e = tid; e < n * W; e += kThreads) {
+        const int i = e / W, j = e - i * W;
+        bad |= !isfinite(M[i * P + j]);
+      }
+    }
+    if (__syncthreads_or(bad)) status = -3;
+  }
+  const bool zero_all = ruda && status != 0;
+  const bool zero_x = status != 0;
   if (layout == kRowMajor) {
     for (int e = tid; e < n * n; e += kThreads) {
       const int i = e / n, j = e - i * n;
-      A[e] = M[i * P + j];
+      A[e] = zero_all ? T(0) : M[i * P + j];
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int i = e / nrhs, c = e - i * nrhs;
@@ -182,15 +227,15 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   } else {
     for (int e = tid; e < n * n; e += kThreads) {
       const int j = e / n, i = e - j * n;
-      A[e] = M[i * P + j];
+      A[e] = zero_all ? T(0) : M[i * P + j];
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int c = e / n, i = e - c * n;
       B[e] = zero_x ? T(0) : M[i * P + n + c];
     }
   }
-  for (int k = tid; k < n; k += kThreads) ipiv[s * n + k] = piv[k];
-  if (tid == 0) info[s] = s_info;
+  for (int k = tid; k < n; k += kThreads) ipiv[s * n + k] = zero_all ? -1 : piv[k];
+  if (tid == 0) info[s] = status;
 }
 
 }  // namespace
@@ -202,8 +247,9 @@ size_t lu_cta_bytes(int n, int nrhs, int elem_size) {
 }
 
 template <typename T>
-cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                           int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                              int32_t* ipiv, int32_t* info, double tau, int ruda,
+                              cudaStream_t stream) {
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = lu_cta_bytes(n, nrhs, sizeof(T));
   cudaError_t e = cudaFuncSetAttribute(lu_cta_kernel<T>,
@@ -211,13 +257,23 @@ cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* 
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   lu_cta_kernel<T><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
-      n, nrhs, layout, batch, A, B, ipiv, info);
+      n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                           int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  return launch_lu_smem_ex<T>(layout, n, nrhs, batch, A, B, ipiv, info, 1.0, 0, stream);
 }
 
 template cudaError_t launch_lu_smem<float>(int, int, int, int64_t, float*, float*, int32_t*,
                                            int32_t*, cudaStream_t);
 template cudaError_t launch_lu_smem<double>(int, int, int, int64_t, double*, double*, int32_t*,
                                             int32_t*, cudaStream_t);
+template cudaError_t launch_lu_smem_ex<float>(int, int, int, int64_t, float*, float*, int32_t*,
+                                              int32_t*, double, int, cudaStream_t);
+template cudaError_t launch_lu_smem_ex<double>(int, int, int, int64_t, double*, double*,
+                                               int32_t*, int32_t*, double, int, cudaStream_t);
 
 }  // namespace bsolve

@@ -10,7 +10,10 @@
 //
 // Cholesky: right-looking lower factorization (cuSolverDx docs, "Cholesky
 // Factorization": only the lower triangle is read and written), the forward solve
-// folded in, then L^T x = y.
+// folded in, then L^T x = y. Under the RUDA status contract of the _ex call (RUDA docs,
+// "ruSOLVER: small-matrix kernel optimisation", unchanged failure contract) the whole
+// matrix is loaded so that its symmetry can be checked: -1 a non-finite input, -2 an input
+// that is not symmetric, -3 a non-finite result; failures return zeros.
 // The arithmetic is the CPU oracle's, operation by operation.
 #include "common.cuh"
 #include "kernels.h"
@@ -72,7 +75,7 @@ __device__ __forceinline__ void store_system(T* __restrict__ A, T* __restrict__ 
 template <typename T>
 __global__ void __launch_bounds__(32)
 chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
-                 T* __restrict__ B, int32_t* __restrict__ info) {
+                 T* __restrict__ B, int32_t* __restrict__ info, int ruda) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x;
   const int64_t s = blockIdx.x;
@@ -83,11 +86,24 @@ chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
 
   A += s * n * n;
   B += s * n * nrhs;
-  load_system<T>(A, B, M, n, nrhs, P, layouts, true, lane);
+  // the RUDA status contract reads the whole matrix: its symmetry is checked
+  load_system<T>(A, B, M, n, nrhs, P, layouts, !ruda, lane);
   __syncwarp();
 
   int inf = 0;
-  for (int k = 0; k < n; ++k) {
+  if (ruda) {
+    bool bad = false, asym = false;
+    const int W = n + nrhs;
+    for (int e = lane; e < n * W; e += 32) {
+      const int i = e / W, j = e - i * W;
+      const T v = M[i * P + j];
+      bad = bad || !isfinite(v);
+      if (j < i) asym = asym || !(v == M[j * P + i]);
+    }
+    if (__any_sync(0xFFFFFFFFu, bad)) inf = -1;
+    else if (__any_sync(0xFFFFFFFFu, asym)) inf = -2;
+  }
+  for (int k = 0; k < n && inf == 0; ++k) {
     const T d = M[k * P + k];
     if (!(d > T(0))) {
       inf = k + 1;
@@ -143,6 +159,25 @@ chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
       __syncwarp();
     }
   }
+  if (ruda) {
+    // -3: a non-finite factor or solution after a sweep without a failing minor; a failed
+    // system returns the factor's triangle and X as zeros
+    if (inf == 0) {
+      bool bad = false;
+      for (int e = lane; e < n * (n + nrhs); e += 32) {
+        const int i = e / (n + nrhs), j = e - i * (n + nrhs);
+        if (j <= i || j >= n) bad = bad || !isfinite(M[i * P + j]);
+      }
+      if (__any_sync(0xFFFFFFFFu, bad)) inf = -3;
+    }
+    if (inf != 0) {
+      for (int e = lane; e < n * n; e += 32) {
+        const int i = e / n, j = e - i * n;
+        if (j <= i) M[i * P + j] = T(0);
+      }
+    }
+    __syncwarp();
+  }
   store_system<T>(A, B, M, n, nrhs, P, layouts, true, inf != 0, lane);
   if (lane == 0) info[s] = inf;
 }
@@ -155,8 +190,8 @@ size_t chol_smem_bytes(int n, int nrhs, int elem_size) {
 }
 
 template <typename T>
-cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                             int32_t* info, cudaStream_t stream) {
+cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                                int32_t* info, int ruda, cudaStream_t stream) {
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = chol_smem_bytes(n, nrhs, sizeof(T));
   cudaError_t e = cudaFuncSetAttribute(chol_smem_kernel<T>,
@@ -164,10 +199,21 @@ cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   chol_smem_kernel<T><<<static_cast<unsigned>(batch), 32, bytes, stream>>>(n, nrhs, layout,
-                                                                           batch, A, B, info);
+                                                                           batch, A, B, info,
+                                                                           ruda);
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                             int32_t* info, cudaStream_t stream) {
+  return launch_chol_smem_ex<T>(layout, n, nrhs, batch, A, B, info, 0, stream);
+}
+
+template cudaError_t launch_chol_smem_ex<float>(int, int, int, int64_t, float*, float*, int32_t*,
+                                                int, cudaStream_t);
+template cudaError_t launch_chol_smem_ex<double>(int, int, int, int64_t, double*, double*,
+                                                 int32_t*, int, cudaStream_t);
 template cudaError_t launch_chol_smem<float>(int, int, int, int64_t, float*, float*, int32_t*,
                                              cudaStream_t);
 template cudaError_t launch_chol_smem<double>(int, int, int, int64_t, double*, double*,

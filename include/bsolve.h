@@ -136,6 +136,45 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
                           void* strips, void* x_padded, int32_t* info, void* stream);
 
 /*
+ * Contract variants of the two fused dense calls.
+ *
+ * Source: TDLS API, "solver_static.hpp File Reference", Detailed Description
+ * (Config.relative_pivot_threshold: 1 keeps the choice of MAGMA and LAPACK, a smaller value
+ * keeps the row in place more often); RUDA docs, "ruSOLVER: small-matrix kernel
+ * optimisation" (unchanged numerical and failure contract: status codes and failed
+ * outputs).
+ *
+ *   pivot_threshold  tau in (0, 1] (LU only). At step k, with m the magnitude partial
+ *                    pivoting finds, the row in place stays the pivot when
+ *                    |a_kk| >= tau * m (the product rounded in the dtype); otherwise the
+ *                    first maximum is taken. 1 = partial pivoting. Every multiplier then
+ *                    obeys |l_ik| <= 1/tau.
+ *   status_contract  BS_CONTRACT_DEFAULT: as the plain calls. BS_CONTRACT_RUDA: info is
+ *                    0 success, k > 0 the first failing pivot or minor, -1 a non-finite
+ *                    entry in A or B, -2 (Cholesky) A not exactly symmetric (the whole
+ *                    matrix is read), -3 a non-finite entry of the factor or X after a
+ *                    sweep without a failing pivot; a failed system (info != 0) returns
+ *                    its factor (Cholesky: the fill triangle) and X as zeros and, for LU,
+ *                    every ipiv entry as -1.
+ * opts == NULL or default options run the plain call. Other options run one system per
+ * CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the CPU oracle's bit for
+ * bit. A threshold outside (0, 1] or an unknown contract is BS_ERR_INVALID_ARG.
+ */
+typedef enum { BS_CONTRACT_DEFAULT = 0, BS_CONTRACT_RUDA = 1 } bs_contract;
+
+typedef struct {
+  double pivot_threshold; /* in (0, 1]; 1 = partial pivoting */
+  int status_contract;    /* a bs_contract */
+} bs_options;
+
+BS_API bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                           int64_t batch, void* A, void* B, int32_t* ipiv,
+                                           int32_t* info, const bs_options* opts, void* stream);
+BS_API bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                           int nrhs, int64_t batch, void* A, void* B,
+                                           int32_t* info, const bs_options* opts, void* stream);
+
+/*
  * Factor once, solve per right-hand side: the two halves of the fused calls above.
  *
  * Source: GLASS API reference, "Block-tridiagonal Ops", "Direct solve (glass::bdsv)"

@@ -139,6 +139,29 @@ def test_split_argument_errors(lib):
     assert f(bs.BS_FP64, 32, 8, 4, A, B, A, None) == bs.BS_ERR_INVALID_ARG          # y over strips
 
 
+def test_contract_variant_argument_errors(lib):
+    """Options are checked before anything else: a threshold outside (0, 1] or an unknown
+    contract is an argument error; options other than the defaults hold 8 right-hand
+    sides at most."""
+    import ctypes
+    A, B, P, I = FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000
+    f = lib.bs_getrf_getrs_batched_ex
+    o = lambda tau, c: ctypes.byref(bs.Options(tau, c))  # noqa: E731
+    assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, o(0.5, 0), None) == bs.BS_OK
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, o(0.0, 0), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, o(1.5, 0), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, o(float("nan"), 0), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, o(1.0, 7), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, o(0.5, 0), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 129, 4, 5, A, B, P, I, o(0.5, 1), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 4, 5, None, B, P, I, o(0.5, 1), None) == bs.BS_ERR_INVALID_ARG
+    g = lib.bs_potrf_potrs_batched_ex
+    assert g(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None, o(1.0, 1), None) == bs.BS_OK
+    assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, o(1.0, 2), None) == bs.BS_ERR_INVALID_ARG
+    assert g(bs.BS_FP64, 1, 0, 32, 9, 5, A, B, I, o(1.0, 1), None) == bs.BS_ERR_UNSUPPORTED
+    assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, None, I, o(1.0, 1), None) == bs.BS_ERR_INVALID_ARG
+
+
 def test_binding_refuses_host_tensors():
     import torch
     A = torch.zeros((2, 4, 4))

@@ -1,0 +1,118 @@
+"""Contract variants of the fused calls (TDLS threshold pivoting, RUDA status contract):
+the CUDA path through the C ABI against the CPU oracle, bit for bit.
+
+Threshold pivoting over the orders 1..128 with both layouts and dtypes (compared on the
+systems where the oracle met no near tie, pivot choice included); the RUDA contract on
+constructed systems for every status code (-1 non-finite input, -2 non-symmetric,
+k > 0 failing pivot or minor, -3 overflow), both fills for Cholesky.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import dense_linear_solvers_gb300 as bs
+import oracle
+from gen.workloads import COL_MAJOR, ROW_MAJOR, to_storage
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+NT = os.cpu_count() or 1
+SENT = parity.SENTINEL
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bs.lib()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def _host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def gpu_lu_ex(A, B, layout, tau, contract):
+    tA, tB = _dev(A), _dev(B)
+    batch, n = A.shape[0], A.shape[1]
+    ipiv = torch.full((batch, n), SENT, dtype=torch.int32, device="cuda")
+    info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+    bs.bs_getrf_getrs_batched_ex(tA, tB, ipiv, info, layout, tau, contract)
+    return _host(tA), _host(tB), _host(ipiv), _host(info)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_threshold_pivoting(dtype, layout):
+    rng = np.random.default_rng(1212 + layout)
+    for n in list(range(1, 40)) + [64, 100, 128]:
+        for tau in (0.3, 0.8):
+            nrhs = int(rng.integers(1, 9))
+            Al = rng.standard_normal((17, n, n)).astype(dtype)
+            if n > 1:
+                Al[3, :, n // 2] = 0
+            A = to_storage(Al, layout)
+            B = to_storage(rng.standard_normal((17, n, nrhs)).astype(dtype), layout)
+            LUo, Xo, ipo, info_o, tie = oracle.getrf_getrs_ex(A, B, layout, tau=tau, nthreads=NT)
+            LUg, Xg, ipg, infg = gpu_lu_ex(A, B, layout, tau, bs.BS_CONTRACT_DEFAULT)
+            clean = tie < 0
+            assert np.array_equal(infg[clean], info_o[clean]), (n, tau)
+            assert np.array_equal(ipg[clean], ipo[clean]), (n, tau)
+            assert np.array_equal(LUg[clean], LUo[clean]) and np.array_equal(Xg[clean], Xo[clean])
+            assert np.all(Xg[infg != 0] == 0)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_ruda_status_lu(dtype, layout):
+    rng = np.random.default_rng(1313 + layout)
+    big = np.finfo(dtype).max
+    for n in (2, 4, 16, 40, 128):
+        Al = rng.standard_normal((6, n, n)).astype(dtype) + 3 * np.eye(n, dtype=dtype)
+        Bl = rng.standard_normal((6, n, 2)).astype(dtype)
+        Al[0, n - 1, 0] = np.nan
+        Bl[1, 0, 1] = -np.inf
+        Al[2, :, n - 1] = 0
+        Al[3] = np.eye(n, dtype=dtype)
+        Al[3, 0, 0] = np.finfo(dtype).tiny * 2
+        Bl[3, 0, 0] = big / 2
+        A, B = to_storage(Al, layout), to_storage(Bl, layout)
+        LUo, Xo, ipo, info_o, tie = oracle.getrf_getrs_ex(A, B, layout, ruda=1)
+        LUg, Xg, ipg, infg = gpu_lu_ex(A, B, layout, 1.0, bs.BS_CONTRACT_RUDA)
+        assert list(info_o) == [-1, -1, n, -3, 0, 0], info_o
+        assert np.array_equal(infg, info_o)
+        assert np.array_equal(ipg, ipo) and np.array_equal(LUg, LUo) and np.array_equal(Xg, Xo)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_ruda_status_cholesky(dtype, layout):
+    rng = np.random.default_rng(1414 + layout)
+    for n in (1, 3, 16, 33, 128):
+        G = rng.standard_normal((7, n, n))
+        Al = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dtype)
+        Bl = rng.standard_normal((7, n, 3)).astype(dtype)
+        Al[0, n - 1, n - 1] = np.nan
+        Bl[1, n - 1, 2] = np.inf
+        if n > 1:
+            Al[2, n - 1, 0] = np.nextafter(Al[2, n - 1, 0], dtype(np.inf))
+        Al[3, n - 1, n - 1] = -1.0
+        Al[4] = np.diag(np.full(n, np.finfo(dtype).tiny * 4)).astype(dtype)
+        Bl[4] = np.finfo(dtype).max / 8
+        A, B = to_storage(Al, layout), to_storage(Bl, layout)
+        for fill in (bs.BS_LOWER, bs.BS_UPPER):
+            Lo, Xo, info_o = oracle.potrf_potrs_ex(A, B, layout, fill=fill, ruda=1)
+            tA, tB = _dev(A), _dev(B)
+            info = torch.full((7,), SENT, dtype=torch.int32, device="cuda")
+            bs.bs_potrf_potrs_batched_ex(tA, tB, info, layout, fill, bs.BS_CONTRACT_RUDA)
+            want = [-1, -1, -2 if n > 1 else 0, n, -3, 0, 0]
+            assert list(info_o) == want, (n, fill, info_o)
+            assert np.array_equal(_host(info), info_o)
+            assert np.array_equal(_host(tA), Lo, equal_nan=True)
+            assert np.array_equal(_host(tB), Xo)
