@@ -75,6 +75,7 @@ class Oracle:
         }
         sig["getrf_getrs_ex"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32, i32]
         sig["potrf_potrs_ex"] = [i32, i32, i32, i32, i64, vp, vp, vp, i32, i32]
+        sig["getrf_getrs_mirror"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32]
         for op, args in sig.items():
             for sfx in ("f32", "f64"):
                 fn = getattr(lib, f"oracle_{op}_{sfx}")
@@ -242,6 +243,24 @@ class Oracle:
             raise ValueError("oracle potrf_potrs_ex rejected its arguments")
         return A, B, info
 
+    def getrf_getrs_mirror(self, A, B, layout: int = ROW_MAJOR, tau: float = 1.0,
+                           nthreads: int = 1):
+        """TDLS row-major reading: factor S (the stored array read column-major, S = A^T for
+        row-major storage), then U^T z = b, L^T w = z, x = P^T w. Returns
+        (S factored in the stored array, X, ipiv, info, tie_step)."""
+        A = np.ascontiguousarray(A).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).copy()
+        batch, n = A.shape[0], A.shape[1]
+        nrhs = B.shape[-1] if layout == ROW_MAJOR else B.shape[-2]
+        ipiv = np.zeros((batch, n), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_getrs_mirror_" + _suffix(A.dtype))
+        if fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
+              float(tau), nthreads) != 0:
+            raise ValueError("oracle getrf_getrs_mirror rejected its arguments")
+        return A, B, ipiv, info, tie
+
 
 def default() -> Oracle:
     global _default
@@ -299,6 +318,10 @@ def getrf_getrs_ex(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, ruda: int = 
 def potrf_potrs_ex(A, B, layout: int = COL_MAJOR, fill: int = LOWER, ruda: int = 0,
                    nthreads: int = 1):
     return default().potrf_potrs_ex(A, B, layout, fill, ruda, nthreads)
+
+
+def getrf_getrs_mirror(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, nthreads: int = 1):
+    return default().getrf_getrs_mirror(A, B, layout, tau, nthreads)
 
 
 def _suffix(dtype) -> str:

@@ -25,6 +25,7 @@
 //   [cuSolverDx] cuSolverDx docs, "Cholesky Factorization" (POTRF).
 #include <cfloat>
 #include <cmath>
+#include <utility>
 #include <cstdint>
 #include <cstring>
 #include <thread>
@@ -456,6 +457,38 @@ void bdmv_one(int nbr, int bs, const T* strips, const T* xpad, T* ypad) {
     }
 }
 
+// [TDLS] the row-major reading: the solver factors S, the stored matrix read column-major
+// (S = A^T for row-major storage): P S = L U, so A = U^T L^T P, and the solve is the
+// mirror of the default one: U^T z = b (column by column: z_k = b_k * r_k, then
+// b_j -= u_kj z_k for j > k, in increasing k; r_k as in getrs), L^T w = z (unit
+// diagonal, from the last: b_i -= l_ki w_k for i < k, in decreasing k), x = P^T w (the
+// swaps applied to w in reverse step order). The factor is getrf_getrs_ex_one's on the
+// memory read column-major; B keeps its storage order. Under column-major storage S = A
+// and TDLS's solve is the default one.
+template <typename T>
+void getrs_mirror_one(int b_layout, int n, int nrhs, const T* S, const int32_t* ipiv, T* B) {
+  const T floor_v = Limits<T>::floor_();
+  auto s_ = [&](int r, int c) -> T { return S[at(1, n, n, r, c)]; };
+  auto b = [&](int r, int c) -> T& { return B[at(b_layout, n, nrhs, r, c)]; };
+  for (int k = 0; k < n; ++k) {
+    const T piv = s_(k, k);
+    const T r = (std::fabs(piv) >= floor_v) ? T(1) / piv : T(1);
+    for (int c = 0; c < nrhs; ++c) {
+      const T z = b(k, c) * r;
+      b(k, c) = z;
+      for (int j = k + 1; j < n; ++j) b(j, c) = std::fma(-s_(k, j), z, b(j, c));
+    }
+  }
+  for (int k = n - 1; k >= 0; --k)
+    for (int c = 0; c < nrhs; ++c)
+      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c), b(i, c));
+  for (int k = n - 1; k >= 0; --k) {  // x = P^T w: step k's interchange undone
+    const int q = ipiv[k] - 1;
+    if (q == k) continue;
+    for (int c = 0; c < nrhs; ++c) std::swap(b(k, c), b(q, c));
+  }
+}
+
 template <typename T>
 void potrf_potrs_ex_one(int a_layout, int b_layout, int n, int nrhs, T* A, T* B, int32_t* info,
                         int ruda) {
@@ -636,6 +669,34 @@ int getrf_getrs_ex_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* 
 }
 
 template <typename T>
+int getrf_getrs_mirror_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                               int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
+                               int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || !(tau > 0.0) ||
+      !(tau <= 1.0))
+    return 1;
+  const T t = static_cast<T>(tau);
+  for_systems(batch, nthreads, [&](int64_t s) {
+    T* As = A + s * n * n;
+    T* Bs = B + s * n * nrhs;
+    int32_t* inf = info + s;
+    if (layout == 1) {
+      // column-major storage: S = A and the solve is the default one
+      getrf_getrs_ex_one<T>(1, n, nrhs, As, Bs, ipiv + s * n, inf,
+                            tie_step ? tie_step + s : nullptr, t, 0);
+      return;
+    }
+    // S = the stored array read column-major (A^T), factored in place; B row-major
+    getrf_getrs_ex_one<T>(1, n, 0, As, nullptr, ipiv + s * n, inf,
+                          tie_step ? tie_step + s : nullptr, t, 0);
+    getrs_mirror_one<T>(layout, n, nrhs, As, ipiv + s * n, Bs);
+    if (*inf != 0)
+      for (int i = 0; i < n * nrhs; ++i) Bs[i] = T(0);
+  });
+  return 0;
+}
+
+template <typename T>
 int potrf_potrs_ex_batched(int layout, int fill, int n, int nrhs, int64_t batch, T* A, T* B,
                            int32_t* info, int ruda, int nthreads) {
   if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 || batch < 0)
@@ -752,6 +813,18 @@ int oracle_getrf_getrs_ex_f64(int layout, int n, int nrhs, int64_t batch, double
 int oracle_potrf_potrs_ex_f64(int layout, int fill, int n, int nrhs, int64_t batch, double* A,
                               double* B, int32_t* info, int ruda, int nthreads) {
   return potrf_potrs_ex_batched<double>(layout, fill, n, nrhs, batch, A, B, info, ruda, nthreads);
+}
+int oracle_getrf_getrs_mirror_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
+                                  int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
+                                  int nthreads) {
+  return getrf_getrs_mirror_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
+                                         nthreads);
+}
+int oracle_getrf_getrs_mirror_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
+                                  int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
+                                  int nthreads) {
+  return getrf_getrs_mirror_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
+                                         nthreads);
 }
 
 }  // extern "C"

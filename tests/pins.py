@@ -483,6 +483,40 @@ def pin_ruda_status_chol(orc):
         assert np.array_equal(L[4], d[0][0]) and np.array_equal(X[4], d[1][0])
 
 
+def pin_tdls_row_major_reading(orc):
+    """TDLS row-major reading (P A^T = L U, A = U^T L^T P): the hand-worked 2x2 A =
+    [[1, 2], [3, 4]] factors S = A^T = [[1, 3], [2, 4]] with ipiv = (2, 2), L = [[1, 0],
+    [0.5, 1]], U = [[2, 4], [0, 1]], stored back through the column-major reading as rows
+    (2, 0.5) and (4, 1); b = (5, 6) gives x = (-4, 4.5) exactly. On random systems the
+    factor is the default factor of the memory read column-major (bit for bit), the
+    solution meets the backward-error bound, and column-major storage is the default
+    path."""
+    A = np.array([[[1.0, 2.0], [3.0, 4.0]]])
+    b = np.array([[[5.0], [6.0]]])
+    S, X, ipiv, info, _ = orc.getrf_getrs_mirror(A, b, ROW_MAJOR)
+    assert list(ipiv[0]) == [2, 2] and info[0] == 0
+    assert np.array_equal(S[0], [[2.0, 0.5], [4.0, 1.0]])
+    assert np.array_equal(X[0, :, 0], [-4.0, 4.5])
+    rng = _rng(54)
+    for dt in (np.float32, np.float64):
+        n = 13
+        A = rng.standard_normal((8, n, n)).astype(dt)
+        B = rng.standard_normal((8, n, 3)).astype(dt)
+        A[2, 4, :] = 0                   # a zero row of A: a zero column of S
+        S, X, ipiv, info, _ = orc.getrf_getrs_mirror(A, B, ROW_MAJOR)
+        S2, ip2, inf2, _ = orc.getrf(A, COL_MAJOR)
+        assert np.array_equal(S, S2) and np.array_equal(ipiv, ip2) and np.array_equal(info, inf2)
+        assert info[2] > 0 and np.all(X[2] == 0)
+        ok = info == 0
+        be = backward_error(A[ok].astype(np.float64), X[ok], B[ok])
+        assert np.all(be <= 8 * n * eps_of(dt))
+        Ac = to_storage(A, COL_MAJOR)
+        Bc = to_storage(B, COL_MAJOR)
+        r1 = orc.getrf_getrs_mirror(Ac, Bc, COL_MAJOR)
+        r2 = orc.getrf_getrs(Ac, Bc, COL_MAJOR)
+        assert all(np.array_equal(x, y) for x, y in zip(r1, r2))
+
+
 # --------------------------------------------------------------------------- bdsv pins
 def _random_bdsv(rng, batch, nbr, bs, dt=np.float64):
     strips = np.zeros((batch, nbr, bs, 3 * bs), dt)
@@ -767,7 +801,8 @@ BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
               pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
 BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
-VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol]
+VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol,
+                pin_tdls_row_major_reading]
 ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS
 
 

@@ -105,6 +105,18 @@ MUTATIONS = [
     ("ruda_chol_input_check_skips_b",
      "    if (!(all_finite(A, (int64_t)n * n) && all_finite(B, (int64_t)n * nrhs))) {\n      fail_ruda(-1);\n      return;\n    }\n    for (int r = 0;",
      "    if (!(all_finite(A, (int64_t)n * n))) {\n      fail_ruda(-1);\n      return;\n    }\n    for (int r = 0;"),
+    ("mirror_forward_not_transposed",
+     "for (int j = k + 1; j < n; ++j) b(j, c) = std::fma(-s_(k, j), z, b(j, c));",
+     "for (int j = k + 1; j < n; ++j) b(j, c) = std::fma(-s_(j, k), z, b(j, c));"),
+    ("mirror_swaps_in_step_order",
+     "  for (int k = n - 1; k >= 0; --k) {  // x = P^T w",
+     "  for (int k = 0; k < n; ++k) {  // x = P^T w"),
+    ("mirror_swaps_skipped", "    if (q == k) continue;", "    continue;"),
+    ("mirror_backward_scaled",
+     "      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c), b(i, c));",
+     "      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c) / s_(k, k), b(i, c));"),
+    ("mirror_reads_row_major", "  auto s_ = [&](int r, int c) -> T { return S[at(1, n, n, r, c)]; };",
+     "  auto s_ = [&](int r, int c) -> T { return S[at(0, n, n, r, c)]; };"),
     ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
      "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
     ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
