@@ -184,12 +184,14 @@ NEXT_ROWS = {
     "bdsv_factor_f64_32x8": ("bdsv_f64_32x8", "bdsv_factor"),
     "bdsv_solve_f64_32x8": ("bdsv_f64_32x8", "bdsv_solve"),
     "bdmv_f64_32x8": ("bdsv_f64_32x8", "bdmv"),
+    "getrf_getrs_T_f32_n16": ("lu_f32_n16", "getrf_getrs_T"),
 }
 KERNEL_SOURCES.update({
     "getrf_f32_n16": ["lu_reg.cuh", "common.cuh"], "getrs_f32_n16": ["solve.cu", "common.cuh"],
     "potrf_f64_n32": ["chol_sys.cu", "common.cuh"], "potrs_f64_n32": ["solve.cu", "common.cuh"],
     "bdsv_factor_f64_32x8": ["bdsv.cu", "common.cuh"],
     "bdsv_solve_f64_32x8": ["bdsv.cu", "common.cuh"], "bdmv_f64_32x8": ["bdmv.cu", "common.cuh"],
+    "getrf_getrs_T_f32_n16": ["solve.cu", "lu_reg.cuh", "common.cuh"],
 })
 
 
@@ -218,6 +220,8 @@ class SplitProblem(Problem):
         elif op == "bdmv":
             self.y = torch.zeros_like(b)
             self.inputs, self.fixed = [], (a, b)
+        elif op == "getrf_getrs_T":   # the fused call under TDLS's row-major reading
+            self.inputs = [a, b]
         else:   # the factor calls mutate A only
             self.inputs = [a]
         torch.cuda.synchronize()
@@ -239,6 +243,10 @@ class SplitProblem(Problem):
             bs.bs_bdsv_factor_batched(self.work[0], self.info, stream)
         elif op == "bdsv_solve":
             bs.bs_bdsv_solve_batched(self.fixed[0], self.work[0], stream)
+        elif op == "getrf_getrs_T":
+            bs.bs_getrf_getrs_batched_ex(self.work[0], self.work[1], self.ipiv, self.info,
+                                         w.layout, 1.0, bs.BS_CONTRACT_DEFAULT,
+                                         transposed_factor=1, stream=stream)
         else:
             bs.bs_bdmv_batched(self.fixed[0], self.fixed[1], self.y, stream)
 

@@ -28,8 +28,12 @@ BS_CONTRACT_DEFAULT, BS_CONTRACT_RUDA = 0, 1
 
 
 class Options(ctypes.Structure):
-    """bs_options: TDLS pivot threshold and the status contract (see bsolve.h)."""
-    _fields_ = [("pivot_threshold", ctypes.c_double), ("status_contract", ctypes.c_int)]
+    """bs_options: TDLS pivot threshold, the status contract and TDLS's row-major reading
+    (see bsolve.h)."""
+    _fields_ = [("pivot_threshold", ctypes.c_double), ("status_contract", ctypes.c_int),
+                ("transposed_factor", ctypes.c_int)]
+
+
 ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
 
 EXPORTED = (
@@ -228,11 +232,13 @@ def bs_bdmv_batched(strips, x_padded, y_padded, stream=None) -> None:
 # --------------------------------------------------------------- contract variants
 def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
                               pivot_threshold: float = 1.0,
-                              status_contract: int = BS_CONTRACT_DEFAULT, stream=None) -> None:
-    """LU + solve with TDLS threshold pivoting and/or the RUDA status contract."""
+                              status_contract: int = BS_CONTRACT_DEFAULT,
+                              transposed_factor: int = 0, stream=None) -> None:
+    """LU + solve with TDLS threshold pivoting, the RUDA status contract, or TDLS's
+    row-major reading (factor of A^T and the mirror solve)."""
     batch, n = A.shape[0], A.shape[1]
     nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
-    opts = Options(float(pivot_threshold), int(status_contract))
+    opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor))
     st = lib().bs_getrf_getrs_batched_ex(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
                                          _ptr(ipiv), _ptr(info), ctypes.byref(opts),
                                          _stream(stream))
@@ -244,7 +250,7 @@ def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = B
     """Cholesky + solve under the RUDA status contract."""
     batch, n = A.shape[0], A.shape[1]
     nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
-    opts = Options(1.0, int(status_contract))
+    opts = Options(1.0, int(status_contract), 0)
     st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                          _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
     _check(st, "bs_potrf_potrs_batched_ex")

@@ -55,6 +55,42 @@ bool bdsv_supported(bs_dtype dtype, int nbr, int bs) {
   return (dtype == BS_FP32 || dtype == BS_FP64) && nbr >= 1 && bs >= 1 && bs <= kMaxBdsvBs;
 }
 
+// The row-major reading of TDLS (TDLS API, "solver_static.hpp File Reference"): the factor
+// of S, the row-major array read column-major (P A^T = L U), by the plain factor kernels
+// (or the one-CTA kernel under a threshold), then the mirror solve U^T z = b, L^T w = z,
+// x = P^T w, which writes X as zeros where info != 0.
+bs_status getrf_getrs_mirror(bs_dtype dtype, int n, int nrhs, int64_t batch, void* A, void* B,
+                             int32_t* ipiv, int32_t* info, double tau, void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, BS_ROW_MAJOR, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tau == 1.0) {
+    const bs_status st = bs_getrf_batched(dtype, BS_COL_MAJOR, n, batch, A, ipiv, info, stream);
+    if (st != BS_OK) return st;
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_smem_ex<float>(BS_COL_MAJOR, n, 0, batch, static_cast<float*>(A),
+                                               nullptr, ipiv, info, tau, 0, s)
+            : bsolve::launch_lu_smem_ex<double>(BS_COL_MAJOR, n, 0, batch,
+                                                static_cast<double*>(A), nullptr, ipiv, info,
+                                                tau, 0, s);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  const int code = BS_COL_MAJOR | (BS_ROW_MAJOR << 1);
+  e = dtype == BS_FP32
+          ? bsolve::launch_getrs_mirror<float>(code, n, nrhs, batch, static_cast<const float*>(A),
+                                               ipiv, static_cast<float*>(B), info, s)
+          : bsolve::launch_getrs_mirror<double>(code, n, nrhs, batch,
+                                                static_cast<const double*>(A), ipiv,
+                                                static_cast<double*>(B), info, s);
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -331,8 +367,13 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
                                     int32_t* info, const bs_options* opts, void* stream) {
   const double tau = opts ? opts->pivot_threshold : 1.0;
   const int contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
+  const int mirror = opts ? opts->transposed_factor : 0;
   if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
+  if (mirror != 0 && mirror != 1) return BS_ERR_INVALID_ARG;
+  if (mirror && contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
+  if (mirror && layout == BS_ROW_MAJOR)
+    return getrf_getrs_mirror(dtype, n, nrhs, batch, A, B, ipiv, info, tau, stream);
   if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT)
     return bs_getrf_getrs_batched(dtype, layout, n, nrhs, batch, A, B, ipiv, info, stream);
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;

@@ -34,6 +34,12 @@ cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
                          const int32_t* zinfo, cudaStream_t stream);
+// The mirror solve of the row-major reading (U^T z = b, L^T w = z, x = P^T w) with the LU
+// factor of S, the stored array read column-major; layout packs S's order (bit 0) and B's.
+template <typename T>
+cudaError_t launch_getrs_mirror(int layout, int n, int nrhs, int64_t batch, const T* S,
+                                const int32_t* ipiv, T* B, const int32_t* zinfo,
+                                cudaStream_t stream);
 
 // The Cholesky launchers (chol_smem, chol_sys, potrs) take a packed storage-order code:
 // bit 0 for A (or the factor), bit 1 for B; upper fill is passed as the lower fill of A in

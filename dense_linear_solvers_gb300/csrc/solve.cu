@@ -18,6 +18,11 @@
 // getrs: lane t loads the right-hand-side row that the swap sequence brings to position
 // t (the swaps undone from the last: pos = t, then for k = n-1..0 pos <- tau_k(pos)); an
 // ipiv entry outside 1..n swaps nothing, so no access leaves the system.
+// The mirror solve (the row-major reading of TDLS, factor of S = A^T): the lane of
+// position p holds column p of S, a contiguous row of the stored array; U^T z = b runs
+// like the Cholesky forward sweep (z_k = b_k r_k at the owner, then b_j -= s_kj z_k for
+// j > k), L^T w = z like the LU backward sweep without the scaling, and x = P^T w is the
+// store: the value of position p goes to the row the swaps bring to p.
 // The arithmetic is the CPU oracle's, operation by operation: b_i -= l_ik y_k for i > k
 // in increasing k (Cholesky: y_k = b_k * (1/l_kk) first), then x_k = y_k * r_k and
 // b_i -= m_ik x_k for i < k in decreasing k; r_k = 1/u_kk (1 for a pivot below the
@@ -31,7 +36,10 @@
 namespace bsolve {
 namespace {
 
-enum SolveKind : int { kSolveLu = 0, kSolveChol = 1 };
+// kSolveLuT: the mirror solve of the row-major reading of an LU factor (TDLS API,
+// "solver_static.hpp File Reference": the factor is of S, the stored array read
+// column-major, P S = L U with S = A^T; then U^T z = b, L^T w = z, x = P^T w).
+enum SolveKind : int { kSolveLu = 0, kSolveChol = 1, kSolveLuT = 2 };
 
 // Positions per lane for the order tiers 8, 16 and 32. Two positions per lane halve the
 // shuffles per system and let a step skip, at compile time, a slot whose rows are all
@@ -52,7 +60,7 @@ template <> struct Floor<double> {
 
 template <typename T, int KIND>
 __device__ __forceinline__ T diag_rcp(T d) {
-  if (KIND == kSolveLu) return (fabs(d) >= Floor<T>::v()) ? T(1) / d : T(1);
+  if (KIND != kSolveChol) return (fabs(d) >= Floor<T>::v()) ? T(1) / d : T(1);
   return T(1) / d;
 }
 
@@ -111,7 +119,7 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
     ok[q] = valid && (FULL || t + q * G < n);
     src[q] = t + q * G;
   }
-  if (KIND == kSolveLu && valid) {
+  if (KIND != kSolveChol && valid) {
     // the swaps undone from the last, on the group's copy of the swap sequence
     int iv[NT];
     if (FULL && (NT % 4) == 0) {
@@ -138,14 +146,17 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
     const int pq = t + q * G;
     rt[q] = T(1);
     if (ok[q]) {
-      if (KIND == kSolveLu && FULL && (layouts & 1) == kRowMajor) {
+      if (FULL && ((KIND == kSolveLu && (layouts & 1) == kRowMajor) ||
+                   (KIND == kSolveLuT && (layouts & 1) == kColMajor))) {
         ldg_row<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
       } else {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
           if (FULL || j < n) {
-            const int r = (KIND == kSolveLu || j <= pq) ? pq : j;
-            const int c = (KIND == kSolveLu || j <= pq) ? j : pq;
+            // LU: row pq; LuT: column pq of S; Cholesky: the symmetric fill of L
+            const bool rowp = KIND == kSolveLu || (KIND == kSolveChol && j <= pq);
+            const int r = rowp ? pq : j;
+            const int c = rowp ? j : pq;
             v[q][j] = __ldg(Ms + idx(layouts & 1, n, n, r, c));
           } else {
             v[q][j] = T(0);
@@ -167,12 +178,14 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
 #pragma unroll
   for (int q = 0; q < R; ++q) {
     if (ok[q]) {
+      // LU: the row the swaps bring to position pq; LuT: row pq (swapped on the way out)
+      const int lrow = KIND == kSolveLuT ? t + q * G : src[q];
       if (FULL && (layouts >> 1) == kRowMajor) {
-        ldg_row<T, RT>(Bs + static_cast<int64_t>(src[q]) * RT, b[q]);
+        ldg_row<T, RT>(Bs + static_cast<int64_t>(lrow) * RT, b[q]);
       } else {
 #pragma unroll
         for (int c = 0; c < RT; ++c)
-          b[q][c] = (c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, src[q], c0 + c)] : T(0);
+          b[q][c] = (c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, lrow, c0 + c)] : T(0);
       }
     } else {
 #pragma unroll
@@ -180,13 +193,13 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
     }
   }
 
-  // forward: L y = P b (unit L) or L y = b. Slot q holds positions qG..qG+G-1: it has
+  // forward: L y = P b (unit L), L y = b or U^T z = b. Slot q holds positions qG..qG+G-1: it has
   // rows below k unless qG + G - 1 <= k (known at compile time).
 #pragma unroll
   for (int k = 0; k < NT; ++k) {
     if (!FULL && k >= n) break;
     const int kq = k / G, kl = k % G;
-    if (KIND == kSolveChol && t == kl) {
+    if (KIND != kSolveLu && t == kl) {
 #pragma unroll
       for (int c = 0; c < RT; ++c) b[kq][c] = b[kq][c] * rt[kq];
     }
@@ -202,12 +215,13 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
       }
     }
   }
-  // backward: U x = y or L^T x = y. Slot q has rows above k unless qG >= k.
+  // backward: U x = y, L^T x = y or L^T w = z (unit L). Slot q has rows above k unless
+  // qG >= k.
 #pragma unroll
   for (int k = NT - 1; k >= 0; --k) {
     if (!FULL && k >= n) continue;
     const int kq = k / G, kl = k % G;
-    if (t == kl) {
+    if (KIND != kSolveLuT && t == kl) {
 #pragma unroll
       for (int c = 0; c < RT; ++c) b[kq][c] = b[kq][c] * rt[kq];
     }
@@ -226,7 +240,7 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
 #pragma unroll
   for (int q = 0; q < R; ++q) {
     if (!ok[q]) continue;
-    const int pq = t + q * G;
+    const int pq = KIND == kSolveLuT ? src[q] : t + q * G;   // LuT: x = P^T w
     if (FULL && (layouts >> 1) == kRowMajor && (RT * sizeof(T)) % 16 == 0) {
       T* dst = Bs + static_cast<int64_t>(pq) * RT;
 #pragma unroll
@@ -309,7 +323,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
       c = e / n;
       r = e - c * n;
     }
-    if (KIND == kSolveLu || c <= r) cp_async_elem<T>(F + r * P + c, Ms + e);
+    if (KIND != kSolveChol || c <= r) cp_async_elem<T>(F + r * P + c, Ms + e);
   }
   cp_async_wait_all();
   __syncwarp();
@@ -317,7 +331,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
   int src[Q];
 #pragma unroll
   for (int q = 0; q < Q; ++q) src[q] = lane + 32 * q;
-  if (KIND == kSolveLu) {
+  if (KIND != kSolveChol) {
     int ip[Q];
 #pragma unroll
     for (int q = 0; q < Q; ++q)
@@ -346,13 +360,14 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
       const bool ok = lane + 32 * q < n;
+      const int lrow = KIND == kSolveLuT ? lane + 32 * q : src[q];
 #pragma unroll
       for (int c = 0; c < RT; ++c)
-        b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, src[q], c0 + c)] : T(0);
+        b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, lrow, c0 + c)] : T(0);
     }
     for (int k = 0; k < n; ++k) {
       const int kq = k >> 5, kl = k & 31;
-      if (KIND == kSolveChol && lane == kl) {
+      if (KIND != kSolveLu && lane == kl) {
 #pragma unroll
         for (int q = 0; q < Q; ++q)
           if (q == kq)
@@ -371,7 +386,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
       for (int q = 0; q < Q; ++q) {
         const int i = lane + 32 * q;
         if (i > k && i < n) {
-          const T l = F[i * P + k];
+          const T l = KIND == kSolveLuT ? F[k * P + i] : F[i * P + k];
 #pragma unroll
           for (int c = 0; c < RT; ++c) b[q][c] = fma_rn<T>(-l, y[c], b[q][c]);
         }
@@ -379,7 +394,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
     }
     for (int k = n - 1; k >= 0; --k) {
       const int kq = k >> 5, kl = k & 31;
-      if (lane == kl) {
+      if (KIND != kSolveLuT && lane == kl) {
 #pragma unroll
         for (int q = 0; q < Q; ++q)
           if (q == kq)
@@ -408,9 +423,10 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
     for (int q = 0; q < Q; ++q) {
       const int i = lane + 32 * q;
       if (i < n) {
+        const int srow = KIND == kSolveLuT ? src[q] : i;   // LuT: x = P^T w
 #pragma unroll
         for (int c = 0; c < RT; ++c)
-          if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, i, c0 + c)] = zero_x ? T(0) : b[q][c];
+          if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, srow, c0 + c)] = zero_x ? T(0) : b[q][c];
       }
     }
   }
@@ -478,6 +494,13 @@ cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L,
   return launch_kind<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, zinfo, stream);
 }
 
+template <typename T>
+cudaError_t launch_getrs_mirror(int layout, int n, int nrhs, int64_t batch, const T* S,
+                                const int32_t* ipiv, T* B, const int32_t* zinfo,
+                                cudaStream_t stream) {
+  return launch_kind<T, kSolveLuT>(layout, n, nrhs, batch, S, ipiv, B, zinfo, stream);
+}
+
 template cudaError_t launch_getrs<float>(int, int, int, int64_t, const float*, const int32_t*,
                                          float*, const int32_t*, cudaStream_t);
 template cudaError_t launch_getrs<double>(int, int, int, int64_t, const double*, const int32_t*,
@@ -486,5 +509,11 @@ template cudaError_t launch_potrs<float>(int, int, int, int64_t, const float*, f
                                          const int32_t*, cudaStream_t);
 template cudaError_t launch_potrs<double>(int, int, int, int64_t, const double*, double*,
                                           const int32_t*, cudaStream_t);
+template cudaError_t launch_getrs_mirror<float>(int, int, int, int64_t, const float*,
+                                                const int32_t*, float*, const int32_t*,
+                                                cudaStream_t);
+template cudaError_t launch_getrs_mirror<double>(int, int, int, int64_t, const double*,
+                                                 const int32_t*, double*, const int32_t*,
+                                                 cudaStream_t);
 
 }  // namespace bsolve

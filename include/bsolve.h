@@ -156,15 +156,27 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    sweep without a failing pivot; a failed system (info != 0) returns
  *                    its factor (Cholesky: the fill triangle) and X as zeros and, for LU,
  *                    every ipiv entry as -1.
- * opts == NULL or default options run the plain call. Other options run one system per
- * CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the CPU oracle's bit for
- * bit. A threshold outside (0, 1] or an unknown contract is BS_ERR_INVALID_ARG.
+ *   transposed_factor  0 or 1 (LU only; TDLS API, "solver_static.hpp File Reference", the
+ *                    row-major layout: the solver factors S, the stored array read
+ *                    column-major). 1 with BS_ROW_MAJOR factors S = A^T in place,
+ *                    P A^T = L U (ipiv: LAPACK's 1-based swap sequence of that factor,
+ *                    i.e. interchanges of columns of A), and solves the mirror
+ *                    U^T z = b, L^T w = z, x = P^T w; X is zeros where info != 0. A then
+ *                    holds the factor of A^T in the column-major reading. With
+ *                    BS_COL_MAJOR, S = A and the call is the plain one. Runs as a factor
+ *                    launch and a solve launch, for 1 <= n <= 128, 1 <= nrhs <= 65536;
+ *                    with BS_CONTRACT_RUDA it is BS_ERR_UNSUPPORTED.
+ * opts == NULL or default options run the plain call. Thresholds and the RUDA contract
+ * run one system per CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the
+ * CPU oracle's bit for bit. A threshold outside (0, 1], an unknown contract or a
+ * transposed_factor other than 0 or 1 is BS_ERR_INVALID_ARG.
  */
 typedef enum { BS_CONTRACT_DEFAULT = 0, BS_CONTRACT_RUDA = 1 } bs_contract;
 
 typedef struct {
   double pivot_threshold; /* in (0, 1]; 1 = partial pivoting */
   int status_contract;    /* a bs_contract */
+  int transposed_factor;  /* 1: TDLS's row-major reading (factor of A^T, mirror solve) */
 } bs_options;
 
 BS_API bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,

@@ -116,3 +116,52 @@ def test_ruda_status_cholesky(dtype, layout):
             assert np.array_equal(_host(info), info_o)
             assert np.array_equal(_host(tA), Lo, equal_nan=True)
             assert np.array_equal(_host(tB), Xo)
+
+
+def gpu_lu_mirror(A, B, layout, tau):
+    tA, tB = _dev(A), _dev(B)
+    batch, n = A.shape[0], A.shape[1]
+    ipiv = torch.full((batch, n), SENT, dtype=torch.int32, device="cuda")
+    info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+    bs.bs_getrf_getrs_batched_ex(tA, tB, ipiv, info, layout, tau, bs.BS_CONTRACT_DEFAULT,
+                                 transposed_factor=1)
+    return _host(tA), _host(tB), _host(ipiv), _host(info)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("tau", [1.0, 0.5])
+def test_transposed_factor_row_major(dtype, tau):
+    """TDLS's row-major reading: factor of A^T in the stored array, mirror solve; every
+    register tier, the shared-memory tiers, ragged right-hand-side chunks, singular
+    systems."""
+    rng = np.random.default_rng(1414 + int(tau * 10))
+    orders = list(range(1, 34)) + [40, 64, 65, 100, 128]
+    for n in orders:
+        nrhs = int(rng.choice([1, 2, 3, 4, 7, 8, 9, 20]))
+        Al = rng.standard_normal((23, n, n)).astype(dtype)
+        Al[5, n // 2, :] = 0           # a zero row of A: a zero column of S
+        if n > 1:
+            Al[7, :, 0] = Al[7, :, n - 1]   # equal columns of A: a singular S as well
+        Bl = rng.standard_normal((23, n, nrhs)).astype(dtype)
+        So, Xo, ipo, info_o, tie = oracle.getrf_getrs_mirror(Al, Bl, ROW_MAJOR, tau=tau,
+                                                              nthreads=NT)
+        Sg, Xg, ipg, infg = gpu_lu_mirror(Al, Bl, ROW_MAJOR, tau)
+        clean = tie < 0
+        assert clean.sum() >= 20, n
+        assert np.array_equal(infg[clean], info_o[clean]), (n, nrhs)
+        assert np.array_equal(ipg[clean], ipo[clean]), (n, nrhs)
+        assert np.array_equal(Sg[clean], So[clean]), (n, nrhs)
+        assert np.array_equal(Xg[clean], Xo[clean]), (n, nrhs)
+        assert infg[5] > 0 and np.all(Xg[infg != 0] == 0)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_transposed_factor_col_major_is_plain(dtype):
+    """Under column-major storage S = A: the option runs the plain call, bit for bit."""
+    rng = np.random.default_rng(1515)
+    for n in (3, 16, 32, 50):
+        A = to_storage(rng.standard_normal((9, n, n)).astype(dtype), COL_MAJOR)
+        B = to_storage(rng.standard_normal((9, n, 4)).astype(dtype), COL_MAJOR)
+        r1 = gpu_lu_mirror(A, B, COL_MAJOR, 1.0)
+        r2 = gpu_lu_ex(A, B, COL_MAJOR, 1.0, bs.BS_CONTRACT_DEFAULT)
+        assert all(np.array_equal(x, y) for x, y in zip(r1, r2))
