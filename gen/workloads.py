@@ -84,6 +84,28 @@ def from_storage(S: np.ndarray, layout: int) -> np.ndarray:
     return S if layout == ROW_MAJOR else np.swapaxes(S, 1, 2)
 
 
+def interleave(S: np.ndarray, w: int) -> np.ndarray:
+    """Per-system storage (batch, ...) -> the flat interleaved batched layout with w
+    systems per block: element e of system s at (s // w) * w * size + e * w + s % w
+    (w = 1: the systems one after another; w >= batch: SoA). Slots of the last block
+    past the batch hold NaN, so that a stray read shows."""
+    batch = S.shape[0]
+    size = int(np.prod(S.shape[1:], dtype=np.int64))
+    nb = -(-batch // w)
+    fill = np.nan if np.issubdtype(S.dtype, np.floating) else -7
+    P = np.full((nb * w, size), fill, dtype=S.dtype)
+    P[:batch] = S.reshape(batch, size)
+    return np.ascontiguousarray(P.reshape(nb, w, size).transpose(0, 2, 1)).reshape(-1)
+
+
+def deinterleave(flat: np.ndarray, batch: int, w: int, shape) -> np.ndarray:
+    """Inverse of interleave: the flat interleaved array -> (batch, *shape)."""
+    size = int(np.prod(shape, dtype=np.int64))
+    nb = -(-batch // w)
+    P = flat[:nb * w * size].reshape(nb, size, w).transpose(0, 2, 1).reshape(nb * w, size)
+    return np.ascontiguousarray(P[:batch]).reshape((batch,) + tuple(shape))
+
+
 def _bmm(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     # Batched matrix product through torch's CPU BLAS binding (NumPy's stacked matmul
     # is slow for many tiny matrices); the inputs are the generator's own draws.

@@ -76,6 +76,8 @@ class Oracle:
         sig["getrf_getrs_ex"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32, i32]
         sig["potrf_potrs_ex"] = [i32, i32, i32, i32, i64, vp, vp, vp, i32, i32]
         sig["getrf_getrs_mirror"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32]
+        sig["getrf_getrs_il"] = [i32, i32, i32, i64, i64, vp, vp, vp, vp, vp, i32]
+        sig["potrf_potrs_il"] = [i32, i32, i32, i32, i64, i64, vp, vp, vp, i32]
         for op, args in sig.items():
             for sfx in ("f32", "f64"):
                 fn = getattr(lib, f"oracle_{op}_{sfx}")
@@ -262,6 +264,42 @@ class Oracle:
         return A, B, ipiv, info, tie
 
 
+    def getrf_getrs_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
+                       layout: int = ROW_MAJOR, nthreads: int = 1):
+        """LU + solve on interleaved batched storage (TDLS: element e of system s at
+        base_s[e * w], base_s = (s // w) * w * size + s % w; w = 1 AoS, w >= batch SoA).
+        A, B: flat arrays of ceil(batch / w) * w systems. Returns (A, B, ipiv, info,
+        tie_step), ipiv flat and interleaved like A."""
+        A = np.ascontiguousarray(A).reshape(-1).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).reshape(-1).copy()
+        nb = -(-batch // w) if batch else 0
+        if A.size < nb * w * n * n or B.size < nb * w * n * nrhs:
+            raise ValueError("interleaved buffers too small")
+        ipiv = np.zeros(max(nb * w * n, 1), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_getrs_il_" + _suffix(A.dtype))
+        if fn(layout, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
+              nthreads) != 0:
+            raise ValueError("oracle getrf_getrs_il rejected its arguments")
+        return A, B, ipiv, info, tie
+
+    def potrf_potrs_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
+                       layout: int = COL_MAJOR, fill: int = LOWER, nthreads: int = 1):
+        """Cholesky + solve on interleaved batched storage (see getrf_getrs_il).
+        Returns (A, B, info)."""
+        A = np.ascontiguousarray(A).reshape(-1).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).reshape(-1).copy()
+        nb = -(-batch // w) if batch else 0
+        if A.size < nb * w * n * n or B.size < nb * w * n * nrhs:
+            raise ValueError("interleaved buffers too small")
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_potrf_potrs_il_" + _suffix(A.dtype))
+        if fn(layout, fill, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(info), nthreads) != 0:
+            raise ValueError("oracle potrf_potrs_il rejected its arguments")
+        return A, B, info
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -322,6 +360,15 @@ def potrf_potrs_ex(A, B, layout: int = COL_MAJOR, fill: int = LOWER, ruda: int =
 
 def getrf_getrs_mirror(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, nthreads: int = 1):
     return default().getrf_getrs_mirror(A, B, layout, tau, nthreads)
+
+
+def getrf_getrs_il(A, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1):
+    return default().getrf_getrs_il(A, B, n, nrhs, batch, w, layout, nthreads)
+
+
+def potrf_potrs_il(A, B, n, nrhs, batch, w, layout: int = COL_MAJOR, fill: int = LOWER,
+                   nthreads: int = 1):
+    return default().potrf_potrs_il(A, B, n, nrhs, batch, w, layout, fill, nthreads)
 
 
 def _suffix(dtype) -> str:

@@ -711,6 +711,67 @@ int potrf_potrs_ex_batched(int layout, int fill, int n, int nrhs, int64_t batch,
 
 }  // namespace
 
+// [TDLS] batched layouts: element e of system s (e the offset of the element in the
+// system's own storage order) lives at base_s[e * stride]; AoS is stride 1 (base_s =
+// s * size), SoA stride = the batch, AoSoA stride W with the systems in blocks of W:
+// base_s = (s / W) * W * size + s % W. One routine covers all three: it gathers each
+// system into a contiguous copy, runs the per-system routine and scatters it back. A, B
+// and ipiv are interleaved; info holds one entry per system.
+template <typename T>
+struct Strided {
+  T* p;
+  int64_t w;
+  int64_t size;   // elements of one system
+  T* base(int64_t s) const { return p + (s / w) * w * size + s % w; }
+  void gather(int64_t s, T* dst) const {
+    const T* b = base(s);
+    for (int64_t e = 0; e < size; ++e) dst[e] = b[e * w];
+  }
+  void scatter(int64_t s, const T* src) const {
+    T* b = base(s);
+    for (int64_t e = 0; e < size; ++e) b[e * w] = src[e];
+  }
+};
+
+template <typename T>
+int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w, T* A, T* B,
+                           int32_t* ipiv, int32_t* info, int32_t* tie_step, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || w < 1) return 1;
+  const Strided<T> a{A, w, (int64_t)n * n}, b{B, w, (int64_t)n * nrhs};
+  const Strided<int32_t> pv{ipiv, w, n};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size), bs(b.size);
+    std::vector<int32_t> ps(n);
+    a.gather(s, as.data());
+    b.gather(s, bs.data());
+    getrf_getrs_one<T>(layout, n, nrhs, as.data(), bs.data(), ps.data(), info + s,
+                       tie_step ? tie_step + s : nullptr);
+    a.scatter(s, as.data());
+    b.scatter(s, bs.data());
+    pv.scatter(s, ps.data());
+  });
+  return 0;
+}
+
+template <typename T>
+int potrf_potrs_il_batched(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w, T* A,
+                           T* B, int32_t* info, int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 ||
+      batch < 0 || w < 1)
+    return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
+  const Strided<T> a{A, w, (int64_t)n * n}, b{B, w, (int64_t)n * nrhs};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size), bs(b.size);
+    a.gather(s, as.data());
+    b.gather(s, bs.data());
+    potrf_potrs_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s);
+    a.scatter(s, as.data());
+    b.scatter(s, bs.data());
+  });
+  return 0;
+}
+
 extern "C" {
 
 int oracle_getrf_getrs_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
@@ -825,6 +886,26 @@ int oracle_getrf_getrs_mirror_f64(int layout, int n, int nrhs, int64_t batch, do
                                   int nthreads) {
   return getrf_getrs_mirror_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
                                          nthreads);
+}
+int oracle_getrf_getrs_il_f32(int layout, int n, int nrhs, int64_t batch, int64_t w, float* A,
+                              float* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
+                              int nthreads) {
+  return getrf_getrs_il_batched<float>(layout, n, nrhs, batch, w, A, B, ipiv, info, tie_step,
+                                       nthreads);
+}
+int oracle_getrf_getrs_il_f64(int layout, int n, int nrhs, int64_t batch, int64_t w, double* A,
+                              double* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
+                              int nthreads) {
+  return getrf_getrs_il_batched<double>(layout, n, nrhs, batch, w, A, B, ipiv, info, tie_step,
+                                        nthreads);
+}
+int oracle_potrf_potrs_il_f32(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
+                              float* A, float* B, int32_t* info, int nthreads) {
+  return potrf_potrs_il_batched<float>(layout, fill, n, nrhs, batch, w, A, B, info, nthreads);
+}
+int oracle_potrf_potrs_il_f64(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
+                              double* A, double* B, int32_t* info, int nthreads) {
+  return potrf_potrs_il_batched<double>(layout, fill, n, nrhs, batch, w, A, B, info, nthreads);
 }
 
 }  // extern "C"

@@ -27,7 +27,8 @@ from fractions import Fraction
 import numpy as np
 import scipy.linalg as sla
 
-from gen.workloads import COL_MAJOR, ROW_MAJOR, assemble_bdsv_dense, from_storage, to_storage
+from gen.workloads import (COL_MAJOR, ROW_MAJOR, assemble_bdsv_dense, deinterleave, from_storage,
+                           interleave, to_storage)
 from tests.numerics import backward_error, eps_of, forward_error, lapack_perm, unpack_lu
 
 
@@ -798,12 +799,77 @@ CHOL_PINS = [pin_chol_hand_worked, pin_chol_2x2_closed_form,
              pin_chol_reconstruction_and_lapack, pin_chol_info_contract, pin_chol_upper_fill]
 BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,
              pin_bdsv_scalar_tridiagonal, pin_bdsv_info]
+def pin_interleaved_literal(orc):
+    """TDLS batched layouts, element e of system s at base_s[e * stride]: three 1x1
+    systems in blocks of two (AoSoA, the last block ragged). A = (2, 4 | 0.5, pad),
+    b = (1, 3 | 5, pad) as stored; x_s = b_s / a_s exactly: (0.5, 0.75 | 10), the pad
+    untouched; Cholesky on a = (4, 16 | 0.25) gives l = (2, 4 | 0.5)."""
+    nan = np.nan
+    A = np.array([2.0, 4.0, 0.5, nan])
+    B = np.array([1.0, 3.0, 5.0, nan])
+    LU, X, ipiv, info, _ = orc.getrf_getrs_il(A, B, 1, 1, 3, 2, ROW_MAJOR)
+    assert np.array_equal(X[:3], [0.5, 0.75, 10.0]) and np.isnan(X[3])
+    assert np.array_equal(LU[:3], A[:3]) and np.isnan(LU[3])
+    assert list(ipiv[:3]) == [1, 1, 1] and list(info) == [0, 0, 0]
+    # two systems of order 2 in one block of two: element e of system s at 2e + s
+    A2 = np.array([[[0.0, 1.0], [1.0, 0.0]], [[4.0, 2.0], [2.0, 2.0]]])
+    B2 = np.array([[[3.0], [5.0]], [[2.0], [2.0]]])
+    flatA = np.array([0.0, 4.0, 1.0, 2.0, 1.0, 2.0, 0.0, 2.0])
+    flatB = np.array([3.0, 2.0, 5.0, 2.0])
+    _, X2, p2, _, _ = orc.getrf_getrs_il(flatA, flatB, 2, 1, 2, 2, ROW_MAJOR)
+    # system 0: the permutation [[0,1],[1,0]] swaps b; system 1: x = (0, 1) by Cramer
+    assert np.array_equal(X2, [5.0, 0.0, 3.0, 1.0]) and list(p2) == [2, 1, 2, 2]
+    assert np.array_equal(interleave(A2, 2), flatA) and np.array_equal(interleave(B2, 2), flatB)
+    L, Xc, infc = orc.potrf_potrs_il(np.array([4.0, 16.0, 0.25, nan]),
+                                     np.array([2.0, 8.0, 1.0, nan]), 1, 1, 3, 2)
+    assert np.array_equal(L[:3], [2.0, 4.0, 0.5]) and np.isnan(L[3])
+    assert np.array_equal(Xc[:3], [0.5, 0.5, 4.0]) and list(infc) == [0, 0, 0]
+
+
+def pin_interleaved_layouts(orc):
+    """The interleaved drivers equal the per-system ones on the same systems, bit for bit,
+    for AoS (w = 1), AoSoA with a ragged last block, SoA (w = batch) and SoA with spare
+    capacity (w > batch), both storage orders, LU and both Cholesky fills; the slots of
+    the last block past the batch are never written."""
+    rng = _rng(77)
+    for dt in (np.float32, np.float64):
+        for (n, nrhs, batch, w) in [(5, 2, 7, 1), (5, 2, 7, 3), (5, 2, 7, 7), (4, 1, 6, 16),
+                                    (16, 4, 33, 32), (3, 3, 10, 4)]:
+            for layout in (ROW_MAJOR, COL_MAJOR):
+                Al = rng.standard_normal((batch, n, n)).astype(dt)
+                Al[1, :, 0] = 0                     # a singular system
+                A = to_storage(Al, layout)
+                B = to_storage(rng.standard_normal((batch, n, nrhs)).astype(dt), layout)
+                ref = orc.getrf_getrs(A, B, layout)
+                got = orc.getrf_getrs_il(interleave(A, w), interleave(B, w), n, nrhs, batch, w,
+                                         layout)
+                assert np.array_equal(deinterleave(got[0], batch, w, A.shape[1:]), ref[0])
+                assert np.array_equal(deinterleave(got[1], batch, w, B.shape[1:]), ref[1])
+                assert np.array_equal(deinterleave(got[2], batch, w, (n,)), ref[2])
+                assert np.array_equal(got[3], ref[3]) and np.array_equal(got[4], ref[4])
+                pads = np.isnan(interleave(A, w))
+                assert np.all(np.isnan(got[0][pads]))
+                G = rng.standard_normal((batch, n, n)).astype(np.float64)
+                Sl = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dt)
+                Sl[2, n - 1, n - 1] = -1.0          # a failing minor
+                for fill in (0, 1):
+                    Sa = to_storage(Sl, layout)
+                    r2 = orc.potrf_potrs(Sa, B, layout, fill=fill)
+                    g2 = orc.potrf_potrs_il(interleave(Sa, w), interleave(B, w), n, nrhs, batch,
+                                            w, layout, fill)
+                    assert np.array_equal(deinterleave(g2[0], batch, w, Sa.shape[1:]), r2[0])
+                    assert np.array_equal(deinterleave(g2[1], batch, w, B.shape[1:]), r2[1])
+                    assert np.array_equal(g2[2], r2[2]) and g2[2][2] == n
+
+
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
               pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
 BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
 VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol,
                 pin_tdls_row_major_reading]
-ALL_PINS = LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS
+LAYOUT_PINS = [pin_interleaved_literal, pin_interleaved_layouts]
+ALL_PINS = (LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS +
+            LAYOUT_PINS)
 
 
 def failing_pins(orc, pins=ALL_PINS):

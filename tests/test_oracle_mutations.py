@@ -91,8 +91,8 @@ MUTATIONS = [
      "  const int a_layout = fill == 0 ? layout : 1 - layout;\n  for_systems(batch, nthreads, [&](int64_t s) {\n    potrf_potrs_one<T>(a_layout, layout, n, nrhs,",
      "  const int a_layout = layout;\n  for_systems(batch, nthreads, [&](int64_t s) {\n    potrf_potrs_one<T>(a_layout, layout, n, nrhs,"),
     ("chol_upper_fill_b_transposed",
-     "    potrf_potrs_one<T>(a_layout, layout, n, nrhs,",
-     "    potrf_potrs_one<T>(a_layout, a_layout, n, nrhs,"),
+     "    potrf_potrs_one<T>(a_layout, layout, n, nrhs, A + s * n * n,",
+     "    potrf_potrs_one<T>(a_layout, a_layout, n, nrhs, A + s * n * n,"),
     ("threshold_comparison_flipped", "if (akk >= bar) p = k;   // the row in place is kept",
      "if (akk <= bar) p = k;   // the row in place is kept"),
     ("threshold_pivot_magnitude_of_max", "const T mag = (p == k) ? akk : best;",
@@ -117,6 +117,14 @@ MUTATIONS = [
      "      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c) / s_(k, k), b(i, c));"),
     ("mirror_reads_row_major", "  auto s_ = [&](int r, int c) -> T { return S[at(1, n, n, r, c)]; };",
      "  auto s_ = [&](int r, int c) -> T { return S[at(0, n, n, r, c)]; };"),
+    ("il_block_offset_missing_w", "T* base(int64_t s) const { return p + (s / w) * w * size + s % w; }",
+     "T* base(int64_t s) const { return p + (s / w) * size + s % w; }"),
+    ("il_gather_contiguous", "for (int64_t e = 0; e < size; ++e) dst[e] = b[e * w];",
+     "for (int64_t e = 0; e < size; ++e) dst[e] = b[e];"),
+    ("il_ipiv_not_interleaved", "    pv.scatter(s, ps.data());",
+     "    for (int k = 0; k < n; ++k) ipiv[s * n + k] = ps[k];"),
+    ("il_chol_fill_ignored", "    potrf_potrs_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s);",
+     "    potrf_potrs_one<T>(layout, layout, n, nrhs, as.data(), bs.data(), info + s);"),
     ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
      "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
     ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
