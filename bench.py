@@ -185,14 +185,28 @@ NEXT_ROWS = {
     "bdsv_solve_f64_32x8": ("bdsv_f64_32x8", "bdsv_solve"),
     "bdmv_f64_32x8": ("bdsv_f64_32x8", "bdmv"),
     "getrf_getrs_T_f32_n16": ("lu_f32_n16", "getrf_getrs_T"),
+    "getrf_getrs_aosoa32_f32_n16": ("lu_f32_n16", "getrf_getrs_il"),
+    "potrf_potrs_soa_f64_n32": ("chol_f64_n32", "potrf_potrs_il"),
 }
+# systems per block of the interleaved rows (None: the whole batch, SoA)
+IL_WIDTH = {"getrf_getrs_aosoa32_f32_n16": 32, "potrf_potrs_soa_f64_n32": None}
 KERNEL_SOURCES.update({
     "getrf_f32_n16": ["lu_reg.cuh", "common.cuh"], "getrs_f32_n16": ["solve.cu", "common.cuh"],
     "potrf_f64_n32": ["chol_sys.cu", "common.cuh"], "potrs_f64_n32": ["solve.cu", "common.cuh"],
     "bdsv_factor_f64_32x8": ["bdsv.cu", "common.cuh"],
     "bdsv_solve_f64_32x8": ["bdsv.cu", "common.cuh"], "bdmv_f64_32x8": ["bdmv.cu", "common.cuh"],
     "getrf_getrs_T_f32_n16": ["solve.cu", "lu_reg.cuh", "common.cuh"],
+    "getrf_getrs_aosoa32_f32_n16": ["lu_reg.cuh", "common.cuh"],
+    "potrf_potrs_soa_f64_n32": ["chol_sys.cu", "common.cuh"],
 })
+
+
+def interleave_device(x, w: int):
+    """(batch, ...) device tensor -> the flat interleaved layout with w systems per block
+    (w divides the batch here): element e of system s at (s // w) * w * size + e * w + s % w."""
+    batch = x.shape[0]
+    size = x[0].numel()
+    return x.reshape(batch // w, w, size).transpose(1, 2).contiguous().reshape(-1)
 
 
 class SplitProblem(Problem):
@@ -222,6 +236,10 @@ class SplitProblem(Problem):
             self.inputs, self.fixed = [], (a, b)
         elif op == "getrf_getrs_T":   # the fused call under TDLS's row-major reading
             self.inputs = [a, b]
+        elif op in ("getrf_getrs_il", "potrf_potrs_il"):   # interleaved batched layout
+            self.ilv = IL_WIDTH[name] or self.batch
+            self.inputs = [interleave_device(a, self.ilv), interleave_device(b, self.ilv)]
+            self.ipiv = self.ipiv.reshape(-1) if self.ipiv is not None else None
         else:   # the factor calls mutate A only
             self.inputs = [a]
         torch.cuda.synchronize()
@@ -247,6 +265,14 @@ class SplitProblem(Problem):
             bs.bs_getrf_getrs_batched_ex(self.work[0], self.work[1], self.ipiv, self.info,
                                          w.layout, 1.0, bs.BS_CONTRACT_DEFAULT,
                                          transposed_factor=1, stream=stream)
+        elif op == "getrf_getrs_il":
+            bs.bs_getrf_getrs_batched_ex(self.work[0], self.work[1], self.ipiv, self.info,
+                                         w.layout, interleave=self.ilv,
+                                         shape=(self.batch, w.n, w.nrhs), stream=stream)
+        elif op == "potrf_potrs_il":
+            bs.bs_potrf_potrs_batched_ex(self.work[0], self.work[1], self.info, w.layout,
+                                         bs.BS_LOWER, interleave=self.ilv,
+                                         shape=(self.batch, w.n, w.nrhs), stream=stream)
         else:
             bs.bs_bdmv_batched(self.fixed[0], self.fixed[1], self.y, stream)
 

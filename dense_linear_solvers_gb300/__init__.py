@@ -31,7 +31,7 @@ class Options(ctypes.Structure):
     """bs_options: TDLS pivot threshold, the status contract and TDLS's row-major reading
     (see bsolve.h)."""
     _fields_ = [("pivot_threshold", ctypes.c_double), ("status_contract", ctypes.c_int),
-                ("transposed_factor", ctypes.c_int)]
+                ("transposed_factor", ctypes.c_int), ("interleave", ctypes.c_int64)]
 
 
 ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
@@ -230,15 +230,26 @@ def bs_bdmv_batched(strips, x_padded, y_padded, stream=None) -> None:
 
 
 # --------------------------------------------------------------- contract variants
+def _il_shape(A, B, layout, interleave, shape):
+    # (batch, n, nrhs): from the tensors' shapes, or, for an interleaved batch, given
+    if interleave > 1:
+        if shape is None:
+            raise ValueError("an interleaved batch needs shape=(batch, n, nrhs)")
+        return tuple(int(v) for v in shape)
+    return A.shape[0], A.shape[1], (B.shape[2] if layout == ROW_MAJOR else B.shape[1])
+
+
 def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
                               pivot_threshold: float = 1.0,
                               status_contract: int = BS_CONTRACT_DEFAULT,
-                              transposed_factor: int = 0, stream=None) -> None:
-    """LU + solve with TDLS threshold pivoting, the RUDA status contract, or TDLS's
-    row-major reading (factor of A^T and the mirror solve)."""
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
-    opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor))
+                              transposed_factor: int = 0, interleave: int = 0, shape=None,
+                              stream=None) -> None:
+    """LU + solve with TDLS threshold pivoting, the RUDA status contract, TDLS's
+    row-major reading (factor of A^T and the mirror solve), or an interleaved batched
+    layout (A, B, ipiv flat; shape=(batch, n, nrhs))."""
+    batch, n, nrhs = _il_shape(A, B, layout, interleave, shape)
+    opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor),
+                   int(interleave))
     st = lib().bs_getrf_getrs_batched_ex(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
                                          _ptr(ipiv), _ptr(info), ctypes.byref(opts),
                                          _stream(stream))
@@ -246,11 +257,12 @@ def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
 
 
 def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = BS_LOWER,
-                              status_contract: int = BS_CONTRACT_DEFAULT, stream=None) -> None:
-    """Cholesky + solve under the RUDA status contract."""
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
-    opts = Options(1.0, int(status_contract), 0)
+                              status_contract: int = BS_CONTRACT_DEFAULT, interleave: int = 0,
+                              shape=None, stream=None) -> None:
+    """Cholesky + solve under the RUDA status contract, or on an interleaved batched
+    layout (A, B flat; shape=(batch, n, nrhs))."""
+    batch, n, nrhs = _il_shape(A, B, layout, interleave, shape)
+    opts = Options(1.0, int(status_contract), 0, int(interleave))
     st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                          _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
     _check(st, "bs_potrf_potrs_batched_ex")

@@ -105,9 +105,10 @@ def bdmv_bytes_flops(nbr: int, bs: int, elem: int):
 def per_system(op: str, n: int, nrhs: int, elem: int, nbr: int = 0):
     """(bytes, flops) of one system of a workload (n is the block size for the
     block-tridiagonal operations)."""
-    if op in ("getrf_getrs", "getrf_getrs_T"):   # T: the row-major reading, same work
+    # T: the row-major reading; il: an interleaved batched layout (the same work)
+    if op in ("getrf_getrs", "getrf_getrs_T", "getrf_getrs_il"):
         return getrf_getrs_bytes(n, nrhs, elem), getrf_getrs_flops(n, nrhs)
-    if op == "potrf_potrs":
+    if op in ("potrf_potrs", "potrf_potrs_il"):
         return potrf_potrs_bytes(n, nrhs, elem), potrf_potrs_flops(n, nrhs)
     if op == "bdsv":
         return bdsv_bytes(nbr, n, elem), bdsv_flops(nbr, n)

@@ -91,6 +91,66 @@ bs_status getrf_getrs_mirror(bs_dtype dtype, int n, int nrhs, int64_t batch, voi
   return from_cuda(e);
 }
 
+// The interleaved batched layout (TDLS API, "solver_static.hpp File Reference": element e
+// of system s at base_s[e * ilv], base_s = (s / ilv) * ilv * size + s % ilv; AoSoA, SoA
+// when ilv >= batch) for A, B and ipiv; info one entry per system. The fused kernels with
+// a stride: the register tier for n <= 32, one CTA per system above.
+bs_status getrf_getrs_il(bs_dtype dtype, bs_layout layout, int n, int nrhs, int64_t batch,
+                         int64_t ilv, void* A, void* B, int32_t* ipiv, int32_t* info,
+                         void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_reg_il<float>(layout, n, nrhs, batch, ilv, static_cast<float*>(A),
+                                              static_cast<float*>(B), ipiv, info, s)
+            : bsolve::launch_lu_reg_il<double>(layout, n, nrhs, batch, ilv,
+                                               static_cast<double*>(A), static_cast<double*>(B),
+                                               ipiv, info, s);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_lu_smem_ex<float>(layout, n, nrhs, batch, static_cast<float*>(A),
+                                               static_cast<float*>(B), ipiv, info, 1.0, 0, s, ilv)
+            : bsolve::launch_lu_smem_ex<double>(layout, n, nrhs, batch, static_cast<double*>(A),
+                                                static_cast<double*>(B), ipiv, info, 1.0, 0, s,
+                                                ilv);
+  }
+  return from_cuda(e);
+}
+
+bs_status potrf_potrs_il(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs,
+                         int64_t batch, int64_t ilv, void* A, void* B, int32_t* info,
+                         void* stream) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !B || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int code = chol_layouts(layout, fill);
+  cudaError_t e;
+  if (n <= kMaxRegN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_sys<float>(code, n, nrhs, batch, static_cast<float*>(A),
+                                             static_cast<float*>(B), info, s, ilv)
+            : bsolve::launch_chol_sys<double>(code, n, nrhs, batch, static_cast<double*>(A),
+                                              static_cast<double*>(B), info, s, ilv);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_smem_ex<float>(code, n, nrhs, batch, static_cast<float*>(A),
+                                                 static_cast<float*>(B), info, 0, s, ilv)
+            : bsolve::launch_chol_smem_ex<double>(code, n, nrhs, batch, static_cast<double*>(A),
+                                                  static_cast<double*>(B), info, 0, s, ilv);
+  }
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -368,10 +428,16 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
   const double tau = opts ? opts->pivot_threshold : 1.0;
   const int contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
   const int mirror = opts ? opts->transposed_factor : 0;
+  const int64_t ilv = opts ? opts->interleave : 0;
   if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
   if (mirror != 0 && mirror != 1) return BS_ERR_INVALID_ARG;
+  if (ilv < 0) return BS_ERR_INVALID_ARG;
   if (mirror && contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
+  if (ilv > 1) {
+    if (mirror || tau != 1.0 || contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
+    return getrf_getrs_il(dtype, layout, n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  }
   if (mirror && layout == BS_ROW_MAJOR)
     return getrf_getrs_mirror(dtype, n, nrhs, batch, A, B, ipiv, info, tau, stream);
   if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT)
@@ -398,8 +464,16 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
                                     const bs_options* opts, void* stream) {
   const double tau = opts ? opts->pivot_threshold : 1.0;
   const int contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
+  const int mirror = opts ? opts->transposed_factor : 0;
+  const int64_t ilv = opts ? opts->interleave : 0;
   if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
+  if ((mirror != 0 && mirror != 1) || ilv < 0) return BS_ERR_INVALID_ARG;
+  if (mirror) return BS_ERR_UNSUPPORTED;   // an LU option
+  if (ilv > 1) {
+    if (contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
+    return potrf_potrs_il(dtype, layout, fill, n, nrhs, batch, ilv, A, B, info, stream);
+  }
   if (contract == BS_CONTRACT_DEFAULT)   // the threshold has no meaning without pivoting
     return bs_potrf_potrs_batched(dtype, layout, fill, n, nrhs, batch, A, B, info, stream);
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;

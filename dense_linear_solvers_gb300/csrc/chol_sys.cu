@@ -39,7 +39,7 @@ __host__ __device__ inline int sys_stride(int n, int nrhs) { return (tri(n) + n 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
-                T* __restrict__ B, int32_t* __restrict__ info) {
+                T* __restrict__ B, int32_t* __restrict__ info, int64_t ilv) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int alay = layouts & 1, blay = layouts >> 1;   // storage orders of A and of B
   const int D = sys_stride(n, nrhs);
@@ -62,15 +62,19 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     const int64_t sys = s0 + q;
     T* const Mq = M + q * D;
     if (sys < batch) {
-      const T* As = A + sys * n * n;
-      const T* Bs = B + sys * n * nrhs;
+      // element e of system sys at As[e * ilv] (ilv = 1: the systems one after another;
+      // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B
+      const int64_t blk = sys / ilv, sl = sys - blk * ilv;
+      const T* As = A + blk * ilv * n * n + sl;
+      const T* Bs = B + blk * ilv * n * nrhs + sl;
       for (int j = 0; j < n; ++j)
         for (int i = j + lane; i < n; i += 32)
-          cp_async_elem<T>(Mq + tri(i) + j, alay == kColMajor ? As + j * n + i : As + i * n + j);
+          cp_async_elem<T>(Mq + tri(i) + j,
+                           As + (alay == kColMajor ? j * n + i : i * n + j) * ilv);
       for (int c = 0; c < nrhs; ++c)
         for (int i = lane; i < n; i += 32)
           cp_async_elem<T>(Mq + TRI + i * nrhs + c,
-                           blay == kColMajor ? Bs + c * n + i : Bs + i * nrhs + c);
+                           Bs + (blay == kColMajor ? c * n + i : i * nrhs + c) * ilv);
     } else {
       // a system past the end of the batch: an identity keeps its lanes finite
       for (int e = lane; e < D; e += 32) Mq[e] = T(0);
@@ -159,25 +163,17 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     const int64_t sys = s0 + q;
     if (sys >= batch) continue;
     const T* const Mq = M + q * D;
-    T* As = A + sys * n * n;
-    T* Bs = B + sys * n * nrhs;
+    const int64_t blk = sys / ilv, sl = sys - blk * ilv;
+    T* As = A + blk * ilv * n * n + sl;
+    T* Bs = B + blk * ilv * n * nrhs + sl;
     const bool failed = sinfo[q] != 0;
     for (int j = 0; j < n; ++j)
-      for (int i = j + lane; i < n; i += 32) {
-        const T v = Mq[tri(i) + j];
-        if (alay == kColMajor)
-          As[j * n + i] = v;
-        else
-          As[i * n + j] = v;
-      }
+      for (int i = j + lane; i < n; i += 32)
+        As[(alay == kColMajor ? j * n + i : i * n + j) * ilv] = Mq[tri(i) + j];
     for (int c = 0; c < nrhs; ++c)
-      for (int i = lane; i < n; i += 32) {
-        const T v = failed ? T(0) : Mq[TRI + i * nrhs + c];
-        if (blay == kColMajor)
-          Bs[c * n + i] = v;
-        else
-          Bs[i * nrhs + c] = v;
-      }
+      for (int i = lane; i < n; i += 32)
+        Bs[(blay == kColMajor ? c * n + i : i * nrhs + c) * ilv] =
+            failed ? T(0) : Mq[TRI + i * nrhs + c];
     if (lane == 0) info[sys] = sinfo[q];
   }
 }
@@ -191,8 +187,8 @@ size_t chol_sys_bytes(int n, int nrhs, int elem_size) {
 
 template <typename T>
 cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                            int32_t* info, cudaStream_t stream) {
-  if (n > kMaxN) return cudaErrorInvalidValue;
+                            int32_t* info, cudaStream_t stream, int64_t ilv) {
+  if (n > kMaxN || ilv < 1) return cudaErrorInvalidValue;
   const int64_t blocks = (batch + kSys - 1) / kSys;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = chol_sys_bytes(n, nrhs, sizeof(T));
@@ -201,13 +197,13 @@ cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T*
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   chol_sys_kernel<T><<<static_cast<unsigned>(blocks), kWarps * 32, bytes, stream>>>(
-      n, nrhs, layout, batch, A, B, info);
+      n, nrhs, layout, batch, A, B, info, ilv);
   return cudaGetLastError();
 }
 
 template cudaError_t launch_chol_sys<float>(int, int, int, int64_t, float*, float*, int32_t*,
-                                            cudaStream_t);
+                                            cudaStream_t, int64_t);
 template cudaError_t launch_chol_sys<double>(int, int, int, int64_t, double*, double*,
-                                             int32_t*, cudaStream_t);
+                                             int32_t*, cudaStream_t, int64_t);
 
 }  // namespace bsolve

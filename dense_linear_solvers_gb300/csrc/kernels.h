@@ -11,6 +11,11 @@ namespace bsolve {
 template <typename T>
 cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                           int32_t* ipiv, int32_t* info, cudaStream_t stream);
+// The same on the interleaved batched layout (element e of system s at
+// (s / ilv) * ilv * size + e * ilv + s % ilv for A, B and ipiv), 1 <= nrhs <= 8.
+template <typename T>
+cudaError_t launch_lu_reg_il(int layout, int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
+                             int32_t* ipiv, int32_t* info, cudaStream_t stream);
 
 // LU + solve, one block of four warps per system in shared memory, 1 <= n <= 128, 0 <= nrhs <= 8.
 template <typename T>
@@ -22,7 +27,7 @@ cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* 
 template <typename T>
 cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                               int32_t* ipiv, int32_t* info, double tau, int ruda,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int64_t ilv = 1);
 
 // Solve with a stored factor: getrs (L\U and the 1-based swap sequence of getrf) and
 // potrs (Cholesky factor), 1 <= n <= 128.
@@ -53,12 +58,12 @@ cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T
 // not symmetric (the whole matrix is read), -3 non-finite result; failures zeroed.
 template <typename T>
 cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                                int32_t* info, int ruda, cudaStream_t stream);
+                                int32_t* info, int ruda, cudaStream_t stream, int64_t ilv = 1);
 
 // Lower Cholesky + solve, sixteen systems per block in lockstep, 1 <= n <= 32.
 template <typename T>
 cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                            int32_t* info, cudaStream_t stream);
+                            int32_t* info, cudaStream_t stream, int64_t ilv = 1);
 
 // Block-tridiagonal block-Cholesky sweep, one thread per system, 1 <= bs <= 8.
 template <typename T>

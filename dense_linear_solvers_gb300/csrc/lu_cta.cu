@@ -41,7 +41,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
               T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info,
-              T tau, int ruda) {
+              T tau, int ruda, int64_t ilv) {
   using Key = typename Traits<T>::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x;
@@ -55,26 +55,30 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   int* const piv = reinterpret_cast<int*>(rcp + n);
   __shared__ int s_info;
 
-  A += s * n * n;
-  B += s * n * nrhs;
+  // element e of the system at A[e * ilv] (ilv = 1: the systems one after another;
+  // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B, ipiv
+  const int64_t blk = s / ilv, sl = s - blk * ilv;
+  A += blk * ilv * n * n + sl;
+  B += blk * ilv * n * nrhs + sl;
+  ipiv += blk * ilv * n + sl;
   // asynchronous element copies: every load of the system is in flight at once
   if (layout == kRowMajor) {
     for (int e = tid; e < n * n; e += kThreads) {
       const int i = e / n, j = e - i * n;
-      cp_async_elem<T>(M + i * P + j, A + e);
+      cp_async_elem<T>(M + i * P + j, A + e * ilv);
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int i = e / nrhs, c = e - i * nrhs;
-      cp_async_elem<T>(M + i * P + n + c, B + e);
+      cp_async_elem<T>(M + i * P + n + c, B + e * ilv);
     }
   } else {
     for (int e = tid; e < n * n; e += kThreads) {
       const int j = e / n, i = e - j * n;
-      cp_async_elem<T>(M + i * P + j, A + e);
+      cp_async_elem<T>(M + i * P + j, A + e * ilv);
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int c = e / n, i = e - c * n;
-      cp_async_elem<T>(M + i * P + n + c, B + e);
+      cp_async_elem<T>(M + i * P + n + c, B + e * ilv);
     }
   }
   if (tid == 0) s_info = 0;
@@ -89,9 +93,9 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       bad |= !isfinite(M[i * P + j]);
     }
     if (__syncthreads_or(bad)) {
-      for (int e = tid; e < n * n; e += kThreads) A[e] = T(0);
-      for (int e = tid; e < n * nrhs; e += kThreads) B[e] = T(0);
-      for (int k = tid; k < n; k += kThreads) ipiv[s * n + k] = -1;
+      for (int e = tid; e < n * n; e += kThreads) A[e * ilv] = T(0);
+      for (int e = tid; e < n * nrhs; e += kThreads) B[e * ilv] = T(0);
+      for (int k = tid; k < n; k += kThreads) ipiv[k * ilv] = -1;
       if (tid == 0) info[s] = -1;
       return;
     }
@@ -218,23 +222,23 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   if (layout == kRowMajor) {
     for (int e = tid; e < n * n; e += kThreads) {
       const int i = e / n, j = e - i * n;
-      A[e] = zero_all ? T(0) : M[i * P + j];
+      A[e * ilv] = zero_all ? T(0) : M[i * P + j];
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int i = e / nrhs, c = e - i * nrhs;
-      B[e] = zero_x ? T(0) : M[i * P + n + c];
+      B[e * ilv] = zero_x ? T(0) : M[i * P + n + c];
     }
   } else {
     for (int e = tid; e < n * n; e += kThreads) {
       const int j = e / n, i = e - j * n;
-      A[e] = zero_all ? T(0) : M[i * P + j];
+      A[e * ilv] = zero_all ? T(0) : M[i * P + j];
     }
     for (int e = tid; e < n * nrhs; e += kThreads) {
       const int c = e / n, i = e - c * n;
-      B[e] = zero_x ? T(0) : M[i * P + n + c];
+      B[e * ilv] = zero_x ? T(0) : M[i * P + n + c];
     }
   }
-  for (int k = tid; k < n; k += kThreads) ipiv[s * n + k] = zero_all ? -1 : piv[k];
+  for (int k = tid; k < n; k += kThreads) ipiv[k * ilv] = zero_all ? -1 : piv[k];
   if (tid == 0) info[s] = status;
 }
 
@@ -249,7 +253,8 @@ size_t lu_cta_bytes(int n, int nrhs, int elem_size) {
 template <typename T>
 cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                               int32_t* ipiv, int32_t* info, double tau, int ruda,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, int64_t ilv) {
+  if (ilv < 1) return cudaErrorInvalidValue;
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = lu_cta_bytes(n, nrhs, sizeof(T));
   cudaError_t e = cudaFuncSetAttribute(lu_cta_kernel<T>,
@@ -257,14 +262,14 @@ cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, 
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   lu_cta_kernel<T><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
-      n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda);
+      n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, ilv);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                            int32_t* ipiv, int32_t* info, cudaStream_t stream) {
-  return launch_lu_smem_ex<T>(layout, n, nrhs, batch, A, B, ipiv, info, 1.0, 0, stream);
+  return launch_lu_smem_ex<T>(layout, n, nrhs, batch, A, B, ipiv, info, 1.0, 0, stream, 1);
 }
 
 template cudaError_t launch_lu_smem<float>(int, int, int, int64_t, float*, float*, int32_t*,
@@ -272,8 +277,9 @@ template cudaError_t launch_lu_smem<float>(int, int, int, int64_t, float*, float
 template cudaError_t launch_lu_smem<double>(int, int, int, int64_t, double*, double*, int32_t*,
                                             int32_t*, cudaStream_t);
 template cudaError_t launch_lu_smem_ex<float>(int, int, int, int64_t, float*, float*, int32_t*,
-                                              int32_t*, double, int, cudaStream_t);
+                                              int32_t*, double, int, cudaStream_t, int64_t);
 template cudaError_t launch_lu_smem_ex<double>(int, int, int, int64_t, double*, double*,
-                                               int32_t*, int32_t*, double, int, cudaStream_t);
+                                               int32_t*, int32_t*, double, int, cudaStream_t,
+                                               int64_t);
 
 }  // namespace bsolve

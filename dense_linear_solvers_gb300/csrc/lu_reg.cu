@@ -8,7 +8,20 @@ namespace lu_reg_detail {
 template <typename T, int LAYOUT>
 cudaError_t launch_layout(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
                           int32_t* info, cudaStream_t stream);
+template <typename T, int LAYOUT>
+cudaError_t launch_layout_il(int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
+                             int32_t* ipiv, int32_t* info, cudaStream_t stream);
 }  // namespace lu_reg_detail
+
+template <typename T>
+cudaError_t launch_lu_reg_il(int layout, int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
+                             int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if (layout == kRowMajor)
+    return lu_reg_detail::launch_layout_il<T, kRowMajor>(n, nrhs, batch, ilv, A, B, ipiv, info,
+                                                         stream);
+  return lu_reg_detail::launch_layout_il<T, kColMajor>(n, nrhs, batch, ilv, A, B, ipiv, info,
+                                                       stream);
+}
 
 template <typename T>
 cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
@@ -20,6 +33,10 @@ cudaError_t launch_lu_reg(int layout, int n, int nrhs, int64_t batch, T* A, T* B
 
 template cudaError_t launch_lu_reg<float>(int, int, int, int64_t, float*, float*, int32_t*,
                                           int32_t*, cudaStream_t);
+template cudaError_t launch_lu_reg_il<float>(int, int, int, int64_t, int64_t, float*, float*,
+                                             int32_t*, int32_t*, cudaStream_t);
+template cudaError_t launch_lu_reg_il<double>(int, int, int, int64_t, int64_t, double*, double*,
+                                              int32_t*, int32_t*, cudaStream_t);
 template cudaError_t launch_lu_reg<double>(int, int, int, int64_t, double*, double*, int32_t*,
                                            int32_t*, cudaStream_t);
 

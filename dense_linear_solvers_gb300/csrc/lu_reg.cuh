@@ -135,10 +135,13 @@ __device__ __forceinline__ void load_vec_shared(const T* p, T (&r)[N]) {
 }
 
 // FULL: n == NT and nrhs == RT (every guard compiles away). RT = 0: factor only (getrf).
-template <typename T, int NT, int RT, int LAYOUT, bool FULL>
+// IL: the interleaved batched layout (TDLS API, "solver_static.hpp File Reference":
+// element e of system s at base_s[e * ilv], base_s = (s / ilv) * ilv * size + s % ilv,
+// for A, B and ipiv; info one entry per system); ilv is read only when IL.
+template <typename T, int NT, int RT, int LAYOUT, bool FULL, bool IL = false>
 __global__ void __launch_bounds__(kThreads)
 lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict__ B,
-              int32_t* __restrict__ ipiv, int32_t* __restrict__ info) {
+              int32_t* __restrict__ ipiv, int32_t* __restrict__ info, int64_t ilv) {
   using Key = typename Traits<T>::Key;
   constexpr int G = NT;
   constexpr int GPW = 32 / G;                 // groups (systems) per warp
@@ -165,7 +168,21 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
   T b[RB];
   const int64_t sA = s * n * n;
   const int64_t sB = s * n * nrhs;
-  if (row_ok) {
+  // interleaved: the system's first element of A, B and ipiv, and the element stride
+  const int64_t blk = IL ? s / ilv : 0;
+  const int64_t sl = IL ? s - blk * ilv : 0;
+  const int64_t eA = IL ? blk * ilv * n * n + sl : 0;
+  const int64_t eB = IL ? blk * ilv * n * nrhs + sl : 0;
+  if (IL && row_ok) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      a[j] = (FULL || j < n) ? A[eA + (LAYOUT == kRowMajor ? t * n + j : j * n + t) * ilv] : T(0);
+#pragma unroll
+    for (int c = 0; c < RT; ++c)
+      b[c] = (FULL || c < nrhs)
+                 ? B[eB + (LAYOUT == kRowMajor ? t * nrhs + c : c * n + t) * ilv] : T(0);
+    if constexpr (!kSolve) b[0] = T(0);
+  } else if (row_ok) {
     if (LAYOUT == kRowMajor) {
       if (FULL) {
         load_vec<T, NT>(A + sA + static_cast<int64_t>(t) * NT, a);
@@ -317,7 +334,20 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     }
   }
 
-  if (row_ok) {
+  if (IL && row_ok) {
+    if (inf != 0) {
+#pragma unroll
+      for (int c = 0; c < RT; ++c) b[c] = T(0);
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      if (FULL || j < n) A[eA + (LAYOUT == kRowMajor ? pos * n + j : j * n + pos) * ilv] = a[j];
+#pragma unroll
+    for (int c = 0; c < RT; ++c)
+      if (FULL || c < nrhs) B[eB + (LAYOUT == kRowMajor ? pos * nrhs + c : c * n + pos) * ilv] = b[c];
+    ipiv[blk * ilv * n + sl + pos * ilv] = my_ipiv;
+    if (t == 0) info[s] = inf;
+  } else if (row_ok) {
     if (inf != 0) {
 #pragma unroll
       for (int c = 0; c < RT; ++c) b[c] = T(0);
@@ -354,12 +384,44 @@ cudaError_t launch_tier(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipi
   const int64_t blocks = (batch + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   if (n == NT && nrhs == RT)
-    lu_reg_kernel<T, NT, RT, LAYOUT, true>
-        <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv, info);
+    lu_reg_kernel<T, NT, RT, LAYOUT, true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        n, nrhs, batch, A, B, ipiv, info, 1);
   else
-    lu_reg_kernel<T, NT, RT, LAYOUT, false>
-        <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv, info);
+    lu_reg_kernel<T, NT, RT, LAYOUT, false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        n, nrhs, batch, A, B, ipiv, info, 1);
   return cudaGetLastError();
+}
+
+// The interleaved batched layout: one instance per tier (the order and right-hand-side
+// guards kept), systems in blocks of ilv.
+template <typename T, int NT, int RT, int LAYOUT>
+cudaError_t launch_tier_il(int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
+                           int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  constexpr int per_block = kWarps * (32 / NT);
+  const int64_t blocks = (batch + per_block - 1) / per_block;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  lu_reg_kernel<T, NT, RT, LAYOUT, false, true>
+      <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv, info,
+                                                               ilv);
+  return cudaGetLastError();
+}
+
+template <typename T, int NT, int LAYOUT>
+cudaError_t launch_rhs_il(int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
+                          int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if (nrhs <= 1) return launch_tier_il<T, NT, 1, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (nrhs <= 2) return launch_tier_il<T, NT, 2, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (nrhs <= 4) return launch_tier_il<T, NT, 4, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  return launch_tier_il<T, NT, 8, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+}
+
+template <typename T, int LAYOUT>
+cudaError_t launch_layout_il(int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
+                             int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if (n <= 4) return launch_rhs_il<T, 4, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (n <= 8) return launch_rhs_il<T, 8, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (n <= 16) return launch_rhs_il<T, 16, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  return launch_rhs_il<T, 32, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
 }
 
 template <typename T, int NT, int LAYOUT>

@@ -23,59 +23,61 @@ namespace {
 
 __host__ __device__ inline int odd_pitch(int w) { return w | 1; }
 
-// layouts: bit 0 the storage order of A, bit 1 that of B.
+// layouts: bit 0 the storage order of A, bit 1 that of B. Element e of the system lives at
+// A[e * st] (st = 1: the systems one after another; otherwise the interleaved batched
+// layout), likewise B.
 template <typename T>
 __device__ __forceinline__ void load_system(const T* __restrict__ A, const T* __restrict__ B,
                                             T* M, int n, int nrhs, int P, int layouts,
-                                            bool lower_only, int lane) {
+                                            bool lower_only, int lane, int64_t st) {
   if ((layouts & 1) == kRowMajor) {
     for (int i = 0; i < n; ++i) {
       const int jend = lower_only ? i + 1 : n;
-      for (int j = lane; j < jend; j += 32) M[i * P + j] = A[i * n + j];
+      for (int j = lane; j < jend; j += 32) M[i * P + j] = A[(i * n + j) * st];
     }
   } else {
     for (int j = 0; j < n; ++j)
-      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) M[i * P + j] = A[j * n + i];
+      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) M[i * P + j] = A[(j * n + i) * st];
   }
   if ((layouts >> 1) == kRowMajor) {
     for (int e = lane; e < n * nrhs; e += 32) {
       const int i = e / nrhs, c = e - i * nrhs;
-      M[i * P + n + c] = B[e];
+      M[i * P + n + c] = B[e * st];
     }
   } else {
     for (int c = 0; c < nrhs; ++c)
-      for (int i = lane; i < n; i += 32) M[i * P + n + c] = B[c * n + i];
+      for (int i = lane; i < n; i += 32) M[i * P + n + c] = B[(c * n + i) * st];
   }
 }
 
 template <typename T>
 __device__ __forceinline__ void store_system(T* __restrict__ A, T* __restrict__ B, const T* M,
                                              int n, int nrhs, int P, int layouts,
-                                             bool lower_only, bool zero_x, int lane) {
+                                             bool lower_only, bool zero_x, int lane, int64_t st) {
   if ((layouts & 1) == kRowMajor) {
     for (int i = 0; i < n; ++i) {
       const int jend = lower_only ? i + 1 : n;
-      for (int j = lane; j < jend; j += 32) A[i * n + j] = M[i * P + j];
+      for (int j = lane; j < jend; j += 32) A[(i * n + j) * st] = M[i * P + j];
     }
   } else {
     for (int j = 0; j < n; ++j)
-      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) A[j * n + i] = M[i * P + j];
+      for (int i = (lower_only ? j : 0) + lane; i < n; i += 32) A[(j * n + i) * st] = M[i * P + j];
   }
   if ((layouts >> 1) == kRowMajor) {
     for (int e = lane; e < n * nrhs; e += 32) {
       const int i = e / nrhs, c = e - i * nrhs;
-      B[e] = zero_x ? T(0) : M[i * P + n + c];
+      B[e * st] = zero_x ? T(0) : M[i * P + n + c];
     }
   } else {
     for (int c = 0; c < nrhs; ++c)
-      for (int i = lane; i < n; i += 32) B[c * n + i] = zero_x ? T(0) : M[i * P + n + c];
+      for (int i = lane; i < n; i += 32) B[(c * n + i) * st] = zero_x ? T(0) : M[i * P + n + c];
   }
 }
 
 template <typename T>
 __global__ void __launch_bounds__(32)
 chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
-                 T* __restrict__ B, int32_t* __restrict__ info, int ruda) {
+                 T* __restrict__ B, int32_t* __restrict__ info, int ruda, int64_t ilv) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x;
   const int64_t s = blockIdx.x;
@@ -84,10 +86,11 @@ chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
   T* M = reinterpret_cast<T*>(smem_raw);
   T* rcp = M + n * P;
 
-  A += s * n * n;
-  B += s * n * nrhs;
+  const int64_t blk = s / ilv, sl = s - blk * ilv;
+  A += blk * ilv * n * n + sl;
+  B += blk * ilv * n * nrhs + sl;
   // the RUDA status contract reads the whole matrix: its symmetry is checked
-  load_system<T>(A, B, M, n, nrhs, P, layouts, !ruda, lane);
+  load_system<T>(A, B, M, n, nrhs, P, layouts, !ruda, lane, ilv);
   __syncwarp();
 
   int inf = 0;
@@ -178,7 +181,7 @@ chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     }
     __syncwarp();
   }
-  store_system<T>(A, B, M, n, nrhs, P, layouts, true, inf != 0, lane);
+  store_system<T>(A, B, M, n, nrhs, P, layouts, true, inf != 0, lane, ilv);
   if (lane == 0) info[s] = inf;
 }
 
@@ -191,8 +194,9 @@ size_t chol_smem_bytes(int n, int nrhs, int elem_size) {
 
 template <typename T>
 cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                                int32_t* info, int ruda, cudaStream_t stream) {
+                                int32_t* info, int ruda, cudaStream_t stream, int64_t ilv) {
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  if (ilv < 1) return cudaErrorInvalidValue;
   const size_t bytes = chol_smem_bytes(n, nrhs, sizeof(T));
   cudaError_t e = cudaFuncSetAttribute(chol_smem_kernel<T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -200,20 +204,20 @@ cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A
   if (e != cudaSuccess) return e;
   chol_smem_kernel<T><<<static_cast<unsigned>(batch), 32, bytes, stream>>>(n, nrhs, layout,
                                                                            batch, A, B, info,
-                                                                           ruda);
+                                                                           ruda, ilv);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_chol_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                              int32_t* info, cudaStream_t stream) {
-  return launch_chol_smem_ex<T>(layout, n, nrhs, batch, A, B, info, 0, stream);
+  return launch_chol_smem_ex<T>(layout, n, nrhs, batch, A, B, info, 0, stream, 1);
 }
 
 template cudaError_t launch_chol_smem_ex<float>(int, int, int, int64_t, float*, float*, int32_t*,
-                                                int, cudaStream_t);
+                                                int, cudaStream_t, int64_t);
 template cudaError_t launch_chol_smem_ex<double>(int, int, int, int64_t, double*, double*,
-                                                 int32_t*, int, cudaStream_t);
+                                                 int32_t*, int, cudaStream_t, int64_t);
 template cudaError_t launch_chol_smem<float>(int, int, int, int64_t, float*, float*, int32_t*,
                                              cudaStream_t);
 template cudaError_t launch_chol_smem<double>(int, int, int, int64_t, double*, double*,

@@ -166,6 +166,17 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    BS_COL_MAJOR, S = A and the call is the plain one. Runs as a factor
  *                    launch and a solve launch, for 1 <= n <= 128, 1 <= nrhs <= 65536;
  *                    with BS_CONTRACT_RUDA it is BS_ERR_UNSUPPORTED.
+ *   interleave       the batched layout (TDLS API, "solver_static.hpp File Reference":
+ *                    element e of a system at base[e * stride]). 0 or 1: AoS, system s
+ *                    at s * size (the plain layout). W > 1: AoSoA, the systems in blocks
+ *                    of W, element e of system s (e its offset in the system's own storage
+ *                    order, size = n*n for A, n*nrhs for B, n for ipiv) at
+ *                    (s / W) * W * size + e * W + s % W; W >= batch is SoA. A, B and
+ *                    ipiv then hold ceil(batch / W) * W systems each (the slots of the last
+ *                    block past the batch are neither read nor written); info keeps one
+ *                    entry per system. For both calls, nrhs <= 8, default contract, and
+ *                    for LU tau = 1 and no transposed_factor (others: BS_ERR_UNSUPPORTED);
+ *                    negative: BS_ERR_INVALID_ARG.
  * opts == NULL or default options run the plain call. Thresholds and the RUDA contract
  * run one system per CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the
  * CPU oracle's bit for bit. A threshold outside (0, 1], an unknown contract or a
@@ -177,6 +188,7 @@ typedef struct {
   double pivot_threshold; /* in (0, 1]; 1 = partial pivoting */
   int status_contract;    /* a bs_contract */
   int transposed_factor;  /* 1: TDLS's row-major reading (factor of A^T, mirror solve) */
+  int64_t interleave;     /* batched layout: 0/1 AoS, W > 1 AoSoA blocks of W (SoA: >= batch) */
 } bs_options;
 
 BS_API bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,

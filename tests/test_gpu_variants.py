@@ -165,3 +165,83 @@ def test_transposed_factor_col_major_is_plain(dtype):
         r1 = gpu_lu_mirror(A, B, COL_MAJOR, 1.0)
         r2 = gpu_lu_ex(A, B, COL_MAJOR, 1.0, bs.BS_CONTRACT_DEFAULT)
         assert all(np.array_equal(x, y) for x, y in zip(r1, r2))
+
+
+# ------------------------------------------------------------ interleaved batched layouts
+def _il_case(rng, dtype, batch, n, nrhs, layout, spd=False):
+    if spd:
+        G = rng.standard_normal((batch, n, n))
+        Al = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dtype)
+        Al[batch // 2, n - 1, n - 1] = -1.0          # a failing minor
+    else:
+        Al = rng.standard_normal((batch, n, n)).astype(dtype)
+        Al[batch // 2, :, n // 2] = 0                # a singular system
+    Bl = rng.standard_normal((batch, n, nrhs)).astype(dtype)
+    return to_storage(Al, layout), to_storage(Bl, layout)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_interleaved_lu(dtype, layout):
+    """AoSoA (blocks of 2, 3 and 32, the last block ragged), SoA (W = batch) and SoA
+    with spare capacity, every tier of the register kernel and the one-CTA kernel,
+    against the oracle bit for bit; the slots past the batch are never written."""
+    from gen.workloads import deinterleave, interleave
+    rng = np.random.default_rng(1616 + layout)
+    batch = 45
+    for n in (1, 2, 3, 5, 8, 13, 16, 17, 31, 32, 33, 40, 64, 65, 128):
+        for w in (2, 3, 32, batch, batch + 5):
+            nrhs = int(rng.integers(1, 9))
+            A, B = _il_case(rng, dtype, batch, n, nrhs, layout)
+            Af, Bf = interleave(A, w), interleave(B, w)
+            So, Xo, ipo, info_o, tie = oracle.getrf_getrs_il(Af, Bf, n, nrhs, batch, w, layout,
+                                                             nthreads=NT)
+            tA, tB = _dev(Af), _dev(Bf)
+            ipiv = torch.full((Af.size // n,), SENT, dtype=torch.int32, device="cuda")
+            info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+            bs.bs_getrf_getrs_batched_ex(tA, tB, ipiv, info, layout, interleave=w,
+                                         shape=(batch, n, nrhs))
+            Ag, Bg, ipg, infg = _host(tA), _host(tB), _host(ipiv), _host(info)
+            clean = tie < 0
+            assert clean.sum() >= batch - 3, (n, w)
+            for got, ref, shape in ((Ag, So, A.shape[1:]), (Bg, Xo, B.shape[1:])):
+                g2 = deinterleave(got, batch, w, shape)
+                r2 = deinterleave(ref, batch, w, shape)
+                assert np.array_equal(g2[clean], r2[clean]), (n, w)
+                assert np.all(np.isnan(got[np.isnan(interleave(np.zeros((batch,) + shape), w))]))
+            pg = deinterleave(ipg, batch, w, (n,))
+            assert np.array_equal(pg[clean], deinterleave(ipo, batch, w, (n,))[clean]), (n, w)
+            pads = np.isnan(interleave(np.zeros((batch, n)), w))
+            assert np.all(ipg[:pads.size][pads] == SENT)
+            assert np.array_equal(infg[clean], info_o[clean]) and infg[batch // 2] > 0
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+@pytest.mark.parametrize("fill", [bs.BS_LOWER, bs.BS_UPPER])
+def test_interleaved_cholesky(dtype, layout, fill):
+    from gen.workloads import deinterleave, interleave
+    rng = np.random.default_rng(1717 + 2 * layout + fill)
+    batch = 37
+    for n in (1, 2, 4, 7, 16, 31, 32, 33, 64, 100):
+        for w in (2, 16, 32, batch, batch + 3):
+            nrhs = int(rng.integers(1, 9))
+            A, B = _il_case(rng, dtype, batch, n, nrhs, layout, spd=True)
+            Af, Bf = interleave(A, w), interleave(B, w)
+            Lo, Xo, info_o = oracle.potrf_potrs_il(Af, Bf, n, nrhs, batch, w, layout, fill,
+                                                   nthreads=NT)
+            tA, tB = _dev(Af), _dev(Bf)
+            info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+            bs.bs_potrf_potrs_batched_ex(tA, tB, info, layout, fill, interleave=w,
+                                         shape=(batch, n, nrhs))
+            Ag, Bg, infg = _host(tA), _host(tB), _host(info)
+            assert np.array_equal(infg, info_o) and infg[batch // 2] == n, (n, w)
+            ok = infg == 0
+            for got, ref, shape in ((Ag, Lo, A.shape[1:]), (Bg, Xo, B.shape[1:])):
+                # the systems that factored, bit for bit (the untouched triangle too)
+                g2 = deinterleave(got, batch, w, shape)
+                assert np.array_equal(g2[ok], deinterleave(ref, batch, w, shape)[ok]), (n, w)
+                # the slots past the batch are never written
+                pads = np.isnan(interleave(np.zeros((batch,) + shape), w))
+                assert np.all(np.isnan(got[pads]))
+            assert np.all(deinterleave(Bg, batch, w, B.shape[1:])[~ok] == 0)
