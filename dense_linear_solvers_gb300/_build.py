@@ -23,7 +23,8 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 LIB_SOURCES = ["api.cu", "lu_reg.cu", "lu_reg_f32_row.cu", "lu_reg_f32_col.cu", "lu_reg_f64_row.cu",
                "lu_reg_f64_col.cu", "lu_reg_il_f32.cu", "lu_reg_il_f64.cu", "lu_cta.cu",
-               "smem_solvers.cu", "chol_sys.cu", "bdsv.cu", "bdmv.cu", "solve.cu"]
+               "smem_solvers.cu", "chol_sys.cu", "bdsv.cu", "bdmv.cu", "solve.cu",
+               "solve_lane.cu"]
 PROBE_SOURCES = ["fma_peak.cu"]
 
 

@@ -39,6 +39,11 @@ cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
                          const int32_t* zinfo, cudaStream_t stream);
+// potrs for FP64, 1 <= n <= 32, nrhs == 1: one system per lane, the factor streamed by
+// columns through shared memory (layout bit 0: the factor's storage order).
+cudaError_t launch_potrs_lane(int layout, int n, int nrhs, int64_t batch, const double* L,
+                              double* B, const int32_t* zinfo, cudaStream_t stream);
+
 // The mirror solve of the row-major reading (U^T z = b, L^T w = z, x = P^T w) with the LU
 // factor of S, the stored array read column-major; layout packs S's order (bit 0) and B's.
 template <typename T>

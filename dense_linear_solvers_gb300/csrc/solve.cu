@@ -491,6 +491,9 @@ cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
                          const int32_t* zinfo, cudaStream_t stream) {
+  // FP64, n <= 32, one right-hand side: one system per lane (solve_lane.cu)
+  if constexpr (std::is_same<T, double>::value)
+    if (n <= 32 && nrhs == 1) return launch_potrs_lane(layout, n, nrhs, batch, L, B, zinfo, stream);
   return launch_kind<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, zinfo, stream);
 }
 

@@ -19,7 +19,7 @@ import torch
 import dense_linear_solvers_gb300 as bs
 import oracle
 from gen import workloads as W
-from gen.workloads import COL_MAJOR, ROW_MAJOR, to_storage
+from gen.workloads import COL_MAJOR, ROW_MAJOR, from_storage, to_storage
 from tests import parity
 
 pytestmark = pytest.mark.gpu
@@ -191,6 +191,31 @@ def test_potrf_potrs_every_order(dtype, layout):
         A = to_storage(Al.astype(dtype), layout)
         B = to_storage(rng.standard_normal((19, n, nrhs)).astype(dtype), layout)
         _chol_case(A, B, layout)
+
+
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+@pytest.mark.parametrize("fill", [bs.BS_LOWER, bs.BS_UPPER])
+def test_potrs_fp64_one_rhs_every_order(layout, fill):
+    """FP64 potrs with one right-hand side runs one system per lane: every order 1..32,
+    both storage orders and fills, a batch of several warps and blocks with a ragged
+    tail, the unread triangle NaN; X equals the oracle's bit for bit."""
+    rng = np.random.default_rng(1818 + 2 * layout + fill)
+    batch = 197
+    for n in range(1, 33):
+        G = rng.standard_normal((batch, n, n))
+        Al = G @ np.swapaxes(G, 1, 2) + n * np.eye(n)
+        A = to_storage(Al, layout)
+        Lo, info_o = oracle.potrf(A, layout, fill=fill, nthreads=NT)
+        assert np.all(info_o == 0)
+        tri = np.triu_indices(n, 1) if fill == bs.BS_LOWER else np.tril_indices(n, -1)
+        Ll = from_storage(Lo, layout).copy()
+        Ll[:, tri[0], tri[1]] = np.nan
+        Ln = to_storage(Ll, layout)
+        B = to_storage(rng.standard_normal((batch, n, 1)), layout)
+        Xo = oracle.potrs(Ln, B, layout, fill=fill, nthreads=NT)
+        tB = _dev(B)
+        bs.bs_potrs_batched(_dev(Ln), tB, layout, fill)
+        assert np.array_equal(_host(tB), Xo), n
 
 
 # ------------------------------------------------------------------ bdsv
