@@ -36,10 +36,12 @@ __host__ __device__ inline int tri(int i) { return i * (i + 1) / 2; }
 
 __host__ __device__ inline int sys_stride(int n, int nrhs) { return (tri(n) + n * nrhs) | 1; }
 
-template <typename T>
+// IL: the interleaved batched layout (element stride ilv); the plain instance has stride 1
+template <typename T, bool IL>
 __global__ void __launch_bounds__(kWarps * 32)
 chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
-                T* __restrict__ B, int32_t* __restrict__ info, int64_t ilv) {
+                T* __restrict__ B, int32_t* __restrict__ info, int64_t ilv_) {
+  const int64_t ilv = IL ? ilv_ : 1;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int alay = layouts & 1, blay = layouts >> 1;   // storage orders of A and of B
   const int D = sys_stride(n, nrhs);
@@ -64,7 +66,7 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     if (sys < batch) {
       // element e of system sys at As[e * ilv] (ilv = 1: the systems one after another;
       // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B
-      const int64_t blk = sys / ilv, sl = sys - blk * ilv;
+      const int64_t blk = IL ? sys / ilv : sys, sl = IL ? sys - blk * ilv : 0;
       const T* As = A + blk * ilv * n * n + sl;
       const T* Bs = B + blk * ilv * n * nrhs + sl;
       for (int j = 0; j < n; ++j)
@@ -163,7 +165,7 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     const int64_t sys = s0 + q;
     if (sys >= batch) continue;
     const T* const Mq = M + q * D;
-    const int64_t blk = sys / ilv, sl = sys - blk * ilv;
+    const int64_t blk = IL ? sys / ilv : sys, sl = IL ? sys - blk * ilv : 0;
     T* As = A + blk * ilv * n * n + sl;
     T* Bs = B + blk * ilv * n * nrhs + sl;
     const bool failed = sinfo[q] != 0;
@@ -192,12 +194,16 @@ cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T*
   const int64_t blocks = (batch + kSys - 1) / kSys;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = chol_sys_bytes(n, nrhs, sizeof(T));
-  cudaError_t e = cudaFuncSetAttribute(chol_sys_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
+  cudaError_t e = cudaFuncSetAttribute(
+      ilv == 1 ? chol_sys_kernel<T, false> : chol_sys_kernel<T, true>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  chol_sys_kernel<T><<<static_cast<unsigned>(blocks), kWarps * 32, bytes, stream>>>(
-      n, nrhs, layout, batch, A, B, info, ilv);
+  if (ilv == 1)
+    chol_sys_kernel<T, false><<<static_cast<unsigned>(blocks), kWarps * 32, bytes, stream>>>(
+        n, nrhs, layout, batch, A, B, info, 1);
+  else
+    chol_sys_kernel<T, true><<<static_cast<unsigned>(blocks), kWarps * 32, bytes, stream>>>(
+        n, nrhs, layout, batch, A, B, info, ilv);
   return cudaGetLastError();
 }
 

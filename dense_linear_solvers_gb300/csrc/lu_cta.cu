@@ -37,11 +37,13 @@ constexpr int kBlk = 4;  // rows per back-substitution block
 
 __host__ __device__ inline int odd_pitch(int w) { return w | 1; }
 
-template <typename T>
+// IL: the interleaved batched layout (element stride ilv); the plain instance has stride 1
+template <typename T, bool IL>
 __global__ void __launch_bounds__(kThreads)
 lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
               T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info,
-              T tau, int ruda, int64_t ilv) {
+              T tau, int ruda, int64_t ilv_) {
+  const int64_t ilv = IL ? ilv_ : 1;
   using Key = typename Traits<T>::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x;
@@ -57,7 +59,7 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
 
   // element e of the system at A[e * ilv] (ilv = 1: the systems one after another;
   // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B, ipiv
-  const int64_t blk = s / ilv, sl = s - blk * ilv;
+  const int64_t blk = IL ? s / ilv : s, sl = IL ? s - blk * ilv : 0;
   A += blk * ilv * n * n + sl;
   B += blk * ilv * n * nrhs + sl;
   ipiv += blk * ilv * n + sl;
@@ -257,12 +259,16 @@ cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, 
   if (ilv < 1) return cudaErrorInvalidValue;
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = lu_cta_bytes(n, nrhs, sizeof(T));
-  cudaError_t e = cudaFuncSetAttribute(lu_cta_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
+  cudaError_t e = cudaFuncSetAttribute(
+      ilv == 1 ? lu_cta_kernel<T, false> : lu_cta_kernel<T, true>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  lu_cta_kernel<T><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
-      n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, ilv);
+  if (ilv == 1)
+    lu_cta_kernel<T, false><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
+        n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, 1);
+  else
+    lu_cta_kernel<T, true><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
+        n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, ilv);
   return cudaGetLastError();
 }
 

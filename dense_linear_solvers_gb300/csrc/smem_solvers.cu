@@ -74,10 +74,12 @@ __device__ __forceinline__ void store_system(T* __restrict__ A, T* __restrict__ 
   }
 }
 
-template <typename T>
+// IL: the interleaved batched layout (element stride ilv); the plain instance has stride 1
+template <typename T, bool IL>
 __global__ void __launch_bounds__(32)
 chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
-                 T* __restrict__ B, int32_t* __restrict__ info, int ruda, int64_t ilv) {
+                 T* __restrict__ B, int32_t* __restrict__ info, int ruda, int64_t ilv_) {
+  const int64_t ilv = IL ? ilv_ : 1;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x;
   const int64_t s = blockIdx.x;
@@ -86,7 +88,7 @@ chol_smem_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
   T* M = reinterpret_cast<T*>(smem_raw);
   T* rcp = M + n * P;
 
-  const int64_t blk = s / ilv, sl = s - blk * ilv;
+  const int64_t blk = IL ? s / ilv : s, sl = IL ? s - blk * ilv : 0;
   A += blk * ilv * n * n + sl;
   B += blk * ilv * n * nrhs + sl;
   // the RUDA status contract reads the whole matrix: its symmetry is checked
@@ -198,13 +200,16 @@ cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   if (ilv < 1) return cudaErrorInvalidValue;
   const size_t bytes = chol_smem_bytes(n, nrhs, sizeof(T));
-  cudaError_t e = cudaFuncSetAttribute(chol_smem_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
+  cudaError_t e = cudaFuncSetAttribute(
+      ilv == 1 ? chol_smem_kernel<T, false> : chol_smem_kernel<T, true>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  chol_smem_kernel<T><<<static_cast<unsigned>(batch), 32, bytes, stream>>>(n, nrhs, layout,
-                                                                           batch, A, B, info,
-                                                                           ruda, ilv);
+  if (ilv == 1)
+    chol_smem_kernel<T, false><<<static_cast<unsigned>(batch), 32, bytes, stream>>>(
+        n, nrhs, layout, batch, A, B, info, ruda, 1);
+  else
+    chol_smem_kernel<T, true><<<static_cast<unsigned>(batch), 32, bytes, stream>>>(
+        n, nrhs, layout, batch, A, B, info, ruda, ilv);
   return cudaGetLastError();
 }
 
