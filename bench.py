@@ -212,10 +212,10 @@ def interleave_device(x, w: int):
 class SplitProblem(Problem):
     """One of NEXT_ROWS: the inputs of its base workload, the operation alone."""
 
-    def __init__(self, name: str, device):
+    def __init__(self, name: str, device, batch: int | None = None):
         import torch
         base, op = NEXT_ROWS[name]
-        super().__init__(base, None, device)
+        super().__init__(base, batch, device)
         self.op = op
         bs, w = self.bs, self.w
         a, b = self.inputs
