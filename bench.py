@@ -192,7 +192,8 @@ NEXT_ROWS = {
 IL_WIDTH = {"getrf_getrs_aosoa32_f32_n16": 32, "potrf_potrs_soa_f64_n32": None}
 KERNEL_SOURCES.update({
     "getrf_f32_n16": ["lu_reg.cuh", "common.cuh"], "getrs_f32_n16": ["solve.cu", "common.cuh"],
-    "potrf_f64_n32": ["chol_sys.cu", "common.cuh"], "potrs_f64_n32": ["solve_lane.cu", "common.cuh"],
+    "potrf_f64_n32": ["chol_sys.cu", "common.cuh"],
+    "potrs_f64_n32": ["solve_lane.cu", "common.cuh"],
     "bdsv_factor_f64_32x8": ["bdsv.cu", "common.cuh"],
     "bdsv_solve_f64_32x8": ["bdsv.cu", "common.cuh"], "bdmv_f64_32x8": ["bdmv.cu", "common.cuh"],
     "getrf_getrs_T_f32_n16": ["solve.cu", "lu_reg.cuh", "common.cuh"],

@@ -64,8 +64,9 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(
-                    f"{LIB_PATH} is missing: build it with dense_linear_solvers_gb300._build.build() "
-                    "(or __graft_entry__.build()); there is no fallback path")
+                    f"{LIB_PATH} is missing: build it with "
+                    "dense_linear_solvers_gb300._build.build() (or __graft_entry__.build()); "
+                    "there is no fallback path")
             L = ctypes.CDLL(LIB_PATH)
             i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
             L.bs_getrf_getrs_batched.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp, vp]

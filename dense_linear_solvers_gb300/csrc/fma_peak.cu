@@ -32,8 +32,10 @@ __global__ void fma_chains_kernel(T* __restrict__ sink, int iters, T a, T b) {
 
 }  // namespace
 
-extern "C" __attribute__((visibility("default"))) int bs_probe_fma_launch(int dtype, int blocks, int threads, int iters,
-                                   void* sink, void* stream) {
+#define BS_PROBE_API extern "C" __attribute__((visibility("default")))
+
+BS_PROBE_API int bs_probe_fma_launch(int dtype, int blocks, int threads, int iters, void* sink,
+                                     void* stream) {
   if (blocks <= 0 || threads <= 0 || threads > 1024 || iters <= 0 || sink == nullptr)
     return 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -49,4 +51,4 @@ extern "C" __attribute__((visibility("default"))) int bs_probe_fma_launch(int dt
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
-extern "C" __attribute__((visibility("default"))) int64_t bs_probe_fma_flops_per_thread_iter(void) { return 2LL * CHAINS * UNROLL; }
+BS_PROBE_API int64_t bs_probe_fma_flops_per_thread_iter(void) { return 2LL * CHAINS * UNROLL; }

@@ -4,7 +4,7 @@
 
 namespace bsolve {
 namespace lu_reg_detail {
-template cudaError_t launch_layout<float, kRowMajor>(int, int, int64_t, float*, float*, int32_t*, int32_t*,
-                                            cudaStream_t);
+template cudaError_t launch_layout<float, kRowMajor>(int, int, int64_t, float*, float*, int32_t*,
+                                                int32_t*, cudaStream_t);
 }  // namespace lu_reg_detail
 }  // namespace bsolve

@@ -4,7 +4,7 @@
 
 namespace bsolve {
 namespace lu_reg_detail {
-template cudaError_t launch_layout<double, kColMajor>(int, int, int64_t, double*, double*, int32_t*, int32_t*,
-                                            cudaStream_t);
+template cudaError_t launch_layout<double, kColMajor>(int, int, int64_t, double*, double*, int32_t*,
+                                                int32_t*, cudaStream_t);
 }  // namespace lu_reg_detail
 }  // namespace bsolve

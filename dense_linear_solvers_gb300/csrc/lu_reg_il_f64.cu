@@ -4,9 +4,11 @@
 
 namespace bsolve {
 namespace lu_reg_detail {
-template cudaError_t launch_layout_il<double, kRowMajor>(int, int, int64_t, int64_t, double*, double*,
-                                                     int32_t*, int32_t*, cudaStream_t);
-template cudaError_t launch_layout_il<double, kColMajor>(int, int, int64_t, int64_t, double*, double*,
-                                                     int32_t*, int32_t*, cudaStream_t);
+template cudaError_t launch_layout_il<double, kRowMajor>(int, int, int64_t, int64_t, double*,
+                                                        double*, int32_t*, int32_t*,
+                                                        cudaStream_t);
+template cudaError_t launch_layout_il<double, kColMajor>(int, int, int64_t, int64_t, double*,
+                                                        double*, int32_t*, int32_t*,
+                                                        cudaStream_t);
 }  // namespace lu_reg_detail
 }  // namespace bsolve

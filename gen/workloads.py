@@ -188,7 +188,8 @@ def _make_bdsv(w: Workload, batch: int) -> dict:
         m = hi - lo
         C = _rng(w.seed, 0, c).uniform(-0.5, 0.5, (m, nbr - 1, bs, bs)) / 8.0
         M = _rng(w.seed, 1, c).standard_normal((m, nbr, bs, bs)) / np.sqrt(8.0)
-        D = _bmm(M.reshape(-1, bs, bs), np.swapaxes(M, 2, 3).reshape(-1, bs, bs)).reshape(M.shape) + 10.0 * np.eye(bs)
+        MMt = _bmm(M.reshape(-1, bs, bs), np.swapaxes(M, 2, 3).reshape(-1, bs, bs))
+        D = MMt.reshape(M.shape) + 10.0 * np.eye(bs)
         strips[lo:hi, :, :, bs:2 * bs] = D
         strips[lo:hi, :nbr - 1, :, 2 * bs:] = C                       # R_i = C_i
         strips[lo:hi, 1:, :, :bs] = np.swapaxes(C, 2, 3)             # L_{i+1} = C_i^T

@@ -270,7 +270,8 @@ BS_API int bs_last_cuda_error(void);
 
 /* 1 if the call with these arguments has a kernel instance, else 0 (no launch). */
 BS_API int bs_getrf_getrs_supported(bs_dtype dtype, bs_layout layout, int n, int nrhs);
-BS_API int bs_potrf_potrs_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs);
+BS_API int bs_potrf_potrs_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                     int nrhs);
 BS_API int bs_bdsv_supported(bs_dtype dtype, int num_block_rows, int block_size);
 
 /* Library ABI version (major*10000 + minor*100 + patch). */
