@@ -76,8 +76,9 @@ class Oracle:
         sig["getrf_getrs_ex"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32, i32]
         sig["potrf_potrs_ex"] = [i32, i32, i32, i32, i64, vp, vp, vp, i32, i32]
         sig["getrf_getrs_mirror"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32]
-        sig["getrf_getrs_il"] = [i32, i32, i32, i64, i64, vp, vp, vp, vp, vp, i32]
-        sig["potrf_potrs_il"] = [i32, i32, i32, i32, i64, i64, vp, vp, vp, i32]
+        sig["getrf_getrs_il"] = [i32, i32, i32, i64, i64, vp, vp, vp, vp, vp, ctypes.c_double,
+                                 i32, i32]
+        sig["potrf_potrs_il"] = [i32, i32, i32, i32, i64, i64, vp, vp, vp, i32, i32]
         for op, args in sig.items():
             for sfx in ("f32", "f64"):
                 fn = getattr(lib, f"oracle_{op}_{sfx}")
@@ -265,11 +266,13 @@ class Oracle:
 
 
     def getrf_getrs_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
-                       layout: int = ROW_MAJOR, nthreads: int = 1):
+                       layout: int = ROW_MAJOR, nthreads: int = 1, tau: float = 1.0,
+                       ruda: int = 0):
         """LU + solve on interleaved batched storage (TDLS: element e of system s at
         base_s[e * w], base_s = (s // w) * w * size + s % w; w = 1 AoS, w >= batch SoA).
         A, B: flat arrays of ceil(batch / w) * w systems. Returns (A, B, ipiv, info,
-        tie_step), ipiv flat and interleaved like A."""
+        tie_step), ipiv flat and interleaved like A. tau and ruda: the contract options of
+        getrf_getrs_ex."""
         A = np.ascontiguousarray(A).reshape(-1).copy()
         B = np.ascontiguousarray(B, dtype=A.dtype).reshape(-1).copy()
         nb = -(-batch // w) if batch else 0
@@ -280,14 +283,15 @@ class Oracle:
         tie = np.zeros(batch, np.int32)
         fn = getattr(self.lib, "oracle_getrf_getrs_il_" + _suffix(A.dtype))
         if fn(layout, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
-              nthreads) != 0:
+              float(tau), int(ruda), nthreads) != 0:
             raise ValueError("oracle getrf_getrs_il rejected its arguments")
         return A, B, ipiv, info, tie
 
     def potrf_potrs_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
-                       layout: int = COL_MAJOR, fill: int = LOWER, nthreads: int = 1):
-        """Cholesky + solve on interleaved batched storage (see getrf_getrs_il).
-        Returns (A, B, info)."""
+                       layout: int = COL_MAJOR, fill: int = LOWER, nthreads: int = 1,
+                       ruda: int = 0):
+        """Cholesky + solve on interleaved batched storage (see getrf_getrs_il; ruda: the
+        status contract of potrf_potrs_ex). Returns (A, B, info)."""
         A = np.ascontiguousarray(A).reshape(-1).copy()
         B = np.ascontiguousarray(B, dtype=A.dtype).reshape(-1).copy()
         nb = -(-batch // w) if batch else 0
@@ -295,7 +299,8 @@ class Oracle:
             raise ValueError("interleaved buffers too small")
         info = np.zeros(batch, np.int32)
         fn = getattr(self.lib, "oracle_potrf_potrs_il_" + _suffix(A.dtype))
-        if fn(layout, fill, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(info), nthreads) != 0:
+        if fn(layout, fill, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(info), int(ruda),
+              nthreads) != 0:
             raise ValueError("oracle potrf_potrs_il rejected its arguments")
         return A, B, info
 
@@ -362,13 +367,14 @@ def getrf_getrs_mirror(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, nthreads
     return default().getrf_getrs_mirror(A, B, layout, tau, nthreads)
 
 
-def getrf_getrs_il(A, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1):
-    return default().getrf_getrs_il(A, B, n, nrhs, batch, w, layout, nthreads)
+def getrf_getrs_il(A, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1,
+                   tau: float = 1.0, ruda: int = 0):
+    return default().getrf_getrs_il(A, B, n, nrhs, batch, w, layout, nthreads, tau, ruda)
 
 
 def potrf_potrs_il(A, B, n, nrhs, batch, w, layout: int = COL_MAJOR, fill: int = LOWER,
-                   nthreads: int = 1):
-    return default().potrf_potrs_il(A, B, n, nrhs, batch, w, layout, fill, nthreads)
+                   nthreads: int = 1, ruda: int = 0):
+    return default().potrf_potrs_il(A, B, n, nrhs, batch, w, layout, fill, nthreads, ruda)
 
 
 def _suffix(dtype) -> str:

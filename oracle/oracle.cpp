@@ -716,7 +716,8 @@ int potrf_potrs_ex_batched(int layout, int fill, int n, int nrhs, int64_t batch,
 // s * size), SoA stride = the batch, AoSoA stride W with the systems in blocks of W:
 // base_s = (s / W) * W * size + s % W. One routine covers all three: it gathers each
 // system into a contiguous copy, runs the per-system routine and scatters it back. A, B
-// and ipiv are interleaved; info holds one entry per system.
+// and ipiv are interleaved; info holds one entry per system. The contract options (the
+// relative pivot threshold, the RUDA status contract) are the per-system routines' own.
 template <typename T>
 struct Strided {
   T* p;
@@ -735,8 +736,12 @@ struct Strided {
 
 template <typename T>
 int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w, T* A, T* B,
-                           int32_t* ipiv, int32_t* info, int32_t* tie_step, int nthreads) {
-  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || w < 1) return 1;
+                           int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau, int ruda,
+                           int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || w < 1 ||
+      !(tau > 0.0) || !(tau <= 1.0))
+    return 1;
+  const T t = static_cast<T>(tau);
   const Strided<T> a{A, w, (int64_t)n * n}, b{B, w, (int64_t)n * nrhs};
   const Strided<int32_t> pv{ipiv, w, n};
   for_systems(batch, nthreads, [&](int64_t s) {
@@ -744,8 +749,8 @@ int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w
     std::vector<int32_t> ps(n);
     a.gather(s, as.data());
     b.gather(s, bs.data());
-    getrf_getrs_one<T>(layout, n, nrhs, as.data(), bs.data(), ps.data(), info + s,
-                       tie_step ? tie_step + s : nullptr);
+    getrf_getrs_ex_one<T>(layout, n, nrhs, as.data(), bs.data(), ps.data(), info + s,
+                          tie_step ? tie_step + s : nullptr, t, ruda);
     a.scatter(s, as.data());
     b.scatter(s, bs.data());
     pv.scatter(s, ps.data());
@@ -755,7 +760,7 @@ int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w
 
 template <typename T>
 int potrf_potrs_il_batched(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w, T* A,
-                           T* B, int32_t* info, int nthreads) {
+                           T* B, int32_t* info, int ruda, int nthreads) {
   if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 ||
       batch < 0 || w < 1)
     return 1;
@@ -765,7 +770,7 @@ int potrf_potrs_il_batched(int layout, int fill, int n, int nrhs, int64_t batch,
     std::vector<T> as(a.size), bs(b.size);
     a.gather(s, as.data());
     b.gather(s, bs.data());
-    potrf_potrs_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s);
+    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);
     a.scatter(s, as.data());
     b.scatter(s, bs.data());
   });
@@ -889,23 +894,25 @@ int oracle_getrf_getrs_mirror_f64(int layout, int n, int nrhs, int64_t batch, do
 }
 int oracle_getrf_getrs_il_f32(int layout, int n, int nrhs, int64_t batch, int64_t w, float* A,
                               float* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
-                              int nthreads) {
+                              double tau, int ruda, int nthreads) {
   return getrf_getrs_il_batched<float>(layout, n, nrhs, batch, w, A, B, ipiv, info, tie_step,
-                                       nthreads);
+                                     tau, ruda, nthreads);
 }
 int oracle_getrf_getrs_il_f64(int layout, int n, int nrhs, int64_t batch, int64_t w, double* A,
                               double* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
-                              int nthreads) {
+                              double tau, int ruda, int nthreads) {
   return getrf_getrs_il_batched<double>(layout, n, nrhs, batch, w, A, B, ipiv, info, tie_step,
-                                        nthreads);
+                                     tau, ruda, nthreads);
 }
 int oracle_potrf_potrs_il_f32(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
-                              float* A, float* B, int32_t* info, int nthreads) {
-  return potrf_potrs_il_batched<float>(layout, fill, n, nrhs, batch, w, A, B, info, nthreads);
+                              float* A, float* B, int32_t* info, int ruda, int nthreads) {
+  return potrf_potrs_il_batched<float>(layout, fill, n, nrhs, batch, w, A, B, info, ruda,
+                                     nthreads);
 }
 int oracle_potrf_potrs_il_f64(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
-                              double* A, double* B, int32_t* info, int nthreads) {
-  return potrf_potrs_il_batched<double>(layout, fill, n, nrhs, batch, w, A, B, info, nthreads);
+                              double* A, double* B, int32_t* info, int ruda, int nthreads) {
+  return potrf_potrs_il_batched<double>(layout, fill, n, nrhs, batch, w, A, B, info, ruda,
+                                     nthreads);
 }
 
 }  // extern "C"

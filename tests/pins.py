@@ -862,12 +862,50 @@ def pin_interleaved_layouts(orc):
                     assert np.array_equal(g2[2], r2[2]) and g2[2][2] == n
 
 
+def pin_interleaved_contract_options(orc):
+    """The interleaved drivers with a pivot threshold or the RUDA status contract equal the
+    per-system contract drivers on the same systems, bit for bit (ipiv -1 and zeros for a
+    failed RUDA system included), the slots past the batch untouched."""
+    rng = _rng(78)
+    for dt in (np.float32, np.float64):
+        for (n, nrhs, batch, w) in [(6, 2, 11, 4), (17, 3, 9, 9), (5, 1, 7, 16)]:
+            for layout in (ROW_MAJOR, COL_MAJOR):
+                Al = rng.standard_normal((batch, n, n)).astype(dt)
+                Al[1, 0, 0] = np.inf                   # RUDA -1
+                Al[2, :, 1] = 0                        # a singular system
+                A = to_storage(Al, layout)
+                B = to_storage(rng.standard_normal((batch, n, nrhs)).astype(dt), layout)
+                for tau, ruda in ((0.5, 0), (1.0, 1), (0.3, 1)):
+                    ref = orc.getrf_getrs_ex(A, B, layout, tau=tau, ruda=ruda)
+                    got = orc.getrf_getrs_il(interleave(A, w), interleave(B, w), n, nrhs, batch,
+                                             w, layout, tau=tau, ruda=ruda)
+                    assert np.array_equal(deinterleave(got[0], batch, w, A.shape[1:]), ref[0],
+                                          equal_nan=True)
+                    assert np.array_equal(deinterleave(got[1], batch, w, B.shape[1:]), ref[1])
+                    assert np.array_equal(deinterleave(got[2], batch, w, (n,)), ref[2])
+                    assert np.array_equal(got[3], ref[3])
+                    assert np.all(np.isnan(got[0][np.isnan(interleave(A, w))]))
+                G = rng.standard_normal((batch, n, n))
+                Sl = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dt)
+                Sl[3, n - 1, 0] += 1.0                 # RUDA -2 (not symmetric)
+                Sl[4, n // 2, n // 2] = -1.0           # a failing minor
+                Sa = to_storage(Sl, layout)
+                for fill in (0, 1):
+                    r2 = orc.potrf_potrs_ex(Sa, B, layout, fill=fill, ruda=1)
+                    g2 = orc.potrf_potrs_il(interleave(Sa, w), interleave(B, w), n, nrhs, batch,
+                                            w, layout, fill, ruda=1)
+                    assert np.array_equal(deinterleave(g2[0], batch, w, Sa.shape[1:]), r2[0])
+                    assert np.array_equal(deinterleave(g2[1], batch, w, B.shape[1:]), r2[1])
+                    assert np.array_equal(g2[2], r2[2]) and g2[2][3] == -2
+
+
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
               pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
 BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
 VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol,
                 pin_tdls_row_major_reading]
-LAYOUT_PINS = [pin_interleaved_literal, pin_interleaved_layouts]
+LAYOUT_PINS = [pin_interleaved_literal, pin_interleaved_layouts,
+               pin_interleaved_contract_options]
 ALL_PINS = (LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS +
             LAYOUT_PINS)
 

@@ -123,8 +123,14 @@ MUTATIONS = [
      "for (int64_t e = 0; e < size; ++e) dst[e] = b[e];"),
     ("il_ipiv_not_interleaved", "    pv.scatter(s, ps.data());",
      "    for (int k = 0; k < n; ++k) ipiv[s * n + k] = ps[k];"),
-    ("il_chol_fill_ignored", "    potrf_potrs_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s);",
-     "    potrf_potrs_one<T>(layout, layout, n, nrhs, as.data(), bs.data(), info + s);"),
+    ("il_chol_fill_ignored",
+     "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);",
+     "    potrf_potrs_ex_one<T>(layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);"),
+    ("il_threshold_dropped", "                          tie_step ? tie_step + s : nullptr, t, ruda);",
+     "                          tie_step ? tie_step + s : nullptr, T(1), ruda);"),
+    ("il_chol_contract_dropped",
+     "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);",
+     "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, 0);"),
     ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
      "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
     ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
