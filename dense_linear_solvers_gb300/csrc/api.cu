@@ -433,15 +433,14 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
   if (mirror != 0 && mirror != 1) return BS_ERR_INVALID_ARG;
   if (ilv < 0) return BS_ERR_INVALID_ARG;
-  if (mirror && contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
-  if (ilv > 1) {
-    if (mirror || tau != 1.0 || contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
-    return getrf_getrs_il(dtype, layout, n, nrhs, batch, ilv, A, B, ipiv, info, stream);
-  }
+  const int64_t il = ilv > 1 ? ilv : 1;   // element stride of the batched layout
+  if (mirror && (contract != BS_CONTRACT_DEFAULT || il > 1)) return BS_ERR_UNSUPPORTED;
   if (mirror && layout == BS_ROW_MAJOR)
     return getrf_getrs_mirror(dtype, n, nrhs, batch, A, B, ipiv, info, tau, stream);
   if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT)
-    return bs_getrf_getrs_batched(dtype, layout, n, nrhs, batch, A, B, ipiv, info, stream);
+    return il > 1 ? getrf_getrs_il(dtype, layout, n, nrhs, batch, il, A, B, ipiv, info, stream)
+                  : bs_getrf_getrs_batched(dtype, layout, n, nrhs, batch, A, B, ipiv, info,
+                                           stream);
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
   if (!lu_supported(dtype, layout, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
@@ -453,9 +452,11 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
   cudaError_t e =
       dtype == BS_FP32
           ? bsolve::launch_lu_smem_ex<float>(layout, n, nrhs, batch, static_cast<float*>(A),
-                                             static_cast<float*>(B), ipiv, info, tau, ruda, s)
+                                             static_cast<float*>(B), ipiv, info, tau, ruda, s,
+                                             il)
           : bsolve::launch_lu_smem_ex<double>(layout, n, nrhs, batch, static_cast<double*>(A),
-                                              static_cast<double*>(B), ipiv, info, tau, ruda, s);
+                                              static_cast<double*>(B), ipiv, info, tau, ruda, s,
+                                              il);
   return from_cuda(e);
 }
 
@@ -470,12 +471,11 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
   if ((mirror != 0 && mirror != 1) || ilv < 0) return BS_ERR_INVALID_ARG;
   if (mirror) return BS_ERR_UNSUPPORTED;   // an LU option
-  if (ilv > 1) {
-    if (contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
-    return potrf_potrs_il(dtype, layout, fill, n, nrhs, batch, ilv, A, B, info, stream);
-  }
+  const int64_t il = ilv > 1 ? ilv : 1;   // element stride of the batched layout
   if (contract == BS_CONTRACT_DEFAULT)   // the threshold has no meaning without pivoting
-    return bs_potrf_potrs_batched(dtype, layout, fill, n, nrhs, batch, A, B, info, stream);
+    return il > 1 ? potrf_potrs_il(dtype, layout, fill, n, nrhs, batch, il, A, B, info, stream)
+                  : bs_potrf_potrs_batched(dtype, layout, fill, n, nrhs, batch, A, B, info,
+                                           stream);
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
   if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
@@ -486,10 +486,10 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
       dtype == BS_FP32
           ? bsolve::launch_chol_smem_ex<float>(chol_layouts(layout, fill), n, nrhs, batch,
                                                static_cast<float*>(A), static_cast<float*>(B),
-                                               info, 1, s)
+                                               info, 1, s, il)
           : bsolve::launch_chol_smem_ex<double>(chol_layouts(layout, fill), n, nrhs, batch,
                                                 static_cast<double*>(A),
-                                                static_cast<double*>(B), info, 1, s);
+                                                static_cast<double*>(B), info, 1, s, il);
   return from_cuda(e);
 }
 

@@ -174,9 +174,9 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    (s / W) * W * size + e * W + s % W; W >= batch is SoA. A, B and
  *                    ipiv then hold ceil(batch / W) * W systems each (the slots of the last
  *                    block past the batch are neither read nor written); info keeps one
- *                    entry per system. For both calls, nrhs <= 8, default contract, and
- *                    for LU tau = 1 and no transposed_factor (others: BS_ERR_UNSUPPORTED);
- *                    negative: BS_ERR_INVALID_ARG.
+ *                    entry per system. For both calls nrhs <= 8; it combines with the
+ *                    threshold and the RUDA contract (one system per CTA) but not with
+ *                    transposed_factor (BS_ERR_UNSUPPORTED); negative: BS_ERR_INVALID_ARG.
  * opts == NULL or default options run the plain call. Thresholds and the RUDA contract
  * run one system per CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the
  * CPU oracle's bit for bit. A threshold outside (0, 1], an unknown contract or a

@@ -172,19 +172,19 @@ def test_contract_variant_argument_errors(lib):
     assert f(bs.BS_FP32, 0, 16, 9, 0, None, None, None, None, m(0.5, 0, 1), None) == bs.BS_OK
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, None, I, m(0.5, 0, 1), None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 9, 5, A + 4, B, P, I, m(1.0, 0, 1), None) == bs.BS_ERR_INVALID_ARG
-    # the interleaved batched layout: W >= 0; with W > 1 only the default options and at
-    # most 8 right-hand sides
+    # the interleaved batched layout: W >= 0; with W > 1 at most 8 right-hand sides and not
+    # with the row-major reading
     w = lambda tau, c, t, il: ctypes.byref(bs.Options(tau, c, t, il))  # noqa: E731
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(1.0, 0, 0, -1), None) == bs.BS_ERR_INVALID_ARG
-    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(0.5, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
-    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(1.0, 1, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, w(0.5, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, w(1.0, 1, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(1.0, 0, 1, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, w(1.0, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 129, 4, 5, A, B, P, I, w(1.0, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, w(1.0, 0, 0, 32), None) == bs.BS_OK
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P + 8, I, w(1.0, 0, 0, 32), None) == bs.BS_ERR_INVALID_ARG
     assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, w(1.0, 0, 0, -3), None) == bs.BS_ERR_INVALID_ARG
-    assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, w(1.0, 1, 0, 64), None) == bs.BS_ERR_UNSUPPORTED
+    assert g(bs.BS_FP64, 1, 0, 32, 9, 5, A, B, I, w(1.0, 1, 0, 64), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, w(1.0, 0, 1, 0), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 9, 5, A, B, I, w(1.0, 0, 0, 64), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None, w(1.0, 0, 0, 64), None) == bs.BS_OK

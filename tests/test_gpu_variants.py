@@ -245,3 +245,55 @@ def test_interleaved_cholesky(dtype, layout, fill):
                 pads = np.isnan(interleave(np.zeros((batch,) + shape), w))
                 assert np.all(np.isnan(got[pads]))
             assert np.all(deinterleave(Bg, batch, w, B.shape[1:])[~ok] == 0)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_interleaved_with_contract_options(dtype, layout):
+    """Interleaved layouts with a pivot threshold or the RUDA contract (one system per
+    CTA, the element stride in every access): LU with tau 0.5 and with RUDA status codes,
+    Cholesky under RUDA (-2 and a failing minor), against the oracle bit for bit."""
+    from gen.workloads import deinterleave, interleave
+    rng = np.random.default_rng(1919 + layout)
+    batch = 21
+    for n in (3, 16, 33, 64):
+        for w in (4, 32):
+            nrhs = int(rng.integers(1, 9))
+            Al = rng.standard_normal((batch, n, n)).astype(dtype)
+            Al[1, 0, 0] = np.inf
+            Al[2, :, n // 2] = 0
+            A, B = to_storage(Al, layout), to_storage(
+                rng.standard_normal((batch, n, nrhs)).astype(dtype), layout)
+            Af, Bf = interleave(A, w), interleave(B, w)
+            for tau, ruda in ((0.5, 0), (1.0, 1)):
+                So, Xo, ipo, info_o, tie = oracle.getrf_getrs_il(Af, Bf, n, nrhs, batch, w, layout,
+                                                                 nthreads=NT, tau=tau, ruda=ruda)
+                tA, tB = _dev(Af), _dev(Bf)
+                ipiv = torch.full((Af.size // n,), SENT, dtype=torch.int32, device="cuda")
+                info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+                bs.bs_getrf_getrs_batched_ex(tA, tB, ipiv, info, layout, tau,
+                                             bs.BS_CONTRACT_RUDA if ruda else 0, interleave=w,
+                                             shape=(batch, n, nrhs))
+                Ag, Bg, ipg, infg = _host(tA), _host(tB), _host(ipiv), _host(info)
+                clean = tie < 0
+                assert np.array_equal(infg[clean], info_o[clean]), (n, w, tau, ruda)
+                for got, ref, shape in ((Ag, So, A.shape[1:]), (Bg, Xo, B.shape[1:]),
+                                        (ipg, ipo, (n,))):
+                    g2, r2 = (deinterleave(got, batch, w, shape),
+                              deinterleave(ref, batch, w, shape))
+                    assert np.array_equal(g2[clean], r2[clean], equal_nan=True), (n, w, tau)
+            G = rng.standard_normal((batch, n, n))
+            Sl = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dtype)
+            Sl[3, n - 1, 0] += 1.0
+            Sl[4, n // 2, n // 2] = -1.0
+            for fill in (bs.BS_LOWER, bs.BS_UPPER):
+                Sa = interleave(to_storage(Sl, layout), w)
+                Lo, Xo, info_o = oracle.potrf_potrs_il(Sa, Bf, n, nrhs, batch, w, layout, fill,
+                                                       nthreads=NT, ruda=1)
+                tA, tB = _dev(Sa), _dev(Bf)
+                info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+                bs.bs_potrf_potrs_batched_ex(tA, tB, info, layout, fill, bs.BS_CONTRACT_RUDA,
+                                             interleave=w, shape=(batch, n, nrhs))
+                assert np.array_equal(_host(info), info_o) and info_o[3] == -2
+                assert np.array_equal(_host(tA), Lo, equal_nan=True), (n, w, fill)
+                assert np.array_equal(_host(tB), Xo, equal_nan=True), (n, w, fill)
