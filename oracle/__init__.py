@@ -73,11 +73,12 @@ class Oracle:
             "bdsv_solve": [i32, i32, i64, vp, vp, i32],
             "bdmv": [i32, i32, i64, vp, vp, vp, i32],
         }
-        sig["getrf_getrs_ex"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32, i32]
+        sig["getrf_getrs_ex"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32, i32,
+                                 i32]
         sig["potrf_potrs_ex"] = [i32, i32, i32, i32, i64, vp, vp, vp, i32, i32]
         sig["getrf_getrs_mirror"] = [i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_double, i32]
         sig["getrf_getrs_il"] = [i32, i32, i32, i64, i64, vp, vp, vp, vp, vp, ctypes.c_double,
-                                 i32, i32]
+                                 i32, i32, i32]
         sig["potrf_potrs_il"] = [i32, i32, i32, i32, i64, i64, vp, vp, vp, i32, i32]
         for op, args in sig.items():
             for sfx in ("f32", "f64"):
@@ -217,9 +218,10 @@ class Oracle:
 
     # --- contract variants ------------------------------------------------------------
     def getrf_getrs_ex(self, A, B, layout: int = ROW_MAJOR, tau: float = 1.0, ruda: int = 0,
-                       nthreads: int = 1):
-        """LU + solve with TDLS threshold pivoting (tau) and/or the RUDA status contract.
-        Returns (LU, X, ipiv, info, tie_step)."""
+                       nthreads: int = 1, scale: int = 0):
+        """LU + solve with TDLS threshold pivoting (tau), the RUDA status contract and/or
+        RUDA's scaling by the largest magnitude of the matrix (scale). Returns (LU, X,
+        ipiv, info, tie_step)."""
         A = np.ascontiguousarray(A).copy()
         B = np.ascontiguousarray(B, dtype=A.dtype).copy()
         batch, n = A.shape[0], A.shape[1]
@@ -229,7 +231,7 @@ class Oracle:
         tie = np.zeros(batch, np.int32)
         fn = getattr(self.lib, "oracle_getrf_getrs_ex_" + _suffix(A.dtype))
         if fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
-              float(tau), int(ruda), nthreads) != 0:
+              float(tau), int(ruda), int(scale), nthreads) != 0:
             raise ValueError("oracle getrf_getrs_ex rejected its arguments")
         return A, B, ipiv, info, tie
 
@@ -267,7 +269,7 @@ class Oracle:
 
     def getrf_getrs_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
                        layout: int = ROW_MAJOR, nthreads: int = 1, tau: float = 1.0,
-                       ruda: int = 0):
+                       ruda: int = 0, scale: int = 0):
         """LU + solve on interleaved batched storage (TDLS: element e of system s at
         base_s[e * w], base_s = (s // w) * w * size + s % w; w = 1 AoS, w >= batch SoA).
         A, B: flat arrays of ceil(batch / w) * w systems. Returns (A, B, ipiv, info,
@@ -283,7 +285,7 @@ class Oracle:
         tie = np.zeros(batch, np.int32)
         fn = getattr(self.lib, "oracle_getrf_getrs_il_" + _suffix(A.dtype))
         if fn(layout, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
-              float(tau), int(ruda), nthreads) != 0:
+              float(tau), int(ruda), int(scale), nthreads) != 0:
             raise ValueError("oracle getrf_getrs_il rejected its arguments")
         return A, B, ipiv, info, tie
 
@@ -354,8 +356,8 @@ def bdmv(strips, xpad, ypad=None, nthreads: int = 1):
 
 
 def getrf_getrs_ex(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, ruda: int = 0,
-                   nthreads: int = 1):
-    return default().getrf_getrs_ex(A, B, layout, tau, ruda, nthreads)
+                   nthreads: int = 1, scale: int = 0):
+    return default().getrf_getrs_ex(A, B, layout, tau, ruda, nthreads, scale)
 
 
 def potrf_potrs_ex(A, B, layout: int = COL_MAJOR, fill: int = LOWER, ruda: int = 0,
@@ -368,8 +370,9 @@ def getrf_getrs_mirror(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, nthreads
 
 
 def getrf_getrs_il(A, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1,
-                   tau: float = 1.0, ruda: int = 0):
-    return default().getrf_getrs_il(A, B, n, nrhs, batch, w, layout, nthreads, tau, ruda)
+                   tau: float = 1.0, ruda: int = 0, scale: int = 0):
+    return default().getrf_getrs_il(A, B, n, nrhs, batch, w, layout, nthreads, tau, ruda,
+                                    scale)
 
 
 def potrf_potrs_il(A, B, n, nrhs, batch, w, layout: int = COL_MAJOR, fill: int = LOWER,

@@ -99,7 +99,7 @@ bool all_finite(const T* p, int64_t count) {
 
 template <typename T>
 void getrf_getrs_ex_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int32_t* info,
-                        int32_t* tie_step, T tau, int ruda) {
+                        int32_t* tie_step, T tau, int ruda, int scale = 0) {
   const T floor_v = Limits<T>::floor_();
   auto fail_ruda = [&](int32_t code) {
     for (int i = 0; i < n * n; ++i) A[i] = T(0);
@@ -111,6 +111,16 @@ void getrf_getrs_ex_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, 
     fail_ruda(-1);
     if (tie_step) *tie_step = -1;
     return;
+  }
+  // [RUDA] scaling by the largest magnitude of the whole matrix: when it is finite and
+  // positive, every entry is divided by it before the sweep and U gets the scale back
+  // after it (U <- U * m, the diagonal included; L is scale-free)
+  T msc = T(0);
+  if (scale && all_finite(A, (int64_t)n * n)) {
+    for (int i = 0; i < n * n; ++i)
+      if (std::fabs(A[i]) > msc) msc = std::fabs(A[i]);
+    if (msc > T(0))
+      for (int i = 0; i < n * n; ++i) A[i] = A[i] / msc;
   }
   int32_t inf = 0;
   int32_t tie = -1;
@@ -165,6 +175,9 @@ void getrf_getrs_ex_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, 
       for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));
     }
   }
+  if (msc > T(0))
+    for (int k = 0; k < n; ++k)
+      for (int j = k; j < n; ++j) a(k, j) = a(k, j) * msc;   // U's scale restored
   for (int k = n - 1; k >= 0; --k) {
     const T piv = a(k, k);
     const T r = (std::fabs(piv) >= floor_v) ? T(1) / piv : T(1);
@@ -655,7 +668,7 @@ int bdmv_batched(int nbr, int bs, int64_t batch, const T* strips, const T* xpad,
 
 template <typename T>
 int getrf_getrs_ex_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipiv,
-                           int32_t* info, int32_t* tie_step, double tau, int ruda,
+                           int32_t* info, int32_t* tie_step, double tau, int ruda, int scale,
                            int nthreads) {
   if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || !(tau > 0.0) ||
       !(tau <= 1.0))
@@ -663,7 +676,7 @@ int getrf_getrs_ex_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* 
   const T t = static_cast<T>(tau);
   for_systems(batch, nthreads, [&](int64_t s) {
     getrf_getrs_ex_one<T>(layout, n, nrhs, A + s * n * n, B + s * n * nrhs, ipiv + s * n,
-                          info + s, tie_step ? tie_step + s : nullptr, t, ruda);
+                          info + s, tie_step ? tie_step + s : nullptr, t, ruda, scale);
   });
   return 0;
 }
@@ -737,7 +750,7 @@ struct Strided {
 template <typename T>
 int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w, T* A, T* B,
                            int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau, int ruda,
-                           int nthreads) {
+                           int scale, int nthreads) {
   if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || w < 1 ||
       !(tau > 0.0) || !(tau <= 1.0))
     return 1;
@@ -750,7 +763,7 @@ int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w
     a.gather(s, as.data());
     b.gather(s, bs.data());
     getrf_getrs_ex_one<T>(layout, n, nrhs, as.data(), bs.data(), ps.data(), info + s,
-                          tie_step ? tie_step + s : nullptr, t, ruda);
+                          tie_step ? tie_step + s : nullptr, t, ruda, scale);
     a.scatter(s, as.data());
     b.scatter(s, bs.data());
     pv.scatter(s, ps.data());
@@ -862,9 +875,9 @@ int oracle_bdmv_f64(int nbr, int bs, int64_t batch, const double* strips, const 
 }
 int oracle_getrf_getrs_ex_f32(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
                               int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
-                              int ruda, int nthreads) {
-  return getrf_getrs_ex_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau, ruda,
-                                     nthreads);
+                              int ruda, int scale, int nthreads) {
+  return getrf_getrs_ex_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
+                                     ruda, scale, nthreads);
 }
 int oracle_potrf_potrs_ex_f32(int layout, int fill, int n, int nrhs, int64_t batch, float* A,
                               float* B, int32_t* info, int ruda, int nthreads) {
@@ -872,9 +885,9 @@ int oracle_potrf_potrs_ex_f32(int layout, int fill, int n, int nrhs, int64_t bat
 }
 int oracle_getrf_getrs_ex_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
                               int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
-                              int ruda, int nthreads) {
-  return getrf_getrs_ex_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau, ruda,
-                                     nthreads);
+                              int ruda, int scale, int nthreads) {
+  return getrf_getrs_ex_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
+                                     ruda, scale, nthreads);
 }
 int oracle_potrf_potrs_ex_f64(int layout, int fill, int n, int nrhs, int64_t batch, double* A,
                               double* B, int32_t* info, int ruda, int nthreads) {
@@ -894,15 +907,15 @@ int oracle_getrf_getrs_mirror_f64(int layout, int n, int nrhs, int64_t batch, do
 }
 int oracle_getrf_getrs_il_f32(int layout, int n, int nrhs, int64_t batch, int64_t w, float* A,
                               float* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
-                              double tau, int ruda, int nthreads) {
+                              double tau, int ruda, int scale, int nthreads) {
   return getrf_getrs_il_batched<float>(layout, n, nrhs, batch, w, A, B, ipiv, info, tie_step,
-                                     tau, ruda, nthreads);
+                                     tau, ruda, scale, nthreads);
 }
 int oracle_getrf_getrs_il_f64(int layout, int n, int nrhs, int64_t batch, int64_t w, double* A,
                               double* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
-                              double tau, int ruda, int nthreads) {
+                              double tau, int ruda, int scale, int nthreads) {
   return getrf_getrs_il_batched<double>(layout, n, nrhs, batch, w, A, B, ipiv, info, tie_step,
-                                     tau, ruda, nthreads);
+                                     tau, ruda, scale, nthreads);
 }
 int oracle_potrf_potrs_il_f32(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
                               float* A, float* B, int32_t* info, int ruda, int nthreads) {

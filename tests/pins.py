@@ -899,11 +899,62 @@ def pin_interleaved_contract_options(orc):
                     assert np.array_equal(g2[2], r2[2]) and g2[2][3] == -2
 
 
+def pin_ruda_scaling(orc):
+    """RUDA's scaling by the largest magnitude of the matrix, with U's scale restored at the
+    end (RUDA docs, unchanged numerical contract). Dividing by a power of two is exact and
+    commutes with every rounding of the sweep, so with max |a_ij| a power of two the result
+    is the unscaled one bit for bit; for any other maximum the factor reconstructs P A =
+    L U and the solution meets the backward-error bound; a zero matrix is left unscaled
+    (singular at step 1) and a non-finite input fails with -1 under the RUDA contract."""
+    rng = _rng(91)
+    for dt in (np.float32, np.float64):
+        eps = eps_of(dt)
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            for n, nrhs in ((1, 1), (5, 2), (16, 4), (33, 3)):
+                Al = rng.uniform(-1, 1, (6, n, n)).astype(dt)
+                Al[0, 0, n - 1] = 4.0               # max |a| = 4
+                Al[1] *= dt(2.0 ** -5)
+                Al[1, n - 1, 0] = -dt(2.0 ** -4)     # max |a| = 1/16
+                Al[2, 0, 0] = -dt(2.0 ** 20)        # max |a| = 2^20
+                Al[3] = 0
+                Al[3, 0, 0] = 8.0
+                A = to_storage(Al[:4], layout)
+                B = to_storage(rng.standard_normal((4, n, nrhs)).astype(dt), layout)
+                for tau, ruda in ((1.0, 0), (0.5, 1)):
+                    r0 = orc.getrf_getrs_ex(A, B, layout, tau=tau, ruda=ruda)
+                    r1 = orc.getrf_getrs_ex(A, B, layout, tau=tau, ruda=ruda, scale=1)
+                    assert all(np.array_equal(x, y) for x, y in zip(r0, r1)), (n, tau)
+                # a maximum that is not a power of two
+                Ag = rng.uniform(-1, 1, (7, n, n)).astype(dt) * dt(3.7)
+                Bg = rng.standard_normal((7, n, nrhs)).astype(dt)
+                LU, X, ipiv, info, _ = orc.getrf_getrs_ex(to_storage(Ag, layout),
+                                                          to_storage(Bg, layout), layout,
+                                                          scale=1)
+                LU, X = from_storage(LU, layout), from_storage(X, layout)
+                ok = info == 0
+                assert ok.sum() >= 5
+                be = backward_error(Ag[ok].astype(np.float64), X[ok], Bg[ok])
+                assert np.all(be <= 8 * n * eps)
+                for sidx in np.nonzero(ok)[0]:
+                    L, U = unpack_lu(LU[sidx])
+                    PA = Ag[sidx].astype(np.float64)[lapack_perm(ipiv[sidx])]
+                    nA = np.abs(Ag[sidx]).sum(axis=1).max()
+                    assert np.abs(PA - L @ U).max() <= 4 * n * eps * nA
+        Z = np.zeros((1, 3, 3), dt)
+        r0 = orc.getrf_getrs_ex(Z, np.ones((1, 3, 1), dt), ROW_MAJOR)
+        r1 = orc.getrf_getrs_ex(Z, np.ones((1, 3, 1), dt), ROW_MAJOR, scale=1)
+        assert all(np.array_equal(x, y) for x, y in zip(r0, r1)) and r1[3][0] == 1
+        Ai = np.eye(3, dtype=dt)[None].copy()
+        Ai[0, 1, 2] = np.inf
+        r = orc.getrf_getrs_ex(Ai, np.ones((1, 3, 1), dt), ROW_MAJOR, ruda=1, scale=1)
+        assert r[3][0] == -1 and np.all(r[2] == -1)
+
+
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
               pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
 BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
 VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol,
-                pin_tdls_row_major_reading]
+                pin_tdls_row_major_reading, pin_ruda_scaling]
 LAYOUT_PINS = [pin_interleaved_literal, pin_interleaved_layouts,
                pin_interleaved_contract_options]
 ALL_PINS = (LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS +

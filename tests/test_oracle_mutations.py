@@ -35,8 +35,8 @@ MUTATIONS = [
     ("lu_schur_transposed_operand", "a(i, j) = std::fma(-l, a(k, j), a(i, j));",
      "a(i, j) = std::fma(-l, a(j, k), a(i, j));"),
     ("lu_forward_solve_dropped",
-     "      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));\n    }\n  }\n  for (int k = n - 1",
-     "    }\n  }\n  for (int k = n - 1"),
+     "      for (int c = 0; c < nrhs; ++c) b(i, c) = std::fma(-l, b(k, c), b(i, c));\n    }\n  }\n  if (msc",
+     "    }\n  }\n  if (msc"),
     ("lu_back_subst_transposed",
      "b(i, c) = std::fma(-a(i, k), x, b(i, c));\n    }\n  }\n  if (tie_step) *tie_step = tie;",
      "b(i, c) = std::fma(-a(k, i), x, b(i, c));\n    }\n  }\n  if (tie_step) *tie_step = tie;"),
@@ -126,11 +126,20 @@ MUTATIONS = [
     ("il_chol_fill_ignored",
      "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);",
      "    potrf_potrs_ex_one<T>(layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);"),
-    ("il_threshold_dropped", "                          tie_step ? tie_step + s : nullptr, t, ruda);",
-     "                          tie_step ? tie_step + s : nullptr, T(1), ruda);"),
+    ("il_threshold_dropped",
+     "                          tie_step ? tie_step + s : nullptr, t, ruda, scale);",
+     "                          tie_step ? tie_step + s : nullptr, T(1), ruda, scale);"),
     ("il_chol_contract_dropped",
      "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);",
      "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, 0);"),
+    ("scaling_u_not_restored", "      for (int j = k; j < n; ++j) a(k, j) = a(k, j) * msc;   // U's scale restored",
+     "      for (int j = k; j < n; ++j) a(k, j) = a(k, j);   // U's scale restored"),
+    ("scaling_restores_l_too", "      for (int j = k; j < n; ++j) a(k, j) = a(k, j) * msc;   // U's scale restored",
+     "      for (int j = 0; j < n; ++j) a(k, j) = a(k, j) * msc;   // U's scale restored"),
+    ("scaling_first_row_max", "    for (int i = 0; i < n * n; ++i)\n      if (std::fabs(A[i]) > msc) msc = std::fabs(A[i]);",
+     "    for (int i = 0; i < n; ++i)\n      if (std::fabs(A[i]) > msc) msc = std::fabs(A[i]);"),
+    ("scaling_multiplies", "      for (int i = 0; i < n * n; ++i) A[i] = A[i] / msc;",
+     "      for (int i = 0; i < n * n; ++i) A[i] = A[i] * msc;"),
     ("bdmv_window_one_block_late", "const T* xw = xpad + (int64_t)br * bs;",
      "const T* xw = xpad + (int64_t)(br + 1) * bs;"),
     ("bdmv_output_into_pad", "ypad[(int64_t)(br + 1) * bs + row] = acc;",
