@@ -31,7 +31,8 @@ class Options(ctypes.Structure):
     """bs_options: TDLS pivot threshold, the status contract and TDLS's row-major reading
     (see bsolve.h)."""
     _fields_ = [("pivot_threshold", ctypes.c_double), ("status_contract", ctypes.c_int),
-                ("transposed_factor", ctypes.c_int), ("interleave", ctypes.c_int64)]
+                ("transposed_factor", ctypes.c_int), ("interleave", ctypes.c_int64),
+                ("scaling", ctypes.c_int)]
 
 
 ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
@@ -244,13 +245,13 @@ def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
                               pivot_threshold: float = 1.0,
                               status_contract: int = BS_CONTRACT_DEFAULT,
                               transposed_factor: int = 0, interleave: int = 0, shape=None,
-                              stream=None) -> None:
+                              scaling: int = 0, stream=None) -> None:
     """LU + solve with TDLS threshold pivoting, the RUDA status contract, TDLS's
     row-major reading (factor of A^T and the mirror solve), or an interleaved batched
-    layout (A, B, ipiv flat; shape=(batch, n, nrhs))."""
+    layout (A, B, ipiv flat; shape=(batch, n, nrhs)), or RUDA's max-abs scaling."""
     batch, n, nrhs = _il_shape(A, B, layout, interleave, shape)
     opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor),
-                   int(interleave))
+                   int(interleave), int(scaling))
     st = lib().bs_getrf_getrs_batched_ex(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
                                          _ptr(ipiv), _ptr(info), ctypes.byref(opts),
                                          _stream(stream))
@@ -263,7 +264,7 @@ def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = B
     """Cholesky + solve under the RUDA status contract, or on an interleaved batched
     layout (A, B flat; shape=(batch, n, nrhs))."""
     batch, n, nrhs = _il_shape(A, B, layout, interleave, shape)
-    opts = Options(1.0, int(status_contract), 0, int(interleave))
+    opts = Options(1.0, int(status_contract), 0, int(interleave), 0)
     st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                          _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
     _check(st, "bs_potrf_potrs_batched_ex")

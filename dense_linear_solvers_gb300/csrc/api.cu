@@ -429,15 +429,16 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
   const int contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
   const int mirror = opts ? opts->transposed_factor : 0;
   const int64_t ilv = opts ? opts->interleave : 0;
+  const int scaling = opts ? opts->scaling : 0;
   if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
   if (mirror != 0 && mirror != 1) return BS_ERR_INVALID_ARG;
-  if (ilv < 0) return BS_ERR_INVALID_ARG;
+  if (ilv < 0 || (scaling != 0 && scaling != 1)) return BS_ERR_INVALID_ARG;
   const int64_t il = ilv > 1 ? ilv : 1;   // element stride of the batched layout
-  if (mirror && (contract != BS_CONTRACT_DEFAULT || il > 1)) return BS_ERR_UNSUPPORTED;
+  if (mirror && (contract != BS_CONTRACT_DEFAULT || il > 1 || scaling)) return BS_ERR_UNSUPPORTED;
   if (mirror && layout == BS_ROW_MAJOR)
     return getrf_getrs_mirror(dtype, n, nrhs, batch, A, B, ipiv, info, tau, stream);
-  if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT)
+  if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT && !scaling)
     return il > 1 ? getrf_getrs_il(dtype, layout, n, nrhs, batch, il, A, B, ipiv, info, stream)
                   : bs_getrf_getrs_batched(dtype, layout, n, nrhs, batch, A, B, ipiv, info,
                                            stream);
@@ -453,10 +454,10 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
       dtype == BS_FP32
           ? bsolve::launch_lu_smem_ex<float>(layout, n, nrhs, batch, static_cast<float*>(A),
                                              static_cast<float*>(B), ipiv, info, tau, ruda, s,
-                                             il)
+                                             il, scaling)
           : bsolve::launch_lu_smem_ex<double>(layout, n, nrhs, batch, static_cast<double*>(A),
                                               static_cast<double*>(B), ipiv, info, tau, ruda, s,
-                                              il);
+                                              il, scaling);
   return from_cuda(e);
 }
 
@@ -469,8 +470,10 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
   const int64_t ilv = opts ? opts->interleave : 0;
   if (!(tau > 0.0 && tau <= 1.0)) return BS_ERR_INVALID_ARG;
   if (contract != BS_CONTRACT_DEFAULT && contract != BS_CONTRACT_RUDA) return BS_ERR_INVALID_ARG;
-  if ((mirror != 0 && mirror != 1) || ilv < 0) return BS_ERR_INVALID_ARG;
-  if (mirror) return BS_ERR_UNSUPPORTED;   // an LU option
+  const int scaling = opts ? opts->scaling : 0;
+  if ((mirror != 0 && mirror != 1) || ilv < 0 || (scaling != 0 && scaling != 1))
+    return BS_ERR_INVALID_ARG;
+  if (mirror || scaling) return BS_ERR_UNSUPPORTED;   // LU options
   const int64_t il = ilv > 1 ? ilv : 1;   // element stride of the batched layout
   if (contract == BS_CONTRACT_DEFAULT)   // the threshold has no meaning without pivoting
     return il > 1 ? potrf_potrs_il(dtype, layout, fill, n, nrhs, batch, il, A, B, info, stream)

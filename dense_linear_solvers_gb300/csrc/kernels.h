@@ -27,7 +27,7 @@ cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* 
 template <typename T>
 cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                               int32_t* ipiv, int32_t* info, double tau, int ruda,
-                              cudaStream_t stream, int64_t ilv = 1);
+                              cudaStream_t stream, int64_t ilv = 1, int scale = 0);
 
 // Solve with a stored factor: getrs (L\U and the 1-based swap sequence of getrf) and
 // potrs (Cholesky factor), 1 <= n <= 128.

@@ -20,11 +20,16 @@
 // Options of the _ex calls (run here for every n): TDLS threshold pivoting (the row in
 // place stays when |a_kk| >= tau * m, m the magnitude the search found) and the RUDA
 // status contract (-1 for a non-finite input before the sweep, -3 for a non-finite factor
-// or solution after it, failed systems returned as zeros with pivots -1).
+// or solution after it, failed systems returned as zeros with pivots -1), and RUDA's
+// scaling by the largest magnitude of the matrix (A divided by it before the sweep when it
+// is finite and positive, U multiplied by it after, the back substitution on the restored
+// U with its reciprocals recomputed).
 // Back substitution runs by blocks of four rows: one warp solves the 4 x 4 diagonal block,
 // then all warps apply its four columns to every row above, each element taking the four
 // updates in decreasing column order -- the oracle's order, so the arithmetic is the
 // CPU oracle's, operation by operation.
+#include <cfloat>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -42,7 +47,7 @@ template <typename T, bool IL>
 __global__ void __launch_bounds__(kThreads)
 lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
               T* __restrict__ B, int32_t* __restrict__ ipiv, int32_t* __restrict__ info,
-              T tau, int ruda, int64_t ilv_) {
+              T tau, int ruda, int64_t ilv_, int scale) {
   const int64_t ilv = IL ? ilv_ : 1;
   using Key = typename Traits<T>::Key;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -56,6 +61,7 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   T* const rcp = M + n * P;
   int* const piv = reinterpret_cast<int*>(rcp + n);
   __shared__ int s_info;
+  __shared__ Key s_max;
 
   // element e of the system at A[e * ilv] (ilv = 1: the systems one after another;
   // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B, ipiv
@@ -83,7 +89,10 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       cp_async_elem<T>(M + i * P + n + c, B + e * ilv);
     }
   }
-  if (tid == 0) s_info = 0;
+  if (tid == 0) {
+    s_info = 0;
+    s_max = 0;
+  }
   cp_async_wait_all();
   __syncthreads();
 
@@ -101,6 +110,35 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       if (tid == 0) info[s] = -1;
       return;
     }
+  }
+
+  // RUDA scaling: m = max |a_ij| (as magnitude bits: their order is the values'); a
+  // non-finite entry leaves the system unscaled
+  T msc = T(0);
+  if (scale) {
+    Key mk = 0;
+    int nonfin = 0;
+    for (int e = tid; e < n * n; e += kThreads) {
+      const int i = e / n, j = e - i * n;
+      const Key kb = Traits<T>::mag_bits(M[i * P + j]);
+      nonfin |= kb >= Traits<T>::kInfBits;
+      mk = kb > mk ? kb : mk;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const Key o = shfl_xor_key(mk, off, 32);
+      mk = o > mk ? o : mk;
+    }
+    if (lane == 0) atomicMax(&s_max, mk);
+    nonfin = __syncthreads_or(nonfin);
+    if (!nonfin && s_max > 0) {
+      msc = pivot_from_key<T>(s_max + 1, 0u);   // a key is the magnitude bits + 1
+      for (int e = tid; e < n * n; e += kThreads) {
+        const int i = e / n, j = e - i * n;
+        M[i * P + j] = M[i * P + j] / msc;
+      }
+    }
+    __syncthreads();
   }
 
   for (int k = 0; k < n; ++k) {
@@ -173,6 +211,22 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
           ++jj;
         }
       }
+    }
+    __syncthreads();
+  }
+
+  // RUDA scaling: U's scale restored, and the reciprocals of its diagonal recomputed for
+  // the back substitution (a pivot below the smallest normal number gets 1)
+  if (msc > T(0)) {
+    for (int e = tid; e < n * n; e += kThreads) {
+      const int i = e / n, j = e - i * n;
+      if (j >= i) M[i * P + j] = M[i * P + j] * msc;
+    }
+    __syncthreads();
+    const T fl = sizeof(T) == 4 ? T(FLT_MIN) : T(DBL_MIN);
+    for (int k = tid; k < n; k += kThreads) {
+      const T u = M[k * P + k];
+      rcp[k] = fabs(u) >= fl ? rcp_rn<T>(u) : T(1);
     }
     __syncthreads();
   }
@@ -255,7 +309,7 @@ size_t lu_cta_bytes(int n, int nrhs, int elem_size) {
 template <typename T>
 cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                               int32_t* ipiv, int32_t* info, double tau, int ruda,
-                              cudaStream_t stream, int64_t ilv) {
+                              cudaStream_t stream, int64_t ilv, int scale) {
   if (ilv < 1) return cudaErrorInvalidValue;
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = lu_cta_bytes(n, nrhs, sizeof(T));
@@ -265,17 +319,17 @@ cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, 
   if (e != cudaSuccess) return e;
   if (ilv == 1)
     lu_cta_kernel<T, false><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
-        n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, 1);
+        n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, 1, scale);
   else
     lu_cta_kernel<T, true><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
-        n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, ilv);
+        n, nrhs, layout, batch, A, B, ipiv, info, static_cast<T>(tau), ruda, ilv, scale);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                            int32_t* ipiv, int32_t* info, cudaStream_t stream) {
-  return launch_lu_smem_ex<T>(layout, n, nrhs, batch, A, B, ipiv, info, 1.0, 0, stream, 1);
+  return launch_lu_smem_ex<T>(layout, n, nrhs, batch, A, B, ipiv, info, 1.0, 0, stream, 1, 0);
 }
 
 template cudaError_t launch_lu_smem<float>(int, int, int, int64_t, float*, float*, int32_t*,
@@ -283,9 +337,9 @@ template cudaError_t launch_lu_smem<float>(int, int, int, int64_t, float*, float
 template cudaError_t launch_lu_smem<double>(int, int, int, int64_t, double*, double*, int32_t*,
                                             int32_t*, cudaStream_t);
 template cudaError_t launch_lu_smem_ex<float>(int, int, int, int64_t, float*, float*, int32_t*,
-                                              int32_t*, double, int, cudaStream_t, int64_t);
+                                              int32_t*, double, int, cudaStream_t, int64_t, int);
 template cudaError_t launch_lu_smem_ex<double>(int, int, int, int64_t, double*, double*,
                                                int32_t*, int32_t*, double, int, cudaStream_t,
-                                               int64_t);
+                                               int64_t, int);
 
 }  // namespace bsolve

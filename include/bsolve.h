@@ -177,6 +177,16 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    entry per system. For both calls nrhs <= 8; it combines with the
  *                    threshold and the RUDA contract (one system per CTA) but not with
  *                    transposed_factor (BS_ERR_UNSUPPORTED); negative: BS_ERR_INVALID_ARG.
+ *   scaling          0 or 1 (LU only; RUDA docs, unchanged numerical contract: the LU keeps
+ *                    the scaling by the whole matrix's largest magnitude and restores U's
+ *                    scale at the end). 1: with m = max |a_ij| finite and positive, A is
+ *                    divided by m before the sweep (each entry rounded once), U (diagonal
+ *                    included) is multiplied by m after it, and the back substitution uses
+ *                    the restored U (reciprocals of its diagonal recomputed; 1 for one below
+ *                    the smallest normal number); a non-finite entry or a zero matrix leaves
+ *                    the system unscaled; info reports the scaled sweep's pivots. One
+ *                    system per CTA; combines with the threshold, the RUDA contract and
+ *                    interleaving, not with transposed_factor (BS_ERR_UNSUPPORTED).
  * opts == NULL or default options run the plain call. Thresholds and the RUDA contract
  * run one system per CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the
  * CPU oracle's bit for bit. A threshold outside (0, 1], an unknown contract or a
@@ -189,6 +199,7 @@ typedef struct {
   int status_contract;    /* a bs_contract */
   int transposed_factor;  /* 1: TDLS's row-major reading (factor of A^T, mirror solve) */
   int64_t interleave;     /* batched layout: 0/1 AoS, W > 1 AoSoA blocks of W (SoA: >= batch) */
+  int scaling;            /* 1: RUDA's max-abs scaling with U's scale restored (LU) */
 } bs_options;
 
 BS_API bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,

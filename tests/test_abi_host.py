@@ -163,7 +163,7 @@ def test_contract_variant_argument_errors(lib):
     # TDLS's row-major reading: 0 or 1, not with the RUDA contract, up to 65536
     # right-hand sides (a factor launch and a solve launch); the size of bs_options is
     # a double and two ints
-    assert ctypes.sizeof(bs.Options) == 24
+    assert ctypes.sizeof(bs.Options) == 32
     m = lambda tau, c, t: ctypes.byref(bs.Options(tau, c, t))  # noqa: E731
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, m(1.0, 0, 2), None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, m(1.0, 1, 1), None) == bs.BS_ERR_UNSUPPORTED
@@ -188,6 +188,14 @@ def test_contract_variant_argument_errors(lib):
     assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, w(1.0, 0, 1, 0), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 9, 5, A, B, I, w(1.0, 0, 0, 64), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None, w(1.0, 0, 0, 64), None) == bs.BS_OK
+    # RUDA's max-abs scaling: 0 or 1, LU only, not with the row-major reading
+    sc = lambda tau, c, t, il, k: ctypes.byref(bs.Options(tau, c, t, il, k))  # noqa: E731
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, sc(1.0, 0, 0, 0, 2), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, sc(1.0, 0, 1, 0, 1), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, sc(1.0, 0, 0, 0, 1), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, sc(1.0, 0, 0, 0, 1), None) == bs.BS_OK
+    assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, sc(1.0, 0, 0, 0, 1), None) == bs.BS_ERR_UNSUPPORTED
+    assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, sc(1.0, 0, 0, 0, 3), None) == bs.BS_ERR_INVALID_ARG
 
 
 def test_binding_refuses_host_tensors():

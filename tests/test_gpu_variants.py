@@ -297,3 +297,59 @@ def test_interleaved_with_contract_options(dtype, layout):
                 assert np.array_equal(_host(info), info_o) and info_o[3] == -2
                 assert np.array_equal(_host(tA), Lo, equal_nan=True), (n, w, fill)
                 assert np.array_equal(_host(tB), Xo, equal_nan=True), (n, w, fill)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+def test_ruda_scaling(dtype, layout):
+    """RUDA's max-abs scaling with U's scale restored: every order class (register-size,
+    n > 32, n = 128), magnitudes far from 1, a power-of-two maximum, a singular system, a
+    NaN (left unscaled), with the threshold, the RUDA contract and interleaving, against
+    the oracle bit for bit."""
+    from gen.workloads import deinterleave, interleave
+    rng = np.random.default_rng(2020 + layout)
+    batch = 13
+    big = 1e15 if dtype == np.float32 else 1e150
+    for n in (1, 2, 7, 16, 31, 32, 33, 64, 128):
+        nrhs = int(rng.integers(1, 9))
+        Al = rng.uniform(-1, 1, (batch, n, n)).astype(dtype)
+        Al[0] *= dtype(3.7)
+        Al[1] *= dtype(1.0 / big)
+        Al[2] *= dtype(big)
+        Al[3, 0, n - 1] = 4.0
+        Al[4, :, n // 2] = 0
+        Al[5, n - 1, 0] = np.nan
+        A = to_storage(Al, layout)
+        B = to_storage(rng.standard_normal((batch, n, nrhs)).astype(dtype), layout)
+        for tau, ruda, w in ((1.0, 0, 0), (0.5, 0, 0), (1.0, 1, 0), (1.0, 0, 4)):
+            if w:
+                So, Xo, ipo, info_o, tie = oracle.getrf_getrs_il(
+                    interleave(A, w), interleave(B, w), n, nrhs, batch, w, layout, nthreads=NT,
+                    tau=tau, ruda=ruda, scale=1)
+                tA, tB = _dev(interleave(A, w)), _dev(interleave(B, w))
+                ipiv = torch.full((interleave(A, w).size // n,), SENT, dtype=torch.int32,
+                                  device="cuda")
+            else:
+                So, Xo, ipo, info_o, tie = oracle.getrf_getrs_ex(A, B, layout, tau=tau,
+                                                                 ruda=ruda, nthreads=NT,
+                                                                 scale=1)
+                tA, tB = _dev(A), _dev(B)
+                ipiv = torch.full((batch, n), SENT, dtype=torch.int32, device="cuda")
+            info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+            bs.bs_getrf_getrs_batched_ex(tA, tB, ipiv, info, layout, tau,
+                                         bs.BS_CONTRACT_RUDA if ruda else 0, interleave=w,
+                                         shape=(batch, n, nrhs), scaling=1)
+            Ag, Bg, ipg, infg = _host(tA), _host(tB), _host(ipiv), _host(info)
+            if w:
+                So, Xo, ipo = (deinterleave(So, batch, w, A.shape[1:]),
+                               deinterleave(Xo, batch, w, B.shape[1:]),
+                               deinterleave(ipo, batch, w, (n,)))
+                Ag, Bg, ipg = (deinterleave(Ag, batch, w, A.shape[1:]),
+                               deinterleave(Bg, batch, w, B.shape[1:]),
+                               deinterleave(ipg, batch, w, (n,)))
+            clean = tie < 0
+            assert clean.sum() >= batch - 4, (n, tau, ruda, w)
+            assert np.array_equal(infg[clean], info_o[clean]), (n, tau, ruda, w)
+            assert np.array_equal(ipg[clean], ipo[clean]), (n, tau, ruda, w)
+            assert np.array_equal(Ag[clean], So[clean], equal_nan=True), (n, tau, ruda, w)
+            assert np.array_equal(Bg[clean], Xo[clean], equal_nan=True), (n, tau, ruda, w)
