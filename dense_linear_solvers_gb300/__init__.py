@@ -42,6 +42,9 @@ EXPORTED = (
     "bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched", "bs_potrs_batched",
     "bs_bdsv_factor_batched", "bs_bdsv_solve_batched", "bs_bdmv_batched",
     "bs_getrf_getrs_batched_ex", "bs_potrf_potrs_batched_ex",
+    "bs_getrf_getrs_host_workspace", "bs_getrf_getrs_batched_host",
+    "bs_potrf_potrs_host_workspace", "bs_potrf_potrs_batched_host",
+    "bs_bdsv_host_workspace", "bs_bdsv_batched_host",
     "bs_status_string", "bs_last_cuda_error", "bs_getrf_getrs_supported",
     "bs_potrf_potrs_supported", "bs_bdsv_supported", "bs_version",
 )
@@ -92,6 +95,22 @@ def lib() -> ctypes.CDLL:
             for name in ("bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched",
                          "bs_potrs_batched", "bs_bdsv_factor_batched", "bs_bdsv_solve_batched",
                          "bs_bdmv_batched"):
+                getattr(L, name).restype = i32
+            sz = ctypes.c_size_t
+            L.bs_getrf_getrs_host_workspace.argtypes = [i32, i32, i32, i64]
+            L.bs_potrf_potrs_host_workspace.argtypes = [i32, i32, i32, i64]
+            L.bs_bdsv_host_workspace.argtypes = [i32, i32, i32, i64]
+            for name in ("bs_getrf_getrs_host_workspace", "bs_potrf_potrs_host_workspace",
+                         "bs_bdsv_host_workspace"):
+                getattr(L, name).restype = sz
+            L.bs_getrf_getrs_batched_host.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp,
+                                                      vp, sz, i64, vp, vp]
+            L.bs_potrf_potrs_batched_host.argtypes = [i32, i32, i32, i32, i32, i64, vp, vp, vp,
+                                                      vp, sz, i64, vp, vp]
+            L.bs_bdsv_batched_host.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, sz, i64, vp,
+                                               vp]
+            for name in ("bs_getrf_getrs_batched_host", "bs_potrf_potrs_batched_host",
+                         "bs_bdsv_batched_host"):
                 getattr(L, name).restype = i32
             L.bs_status_string.argtypes = [i32]
             L.bs_status_string.restype = ctypes.c_char_p
@@ -268,3 +287,86 @@ def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = B
     st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                          _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
     _check(st, "bs_potrf_potrs_batched_ex")
+
+
+# ------------------------------------------------------------ host-resident batches
+def _host_ptr(t) -> int:
+    if t.is_cuda:
+        raise ValueError("the *_host calls take host (CPU) tensors; pinned memory overlaps")
+    if not t.is_contiguous():
+        raise ValueError("bsolve operands must be contiguous")
+    return t.data_ptr()
+
+
+class HostPlan:
+    """Device workspace and the two streams of the *_host calls (plumbing: the workspace
+    is a torch CUDA tensor sized by the library's query; the library allocates nothing)."""
+
+    def __init__(self, work_bytes: int, streams=None):
+        import torch
+        self.work = torch.empty(max(int(work_bytes), 1), dtype=torch.uint8, device="cuda")
+        self.streams = tuple(streams) if streams else (torch.cuda.Stream(), torch.cuda.Stream())
+
+    def synchronize(self):
+        for st in self.streams:
+            st.synchronize()
+
+
+def getrf_getrs_host_plan(dtype_code: int, n: int, nrhs: int, chunk: int, streams=None):
+    return HostPlan(lib().bs_getrf_getrs_host_workspace(dtype_code, n, nrhs, chunk), streams)
+
+
+def potrf_potrs_host_plan(dtype_code: int, n: int, nrhs: int, chunk: int, streams=None):
+    return HostPlan(lib().bs_potrf_potrs_host_workspace(dtype_code, n, nrhs, chunk), streams)
+
+
+def bdsv_host_plan(dtype_code: int, nbr: int, bsz: int, chunk: int, streams=None):
+    return HostPlan(lib().bs_bdsv_host_workspace(dtype_code, nbr, bsz, chunk), streams)
+
+
+def bs_getrf_getrs_batched_host(A, B, ipiv, info, layout: int = ROW_MAJOR, chunk: int = 8192,
+                                plan: HostPlan | None = None, sync: bool = True) -> HostPlan:
+    """LU + solve on host tensors, in place, copied in and out by chunks on two streams."""
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    plan = plan or getrf_getrs_host_plan(_dtype_code(A), n, nrhs, chunk)
+    st = lib().bs_getrf_getrs_batched_host(
+        _dtype_code(A), layout, n, nrhs, batch, _host_ptr(A), _host_ptr(B), _host_ptr(ipiv),
+        _host_ptr(info), plan.work.data_ptr(), plan.work.numel(), chunk,
+        _stream(plan.streams[0]), _stream(plan.streams[1]))
+    _check(st, "bs_getrf_getrs_batched_host")
+    if sync:
+        plan.synchronize()
+    return plan
+
+
+def bs_potrf_potrs_batched_host(A, B, info, layout: int = COL_MAJOR, fill: int = BS_LOWER,
+                                chunk: int = 8192, plan: HostPlan | None = None,
+                                sync: bool = True) -> HostPlan:
+    """Cholesky + solve on host tensors, in place, by chunks on two streams."""
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    plan = plan or potrf_potrs_host_plan(_dtype_code(A), n, nrhs, chunk)
+    st = lib().bs_potrf_potrs_batched_host(
+        _dtype_code(A), layout, fill, n, nrhs, batch, _host_ptr(A), _host_ptr(B),
+        _host_ptr(info), plan.work.data_ptr(), plan.work.numel(), chunk,
+        _stream(plan.streams[0]), _stream(plan.streams[1]))
+    _check(st, "bs_potrf_potrs_batched_host")
+    if sync:
+        plan.synchronize()
+    return plan
+
+
+def bs_bdsv_batched_host(strips, x_padded, info, chunk: int = 2048,
+                         plan: HostPlan | None = None, sync: bool = True) -> HostPlan:
+    """Block-tridiagonal solve on host tensors, in place, by chunks on two streams."""
+    batch, nbr, bsz = strips.shape[0], strips.shape[1], strips.shape[2]
+    plan = plan or bdsv_host_plan(_dtype_code(strips), nbr, bsz, chunk)
+    st = lib().bs_bdsv_batched_host(
+        _dtype_code(strips), nbr, bsz, batch, _host_ptr(strips), _host_ptr(x_padded),
+        _host_ptr(info), plan.work.data_ptr(), plan.work.numel(), chunk,
+        _stream(plan.streams[0]), _stream(plan.streams[1]))
+    _check(st, "bs_bdsv_batched_host")
+    if sync:
+        plan.synchronize()
+    return plan

@@ -151,9 +151,158 @@ bs_status potrf_potrs_il(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, 
   return from_cuda(e);
 }
 
+// ---------------------------------------------------------------- host-resident batches
+// One operand of a host pipeline: the host array, its bytes per system, and whether it is
+// copied in (H2D) and out (D2H).
+struct HostOperand {
+  char* host;
+  size_t per_sys;
+  bool in, out;
+};
+
+constexpr size_t kWorkAlign = 256;
+
+size_t round_up(size_t x) { return (x + kWorkAlign - 1) / kWorkAlign * kWorkAlign; }
+
+// Bytes of one slot of the workspace (a chunk of every operand, each 256-byte aligned);
+// the workspace holds two slots.
+size_t slot_bytes(const HostOperand* ops, int nops, int64_t chunk) {
+  size_t b = 0;
+  for (int i = 0; i < nops; ++i) b += round_up(ops[i].per_sys * static_cast<size_t>(chunk));
+  return b;
+}
+
+// The batch in chunks of `chunk` systems; chunk c runs its copies in, its solve and its
+// copies out on stream c % 2 with workspace slot c % 2, so that one chunk's copies
+// overlap the other stream's solve and copies, and a slot is reused only after its
+// stream has finished with it (stream order: no event needed). `call` gets the device
+// pointers of the operands, the chunk's system count and the stream.
+template <class Call>
+bs_status host_pipeline(int64_t batch, int64_t chunk, HostOperand* ops, int nops, void* work,
+                        size_t work_bytes, void* stream0, void* stream1, Call call) {
+  if (batch < 0 || chunk < 1) return BS_ERR_INVALID_ARG;
+  if (batch == 0) return BS_OK;
+  if (!work || (reinterpret_cast<uintptr_t>(work) % kWorkAlign) != 0) return BS_ERR_INVALID_ARG;
+  for (int i = 0; i < nops; ++i)
+    if (!ops[i].host) return BS_ERR_INVALID_ARG;
+  const size_t slot = slot_bytes(ops, nops, chunk);
+  if (work_bytes < 2 * slot) return BS_ERR_INVALID_ARG;
+  cudaStream_t st[2] = {static_cast<cudaStream_t>(stream0), static_cast<cudaStream_t>(stream1)};
+  char* dev[8];
+  for (int64_t c0 = 0, c = 0; c0 < batch; c0 += chunk, ++c) {
+    const int64_t m = batch - c0 < chunk ? batch - c0 : chunk;
+    cudaStream_t s = st[c & 1];
+    char* base = static_cast<char*>(work) + (c & 1) * slot;
+    for (int i = 0; i < nops; ++i) {
+      dev[i] = base;
+      base += round_up(ops[i].per_sys * static_cast<size_t>(chunk));
+      if (ops[i].in) {
+        const cudaError_t e = cudaMemcpyAsync(dev[i], ops[i].host + c0 * ops[i].per_sys,
+                                              m * ops[i].per_sys, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return from_cuda(e);
+      }
+    }
+    const bs_status r = call(dev, m, s);
+    if (r != BS_OK) return r;
+    for (int i = 0; i < nops; ++i) {
+      if (!ops[i].out) continue;
+      const cudaError_t e = cudaMemcpyAsync(ops[i].host + c0 * ops[i].per_sys, dev[i],
+                                            m * ops[i].per_sys, cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
+  }
+  return BS_OK;
+}
+
+size_t elem_size(bs_dtype dtype) { return dtype == BS_FP32 ? 4 : 8; }
+
 }  // namespace
 
 extern "C" {
+
+size_t bs_getrf_getrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk) {
+  if (n < 1 || nrhs < 1 || chunk < 1) return 0;
+  HostOperand ops[4] = {{nullptr, elem_size(dtype) * n * n, true, true},
+                        {nullptr, elem_size(dtype) * n * nrhs, true, true},
+                        {nullptr, sizeof(int32_t) * n, false, true},
+                        {nullptr, sizeof(int32_t), false, true}};
+  return 2 * slot_bytes(ops, 4, chunk);
+}
+
+bs_status bs_getrf_getrs_batched_host(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                      int64_t batch, void* A, void* B, int32_t* ipiv,
+                                      int32_t* info, void* work, size_t work_bytes,
+                                      int64_t chunk, void* stream0, void* stream1) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  const size_t es = elem_size(dtype);
+  HostOperand ops[4] = {{static_cast<char*>(A), es * n * n, true, true},
+                        {static_cast<char*>(B), es * n * nrhs, true, true},
+                        {reinterpret_cast<char*>(ipiv), sizeof(int32_t) * n, false, true},
+                        {reinterpret_cast<char*>(info), sizeof(int32_t), false, true}};
+  return host_pipeline(batch, chunk, ops, 4, work, work_bytes, stream0, stream1,
+                       [&](char** d, int64_t m, cudaStream_t s) {
+                         return bs_getrf_getrs_batched(dtype, layout, n, nrhs, m, d[0], d[1],
+                                                       reinterpret_cast<int32_t*>(d[2]),
+                                                       reinterpret_cast<int32_t*>(d[3]), s);
+                       });
+}
+
+size_t bs_potrf_potrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk) {
+  if (n < 1 || nrhs < 1 || chunk < 1) return 0;
+  HostOperand ops[3] = {{nullptr, elem_size(dtype) * n * n, true, true},
+                        {nullptr, elem_size(dtype) * n * nrhs, true, true},
+                        {nullptr, sizeof(int32_t), false, true}};
+  return 2 * slot_bytes(ops, 3, chunk);
+}
+
+bs_status bs_potrf_potrs_batched_host(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                      int nrhs, int64_t batch, void* A, void* B, int32_t* info,
+                                      void* work, size_t work_bytes, int64_t chunk,
+                                      void* stream0, void* stream1) {
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  const size_t es = elem_size(dtype);
+  HostOperand ops[3] = {{static_cast<char*>(A), es * n * n, true, true},
+                        {static_cast<char*>(B), es * n * nrhs, true, true},
+                        {reinterpret_cast<char*>(info), sizeof(int32_t), false, true}};
+  return host_pipeline(batch, chunk, ops, 3, work, work_bytes, stream0, stream1,
+                       [&](char** d, int64_t m, cudaStream_t s) {
+                         return bs_potrf_potrs_batched(dtype, layout, fill, n, nrhs, m, d[0],
+                                                       d[1], reinterpret_cast<int32_t*>(d[2]),
+                                                       s);
+                       });
+}
+
+size_t bs_bdsv_host_workspace(bs_dtype dtype, int num_block_rows, int block_size,
+                              int64_t chunk) {
+  if (num_block_rows < 1 || block_size < 1 || chunk < 1) return 0;
+  const size_t es = elem_size(dtype);
+  HostOperand ops[3] = {
+      {nullptr, es * num_block_rows * block_size * 3 * block_size, true, true},
+      {nullptr, es * (num_block_rows + 2) * block_size, true, true},
+      {nullptr, sizeof(int32_t), false, true}};
+  return 2 * slot_bytes(ops, 3, chunk);
+}
+
+bs_status bs_bdsv_batched_host(bs_dtype dtype, int num_block_rows, int block_size,
+                               int64_t batch, void* strips, void* x_padded, int32_t* info,
+                               void* work, size_t work_bytes, int64_t chunk, void* stream0,
+                               void* stream1) {
+  if (num_block_rows < 0 || block_size < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!bdsv_supported(dtype, num_block_rows, block_size)) return BS_ERR_UNSUPPORTED;
+  const size_t es = elem_size(dtype);
+  HostOperand ops[3] = {
+      {static_cast<char*>(strips), es * num_block_rows * block_size * 3 * block_size, true,
+       true},
+      {static_cast<char*>(x_padded), es * (num_block_rows + 2) * block_size, true, true},
+      {reinterpret_cast<char*>(info), sizeof(int32_t), false, true}};
+  return host_pipeline(batch, chunk, ops, 3, work, work_bytes, stream0, stream1,
+                       [&](char** d, int64_t m, cudaStream_t s) {
+                         return bs_bdsv_batched(dtype, num_block_rows, block_size, m, d[0], d[1],
+                                                reinterpret_cast<int32_t*>(d[2]), s);
+                       });
+}
 
 bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nrhs,
                                  int64_t batch, void* A, void* B, int32_t* ipiv,

@@ -24,6 +24,7 @@
 #ifndef BSOLVE_H
 #define BSOLVE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -275,6 +276,49 @@ BS_API bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_s
 
 /* Human-readable name of a status code (a static string). */
 BS_API const char* bs_status_string(bs_status status);
+
+/*
+ * Host-resident batches: the fused calls on arrays in host memory, copied in and out by
+ * the library in chunks that overlap the copies with the solves.
+ *
+ * Source: the fused calls above (same operands, layouts, results and status contract);
+ * RUDA docs, "ruSOLVER: small-matrix kernel optimisation" (a user call validates on the
+ * host before anything is submitted; an empty batch submits nothing).
+ *
+ *   A, B, ipiv, info, strips, x_padded  HOST arrays in the layouts of the fused calls,
+ *             read and overwritten in place with the results. Page-locked (pinned) memory
+ *             is what lets the copies run asynchronously and overlap; pageable memory
+ *             works but the copies then serialise.
+ *   work      DEVICE workspace of at least bs_*_host_workspace(...) bytes, 256-byte
+ *             aligned, owned by the caller (the library allocates nothing). Two slots of
+ *             one chunk of every operand.
+ *   chunk     systems per chunk (>= 1); chunk c runs its host-to-device copies, its solve
+ *             and its device-to-host copies on stream (c % 2 ? stream1 : stream0), in
+ *             workspace slot c % 2, so the two streams alternate and overlap (stream1 may
+ *             equal stream0: correct, no overlap).
+ * The call enqueues and returns: the results are in the host arrays once both streams
+ * have completed (e.g. cudaStreamSynchronize on each); the host arrays and the workspace
+ * must stay valid until then. Errors: the fused calls' (shape, dtype, null pointers),
+ * plus BS_ERR_INVALID_ARG for chunk < 1 or a workspace too small or misaligned. A CUDA
+ * error of a copy returns BS_ERR_CUDA; chunks already enqueued then complete or fail on
+ * their own. The *_host_workspace queries return 0 for invalid sizes.
+ */
+BS_API size_t bs_getrf_getrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk);
+BS_API bs_status bs_getrf_getrs_batched_host(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                             int64_t batch, void* A, void* B, int32_t* ipiv,
+                                             int32_t* info, void* work, size_t work_bytes,
+                                             int64_t chunk, void* stream0, void* stream1);
+BS_API size_t bs_potrf_potrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk);
+BS_API bs_status bs_potrf_potrs_batched_host(bs_dtype dtype, bs_layout layout, bs_fill fill,
+                                             int n, int nrhs, int64_t batch, void* A, void* B,
+                                             int32_t* info, void* work, size_t work_bytes,
+                                             int64_t chunk, void* stream0, void* stream1);
+BS_API size_t bs_bdsv_host_workspace(bs_dtype dtype, int num_block_rows, int block_size,
+                                     int64_t chunk);
+BS_API bs_status bs_bdsv_batched_host(bs_dtype dtype, int num_block_rows, int block_size,
+                                      int64_t batch, void* strips, void* x_padded,
+                                      int32_t* info, void* work, size_t work_bytes,
+                                      int64_t chunk, void* stream0, void* stream1);
 
 /* The CUDA error code of the last BS_ERR_CUDA returned on this host thread (0 if none). */
 BS_API int bs_last_cuda_error(void);

@@ -206,3 +206,31 @@ def test_binding_refuses_host_tensors():
     info = torch.zeros(2, dtype=torch.int32)
     with pytest.raises(ValueError):
         bs.bs_getrf_getrs_batched(A, B, ipiv, info)
+
+
+def test_host_resident_argument_errors(lib):
+    """The *_host calls check everything before the first copy: chunk, workspace (null,
+    misaligned, too small), host pointers, shapes; an empty batch submits nothing."""
+    import ctypes
+    W = 2 * (((8192 * 1024 + 255) // 256) * 256 + ((8192 * 256 + 255) // 256) * 256
+             + ((8192 * 64 + 255) // 256) * 256 + ((8192 * 4 + 255) // 256) * 256)
+    assert lib.bs_getrf_getrs_host_workspace(bs.BS_FP32, 16, 4, 8192) == W
+    assert lib.bs_getrf_getrs_host_workspace(bs.BS_FP32, 0, 4, 8192) == 0
+    assert lib.bs_potrf_potrs_host_workspace(bs.BS_FP64, 32, 1, 0) == 0
+    assert lib.bs_bdsv_host_workspace(bs.BS_FP64, 32, 8, 16) > 16 * 32 * 8 * 24 * 8
+    A, B, P, I, WK = FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x1000000
+    f = lib.bs_getrf_getrs_batched_host
+    assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, None, 0, 1, None, None) == bs.BS_OK
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, WK, W, 0, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, None, W, 8192, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, WK + 16, W, 8192, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, WK, W - 1, 8192, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, None, P, I, WK, W, 8192, None, None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 129, 4, 5, A, B, P, I, WK, W, 8192, None, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, -1, 5, A, B, P, I, WK, W, 8192, None, None) == bs.BS_ERR_INVALID_ARG
+    g = lib.bs_potrf_potrs_batched_host
+    assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, WK, 16, 8, None, None) == bs.BS_ERR_INVALID_ARG
+    assert g(bs.BS_FP64, 1, 2, 32, 1, 5, A, B, I, WK, 1 << 30, 8, None, None) == bs.BS_ERR_UNSUPPORTED
+    h = lib.bs_bdsv_batched_host
+    assert h(bs.BS_FP64, 32, 9, 5, A, B, I, WK, 1 << 30, 8, None, None) == bs.BS_ERR_UNSUPPORTED
+    assert h(bs.BS_FP64, 32, 8, 5, A, B, None, WK, 1 << 30, 8, None, None) == bs.BS_ERR_INVALID_ARG
