@@ -153,6 +153,15 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
 
   __shared__ __align__(16) T prow[kWarps][GPW][2][WP];
   __shared__ __align__(16) T xbuf[kWarps][GPW][2][RB];
+  // interleaved layout, staged: the block's systems (one AoSoA block holds them all) go
+  // through shared memory with 16-byte accesses, each holding one element of VS systems;
+  // row r of system j at (j*NT + r) * pitch (odd pitch: the lanes reading their rows hit
+  // distinct banks)
+  constexpr int SPC = kWarps * GPW;           // systems of a thread block
+  constexpr int PA = NT + 1, PB = RB + 1;
+  __shared__ __align__(16) T st_a[IL ? SPC * NT * PA : 1];
+  __shared__ __align__(16) T st_b[IL ? SPC * NT * PB : 1];
+  __shared__ __align__(16) int32_t st_p[IL ? SPC * NT : 1];
 
   const int n = FULL ? NT : n_;
   const int nrhs = FULL ? RT : nrhs_;
@@ -173,7 +182,52 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
   const int64_t sl = IL ? s - blk * ilv : 0;
   const int64_t eA = IL ? blk * ilv * n * n + sl : 0;
   const int64_t eB = IL ? blk * ilv * n * nrhs + sl : 0;
-  if (IL && row_ok) {
+  // staged when the block's systems fill whole 16-byte groups of one AoSoA block (the
+  // last, partial thread block of a batch takes the scalar path): uniform per block
+  const int64_t s_first = static_cast<int64_t>(blockIdx.x) * SPC;
+  const bool staged = IL && ilv % SPC == 0 && s_first + SPC <= batch;
+  const int jl = warp * GPW + g;                      // this group's system in the block
+  constexpr int VS = 16 / sizeof(T);                 // elements of a 16-byte access
+  const int64_t blk0 = IL ? s_first / ilv : 0;
+  const int64_t sl0 = IL ? s_first - blk0 * ilv : 0;
+  if (staged) {
+    const T* const Ab = A + blk0 * ilv * n * n + sl0;
+    const T* const Bb = B + blk0 * ilv * n * nrhs + sl0;
+    constexpr int PER = SPC / VS;                      // vectors per element
+    for (int idx = threadIdx.x; idx < n * n * PER; idx += kThreads) {
+      const int e = idx / PER, q = idx - e * PER;
+      const int r = LAYOUT == kRowMajor ? e / n : e % n;
+      const int c = LAYOUT == kRowMajor ? e % n : e / n;
+      T v[VS];
+      ld_chunk<T, VS>(Ab + static_cast<int64_t>(e) * ilv + q * VS, v, 0);
+#pragma unroll
+      for (int u = 0; u < VS; ++u) st_a[((q * VS + u) * NT + r) * PA + c] = v[u];
+    }
+    if constexpr (kSolve) {
+      for (int idx = threadIdx.x; idx < n * nrhs * PER; idx += kThreads) {
+        const int e = idx / PER, q = idx - e * PER;
+        const int r = LAYOUT == kRowMajor ? e / nrhs : e % n;
+        const int c = LAYOUT == kRowMajor ? e % nrhs : e / n;
+        T v[VS];
+        ld_chunk<T, VS>(Bb + static_cast<int64_t>(e) * ilv + q * VS, v, 0);
+#pragma unroll
+        for (int u = 0; u < VS; ++u) st_b[((q * VS + u) * NT + r) * PB + c] = v[u];
+      }
+    }
+    __syncthreads();
+    if (row_ok) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) a[j] = j < n ? st_a[(jl * NT + t) * PA + j] : T(0);
+#pragma unroll
+      for (int c = 0; c < RB; ++c)
+        b[c] = (kSolve && c < nrhs) ? st_b[(jl * NT + t) * PB + c] : T(0);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) a[j] = T(0);
+#pragma unroll
+      for (int c = 0; c < RB; ++c) b[c] = T(0);
+    }
+  } else if (IL && row_ok) {
 #pragma unroll
     for (int j = 0; j < NT; ++j)
       a[j] = (FULL || j < n) ? A[eA + (LAYOUT == kRowMajor ? t * n + j : j * n + t) * ilv] : T(0);
@@ -334,7 +388,54 @@ lu_reg_kernel(int n_, int nrhs_, int64_t batch, T* __restrict__ A, T* __restrict
     }
   }
 
-  if (IL && row_ok) {
+  if (staged) {
+    if (row_ok) {
+      if (inf != 0) {
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[c] = T(0);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+        if (j < n) st_a[(jl * NT + pos) * PA + j] = a[j];
+#pragma unroll
+      for (int c = 0; c < RT; ++c)
+        if (c < nrhs) st_b[(jl * NT + pos) * PB + c] = b[c];
+      st_p[jl * NT + pos] = my_ipiv;
+      if (t == 0) info[s] = inf;
+    }
+    __syncthreads();
+    T* const Ab = A + blk0 * ilv * n * n + sl0;
+    T* const Bb = B + blk0 * ilv * n * nrhs + sl0;
+    int32_t* const Pb = ipiv + blk0 * ilv * n + sl0;
+    constexpr int PER = SPC / VS;
+    for (int idx = threadIdx.x; idx < n * n * PER; idx += kThreads) {
+      const int e = idx / PER, q = idx - e * PER;
+      const int r = LAYOUT == kRowMajor ? e / n : e % n;
+      const int c = LAYOUT == kRowMajor ? e % n : e / n;
+      T v[VS];
+#pragma unroll
+      for (int u = 0; u < VS; ++u) v[u] = st_a[((q * VS + u) * NT + r) * PA + c];
+      st_chunk<T, VS>(Ab + static_cast<int64_t>(e) * ilv + q * VS, v, 0);
+    }
+    if constexpr (kSolve) {
+      for (int idx = threadIdx.x; idx < n * nrhs * PER; idx += kThreads) {
+        const int e = idx / PER, q = idx - e * PER;
+        const int r = LAYOUT == kRowMajor ? e / nrhs : e % n;
+        const int c = LAYOUT == kRowMajor ? e % nrhs : e / n;
+        T v[VS];
+#pragma unroll
+        for (int u = 0; u < VS; ++u) v[u] = st_b[((q * VS + u) * NT + r) * PB + c];
+        st_chunk<T, VS>(Bb + static_cast<int64_t>(e) * ilv + q * VS, v, 0);
+      }
+    }
+    constexpr int PERI = SPC / 4;                     // ipiv: four systems per 16 bytes
+    for (int idx = threadIdx.x; idx < n * PERI; idx += kThreads) {
+      const int k = idx / PERI, q = idx - k * PERI;
+      *reinterpret_cast<int4*>(Pb + static_cast<int64_t>(k) * ilv + q * 4) =
+          make_int4(st_p[(q * 4) * NT + k], st_p[(q * 4 + 1) * NT + k],
+                    st_p[(q * 4 + 2) * NT + k], st_p[(q * 4 + 3) * NT + k]);
+    }
+  } else if (IL && row_ok) {
     if (inf != 0) {
 #pragma unroll
       for (int c = 0; c < RT; ++c) b[c] = T(0);
