@@ -502,6 +502,7 @@ def run_native(args) -> None:
         "e2e": {"value": round(whole_job_rate(prob.batch, world, e2e_ms), 1), "unit": "systems/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
+                "gpu_launches_per_step": -(-prob.batch // args.e2e_chunk),
                 "call": "bs_*_batched_host: pinned host arrays, chunks of "
                         f"{args.e2e_chunk} systems on two streams (copies overlap solves)"},
         "gpu_launches": args.steps,
