@@ -44,7 +44,7 @@ EXPORTED = (
     "bs_getrf_getrs_batched_ex", "bs_potrf_potrs_batched_ex",
     "bs_getrf_getrs_host_workspace", "bs_getrf_getrs_batched_host",
     "bs_potrf_potrs_host_workspace", "bs_potrf_potrs_batched_host",
-    "bs_bdsv_host_workspace", "bs_bdsv_batched_host",
+    "bs_bdsv_host_workspace", "bs_bdsv_batched_host", "bs_getrf_getrs_batched_host_static",
     "bs_status_string", "bs_last_cuda_error", "bs_getrf_getrs_supported",
     "bs_potrf_potrs_supported", "bs_bdsv_supported", "bs_version",
 )
@@ -109,8 +109,10 @@ def lib() -> ctypes.CDLL:
                                                       vp, sz, i64, vp, vp]
             L.bs_bdsv_batched_host.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, sz, i64, vp,
                                                vp]
+            L.bs_getrf_getrs_batched_host_static.argtypes = [i32, i32, i32, i32, i64, vp, vp,
+                                                             vp, vp, i64, vp, vp]
             for name in ("bs_getrf_getrs_batched_host", "bs_potrf_potrs_batched_host",
-                         "bs_bdsv_batched_host"):
+                         "bs_bdsv_batched_host", "bs_getrf_getrs_batched_host_static"):
                 getattr(L, name).restype = i32
             L.bs_status_string.argtypes = [i32]
             L.bs_status_string.restype = ctypes.c_char_p
@@ -370,3 +372,22 @@ def bs_bdsv_batched_host(strips, x_padded, info, chunk: int = 2048,
     if sync:
         plan.synchronize()
     return plan
+
+
+def bs_getrf_getrs_batched_host_static(A, B, ipiv, info, layout: int = ROW_MAJOR,
+                                       chunk: int = 16384, streams=None,
+                                       sync: bool = True):
+    """bs_getrf_getrs_batched_host on the library's static device scratch (no workspace
+    argument; see bsolve.h for the one-call-at-a-time rule). Returns the two streams."""
+    import torch
+    batch, n = A.shape[0], A.shape[1]
+    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    streams = tuple(streams) if streams else (torch.cuda.Stream(), torch.cuda.Stream())
+    st = lib().bs_getrf_getrs_batched_host_static(
+        _dtype_code(A), layout, n, nrhs, batch, _host_ptr(A), _host_ptr(B), _host_ptr(ipiv),
+        _host_ptr(info), chunk, _stream(streams[0]), _stream(streams[1]))
+    _check(st, "bs_getrf_getrs_batched_host_static")
+    if sync:
+        for s_ in streams:
+            s_.synchronize()
+    return streams

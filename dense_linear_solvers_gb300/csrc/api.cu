@@ -216,6 +216,11 @@ bs_status host_pipeline(int64_t batch, int64_t chunk, HostOperand* ops, int nops
 
 size_t elem_size(bs_dtype dtype) { return dtype == BS_FP32 ? 4 : 8; }
 
+// Scratch of the entry point that takes no workspace: one static device array, placed by
+// the driver when the library's module loads (no call allocates).
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
 }  // namespace
 
 extern "C" {
@@ -246,6 +251,26 @@ bs_status bs_getrf_getrs_batched_host(bs_dtype dtype, bs_layout layout, int n, i
                                                        reinterpret_cast<int32_t*>(d[2]),
                                                        reinterpret_cast<int32_t*>(d[3]), s);
                        });
+}
+
+bs_status bs_getrf_getrs_batched_host_static(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                             int64_t batch, void* A, void* B, int32_t* ipiv,
+                                             int32_t* info, int64_t chunk, void* stream0,
+                                             void* stream1) {
+  if (n < 0 || nrhs < 0 || batch < 0 || chunk < 1) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  // the largest chunk, up to the requested one, whose two slots fit the static scratch
+  int64_t c = chunk;
+  while (c > 1 && bs_getrf_getrs_host_workspace(dtype, n, nrhs, c) > kStaticScratchBytes)
+    c = c / 2;
+  if (bs_getrf_getrs_host_workspace(dtype, n, nrhs, c) > kStaticScratchBytes)
+    return BS_ERR_UNSUPPORTED;
+  void* work = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&work, g_static_scratch);
+  if (e != cudaSuccess) return from_cuda(e);
+  return bs_getrf_getrs_batched_host(dtype, layout, n, nrhs, batch, A, B, ipiv, info, work,
+                                     kStaticScratchBytes, c, stream0, stream1);
 }
 
 size_t bs_potrf_potrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk) {

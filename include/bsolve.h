@@ -308,6 +308,20 @@ BS_API bs_status bs_getrf_getrs_batched_host(bs_dtype dtype, bs_layout layout, i
                                              int64_t batch, void* A, void* B, int32_t* ipiv,
                                              int32_t* info, void* work, size_t work_bytes,
                                              int64_t chunk, void* stream0, void* stream1);
+/*
+ * bs_getrf_getrs_batched_host without a workspace argument: the library's own static
+ * device scratch (64 MiB, placed when the library loads; the call allocates nothing)
+ * holds the two chunk slots, and the chunk is the requested one halved until its slots
+ * fit (BS_ERR_UNSUPPORTED if one system does not fit). One scratch serves the whole
+ * process: a call may start only once the previous call's chunks are done or are queued
+ * on the same two streams (stream order then keeps them apart); concurrent calls from
+ * several host threads on other streams must not overlap. Otherwise as
+ * bs_getrf_getrs_batched_host.
+ */
+BS_API bs_status bs_getrf_getrs_batched_host_static(bs_dtype dtype, bs_layout layout, int n,
+                                                    int nrhs, int64_t batch, void* A, void* B,
+                                                    int32_t* ipiv, int32_t* info, int64_t chunk,
+                                                    void* stream0, void* stream1);
 BS_API size_t bs_potrf_potrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk);
 BS_API bs_status bs_potrf_potrs_batched_host(bs_dtype dtype, bs_layout layout, bs_fill fill,
                                              int n, int nrhs, int64_t batch, void* A, void* B,
