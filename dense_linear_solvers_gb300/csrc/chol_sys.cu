@@ -19,6 +19,10 @@
 // The factorization is right-looking (cuSolverDx docs, "Cholesky Factorization": only
 // the lower triangle is read and replaced by L; info = the smallest leading minor that
 // is not positive definite), with the forward solve folded into it; then L^T x = y.
+// Per column k: scale column k (all warps), barrier, then the trailing update on all warps
+// but one, the chain warp of column k+1, which updates a_{k+1,k+1} only and takes column
+// k+1's square root and reciprocal at once (look-ahead: the serial chain overlaps the
+// update and needs no barrier of its own), barrier.
 // The arithmetic is the CPU oracle's, operation by operation. A system whose minor
 // fails keeps computing (no branch depends on the data) and returns X = 0.
 #include "common.cuh"
@@ -88,19 +92,22 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
   cp_async_wait_all();
   __syncthreads();
 
+  // A: the pivot of column kk, one lane per system (lanes 0..15 of the chain warp): the
+  //    square root and its reciprocal; the first failing minor sets info
+  auto pivot = [&](int kk) {
+    const T d = Ms[tri(kk) + kk];
+    if (!(d > T(0)) && sinfo[s] == 0) sinfo[s] = kk + 1;
+    const T l = sqrt_rn<T>(d);
+    Ms[tri(kk) + kk] = l;
+    rr[kk * kSys + s] = rcp_rn<T>(l);
+  };
+  // the chain warp of column kk rotates with the column and the block: warp w runs on SM
+  // sub-partition w % 4, so a fixed warp would put every block's chain on one FP64 pipe
+  auto chain_warp = [&](int kk) { return (static_cast<int>(blockIdx.x) + kk) & (kWarps - 1); };
+  if (warp == chain_warp(0) && lane < kSys) pivot(0);
+  __syncthreads();
+
   for (int k = 0; k < n; ++k) {
-    // A: the pivot square root and reciprocal of column k, one lane per system, on lanes
-    //    0..15 of a warp that rotates with the column and the block: warp w runs on SM
-    //    sub-partition w % 4, so a fixed warp would put every block's chain on one FP64 pipe
-    const int cw = (static_cast<int>(blockIdx.x) + k) & (kWarps - 1);
-    if (warp == cw && lane < kSys) {
-      const T d = Ms[tri(k) + k];
-      if (!(d > T(0)) && sinfo[s] == 0) sinfo[s] = k + 1;
-      const T l = sqrt_rn<T>(d);
-      Ms[tri(k) + k] = l;
-      rr[k * kSys + s] = rcp_rn<T>(l);
-    }
-    __syncthreads();
     // B: scale column k below the diagonal, and y_k
     {
       const int m = n - 1 - k;
@@ -117,28 +124,41 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     }
     __syncthreads();
     // C: trailing lower triangle (row by row: row i holds columns k+1..i), then the
-    //    forward solve of rows k+1..n-1
+    //    forward solve of rows k+1..n-1. Element 0, a_{k+1,k+1}, belongs to the chain
+    //    warp of column k+1, which then takes that column's pivot (A) at once and does
+    //    nothing else, so the serial chain overlaps the rest of the update (spread over
+    //    the other warps' slots) and needs no barrier of its own.
     {
       const int m = n - 1 - k;
       const int T_k = m * (m + 1) / 2;
-      int i = k + 1, j = k + 1 + slot;
-      while (i < n && j > i) {
-        j -= i - k;
-        ++i;
-      }
-      int e = slot;
-      for (; e < T_k; e += kSlots) {
-        const int ti = tri(i);
-        Ms[ti + j] = fma_rn<T>(-Ms[ti + k], Ms[tri(j) + k], Ms[ti + j]);
-        j += kSlots;
+      const int cw = chain_warp(k + 1);
+      if (warp == cw) {
+        if (m > 0 && lane < kSys) {
+          const int t1 = tri(k + 1);
+          Ms[t1 + k + 1] = fma_rn<T>(-Ms[t1 + k], Ms[t1 + k], Ms[t1 + k + 1]);
+          pivot(k + 1);
+        }
+      } else {
+        constexpr int kOther = kSlots - 2;             // the other warps' slots
+        const int vs = slot < 2 * cw ? slot : slot - 2;
+        int i = k + 1, j = k + 2 + vs;                 // element 1 + vs
         while (i < n && j > i) {
           j -= i - k;
           ++i;
         }
-      }
-      for (e -= T_k; e < m * nrhs; e += kSlots) {
-        const int ii = k + 1 + e / nrhs, c = e - (e / nrhs) * nrhs;
-        Ys[ii * nrhs + c] = fma_rn<T>(-Ms[tri(ii) + k], Ys[k * nrhs + c], Ys[ii * nrhs + c]);
+        for (int e = 1 + vs; e < T_k; e += kOther) {
+          const int ti = tri(i);
+          Ms[ti + j] = fma_rn<T>(-Ms[ti + k], Ms[tri(j) + k], Ms[ti + j]);
+          j += kOther;
+          while (i < n && j > i) {
+            j -= i - k;
+            ++i;
+          }
+        }
+        for (int f = vs; f < m * nrhs; f += kOther) {
+          const int ii = k + 1 + f / nrhs, c = f - (f / nrhs) * nrhs;
+          Ys[ii * nrhs + c] = fma_rn<T>(-Ms[tri(ii) + k], Ys[k * nrhs + c], Ys[ii * nrhs + c]);
+        }
       }
     }
     __syncthreads();
