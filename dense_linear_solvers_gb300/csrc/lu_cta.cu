@@ -6,12 +6,13 @@
 // looking factorization follows LAPACK's order with physical row interchanges (TDLS
 // API, "solver_static.hpp File Reference", Detailed Description: physical and logical
 // interchanges choose the same pivots and run the same operations):
-//   phase 1 (one warp): pivot search over column k with integer magnitude keys and the
-//     lowest-row tie rule, interchange of rows k and p, the correctly rounded pivot
-//     reciprocal, the multipliers of column k;
-//   phase 2 (all warps): the rank-1 update of rows k+1.., columns k+1.. of [A | B]
-//     (the forward solve L y = P b folded in), spread element by element over the
-//     block's 128 lanes so that lanes stay busy however small the trailing block gets.
+//   phase 1 (one warp, during the previous step's update: look-ahead): the update of
+//     column k, then its pivot search with integer magnitude keys and the lowest-row tie
+//     rule, and the correctly rounded pivot reciprocal;
+//   phase 2 (all warps): the interchange of rows k and p and the multipliers of column k;
+//   phase 3 (the other warps): the rank-1 update of rows k+1.., columns k+2.. of [A | B]
+//     (the forward solve L y = P b folded in), spread element by element over their
+//     lanes so that lanes stay busy however small the trailing block gets.
 // On this part a warp FP64 instruction is charged whatever its active lanes, so the
 // lane count that does useful FP64 work is what sets the speed; four warps per system
 // also give the SM enough warps to cover each system's serial pivot phase. The serial
@@ -62,6 +63,8 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
   int* const piv = reinterpret_cast<int*>(rcp + n);
   __shared__ int s_info;
   __shared__ Key s_max;
+  __shared__ int s_p;      // pivot row of the step being prepared
+  __shared__ T s_pv, s_akk;
 
   // element e of the system at A[e * ilv] (ilv = 1: the systems one after another;
   // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B, ipiv
@@ -141,68 +144,105 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
     __syncthreads();
   }
 
-  for (int k = 0; k < n; ++k) {
-    // the serial part of step k runs on a warp that rotates with the step and the block:
-    // warp w runs on SM sub-partition w % 4, and a fixed warp would put every block's
-    // serial work on one sub-partition
-    if (warp == ((static_cast<int>(blockIdx.x) + k) & (kWarps - 1))) {
-      // pivot search over rows k..n-1 of column k; a lane keeps its first maximum
-      Key best = 0;
-      int bi = 0x7FFFFFFF;
-      for (int i = k + lane; i < n; i += 32) {
-        const Key key = pivot_key<T>(M[i * P + k], i == k);
-        if (key > best) {
-          best = key;
-          bi = i;
-        }
+  // The pivot search of column kk (rows kk..n-1) on the calling warp; it moves no data:
+  // the pivot row, the pivot and the old a_kk go to shared scalars, ipiv, info and the
+  // pivot reciprocal to their arrays. A lane keeps its first maximum; the lowest row wins
+  // a tie.
+  auto search = [&](int kk) {
+    Key best = 0;
+    int bi = 0x7FFFFFFF;
+    for (int i = kk + lane; i < n; i += 32) {
+      const Key key = pivot_key<T>(M[i * P + kk], i == kk);
+      if (key > best) {
+        best = key;
+        bi = i;
       }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const Key ob = shfl_xor_key(best, off, 32);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (ob > best || (ob == best && oi < bi)) {
-          best = ob;
-          bi = oi;
-        }
-      }
-      int p = bi;
-      Key pkey = best;
-      if (p != k && tau < T(1)) {
-        // threshold pivoting: the row in place stays when |a_kk| >= tau * m, m the
-        // magnitude the search found (not a NaN: a NaN in place would have won)
-        const T akk = M[k * P + k];
-        if (fabs(akk) >= tau * pivot_from_key<T>(best, 0u)) {
-          p = k;
-          pkey = pivot_key<T>(akk, true);
-        }
-      }
-      const bool ok = pivot_ok<T>(pkey);
-      if (lane == 0) {
-        piv[k] = p + 1;
-        if (!ok && s_info == 0) s_info = k + 1;
-      }
-      if (p != k) {
-        for (int j = lane; j < W; j += 32) {
-          const T t = M[k * P + j];
-          M[k * P + j] = M[p * P + j];
-          M[p * P + j] = t;
-        }
-      }
-      __syncwarp();
-      const T r = ok ? rcp_rn<T>(M[k * P + k]) : T(1);
-      if (lane == 0) rcp[k] = r;
-      for (int i = k + 1 + lane; i < n; i += 32) M[i * P + k] = M[i * P + k] * r;
     }
-    __syncthreads();
-    // rank-1 update of rows k+1..n-1, columns k+1..W-1, walked column by column
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const Key ob = shfl_xor_key(best, off, 32);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+      if (ob > best || (ob == best && oi < bi)) {
+        best = ob;
+        bi = oi;
+      }
+    }
+    int p = bi;
+    Key pkey = best;
+    const T akk = M[kk * P + kk];
+    if (p != kk && tau < T(1)) {
+      // threshold pivoting: the row in place stays when |a_kk| >= tau * m, m the
+      // magnitude the search found (not a NaN: a NaN in place would have won)
+      if (fabs(akk) >= tau * pivot_from_key<T>(best, 0u)) {
+        p = kk;
+        pkey = pivot_key<T>(akk, true);
+      }
+    }
+    const bool ok = pivot_ok<T>(pkey);
+    if (lane == 0) {
+      const T pv = M[p * P + kk];
+      piv[kk] = p + 1;
+      if (!ok && s_info == 0) s_info = kk + 1;
+      rcp[kk] = ok ? rcp_rn<T>(pv) : T(1);
+      s_p = p;
+      s_pv = pv;
+      s_akk = akk;
+    }
+  };
+  // All threads: rows kk and p exchanged over every column but kk, and column kk below the
+  // diagonal scaled by the pivot reciprocal, its entries at kk and p taken from the
+  // scalars the search saved (so no thread reads what another writes).
+  auto swap_scale = [&](int kk) {
+    const int p = s_p;
+    const T r = rcp[kk];
+    if (p != kk) {
+      for (int j = tid; j < W; j += kThreads) {
+        if (j == kk) continue;
+        const T t = M[kk * P + j];
+        M[kk * P + j] = M[p * P + j];
+        M[p * P + j] = t;
+      }
+    }
+    for (int i = kk + tid; i < n; i += kThreads) {
+      if (i == kk)
+        M[i * P + kk] = s_pv;
+      else if (i == p)
+        M[i * P + kk] = s_akk * r;
+      else
+        M[i * P + kk] = M[i * P + kk] * r;
+    }
+  };
+  // the search of column kk runs on a warp that rotates with the column and the block:
+  // warp w runs on SM sub-partition w % 4, and a fixed warp would put every block's
+  // serial work on one sub-partition
+  auto chain = [&](int kk) { return (static_cast<int>(blockIdx.x) + kk) & (kWarps - 1); };
+
+  if (warp == chain(0)) search(0);
+  __syncthreads();
+  swap_scale(0);
+  __syncthreads();
+  for (int k = 0; k < n; ++k) {
+    // rank-1 update of rows k+1..n-1, columns k+1..W-1 (look-ahead: the chain warp of
+    // column k+1 updates that column and searches its pivot while the other warps update
+    // the columns after it; the exchange and scaling of step k+1 follow the barrier)
     const int m = n - k - 1;
-    const int w = W - k - 1;
-    if (m > 0) {
+    const bool ahead = k + 1 < n;
+    const int cw = ahead ? chain(k + 1) : -1;
+    if (warp == cw) {
+      for (int i = k + 1 + lane; i < n; i += 32)
+        M[i * P + k + 1] = fma_rn<T>(-M[i * P + k], M[k * P + k + 1], M[i * P + k + 1]);
+      __syncwarp();
+      search(k + 1);
+    } else if (m > 0) {
+      const int j0 = ahead ? k + 2 : k + 1;
+      const int w = W - j0;
+      const int nth = ahead ? kThreads - 32 : kThreads;
+      const int t = (ahead && warp > cw) ? tid - 32 : tid;
       const int total = m * w;
-      const int dq = kThreads / m, dr = kThreads - dq * m;
-      int ii = tid % m, jj = tid / m;
-      for (int e = tid; e < total; e += kThreads) {
-        const int i = k + 1 + ii, j = k + 1 + jj;
+      const int dq = nth / m, dr = nth - dq * m;
+      int ii = t % m, jj = t / m;
+      for (int e = t; e < total; e += nth) {
+        const int i = k + 1 + ii, j = j0 + jj;
         M[i * P + j] = fma_rn<T>(-M[i * P + k], M[k * P + j], M[i * P + j]);
         ii += dr;
         jj += dq;
@@ -213,6 +253,10 @@ lu_cta_kernel(int n, int nrhs, int layout, int64_t batch, T* __restrict__ A,
       }
     }
     __syncthreads();
+    if (ahead) {
+      swap_scale(k + 1);
+      __syncthreads();
+    }
   }
 
   // RUDA scaling: U's scale restored, and the reciprocals of its diagonal recomputed for
