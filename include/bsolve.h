@@ -3,14 +3,18 @@
  * linear systems A x = b on one GPU (sm_103a).
  *
  * Every entry point solves `batch` independent systems in one asynchronous launch (two
- * for a fused call with more than 8 right-hand sides: the factor, then the solve) on
- * the caller's CUDA stream. All matrix and vector pointers are DEVICE pointers owned by
- * the caller; the library allocates no memory, keeps no state between calls and never
- * synchronizes the host. Results are valid once the stream has reached the launch;
- * the per-system `info` array is read back by the caller when it needs it.
+ * when a factor and a solve run apart: a fused call with more than 8 right-hand sides,
+ * the row-major reading of the _ex call) on the caller's CUDA stream. All matrix and
+ * vector pointers are DEVICE pointers owned by the caller, except those of the
+ * *_batched_host calls (host arrays, copied in and out by chunks on two streams); the
+ * library allocates no memory, keeps no state between calls and never synchronizes the
+ * host. Results are valid once the stream has reached the launch; the per-system `info`
+ * array is read back by the caller when it needs it. Calls may run concurrently on
+ * different streams and may be captured into CUDA graphs.
  *
  * Batched storage: system s of a batched operand starts at element s * (elements per
- * system); there is no padding between systems. Offsets are 64-bit.
+ * system); there is no padding between systems. Offsets are 64-bit. (The _ex calls also
+ * take the interleaved AoSoA/SoA layouts: bs_options.interleave.)
  *
  * Errors are reported synchronously, before anything is launched:
  *   BS_ERR_INVALID_ARG  null pointer, negative size, or a base address not 16-byte aligned;
