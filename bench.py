@@ -469,7 +469,9 @@ def run_native(args) -> None:
     ranks.barrier()
     clocks = sampler.stop(local)
     ms = statistics.fmean(times)
+    ranks.barrier()                   # the end-to-end steps start together on every rank
     e2e_times, h2d, d2h = time_e2e(prob, max(3, min(args.steps, 20)), 2, args.e2e_chunk)
+    ranks.barrier()
     e2e_ms = statistics.fmean(e2e_times)
     ms, e2e_ms = ranks.max([ms, e2e_ms], device=dev)
     if rank != 0:
