@@ -1,6 +1,9 @@
 // C ABI of libbsolve.so: argument checks and dispatch to the kernel launchers.
 // See include/bsolve.h for the contract of every entry point.
 #include <cstdint>
+#include <initializer_list>
+#include <utility>
+
 #include <cuda_runtime.h>
 
 #include "bsolve.h"
@@ -22,6 +25,37 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
+}
+
+// Whether the byte ranges are pairwise disjoint: the operands of one call must not alias.
+using Range = std::pair<const void*, size_t>;
+bool disjoint(std::initializer_list<Range> rs) {
+  for (auto a = rs.begin(); a != rs.end(); ++a)
+    for (auto b = a + 1; b != rs.end(); ++b)
+      if (overlap(a->first, a->second, b->first, b->second)) return false;
+  return true;
+}
+
+// Systems a batched operand holds: the batch, rounded up to whole blocks of an
+// interleaved layout (ilv > 1).
+size_t held(int64_t batch, int64_t ilv) {
+  return static_cast<size_t>(ilv > 1 ? (batch + ilv - 1) / ilv * ilv : batch);
+}
+
+// The four operands of an LU call (A, B, ipiv, info) do not alias.
+bool lu_disjoint(bs_dtype dtype, int n, int nrhs, int64_t batch, int64_t ilv, const void* A,
+                 const void* B, const void* ipiv, const void* info) {
+  const size_t es = dtype == BS_FP32 ? 4 : 8, h = held(batch, ilv);
+  return disjoint({{A, h * n * n * es}, {B, h * n * nrhs * es}, {ipiv, h * n * 4},
+                   {info, static_cast<size_t>(batch) * 4}});
+}
+
+// The three operands of a Cholesky call (A, B, info) do not alias.
+bool chol_disjoint(bs_dtype dtype, int n, int nrhs, int64_t batch, int64_t ilv, const void* A,
+                   const void* B, const void* info) {
+  const size_t es = dtype == BS_FP32 ? 4 : 8, h = held(batch, ilv);
+  return disjoint({{A, h * n * n * es}, {B, h * n * nrhs * es},
+                   {info, static_cast<size_t>(batch) * 4}});
 }
 
 bs_status from_cuda(cudaError_t e) {
@@ -67,6 +101,7 @@ bs_status getrf_getrs_mirror(bs_dtype dtype, int n, int nrhs, int64_t batch, voi
   if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
     return BS_ERR_INVALID_ARG;
+  if (!lu_disjoint(dtype, n, nrhs, batch, 1, A, B, ipiv, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (tau == 1.0) {
@@ -104,6 +139,7 @@ bs_status getrf_getrs_il(bs_dtype dtype, bs_layout layout, int n, int nrhs, int6
   if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
     return BS_ERR_INVALID_ARG;
+  if (!lu_disjoint(dtype, n, nrhs, batch, ilv, A, B, ipiv, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (n <= kMaxRegN) {
@@ -132,6 +168,7 @@ bs_status potrf_potrs_il(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, 
   if (batch == 0) return BS_OK;
   if (!A || !B || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!chol_disjoint(dtype, n, nrhs, batch, ilv, A, B, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int code = chol_layouts(layout, fill);
   cudaError_t e;
@@ -183,8 +220,12 @@ bs_status host_pipeline(int64_t batch, int64_t chunk, HostOperand* ops, int nops
   if (batch < 0 || chunk < 1) return BS_ERR_INVALID_ARG;
   if (batch == 0) return BS_OK;
   if (!work || (reinterpret_cast<uintptr_t>(work) % kWorkAlign) != 0) return BS_ERR_INVALID_ARG;
-  for (int i = 0; i < nops; ++i)
+  for (int i = 0; i < nops; ++i) {
     if (!ops[i].host) return BS_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)   // the host arrays do not alias
+      if (overlap(ops[i].host, ops[i].per_sys * batch, ops[j].host, ops[j].per_sys * batch))
+        return BS_ERR_INVALID_ARG;
+  }
   const size_t slot = slot_bytes(ops, nops, chunk);
   if (work_bytes < 2 * slot) return BS_ERR_INVALID_ARG;
   cudaStream_t st[2] = {static_cast<cudaStream_t>(stream0), static_cast<cudaStream_t>(stream1)};
@@ -338,6 +379,7 @@ bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n, int nr
   if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
     return BS_ERR_INVALID_ARG;
+  if (!lu_disjoint(dtype, n, nrhs, batch, 1, A, B, ipiv, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (nrhs > kMaxNrhs) {
@@ -376,6 +418,7 @@ bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill,
   if (batch == 0) return BS_OK;
   if (!A || !B || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!chol_disjoint(dtype, n, nrhs, batch, 1, A, B, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (nrhs > kMaxNrhs) {
@@ -416,6 +459,12 @@ bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_size, in
   if (batch == 0) return BS_OK;
   if (!strips || !x_padded || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(strips) || !aligned16(x_padded) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  {
+    const size_t es = dtype == BS_FP32 ? 4 : 8, b = static_cast<size_t>(batch);
+    if (!disjoint({{strips, b * num_block_rows * block_size * 3 * block_size * es},
+                   {x_padded, b * (num_block_rows + 2) * block_size * es}, {info, b * 4}}))
+      return BS_ERR_INVALID_ARG;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == BS_FP32
@@ -435,6 +484,11 @@ bs_status bs_getrf_batched(bs_dtype dtype, bs_layout layout, int n, int64_t batc
   if (batch == 0) return BS_OK;
   if (!A || !ipiv || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(ipiv) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  {
+    const size_t es = dtype == BS_FP32 ? 4 : 8, b = static_cast<size_t>(batch);
+    if (!disjoint({{A, b * n * n * es}, {ipiv, b * n * 4}, {info, b * 4}}))
+      return BS_ERR_INVALID_ARG;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (n <= kMaxRegN) {
@@ -484,6 +538,9 @@ bs_status bs_potrf_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n
   if (batch == 0) return BS_OK;
   if (!A || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!disjoint({{A, static_cast<size_t>(batch) * n * n * (dtype == BS_FP32 ? 4 : 8)},
+                 {info, static_cast<size_t>(batch) * 4}}))
+    return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (n <= kMaxRegN) {
@@ -532,6 +589,10 @@ bs_status bs_bdsv_factor_batched(bs_dtype dtype, int num_block_rows, int block_s
   if (batch == 0) return BS_OK;
   if (!strips || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(strips) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!disjoint({{strips, static_cast<size_t>(batch) * num_block_rows * block_size * 3 *
+                              block_size * (dtype == BS_FP32 ? 4 : 8)},
+                 {info, static_cast<size_t>(batch) * 4}}))
+    return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == BS_FP32
@@ -622,6 +683,7 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
   if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
     return BS_ERR_INVALID_ARG;
+  if (!lu_disjoint(dtype, n, nrhs, batch, il, A, B, ipiv, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int ruda = contract == BS_CONTRACT_RUDA;
   cudaError_t e =
@@ -658,6 +720,7 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
   if (batch == 0) return BS_OK;
   if (!A || !B || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!chol_disjoint(dtype, n, nrhs, batch, il, A, B, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == BS_FP32

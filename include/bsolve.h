@@ -17,7 +17,8 @@
  * take the interleaved AoSoA/SoA layouts: bs_options.interleave.)
  *
  * Errors are reported synchronously, before anything is launched:
- *   BS_ERR_INVALID_ARG  null pointer, negative size, or a base address not 16-byte aligned;
+ *   BS_ERR_INVALID_ARG  null pointer, negative size, a base address not 16-byte aligned,
+ *                       or two operands of the call whose byte ranges overlap;
  *   BS_ERR_UNSUPPORTED  a shape, dtype, layout or fill with no kernel instance (there is
  *                       no CPU fallback: the caller chooses another path);
  *   BS_ERR_CUDA         the launch itself failed (bs_last_cuda_error() gives the code).

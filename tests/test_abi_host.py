@@ -234,3 +234,34 @@ def test_host_resident_argument_errors(lib):
     h = lib.bs_bdsv_batched_host
     assert h(bs.BS_FP64, 32, 9, 5, A, B, I, WK, 1 << 30, 8, None, None) == bs.BS_ERR_UNSUPPORTED
     assert h(bs.BS_FP64, 32, 8, 5, A, B, None, WK, 1 << 30, 8, None, None) == bs.BS_ERR_INVALID_ARG
+
+
+def test_aliased_operands_are_rejected(lib):
+    """Operands of one call must not alias: every entry point checks the byte ranges of
+    its operands (the interleaved layouts with their whole blocks) before launching."""
+    import ctypes
+    A = FAKE
+    # LU FP32 n=16 nrhs=4 batch 5: A takes 5 KB; B placed inside it, then just after it
+    assert lib.bs_getrf_getrs_batched(bs.BS_FP32, 0, 16, 4, 5, A, A + 4096, A + 0x100000,
+                                      A + 0x200000, None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_getrf_getrs_batched(bs.BS_FP32, 0, 16, 4, 5, A, A + 0x100000, A + 0x100000 + 1264,
+                                      A + 0x200000, None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_getrf_getrs_batched(bs.BS_FP32, 0, 16, 4, 5, A, A + 0x100000, A + 0x200000,
+                                      A + 0x200000 + 304, None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_potrf_potrs_batched(bs.BS_FP64, 1, 0, 32, 1, 5, A, A + 40960 - 16,
+                                      A + 0x100000, None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_bdsv_batched(bs.BS_FP64, 32, 8, 2, A, A + 0x100000, A + 0x100000 + 528,
+                               None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_getrf_batched(bs.BS_FP64, 1, 8, 3, A, A + 8 * 8 * 8 * 2, A + 0x100000,
+                                None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_potrf_batched(bs.BS_FP64, 1, 0, 8, 3, A, A + 512, None) == bs.BS_ERR_INVALID_ARG
+    assert lib.bs_bdsv_factor_batched(bs.BS_FP64, 4, 2, 3, A, A + 16, None) == bs.BS_ERR_INVALID_ARG
+    # interleaved: 5 systems in blocks of 4 hold 8 systems' room (8 KB for FP64 n=8)
+    o = ctypes.byref(bs.Options(1.0, 0, 0, 4, 0))
+    assert lib.bs_getrf_getrs_batched_ex(bs.BS_FP64, 0, 8, 1, 5, A, A + 5 * 512, A + 0x100000,
+                                         A + 0x200000, o, None) == bs.BS_ERR_INVALID_ARG
+    # host arrays of the host-resident call
+    W = lib.bs_getrf_getrs_host_workspace(bs.BS_FP32, 16, 4, 8)
+    assert lib.bs_getrf_getrs_batched_host(bs.BS_FP32, 0, 16, 4, 5, A, A + 1024, A + 0x100000,
+                                           A + 0x200000, A + 0x1000000, W, 8, None,
+                                           None) == bs.BS_ERR_INVALID_ARG
