@@ -153,6 +153,56 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
+def _expect(t, name: str, dtype, numel: int) -> None:
+    """An operand's element type and element count, checked before its pointer is taken:
+    the library sees only pointers and sizes, so a tensor of another type or size would be
+    read as if it were the expected one. None passes (the library reports the null)."""
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+
+
+def _dense(A, B, layout: int):
+    """(batch, n, nrhs) of a dense call, B checked against A: A is (batch, n, n); B is
+    (batch, n, nrhs) in row-major storage, (batch, nrhs, n) in column-major, of A's dtype.
+    B None: a factor call (nrhs 0)."""
+    if A.dim() != 3 or A.shape[1] != A.shape[2]:
+        raise ValueError(f"A: shape {tuple(A.shape)}, expected (batch, n, n)")
+    batch, n = A.shape[0], A.shape[1]
+    if B is None:
+        return batch, n, 0
+    if B.dim() != 3 or B.shape[0] != batch or B.shape[1 if layout == ROW_MAJOR else 2] != n:
+        want = "(batch, n, nrhs)" if layout == ROW_MAJOR else "(batch, nrhs, n)"
+        raise ValueError(f"B: shape {tuple(B.shape)}, expected {want} with batch {batch}, n {n}")
+    if B.dtype != A.dtype:
+        raise TypeError(f"B: dtype {B.dtype}, expected A's {A.dtype}")
+    return batch, n, (B.shape[2] if layout == ROW_MAJOR else B.shape[1])
+
+
+def _pivots(ipiv, info, batch: int, n: int, held: int | None = None) -> None:
+    # ipiv: n int32 per system (held systems of an interleaved batch); info: one per system
+    import torch
+    _expect(ipiv, "ipiv", torch.int32, (batch if held is None else held) * n)
+    _expect(info, "info", torch.int32, batch)
+
+
+def _strips(strips, vectors, info):
+    """(batch, nbr, bs) of a block-tridiagonal call: strips (batch, nbr, bs, 3*bs); each
+    padded vector (nbr + 2) * bs per system, of the strips' dtype; info one int32 each."""
+    import torch
+    if strips.dim() != 4 or strips.shape[3] != 3 * strips.shape[2]:
+        raise ValueError(f"strips: shape {tuple(strips.shape)}, expected (batch, nbr, bs, 3*bs)")
+    batch, nbr, bsz = strips.shape[0], strips.shape[1], strips.shape[2]
+    for name, v in vectors:
+        _expect(v, name, strips.dtype, batch * (nbr + 2) * bsz)
+    if info is not None:
+        _expect(info, "info", torch.int32, batch)
+    return batch, nbr, bsz
+
+
 def _stream(stream) -> int:
     import torch
     if stream is None:
@@ -167,8 +217,8 @@ def _check(status: int, what: str) -> None:
 
 def bs_getrf_getrs_batched(A, B, ipiv, info, layout: int = ROW_MAJOR, stream=None) -> None:
     """LU with partial pivoting + solve of A[s] X = B[s], in place (see bsolve.h)."""
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(A, B, layout)
+    _pivots(ipiv, info, batch, n)
     st = lib().bs_getrf_getrs_batched(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
                                       _ptr(ipiv), _ptr(info), _stream(stream))
     _check(st, "bs_getrf_getrs_batched")
@@ -177,8 +227,8 @@ def bs_getrf_getrs_batched(A, B, ipiv, info, layout: int = ROW_MAJOR, stream=Non
 def bs_potrf_potrs_batched(A, B, info, layout: int = COL_MAJOR, fill: int = BS_LOWER,
                            stream=None) -> None:
     """Cholesky + solve of SPD systems, in place (see bsolve.h)."""
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(A, B, layout)
+    _pivots(None, info, batch, n)
     st = lib().bs_potrf_potrs_batched(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                       _ptr(B), _ptr(info), _stream(stream))
     _check(st, "bs_potrf_potrs_batched")
@@ -186,7 +236,7 @@ def bs_potrf_potrs_batched(A, B, info, layout: int = COL_MAJOR, fill: int = BS_L
 
 def bs_bdsv_batched(strips, x_padded, info, stream=None) -> None:
     """Block-tridiagonal block-Cholesky solve, in place (see bsolve.h)."""
-    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    batch, nbr, bs = _strips(strips, [("x_padded", x_padded)], info)
     st = lib().bs_bdsv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
                                _ptr(info), _stream(stream))
     _check(st, "bs_bdsv_batched")
@@ -195,7 +245,8 @@ def bs_bdsv_batched(strips, x_padded, info, stream=None) -> None:
 # --------------------------------------------- factor once, solve per right-hand side
 def bs_getrf_batched(A, ipiv, info, layout: int = ROW_MAJOR, stream=None) -> None:
     """LU with partial pivoting alone, in place: A <- L\\U, ipiv, info (see bsolve.h)."""
-    batch, n = A.shape[0], A.shape[1]
+    batch, n, _ = _dense(A, None, layout)
+    _pivots(ipiv, info, batch, n)
     st = lib().bs_getrf_batched(_dtype_code(A), layout, n, batch, _ptr(A), _ptr(ipiv), _ptr(info),
                                 _stream(stream))
     _check(st, "bs_getrf_batched")
@@ -203,8 +254,8 @@ def bs_getrf_batched(A, ipiv, info, layout: int = ROW_MAJOR, stream=None) -> Non
 
 def bs_getrs_batched(LU, ipiv, B, layout: int = ROW_MAJOR, stream=None) -> None:
     """Solve with a getrf factor: B <- X (see bsolve.h)."""
-    batch, n = LU.shape[0], LU.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(LU, B, layout)
+    _pivots(ipiv, None, batch, n)
     st = lib().bs_getrs_batched(_dtype_code(LU), layout, n, nrhs, batch, _ptr(LU), _ptr(ipiv),
                                 _ptr(B), _stream(stream))
     _check(st, "bs_getrs_batched")
@@ -212,7 +263,8 @@ def bs_getrs_batched(LU, ipiv, B, layout: int = ROW_MAJOR, stream=None) -> None:
 
 def bs_potrf_batched(A, info, layout: int = COL_MAJOR, fill: int = BS_LOWER, stream=None) -> None:
     """Cholesky alone, in place: the lower triangle of A <- L, info (see bsolve.h)."""
-    batch, n = A.shape[0], A.shape[1]
+    batch, n, _ = _dense(A, None, layout)
+    _pivots(None, info, batch, n)
     st = lib().bs_potrf_batched(_dtype_code(A), layout, fill, n, batch, _ptr(A), _ptr(info),
                                 _stream(stream))
     _check(st, "bs_potrf_batched")
@@ -220,8 +272,7 @@ def bs_potrf_batched(A, info, layout: int = COL_MAJOR, fill: int = BS_LOWER, str
 
 def bs_potrs_batched(L, B, layout: int = COL_MAJOR, fill: int = BS_LOWER, stream=None) -> None:
     """Solve with a potrf factor: B <- X (see bsolve.h)."""
-    batch, n = L.shape[0], L.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(L, B, layout)
     st = lib().bs_potrs_batched(_dtype_code(L), layout, fill, n, nrhs, batch, _ptr(L), _ptr(B),
                                 _stream(stream))
     _check(st, "bs_potrs_batched")
@@ -229,7 +280,7 @@ def bs_potrs_batched(L, B, layout: int = COL_MAJOR, fill: int = BS_LOWER, stream
 
 def bs_bdsv_factor_batched(strips, info, stream=None) -> None:
     """Block-Cholesky factor sweep alone, in place on the strips (see bsolve.h)."""
-    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    batch, nbr, bs = _strips(strips, [], info)
     st = lib().bs_bdsv_factor_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips),
                                       _ptr(info), _stream(stream))
     _check(st, "bs_bdsv_factor_batched")
@@ -238,7 +289,7 @@ def bs_bdsv_factor_batched(strips, info, stream=None) -> None:
 def bs_bdsv_solve_batched(strips, x_padded, stream=None) -> None:
     """Forward/backward block substitution with factored strips, in place on x (see
     bsolve.h)."""
-    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    batch, nbr, bs = _strips(strips, [("x_padded", x_padded)], None)
     st = lib().bs_bdsv_solve_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips),
                                      _ptr(x_padded), _stream(stream))
     _check(st, "bs_bdsv_solve_batched")
@@ -246,20 +297,31 @@ def bs_bdsv_solve_batched(strips, x_padded, stream=None) -> None:
 
 def bs_bdmv_batched(strips, x_padded, y_padded, stream=None) -> None:
     """Block-tridiagonal matvec: the interior of y_padded <- A x (see bsolve.h)."""
-    batch, nbr, bs = strips.shape[0], strips.shape[1], strips.shape[2]
+    batch, nbr, bs = _strips(strips, [("x_padded", x_padded), ("y_padded", y_padded)], None)
     st = lib().bs_bdmv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
                                _ptr(y_padded), _stream(stream))
     _check(st, "bs_bdmv_batched")
 
 
 # --------------------------------------------------------------- contract variants
-def _il_shape(A, B, layout, interleave, shape):
-    # (batch, n, nrhs): from the tensors' shapes, or, for an interleaved batch, given
+def _il_shape(A, B, ipiv, info, layout, interleave, shape):
+    """(batch, n, nrhs) of a contract-variant call, the operands checked. The plain batched
+    layout: from the tensors' shapes, as the plain calls. Interleaved (interleave = W > 1):
+    given as shape; A, B and ipiv are flat and hold whole blocks, ceil(batch / W) * W
+    systems each; info one entry per system."""
     if interleave > 1:
         if shape is None:
             raise ValueError("an interleaved batch needs shape=(batch, n, nrhs)")
-        return tuple(int(v) for v in shape)
-    return A.shape[0], A.shape[1], (B.shape[2] if layout == ROW_MAJOR else B.shape[1])
+        batch, n, nrhs = (int(v) for v in shape)
+        held = -(-batch // interleave) * interleave
+        _dtype_code(A)
+        _expect(A, "A", A.dtype, held * n * n)
+        _expect(B, "B", A.dtype, held * n * nrhs)
+        _pivots(ipiv, info, batch, n, held)
+        return batch, n, nrhs
+    batch, n, nrhs = _dense(A, B, layout)
+    _pivots(ipiv, info, batch, n)
+    return batch, n, nrhs
 
 
 def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
@@ -270,7 +332,7 @@ def bs_getrf_getrs_batched_ex(A, B, ipiv, info, layout: int = ROW_MAJOR,
     """LU + solve with TDLS threshold pivoting, the RUDA status contract, TDLS's
     row-major reading (factor of A^T and the mirror solve), or an interleaved batched
     layout (A, B, ipiv flat; shape=(batch, n, nrhs)), or RUDA's max-abs scaling."""
-    batch, n, nrhs = _il_shape(A, B, layout, interleave, shape)
+    batch, n, nrhs = _il_shape(A, B, ipiv, info, layout, interleave, shape)
     opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor),
                    int(interleave), int(scaling))
     st = lib().bs_getrf_getrs_batched_ex(_dtype_code(A), layout, n, nrhs, batch, _ptr(A), _ptr(B),
@@ -284,7 +346,7 @@ def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = B
                               shape=None, stream=None) -> None:
     """Cholesky + solve under the RUDA status contract, or on an interleaved batched
     layout (A, B flat; shape=(batch, n, nrhs))."""
-    batch, n, nrhs = _il_shape(A, B, layout, interleave, shape)
+    batch, n, nrhs = _il_shape(A, B, None, info, layout, interleave, shape)
     opts = Options(1.0, int(status_contract), 0, int(interleave), 0)
     st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                          _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
@@ -329,8 +391,8 @@ def bdsv_host_plan(dtype_code: int, nbr: int, bsz: int, chunk: int, streams=None
 def bs_getrf_getrs_batched_host(A, B, ipiv, info, layout: int = ROW_MAJOR, chunk: int = 8192,
                                 plan: HostPlan | None = None, sync: bool = True) -> HostPlan:
     """LU + solve on host tensors, in place, copied in and out by chunks on two streams."""
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(A, B, layout)
+    _pivots(ipiv, info, batch, n)
     plan = plan or getrf_getrs_host_plan(_dtype_code(A), n, nrhs, chunk)
     st = lib().bs_getrf_getrs_batched_host(
         _dtype_code(A), layout, n, nrhs, batch, _host_ptr(A), _host_ptr(B), _host_ptr(ipiv),
@@ -346,8 +408,8 @@ def bs_potrf_potrs_batched_host(A, B, info, layout: int = COL_MAJOR, fill: int =
                                 chunk: int = 8192, plan: HostPlan | None = None,
                                 sync: bool = True) -> HostPlan:
     """Cholesky + solve on host tensors, in place, by chunks on two streams."""
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(A, B, layout)
+    _pivots(None, info, batch, n)
     plan = plan or potrf_potrs_host_plan(_dtype_code(A), n, nrhs, chunk)
     st = lib().bs_potrf_potrs_batched_host(
         _dtype_code(A), layout, fill, n, nrhs, batch, _host_ptr(A), _host_ptr(B),
@@ -362,7 +424,7 @@ def bs_potrf_potrs_batched_host(A, B, info, layout: int = COL_MAJOR, fill: int =
 def bs_bdsv_batched_host(strips, x_padded, info, chunk: int = 2048,
                          plan: HostPlan | None = None, sync: bool = True) -> HostPlan:
     """Block-tridiagonal solve on host tensors, in place, by chunks on two streams."""
-    batch, nbr, bsz = strips.shape[0], strips.shape[1], strips.shape[2]
+    batch, nbr, bsz = _strips(strips, [("x_padded", x_padded)], info)
     plan = plan or bdsv_host_plan(_dtype_code(strips), nbr, bsz, chunk)
     st = lib().bs_bdsv_batched_host(
         _dtype_code(strips), nbr, bsz, batch, _host_ptr(strips), _host_ptr(x_padded),
@@ -380,8 +442,8 @@ def bs_getrf_getrs_batched_host_static(A, B, ipiv, info, layout: int = ROW_MAJOR
     """bs_getrf_getrs_batched_host on the library's static device scratch (no workspace
     argument; see bsolve.h for the one-call-at-a-time rule). Returns the two streams."""
     import torch
-    batch, n = A.shape[0], A.shape[1]
-    nrhs = B.shape[2] if layout == ROW_MAJOR else B.shape[1]
+    batch, n, nrhs = _dense(A, B, layout)
+    _pivots(ipiv, info, batch, n)
     streams = tuple(streams) if streams else (torch.cuda.Stream(), torch.cuda.Stream())
     st = lib().bs_getrf_getrs_batched_host_static(
         _dtype_code(A), layout, n, nrhs, batch, _host_ptr(A), _host_ptr(B), _host_ptr(ipiv),

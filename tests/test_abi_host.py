@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import dense_linear_solvers_gb300 as bs
@@ -61,6 +62,7 @@ def test_supported_queries(lib):
     assert lib.bs_bdsv_supported(bs.BS_FP64, 32, 9) == 0
 
 
+COL = bs.BS_COL_MAJOR
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below returns early
 
 
@@ -265,3 +267,111 @@ def test_aliased_operands_are_rejected(lib):
     assert lib.bs_getrf_getrs_batched_host(bs.BS_FP32, 0, 16, 4, 5, A, A + 1024, A + 0x100000,
                                            A + 0x200000, A + 0x1000000, W, 8, None,
                                            None) == bs.BS_ERR_INVALID_ARG
+
+
+def _cpu(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def _refused_as_host(fn, *args, **kw):
+    """The operand checks pass; the call then stops at the device check of the first
+    pointer (these are CPU tensors), before anything reaches the library."""
+    with pytest.raises(ValueError, match="device tensors"):
+        fn(*args, **kw)
+
+
+def test_binding_operand_checks_accept_the_workloads():
+    """Every workload's operands, shaped as the tests and the benchmark pass them, get
+    through the binding's dtype / shape checks of every wrapper."""
+    import torch
+    from gen import workloads as W
+    for name, w in W.WORKLOADS.items():
+        d = W.make(name, 37)
+        if w.op == "bdsv":
+            S, X = _cpu(d["strips"]), _cpu(d["x"])
+            info = torch.zeros(37, dtype=torch.int32)
+            _refused_as_host(bs.bs_bdsv_batched, S, X, info)
+            _refused_as_host(bs.bs_bdsv_factor_batched, S, info)
+            _refused_as_host(bs.bs_bdsv_solve_batched, S, X)
+            _refused_as_host(bs.bs_bdmv_batched, S, X, X.clone())
+            continue
+        A, B = _cpu(d["A"]), _cpu(d["B"])
+        n = A.shape[1]
+        ipiv = torch.zeros((37, n), dtype=torch.int32)
+        info = torch.zeros(37, dtype=torch.int32)
+        if w.op == "getrf_getrs":
+            _refused_as_host(bs.bs_getrf_getrs_batched, A, B, ipiv, info, w.layout)
+            _refused_as_host(bs.bs_getrf_batched, A, ipiv, info, w.layout)
+            _refused_as_host(bs.bs_getrs_batched, A, ipiv, B, w.layout)
+            _refused_as_host(bs.bs_getrf_getrs_batched_ex, A, B, ipiv, info, w.layout, 0.5)
+            for wd in (4, 32, 40):   # interleaved: flat operands holding whole blocks
+                Ai, Bi = _cpu(W.interleave(d["A"], wd)), _cpu(W.interleave(d["B"], wd))
+                ip = torch.zeros(Ai.numel() // n, dtype=torch.int32)
+                _refused_as_host(bs.bs_getrf_getrs_batched_ex, Ai, Bi, ip, info, w.layout,
+                                 interleave=wd, shape=(37, n, w.nrhs))
+        else:
+            _refused_as_host(bs.bs_potrf_potrs_batched, A, B, info, w.layout)
+            _refused_as_host(bs.bs_potrf_batched, A, info, w.layout)
+            _refused_as_host(bs.bs_potrs_batched, A, B, w.layout)
+            Ai, Bi = _cpu(W.interleave(d["A"], 37)), _cpu(W.interleave(d["B"], 37))
+            _refused_as_host(bs.bs_potrf_potrs_batched_ex, Ai, Bi, info, w.layout,
+                             interleave=37, shape=(37, n, w.nrhs))
+
+
+def test_binding_operand_checks_reject_mismatches():
+    """A tensor of another dtype or size than the call's shape implies is refused with a
+    TypeError / ValueError naming the operand, before any pointer reaches the library
+    (which would otherwise read it as the expected type and size)."""
+    import torch
+    A = torch.zeros((5, 16, 16))
+    B = torch.zeros((5, 16, 4))
+    ipiv = torch.zeros((5, 16), dtype=torch.int32)
+    info = torch.zeros(5, dtype=torch.int32)
+    f = bs.bs_getrf_getrs_batched
+    with pytest.raises(TypeError, match="B: dtype"):
+        f(A, B.double(), ipiv, info)
+    with pytest.raises(TypeError, match="ipiv: dtype"):
+        f(A, B, ipiv.long(), info)
+    with pytest.raises(TypeError, match="info: dtype"):
+        f(A, B, ipiv, info.float())
+    with pytest.raises(ValueError, match="info: 4 elements"):
+        f(A, B, ipiv, info[:4])
+    with pytest.raises(ValueError, match="ipiv: 75 elements"):
+        f(A, B, ipiv[:, :15].contiguous(), info)
+    with pytest.raises(ValueError, match="A: shape"):
+        f(A[:, :, :15].contiguous(), B, ipiv, info)
+    with pytest.raises(ValueError, match="B: shape"):
+        f(A, torch.zeros((4, 16, 4)), ipiv, info)
+    with pytest.raises(ValueError, match="B: shape"):          # column-major B is (batch, nrhs, n)
+        f(A, B, ipiv, info, COL)
+    with pytest.raises(TypeError, match="unsupported dtype"):
+        f(A.half(), B.half(), ipiv, info)
+    with pytest.raises(ValueError, match="B: shape"):
+        bs.bs_potrs_batched(A.double(), torch.zeros((5, 16), dtype=torch.float64))
+    S = torch.zeros((3, 32, 8, 24), dtype=torch.float64)
+    X = torch.zeros((3, 34 * 8), dtype=torch.float64)
+    binfo = torch.zeros(3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="strips: shape"):
+        bs.bs_bdsv_batched(S[..., :16].contiguous(), X, binfo)
+    with pytest.raises(ValueError, match="x_padded: 264 elements"):
+        bs.bs_bdsv_batched(S, X[:, :88].contiguous(), binfo)
+    with pytest.raises(TypeError, match="y_padded: dtype"):
+        bs.bs_bdmv_batched(S, X, X.float())
+    # interleaved: ipiv and B hold whole blocks (5 systems in blocks of 4: 8 systems' room)
+    Ai, Bi = torch.zeros(8 * 256), torch.zeros(8 * 64)
+    with pytest.raises(ValueError, match="ipiv: 80 elements"):
+        bs.bs_getrf_getrs_batched_ex(Ai, Bi, torch.zeros(80, dtype=torch.int32), info,
+                                     interleave=4, shape=(5, 16, 4))
+    with pytest.raises(ValueError, match="B: 320 elements"):
+        bs.bs_getrf_getrs_batched_ex(Ai, Bi[:320].contiguous(),
+                                     torch.zeros(128, dtype=torch.int32), info,
+                                     interleave=4, shape=(5, 16, 4))
+    # host-resident calls check the same before planning anything
+    with pytest.raises(TypeError, match="B: dtype"):
+        bs.bs_getrf_getrs_batched_host(A, B.double(), ipiv, info)
+    with pytest.raises(ValueError, match="info: 4 elements"):
+        bs.bs_potrf_potrs_batched_host(A.double(), torch.zeros((5, 4, 16), dtype=torch.float64),
+                                       info[:4], COL)
+    with pytest.raises(ValueError, match="x_padded"):
+        bs.bs_bdsv_batched_host(S, X[:2].contiguous(), binfo)
