@@ -239,6 +239,9 @@ class SplitProblem(Problem):
             self.inputs = [a, b]
         elif op in ("getrf_getrs_il", "potrf_potrs_il"):   # interleaved batched layout
             self.ilv = IL_WIDTH[name] or self.batch
+            if self.batch % self.ilv:
+                raise ValueError(f"{name}: batch {self.batch} is not a whole number of blocks "
+                                 f"of {self.ilv} systems")
             self.inputs = [interleave_device(a, self.ilv), interleave_device(b, self.ilv)]
             self.ipiv = self.ipiv.reshape(-1) if self.ipiv is not None else None
         else:   # the factor calls mutate A only
