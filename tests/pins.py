@@ -792,9 +792,38 @@ def pin_bdmv_inverts_bdsv(orc):
     assert np.all(np.abs(Y[:, bs:bs + N] - b).max(axis=1) <= 8 * N * eps_of(np.float64) * scale)
 
 
+def pin_lu_nan_candidates(orc):
+    """NaN in the pivot column, worked by hand under the search's strict "larger magnitude"
+    test from the row in place (BLAS i_amax's comparison): a NaN below never displaces the
+    current best; a NaN in the row in place is never displaced, becomes the pivot and
+    makes the step singular (!(|p| >= floor)), with a reciprocal of 1.
+
+    * [[1, 0], [NaN, 1]]: row 1 stays (NaN > 1 is false); the multiplier NaN * 1 turns the
+      trailing entry into NaN, so step 2 is singular: ipiv = [1, 2], info = 2.
+    * [[NaN, 0], [2, 1]]: the NaN in place stays (2 > NaN is false): info = 1, and with a
+      reciprocal of 1 the multiplier is 2 exactly and the trailing entry 1 - 2 * 0 = 1.
+    * [[1, 0, 0], [NaN, 1, 0], [2, 0, 1]]: the finite 2 wins step 1 over the NaN below
+      (ipiv[0] = 3); the NaN row then sits in place at step 2: ipiv = [3, 2, 3], info = 2.
+    Failed systems return X = 0; both storage orders and both precisions agree."""
+    nan = np.nan
+    for dt in (np.float64, np.float32):
+        for layout in (ROW_MAJOR, COL_MAJOR):
+            b2 = np.ones((1, 2, 1), dt)
+            LU, X, ipiv, info, _ = _lu(orc, np.array([[[1, 0], [nan, 1]]], dt), b2, layout)
+            assert list(ipiv[0]) == [1, 2] and info[0] == 2 and np.all(X == 0)
+            assert LU[0, 0, 0] == 1 and LU[0, 0, 1] == 0 and np.isnan(LU[0, 1, 0])
+            LU, X, ipiv, info, _ = _lu(orc, np.array([[[nan, 0], [2, 1]]], dt), b2, layout)
+            assert list(ipiv[0]) == [1, 2] and info[0] == 1 and np.all(X == 0)
+            assert np.isnan(LU[0, 0, 0]) and LU[0, 1, 0] == 2 and LU[0, 1, 1] == 1
+            A3 = np.array([[[1, 0, 0], [nan, 1, 0], [2, 0, 1]]], dt)
+            LU, X, ipiv, info, _ = _lu(orc, A3, np.ones((1, 3, 1), dt), layout)
+            assert list(ipiv[0]) == [3, 2, 3] and info[0] == 2 and np.all(X == 0)
+            assert list(LU[0, 0]) == [2, 0, 1] and LU[0, 2, 0] == dt(0.5)
+
+
 LU_PINS = [pin_lu_3x3_hand_worked, pin_lu_2x2_closed_form, pin_lu_cramer_bruteforce,
            pin_lu_reconstruction, pin_lu_matches_lapack, pin_lu_info_contract,
-           pin_lu_layout_invariance, pin_lu_near_tie_flag]
+           pin_lu_layout_invariance, pin_lu_near_tie_flag, pin_lu_nan_candidates]
 CHOL_PINS = [pin_chol_hand_worked, pin_chol_2x2_closed_form,
              pin_chol_reconstruction_and_lapack, pin_chol_info_contract, pin_chol_upper_fill]
 BDSV_PINS = [pin_bdsv_dense_equivalence, pin_bdsv_single_block_is_potrf,

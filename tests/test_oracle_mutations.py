@@ -21,6 +21,10 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.cpp")
 
 MUTATIONS = [
     ("lu_tie_rule_last_max", "      if (v > best) {", "      if (v >= best) {"),
+    ("lu_nan_candidate_wins", "      if (v > best) {", "      if (!(v <= best)) {"),
+    ("lu_nan_in_place_skipped",
+     "    T best = std::fabs(a(k, k));\n    for (int i = k + 1; i < n; ++i) {",
+     "    T best = T(-1);\n    for (int i = k; i < n; ++i) {"),
     ("lu_search_skips_last_row",
      "    for (int i = k + 1; i < n; ++i) {\n      T v = std::fabs(a(i, k));\n      if (v > best)",
      "    for (int i = k + 1; i < n - 1; ++i) {\n      T v = std::fabs(a(i, k));\n      if (v > best)"),
