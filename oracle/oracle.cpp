@@ -211,7 +211,8 @@ void getrf_getrs_one(int layout, int n, int nrhs, T* A, T* B, int32_t* ipiv, int
 // getrs: solve with a stored factor ([TDLS] separate substitution; [GLASS] "factor once,
 // call this per right-hand side"). LU holds L\U as left by getrf_getrs_one (nrhs = 0 gives
 // getrf), ipiv the 1-based swap sequence. B <- X:
-//   1. the interchanges in step order: rows k and ipiv[k]-1 of B for k = 0..n-1;
+//   1. the interchanges in step order: rows k and ipiv[k]-1 of B for k = 0..n-1 (an
+//      entry outside 1..n swaps nothing: the solve steps take no status to report it);
 //   2. L y = P b with unit L, column by column: b_i -= l_ik b_k for i > k (each b_i takes
 //      its updates in increasing k, as in the fused sweep);
 //   3. U x = y as in getrf_getrs_one, a pivot reciprocal of 1 for a singular u_kk.
@@ -224,7 +225,7 @@ void getrs_one(int layout, int n, int nrhs, const T* LU, const int32_t* ipiv, T*
   auto b = [&](int r, int c) -> T& { return B[at(layout, n, nrhs, r, c)]; };
   for (int k = 0; k < n; ++k) {
     const int p = ipiv[k] - 1;
-    if (p != k)
+    if (p != k && p >= 0 && p < n)
       for (int c = 0; c < nrhs; ++c) {
         T t = b(k, c);
         b(k, c) = b(p, c);
@@ -497,7 +498,7 @@ void getrs_mirror_one(int b_layout, int n, int nrhs, const T* S, const int32_t* 
       for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c), b(i, c));
   for (int k = n - 1; k >= 0; --k) {  // x = P^T w: step k's interchange undone
     const int q = ipiv[k] - 1;
-    if (q == k) continue;
+    if (q == k || q < 0 || q >= n) continue;   // out of range: no interchange
     for (int c = 0; c < nrhs; ++c) std::swap(b(k, c), b(q, c));
   }
 }

@@ -635,7 +635,7 @@ def pin_getrs_composition(orc):
 
 def pin_getrs_permutation_only(orc):
     """With L = U = I the solve is the swap sequence alone: row k of B exchanged with row
-    ipiv[k]-1 for k = 0..n-1, in that order (exact)."""
+    ipiv[k]-1 for k = 0..n-1, in that order (exact); an entry outside 1..n swaps nothing."""
     rng = _rng(42)
     n, nrhs = 6, 3
     LU = np.broadcast_to(np.eye(n), (5, n, n)).copy()
@@ -648,6 +648,14 @@ def pin_getrs_permutation_only(orc):
             p = ipiv[s, k] - 1
             want[[k, p]] = want[[p, k]]
         assert np.array_equal(X[s], want)
+    # entries outside 1..n swap nothing (the solve reports no status): zero, negative and
+    # past-the-end entries leave their rows where they are, in-range ones still swap
+    bad = np.array([[0, 3, 7, -2, 6, 2 ** 31 - 1]], np.int32)
+    X = orc.getrs(np.eye(n)[None].copy(), bad, B[:1], ROW_MAJOR)
+    want = B[0].copy()
+    want[[1, 2]] = want[[2, 1]]             # k = 1: row 3
+    want[[4, 5]] = want[[5, 4]]             # k = 4: row 6
+    assert np.array_equal(X[0], want)
 
 
 def pin_getrs_cramer(orc):

@@ -74,8 +74,11 @@ MUTATIONS = [
      "s = std::fma(-blk(k, MAIN, m, j), x[k * bs + m], s);",
      "s = std::fma(-blk(k, MAIN, j, m), x[k * bs + m], s);"),
     ("bdsv_info_local_index", "inf = k * bs + c + 1;", "inf = c + 1;"),
-    ("getrs_swaps_skipped", "    if (p != k)\n      for (int c = 0; c < nrhs; ++c) {",
+    ("getrs_swaps_skipped", "    if (p != k && p >= 0 && p < n)\n      for (int c = 0; c < nrhs; ++c) {",
      "    if (false)\n      for (int c = 0; c < nrhs; ++c) {"),
+    ("getrs_last_row_never_swapped",
+     "    if (p != k && p >= 0 && p < n)\n      for (int c = 0; c < nrhs; ++c) {",
+     "    if (p != k && p >= 0 && p < n - 1)\n      for (int c = 0; c < nrhs; ++c) {"),
     ("getrs_swaps_reverse_order",
      "  for (int k = 0; k < n; ++k) {\n    const int p = ipiv[k] - 1;",
      "  for (int k = n - 1; k >= 0; --k) {\n    const int p = ipiv[k] - 1;"),
@@ -115,7 +118,7 @@ MUTATIONS = [
     ("mirror_swaps_in_step_order",
      "  for (int k = n - 1; k >= 0; --k) {  // x = P^T w",
      "  for (int k = 0; k < n; ++k) {  // x = P^T w"),
-    ("mirror_swaps_skipped", "    if (q == k) continue;", "    continue;"),
+    ("mirror_swaps_skipped", "    if (q == k || q < 0 || q >= n) continue;", "    continue;"),
     ("mirror_backward_scaled",
      "      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c), b(i, c));",
      "      for (int i = 0; i < k; ++i) b(i, c) = std::fma(-s_(k, i), b(k, c) / s_(k, k), b(i, c));"),
