@@ -403,11 +403,30 @@ def cpu_baseline(name: str, batch: int | None, seconds: float) -> dict:
         el = time.time() - t0
         if el >= seconds:
             break
-    return {"value": round(reps * d["batch"] / el, 1), "unit": "systems/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"{reps} passes over the {d['batch']}-system batch of {name} "
-                      f"({el:.1f} s wall, oracle built with g++ -O2, systems split over "
-                      f"{cores} threads)"}
+    out = {"value": round(reps * d["batch"] / el, 1), "unit": "systems/s", "cores": cores,
+           "kind": "oracle",
+           "sample": f"{reps} passes over the {d['batch']}-system batch of {name} "
+                     f"({el:.1f} s wall, oracle built with g++ -O2, systems split over "
+                     f"{cores} threads)"}
+    # the same oracle on one thread, over the first systems of the batch (a few seconds)
+    sub = min(d["batch"], 4096)
+    arrays = (d["strips"][:sub], d["x"][:sub]) if w.op == "bdsv" else (d["A"][:sub], d["B"][:sub])
+    reps1, t1 = 0, time.time()
+    while True:
+        if w.op == "getrf_getrs":
+            oracle.getrf_getrs(*arrays, w.layout, nthreads=1)
+        elif w.op == "potrf_potrs":
+            oracle.potrf_potrs(*arrays, w.layout, nthreads=1)
+        else:
+            oracle.bdsv(*arrays, nthreads=1)
+        reps1 += 1
+        el1 = time.time() - t1
+        if el1 >= min(3.0, seconds / 3):
+            break
+    out["one_core"] = {"value": round(reps1 * sub / el1, 1), "unit": "systems/s",
+                       "sample": f"{reps1} passes over the first {sub} systems on 1 thread "
+                                 f"({el1:.1f} s wall)"}
+    return out
 
 
 class Ranks:

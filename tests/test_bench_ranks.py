@@ -82,3 +82,10 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["config"]["workload"].startswith("lu_f32_n16")
     assert d["e2e"]["value"] == d["value"] and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+
+
+def test_cpu_baseline_reports_all_cores_and_one_core():
+    r = bench.cpu_baseline("lu_f64_n8", 256, 0.3)
+    assert r["kind"] == "oracle" and r["unit"] == "systems/s" and r["value"] > 0
+    assert r["cores"] >= 1 and "256-system batch" in r["sample"]
+    assert r["one_core"]["value"] > 0 and "on 1 thread" in r["one_core"]["sample"]
