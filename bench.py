@@ -133,6 +133,44 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def verify_sample(d: dict, fetch, k: int = 256) -> dict:
+    """Check after timing: k systems spread over the batch, recomputed by the CPU oracle
+    from the pristine inputs, against the outputs of the last timed step, bit for bit.
+    fetch(idx) returns those systems' outputs as NumPy arrays in the call's order: (A, B,
+    ipiv, info) for LU, (A, B, info) for Cholesky, (strips, x, info) for bdsv. LU systems
+    whose pivot search met a near tie are counted apart (a legitimate rounding may pick
+    the other row), and a failed system's factor is unspecified: its X and info are
+    compared, its factor not."""
+    import oracle
+    w = d["workload"]
+    idx = np.unique(np.linspace(0, d["batch"] - 1, min(k, d["batch"])).astype(np.int64))
+    same = lambda x, y: np.array_equal(x, y, equal_nan=True)  # noqa: E731
+    exempt = 0
+    if w.op == "getrf_getrs":
+        LU, X, ipiv, info, tie = oracle.getrf_getrs(d["A"][idx], d["B"][idx], w.layout)
+        got = fetch(idx)
+        ok_all = []
+        for j in range(len(idx)):
+            if tie[j] >= 0:
+                exempt += 1
+                continue
+            ok = same(got[1][j], X[j]) and same(got[2][j], ipiv[j]) and got[3][j] == info[j]
+            if info[j] == 0:
+                ok = ok and same(got[0][j], LU[j])
+            ok_all.append(ok)
+    else:
+        if w.op == "potrf_potrs":
+            F, X, info = oracle.potrf_potrs(d["A"][idx], d["B"][idx], w.layout)
+        else:
+            F, X, info = oracle.bdsv(d["strips"][idx], d["x"][idx])
+        got = fetch(idx)
+        ok_all = [same(got[1][j], X[j]) and got[2][j] == info[j]
+                  and (info[j] != 0 or same(got[0][j], F[j])) for j in range(len(idx))]
+    return {"sampled_systems": int(len(idx)), "bit_identical": int(sum(ok_all)),
+            "near_tie_exempt": exempt,
+            "mismatches": int(len(ok_all) - sum(ok_all))}
+
+
 # ------------------------------------------------------------------ GPU arm
 class Problem:
     """Device buffers of one workload, a pristine copy and the solver call."""
@@ -172,6 +210,13 @@ class Problem:
     def restore(self):
         for dst, src in zip(self.work, self.inputs):
             dst.copy_(src)
+
+    def outputs(self, idx):
+        """Systems idx of the last call's buffers, gathered on the device and copied to
+        the host, in the order verify_sample takes."""
+        sel = self.torch.as_tensor(idx, dtype=self.torch.int64, device=self.device)
+        outs = list(self.work) + ([self.ipiv] if self.ipiv is not None else []) + [self.info]
+        return [x.index_select(0, sel).cpu().numpy() for x in outs]
 
 
 # The factor / solve halves and the block-tridiagonal matvec, each measured on the inputs of
@@ -491,6 +536,10 @@ def run_native(args) -> None:
     ranks.barrier()
     clocks = sampler.stop(local)
     ms = statistics.fmean(times)
+    try:   # the last timed step's outputs against the oracle, on a sample of systems
+        verified = verify_sample(prob.d, prob.outputs)
+    except Exception as e:  # reported in the line rather than lost with it
+        verified = {"error": repr(e)[:200]}
     ranks.barrier()                   # the end-to-end steps start together on every rank
     e2e_times, h2d, d2h = time_e2e(prob, max(3, min(args.steps, 20)), 2, args.e2e_chunk)
     ranks.barrier()
@@ -531,6 +580,7 @@ def run_native(args) -> None:
                         f"{args.e2e_chunk} systems on two streams (copies overlap solves)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
+        "verified": verified,
     }
     line["cpu_baseline"] = cpu_baseline(args.workload, args.batch, args.cpu_seconds)
     if not args.headline_only:

@@ -89,3 +89,53 @@ def test_cpu_baseline_reports_all_cores_and_one_core():
     assert r["kind"] == "oracle" and r["unit"] == "systems/s" and r["value"] > 0
     assert r["cores"] >= 1 and "256-system batch" in r["sample"]
     assert r["one_core"]["value"] > 0 and "on 1 thread" in r["one_core"]["sample"]
+
+
+def _oracle_outputs(name, batch):
+    import oracle
+    from gen import workloads as W
+    d = W.make(name, batch)
+    w = d["workload"]
+    if w.op == "getrf_getrs":
+        LU, X, ipiv, info, _ = oracle.getrf_getrs(d["A"], d["B"], w.layout)
+        return d, [LU, X, ipiv, info]
+    if w.op == "potrf_potrs":
+        return d, list(oracle.potrf_potrs(d["A"], d["B"], w.layout))
+    return d, list(oracle.bdsv(d["strips"], d["x"]))
+
+
+@pytest.mark.parametrize("name,batch", [("lu_f64_n8", 1024), ("lu_f32_n16", 700),
+                                        ("chol_f64_n32", 500), ("bdsv_f64_32x8", 40)])
+def test_post_timing_check_accepts_the_oracle_and_flags_one_ulp(name, batch):
+    """The bench's check after timing: outputs equal to the oracle's pass (planted
+    failures included); one output one ulp off in one sampled system is one mismatch."""
+    import numpy as np
+    d, outs = _oracle_outputs(name, batch)
+    fetch = lambda idx: [o[idx] for o in outs]  # noqa: E731
+    k = min(64, batch)
+    r = bench.verify_sample(d, fetch, k=64)
+    assert r["mismatches"] == 0 and r["sampled_systems"] == k
+    assert r["bit_identical"] + r["near_tie_exempt"] == k
+    idx = np.unique(np.linspace(0, batch - 1, k).astype(np.int64))
+    j = next(int(i) for i in idx if outs[-1][i] == 0)          # a system that did not fail
+    X = outs[1].copy()
+    flat = X[j].reshape(-1)
+    flat[0] = np.nextafter(flat[0], np.inf)
+    bad = [outs[0], X] + outs[2:]
+    r = bench.verify_sample(d, lambda ix: [o[ix] for o in bad], k=64)
+    assert r["mismatches"] == 1 or (r["near_tie_exempt"] > 0 and r["mismatches"] <= 1)
+
+
+def test_problem_outputs_gathers_the_sampled_systems():
+    """Problem.outputs gathers systems idx of every output buffer (here CPU tensors
+    holding the oracle's results) in the order the check takes."""
+    import torch
+    d, outs = _oracle_outputs("lu_f64_n8", 1024)
+    prob = bench.Problem("lu_f64_n8", None, torch.device("cpu"))
+    for dst, src in zip(prob.work + [prob.ipiv, prob.info], outs):
+        dst.copy_(torch.from_numpy(src))
+    r = bench.verify_sample(prob.d, prob.outputs, k=256)
+    assert r == {"sampled_systems": 256, "bit_identical": 256 - r["near_tie_exempt"],
+                 "near_tie_exempt": r["near_tie_exempt"], "mismatches": 0}
+    prob.info[512] = 7
+    assert bench.verify_sample(prob.d, prob.outputs, k=1024)["mismatches"] == 1
