@@ -11,7 +11,10 @@ both happen outside the CUDA events, which bracket the solver launch alone on th
 launching stream. ``value`` = systems per second over all ranks (weak scaling: every
 rank solves its own batch). ``e2e`` times the same call with pinned host buffers, the
 host-to-device copy of A and B and the device-to-host copy of every output inside the
-timed region. ``cpu_baseline`` is the CPU oracle on this host's cores.
+timed region (the host-resident call: chunks copied in, solved and copied out on two
+streams). ``cpu_baseline`` is the CPU oracle on this host's cores, with a one-thread
+figure beside it. ``verified``: after timing, 256 systems of the last timed step are
+compared bit for bit with the oracle on the same inputs.
 
 ``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
 """
