@@ -139,3 +139,16 @@ def test_problem_outputs_gathers_the_sampled_systems():
                  "near_tie_exempt": r["near_tie_exempt"], "mismatches": 0}
     prob.info[512] = 7
     assert bench.verify_sample(prob.d, prob.outputs, k=1024)["mismatches"] == 1
+
+
+def test_bench_interleave_matches_the_generator():
+    """bench.interleave_device (torch, on the timed device) lays systems out exactly as
+    gen.workloads.interleave does for the parity tests (whole blocks)."""
+    import numpy as np
+    import torch
+    from gen import workloads as W
+    rng = np.random.default_rng(5)
+    S = rng.standard_normal((96, 16, 4)).astype(np.float32)
+    for w in (1, 32, 96):
+        got = bench.interleave_device(torch.from_numpy(S), w).numpy()
+        assert np.array_equal(got, W.interleave(S, w)), w
