@@ -6,9 +6,9 @@
  * when a factor and a solve run apart: a fused call with more than 8 right-hand sides,
  * the row-major reading of the _ex call) on the caller's CUDA stream. All matrix and
  * vector pointers are DEVICE pointers owned by the caller, except those of the
- * *_batched_host calls (host arrays, copied in and out by chunks on two streams); the
- * library allocates no memory, keeps no state between calls and never synchronizes the
- * host. Results are valid once the stream has reached the launch; the per-system `info`
+ * *_batched_host calls (host arrays, copied in and out by chunks on two streams); no
+ * call allocates memory (the one device scratch, of the _static host call, is placed when
+ * the library loads), keeps state for a later call or synchronizes the host. Results are valid once the stream has reached the launch; the per-system `info`
  * array is read back by the caller when it needs it. Calls may run concurrently on
  * different streams and may be captured into CUDA graphs.
  *
