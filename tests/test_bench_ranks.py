@@ -152,3 +152,19 @@ def test_bench_interleave_matches_the_generator():
     for w in (1, 32, 96):
         got = bench.interleave_device(torch.from_numpy(S), w).numpy()
         assert np.array_equal(got, W.interleave(S, w)), w
+
+
+def test_traffic_records_point_at_committed_summaries():
+    """Every benchmarked row names the kernel sources its traffic record is keyed on, and
+    each record in profiles/ncu_traffic.json points at a committed ncu summary."""
+    rows = set(bench.KERNEL_SOURCES)
+    assert set(bench.W.WORKLOADS) <= rows and set(bench.NEXT_ROWS) <= rows
+    for name, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, "dense_linear_solvers_gb300", "csrc", f)), f
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as fh:
+        records = json.load(fh)
+    for name, rec in records.items():
+        assert name in rows, name
+        assert os.path.exists(os.path.join(ROOT, rec["profile"])), rec["profile"]
+        assert rec["dram_bytes_per_launch"] > 0 and rec["captured_batch"] > 0
