@@ -12,9 +12,9 @@ launching stream. ``value`` = systems per second over all ranks (weak scaling: e
 rank solves its own batch). ``e2e`` times the same call with pinned host buffers, the
 host-to-device copy of A and B and the device-to-host copy of every output inside the
 timed region (the host-resident call: chunks copied in, solved and copied out on two
-streams). ``cpu_baseline`` is the CPU oracle on this host's cores, with a one-thread
-figure beside it. ``verified``: after timing, 256 systems of the last timed step are
-compared bit for bit with the oracle on the same inputs.
+streams). ``cpu_baseline`` (N = 1) is the CPU oracle on this host's cores, with a
+one-thread figure beside it; its last pass also gives ``verified``: 256 systems of the
+last timed step compared bit for bit with the oracle's results on the same inputs.
 
 ``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
 """
@@ -136,21 +136,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def verify_sample(d: dict, fetch, k: int = 256) -> dict:
-    """Check after timing: k systems spread over the batch, recomputed by the CPU oracle
-    from the pristine inputs, against the outputs of the last timed step, bit for bit.
-    fetch(idx) returns those systems' outputs as NumPy arrays in the call's order: (A, B,
-    ipiv, info) for LU, (A, B, info) for Cholesky, (strips, x, info) for bdsv. LU systems
-    whose pivot search met a near tie are counted apart (a legitimate rounding may pick
-    the other row), and a failed system's factor is unspecified: its X and info are
-    compared, its factor not."""
-    import oracle
+def verify_sample(d: dict, fetch, ref, k: int = 256) -> dict:
+    """Check after timing: k systems spread over the batch, the outputs of the last timed
+    step against the CPU oracle's on the same pristine inputs, bit for bit. ref holds the
+    oracle's outputs for the whole batch as it returns them: (LU, X, ipiv, info, near-tie
+    step) for LU, (factor, X, info) for Cholesky and bdsv. fetch(idx) returns the timed
+    outputs of systems idx as NumPy arrays in the call's order: (A, B, ipiv, info) for LU,
+    (A, B, info) for Cholesky, (strips, x, info) for bdsv. LU systems whose pivot search
+    met a near tie are counted apart (a legitimate rounding may pick the other row), and a
+    failed system's factor is unspecified: its X and info are compared, its factor not."""
     w = d["workload"]
     idx = np.unique(np.linspace(0, d["batch"] - 1, min(k, d["batch"])).astype(np.int64))
     same = lambda x, y: np.array_equal(x, y, equal_nan=True)  # noqa: E731
     exempt = 0
     if w.op == "getrf_getrs":
-        LU, X, ipiv, info, tie = oracle.getrf_getrs(d["A"][idx], d["B"][idx], w.layout)
+        LU, X, ipiv, info, tie = (r[idx] for r in ref)
         got = fetch(idx)
         ok_all = []
         for j in range(len(idx)):
@@ -162,10 +162,7 @@ def verify_sample(d: dict, fetch, k: int = 256) -> dict:
                 ok = ok and same(got[0][j], LU[j])
             ok_all.append(ok)
     else:
-        if w.op == "potrf_potrs":
-            F, X, info = oracle.potrf_potrs(d["A"][idx], d["B"][idx], w.layout)
-        else:
-            F, X, info = oracle.bdsv(d["strips"][idx], d["x"][idx])
+        F, X, info = (r[idx] for r in ref)
         got = fetch(idx)
         ok_all = [same(got[1][j], X[j]) and got[2][j] == info[j]
                   and (info[j] != 0 or same(got[0][j], F[j])) for j in range(len(idx))]
@@ -434,7 +431,11 @@ def roofline(prob: Problem, ms: float, peaks: dict, name: str) -> dict:
             "achieved_gbs": round(bytes_launch / (ms * 1e-3) / 1e9, 1)}
 
 
-def cpu_baseline(name: str, batch: int | None, seconds: float) -> dict:
+def cpu_baseline(name: str, batch: int | None, seconds: float, fetch=None):
+    """The CPU oracle timed on this host's cores over the workload's batch, and on one
+    thread over its first systems. With fetch (the timed GPU outputs of given systems),
+    the oracle's results of the last pass also check a sample of those outputs
+    (verify_sample). Returns (baseline, check or None)."""
     import oracle
     d = W.make(name, batch)
     w = d["workload"]
@@ -442,11 +443,11 @@ def cpu_baseline(name: str, batch: int | None, seconds: float) -> dict:
     reps, t0 = 0, time.time()
     while True:
         if w.op == "getrf_getrs":
-            oracle.getrf_getrs(d["A"], d["B"], w.layout, nthreads=cores)
+            res = oracle.getrf_getrs(d["A"], d["B"], w.layout, nthreads=cores)
         elif w.op == "potrf_potrs":
-            oracle.potrf_potrs(d["A"], d["B"], w.layout, nthreads=cores)
+            res = oracle.potrf_potrs(d["A"], d["B"], w.layout, nthreads=cores)
         else:
-            oracle.bdsv(d["strips"], d["x"], nthreads=cores)
+            res = oracle.bdsv(d["strips"], d["x"], nthreads=cores)
         reps += 1
         el = time.time() - t0
         if el >= seconds:
@@ -474,7 +475,13 @@ def cpu_baseline(name: str, batch: int | None, seconds: float) -> dict:
     out["one_core"] = {"value": round(reps1 * sub / el1, 1), "unit": "systems/s",
                        "sample": f"{reps1} passes over the first {sub} systems on 1 thread "
                                  f"({el1:.1f} s wall)"}
-    return out
+    check = None
+    if fetch is not None:
+        try:
+            check = verify_sample(d, fetch, res)
+        except Exception as e:  # reported in the line rather than lost with it
+            check = {"error": repr(e)[:200]}
+    return out, check
 
 
 class Ranks:
@@ -539,10 +546,6 @@ def run_native(args) -> None:
     ranks.barrier()
     clocks = sampler.stop(local)
     ms = statistics.fmean(times)
-    try:   # the last timed step's outputs against the oracle, on a sample of systems
-        verified = verify_sample(prob.d, prob.outputs)
-    except Exception as e:  # reported in the line rather than lost with it
-        verified = {"error": repr(e)[:200]}
     ranks.barrier()                   # the end-to-end steps start together on every rank
     e2e_times, h2d, d2h = time_e2e(prob, max(3, min(args.steps, 20)), 2, args.e2e_chunk)
     ranks.barrier()
@@ -583,9 +586,10 @@ def run_native(args) -> None:
                         f"{args.e2e_chunk} systems on two streams (copies overlap solves)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "verified": verified,
     }
-    line["cpu_baseline"] = cpu_baseline(args.workload, args.batch, args.cpu_seconds)
+    if world == 1:   # the CPU leg, which also checks a sample of the last timed step
+        line["cpu_baseline"], line["verified"] = cpu_baseline(
+            args.workload, args.batch, args.cpu_seconds, fetch=prob.outputs)
     if not args.headline_only:
         extra = {}
         for name in W.WORKLOADS:

@@ -85,7 +85,8 @@ def test_reference_arm_under_torchrun_prints_once():
 
 
 def test_cpu_baseline_reports_all_cores_and_one_core():
-    r = bench.cpu_baseline("lu_f64_n8", 256, 0.3)
+    r, check = bench.cpu_baseline("lu_f64_n8", 256, 0.3)
+    assert check is None
     assert r["kind"] == "oracle" and r["unit"] == "systems/s" and r["value"] > 0
     assert r["cores"] >= 1 and "256-system batch" in r["sample"]
     assert r["one_core"]["value"] > 0 and "on 1 thread" in r["one_core"]["sample"]
@@ -97,11 +98,13 @@ def _oracle_outputs(name, batch):
     d = W.make(name, batch)
     w = d["workload"]
     if w.op == "getrf_getrs":
-        LU, X, ipiv, info, _ = oracle.getrf_getrs(d["A"], d["B"], w.layout)
-        return d, [LU, X, ipiv, info]
+        ref = oracle.getrf_getrs(d["A"], d["B"], w.layout)
+        return d, ref, list(ref[:4])
     if w.op == "potrf_potrs":
-        return d, list(oracle.potrf_potrs(d["A"], d["B"], w.layout))
-    return d, list(oracle.bdsv(d["strips"], d["x"]))
+        ref = oracle.potrf_potrs(d["A"], d["B"], w.layout)
+    else:
+        ref = oracle.bdsv(d["strips"], d["x"])
+    return d, ref, list(ref)
 
 
 @pytest.mark.parametrize("name,batch", [("lu_f64_n8", 1024), ("lu_f32_n16", 700),
@@ -110,10 +113,10 @@ def test_post_timing_check_accepts_the_oracle_and_flags_one_ulp(name, batch):
     """The bench's check after timing: outputs equal to the oracle's pass (planted
     failures included); one output one ulp off in one sampled system is one mismatch."""
     import numpy as np
-    d, outs = _oracle_outputs(name, batch)
+    d, ref, outs = _oracle_outputs(name, batch)
     fetch = lambda idx: [o[idx] for o in outs]  # noqa: E731
     k = min(64, batch)
-    r = bench.verify_sample(d, fetch, k=64)
+    r = bench.verify_sample(d, fetch, ref, k=64)
     assert r["mismatches"] == 0 and r["sampled_systems"] == k
     assert r["bit_identical"] + r["near_tie_exempt"] == k
     idx = np.unique(np.linspace(0, batch - 1, k).astype(np.int64))
@@ -122,7 +125,7 @@ def test_post_timing_check_accepts_the_oracle_and_flags_one_ulp(name, batch):
     flat = X[j].reshape(-1)
     flat[0] = np.nextafter(flat[0], np.inf)
     bad = [outs[0], X] + outs[2:]
-    r = bench.verify_sample(d, lambda ix: [o[ix] for o in bad], k=64)
+    r = bench.verify_sample(d, lambda ix: [o[ix] for o in bad], ref, k=64)
     assert r["mismatches"] == 1 or (r["near_tie_exempt"] > 0 and r["mismatches"] <= 1)
 
 
@@ -130,15 +133,20 @@ def test_problem_outputs_gathers_the_sampled_systems():
     """Problem.outputs gathers systems idx of every output buffer (here CPU tensors
     holding the oracle's results) in the order the check takes."""
     import torch
-    d, outs = _oracle_outputs("lu_f64_n8", 1024)
+    d, ref, outs = _oracle_outputs("lu_f64_n8", 1024)
     prob = bench.Problem("lu_f64_n8", None, torch.device("cpu"))
     for dst, src in zip(prob.work + [prob.ipiv, prob.info], outs):
         dst.copy_(torch.from_numpy(src))
-    r = bench.verify_sample(prob.d, prob.outputs, k=256)
+    r = bench.verify_sample(prob.d, prob.outputs, ref, k=256)
     assert r == {"sampled_systems": 256, "bit_identical": 256 - r["near_tie_exempt"],
                  "near_tie_exempt": r["near_tie_exempt"], "mismatches": 0}
-    prob.info[512] = 7
-    assert bench.verify_sample(prob.d, prob.outputs, k=1024)["mismatches"] == 1
+    import numpy as np
+    j = int(np.unique(np.linspace(0, 1023, 256).astype(np.int64))[100])   # a sampled system
+    prob.info[j] = 7
+    assert bench.verify_sample(prob.d, prob.outputs, ref, k=256)["mismatches"] == 1
+    # the CPU leg runs the check on its own last pass over the same batch
+    base, check = bench.cpu_baseline("lu_f64_n8", None, 0.2, fetch=prob.outputs)
+    assert base["value"] > 0 and check["sampled_systems"] == 256 and check["mismatches"] == 1
 
 
 def test_bench_interleave_matches_the_generator():
