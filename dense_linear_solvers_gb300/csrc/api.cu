@@ -202,11 +202,18 @@ constexpr size_t kWorkAlign = 256;
 size_t round_up(size_t x) { return (x + kWorkAlign - 1) / kWorkAlign * kWorkAlign; }
 
 // Bytes of one slot of the workspace (a chunk of every operand, each 256-byte aligned);
-// the workspace holds two slots.
+// the workspace holds two slots. A size past kTooBig (no workspace is that large) is
+// returned as kTooBig, so that no product or sum below can wrap around.
+constexpr size_t kTooBig = SIZE_MAX / 4;
 size_t slot_bytes(const HostOperand* ops, int nops, int64_t chunk) {
+  const size_t c = static_cast<size_t>(chunk);
   size_t b = 0;
-  for (int i = 0; i < nops; ++i) b += round_up(ops[i].per_sys * static_cast<size_t>(chunk));
-  return b;
+  for (int i = 0; i < nops; ++i) {
+    const size_t per = ops[i].per_sys;
+    if (per != 0 && c > (kTooBig - b) / per / 2) return kTooBig;
+    b += round_up(per * c);
+  }
+  return b < kTooBig ? b : kTooBig;
 }
 
 // The batch in chunks of `chunk` systems; chunk c runs its copies in, its solve and its
@@ -227,7 +234,7 @@ bs_status host_pipeline(int64_t batch, int64_t chunk, HostOperand* ops, int nops
         return BS_ERR_INVALID_ARG;
   }
   const size_t slot = slot_bytes(ops, nops, chunk);
-  if (work_bytes < 2 * slot) return BS_ERR_INVALID_ARG;
+  if (slot >= kTooBig || work_bytes < 2 * slot) return BS_ERR_INVALID_ARG;
   cudaStream_t st[2] = {static_cast<cudaStream_t>(stream0), static_cast<cudaStream_t>(stream1)};
   char* dev[8];
   for (int64_t c0 = 0, c = 0; c0 < batch; c0 += chunk, ++c) {
@@ -257,6 +264,15 @@ bs_status host_pipeline(int64_t batch, int64_t chunk, HostOperand* ops, int nops
 
 size_t elem_size(bs_dtype dtype) { return dtype == BS_FP32 ? 4 : 8; }
 
+// Workspace bytes of the host-resident LU for a chunk (2 * kTooBig when too large).
+size_t lu_host_bytes(bs_dtype dtype, int n, int nrhs, int64_t chunk) {
+  HostOperand ops[4] = {{nullptr, elem_size(dtype) * n * n, true, true},
+                        {nullptr, elem_size(dtype) * n * nrhs, true, true},
+                        {nullptr, sizeof(int32_t) * n, false, true},
+                        {nullptr, sizeof(int32_t), false, true}};
+  return 2 * slot_bytes(ops, 4, chunk);
+}
+
 // Scratch of the entry point that takes no workspace: one static device array, placed by
 // the driver when the library's module loads (no call allocates).
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
@@ -268,11 +284,8 @@ extern "C" {
 
 size_t bs_getrf_getrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk) {
   if (n < 1 || nrhs < 1 || chunk < 1) return 0;
-  HostOperand ops[4] = {{nullptr, elem_size(dtype) * n * n, true, true},
-                        {nullptr, elem_size(dtype) * n * nrhs, true, true},
-                        {nullptr, sizeof(int32_t) * n, false, true},
-                        {nullptr, sizeof(int32_t), false, true}};
-  return 2 * slot_bytes(ops, 4, chunk);
+  const size_t w = lu_host_bytes(dtype, n, nrhs, chunk);
+  return w >= 2 * kTooBig ? 0 : w;
 }
 
 bs_status bs_getrf_getrs_batched_host(bs_dtype dtype, bs_layout layout, int n, int nrhs,
@@ -303,10 +316,8 @@ bs_status bs_getrf_getrs_batched_host_static(bs_dtype dtype, bs_layout layout, i
   if (batch == 0) return BS_OK;
   // the largest chunk, up to the requested one, whose two slots fit the static scratch
   int64_t c = chunk;
-  while (c > 1 && bs_getrf_getrs_host_workspace(dtype, n, nrhs, c) > kStaticScratchBytes)
-    c = c / 2;
-  if (bs_getrf_getrs_host_workspace(dtype, n, nrhs, c) > kStaticScratchBytes)
-    return BS_ERR_UNSUPPORTED;
+  while (c > 1 && lu_host_bytes(dtype, n, nrhs, c) > kStaticScratchBytes) c = c / 2;
+  if (lu_host_bytes(dtype, n, nrhs, c) > kStaticScratchBytes) return BS_ERR_UNSUPPORTED;
   void* work = nullptr;
   const cudaError_t e = cudaGetSymbolAddress(&work, g_static_scratch);
   if (e != cudaSuccess) return from_cuda(e);
@@ -319,7 +330,8 @@ size_t bs_potrf_potrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t ch
   HostOperand ops[3] = {{nullptr, elem_size(dtype) * n * n, true, true},
                         {nullptr, elem_size(dtype) * n * nrhs, true, true},
                         {nullptr, sizeof(int32_t), false, true}};
-  return 2 * slot_bytes(ops, 3, chunk);
+  const size_t slot = slot_bytes(ops, 3, chunk);
+  return slot >= kTooBig ? 0 : 2 * slot;
 }
 
 bs_status bs_potrf_potrs_batched_host(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
@@ -348,7 +360,8 @@ size_t bs_bdsv_host_workspace(bs_dtype dtype, int num_block_rows, int block_size
       {nullptr, es * num_block_rows * block_size * 3 * block_size, true, true},
       {nullptr, es * (num_block_rows + 2) * block_size, true, true},
       {nullptr, sizeof(int32_t), false, true}};
-  return 2 * slot_bytes(ops, 3, chunk);
+  const size_t slot = slot_bytes(ops, 3, chunk);
+  return slot >= kTooBig ? 0 : 2 * slot;
 }
 
 bs_status bs_bdsv_batched_host(bs_dtype dtype, int num_block_rows, int block_size,

@@ -375,3 +375,22 @@ def test_binding_operand_checks_reject_mismatches():
                                        info[:4], COL)
     with pytest.raises(ValueError, match="x_padded"):
         bs.bs_bdsv_batched_host(S, X[:2].contiguous(), binfo)
+
+
+def test_huge_chunks_do_not_wrap_the_workspace_size(lib):
+    """A chunk whose slots would not fit any memory makes the workspace queries return 0
+    (no wrapped-around small size), and a host call with such a chunk is refused before
+    any copy (the workspace it needs exceeds any that can be passed)."""
+    huge = 2 ** 62
+    assert lib.bs_getrf_getrs_host_workspace(bs.BS_FP32, 16, 4, huge) == 0
+    assert lib.bs_potrf_potrs_host_workspace(bs.BS_FP64, 32, 1, huge) == 0
+    assert lib.bs_bdsv_host_workspace(bs.BS_FP64, 32, 8, huge) == 0
+    assert lib.bs_getrf_getrs_host_workspace(bs.BS_FP32, 16, 4, 2 ** 40) > 2 ** 40 * 1348
+    A, B, P, I, WK = FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x1000000
+    for chunk in (huge, 2 ** 63 - 1):
+        assert lib.bs_getrf_getrs_batched_host(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, WK, 4096,
+                                               chunk, None, None) == bs.BS_ERR_INVALID_ARG
+        assert lib.bs_potrf_potrs_batched_host(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, WK, 4096,
+                                               chunk, None, None) == bs.BS_ERR_INVALID_ARG
+        assert lib.bs_bdsv_batched_host(bs.BS_FP64, 32, 8, 5, A, B, I, WK, 4096, chunk, None,
+                                        None) == bs.BS_ERR_INVALID_ARG
