@@ -385,6 +385,31 @@ def test_many_right_hand_sides(dtype, layout):
             assert np.array_equal(_host(tB2)[okc], Xco[okc])
 
 
+@pytest.mark.parametrize("dtype,layout,n,nrhs", [(np.float32, ROW_MAJOR, 16, 1003),
+                                                (np.float64, COL_MAJOR, 64, 257)])
+def test_hundreds_of_right_hand_sides(dtype, layout, n, nrhs):
+    """Hundreds of right-hand sides (a ragged last chunk of 8): the fused LU and Cholesky
+    calls still leave the oracle's fused results bit for bit."""
+    rng = np.random.default_rng(1212 + layout)
+    Al = rng.standard_normal((5, n, n)).astype(dtype)
+    Al[2, :, n // 2] = 0
+    A = to_storage(Al, layout)
+    B = to_storage(rng.standard_normal((5, n, nrhs)).astype(dtype), layout)
+    LUo, Xo, ipo, info_o, tie = oracle.getrf_getrs(A, B, layout, nthreads=NT)
+    LUg, Xg, ipg, infg = parity.gpu_lu(A, B, layout)
+    clean = tie < 0
+    assert np.array_equal(infg[clean], info_o[clean]) and info_o[2] == n // 2 + 1
+    assert np.array_equal(LUg[clean], LUo[clean]) and np.array_equal(Xg[clean], Xo[clean])
+    G = rng.standard_normal((5, n, n))
+    As = to_storage((G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dtype), layout)
+    Lo, Xco, inf_co = oracle.potrf_potrs(As, B, layout, nthreads=NT)
+    tA, tB = _dev(As), _dev(B)
+    info = torch.full((5,), SENT, dtype=torch.int32, device="cuda")
+    bs.bs_potrf_potrs_batched(tA, tB, info, layout, bs.BS_LOWER)
+    assert np.array_equal(_host(info), inf_co) and np.all(inf_co == 0)
+    assert np.array_equal(_host(tA), Lo) and np.array_equal(_host(tB), Xco)
+
+
 # ------------------------------------------------------------------ orders 65..128
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 @pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
