@@ -40,7 +40,7 @@ ROW_MAJOR, COL_MAJOR = BS_ROW_MAJOR, BS_COL_MAJOR
 EXPORTED = (
     "bs_getrf_getrs_batched", "bs_potrf_potrs_batched", "bs_bdsv_batched",
     "bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched", "bs_potrs_batched",
-    "bs_bdsv_factor_batched", "bs_bdsv_solve_batched", "bs_bdmv_batched",
+    "bs_bdsv_factor_batched", "bs_bdsv_solve_batched", "bs_bdmv_batched", "bs_bdmv2_batched",
     "bs_getrf_getrs_batched_ex", "bs_potrf_potrs_batched_ex",
     "bs_getrf_getrs_host_workspace", "bs_getrf_getrs_batched_host",
     "bs_potrf_potrs_host_workspace", "bs_potrf_potrs_batched_host",
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             L.bs_bdsv_factor_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp]
             L.bs_bdsv_solve_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp]
             L.bs_bdmv_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp]
+            L.bs_bdmv2_batched.argtypes = [i32, i32, i32, i64, vp, vp, vp, vp, vp]
             L.bs_getrf_getrs_batched_ex.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, vp,
                                                     ctypes.POINTER(Options), vp]
             L.bs_potrf_potrs_batched_ex.argtypes = [i32, i32, i32, i32, i32, i64, vp, vp, vp,
@@ -94,7 +95,7 @@ def lib() -> ctypes.CDLL:
             L.bs_potrf_potrs_batched_ex.restype = i32
             for name in ("bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched",
                          "bs_potrs_batched", "bs_bdsv_factor_batched", "bs_bdsv_solve_batched",
-                         "bs_bdmv_batched"):
+                         "bs_bdmv_batched", "bs_bdmv2_batched"):
                 getattr(L, name).restype = i32
             sz = ctypes.c_size_t
             L.bs_getrf_getrs_host_workspace.argtypes = [i32, i32, i32, i64]
@@ -301,6 +302,16 @@ def bs_bdmv_batched(strips, x_padded, y_padded, stream=None) -> None:
     st = lib().bs_bdmv_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips), _ptr(x_padded),
                                _ptr(y_padded), _stream(stream))
     _check(st, "bs_bdmv_batched")
+
+
+def bs_bdmv2_batched(strips, x_padded, y_padded, y2_padded, stream=None) -> None:
+    """The matvec stored into two padded outputs in one pass (see bsolve.h)."""
+    batch, nbr, bs = _strips(strips, [("x_padded", x_padded), ("y_padded", y_padded),
+                                      ("y2_padded", y2_padded)], None)
+    st = lib().bs_bdmv2_batched(_dtype_code(strips), nbr, bs, batch, _ptr(strips),
+                                _ptr(x_padded), _ptr(y_padded), _ptr(y2_padded),
+                                _stream(stream))
+    _check(st, "bs_bdmv2_batched")
 
 
 # --------------------------------------------------------------- contract variants

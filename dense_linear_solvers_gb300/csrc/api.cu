@@ -641,14 +641,17 @@ bs_status bs_bdsv_solve_batched(bs_dtype dtype, int num_block_rows, int block_si
   return from_cuda(e);
 }
 
-bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+// bdmv with one output (two == false, y2_padded unused) or two
+static bs_status bdmv_any(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
                           const void* strips, const void* x_padded, void* y_padded,
-                          void* stream) {
+                          void* y2_padded, bool two, void* stream) {
   if (num_block_rows < 0 || block_size < 0 || batch < 0) return BS_ERR_INVALID_ARG;
   if (!bdsv_supported(dtype, num_block_rows, block_size)) return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
-  if (!strips || !x_padded || !y_padded) return BS_ERR_INVALID_ARG;
-  if (!aligned16(strips) || !aligned16(x_padded) || !aligned16(y_padded))
+  if (!two) y2_padded = nullptr;
+  if (!strips || !x_padded || !y_padded || (two && !y2_padded)) return BS_ERR_INVALID_ARG;
+  if (!aligned16(strips) || !aligned16(x_padded) || !aligned16(y_padded) ||
+      (y2_padded && !aligned16(y2_padded)))
     return BS_ERR_INVALID_ARG;
   const size_t es = dtype == BS_FP32 ? 4 : 8;
   const size_t sbytes = static_cast<size_t>(batch) * num_block_rows * block_size * 3 *
@@ -656,18 +659,37 @@ bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_size, in
   const size_t vbytes = static_cast<size_t>(batch) * (num_block_rows + 2) * block_size * es;
   if (overlap(y_padded, vbytes, strips, sbytes) || overlap(y_padded, vbytes, x_padded, vbytes))
     return BS_ERR_INVALID_ARG;
+  if (y2_padded && !disjoint({{y2_padded, vbytes}, {strips, sbytes}, {x_padded, vbytes},
+                              {y_padded, vbytes}}))
+    return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e =
       dtype == BS_FP32
           ? bsolve::launch_bdmv<float>(num_block_rows, block_size, batch,
                                        static_cast<const float*>(strips),
                                        static_cast<const float*>(x_padded),
-                                       static_cast<float*>(y_padded), s)
+                                       static_cast<float*>(y_padded),
+                                       static_cast<float*>(y2_padded), s)
           : bsolve::launch_bdmv<double>(num_block_rows, block_size, batch,
                                         static_cast<const double*>(strips),
                                         static_cast<const double*>(x_padded),
-                                        static_cast<double*>(y_padded), s);
+                                        static_cast<double*>(y_padded),
+                                        static_cast<double*>(y2_padded), s);
   return from_cuda(e);
+}
+
+bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+                          const void* strips, const void* x_padded, void* y_padded,
+                          void* stream) {
+  return bdmv_any(dtype, num_block_rows, block_size, batch, strips, x_padded, y_padded, nullptr,
+                  false, stream);
+}
+
+bs_status bs_bdmv2_batched(bs_dtype dtype, int num_block_rows, int block_size, int64_t batch,
+                           const void* strips, const void* x_padded, void* y_padded,
+                           void* y2_padded, void* stream) {
+  return bdmv_any(dtype, num_block_rows, block_size, batch, strips, x_padded, y_padded,
+                  y2_padded, true, stream);
 }
 
 bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,

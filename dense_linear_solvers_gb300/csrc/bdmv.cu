@@ -19,10 +19,11 @@
 namespace bsolve {
 namespace {
 
-template <typename T, int BS>
+// DUAL: the page's second form, the same product stored into a second padded output too
+template <typename T, int BS, bool DUAL>
 __global__ void __launch_bounds__(256)
 bdmv_kernel(int nbr, int64_t batch, const T* __restrict__ strips, const T* __restrict__ xpad,
-            T* __restrict__ ypad) {
+            T* __restrict__ ypad, T* __restrict__ ypad2) {
   constexpr int W = 3 * BS;
   constexpr bool kVec = (W * sizeof(T)) % 16 == 0;
   constexpr int V = 16 / sizeof(T);
@@ -58,20 +59,26 @@ bdmv_kernel(int nbr, int64_t batch, const T* __restrict__ strips, const T* __res
     T acc = T(0);
 #pragma unroll
     for (int c = 0; c < W; ++c) acc = fma_rn<T>(v[c], __ldg(xw + c), acc);
-    ypad[s * vstride + static_cast<int64_t>(br + 1) * BS + r] = acc;
+    const int64_t at = s * vstride + static_cast<int64_t>(br + 1) * BS + r;
+    ypad[at] = acc;
+    if constexpr (DUAL) ypad2[at] = acc;
   }
 }
 
 template <typename T, int BS>
 cudaError_t launch_bs(int nbr, int64_t batch, const T* strips, const T* xpad, T* ypad,
-                      cudaStream_t stream) {
+                      T* ypad2, cudaStream_t stream) {
   const int per = nbr * BS;
   const int threads = per >= 256 ? 256 : (per + 31) / 32 * 32;
   const int64_t bx = (per + threads - 1) / threads;
   if (bx > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const unsigned by = static_cast<unsigned>(batch < 65535 ? batch : 65535);
-  bdmv_kernel<T, BS><<<dim3(static_cast<unsigned>(bx), by), threads, 0, stream>>>(
-      nbr, batch, strips, xpad, ypad);
+  const dim3 grid(static_cast<unsigned>(bx), by);
+  if (ypad2 != nullptr)
+    bdmv_kernel<T, BS, true><<<grid, threads, 0, stream>>>(nbr, batch, strips, xpad, ypad, ypad2);
+  else
+    bdmv_kernel<T, BS, false><<<grid, threads, 0, stream>>>(nbr, batch, strips, xpad, ypad,
+                                                            nullptr);
   return cudaGetLastError();
 }
 
@@ -79,23 +86,23 @@ cudaError_t launch_bs(int nbr, int64_t batch, const T* strips, const T* xpad, T*
 
 template <typename T>
 cudaError_t launch_bdmv(int nbr, int bs, int64_t batch, const T* strips, const T* xpad, T* ypad,
-                        cudaStream_t stream) {
+                        T* ypad2, cudaStream_t stream) {
   switch (bs) {
-    case 1: return launch_bs<T, 1>(nbr, batch, strips, xpad, ypad, stream);
-    case 2: return launch_bs<T, 2>(nbr, batch, strips, xpad, ypad, stream);
-    case 3: return launch_bs<T, 3>(nbr, batch, strips, xpad, ypad, stream);
-    case 4: return launch_bs<T, 4>(nbr, batch, strips, xpad, ypad, stream);
-    case 5: return launch_bs<T, 5>(nbr, batch, strips, xpad, ypad, stream);
-    case 6: return launch_bs<T, 6>(nbr, batch, strips, xpad, ypad, stream);
-    case 7: return launch_bs<T, 7>(nbr, batch, strips, xpad, ypad, stream);
-    case 8: return launch_bs<T, 8>(nbr, batch, strips, xpad, ypad, stream);
+    case 1: return launch_bs<T, 1>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 2: return launch_bs<T, 2>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 3: return launch_bs<T, 3>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 4: return launch_bs<T, 4>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 5: return launch_bs<T, 5>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 6: return launch_bs<T, 6>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 7: return launch_bs<T, 7>(nbr, batch, strips, xpad, ypad, ypad2, stream);
+    case 8: return launch_bs<T, 8>(nbr, batch, strips, xpad, ypad, ypad2, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template cudaError_t launch_bdmv<float>(int, int, int64_t, const float*, const float*, float*,
-                                        cudaStream_t);
+                                        float*, cudaStream_t);
 template cudaError_t launch_bdmv<double>(int, int, int64_t, const double*, const double*,
-                                         double*, cudaStream_t);
+                                         double*, double*, cudaStream_t);
 
 }  // namespace bsolve

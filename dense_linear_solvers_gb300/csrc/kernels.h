@@ -83,10 +83,11 @@ template <typename T>
 cudaError_t launch_bdsv_solve(int nbr, int bs, int64_t batch, const T* strips, T* xpad,
                               cudaStream_t stream);
 
-// Block-tridiagonal matrix-vector product on padded vectors, 1 <= bs <= 8.
+// Block-tridiagonal matrix-vector product on padded vectors, 1 <= bs <= 8; ypad2, when
+// not null, receives the same product too.
 template <typename T>
 cudaError_t launch_bdmv(int nbr, int bs, int64_t batch, const T* strips, const T* xpad, T* ypad,
-                        cudaStream_t stream);
+                        T* ypad2, cudaStream_t stream);
 
 // Shared memory one system needs in the shared-memory kernels.
 size_t lu_cta_bytes(int n, int nrhs, int elem_size);

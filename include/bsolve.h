@@ -279,6 +279,19 @@ BS_API bs_status bs_bdmv_batched(bs_dtype dtype, int num_block_rows, int block_s
                                  const void* strips, const void* x_padded, void* y_padded,
                                  void* stream);
 
+/*
+ * The second form of the same page's matvec: one pass that stores the product into two
+ * padded outputs (the page's use: z = p = A r at the start of a conjugate-gradient
+ * solve). Arguments as bs_bdmv_batched, plus
+ *   y2_padded  a second output of y_padded's shape receiving the same values (the pad
+ *              blocks not written); must not be null (when batch > 0) and must overlap
+ *              none of strips, x_padded and y_padded (BS_ERR_INVALID_ARG).
+ * Both outputs hold exactly the values bs_bdmv_batched writes.
+ */
+BS_API bs_status bs_bdmv2_batched(bs_dtype dtype, int num_block_rows, int block_size,
+                                  int64_t batch, const void* strips, const void* x_padded,
+                                  void* y_padded, void* y2_padded, void* stream);
+
 /* Human-readable name of a status code (a static string). */
 BS_API const char* bs_status_string(bs_status status);
 

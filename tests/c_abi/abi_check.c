@@ -69,6 +69,7 @@ int main(void) {
   CHECK(bs_bdsv_factor_batched(BS_FP64, 32, 8, 0, NULL, NULL, NULL) == BS_OK);
   CHECK(bs_bdsv_solve_batched(BS_FP64, 32, 8, 0, NULL, NULL, NULL) == BS_OK);
   CHECK(bs_bdmv_batched(BS_FP64, 32, 8, 0, NULL, NULL, NULL, NULL) == BS_OK);
+  CHECK(bs_bdmv2_batched(BS_FP64, 32, 8, 0, NULL, NULL, NULL, NULL, NULL) == BS_OK);
 
   /* argument errors and unsupported shapes */
   CHECK(bs_getrf_getrs_batched(BS_FP32, BS_ROW_MAJOR, 16, 4, -1, A, B, ipiv, info, NULL) ==
@@ -87,6 +88,7 @@ int main(void) {
   CHECK(bs_getrs_batched(BS_FP32, BS_ROW_MAJOR, 16, 4, 5, A, ipiv, fake(16), NULL) ==
         BS_ERR_INVALID_ARG); /* B over the factor */
   CHECK(bs_bdmv_batched(BS_FP64, 32, 8, 4, A, B, B, NULL) == BS_ERR_INVALID_ARG);
+  CHECK(bs_bdmv2_batched(BS_FP64, 32, 8, 4, A, B, ipiv, ipiv, NULL) == BS_ERR_INVALID_ARG);
 
   /* the contract options */
   memset(&o, 0, sizeof o);

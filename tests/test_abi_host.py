@@ -139,6 +139,14 @@ def test_split_argument_errors(lib):
     assert f(bs.BS_FP64, 32, 8, 4, A, B, None, None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP64, 32, 8, 4, A, B, B + 16, None) == bs.BS_ERR_INVALID_ARG     # y over x
     assert f(bs.BS_FP64, 32, 8, 4, A, B, A, None) == bs.BS_ERR_INVALID_ARG          # y over strips
+    f = lib.bs_bdmv2_batched
+    assert f(bs.BS_FP64, 32, 8, 0, None, None, None, None, None) == bs.BS_OK
+    assert f(bs.BS_FP64, 32, 0, 4, A, B, P, I, None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, P, None, None) == bs.BS_ERR_INVALID_ARG    # no y2
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, P, I + 8, None) == bs.BS_ERR_INVALID_ARG   # misaligned
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, P, P + 16, None) == bs.BS_ERR_INVALID_ARG  # y2 over y
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, P, A, None) == bs.BS_ERR_INVALID_ARG       # y2 over strips
+    assert f(bs.BS_FP64, 32, 8, 4, A, B, P, B, None) == bs.BS_ERR_INVALID_ARG       # y2 over x
 
 
 def test_contract_variant_argument_errors(lib):
@@ -295,6 +303,7 @@ def test_binding_operand_checks_accept_the_workloads():
             _refused_as_host(bs.bs_bdsv_factor_batched, S, info)
             _refused_as_host(bs.bs_bdsv_solve_batched, S, X)
             _refused_as_host(bs.bs_bdmv_batched, S, X, X.clone())
+            _refused_as_host(bs.bs_bdmv2_batched, S, X, X.clone(), X.clone())
             continue
         A, B = _cpu(d["A"]), _cpu(d["B"])
         n = A.shape[1]

@@ -302,6 +302,29 @@ def test_bdmv_every_block_size(dtype):
             assert np.array_equal(yg, yo), (bsz, nbr)
 
 
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_bdmv_two_outputs(dtype):
+    """The second matvec form stores the oracle's bdmv values into both outputs (the pad
+    blocks of each keep what they held); at the full workload size and over every block
+    size."""
+    rng = np.random.default_rng(818)
+    cases = [(W.make("bdsv_f64_32x8")["strips"], W.make("bdsv_f64_32x8")["x"])] \
+        if dtype == np.float64 else []
+    for bsz in (1, 3, 8):
+        for nbr in (1, 5, 33):
+            strips = rng.standard_normal((61, nbr, bsz, 3 * bsz)).astype(dtype)
+            xpad = rng.standard_normal((61, (nbr + 2) * bsz)).astype(dtype)
+            xpad[:, :bsz] = 0
+            xpad[:, (nbr + 1) * bsz:] = 0
+            cases.append((strips, xpad))
+    for strips, xpad in cases:
+        y1, y2 = np.full_like(xpad, 3.5), np.full_like(xpad, -1.25)
+        t1, t2 = _dev(y1), _dev(y2)
+        bs.bs_bdmv2_batched(_dev(strips), _dev(xpad), t1, t2)
+        assert np.array_equal(_host(t1), oracle.bdmv(strips, xpad, y1, nthreads=NT))
+        assert np.array_equal(_host(t2), oracle.bdmv(strips, xpad, y2, nthreads=NT))
+
+
 # ------------------------------------------------------------------ Cholesky, upper fill
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 @pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
