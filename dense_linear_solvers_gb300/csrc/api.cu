@@ -1,5 +1,6 @@
 // C ABI of libbsolve.so: argument checks and dispatch to the kernel launchers.
 // See include/bsolve.h for the contract of every entry point.
+#include <atomic>
 #include <cstdint>
 #include <initializer_list>
 #include <utility>
@@ -221,26 +222,35 @@ size_t slot_bytes(const HostOperand* ops, int nops, int64_t chunk) {
 // overlap the other stream's solve and copies, and a slot is reused only after its
 // stream has finished with it (stream order: no event needed). `call` gets the device
 // pointers of the operands, the chunk's system count and the stream.
+// Slot 1 starts `stride` bytes after slot 0 (0: right after it, i.e. at the slot size).
 template <class Call>
 bs_status host_pipeline(int64_t batch, int64_t chunk, HostOperand* ops, int nops, void* work,
-                        size_t work_bytes, void* stream0, void* stream1, Call call) {
+                        size_t work_bytes, void* stream0, void* stream1, Call call,
+                        size_t stride = 0) {
   if (batch < 0 || chunk < 1) return BS_ERR_INVALID_ARG;
   if (batch == 0) return BS_OK;
   if (!work || (reinterpret_cast<uintptr_t>(work) % kWorkAlign) != 0) return BS_ERR_INVALID_ARG;
   for (int i = 0; i < nops; ++i) {
     if (!ops[i].host) return BS_ERR_INVALID_ARG;
+    // the extent of a host array must be representable before the alias test below
+    if (ops[i].per_sys != 0 && static_cast<size_t>(batch) > kTooBig / ops[i].per_sys)
+      return BS_ERR_INVALID_ARG;
     for (int j = 0; j < i; ++j)   // the host arrays do not alias
       if (overlap(ops[i].host, ops[i].per_sys * batch, ops[j].host, ops[j].per_sys * batch))
         return BS_ERR_INVALID_ARG;
   }
   const size_t slot = slot_bytes(ops, nops, chunk);
-  if (slot >= kTooBig || work_bytes < 2 * slot) return BS_ERR_INVALID_ARG;
+  if (slot >= kTooBig) return BS_ERR_INVALID_ARG;
+  if (stride == 0) stride = slot;
+  if (stride < slot || stride % kWorkAlign != 0 || work_bytes < stride ||
+      work_bytes - stride < slot)
+    return BS_ERR_INVALID_ARG;
   cudaStream_t st[2] = {static_cast<cudaStream_t>(stream0), static_cast<cudaStream_t>(stream1)};
   char* dev[8];
   for (int64_t c0 = 0, c = 0; c0 < batch; c0 += chunk, ++c) {
     const int64_t m = batch - c0 < chunk ? batch - c0 : chunk;
     cudaStream_t s = st[c & 1];
-    char* base = static_cast<char*>(work) + (c & 1) * slot;
+    char* base = static_cast<char*>(work) + (c & 1) * stride;
     for (int i = 0; i < nops; ++i) {
       dev[i] = base;
       base += round_up(ops[i].per_sys * static_cast<size_t>(chunk));
@@ -274,9 +284,34 @@ size_t lu_host_bytes(bs_dtype dtype, int n, int nrhs, int64_t chunk) {
 }
 
 // Scratch of the entry point that takes no workspace: one static device array, placed by
-// the driver when the library's module loads (no call allocates).
+// the driver when the library's module loads (no call allocates). Its two chunk slots sit
+// at fixed offsets, 0 and half the array, whatever the shape of a call, so that calls
+// queued one after another on the same two streams (in the same order) never let one
+// call's chunk overwrite a slot that the other stream is still reading.
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+constexpr size_t kStaticSlotBytes = kStaticScratchBytes / 2;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// The device address of g_static_scratch on the current device. In host code the array's
+// name is only a host-side stand-in, so its address is looked up once per device (with
+// that device current) and kept; later calls on that device reuse it.
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_static_scratch_ptr[kMaxDevices];
+
+cudaError_t static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* p = g_static_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_scratch_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -314,15 +349,25 @@ bs_status bs_getrf_getrs_batched_host_static(bs_dtype dtype, bs_layout layout, i
   if (n < 0 || nrhs < 0 || batch < 0 || chunk < 1) return BS_ERR_INVALID_ARG;
   if (!lu_supported(dtype, layout, n, nrhs)) return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
-  // the largest chunk, up to the requested one, whose two slots fit the static scratch
+  // the largest chunk, up to the requested one, whose slot fits half the static scratch
   int64_t c = chunk;
-  while (c > 1 && lu_host_bytes(dtype, n, nrhs, c) > kStaticScratchBytes) c = c / 2;
-  if (lu_host_bytes(dtype, n, nrhs, c) > kStaticScratchBytes) return BS_ERR_UNSUPPORTED;
+  while (c > 1 && lu_host_bytes(dtype, n, nrhs, c) / 2 > kStaticSlotBytes) c = c / 2;
+  if (lu_host_bytes(dtype, n, nrhs, c) / 2 > kStaticSlotBytes) return BS_ERR_UNSUPPORTED;
   void* work = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&work, g_static_scratch);
+  const cudaError_t e = static_scratch_address(&work);
   if (e != cudaSuccess) return from_cuda(e);
-  return bs_getrf_getrs_batched_host(dtype, layout, n, nrhs, batch, A, B, ipiv, info, work,
-                                     kStaticScratchBytes, c, stream0, stream1);
+  const size_t es = elem_size(dtype);
+  HostOperand ops[4] = {{static_cast<char*>(A), es * n * n, true, true},
+                        {static_cast<char*>(B), es * n * nrhs, true, true},
+                        {reinterpret_cast<char*>(ipiv), sizeof(int32_t) * n, false, true},
+                        {reinterpret_cast<char*>(info), sizeof(int32_t), false, true}};
+  return host_pipeline(batch, c, ops, 4, work, kStaticScratchBytes, stream0, stream1,
+                       [&](char** d, int64_t m, cudaStream_t s) {
+                         return bs_getrf_getrs_batched(dtype, layout, n, nrhs, m, d[0], d[1],
+                                                       reinterpret_cast<int32_t*>(d[2]),
+                                                       reinterpret_cast<int32_t*>(d[3]), s);
+                       },
+                       kStaticSlotBytes);
 }
 
 size_t bs_potrf_potrs_host_workspace(bs_dtype dtype, int n, int nrhs, int64_t chunk) {

@@ -8,9 +8,11 @@
  * vector pointers are DEVICE pointers owned by the caller, except those of the
  * *_batched_host calls (host arrays, copied in and out by chunks on two streams); no
  * call allocates memory (the one device scratch, of the _static host call, is placed when
- * the library loads), keeps state for a later call or synchronizes the host. Results are valid once the stream has reached the launch; the per-system `info`
- * array is read back by the caller when it needs it. Calls may run concurrently on
- * different streams and may be captured into CUDA graphs.
+ * the library loads), keeps state for a later call or synchronizes the host. Results are
+ * valid once the stream has reached the launch; the per-system `info` array is read back
+ * by the caller when it needs it. Calls may run concurrently on different streams and may
+ * be captured into CUDA graphs (the _static host call excepted: its entry below says how
+ * calls to it may overlap).
  *
  * Batched storage: system s of a batched operand starts at element s * (elements per
  * system); there is no padding between systems. Offsets are 64-bit. (The _ex calls also
@@ -327,14 +329,24 @@ BS_API bs_status bs_getrf_getrs_batched_host(bs_dtype dtype, bs_layout layout, i
                                              int32_t* info, void* work, size_t work_bytes,
                                              int64_t chunk, void* stream0, void* stream1);
 /*
- * bs_getrf_getrs_batched_host without a workspace argument: the library's own static
- * device scratch (64 MiB, placed when the library loads; the call allocates nothing)
- * holds the two chunk slots, and the chunk is the requested one halved until its slots
- * fit (BS_ERR_UNSUPPORTED if one system does not fit). One scratch serves the whole
- * process: a call may start only once the previous call's chunks are done or are queued
- * on the same two streams (stream order then keeps them apart); concurrent calls from
- * several host threads on other streams must not overlap. Otherwise as
- * bs_getrf_getrs_batched_host.
+ * bs_getrf_getrs_batched_host without a workspace argument, for callers that cannot
+ * allocate device memory themselves (code that must not call cudaMalloc, e.g. because it
+ * runs under an allocator or a memory budget that it does not control). The paper has no
+ * counterpart: the pages solve device-resident batches only.
+ *
+ * The library's own static device scratch (64 MiB, placed by the driver when the library
+ * loads; the call allocates nothing) holds the two chunk slots at fixed offsets, 0 and
+ * 32 MiB, and the chunk is the requested one halved until one slot fits 32 MiB
+ * (BS_ERR_UNSUPPORTED if a single system does not fit). The first call on a device looks
+ * up the scratch's device address on that device (cudaGetSymbolAddress) and keeps it;
+ * make that first call before any stream capture on that device.
+ *
+ * One scratch serves the whole process and keeps the last call's contents (every byte a
+ * call reads there it has copied in first). Calls queued one after another on the same
+ * two streams, passed in the same order, are kept apart by stream order whatever their
+ * shapes; any other pair of calls whose work overlaps on the GPU (other streams, the two
+ * streams swapped, several host threads) races on the scratch and corrupts results:
+ * synchronize between them. Otherwise as bs_getrf_getrs_batched_host.
  */
 BS_API bs_status bs_getrf_getrs_batched_host_static(bs_dtype dtype, bs_layout layout, int n,
                                                     int nrhs, int64_t batch, void* A, void* B,

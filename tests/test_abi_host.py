@@ -244,6 +244,12 @@ def test_host_resident_argument_errors(lib):
     h = lib.bs_bdsv_batched_host
     assert h(bs.BS_FP64, 32, 9, 5, A, B, I, WK, 1 << 30, 8, None, None) == bs.BS_ERR_UNSUPPORTED
     assert h(bs.BS_FP64, 32, 8, 5, A, B, None, WK, 1 << 30, 8, None, None) == bs.BS_ERR_INVALID_ARG
+    # a batch whose host extent (systems x bytes per system) is not representable is refused
+    # before the host arrays are compared for overlap
+    assert f(bs.BS_FP32, 0, 16, 4, 1 << 62, A, B, P, I, WK, W, 8192, None,
+             None) == bs.BS_ERR_INVALID_ARG
+    assert h(bs.BS_FP64, 32, 8, 1 << 60, A, B, I, WK, 1 << 30, 8, None,
+             None) == bs.BS_ERR_INVALID_ARG
 
 
 def test_aliased_operands_are_rejected(lib):

@@ -89,3 +89,34 @@ def test_static_scratch_back_to_back_on_the_same_streams():
     for o in outs:
         for g, r in zip(o, dev):
             assert np.array_equal(g.numpy(), r)
+
+
+@pytest.mark.gpu
+def test_static_scratch_calls_of_different_shapes_on_the_same_streams():
+    """A call with small chunks, then without a sync a call whose chunk slot is far
+    larger, both queued on the same two streams in the same order: the fixed slot offsets
+    keep the second call from overwriting what the first still reads."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    small = W.make("lu_f32_n16", 6000)
+    rng = np.random.default_rng(4040)
+    A64 = rng.standard_normal((700, 64, 64))
+    B64 = rng.standard_normal((700, 64, 8))
+    dev_small = parity.gpu_lu(small["A"], small["B"], small["workload"].layout)
+    dev_large = parity.gpu_lu(A64, B64, W.ROW_MAJOR)
+    streams = (torch.cuda.Stream(), torch.cuda.Stream())
+    calls = [(small["A"], small["B"], small["workload"].layout, 512),
+             (A64, B64, W.ROW_MAJOR, 256)]
+    outs = []
+    for A, B, layout, chunk in calls:
+        tA, tB = _pinned(A), _pinned(B)
+        ipiv = torch.zeros(A.shape[:2], dtype=torch.int32).pin_memory()
+        info = torch.zeros(A.shape[0], dtype=torch.int32).pin_memory()
+        bs.bs_getrf_getrs_batched_host_static(tA, tB, ipiv, info, layout, chunk=chunk,
+                                              streams=streams, sync=False)
+        outs.append((tA, tB, ipiv, info))
+    for s in streams:
+        s.synchronize()
+    for o, dev in zip(outs, (dev_small, dev_large)):
+        for g, r in zip(o, dev):
+            assert np.array_equal(g.numpy(), r)
