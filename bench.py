@@ -93,6 +93,18 @@ def workload_text(w) -> str:
     return f"{w.name}: {w.text}"
 
 
+def config_of(w, batch: int, world: int) -> dict:
+    """The workload of a bench line; the same dict for the GPU arm and the reference arm."""
+    return {
+        "workload": workload_text(w), "op": w.op, "n": w.n, "nrhs": w.nrhs,
+        "batch_per_gpu": batch, "layout": "row-major" if w.layout == 0 else "column-major",
+        "l2": "GPU arm: L2 flushed before every step (256 MiB write), inputs restored from a "
+              "pristine device copy, both outside the CUDA events around the solver launch; "
+              "reference arm: host memory, inputs regenerated once",
+        "parallelism": f"batch shard x{world} (independent systems, no collective)",
+    }
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -422,13 +434,72 @@ def roofline(prob: Problem, ms: float, peaks: dict, name: str) -> dict:
                 "peak_source": f"{hbm_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": bytes_launch}
     ach = flops_launch / (ms * 1e-3) / 1e12
-    return {"bound": "alu", "achieved": round(ach, 4), "peak": round(alu, 4), "unit": "TFLOP/s",
-            "frac": round(ach / alu, 4), "traffic": traffic,
-            "peak_source": (f"{'FP64' if elem == 8 else 'FP32'} FMA: 152 SMs x "
-                            f"{costs.FP64_FMA_PER_CLK_PER_SM if elem == 8 else costs.FP32_FMA_PER_CLK_PER_SM}"
-                            " FMA/clk x 2 flops x 2070 MHz"),
-            "algorithmic_flops_per_launch": flops_launch,
-            "achieved_gbs": round(bytes_launch / (ms * 1e-3) / 1e9, 1)}
+    out = {"bound": "alu", "achieved": round(ach, 4), "peak": round(alu, 4), "unit": "TFLOP/s",
+           "frac": round(ach / alu, 4), "traffic": traffic,
+           "peak_source": (f"{'FP64' if elem == 8 else 'FP32'} FMA: 152 SMs x "
+                           f"{costs.FP64_FMA_PER_CLK_PER_SM if elem == 8 else costs.FP32_FMA_PER_CLK_PER_SM}"
+                           " FMA/clk x 2 flops x 2070 MHz (nominal)"),
+           "algorithmic_flops_per_launch": flops_launch,
+           "algorithmic_bytes_per_launch": bytes_launch,
+           "achieved_gbs": round(bytes_launch / (ms * 1e-3) / 1e9, 1)}
+    measured = peaks.get("fp64_tflops_measured" if elem == 8 else "fp32_tflops_measured")
+    if measured:
+        out["measured_peak"] = round(measured, 4)
+        out["frac_of_measured"] = round(ach / measured, 4)
+    return out
+
+
+def alu_peaks(device_index: int, seconds: float = 0.3) -> dict:
+    """The FP32 and FP64 FMA rates of this GPU, measured: independent FMA chains
+    (csrc/fma_peak.cu, built into libbsolve_probe.so) on every SM, each launch sized to
+    about `seconds`, the best of five timed with CUDA events, with the SM clock sampled
+    while they run. The roofline's nominal FP64 figure is 152 SMs x 2 FMA/clk x 2 flops x
+    2070 MHz; the measured one is reported beside it."""
+    import ctypes
+    import torch
+    from dense_linear_solvers_gb300 import _build
+    lib = ctypes.CDLL(_build.PROBE_LIB)
+    lib.bs_probe_fma_launch.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2
+    lib.bs_probe_fma_flops_per_thread_iter.restype = ctypes.c_int64
+    fpt = lib.bs_probe_fma_flops_per_thread_iter()
+    sms = torch.cuda.get_device_properties(device_index).multi_processor_count
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(None)
+    sampler.start()
+    out = {}
+    for code, name, tdt in ((0, "fp32", torch.float32), (1, "fp64", torch.float64)):
+        best_rate, shape = 0.0, None
+        for bps, thr in ((4, 256), (8, 256)):
+            blocks = sms * bps
+            sink = torch.empty(blocks * thr, dtype=tdt, device=f"cuda:{device_index}")
+
+            def run(iters):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if lib.bs_probe_fma_launch(code, blocks, thr, iters, sink.data_ptr(),
+                                           stream.cuda_stream) != 0:
+                    raise RuntimeError("FMA probe launch failed")
+                e1.record(stream)
+                e1.synchronize()
+                return e0.elapsed_time(e1)
+
+            iters = 64
+            run(iters)
+            t = run(iters)                       # calibrate the launch to about `seconds`
+            iters = max(64, int(iters * seconds * 1e3 / max(t, 1e-3)))
+            best = min(run(iters) for _ in range(5))
+            rate = fpt * iters * blocks * thr / (best * 1e-3) / 1e12
+            if rate > best_rate:
+                best_rate, shape = rate, f"{bps} blocks/SM x {thr} threads, {iters} iterations"
+            del sink
+        out[f"{name}_tflops_measured"] = round(best_rate, 4)
+        out[f"{name}_launch"] = shape
+    clocks = sampler.stop(device_index)
+    out["sm_mhz_median"] = clocks.get("sm_mhz")
+    out["clock_reasons"] = clocks.get("reasons")
+    out["how"] = ("independent FMA chains (8 per thread, csrc/fma_peak.cu) on every SM; best of "
+                  "5 launches of about 0.3 s, CUDA events; 2 flops per FMA")
+    return out
 
 
 def cpu_baseline(name: str, batch: int | None, seconds: float, fetch=None):
@@ -524,6 +595,25 @@ def whole_job_rate(batch_per_rank: int, world: int, ms_per_step: float) -> float
     return batch_per_rank * world / (ms_per_step * 1e-3)
 
 
+def summary_lines(line: dict) -> list:
+    """workload: ms per launch, systems/s, the roofline bound and fraction (of the measured
+    FMA peak too, for an ALU-bound row) and the DRAM traffic over the algorithmic bytes."""
+    rows = [(line["config"]["workload"].split(":")[0], line["ms_per_step"], line["value"],
+             line["roofline"])]
+    rows += [(k, v["ms_per_step"], v["systems_per_s"], v["roofline"])
+             for k, v in line.get("workloads", {}).items() if k != rows[0][0]]
+    rows += [(k, v["ms_per_step"], v["systems_per_s"], v["roofline"])
+             for k, v in line.get("next_rows", {}).items()]
+    out = []
+    for name, ms, rate, rf in rows:
+        alg = rf.get("algorithmic_bytes_per_launch")
+        tr = (f"{rf['traffic'] / alg:.2f}x" if rf.get("traffic") and alg else "n/a")
+        meas = f" ({rf['frac_of_measured']:.3f} of measured)" if "frac_of_measured" in rf else ""
+        out.append(f"{name}: {ms:.4f} ms, {rate:.3g} sys/s, {rf['bound']} {rf['frac']:.3f}"
+                   f"{meas}, traffic {tr}")
+    return out
+
+
 def run_native(args) -> None:
     import torch
     import dense_linear_solvers_gb300 as bs
@@ -568,15 +658,9 @@ def run_native(args) -> None:
         "vs_baseline": None,
         "dtype": dtype_tag(w.dtype),
         "data": "synthetic (seeded NumPy draws with the workload's distributions)",
-        "config": {
-            "workload": workload_text(w), "op": w.op, "n": w.n, "nrhs": w.nrhs,
-            "batch_per_gpu": prob.batch, "layout": "row-major" if w.layout == 0 else "column-major",
-            "l2": "flushed before every step (256 MiB write); inputs restored from a pristine "
-                  "device copy; both outside the CUDA events around the solver launch",
-            "ms_per_step_min": round(min(times), 5),
-            "ms_per_step_median": round(statistics.median(times), 5),
-            "parallelism": f"batch shard x{world} (independent systems, no collective)",
-        },
+        "config": config_of(w, prob.batch, world),
+        "ms_per_step_min": round(min(times), 5),
+        "ms_per_step_median": round(statistics.median(times), 5),
         "roofline": roofline(prob, ms, peaks, args.workload),
         "e2e": {"value": round(whole_job_rate(prob.batch, world, e2e_ms), 1), "unit": "systems/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -591,6 +675,9 @@ def run_native(args) -> None:
         line["cpu_baseline"], line["verified"] = cpu_baseline(
             args.workload, args.batch, args.cpu_seconds, fetch=prob.outputs)
     if not args.headline_only:
+        line["alu_peaks"] = alu_peaks(local)
+        peaks = dict(peaks, **{k: v for k, v in line["alu_peaks"].items()
+                               if k.endswith("_tflops_measured")})
         extra = {}
         for name in W.WORKLOADS:
             if name == args.workload:
@@ -614,6 +701,8 @@ def run_native(args) -> None:
                          "roofline": roofline(p, m, peaks, name)}
             del p
         line["next_rows"] = nxt
+        # one short entry per row at the end of the line, where a truncated tail still holds it
+        line["summary"] = summary_lines(line)
     print(json.dumps(line), flush=True)
     ranks.close()
 
@@ -651,9 +740,7 @@ def run_reference(args) -> None:
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_tag(w.dtype),
         "data": "synthetic (seeded NumPy draws with the workload's distributions)",
-        "config": {"workload": workload_text(w), "op": w.op, "n": w.n, "nrhs": w.nrhs,
-                   "batch_per_gpu": d["batch"],
-                   "layout": "row-major" if w.layout == 0 else "column-major"},
+        "config": config_of(w, d["batch"], int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "systems/s", "cores": cores, "kind": "oracle",
                          "sample": f"the whole {d['batch']}-system batch per step on {cores} "
                                    f"host threads (sequential C++ oracle, g++ -O2)"},

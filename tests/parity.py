@@ -111,10 +111,14 @@ def check_lu(A, B, layout, gpu, orc, kappa=None):
         assert worst <= FWD_TOL[dt], f"forward error {worst:.3e} > {FWD_TOL[dt]:.0e}"
         rep["max_forward_error"] = worst
         rep["forward_checked"] = int(fm.sum())
+    # the kernels perform the oracle's operations in the oracle's order: where the pivots
+    # agree (no near tie) and the factorization succeeded, L\U and X are equal bit for bit
     same = okm & clean & (info_o == 0)
-    rep["bitwise_equal_systems"] = int(
-        np.sum(np.all((LUg[same] == LUo[same]).reshape(same.sum(), -1), axis=1)
-               & np.all((Xg[same] == Xo[same]).reshape(same.sum(), -1), axis=1)))
+    eq = (np.all((LUg[same] == LUo[same]).reshape(same.sum(), -1), axis=1)
+          & np.all((Xg[same] == Xo[same]).reshape(same.sum(), -1), axis=1))
+    bad = np.nonzero(same)[0][~eq]
+    assert bad.size == 0, f"L\\U or X not bitwise equal to the oracle on systems {bad[:10]}"
+    rep["bitwise_equal_systems"] = int(eq.sum())
     rep["compared_for_bitwise"] = int(same.sum())
     return rep
 

@@ -80,6 +80,9 @@ def test_reference_arm_under_torchrun_prints_once():
         assert k in d, k
     assert d["n_gpus"] == 2 and d["steps"] == 1 and d["higher_is_better"] is True
     assert d["config"]["workload"].startswith("lu_f32_n16")
+    # the GPU arm's config for the same workload, batch and world size, key for key
+    from gen import workloads as W
+    assert d["config"] == bench.config_of(W.WORKLOADS["lu_f32_n16"], 256, 2)
     assert d["e2e"]["value"] == d["value"] and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
 
@@ -176,3 +179,20 @@ def test_traffic_records_point_at_committed_summaries():
         assert name in rows, name
         assert os.path.exists(os.path.join(ROOT, rec["profile"])), rec["profile"]
         assert rec["dram_bytes_per_launch"] > 0 and rec["captured_batch"] > 0
+
+
+def test_summary_lines_cover_every_row():
+    rf_hbm = {"bound": "hbm", "frac": 0.5, "traffic": 200.0, "algorithmic_bytes_per_launch": 100.0}
+    rf_alu = {"bound": "alu", "frac": 0.6, "traffic": None, "algorithmic_bytes_per_launch": 10.0,
+              "frac_of_measured": 0.63}
+    line = {"config": {"workload": "lu_f32_n16: LU ..."}, "ms_per_step": 0.05, "value": 1e9,
+            "roofline": rf_hbm,
+            "workloads": {"lu_f32_n16": {}, "chol_f64_n32": {"ms_per_step": 4.0,
+                                                             "systems_per_s": 6e7,
+                                                             "roofline": rf_alu}},
+            "next_rows": {"getrs_f32_n16": {"ms_per_step": 0.03, "systems_per_s": 2e9,
+                                            "roofline": rf_hbm}}}
+    out = bench.summary_lines(line)
+    assert [o.split(":")[0] for o in out] == ["lu_f32_n16", "chol_f64_n32", "getrs_f32_n16"]
+    assert "hbm 0.500" in out[0] and "traffic 2.00x" in out[0]
+    assert "alu 0.600 (0.630 of measured)" in out[1] and "traffic n/a" in out[1]

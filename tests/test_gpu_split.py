@@ -96,7 +96,8 @@ def _lu_case(A, B, layout):
 
 
 @pytest.mark.parametrize("name,batch", [("lu_f32_n16", None), ("lu_f64_n8", None),
-                                        ("lu_f64_n64", 301), ("lu_f32_n16", 1037)])
+                                        ("lu_f64_n64", None), ("lu_f64_n64", 301),
+                                        ("lu_f32_n16", 1037)])
 def test_getrf_getrs_workload(name, batch):
     d = W.make(name, batch)
     _lu_case(d["A"], d["B"], d["workload"].layout)
