@@ -22,8 +22,9 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 LIB_SOURCES = ["api.cu", "lu_reg.cu", "lu_reg_f32_row.cu", "lu_reg_f32_col.cu", "lu_reg_f64_row.cu",
-               "lu_reg_f64_col.cu", "lu_reg_il_f32.cu", "lu_reg_il_f64.cu", "lu_cta.cu",
-               "smem_solvers.cu", "chol_sys.cu", "bdsv.cu", "bdmv.cu", "solve.cu",
+               "lu_reg_f64_col.cu", "lu_reg_il_f32_row.cu", "lu_reg_il_f32_col.cu", "lu_reg_il_f64_row.cu",
+               "lu_reg_il_f64_col.cu", "lu_cta.cu",
+               "smem_solvers.cu", "chol_sys.cu", "chol_cluster.cu", "bdsv.cu", "bdmv.cu", "solve.cu",
                "solve_lane.cu"]
 PROBE_SOURCES = ["fma_peak.cu"]
 

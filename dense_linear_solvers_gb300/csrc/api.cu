@@ -15,6 +15,7 @@ namespace {
 thread_local int g_last_cuda_error = 0;
 
 constexpr int kMaxLuN = 128;
+constexpr int kMaxCholN = 256;       // beyond kMaxLuN: the cluster factor and the big solve
 constexpr int kMaxRegN = 32;
 constexpr int kMaxNrhs = 8;          // right-hand sides a fused kernel holds
 constexpr int kMaxNrhsAny = 65536;   // beyond kMaxNrhs: factor, then a chunked solve
@@ -75,7 +76,7 @@ bool chol_supported(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int n
   return (dtype == BS_FP32 || dtype == BS_FP64) &&
          (layout == BS_ROW_MAJOR || layout == BS_COL_MAJOR) &&
          (fill == BS_LOWER || fill == BS_UPPER) && n >= 1 &&
-         n <= kMaxLuN && nrhs >= 1 && nrhs <= kMaxNrhsAny;
+         n <= kMaxCholN && nrhs >= 1 && nrhs <= kMaxNrhsAny;
 }
 
 // Packed storage-order code of the Cholesky kernels: bit 0 for A (or the factor), bit 1 for
@@ -165,7 +166,8 @@ bs_status potrf_potrs_il(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, 
                          int64_t batch, int64_t ilv, void* A, void* B, int32_t* info,
                          void* stream) {
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
-  if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
+  if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs || n > kMaxLuN)
+    return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
   if (!A || !B || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;
@@ -479,8 +481,9 @@ bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill,
   if (!chol_disjoint(dtype, n, nrhs, batch, 1, A, B, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (nrhs > kMaxNrhs) {
-    // the factor, then the solve that zeroes X where info != 0 (see the LU call)
+  if (nrhs > kMaxNrhs || n > kMaxLuN) {
+    // the factor, then the solve that zeroes X where info != 0 (see the LU call); orders
+    // beyond one CTA always run this way (the cluster factor, then the big solve)
     const bs_status st = bs_potrf_batched(dtype, layout, fill, n, batch, A, info, stream);
     if (st != BS_OK) return st;
     e = dtype == BS_FP32
@@ -601,7 +604,13 @@ bs_status bs_potrf_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n
     return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (n <= kMaxRegN) {
+  if (n > kMaxLuN) {
+    e = dtype == BS_FP32
+            ? bsolve::launch_chol_cluster<float>(chol_layouts(layout, fill), n, batch,
+                                                 static_cast<float*>(A), info, s)
+            : bsolve::launch_chol_cluster<double>(chol_layouts(layout, fill), n, batch,
+                                                  static_cast<double*>(A), info, s);
+  } else if (n <= kMaxRegN) {
     e = dtype == BS_FP32
             ? bsolve::launch_chol_sys<float>(chol_layouts(layout, fill), n, 0, batch,
                                              static_cast<float*>(A), nullptr, info, s)
@@ -796,7 +805,8 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
                   : bs_potrf_potrs_batched(dtype, layout, fill, n, nrhs, batch, A, B, info,
                                            stream);
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
-  if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs) return BS_ERR_UNSUPPORTED;
+  if (!chol_supported(dtype, layout, fill, n, nrhs) || nrhs > kMaxNrhs || n > kMaxLuN)
+    return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
   if (!A || !B || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(info)) return BS_ERR_INVALID_ARG;

@@ -65,6 +65,16 @@ template <typename T>
 cudaError_t launch_chol_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
                                 int32_t* info, int ruda, cudaStream_t stream, int64_t ilv = 1);
 
+// Lower Cholesky factor (potrf) for 128 < n <= 256 on a cluster of four CTAs, the tiles
+// of one system spread over their shared memory; layout bit 0: A's storage order.
+template <typename T>
+cudaError_t launch_chol_cluster(int layout, int n, int64_t batch, T* A, int32_t* info,
+                                cudaStream_t stream);
+// potrs for 128 < n <= 256, any nrhs >= 1: one CTA per system (packed storage-order code).
+template <typename T>
+cudaError_t launch_potrs_big(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
+                             const int32_t* zinfo, cudaStream_t stream);
+
 // Lower Cholesky + solve, sixteen systems per block in lockstep, 1 <= n <= 32.
 template <typename T>
 cudaError_t launch_chol_sys(int layout, int n, int nrhs, int64_t batch, T* A, T* B,

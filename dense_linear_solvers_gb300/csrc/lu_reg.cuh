@@ -493,17 +493,22 @@ cudaError_t launch_tier(int n, int nrhs, int64_t batch, T* A, T* B, int32_t* ipi
   return cudaGetLastError();
 }
 
-// The interleaved batched layout: one instance per tier (the order and right-hand-side
-// guards kept), systems in blocks of ilv.
+// The interleaved batched layout, systems in blocks of ilv: per tier an instance without
+// guards (n and nrhs the tier's) and one with them.
 template <typename T, int NT, int RT, int LAYOUT>
 cudaError_t launch_tier_il(int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
                            int32_t* ipiv, int32_t* info, cudaStream_t stream) {
   constexpr int per_block = kWarps * (32 / NT);
   const int64_t blocks = (batch + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  lu_reg_kernel<T, NT, RT, LAYOUT, false, true>
-      <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv, info,
-                                                               ilv);
+  if (n == NT && nrhs == RT)   // the order and right-hand sides of the tier: no guards
+    lu_reg_kernel<T, NT, RT, LAYOUT, true, true>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv,
+                                                                 info, ilv);
+  else
+    lu_reg_kernel<T, NT, RT, LAYOUT, false, true>
+        <<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv,
+                                                                 info, ilv);
   return cudaGetLastError();
 }
 

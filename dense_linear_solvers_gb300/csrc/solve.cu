@@ -494,6 +494,8 @@ cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L,
   // FP64, n <= 32, one right-hand side: one system per lane (solve_lane.cu)
   if constexpr (std::is_same<T, double>::value)
     if (n <= 32 && nrhs == 1) return launch_potrs_lane(layout, n, nrhs, batch, L, B, zinfo, stream);
+  // orders beyond one CTA's shared memory: one CTA per system, the factor by tile columns
+  if (n > 128) return launch_potrs_big(layout, n, nrhs, batch, L, B, zinfo, stream);
   return launch_kind<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, zinfo, stream);
 }
 

@@ -108,9 +108,13 @@ BS_API bs_status bs_getrf_getrs_batched(bs_dtype dtype, bs_layout layout, int n,
  *   info  batch int32. 0 = success; k > 0 = the leading minor of order k is not positive
  *         definite (the k-th diagonal of the factorization is not > 0, NaN included).
  *         The factor from column k-1 on is then unspecified.
- * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER or BS_UPPER, 1 <= n <= 128,
- * 1 <= nrhs <= 65536 (above 8: bs_potrf_batched then the solve of bs_potrs_batched, X
- * zeroed where info != 0).
+ * Supported: dtype FP32/FP64, both layouts, fill BS_LOWER or BS_UPPER, 1 <= n <= 256,
+ * 1 <= nrhs <= 65536 (above 8 right-hand sides, and for every n > 128:
+ * bs_potrf_batched then the solve of bs_potrs_batched, X zeroed where info != 0). For
+ * 128 < n <= 256 the factor runs on a cluster of four CTAs per system, the 32 x 32 tiles
+ * of the triangle spread over their shared memory and read across the cluster
+ * (cuSolverDx docs, "Cholesky Factorization": the cluster tiling beyond one CTA); the
+ * results are the same operations in the same order as for any other n.
  */
 BS_API bs_status bs_potrf_potrs_batched(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
                                  int nrhs, int64_t batch, void* A, void* B, int32_t* info,
@@ -241,9 +245,9 @@ BS_API bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_
  * bs_bdsv_factor_batched: strips <- F_k (MAIN, lower), E_k (LEFT); info as bs_bdsv_batched.
  * bs_bdsv_solve_batched:  strips from bs_bdsv_factor_batched (read only); interior of
  *                    x_padded: b on entry, x on return (pads neither read nor written).
- * Supported: as the fused calls (getrf/potrf: 1 <= n <= 128; getrs/potrs: 1 <= n <= 128,
- * 1 <= nrhs <= 65536, taken 8 columns at a time; bdsv: 1 <= block_size <= 8), FP32/FP64,
- * both layouts, both fills.
+ * Supported: as the fused calls (getrf: 1 <= n <= 128; potrf: 1 <= n <= 256; getrs:
+ * 1 <= n <= 128, potrs: 1 <= n <= 256, 1 <= nrhs <= 65536, taken 8 columns at a time;
+ * bdsv: 1 <= block_size <= 8), FP32/FP64, both layouts, both fills.
  */
 BS_API bs_status bs_getrf_batched(bs_dtype dtype, bs_layout layout, int n, int64_t batch, void* A,
                                   int32_t* ipiv, int32_t* info, void* stream);

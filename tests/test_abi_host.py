@@ -218,6 +218,25 @@ def test_binding_refuses_host_tensors():
         bs.bs_getrf_getrs_batched(A, B, ipiv, info)
 
 
+def test_cholesky_order_limits(lib):
+    """Cholesky reaches n = 256 (beyond one CTA: the cluster factor); LU stays at 128; the
+    contract options and interleaved layouts stay at n <= 128."""
+    import ctypes
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_LOWER, 256, 1) == 1
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP32, bs.BS_ROW_MAJOR, bs.BS_UPPER, 200, 3) == 1
+    assert lib.bs_potrf_potrs_supported(bs.BS_FP64, bs.BS_COL_MAJOR, bs.BS_LOWER, 257, 1) == 0
+    A, B, I = FAKE, FAKE + 0x1000000, FAKE + 0x2000000
+    assert lib.bs_potrf_potrs_batched(bs.BS_FP64, 1, 0, 257, 1, 5, A, B, I,
+                                      None) == bs.BS_ERR_UNSUPPORTED
+    assert lib.bs_potrf_batched(bs.BS_FP64, 1, 0, 300, 5, A, I, None) == bs.BS_ERR_UNSUPPORTED
+    ruda = ctypes.byref(bs.Options(1.0, bs.BS_CONTRACT_RUDA, 0, 0, 0))
+    assert lib.bs_potrf_potrs_batched_ex(bs.BS_FP64, 1, 0, 200, 1, 5, A, B, I, ruda,
+                                         None) == bs.BS_ERR_UNSUPPORTED
+    il = ctypes.byref(bs.Options(1.0, 0, 0, 4, 0))
+    assert lib.bs_potrf_potrs_batched_ex(bs.BS_FP64, 1, 0, 200, 1, 8, A, B, I, il,
+                                         None) == bs.BS_ERR_UNSUPPORTED
+
+
 def test_host_resident_argument_errors(lib):
     """The *_host calls check everything before the first copy: chunk, workspace (null,
     misaligned, too small), host pointers, shapes; an empty batch submits nothing."""
