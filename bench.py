@@ -244,6 +244,7 @@ NEXT_ROWS = {
     "getrf_getrs_T_f32_n16": ("lu_f32_n16", "getrf_getrs_T"),
     "getrf_getrs_aosoa32_f32_n16": ("lu_f32_n16", "getrf_getrs_il"),
     "potrf_potrs_soa_f64_n32": ("chol_f64_n32", "potrf_potrs_il"),
+    "potrf_potrs_f64_n256": ("chol_f64_n256", "potrf_potrs"),
 }
 # systems per block of the interleaved rows (None: the whole batch, SoA)
 IL_WIDTH = {"getrf_getrs_aosoa32_f32_n16": 32, "potrf_potrs_soa_f64_n32": None}
@@ -256,7 +257,9 @@ KERNEL_SOURCES.update({
     "getrf_getrs_T_f32_n16": ["solve.cu", "lu_reg.cuh", "common.cuh"],
     "getrf_getrs_aosoa32_f32_n16": ["lu_reg.cuh", "common.cuh"],
     "potrf_potrs_soa_f64_n32": ["chol_sys.cu", "common.cuh"],
+    "potrf_potrs_f64_n256": ["chol_cluster.cu", "common.cuh"],
 })
+KERNEL_NAMES["potrf_potrs_f64_n256"] = "chol_cluster_kernel"
 
 
 def interleave_device(x, w: int):
@@ -294,6 +297,8 @@ class SplitProblem(Problem):
             self.inputs, self.fixed = [], (a, b)
         elif op == "getrf_getrs_T":   # the fused call under TDLS's row-major reading
             self.inputs = [a, b]
+        elif op == "potrf_potrs":   # the fused call on a workload of its own
+            self.inputs = [a, b]
         elif op in ("getrf_getrs_il", "potrf_potrs_il"):   # interleaved batched layout
             self.ilv = IL_WIDTH[name] or self.batch
             if self.batch % self.ilv:
@@ -330,6 +335,9 @@ class SplitProblem(Problem):
             bs.bs_getrf_getrs_batched_ex(self.work[0], self.work[1], self.ipiv, self.info,
                                          w.layout, interleave=self.ilv,
                                          shape=(self.batch, w.n, w.nrhs), stream=stream)
+        elif op == "potrf_potrs":
+            bs.bs_potrf_potrs_batched(self.work[0], self.work[1], self.info, w.layout,
+                                      bs.BS_LOWER, stream)
         elif op == "potrf_potrs_il":
             bs.bs_potrf_potrs_batched_ex(self.work[0], self.work[1], self.info, w.layout,
                                          bs.BS_LOWER, interleave=self.ilv,

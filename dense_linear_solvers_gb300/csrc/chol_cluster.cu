@@ -12,9 +12,13 @@
 //      shared memory (distributed shared memory loads) and scales its own tiles (i,k),
 //      i > k, one thread per row, column by column (l_rc = a_rc r_c, then
 //      a_rj -= l_rc l_jc for the tile's later columns);
-//   3. cluster barrier; every CTA copies the panel tiles (i,k) of the other CTAs into a
-//      local buffer and applies the 32 updates of the panel to each of its trailing tiles
-//      (i,j), k < j <= i, element (r, c) taking a_rc -= l_rK l_cK in increasing K.
+//   3. cluster barrier; every CTA applies the 32 updates of the panel to each of its
+//      trailing tiles (i,j), k < j <= i, element (r, c) taking a_rc -= l_rK l_cK in
+//      increasing K, one warp a tile: first the tiles of column k+1, then (look-ahead)
+//      warp 0 of the owner of tile (k+1,k+1) factors it while every other warp updates
+//      the remaining tiles. FP64 reads the panel tiles where they live (the other CTAs'
+//      through distributed-shared-memory loads: an FP64 update costs the pipe far more
+//      than its loads, and no staging buffer keeps two CTAs per SM); FP32 stages them.
 // Every element thus takes the oracle's right-looking updates in increasing column order,
 // each one fused multiply-add, so the factor is the oracle's bit for bit. Orders that are
 // not a multiple of 32 are padded with identity rows and columns at the end: they come
@@ -46,6 +50,7 @@ constexpr int kMaxT = 8;        // tiles per dimension: n <= 256
 constexpr int kMaxTiles = kMaxT * (kMaxT + 1) / 2;
 constexpr int kMaxSlots = (kMaxTiles + CL - 1) / CL;
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kTile = TS * TP;  // elements of one staged tile
 
 __host__ __device__ constexpr int tile_index(int i, int j) { return i * (i + 1) / 2 + j; }
@@ -59,52 +64,102 @@ __device__ __forceinline__ int64_t bidx(int layout, int n, int nrhs, int r, int 
                              : static_cast<int64_t>(c) * n + r;
 }
 
+// FP32 stages the panel tile column in local shared memory (its updates are cheap, remote
+// loads would dominate); FP64 reads the panel tiles where they live (each FP64 update
+// costs the pipe far more than its loads, and no staging keeps two CTAs per SM).
+template <typename T>
+constexpr bool kStagePanel = sizeof(T) == 4;
+
 template <typename T>
 size_t cluster_smem_bytes() {
-  // owned tiles, the staged panel (tile rows 0..kMaxT-1, row k holding L_kk), the diagonal
+  // owned tiles, a staged copy of L_kk, the staged panel (FP32), the diagonal
   // reciprocals (own and staged), the first failure
-  return static_cast<size_t>(kMaxSlots + kMaxT) * kTile * sizeof(T) + 2 * TS * sizeof(T) + 16;
+  return static_cast<size_t>(kMaxSlots + 1 + (kStagePanel<T> ? kMaxT : 0)) * kTile * sizeof(T) +
+         2 * TS * sizeof(T) + 16;
 }
 
-// Factor the diagonal tile at `a` (pitch TP) with one warp; lane r owns row r. k is the
-// tile column (for the global index of a failing minor), n the order.
+// One warp applies the 32 updates of a panel to a 32 x 32 tile: a_rc -= l_iK l_jK for
+// K = 0..31 in order, li / lj the panel tiles of the tile's row and column (pitch TP);
+// lane = a 4 x 4 block of each half of the tile (rows 0-15, then 16-31).
+template <typename T>
+__device__ __forceinline__ void update_tile(T* a, const T* li, const T* lj, int lane) {
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    const int r0 = h * 16 + (lane >> 3) * 4, c0 = (lane & 7) * 4;
+    T acc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) acc[u][v] = a[(r0 + u) * TP + c0 + v];
+#pragma unroll 4
+    for (int K = 0; K < TS; ++K) {
+      T x[4], y[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        x[u] = li[(r0 + u) * TP + K];
+        y[u] = lj[(c0 + u) * TP + K];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = fma_rn<T>(-x[u], y[v], acc[u][v]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) a[(r0 + u) * TP + c0 + v] = acc[u][v];
+  }
+}
+
+__device__ __forceinline__ void tile_coords(int t, int& i, int& j) {
+  i = 0;
+  while (tile_index(i + 1, 0) <= t) ++i;
+  j = t - tile_index(i, 0);
+}
+
+// Factor the diagonal tile at `a` (pitch TP, in shared memory) with one warp; lane r
+// owns row r. k is the tile column (for the global index of a failing minor), n the
+// order. The tile stays in shared memory (the warp's rows would take 64 registers a
+// thread in FP64): column c is scaled by the lanes below it, then each lane applies the
+// column to the rest of its row; one __syncwarp orders each phase.
 template <typename T>
 __device__ void potrf_tile(T* a, T* rc, int k, int n, int* fail) {
   const int r = threadIdx.x & 31;
-  T v[TS];
-#pragma unroll
-  for (int j = 0; j < TS; ++j) v[j] = a[r * TP + j];
   int first = 0x7FFFFFFF;
-#pragma unroll
+#pragma unroll 1
   for (int c = 0; c < TS; ++c) {
-    const T d = __shfl_sync(0xFFFFFFFFu, v[c], c);
+    const T d = a[c * TP + c];
     if (!(d > T(0)) && k * TS + c < n && first == 0x7FFFFFFF) first = k * TS + c + 1;
     const T l = sqrt_rn<T>(d);
     const T rr = rcp_rn<T>(l);
-    if (r == c) v[c] = l;
-    if (r > c) v[c] = v[c] * rr;
+    __syncwarp();
+    if (r == c) a[c * TP + c] = l;
+    if (r > c) a[r * TP + c] = a[r * TP + c] * rr;
     if (r == 0) rc[c] = rr;
-#pragma unroll
-    for (int j = c + 1; j < TS; ++j) {
-      const T ljc = __shfl_sync(0xFFFFFFFFu, v[c], j);
-      if (r >= j) v[j] = fma_rn<T>(-v[c], ljc, v[j]);
+    __syncwarp();
+    if (r > c) {
+      const T lrc = a[r * TP + c];
+#pragma unroll 1
+      for (int j = c + 1; j <= r; ++j)
+        a[r * TP + j] = fma_rn<T>(-lrc, a[j * TP + c], a[r * TP + j]);
     }
+    __syncwarp();
   }
-#pragma unroll
-  for (int j = 0; j < TS; ++j) a[r * TP + j] = v[j];
   if (r == 0 && first < *fail) *fail = first;
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* __restrict__ info) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int64_t s = blockIdx.x / CL;
   extern __shared__ __align__(16) unsigned char raw[];
   T* const tiles = reinterpret_cast<T*>(raw);
-  T* const panel = tiles + kMaxSlots * kTile;
-  T* const rc = panel + kMaxT * kTile;      // reciprocals of the tile this CTA factored
+  T* const lkk = tiles + kMaxSlots * kTile;  // staged L_kk
+  T* const panel = lkk + kTile;              // FP32: the staged panel tiles (i,k) at row i
+  T* const rc = panel + (kStagePanel<T> ? kMaxT : 0) * kTile;   // reciprocals of the tile
+                                                                // this CTA factored
   T* const rcs = rc + TS;                  // staged reciprocals of L_kk
   int* const fail = reinterpret_cast<int*>(rcs + TS);
   const int tid = threadIdx.x;
@@ -133,93 +188,88 @@ chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* 
   if (tid == 0) *fail = 0x7FFFFFFF;
   __syncthreads();
 
+  const int warp = tid >> 5, lane = tid & 31;
+  // the panel tile (i,k): local, staged (FP32) or remote (FP64)
+  auto panel_tile = [&](int i, int k) -> const T* {
+    if constexpr (kStagePanel<T>) {
+      return panel + i * kTile;
+    } else {
+      const int t = tile_index(i, k);
+      return cluster.map_shared_rank(tiles + (t / CL) * kTile, t % CL);
+    }
+  };
+  // tile (0,0) lives in rank 0, slot 0
+  if (rank == 0 && warp == 0) potrf_tile<T>(tiles, rc, 0, n, fail);
   for (int k = 0; k < nt; ++k) {
     const int tkk = tile_index(k, k);
-    if (tkk % CL == rank && tid < 32) potrf_tile<T>(tiles + (tkk / CL) * kTile, rc, k, n, fail);
-    cluster.sync();
+    cluster.sync();   // L_kk is factored
     // L_kk and its reciprocals from the owner
     {
       const T* src = cluster.map_shared_rank(tiles + (tkk / CL) * kTile, tkk % CL);
-      T* dst = panel + k * kTile;
-      for (int e = tid; e < kTile; e += kThreads) dst[e] = src[e];
+      for (int e = tid; e < kTile; e += kThreads) lkk[e] = src[e];
       const T* rsrc = cluster.map_shared_rank(rc, tkk % CL);
       if (tid < TS) rcs[tid] = rsrc[tid];
     }
     __syncthreads();
     // the owned panel tiles (i,k), i > k: one thread per row
     {
-      const T* Lkk = panel + k * kTile;
+      const T* Lkk = lkk;
       int q = 0;   // ordinal of the owned panel tile
       for (int i = k + 1; i < nt; ++i) {
         const int t = tile_index(i, k);
         if (t % CL != rank) continue;
         if (q * TS <= tid && tid < (q + 1) * TS) {
+          // the row stays in shared memory (32 FP64 values would crowd the registers)
           T* row = tiles + (t / CL) * kTile + (tid - q * TS) * TP;
-          T v[TS];
-#pragma unroll
-          for (int c = 0; c < TS; ++c) v[c] = row[c];
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < TS; ++c) {
-            const T l = v[c] * rcs[c];
-            v[c] = l;
-#pragma unroll
-            for (int j = c + 1; j < TS; ++j) v[j] = fma_rn<T>(-l, Lkk[j * TP + c], v[j]);
+            const T l = row[c] * rcs[c];
+            row[c] = l;
+#pragma unroll 4
+            for (int j = c + 1; j < TS; ++j) row[j] = fma_rn<T>(-l, Lkk[j * TP + c], row[j]);
           }
-#pragma unroll
-          for (int c = 0; c < TS; ++c) row[c] = v[c];
         }
         ++q;
       }
     }
     __syncthreads();
-    cluster.sync();
-    // the panel tiles of every CTA into the local buffer (row i at panel + i * kTile)
-    for (int i = k + 1; i < nt; ++i) {
-      const int t = tile_index(i, k);
-      const T* src = t % CL == rank ? tiles + (t / CL) * kTile
-                                    : cluster.map_shared_rank(tiles + (t / CL) * kTile, t % CL);
-      T* dst = panel + i * kTile;
-      for (int e = tid; e < kTile; e += kThreads) dst[e] = src[e];
+    cluster.sync();   // the panel tiles (i,k) are final
+    if constexpr (kStagePanel<T>) {
+      for (int i = k + 1; i < nt; ++i) {
+        const int t = tile_index(i, k);
+        const T* src = cluster.map_shared_rank(tiles + (t / CL) * kTile, t % CL);
+        for (int e = tid; e < kTile; e += kThreads) panel[i * kTile + e] = src[e];
+      }
+      __syncthreads();
+    }
+    // look-ahead: the next tile column first (one warp a tile) ...
+    if (k + 1 < nt) {
+      int q = 0;
+      for (int i = k + 1; i < nt; ++i) {
+        const int t = tile_index(i, k + 1);
+        if (t % CL != rank) continue;
+        if (q % kWarps == warp)
+          update_tile<T>(tiles + (t / CL) * kTile, panel_tile(i, k), panel_tile(k + 1, k), lane);
+        ++q;
+      }
     }
     __syncthreads();
-    // trailing tiles (i,j), k < j <= i: 4 x 4 elements a thread, 64 threads a tile
-    {
-      const int sub = tid >> 6;          // which of four tiles in flight
-      const int w = tid & 63;
-      const int r0 = (w >> 3) * 4, c0 = (w & 7) * 4;
+    // ... then the next diagonal tile is factored by warp 0 of its owner while every other
+    // warp applies this panel to the rest of the trailing tiles
+    const int tn = tile_index(k + 1, k + 1);
+    const bool diag_here = k + 1 < nt && tn % CL == rank;
+    if (diag_here && warp == 0) {
+      potrf_tile<T>(tiles + (tn / CL) * kTile, rc, k + 1, n, fail);
+    } else {
+      const int nw = diag_here ? kWarps - 1 : kWarps;
+      const int wi = diag_here ? warp - 1 : warp;
       int q = 0;
       for (int t = rank; t < ntiles; t += CL) {
-        int i = 0;
-        while (tile_index(i + 1, 0) <= t) ++i;
-        const int j = t - tile_index(i, 0);
-        if (j <= k) continue;
-        if ((q & 3) == sub) {
-          T* a = tiles + (t / CL) * kTile;
-          const T* li = panel + i * kTile;
-          const T* lj = panel + j * kTile;
-          T acc[4][4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) acc[u][v] = a[(r0 + u) * TP + c0 + v];
-#pragma unroll 4
-          for (int K = 0; K < TS; ++K) {
-            T x[4], y[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              x[u] = li[(r0 + u) * TP + K];
-              y[u] = lj[(c0 + u) * TP + K];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int v = 0; v < 4; ++v) acc[u][v] = fma_rn<T>(-x[u], y[v], acc[u][v]);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) a[(r0 + u) * TP + c0 + v] = acc[u][v];
-        }
+        int i, j;
+        tile_coords(t, i, j);
+        if (j <= k + 1) continue;
+        if (q % nw == wi)
+          update_tile<T>(tiles + (t / CL) * kTile, panel_tile(i, k), panel_tile(j, k), lane);
         ++q;
       }
     }
@@ -252,14 +302,14 @@ chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* 
 }
 
 // ------------------------------------------------------------------ solve, n > 128
-constexpr int RC = 8;   // right-hand sides a pass
-
 template <typename T>
-size_t big_solve_smem_bytes(int n) {
-  return static_cast<size_t>(n) * RC * sizeof(T) + static_cast<size_t>(n) * TP * sizeof(T);
+size_t big_solve_smem_bytes(int n, int rc) {
+  return static_cast<size_t>(n) * rc * sizeof(T) + static_cast<size_t>(n) * TP * sizeof(T);
 }
 
-template <typename T>
+// RC right-hand sides a pass (1, 2, 4 or 8: the call's count, up to 8), row-major in
+// shared memory; the diagonal reciprocals of a tile taken by its 32 lanes at once.
+template <typename T, int RC>
 __global__ void __launch_bounds__(kThreads)
 potrs_big_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restrict__ L,
                  T* __restrict__ B, const int32_t* __restrict__ zinfo) {
@@ -301,10 +351,12 @@ potrs_big_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restric
       if (tid < 32) {
         T v[RC];
         const bool own = lane < cols;
+        // y_K = b_K * (1/l_KK): the 32 reciprocals at once, one per lane
+        const T rmine = own ? T(1) / Ls[lane * TP + lane] : T(1);
 #pragma unroll
         for (int c = 0; c < RC; ++c) v[c] = own ? b[(r0 + lane) * RC + c] : T(0);
         for (int K = 0; K < cols; ++K) {
-          const T rk = T(1) / Ls[K * TP + K];
+          const T rk = __shfl_sync(0xFFFFFFFFu, rmine, K);
           if (lane == K) {
 #pragma unroll
             for (int c = 0; c < RC; ++c) v[c] = v[c] * rk;
@@ -322,9 +374,9 @@ potrs_big_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restric
         }
       }
       __syncthreads();
-      // the rows below: 32 updates each, in increasing K
-      for (int e = tid; e < (n - r0 - cols) * RC; e += kThreads) {
-        const int I = r0 + cols + e / RC, c = e % RC;
+      // the rows below: 32 updates each, in increasing K (only the call's columns)
+      for (int e = tid; e < (n - r0 - cols) * nc; e += kThreads) {
+        const int I = r0 + cols + e / nc, c = e % nc;
         T acc = b[I * RC + c];
         const T* lrow = Ls + (I - r0) * TP;
         for (int K = 0; K < cols; ++K) acc = fma_rn<T>(-lrow[K], b[(r0 + K) * RC + c], acc);
@@ -339,8 +391,8 @@ potrs_big_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restric
       const int r0 = k * TS;
       const int cols = n - r0 < TS ? n - r0 : TS;
       // the rows of this block first take the updates of the rows below, decreasing K
-      for (int e = tid; e < cols * RC; e += kThreads) {
-        const int J = e / RC, c = e % RC;
+      for (int e = tid; e < cols * nc; e += kThreads) {
+        const int J = e / nc, c = e % nc;
         T acc = b[(r0 + J) * RC + c];
         for (int K = n - 1; K >= r0 + cols; --K)
           acc = fma_rn<T>(-Ls[(K - r0) * TP + J], b[K * RC + c], acc);
@@ -350,10 +402,11 @@ potrs_big_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restric
       if (tid < 32) {
         T v[RC];
         const bool own = lane < cols;
+        const T rmine = own ? T(1) / Ls[lane * TP + lane] : T(1);
 #pragma unroll
         for (int c = 0; c < RC; ++c) v[c] = own ? b[(r0 + lane) * RC + c] : T(0);
         for (int K = cols - 1; K >= 0; --K) {
-          const T rk = T(1) / Ls[K * TP + K];
+          const T rk = __shfl_sync(0xFFFFFFFFu, rmine, K);
           if (lane == K) {
 #pragma unroll
             for (int c = 0; c < RC; ++c) v[c] = v[c] * rk;
@@ -378,6 +431,19 @@ potrs_big_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restric
     }
     __syncthreads();
   }
+}
+
+template <typename T, int RC>
+cudaError_t launch_big_rc(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
+                          const int32_t* zinfo, cudaStream_t stream) {
+  const size_t bytes = big_solve_smem_bytes<T>(n, RC);
+  cudaError_t e = cudaFuncSetAttribute(potrs_big_kernel<T, RC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  potrs_big_kernel<T, RC><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
+      n, nrhs, layout, batch, L, B, zinfo);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -414,14 +480,10 @@ cudaError_t launch_potrs_big(int layout, int n, int nrhs, int64_t batch, const T
                              const int32_t* zinfo, cudaStream_t stream) {
   if (n <= 128 || n > kMaxT * TS || nrhs < 1) return cudaErrorInvalidValue;
   if (batch > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  const size_t bytes = big_solve_smem_bytes<T>(n);
-  cudaError_t e = cudaFuncSetAttribute(potrs_big_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  potrs_big_kernel<T><<<static_cast<unsigned>(batch), kThreads, bytes, stream>>>(
-      n, nrhs, layout, batch, L, B, zinfo);
-  return cudaGetLastError();
+  if (nrhs == 1) return launch_big_rc<T, 1>(layout, n, nrhs, batch, L, B, zinfo, stream);
+  if (nrhs == 2) return launch_big_rc<T, 2>(layout, n, nrhs, batch, L, B, zinfo, stream);
+  if (nrhs <= 4) return launch_big_rc<T, 4>(layout, n, nrhs, batch, L, B, zinfo, stream);
+  return launch_big_rc<T, 8>(layout, n, nrhs, batch, L, B, zinfo, stream);
 }
 
 template cudaError_t launch_chol_cluster<float>(int, int, int64_t, float*, int32_t*,

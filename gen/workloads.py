@@ -64,6 +64,21 @@ WORKLOADS = {
 }
 
 
+# Inputs of rows measured beside the five workloads (not configurations of their own):
+# Cholesky beyond one CTA, with the recipe of chol_f64_n32 at a larger order.
+EXTRA_WORKLOADS = {
+    "chol_f64_n256": Workload(
+        "chol_f64_n256", "potrf_potrs", np.float64, 256, 1, 2048, COL_MAJOR, SEED_BASE + 5,
+        text="Cholesky FP64 n=256 nrhs=1 batch=2048 column-major lower; A = G G^T + 256 I, "
+             "G iid N(0,1); b iid N(0,1); 1% of systems get A[k][k] = -1"),
+}
+
+
+def workload(name: str) -> Workload:
+    """One of WORKLOADS or EXTRA_WORKLOADS by name."""
+    return WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name]
+
+
 def _rng(seed: int, stream: int, chunk: int) -> np.random.Generator:
     return np.random.default_rng([seed, stream, chunk])
 
@@ -134,7 +149,7 @@ def make(name: str, batch: int | None = None) -> dict:
     Returns a dict with "A", "B" (LU/Cholesky) or "strips", "x" (bdsv), and for
     workloads with planted failures the expected info codes of the planted systems.
     """
-    w = WORKLOADS[name]
+    w = workload(name)
     batch = w.batch if batch is None else int(batch)
     if w.op == "bdsv":
         return _make_bdsv(w, batch)
@@ -150,7 +165,7 @@ def make(name: str, batch: int | None = None) -> dict:
         elif name == "lu_f32_n16":
             A[lo:hi] = _rng(w.seed, 0, c).standard_normal((m, n, n), dtype=np.float32)
             B[lo:hi] = _rng(w.seed, 1, c).standard_normal((m, n, nrhs), dtype=np.float32)
-        elif name == "chol_f64_n32":
+        elif name in ("chol_f64_n32", "chol_f64_n256"):
             G = _rng(w.seed, 0, c).standard_normal((m, n, n))
             A[lo:hi] = _bmm(G, np.swapaxes(G, 1, 2)) + n * np.eye(n)
             B[lo:hi] = _rng(w.seed, 1, c).standard_normal((m, n, nrhs))

@@ -38,7 +38,7 @@ def test_every_bench_row_has_a_cost():
     interleaved layouts count the fused calls' bytes and flops (the same work)."""
     import bench
     for name, (base, op) in bench.NEXT_ROWS.items():
-        w = bench.W.WORKLOADS[base]
+        w = bench.W.workload(base)
         b, f = costs.per_system(op, w.n, w.nrhs, 4 if w.dtype.__name__ == "float32" else 8,
                                 w.nbr)
         assert b > 0 and f > 0, name

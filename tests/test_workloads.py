@@ -102,3 +102,18 @@ def test_bdsv_systems_are_spd_with_margin():
     assert np.all(lam[:, 0] >= 9.0)
     _, _, info = oracle.bdsv(S, x, nthreads=NT)
     assert np.all(info == 0)
+
+
+def test_extra_cholesky_workload_recipe():
+    """chol_f64_n256 (the row beyond one CTA): the chol_f64_n32 recipe at n = 256, a
+    prefix of the full batch, planted minors at their stated positions, SPD otherwise."""
+    d = W.make("chol_f64_n256", 40)
+    w = d["workload"]
+    assert w.n == 256 and w.nrhs == 1 and w.batch == 2048 and w.layout == W.COL_MAJOR
+    A = W.from_storage(d["A"], w.layout)
+    assert A.shape == (40, 256, 256) and np.allclose(A, np.swapaxes(A, 1, 2))
+    for s, k in d["planted_info"].items():
+        assert A[s, k - 1, k - 1] == -1.0
+    ok = [s for s in range(40) if s not in d["planted_info"]]
+    assert np.all(np.linalg.eigvalsh(A[ok]).min(axis=1) > 200)
+    assert np.array_equal(W.make("chol_f64_n256", 20)["A"], d["A"][:20])
