@@ -80,6 +80,12 @@ class Oracle:
         sig["getrf_getrs_il"] = [i32, i32, i32, i64, i64, vp, vp, vp, vp, vp, ctypes.c_double,
                                  i32, i32, i32]
         sig["potrf_potrs_il"] = [i32, i32, i32, i32, i64, i64, vp, vp, vp, i32, i32]
+        sig["getrf_getrs_mirror_ex"] = [i32, i32, i32, i64, i64, vp, vp, vp, vp, vp,
+                                        ctypes.c_double, i32, i32]
+        sig["getrf_il"] = [i32, i32, i64, i64, vp, vp, vp, vp, i32]
+        sig["getrs_il"] = [i32, i32, i32, i64, i64, vp, vp, vp, i32]
+        sig["potrf_il"] = [i32, i32, i32, i64, i64, vp, vp, i32]
+        sig["potrs_il"] = [i32, i32, i32, i32, i64, i64, vp, vp, i32]
         for op, args in sig.items():
             for sfx in ("f32", "f64"):
                 fn = getattr(lib, f"oracle_{op}_{sfx}")
@@ -249,10 +255,11 @@ class Oracle:
         return A, B, info
 
     def getrf_getrs_mirror(self, A, B, layout: int = ROW_MAJOR, tau: float = 1.0,
-                           nthreads: int = 1):
+                           nthreads: int = 1, scale: int = 0):
         """TDLS row-major reading: factor S (the stored array read column-major, S = A^T for
-        row-major storage), then U^T z = b, L^T w = z, x = P^T w. Returns
-        (S factored in the stored array, X, ipiv, info, tie_step)."""
+        row-major storage), then U^T z = b, L^T w = z, x = P^T w; scale: RUDA's max-abs
+        scaling of the factorization. Returns (S factored in the stored array, X, ipiv,
+        info, tie_step)."""
         A = np.ascontiguousarray(A).copy()
         B = np.ascontiguousarray(B, dtype=A.dtype).copy()
         batch, n = A.shape[0], A.shape[1]
@@ -260,9 +267,9 @@ class Oracle:
         ipiv = np.zeros((batch, n), np.int32)
         info = np.zeros(batch, np.int32)
         tie = np.zeros(batch, np.int32)
-        fn = getattr(self.lib, "oracle_getrf_getrs_mirror_" + _suffix(A.dtype))
-        if fn(layout, n, nrhs, batch, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
-              float(tau), nthreads) != 0:
+        fn = getattr(self.lib, "oracle_getrf_getrs_mirror_ex_" + _suffix(A.dtype))
+        if fn(layout, n, nrhs, batch, 1, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
+              float(tau), int(scale), nthreads) != 0:
             raise ValueError("oracle getrf_getrs_mirror rejected its arguments")
         return A, B, ipiv, info, tie
 
@@ -288,6 +295,71 @@ class Oracle:
               float(tau), int(ruda), int(scale), nthreads) != 0:
             raise ValueError("oracle getrf_getrs_il rejected its arguments")
         return A, B, ipiv, info, tie
+
+    def getrf_getrs_mirror_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
+                              layout: int = ROW_MAJOR, tau: float = 1.0, scale: int = 0,
+                              nthreads: int = 1):
+        """The row-major reading (getrf_getrs_mirror) on interleaved batched storage (see
+        getrf_getrs_il). Returns (A, B, ipiv, info, tie_step), ipiv flat and interleaved."""
+        A = np.ascontiguousarray(A).reshape(-1).copy()
+        B = np.ascontiguousarray(B, dtype=A.dtype).reshape(-1).copy()
+        nb = -(-batch // w) if batch else 0
+        if A.size < nb * w * n * n or B.size < nb * w * n * nrhs:
+            raise ValueError("interleaved buffers too small")
+        ipiv = np.zeros(max(nb * w * n, 1), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_getrs_mirror_ex_" + _suffix(A.dtype))
+        if fn(layout, n, nrhs, batch, w, _ptr(A), _ptr(B), _ptr(ipiv), _ptr(info), _ptr(tie),
+              float(tau), int(scale), nthreads) != 0:
+            raise ValueError("oracle getrf_getrs_mirror rejected its arguments")
+        return A, B, ipiv, info, tie
+
+    def getrf_il(self, A, n: int, batch: int, w: int, layout: int = ROW_MAJOR,
+                 nthreads: int = 1):
+        """getrf on interleaved storage. Returns (A, ipiv, info, tie_step)."""
+        A = np.ascontiguousarray(A).reshape(-1).copy()
+        nb = -(-batch // w) if batch else 0
+        if A.size < nb * w * n * n:
+            raise ValueError("interleaved buffers too small")
+        ipiv = np.zeros(max(nb * w * n, 1), np.int32)
+        info = np.zeros(batch, np.int32)
+        tie = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_getrf_il_" + _suffix(A.dtype))
+        if fn(layout, n, batch, w, _ptr(A), _ptr(ipiv), _ptr(info), _ptr(tie), nthreads) != 0:
+            raise ValueError("oracle getrf_il rejected its arguments")
+        return A, ipiv, info, tie
+
+    def getrs_il(self, LU, ipiv, B, n: int, nrhs: int, batch: int, w: int,
+                 layout: int = ROW_MAJOR, nthreads: int = 1):
+        """getrs on interleaved storage (LU and ipiv as getrf_il leaves them). Returns B."""
+        LU = np.ascontiguousarray(LU).reshape(-1)
+        ipiv = np.ascontiguousarray(ipiv, dtype=np.int32).reshape(-1)
+        B = np.ascontiguousarray(B, dtype=LU.dtype).reshape(-1).copy()
+        fn = getattr(self.lib, "oracle_getrs_il_" + _suffix(LU.dtype))
+        if fn(layout, n, nrhs, batch, w, _ptr(LU), _ptr(ipiv), _ptr(B), nthreads) != 0:
+            raise ValueError("oracle getrs_il rejected its arguments")
+        return B
+
+    def potrf_il(self, A, n: int, batch: int, w: int, layout: int = COL_MAJOR,
+                 fill: int = LOWER, nthreads: int = 1):
+        """potrf on interleaved storage. Returns (A, info)."""
+        A = np.ascontiguousarray(A).reshape(-1).copy()
+        info = np.zeros(batch, np.int32)
+        fn = getattr(self.lib, "oracle_potrf_il_" + _suffix(A.dtype))
+        if fn(layout, fill, n, batch, w, _ptr(A), _ptr(info), nthreads) != 0:
+            raise ValueError("oracle potrf_il rejected its arguments")
+        return A, info
+
+    def potrs_il(self, L, B, n: int, nrhs: int, batch: int, w: int, layout: int = COL_MAJOR,
+                 fill: int = LOWER, nthreads: int = 1):
+        """potrs on interleaved storage. Returns B."""
+        L = np.ascontiguousarray(L).reshape(-1)
+        B = np.ascontiguousarray(B, dtype=L.dtype).reshape(-1).copy()
+        fn = getattr(self.lib, "oracle_potrs_il_" + _suffix(L.dtype))
+        if fn(layout, fill, n, nrhs, batch, w, _ptr(L), _ptr(B), nthreads) != 0:
+            raise ValueError("oracle potrs_il rejected its arguments")
+        return B
 
     def potrf_potrs_il(self, A, B, n: int, nrhs: int, batch: int, w: int,
                        layout: int = COL_MAJOR, fill: int = LOWER, nthreads: int = 1,
@@ -365,8 +437,31 @@ def potrf_potrs_ex(A, B, layout: int = COL_MAJOR, fill: int = LOWER, ruda: int =
     return default().potrf_potrs_ex(A, B, layout, fill, ruda, nthreads)
 
 
-def getrf_getrs_mirror(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, nthreads: int = 1):
-    return default().getrf_getrs_mirror(A, B, layout, tau, nthreads)
+def getrf_getrs_mirror(A, B, layout: int = ROW_MAJOR, tau: float = 1.0, nthreads: int = 1,
+                       scale: int = 0):
+    return default().getrf_getrs_mirror(A, B, layout, tau, nthreads, scale)
+
+
+def getrf_getrs_mirror_il(A, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, tau: float = 1.0,
+                          scale: int = 0, nthreads: int = 1):
+    return default().getrf_getrs_mirror_il(A, B, n, nrhs, batch, w, layout, tau, scale, nthreads)
+
+
+def getrf_il(A, n, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1):
+    return default().getrf_il(A, n, batch, w, layout, nthreads)
+
+
+def getrs_il(LU, ipiv, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1):
+    return default().getrs_il(LU, ipiv, B, n, nrhs, batch, w, layout, nthreads)
+
+
+def potrf_il(A, n, batch, w, layout: int = COL_MAJOR, fill: int = LOWER, nthreads: int = 1):
+    return default().potrf_il(A, n, batch, w, layout, fill, nthreads)
+
+
+def potrs_il(L, B, n, nrhs, batch, w, layout: int = COL_MAJOR, fill: int = LOWER,
+             nthreads: int = 1):
+    return default().potrs_il(L, B, n, nrhs, batch, w, layout, fill, nthreads)
 
 
 def getrf_getrs_il(A, B, n, nrhs, batch, w, layout: int = ROW_MAJOR, nthreads: int = 1,

@@ -682,32 +682,21 @@ int getrf_getrs_ex_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* 
   return 0;
 }
 
+// [TDLS] row-major reading, one system: factor S (the stored array read column-major,
+// S = A^T for row-major storage) in place, then U^T z = b, L^T w = z, x = P^T w; X zeros
+// when the factor failed. Column-major storage: S = A and the solve is the default one.
+// scale: RUDA's max-abs scaling of the factorization (U restored before the solve).
 template <typename T>
-int getrf_getrs_mirror_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
-                               int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
-                               int nthreads) {
-  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || !(tau > 0.0) ||
-      !(tau <= 1.0))
-    return 1;
-  const T t = static_cast<T>(tau);
-  for_systems(batch, nthreads, [&](int64_t s) {
-    T* As = A + s * n * n;
-    T* Bs = B + s * n * nrhs;
-    int32_t* inf = info + s;
-    if (layout == 1) {
-      // column-major storage: S = A and the solve is the default one
-      getrf_getrs_ex_one<T>(1, n, nrhs, As, Bs, ipiv + s * n, inf,
-                            tie_step ? tie_step + s : nullptr, t, 0);
-      return;
-    }
-    // S = the stored array read column-major (A^T), factored in place; B row-major
-    getrf_getrs_ex_one<T>(1, n, 0, As, nullptr, ipiv + s * n, inf,
-                          tie_step ? tie_step + s : nullptr, t, 0);
-    getrs_mirror_one<T>(layout, n, nrhs, As, ipiv + s * n, Bs);
-    if (*inf != 0)
-      for (int i = 0; i < n * nrhs; ++i) Bs[i] = T(0);
-  });
-  return 0;
+void mirror_one(int layout, int n, int nrhs, T* As, T* Bs, int32_t* ipiv, int32_t* inf,
+                int32_t* tie, T t, int scale) {
+  if (layout == 1) {
+    getrf_getrs_ex_one<T>(1, n, nrhs, As, Bs, ipiv, inf, tie, t, 0, scale);
+    return;
+  }
+  getrf_getrs_ex_one<T>(1, n, 0, As, nullptr, ipiv, inf, tie, t, 0, scale);
+  getrs_mirror_one<T>(layout, n, nrhs, As, ipiv, Bs);
+  if (*inf != 0)
+    for (int i = 0; i < n * nrhs; ++i) Bs[i] = T(0);
 }
 
 template <typename T>
@@ -747,6 +736,110 @@ struct Strided {
     for (int64_t e = 0; e < size; ++e) b[e * w] = src[e];
   }
 };
+
+template <typename T>
+int getrf_getrs_mirror_batched(int layout, int n, int nrhs, int64_t batch, T* A, T* B,
+                               int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
+                               int nthreads, int64_t w, int scale) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || !(tau > 0.0) ||
+      !(tau <= 1.0) || w < 1)
+    return 1;
+  const T t = static_cast<T>(tau);
+  if (w == 1) {
+    for_systems(batch, nthreads, [&](int64_t s) {
+      mirror_one<T>(layout, n, nrhs, A + s * n * n, B + s * n * nrhs, ipiv + s * n, info + s,
+                    tie_step ? tie_step + s : nullptr, t, scale);
+    });
+    return 0;
+  }
+  // [TDLS] interleaved batched layout: each system gathered, solved and scattered back
+  const Strided<T> a{A, w, (int64_t)n * n}, b{B, w, (int64_t)n * nrhs};
+  const Strided<int32_t> pv{ipiv, w, n};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size), bs(b.size);
+    std::vector<int32_t> ps(n);
+    a.gather(s, as.data());
+    b.gather(s, bs.data());
+    mirror_one<T>(layout, n, nrhs, as.data(), bs.data(), ps.data(), info + s,
+                  tie_step ? tie_step + s : nullptr, t, scale);
+    a.scatter(s, as.data());
+    b.scatter(s, bs.data());
+    pv.scatter(s, ps.data());
+  });
+  return 0;
+}
+
+// [TDLS] the separate factor and substitution steps on the interleaved batched layouts:
+// the per-system getrf / getrs / potrf / potrs between a gather and a scatter.
+template <typename T>
+int getrf_il_batched(int layout, int n, int64_t batch, int64_t w, T* A, int32_t* ipiv,
+                     int32_t* info, int32_t* tie_step, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || batch < 0 || w < 1) return 1;
+  const Strided<T> a{A, w, (int64_t)n * n};
+  const Strided<int32_t> pv{ipiv, w, n};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size);
+    std::vector<int32_t> ps(n);
+    a.gather(s, as.data());
+    getrf_getrs_one<T>(layout, n, 0, as.data(), nullptr, ps.data(), info + s,
+                       tie_step ? tie_step + s : nullptr);
+    a.scatter(s, as.data());
+    pv.scatter(s, ps.data());
+  });
+  return 0;
+}
+
+template <typename T>
+int getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w, const T* LU,
+                     const int32_t* ipiv, T* B, int nthreads) {
+  if ((layout != 0 && layout != 1) || n < 1 || nrhs < 1 || batch < 0 || w < 1) return 1;
+  const Strided<T> a{const_cast<T*>(LU), w, (int64_t)n * n}, b{B, w, (int64_t)n * nrhs};
+  const Strided<int32_t> pv{const_cast<int32_t*>(ipiv), w, n};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size), bs(b.size);
+    std::vector<int32_t> ps(n);
+    a.gather(s, as.data());
+    pv.gather(s, ps.data());
+    b.gather(s, bs.data());
+    getrs_one<T>(layout, n, nrhs, as.data(), ps.data(), bs.data());
+    b.scatter(s, bs.data());
+  });
+  return 0;
+}
+
+template <typename T>
+int potrf_il_batched(int layout, int fill, int n, int64_t batch, int64_t w, T* A,
+                     int32_t* info, int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || batch < 0 || w < 1)
+    return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
+  const Strided<T> a{A, w, (int64_t)n * n};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size);
+    a.gather(s, as.data());
+    potrf_potrs_one<T>(a_layout, layout, n, 0, as.data(), nullptr, info + s);
+    a.scatter(s, as.data());
+  });
+  return 0;
+}
+
+template <typename T>
+int potrs_il_batched(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
+                     const T* L, T* B, int nthreads) {
+  if ((layout != 0 && layout != 1) || (fill != 0 && fill != 1) || n < 1 || nrhs < 1 ||
+      batch < 0 || w < 1)
+    return 1;
+  const int a_layout = fill == 0 ? layout : 1 - layout;
+  const Strided<T> a{const_cast<T*>(L), w, (int64_t)n * n}, b{B, w, (int64_t)n * nrhs};
+  for_systems(batch, nthreads, [&](int64_t s) {
+    std::vector<T> as(a.size), bs(b.size);
+    a.gather(s, as.data());
+    b.gather(s, bs.data());
+    potrs_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data());
+    b.scatter(s, bs.data());
+  });
+  return 0;
+}
 
 template <typename T>
 int getrf_getrs_il_batched(int layout, int n, int nrhs, int64_t batch, int64_t w, T* A, T* B,
@@ -898,13 +991,13 @@ int oracle_getrf_getrs_mirror_f32(int layout, int n, int nrhs, int64_t batch, fl
                                   int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
                                   int nthreads) {
   return getrf_getrs_mirror_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
-                                         nthreads);
+                                         nthreads, 1, 0);
 }
 int oracle_getrf_getrs_mirror_f64(int layout, int n, int nrhs, int64_t batch, double* A, double* B,
                                   int32_t* ipiv, int32_t* info, int32_t* tie_step, double tau,
                                   int nthreads) {
   return getrf_getrs_mirror_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
-                                         nthreads);
+                                         nthreads, 1, 0);
 }
 int oracle_getrf_getrs_il_f32(int layout, int n, int nrhs, int64_t batch, int64_t w, float* A,
                               float* B, int32_t* ipiv, int32_t* info, int32_t* tie_step,
@@ -927,6 +1020,51 @@ int oracle_potrf_potrs_il_f64(int layout, int fill, int n, int nrhs, int64_t bat
                               double* A, double* B, int32_t* info, int ruda, int nthreads) {
   return potrf_potrs_il_batched<double>(layout, fill, n, nrhs, batch, w, A, B, info, ruda,
                                      nthreads);
+}
+
+int oracle_getrf_getrs_mirror_ex_f32(int layout, int n, int nrhs, int64_t batch, int64_t w,
+                                     float* A, float* B, int32_t* ipiv, int32_t* info,
+                                     int32_t* tie_step, double tau, int scale, int nthreads) {
+  return getrf_getrs_mirror_batched<float>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step, tau,
+                                         nthreads, w, scale);
+}
+int oracle_getrf_getrs_mirror_ex_f64(int layout, int n, int nrhs, int64_t batch, int64_t w,
+                                     double* A, double* B, int32_t* ipiv, int32_t* info,
+                                     int32_t* tie_step, double tau, int scale, int nthreads) {
+  return getrf_getrs_mirror_batched<double>(layout, n, nrhs, batch, A, B, ipiv, info, tie_step,
+                                          tau, nthreads, w, scale);
+}
+int oracle_getrf_il_f32(int layout, int n, int64_t batch, int64_t w, float* A, int32_t* ipiv,
+                        int32_t* info, int32_t* tie_step, int nthreads) {
+  return getrf_il_batched<float>(layout, n, batch, w, A, ipiv, info, tie_step, nthreads);
+}
+int oracle_getrf_il_f64(int layout, int n, int64_t batch, int64_t w, double* A, int32_t* ipiv,
+                        int32_t* info, int32_t* tie_step, int nthreads) {
+  return getrf_il_batched<double>(layout, n, batch, w, A, ipiv, info, tie_step, nthreads);
+}
+int oracle_getrs_il_f32(int layout, int n, int nrhs, int64_t batch, int64_t w, const float* LU,
+                        const int32_t* ipiv, float* B, int nthreads) {
+  return getrs_il_batched<float>(layout, n, nrhs, batch, w, LU, ipiv, B, nthreads);
+}
+int oracle_getrs_il_f64(int layout, int n, int nrhs, int64_t batch, int64_t w, const double* LU,
+                        const int32_t* ipiv, double* B, int nthreads) {
+  return getrs_il_batched<double>(layout, n, nrhs, batch, w, LU, ipiv, B, nthreads);
+}
+int oracle_potrf_il_f32(int layout, int fill, int n, int64_t batch, int64_t w, float* A,
+                        int32_t* info, int nthreads) {
+  return potrf_il_batched<float>(layout, fill, n, batch, w, A, info, nthreads);
+}
+int oracle_potrf_il_f64(int layout, int fill, int n, int64_t batch, int64_t w, double* A,
+                        int32_t* info, int nthreads) {
+  return potrf_il_batched<double>(layout, fill, n, batch, w, A, info, nthreads);
+}
+int oracle_potrs_il_f32(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
+                        const float* L, float* B, int nthreads) {
+  return potrs_il_batched<float>(layout, fill, n, nrhs, batch, w, L, B, nthreads);
+}
+int oracle_potrs_il_f64(int layout, int fill, int n, int nrhs, int64_t batch, int64_t w,
+                        const double* L, double* B, int nthreads) {
+  return potrs_il_batched<double>(layout, fill, n, nrhs, batch, w, L, B, nthreads);
 }
 
 }  // extern "C"

@@ -987,13 +987,126 @@ def pin_ruda_scaling(orc):
         assert r[3][0] == -1 and np.all(r[2] == -1)
 
 
+def pin_mirror_scaling(orc):
+    """The row-major reading (S = A^T, the stored row-major array read column-major) with
+    RUDA's max-abs scaling: a maximum that is a power of two divides and multiplies back
+    exactly, so the result is the unscaled reading's bit for bit; for any other maximum
+    the stored factor reconstructs P S = L U with the restored U, and X solves A x = b to
+    the backward-error bound; column-major storage (S = A) is the plain scaled call."""
+    rng = _rng(93)
+    for dt in (np.float32, np.float64):
+        eps = eps_of(dt)
+        for n, nrhs in ((1, 1), (5, 2), (16, 4), (33, 3)):
+            Al = rng.uniform(-1, 1, (4, n, n)).astype(dt)
+            Al[0, n - 1, 0] = 4.0
+            Al[1] *= dt(2.0 ** -5)
+            Al[1, 0, n - 1] = -dt(2.0 ** -4)
+            Al[2, 0, 0] = -dt(2.0 ** 20)
+            A = to_storage(Al[:3], ROW_MAJOR)
+            B = rng.standard_normal((3, n, nrhs)).astype(dt)
+            for tau in (1.0, 0.5):
+                r0 = orc.getrf_getrs_mirror(A, B, ROW_MAJOR, tau=tau)
+                r1 = orc.getrf_getrs_mirror(A, B, ROW_MAJOR, tau=tau, scale=1)
+                assert all(np.array_equal(x, y) for x, y in zip(r0, r1)), (n, tau)
+            Ag = rng.uniform(-1, 1, (6, n, n)).astype(dt) * dt(3.7)
+            Bg = rng.standard_normal((6, n, nrhs)).astype(dt)
+            F, X, ipiv, info, _ = orc.getrf_getrs_mirror(Ag, Bg, ROW_MAJOR, scale=1)
+            ok = info == 0
+            assert ok.sum() >= 4
+            be = backward_error(Ag[ok].astype(np.float64), X[ok], Bg[ok])
+            assert np.all(be <= 8 * n * eps), be
+            for sidx in np.nonzero(ok)[0]:
+                S = np.swapaxes(Ag[sidx], 0, 1).astype(np.float64)   # A^T
+                L, U = unpack_lu(np.swapaxes(F[sidx], 0, 1))           # the factor of S
+                nS = np.abs(S).sum(axis=1).max()
+                assert np.abs(S[lapack_perm(ipiv[sidx])] - L @ U).max() <= 4 * n * eps * nS
+            Ac = to_storage(Ag, COL_MAJOR)
+            Bc = to_storage(Bg, COL_MAJOR)
+            rc = orc.getrf_getrs_mirror(Ac, Bc, COL_MAJOR, scale=1)
+            rd = orc.getrf_getrs_ex(Ac, Bc, COL_MAJOR, scale=1)
+            assert all(np.array_equal(x, y) for x, y in zip(rc, rd))
+        # worked by hand: A = s I with s subnormal. Unscaled, the first pivot is below the
+        # smallest normal: info = 1, X = 0. Scaled, the sweep sees I (info = 0), U = s I is
+        # restored, and its subnormal diagonal takes the reciprocal 1: z = b, w = z, x = b.
+        sub = np.finfo(dt).smallest_subnormal * 8
+        As = np.array([[[sub, 0.0], [0.0, sub]]], dt)
+        Bs = np.array([[[3.0], [-5.0]]], dt)
+        _, X0, _, info0, _ = orc.getrf_getrs_mirror(As, Bs, ROW_MAJOR)
+        assert info0[0] == 1 and np.all(X0 == 0)
+        _, X1, ip1, info1, _ = orc.getrf_getrs_mirror(As, Bs, ROW_MAJOR, scale=1)
+        assert info1[0] == 0 and np.array_equal(X1, Bs) and list(ip1[0]) == [1, 2]
+
+
+def pin_interleaved_split_and_mirror(orc):
+    """TDLS batched layouts on the separate factor and solve steps and on the row-major
+    reading. Literal 1x1 systems in blocks of two (the last block ragged): getrf leaves
+    a = (2, 4 | 0.5) with ipiv 1, getrs gives x = b / a = (0.5, 0.75 | 10); potrf gives
+    l = (2, 4 | 0.5) for a = (4, 16 | 0.25), potrs x = b (1/l)(1/l) = (0.5, 0.5 | 4); the
+    pads never written. Then random systems: every interleaved driver equals its
+    per-system driver on the same systems bit for bit (AoS, ragged AoSoA, SoA, SoA with
+    spare capacity, both storage orders, both fills, a threshold and the scaling for the
+    row-major reading), and getrf then getrs equals the fused interleaved call."""
+    nan = np.nan
+    F, p, info, _ = orc.getrf_il(np.array([2.0, 4.0, 0.5, nan]), 1, 3, 2)
+    assert np.array_equal(F[:3], [2.0, 4.0, 0.5]) and np.isnan(F[3])
+    assert list(p[:3]) == [1, 1, 1] and list(info) == [0, 0, 0]
+    X = orc.getrs_il(F, p, np.array([1.0, 3.0, 5.0, nan]), 1, 1, 3, 2)
+    assert np.array_equal(X[:3], [0.5, 0.75, 10.0]) and np.isnan(X[3])
+    L, infc = orc.potrf_il(np.array([4.0, 16.0, 0.25, nan]), 1, 3, 2)
+    assert np.array_equal(L[:3], [2.0, 4.0, 0.5]) and np.isnan(L[3]) and list(infc) == [0] * 3
+    Xc = orc.potrs_il(L, np.array([2.0, 8.0, 1.0, nan]), 1, 1, 3, 2)
+    assert np.array_equal(Xc[:3], [0.5, 0.5, 4.0]) and np.isnan(Xc[3])
+    rng = _rng(94)
+    for dt in (np.float32, np.float64):
+        for (n, nrhs, batch, w) in [(5, 2, 7, 1), (5, 2, 7, 3), (5, 2, 7, 7), (4, 1, 6, 16),
+                                    (16, 4, 33, 32), (33, 2, 5, 2)]:
+            for layout in (ROW_MAJOR, COL_MAJOR):
+                Al = rng.standard_normal((batch, n, n)).astype(dt)
+                Al[1, :, 0] = 0
+                A = to_storage(Al, layout)
+                B = to_storage(rng.standard_normal((batch, n, nrhs)).astype(dt), layout)
+                di = lambda f, shape: deinterleave(f, batch, w, shape)   # noqa: E731
+                LUo, ipo, info_o, tie_o = orc.getrf(A, layout)
+                LUi, ipi, infi, tiei = orc.getrf_il(interleave(A, w), n, batch, w, layout)
+                assert np.array_equal(di(LUi, A.shape[1:]), LUo)
+                assert np.array_equal(di(ipi, (n,)), ipo) and np.array_equal(infi, info_o)
+                assert np.array_equal(tiei, tie_o)
+                assert np.all(np.isnan(LUi[np.isnan(interleave(A, w))]))
+                Xo = orc.getrs(LUo, ipo, B, layout)
+                Xi = orc.getrs_il(LUi, ipi, interleave(B, w), n, nrhs, batch, w, layout)
+                assert np.array_equal(di(Xi, B.shape[1:]), Xo)
+                fused = orc.getrf_getrs_il(interleave(A, w), interleave(B, w), n, nrhs, batch,
+                                           w, layout)
+                ok = info_o == 0
+                assert np.array_equal(di(fused[1], B.shape[1:])[ok], Xo[ok])
+                for tau, scale in ((1.0, 0), (0.5, 0), (1.0, 1)):
+                    mo = orc.getrf_getrs_mirror(A, B, layout, tau=tau, scale=scale)
+                    mi = orc.getrf_getrs_mirror_il(interleave(A, w), interleave(B, w), n, nrhs,
+                                                   batch, w, layout, tau=tau, scale=scale)
+                    assert np.array_equal(di(mi[0], A.shape[1:]), mo[0])
+                    assert np.array_equal(di(mi[1], B.shape[1:]), mo[1])
+                    assert np.array_equal(di(mi[2], (n,)), mo[2])
+                    assert np.array_equal(mi[3], mo[3]) and np.array_equal(mi[4], mo[4])
+                G = rng.standard_normal((batch, n, n))
+                Sl = (G @ np.swapaxes(G, 1, 2) + n * np.eye(n)).astype(dt)
+                Sl[2 % batch, n - 1, n - 1] = -1.0
+                for fill in (0, 1):
+                    Sa = to_storage(Sl, layout)
+                    Lo, io = orc.potrf(Sa, layout, fill=fill)
+                    Li, ii = orc.potrf_il(interleave(Sa, w), n, batch, w, layout, fill)
+                    assert np.array_equal(di(Li, Sa.shape[1:]), Lo) and np.array_equal(ii, io)
+                    Xo = orc.potrs(Lo, B, layout, fill=fill)
+                    Xi = orc.potrs_il(Li, interleave(B, w), n, nrhs, batch, w, layout, fill)
+                    assert np.array_equal(di(Xi, B.shape[1:]), Xo)
+
+
 SPLIT_PINS = [pin_getrs_composition, pin_getrs_permutation_only, pin_getrs_cramer,
               pin_potrs_composition, pin_potrs_diagonal, pin_potrs_dense, pin_bdsv_split]
 BDMV_PINS = [pin_bdmv_exact_integers, pin_bdmv_dense, pin_bdmv_inverts_bdsv]
 VARIANT_PINS = [pin_threshold_pivoting, pin_ruda_status_lu, pin_ruda_status_chol,
-                pin_tdls_row_major_reading, pin_ruda_scaling]
+                pin_tdls_row_major_reading, pin_ruda_scaling, pin_mirror_scaling]
 LAYOUT_PINS = [pin_interleaved_literal, pin_interleaved_layouts,
-               pin_interleaved_contract_options]
+               pin_interleaved_contract_options, pin_interleaved_split_and_mirror]
 ALL_PINS = (LU_PINS + CHOL_PINS + BDSV_PINS + SPLIT_PINS + BDMV_PINS + VARIANT_PINS +
             LAYOUT_PINS)
 

@@ -128,8 +128,15 @@ MUTATIONS = [
      "T* base(int64_t s) const { return p + (s / w) * size + s % w; }"),
     ("il_gather_contiguous", "for (int64_t e = 0; e < size; ++e) dst[e] = b[e * w];",
      "for (int64_t e = 0; e < size; ++e) dst[e] = b[e];"),
-    ("il_ipiv_not_interleaved", "    pv.scatter(s, ps.data());",
-     "    for (int k = 0; k < n; ++k) ipiv[s * n + k] = ps[k];"),
+    ("il_ipiv_not_interleaved",
+     "                          tie_step ? tie_step + s : nullptr, t, ruda, scale);\n    a.scatter(s, as.data());\n    b.scatter(s, bs.data());\n    pv.scatter(s, ps.data());",
+     "                          tie_step ? tie_step + s : nullptr, t, ruda, scale);\n    a.scatter(s, as.data());\n    b.scatter(s, bs.data());\n    for (int k = 0; k < n; ++k) ipiv[s * n + k] = ps[k];"),
+    ("getrf_il_ipiv_not_interleaved",
+     "                       tie_step ? tie_step + s : nullptr);\n    a.scatter(s, as.data());\n    pv.scatter(s, ps.data());",
+     "                       tie_step ? tie_step + s : nullptr);\n    a.scatter(s, as.data());\n    for (int k = 0; k < n; ++k) ipiv[s * n + k] = ps[k];"),
+    ("mirror_il_ipiv_not_interleaved",
+     "                  tie_step ? tie_step + s : nullptr, t, scale);\n    a.scatter(s, as.data());\n    b.scatter(s, bs.data());\n    pv.scatter(s, ps.data());",
+     "                  tie_step ? tie_step + s : nullptr, t, scale);\n    a.scatter(s, as.data());\n    b.scatter(s, bs.data());\n    for (int k = 0; k < n; ++k) ipiv[s * n + k] = ps[k];"),
     ("il_chol_fill_ignored",
      "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);",
      "    potrf_potrs_ex_one<T>(layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);"),
@@ -139,6 +146,20 @@ MUTATIONS = [
     ("il_chol_contract_dropped",
      "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, ruda);",
      "    potrf_potrs_ex_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data(), info + s, 0);"),
+    ("mirror_scaling_dropped",
+     "  getrf_getrs_ex_one<T>(1, n, 0, As, nullptr, ipiv, inf, tie, t, 0, scale);",
+     "  getrf_getrs_ex_one<T>(1, n, 0, As, nullptr, ipiv, inf, tie, t, 0, 0);"),
+    ("mirror_failed_x_not_zeroed",
+     "  getrs_mirror_one<T>(layout, n, nrhs, As, ipiv, Bs);\n  if (*inf != 0)\n    for (int i = 0; i < n * nrhs; ++i) Bs[i] = T(0);",
+     "  getrs_mirror_one<T>(layout, n, nrhs, As, ipiv, Bs);"),
+    ("getrs_il_pivots_not_gathered", "    pv.gather(s, ps.data());",
+     "    for (int k = 0; k < n; ++k) ps[k] = ipiv[s * n + k];"),
+    ("potrf_il_fill_ignored",
+     "    potrf_potrs_one<T>(a_layout, layout, n, 0, as.data(), nullptr, info + s);",
+     "    potrf_potrs_one<T>(layout, layout, n, 0, as.data(), nullptr, info + s);"),
+    ("potrs_il_fill_ignored",
+     "    potrs_one<T>(a_layout, layout, n, nrhs, as.data(), bs.data());",
+     "    potrs_one<T>(layout, layout, n, nrhs, as.data(), bs.data());"),
     ("scaling_u_not_restored", "      for (int j = k; j < n; ++j) a(k, j) = a(k, j) * msc;   // U's scale restored",
      "      for (int j = k; j < n; ++j) a(k, j) = a(k, j);   // U's scale restored"),
     ("scaling_restores_l_too", "      for (int j = k; j < n; ++j) a(k, j) = a(k, j) * msc;   // U's scale restored",
