@@ -42,6 +42,7 @@ EXPORTED = (
     "bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched", "bs_potrs_batched",
     "bs_bdsv_factor_batched", "bs_bdsv_solve_batched", "bs_bdmv_batched", "bs_bdmv2_batched",
     "bs_getrf_getrs_batched_ex", "bs_potrf_potrs_batched_ex",
+    "bs_getrf_batched_ex", "bs_getrs_batched_ex", "bs_potrf_batched_ex", "bs_potrs_batched_ex",
     "bs_getrf_getrs_host_workspace", "bs_getrf_getrs_batched_host",
     "bs_potrf_potrs_host_workspace", "bs_potrf_potrs_batched_host",
     "bs_bdsv_host_workspace", "bs_bdsv_batched_host", "bs_getrf_getrs_batched_host_static",
@@ -93,6 +94,14 @@ def lib() -> ctypes.CDLL:
                                                     ctypes.POINTER(Options), vp]
             L.bs_getrf_getrs_batched_ex.restype = i32
             L.bs_potrf_potrs_batched_ex.restype = i32
+            opt = ctypes.POINTER(Options)
+            L.bs_getrf_batched_ex.argtypes = [i32, i32, i32, i64, vp, vp, vp, opt, vp]
+            L.bs_getrs_batched_ex.argtypes = [i32, i32, i32, i32, i64, vp, vp, vp, opt, vp]
+            L.bs_potrf_batched_ex.argtypes = [i32, i32, i32, i32, i64, vp, vp, opt, vp]
+            L.bs_potrs_batched_ex.argtypes = [i32, i32, i32, i32, i32, i64, vp, vp, opt, vp]
+            for f in ("bs_getrf_batched_ex", "bs_getrs_batched_ex", "bs_potrf_batched_ex",
+                      "bs_potrs_batched_ex"):
+                getattr(L, f).restype = i32
             for name in ("bs_getrf_batched", "bs_getrs_batched", "bs_potrf_batched",
                          "bs_potrs_batched", "bs_bdsv_factor_batched", "bs_bdsv_solve_batched",
                          "bs_bdmv_batched", "bs_bdmv2_batched"):
@@ -362,6 +371,63 @@ def bs_potrf_potrs_batched_ex(A, B, info, layout: int = COL_MAJOR, fill: int = B
     st = lib().bs_potrf_potrs_batched_ex(_dtype_code(A), layout, fill, n, nrhs, batch, _ptr(A),
                                          _ptr(B), _ptr(info), ctypes.byref(opts), _stream(stream))
     _check(st, "bs_potrf_potrs_batched_ex")
+
+
+def _factor_shape(shape):
+    # a factor call's interleaved shape: (batch, n) or (batch, n, anything)
+    return None if shape is None else (shape[0], shape[1], 0)
+
+
+def bs_getrf_batched_ex(A, ipiv, info, layout: int = ROW_MAJOR, pivot_threshold: float = 1.0,
+                        transposed_factor: int = 0, interleave: int = 0, shape=None,
+                        status_contract: int = BS_CONTRACT_DEFAULT, scaling: int = 0,
+                        stream=None) -> None:
+    """getrf alone with the threshold, the row-major reading or an interleaved layout (A,
+    ipiv flat; shape=(batch, n)): the fused _ex call's factor (see bsolve.h)."""
+    batch, n, _ = _il_shape(A, None, ipiv, info, layout, interleave, _factor_shape(shape))
+    opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor),
+                   int(interleave), int(scaling))
+    st = lib().bs_getrf_batched_ex(_dtype_code(A), layout, n, batch, _ptr(A), _ptr(ipiv),
+                                   _ptr(info), ctypes.byref(opts), _stream(stream))
+    _check(st, "bs_getrf_batched_ex")
+
+
+def bs_getrs_batched_ex(LU, ipiv, B, layout: int = ROW_MAJOR, transposed_factor: int = 0,
+                        interleave: int = 0, shape=None, pivot_threshold: float = 1.0,
+                        status_contract: int = BS_CONTRACT_DEFAULT, scaling: int = 0,
+                        stream=None) -> None:
+    """getrs with a bs_getrf_batched_ex factor: the mirror solve of the row-major reading,
+    or an interleaved layout (LU, ipiv, B flat; shape=(batch, n, nrhs)) (see bsolve.h)."""
+    batch, n, nrhs = _il_shape(LU, B, ipiv, None, layout, interleave, shape)
+    opts = Options(float(pivot_threshold), int(status_contract), int(transposed_factor),
+                   int(interleave), int(scaling))
+    st = lib().bs_getrs_batched_ex(_dtype_code(LU), layout, n, nrhs, batch, _ptr(LU), _ptr(ipiv),
+                                   _ptr(B), ctypes.byref(opts), _stream(stream))
+    _check(st, "bs_getrs_batched_ex")
+
+
+def bs_potrf_batched_ex(A, info, layout: int = COL_MAJOR, fill: int = BS_LOWER,
+                        interleave: int = 0, shape=None,
+                        status_contract: int = BS_CONTRACT_DEFAULT, transposed_factor: int = 0,
+                        stream=None) -> None:
+    """potrf alone on an interleaved layout (A flat; shape=(batch, n)) (see bsolve.h)."""
+    batch, n, _ = _il_shape(A, None, None, info, layout, interleave, _factor_shape(shape))
+    opts = Options(1.0, int(status_contract), int(transposed_factor), int(interleave), 0)
+    st = lib().bs_potrf_batched_ex(_dtype_code(A), layout, fill, n, batch, _ptr(A), _ptr(info),
+                                   ctypes.byref(opts), _stream(stream))
+    _check(st, "bs_potrf_batched_ex")
+
+
+def bs_potrs_batched_ex(L, B, layout: int = COL_MAJOR, fill: int = BS_LOWER,
+                        interleave: int = 0, shape=None,
+                        status_contract: int = BS_CONTRACT_DEFAULT, stream=None) -> None:
+    """potrs with a bs_potrf_batched_ex factor on an interleaved layout (L, B flat;
+    shape=(batch, n, nrhs)) (see bsolve.h)."""
+    batch, n, nrhs = _il_shape(L, B, None, None, layout, interleave, shape)
+    opts = Options(1.0, int(status_contract), 0, int(interleave), 0)
+    st = lib().bs_potrs_batched_ex(_dtype_code(L), layout, fill, n, nrhs, batch, _ptr(L), _ptr(B),
+                                   ctypes.byref(opts), _stream(stream))
+    _check(st, "bs_potrs_batched_ex")
 
 
 # ------------------------------------------------------------ host-resident batches

@@ -93,38 +93,40 @@ bool bdsv_supported(bs_dtype dtype, int nbr, int bs) {
 
 // The row-major reading of TDLS (TDLS API, "solver_static.hpp File Reference"): the factor
 // of S, the row-major array read column-major (P A^T = L U), by the plain factor kernels
-// (or the one-CTA kernel under a threshold), then the mirror solve U^T z = b, L^T w = z,
-// x = P^T w, which writes X as zeros where info != 0.
+// (or the one-CTA kernel under a threshold, an interleaved layout or RUDA's scaling), then
+// the mirror solve U^T z = b, L^T w = z, x = P^T w, which writes X as zeros where
+// info != 0. il: the element stride of an interleaved batched layout (1: plain).
 bs_status getrf_getrs_mirror(bs_dtype dtype, int n, int nrhs, int64_t batch, void* A, void* B,
-                             int32_t* ipiv, int32_t* info, double tau, void* stream) {
+                             int32_t* ipiv, int32_t* info, double tau, int64_t il, int scaling,
+                             void* stream) {
   if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
   if (!lu_supported(dtype, BS_ROW_MAJOR, n, nrhs)) return BS_ERR_UNSUPPORTED;
   if (batch == 0) return BS_OK;
   if (!A || !B || !ipiv || !info) return BS_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(ipiv) || !aligned16(info))
     return BS_ERR_INVALID_ARG;
-  if (!lu_disjoint(dtype, n, nrhs, batch, 1, A, B, ipiv, info)) return BS_ERR_INVALID_ARG;
+  if (!lu_disjoint(dtype, n, nrhs, batch, il, A, B, ipiv, info)) return BS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (tau == 1.0) {
+  if (tau == 1.0 && il == 1 && !scaling) {
     const bs_status st = bs_getrf_batched(dtype, BS_COL_MAJOR, n, batch, A, ipiv, info, stream);
     if (st != BS_OK) return st;
   } else {
     e = dtype == BS_FP32
             ? bsolve::launch_lu_smem_ex<float>(BS_COL_MAJOR, n, 0, batch, static_cast<float*>(A),
-                                               nullptr, ipiv, info, tau, 0, s)
+                                               nullptr, ipiv, info, tau, 0, s, il, scaling)
             : bsolve::launch_lu_smem_ex<double>(BS_COL_MAJOR, n, 0, batch,
                                                 static_cast<double*>(A), nullptr, ipiv, info,
-                                                tau, 0, s);
+                                                tau, 0, s, il, scaling);
     if (e != cudaSuccess) return from_cuda(e);
   }
   const int code = BS_COL_MAJOR | (BS_ROW_MAJOR << 1);
   e = dtype == BS_FP32
           ? bsolve::launch_getrs_mirror<float>(code, n, nrhs, batch, static_cast<const float*>(A),
-                                               ipiv, static_cast<float*>(B), info, s)
+                                               ipiv, static_cast<float*>(B), info, s, il)
           : bsolve::launch_getrs_mirror<double>(code, n, nrhs, batch,
                                                 static_cast<const double*>(A), ipiv,
-                                                static_cast<double*>(B), info, s);
+                                                static_cast<double*>(B), info, s, il);
   return from_cuda(e);
 }
 
@@ -313,6 +315,30 @@ cudaError_t static_scratch_address(void** out) {
   }
   *out = p;
   return cudaSuccess;
+}
+
+// The options a split call takes, validated as the fused _ex calls validate them.
+struct SplitOpts {
+  double tau;
+  int contract, mirror, scaling;
+  int64_t il;   // element stride of the batched layout (1: plain)
+};
+
+bs_status split_opts(const bs_options* opts, SplitOpts* o) {
+  o->tau = opts ? opts->pivot_threshold : 1.0;
+  o->contract = opts ? opts->status_contract : BS_CONTRACT_DEFAULT;
+  o->mirror = opts ? opts->transposed_factor : 0;
+  o->scaling = opts ? opts->scaling : 0;
+  const int64_t ilv = opts ? opts->interleave : 0;
+  if (!(o->tau > 0.0 && o->tau <= 1.0)) return BS_ERR_INVALID_ARG;
+  if (o->contract != BS_CONTRACT_DEFAULT && o->contract != BS_CONTRACT_RUDA)
+    return BS_ERR_INVALID_ARG;
+  if ((o->mirror != 0 && o->mirror != 1) || ilv < 0 || (o->scaling != 0 && o->scaling != 1))
+    return BS_ERR_INVALID_ARG;
+  o->il = ilv > 1 ? ilv : 1;
+  // the RUDA contract and the scaling span the factor and the solve: fused calls only
+  if (o->contract != BS_CONTRACT_DEFAULT || o->scaling) return BS_ERR_UNSUPPORTED;
+  return BS_OK;
 }
 
 }  // namespace
@@ -759,9 +785,9 @@ bs_status bs_getrf_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int
   if (mirror != 0 && mirror != 1) return BS_ERR_INVALID_ARG;
   if (ilv < 0 || (scaling != 0 && scaling != 1)) return BS_ERR_INVALID_ARG;
   const int64_t il = ilv > 1 ? ilv : 1;   // element stride of the batched layout
-  if (mirror && (contract != BS_CONTRACT_DEFAULT || il > 1 || scaling)) return BS_ERR_UNSUPPORTED;
+  if (mirror && contract != BS_CONTRACT_DEFAULT) return BS_ERR_UNSUPPORTED;
   if (mirror && layout == BS_ROW_MAJOR)
-    return getrf_getrs_mirror(dtype, n, nrhs, batch, A, B, ipiv, info, tau, stream);
+    return getrf_getrs_mirror(dtype, n, nrhs, batch, A, B, ipiv, info, tau, il, scaling, stream);
   if (tau == 1.0 && contract == BS_CONTRACT_DEFAULT && !scaling)
     return il > 1 ? getrf_getrs_il(dtype, layout, n, nrhs, batch, il, A, B, ipiv, info, stream)
                   : bs_getrf_getrs_batched(dtype, layout, n, nrhs, batch, A, B, ipiv, info,
@@ -820,6 +846,124 @@ bs_status bs_potrf_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fi
           : bsolve::launch_chol_smem_ex<double>(chol_layouts(layout, fill), n, nrhs, batch,
                                                 static_cast<double*>(A),
                                                 static_cast<double*>(B), info, 1, s, il);
+  return from_cuda(e);
+}
+
+bs_status bs_getrf_batched_ex(bs_dtype dtype, bs_layout layout, int n, int64_t batch, void* A,
+                              int32_t* ipiv, int32_t* info, const bs_options* opts,
+                              void* stream) {
+  SplitOpts o;
+  const bs_status st = split_opts(opts, &o);
+  if (st != BS_OK) return st;
+  // the row-major reading factors S, the stored array read column-major
+  const bs_layout fl = o.mirror ? BS_COL_MAJOR : layout;
+  if (o.tau == 1.0 && o.il == 1)
+    return bs_getrf_batched(dtype, fl, n, batch, A, ipiv, info, stream);
+  if (n < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, fl, n, 1)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !ipiv || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(ipiv) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!lu_disjoint(dtype, n, 0, batch, o.il, A, nullptr, ipiv, info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_lu_smem_ex<float>(fl, n, 0, batch, static_cast<float*>(A), nullptr,
+                                             ipiv, info, o.tau, 0, s, o.il, 0)
+          : bsolve::launch_lu_smem_ex<double>(fl, n, 0, batch, static_cast<double*>(A), nullptr,
+                                              ipiv, info, o.tau, 0, s, o.il, 0);
+  return from_cuda(e);
+}
+
+bs_status bs_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs, int64_t batch,
+                              const void* LU, const int32_t* ipiv, void* B,
+                              const bs_options* opts, void* stream) {
+  SplitOpts o;
+  const bs_status st = split_opts(opts, &o);
+  if (st != BS_OK) return st;
+  const bool mirror = o.mirror && layout == BS_ROW_MAJOR;
+  if (!mirror && o.il == 1)   // the threshold only shapes the factor the solve is given
+    return bs_getrs_batched(dtype, layout, n, nrhs, batch, LU, ipiv, B, stream);
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!lu_supported(dtype, layout, n, nrhs)) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!LU || !ipiv || !B) return BS_ERR_INVALID_ARG;
+  if (!aligned16(LU) || !aligned16(ipiv) || !aligned16(B)) return BS_ERR_INVALID_ARG;
+  const size_t es = dtype == BS_FP32 ? 4 : 8, h = held(batch, o.il);
+  const size_t bbytes = h * n * nrhs * es;
+  if (overlap(B, bbytes, LU, h * n * n * es) || overlap(B, bbytes, ipiv, h * n * 4))
+    return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (mirror) {
+    const int code = BS_COL_MAJOR | (BS_ROW_MAJOR << 1);
+    e = dtype == BS_FP32
+            ? bsolve::launch_getrs_mirror<float>(code, n, nrhs, batch,
+                                                 static_cast<const float*>(LU), ipiv,
+                                                 static_cast<float*>(B), nullptr, s, o.il)
+            : bsolve::launch_getrs_mirror<double>(code, n, nrhs, batch,
+                                                  static_cast<const double*>(LU), ipiv,
+                                                  static_cast<double*>(B), nullptr, s, o.il);
+  } else {
+    e = dtype == BS_FP32
+            ? bsolve::launch_getrs<float>(layout | (layout << 1), n, nrhs, batch,
+                                          static_cast<const float*>(LU), ipiv,
+                                          static_cast<float*>(B), nullptr, s, o.il)
+            : bsolve::launch_getrs<double>(layout | (layout << 1), n, nrhs, batch,
+                                           static_cast<const double*>(LU), ipiv,
+                                           static_cast<double*>(B), nullptr, s, o.il);
+  }
+  return from_cuda(e);
+}
+
+bs_status bs_potrf_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                              int64_t batch, void* A, int32_t* info, const bs_options* opts,
+                              void* stream) {
+  SplitOpts o;
+  const bs_status st = split_opts(opts, &o);
+  if (st != BS_OK) return st;
+  if (o.mirror) return BS_ERR_UNSUPPORTED;   // an LU option
+  if (o.il == 1) return bs_potrf_batched(dtype, layout, fill, n, batch, A, info, stream);
+  if (n < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, 1) || n > kMaxLuN) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!A || !info) return BS_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(info)) return BS_ERR_INVALID_ARG;
+  if (!chol_disjoint(dtype, n, 0, batch, o.il, A, nullptr, info)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int code = chol_layouts(layout, fill);
+  const cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_chol_smem_ex<float>(code, n, 0, batch, static_cast<float*>(A),
+                                               nullptr, info, 0, s, o.il)
+          : bsolve::launch_chol_smem_ex<double>(code, n, 0, batch, static_cast<double*>(A),
+                                                nullptr, info, 0, s, o.il);
+  return from_cuda(e);
+}
+
+bs_status bs_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fill, int n, int nrhs,
+                              int64_t batch, const void* L, void* B, const bs_options* opts,
+                              void* stream) {
+  SplitOpts o;
+  const bs_status st = split_opts(opts, &o);
+  if (st != BS_OK) return st;
+  if (o.mirror) return BS_ERR_UNSUPPORTED;   // an LU option
+  if (o.il == 1) return bs_potrs_batched(dtype, layout, fill, n, nrhs, batch, L, B, stream);
+  if (n < 0 || nrhs < 0 || batch < 0) return BS_ERR_INVALID_ARG;
+  if (!chol_supported(dtype, layout, fill, n, nrhs) || n > kMaxLuN) return BS_ERR_UNSUPPORTED;
+  if (batch == 0) return BS_OK;
+  if (!L || !B) return BS_ERR_INVALID_ARG;
+  if (!aligned16(L) || !aligned16(B)) return BS_ERR_INVALID_ARG;
+  const size_t es = dtype == BS_FP32 ? 4 : 8, h = held(batch, o.il);
+  if (overlap(B, h * n * nrhs * es, L, h * n * n * es)) return BS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int code = chol_layouts(layout, fill);
+  const cudaError_t e =
+      dtype == BS_FP32
+          ? bsolve::launch_potrs<float>(code, n, nrhs, batch, static_cast<const float*>(L),
+                                        static_cast<float*>(B), nullptr, s, o.il)
+          : bsolve::launch_potrs<double>(code, n, nrhs, batch, static_cast<const double*>(L),
+                                         static_cast<double*>(B), nullptr, s, o.il);
   return from_cuda(e);
 }
 

@@ -33,12 +33,15 @@ cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, 
 // potrs (Cholesky factor), 1 <= n <= 128.
 // Any nrhs >= 1 (a register tier's worth at a time). zinfo (may be null): X = 0 where
 // zinfo[s] != 0.
+// ilv: the element stride of an interleaved batched layout (1: the plain layout; > 1:
+// n <= 128, one warp per system).
 template <typename T>
 cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU,
-                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream);
+                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream,
+                         int64_t ilv = 1);
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
-                         const int32_t* zinfo, cudaStream_t stream);
+                         const int32_t* zinfo, cudaStream_t stream, int64_t ilv = 1);
 // potrs for FP64, 1 <= n <= 32, nrhs == 1: one system per lane, the factor streamed by
 // columns through shared memory (layout bit 0: the factor's storage order).
 cudaError_t launch_potrs_lane(int layout, int n, int nrhs, int64_t batch, const double* L,
@@ -49,7 +52,7 @@ cudaError_t launch_potrs_lane(int layout, int n, int nrhs, int64_t batch, const 
 template <typename T>
 cudaError_t launch_getrs_mirror(int layout, int n, int nrhs, int64_t batch, const T* S,
                                 const int32_t* ipiv, T* B, const int32_t* zinfo,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int64_t ilv = 1);
 
 // The Cholesky launchers (chol_smem, chol_sys, potrs) take a packed storage-order code:
 // bit 0 for A (or the factor), bit 1 for B; upper fill is passed as the lower fill of A in

@@ -298,11 +298,14 @@ __device__ __forceinline__ T pick(const T (&v)[Q], int q) {
   return r;
 }
 
+// ilv: the element stride of TDLS's interleaved batched layouts (element e of system s at
+// base_s[e * ilv], base_s = (s / ilv) * ilv * size + s % ilv, for the factor, B and
+// ipiv); 1 for the plain layout, where the offsets are the plain ones.
 template <typename T, int RT, int KIND, int Q, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restrict__ M,
                   const int32_t* __restrict__ ipiv, T* __restrict__ B,
-                  const int32_t* __restrict__ zinfo) {
+                  const int32_t* __restrict__ zinfo, int64_t ilv) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int P = odd_pitch(n);
   const int lane = threadIdx.x & 31;
@@ -310,8 +313,10 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
   const int64_t s = static_cast<int64_t>(blockIdx.x) * WARPS + warp;
   if (s >= batch) return;   // whole warp: no block barrier below
   T* const F = reinterpret_cast<T*>(smem_raw) + static_cast<int64_t>(warp) * n * P;
-  const T* Ms = M + s * n * n;
-  T* Bs = B + s * n * nrhs;
+  const int64_t blk = s / ilv, sl = s - blk * ilv;
+  const T* Ms = M + blk * ilv * n * n + sl;
+  T* Bs = B + blk * ilv * n * nrhs + sl;
+  const int32_t* ips = ipiv == nullptr ? nullptr : ipiv + blk * ilv * n + sl;
 
   // the factor (LU: all of it; Cholesky: the lower triangle only)
   for (int e = lane; e < n * n; e += 32) {
@@ -323,7 +328,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
       c = e / n;
       r = e - c * n;
     }
-    if (KIND != kSolveChol || c <= r) cp_async_elem<T>(F + r * P + c, Ms + e);
+    if (KIND != kSolveChol || c <= r) cp_async_elem<T>(F + r * P + c, Ms + e * ilv);
   }
   cp_async_wait_all();
   __syncwarp();
@@ -335,7 +340,7 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
     int ip[Q];
 #pragma unroll
     for (int q = 0; q < Q; ++q)
-      ip[q] = lane + 32 * q < n ? __ldg(ipiv + s * n + lane + 32 * q) - 1 : 0;
+      ip[q] = lane + 32 * q < n ? __ldg(ips + static_cast<int64_t>(lane + 32 * q) * ilv) - 1 : 0;
     for (int k = n - 1; k >= 0; --k) {
       int p = __shfl_sync(0xFFFFFFFFu, pick<int, Q>(ip, k >> 5), k & 31);
       if (p < 0 || p >= n) p = k;   // an entry out of range swaps nothing
@@ -363,7 +368,8 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
       const int lrow = KIND == kSolveLuT ? lane + 32 * q : src[q];
 #pragma unroll
       for (int c = 0; c < RT; ++c)
-        b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, lrow, c0 + c)] : T(0);
+        b[q][c] = (ok && c0 + c < nrhs) ? Bs[idx(layouts >> 1, n, nrhs, lrow, c0 + c) * ilv]
+                                        : T(0);
     }
     for (int k = 0; k < n; ++k) {
       const int kq = k >> 5, kl = k & 31;
@@ -426,7 +432,8 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
         const int srow = KIND == kSolveLuT ? src[q] : i;   // LuT: x = P^T w
 #pragma unroll
         for (int c = 0; c < RT; ++c)
-          if (c0 + c < nrhs) Bs[idx(layouts >> 1, n, nrhs, srow, c0 + c)] = zero_x ? T(0) : b[q][c];
+          if (c0 + c < nrhs)
+            Bs[idx(layouts >> 1, n, nrhs, srow, c0 + c) * ilv] = zero_x ? T(0) : b[q][c];
       }
     }
   }
@@ -434,7 +441,8 @@ solve_smem_kernel(int n, int nrhs, int layouts, int64_t batch, const T* __restri
 
 template <typename T, int RT, int KIND, int Q, int WARPS>
 cudaError_t launch_smem_q(int layout, int n, int nrhs, int64_t batch, const T* M,
-                          const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
+                          const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream,
+                          int64_t ilv) {
   const int64_t blocks = (batch + WARPS - 1) / WARPS;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const size_t bytes = static_cast<size_t>(WARPS) * n * odd_pitch(n) * sizeof(T);
@@ -443,25 +451,27 @@ cudaError_t launch_smem_q(int layout, int n, int nrhs, int64_t batch, const T* M
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   solve_smem_kernel<T, RT, KIND, Q, WARPS><<<static_cast<unsigned>(blocks), WARPS * 32, bytes,
-                                             stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo);
+                                             stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo,
+                                                       ilv);
   return cudaGetLastError();
 }
 
 template <typename T, int KIND, int Q, int WARPS>
 cudaError_t launch_smem_rhs(int layout, int n, int nrhs, int64_t batch, const T* M,
                             const int32_t* ipiv, T* B, const int32_t* zinfo,
-                            cudaStream_t stream) {
-  if (nrhs <= 1) return launch_smem_q<T, 1, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
-  if (nrhs <= 2) return launch_smem_q<T, 2, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
-  if (nrhs <= 4) return launch_smem_q<T, 4, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
-  return launch_smem_q<T, 8, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+                            cudaStream_t stream, int64_t ilv) {
+  if (nrhs <= 1) return launch_smem_q<T, 1, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream, ilv);
+  if (nrhs <= 2) return launch_smem_q<T, 2, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream, ilv);
+  if (nrhs <= 4) return launch_smem_q<T, 4, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream, ilv);
+  return launch_smem_q<T, 8, KIND, Q, WARPS>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream, ilv);
 }
 
 template <typename T, int KIND>
 cudaError_t launch_smem(int layout, int n, int nrhs, int64_t batch, const T* M,
-                        const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
-  if (n <= 64) return launch_smem_rhs<T, KIND, 2, 2>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
-  return launch_smem_rhs<T, KIND, 4, 1>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream);
+                        const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream,
+                        int64_t ilv = 1) {
+  if (n <= 64) return launch_smem_rhs<T, KIND, 2, 2>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream, ilv);
+  return launch_smem_rhs<T, KIND, 4, 1>(layout, n, nrhs, batch, M, ipiv, B, zinfo, stream, ilv);
 }
 
 template <typename T, int KIND>
@@ -482,15 +492,26 @@ cudaError_t launch_kind(int layout, int n, int nrhs, int64_t batch, const T* M,
 // the lower triangle of the other order). zinfo (may be null): the factor's info, and X is
 // written as zeros where it is not 0 (the fused calls' contract, when they run as a factor
 // and a solve for more right-hand sides than a register tier holds).
+// ilv > 1 (TDLS's interleaved batched layouts): one warp per system in shared memory for
+// every n <= 128, the element offsets multiplied by the stride.
 template <typename T>
 cudaError_t launch_getrs(int layout, int n, int nrhs, int64_t batch, const T* LU,
-                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream) {
+                         const int32_t* ipiv, T* B, const int32_t* zinfo, cudaStream_t stream,
+                         int64_t ilv) {
+  if (ilv > 1) {
+    if (n > 128) return cudaErrorInvalidValue;
+    return launch_smem<T, kSolveLu>(layout, n, nrhs, batch, LU, ipiv, B, zinfo, stream, ilv);
+  }
   return launch_kind<T, kSolveLu>(layout, n, nrhs, batch, LU, ipiv, B, zinfo, stream);
 }
 
 template <typename T>
 cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L, T* B,
-                         const int32_t* zinfo, cudaStream_t stream) {
+                         const int32_t* zinfo, cudaStream_t stream, int64_t ilv) {
+  if (ilv > 1) {
+    if (n > 128) return cudaErrorInvalidValue;
+    return launch_smem<T, kSolveChol>(layout, n, nrhs, batch, L, nullptr, B, zinfo, stream, ilv);
+  }
   // FP64, n <= 32, one right-hand side: one system per lane (solve_lane.cu)
   if constexpr (std::is_same<T, double>::value)
     if (n <= 32 && nrhs == 1) return launch_potrs_lane(layout, n, nrhs, batch, L, B, zinfo, stream);
@@ -502,23 +523,27 @@ cudaError_t launch_potrs(int layout, int n, int nrhs, int64_t batch, const T* L,
 template <typename T>
 cudaError_t launch_getrs_mirror(int layout, int n, int nrhs, int64_t batch, const T* S,
                                 const int32_t* ipiv, T* B, const int32_t* zinfo,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int64_t ilv) {
+  if (ilv > 1) {
+    if (n > 128) return cudaErrorInvalidValue;
+    return launch_smem<T, kSolveLuT>(layout, n, nrhs, batch, S, ipiv, B, zinfo, stream, ilv);
+  }
   return launch_kind<T, kSolveLuT>(layout, n, nrhs, batch, S, ipiv, B, zinfo, stream);
 }
 
 template cudaError_t launch_getrs<float>(int, int, int, int64_t, const float*, const int32_t*,
-                                         float*, const int32_t*, cudaStream_t);
+                                         float*, const int32_t*, cudaStream_t, int64_t);
 template cudaError_t launch_getrs<double>(int, int, int, int64_t, const double*, const int32_t*,
-                                          double*, const int32_t*, cudaStream_t);
+                                          double*, const int32_t*, cudaStream_t, int64_t);
 template cudaError_t launch_potrs<float>(int, int, int, int64_t, const float*, float*,
-                                         const int32_t*, cudaStream_t);
+                                         const int32_t*, cudaStream_t, int64_t);
 template cudaError_t launch_potrs<double>(int, int, int, int64_t, const double*, double*,
-                                          const int32_t*, cudaStream_t);
+                                          const int32_t*, cudaStream_t, int64_t);
 template cudaError_t launch_getrs_mirror<float>(int, int, int, int64_t, const float*,
                                                 const int32_t*, float*, const int32_t*,
-                                                cudaStream_t);
+                                                cudaStream_t, int64_t);
 template cudaError_t launch_getrs_mirror<double>(int, int, int, int64_t, const double*,
                                                  const int32_t*, double*, const int32_t*,
-                                                 cudaStream_t);
+                                                 cudaStream_t, int64_t);
 
 }  // namespace bsolve

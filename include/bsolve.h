@@ -177,7 +177,8 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    holds the factor of A^T in the column-major reading. With
  *                    BS_COL_MAJOR, S = A and the call is the plain one. Runs as a factor
  *                    launch and a solve launch, for 1 <= n <= 128, 1 <= nrhs <= 65536;
- *                    with BS_CONTRACT_RUDA it is BS_ERR_UNSUPPORTED.
+ *                    with BS_CONTRACT_RUDA it is BS_ERR_UNSUPPORTED (the contract zeroes
+ *                    a failed system inside the one fused kernel).
  *   interleave       the batched layout (TDLS API, "solver_static.hpp File Reference":
  *                    element e of a system at base[e * stride]). 0 or 1: AoS, system s
  *                    at s * size (the plain layout). W > 1: AoSoA, the systems in blocks
@@ -186,9 +187,11 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    (s / W) * W * size + e * W + s % W; W >= batch is SoA. A, B and
  *                    ipiv then hold ceil(batch / W) * W systems each (the slots of the last
  *                    block past the batch are neither read nor written); info keeps one
- *                    entry per system. For both calls nrhs <= 8; it combines with the
- *                    threshold and the RUDA contract (one system per CTA) but not with
- *                    transposed_factor (BS_ERR_UNSUPPORTED); negative: BS_ERR_INVALID_ARG.
+ *                    entry per system. Cholesky: n <= 128. nrhs <= 8, except with
+ *                    transposed_factor (the solve there is a launch of its own, taking 8
+ *                    columns at a time: nrhs <= 65536). It combines with the threshold, the
+ *                    RUDA contract (one system per CTA), transposed_factor and scaling;
+ *                    negative: BS_ERR_INVALID_ARG.
  *   scaling          0 or 1 (LU only; RUDA docs, unchanged numerical contract: the LU keeps
  *                    the scaling by the whole matrix's largest magnitude and restores U's
  *                    scale at the end). 1: with m = max |a_ij| finite and positive, A is
@@ -197,8 +200,9 @@ BS_API bs_status bs_bdsv_batched(bs_dtype dtype, int num_block_rows, int block_s
  *                    the restored U (reciprocals of its diagonal recomputed; 1 for one below
  *                    the smallest normal number); a non-finite entry or a zero matrix leaves
  *                    the system unscaled; info reports the scaled sweep's pivots. One
- *                    system per CTA; combines with the threshold, the RUDA contract and
- *                    interleaving, not with transposed_factor (BS_ERR_UNSUPPORTED).
+ *                    system per CTA; combines with the threshold, the RUDA contract,
+ *                    interleaving and transposed_factor (there S, the stored array read
+ *                    column-major, is what is scaled).
  * opts == NULL or default options run the plain call. Thresholds and the RUDA contract
  * run one system per CTA for every n (1 <= n <= 128, 1 <= nrhs <= 8); results equal the
  * CPU oracle's bit for bit. A threshold outside (0, 1], an unknown contract or a
@@ -262,6 +266,50 @@ BS_API bs_status bs_bdsv_factor_batched(bs_dtype dtype, int num_block_rows, int 
 BS_API bs_status bs_bdsv_solve_batched(bs_dtype dtype, int num_block_rows, int block_size,
                                        int64_t batch, const void* strips, void* x_padded,
                                        void* stream);
+
+/*
+ * The split calls with options: the factor and the solve of the LU and Cholesky paths on
+ * the interleaved batched layouts and, for LU, under TDLS's row-major reading and a pivot
+ * threshold.
+ *
+ * Source: TDLS API, "solver_static.hpp File Reference" (the interleaved batched layouts;
+ * the row-major reading; the substitution as a step of its own); RUDA docs (the pivot
+ * threshold).
+ *
+ * Arguments as the split calls above, plus opts (NULL: the plain call), read as the fused
+ * _ex calls read them:
+ *   interleave         every batched operand (A, B, ipiv) in the layout of that name;
+ *                      held ceil(batch / W) * W systems each; info one entry per system.
+ *   transposed_factor  1 with BS_ROW_MAJOR: bs_getrf_batched_ex factors S (the array read
+ *                      column-major), bs_getrs_batched_ex runs the mirror solve with that
+ *                      factor. With BS_COL_MAJOR it changes nothing. Cholesky:
+ *                      BS_ERR_UNSUPPORTED.
+ *   pivot_threshold    bs_getrf_batched_ex: the threshold rule of the fused call. The solve
+ *                      and the Cholesky calls accept any valid value and ignore it.
+ *   status_contract    BS_CONTRACT_RUDA: BS_ERR_UNSUPPORTED (a fused-call contract).
+ *   scaling            1: BS_ERR_UNSUPPORTED (a fused-call option: the solve uses the
+ *                      restored U with recomputed reciprocals).
+ * Results: the factor calls leave info, ipiv and, on every system with info == 0, A
+ * exactly as the fused _ex call with the same options (a Cholesky system that failed may
+ * hold other partial values: interleaved factors of n <= 32 run on another kernel than
+ * the fused call's); the solve calls, given that factor, leave the fused call's X wherever
+ * info == 0 (with a failed factor X is unspecified). Interleaved or threshold factors run
+ * one system per CTA; interleaved or mirror solves one system per warp in shared memory.
+ * Supported: LU 1 <= n <= 128; Cholesky 1 <= n <= 256 on the plain layout, n <= 128
+ * interleaved; 1 <= nrhs <= 65536.
+ */
+BS_API bs_status bs_getrf_batched_ex(bs_dtype dtype, bs_layout layout, int n, int64_t batch,
+                                     void* A, int32_t* ipiv, int32_t* info,
+                                     const bs_options* opts, void* stream);
+BS_API bs_status bs_getrs_batched_ex(bs_dtype dtype, bs_layout layout, int n, int nrhs,
+                                     int64_t batch, const void* LU, const int32_t* ipiv, void* B,
+                                     const bs_options* opts, void* stream);
+BS_API bs_status bs_potrf_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                     int64_t batch, void* A, int32_t* info,
+                                     const bs_options* opts, void* stream);
+BS_API bs_status bs_potrs_batched_ex(bs_dtype dtype, bs_layout layout, bs_fill fill, int n,
+                                     int nrhs, int64_t batch, const void* L, void* B,
+                                     const bs_options* opts, void* stream);
 
 /*
  * Block-tridiagonal matrix-vector product y = A x (glass::bdmv).

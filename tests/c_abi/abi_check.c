@@ -100,10 +100,21 @@ int main(void) {
   CHECK(bs_getrf_getrs_batched_ex(BS_FP32, BS_ROW_MAJOR, 16, 4, 5, A, B, ipiv, info, &o,
                                   NULL) == BS_ERR_INVALID_ARG);
   o.interleave = 4;
-  o.transposed_factor = 1; /* not with interleaving */
+  o.transposed_factor = 1;
+  o.status_contract = BS_CONTRACT_RUDA; /* the row-major reading: not with this contract */
   CHECK(bs_getrf_getrs_batched_ex(BS_FP32, BS_ROW_MAJOR, 16, 4, 5, A, B, ipiv, info, &o,
                                   NULL) == BS_ERR_UNSUPPORTED);
+  /* the split calls with options: the contract stays with the fused calls */
+  CHECK(bs_getrf_batched_ex(BS_FP32, BS_ROW_MAJOR, 16, 5, A, ipiv, info, &o, NULL) ==
+        BS_ERR_UNSUPPORTED);
+  CHECK(bs_getrs_batched_ex(BS_FP32, BS_ROW_MAJOR, 16, 4, 5, A, ipiv, B, &o, NULL) ==
+        BS_ERR_UNSUPPORTED);
+  o.status_contract = BS_CONTRACT_DEFAULT;
+  CHECK(bs_potrf_batched_ex(BS_FP64, BS_COL_MAJOR, BS_LOWER, 32, 5, A, info, &o, NULL) ==
+        BS_ERR_UNSUPPORTED); /* an LU option */
   o.transposed_factor = 0;
+  CHECK(bs_potrs_batched_ex(BS_FP64, BS_COL_MAJOR, BS_LOWER, 200, 1, 5, A, B, &o, NULL) ==
+        BS_ERR_UNSUPPORTED); /* interleaved Cholesky: n <= 128 */
   o.status_contract = 7;
   CHECK(bs_potrf_potrs_batched_ex(BS_FP64, BS_COL_MAJOR, BS_LOWER, 32, 1, 5, A, B, info, &o,
                                   NULL) == BS_ERR_INVALID_ARG);

@@ -182,13 +182,15 @@ def test_contract_variant_argument_errors(lib):
     assert f(bs.BS_FP32, 0, 16, 9, 0, None, None, None, None, m(0.5, 0, 1), None) == bs.BS_OK
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, None, I, m(0.5, 0, 1), None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 9, 5, A + 4, B, P, I, m(1.0, 0, 1), None) == bs.BS_ERR_INVALID_ARG
-    # the interleaved batched layout: W >= 0; with W > 1 at most 8 right-hand sides and not
-    # with the row-major reading
+    # the interleaved batched layout: W >= 0; with W > 1 at most 8 right-hand sides, except
+    # under the row-major reading (a solve launch of its own)
     w = lambda tau, c, t, il: ctypes.byref(bs.Options(tau, c, t, il))  # noqa: E731
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(1.0, 0, 0, -1), None) == bs.BS_ERR_INVALID_ARG
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, w(0.5, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, w(1.0, 1, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
-    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(1.0, 0, 1, 32), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I + 4, w(1.0, 0, 1, 32), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 16, 65537, 5, A, B, P, I, w(1.0, 0, 1, 32), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, w(1.0, 1, 1, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, w(1.0, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 129, 4, 5, A, B, P, I, w(1.0, 0, 0, 32), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, w(1.0, 0, 0, 32), None) == bs.BS_OK
@@ -198,14 +200,49 @@ def test_contract_variant_argument_errors(lib):
     assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, w(1.0, 0, 1, 0), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 9, 5, A, B, I, w(1.0, 0, 0, 64), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 1, 0, None, None, None, w(1.0, 0, 0, 64), None) == bs.BS_OK
-    # RUDA's max-abs scaling: 0 or 1, LU only, not with the row-major reading
+    # RUDA's max-abs scaling: 0 or 1, LU only (the row-major reading included)
     sc = lambda tau, c, t, il, k: ctypes.byref(bs.Options(tau, c, t, il, k))  # noqa: E731
     assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, sc(1.0, 0, 0, 0, 2), None) == bs.BS_ERR_INVALID_ARG
-    assert f(bs.BS_FP32, 0, 16, 4, 5, A, B, P, I, sc(1.0, 0, 1, 0, 1), None) == bs.BS_ERR_UNSUPPORTED
+    assert f(bs.BS_FP32, 0, 16, 4, 5, A + 4, B, P, I, sc(1.0, 0, 1, 0, 1), None) == bs.BS_ERR_INVALID_ARG
+    assert f(bs.BS_FP32, 0, 129, 4, 5, A, B, P, I, sc(1.0, 0, 1, 8, 1), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 9, 5, A, B, P, I, sc(1.0, 0, 0, 0, 1), None) == bs.BS_ERR_UNSUPPORTED
     assert f(bs.BS_FP32, 0, 16, 4, 0, None, None, None, None, sc(1.0, 0, 0, 0, 1), None) == bs.BS_OK
     assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, sc(1.0, 0, 0, 0, 1), None) == bs.BS_ERR_UNSUPPORTED
     assert g(bs.BS_FP64, 1, 0, 32, 1, 5, A, B, I, sc(1.0, 0, 0, 0, 3), None) == bs.BS_ERR_INVALID_ARG
+
+
+def test_split_calls_with_options_argument_errors(lib):
+    """The split _ex calls check their options as the fused _ex calls do; the RUDA
+    contract and the scaling stay with the fused calls, Cholesky takes no LU option;
+    interleaved operands hold whole blocks (5 systems in blocks of 4: room for 8)."""
+    import ctypes
+    A, B, P, I = FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000
+    o = lambda tau=1.0, c=0, t=0, il=0, k=0: ctypes.byref(bs.Options(tau, c, t, il, k))  # noqa: E731
+    gf, gs = lib.bs_getrf_batched_ex, lib.bs_getrs_batched_ex
+    pf, ps = lib.bs_potrf_batched_ex, lib.bs_potrs_batched_ex
+    assert gf(bs.BS_FP64, 0, 8, 5, A, P, I, o(tau=0.0), None) == bs.BS_ERR_INVALID_ARG
+    assert gf(bs.BS_FP64, 0, 8, 5, A, P, I, o(il=-2), None) == bs.BS_ERR_INVALID_ARG
+    assert gf(bs.BS_FP64, 0, 8, 5, A, P, I, o(t=2), None) == bs.BS_ERR_INVALID_ARG
+    assert gf(bs.BS_FP64, 0, 8, 5, A, P, I, o(c=1), None) == bs.BS_ERR_UNSUPPORTED
+    assert gf(bs.BS_FP64, 0, 8, 5, A, P, I, o(k=1), None) == bs.BS_ERR_UNSUPPORTED
+    assert gf(bs.BS_FP64, 0, 129, 5, A, P, I, o(il=4), None) == bs.BS_ERR_UNSUPPORTED
+    assert gf(bs.BS_FP64, 0, 8, 0, None, None, None, o(il=4), None) == bs.BS_OK
+    assert gf(bs.BS_FP64, 0, 8, 5, A, A + 5 * 512, I, o(il=4), None) == bs.BS_ERR_INVALID_ARG
+    assert gf(bs.BS_FP64, 0, 8, 5, A, P, I + 4, o(tau=0.5), None) == bs.BS_ERR_INVALID_ARG
+    assert gf(bs.BS_FP64, 0, 8, 5, None, P, I, o(t=1), None) == bs.BS_ERR_INVALID_ARG
+    assert gs(bs.BS_FP64, 0, 8, 2, 5, A, P, B, o(k=1), None) == bs.BS_ERR_UNSUPPORTED
+    assert gs(bs.BS_FP64, 0, 8, 65537, 5, A, P, B, o(il=4), None) == bs.BS_ERR_UNSUPPORTED
+    assert gs(bs.BS_FP64, 0, 8, 9, 5, A, P, A + 5 * 512, o(il=4, t=1), None) == bs.BS_ERR_INVALID_ARG
+    assert gs(bs.BS_FP64, 0, 8, 9, 5, A, B + 5 * 8 * 9 * 8, B, o(il=4), None) == bs.BS_ERR_INVALID_ARG
+    assert gs(bs.BS_FP64, 0, 8, 9, 0, None, None, None, o(t=1), None) == bs.BS_OK
+    assert pf(bs.BS_FP64, 1, 0, 8, 5, A, I, o(t=1), None) == bs.BS_ERR_UNSUPPORTED
+    assert pf(bs.BS_FP64, 1, 0, 8, 5, A, I, o(c=1), None) == bs.BS_ERR_UNSUPPORTED
+    assert pf(bs.BS_FP64, 1, 0, 200, 5, A, I, o(il=4), None) == bs.BS_ERR_UNSUPPORTED
+    assert pf(bs.BS_FP64, 1, 2, 8, 5, A, I, o(il=4), None) == bs.BS_ERR_UNSUPPORTED
+    assert pf(bs.BS_FP64, 1, 0, 8, 5, A, A + 5 * 512, o(il=4), None) == bs.BS_ERR_INVALID_ARG
+    assert ps(bs.BS_FP64, 1, 0, 8, 1, 5, A, A + 5 * 512, o(il=4), None) == bs.BS_ERR_INVALID_ARG
+    assert ps(bs.BS_FP64, 1, 0, 8, 1, 5, A, B, o(k=1), None) == bs.BS_ERR_UNSUPPORTED
+    assert ps(bs.BS_FP64, 1, 0, 8, 1, 0, None, None, o(il=4), None) == bs.BS_OK
 
 
 def test_binding_refuses_host_tensors():
