@@ -42,14 +42,14 @@ METRIC = "systems/sec per (n, dtype, nrhs); achieved HBM GB/s and % of roofline,
 HEADLINE = "lu_f32_n16"
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {
-    "lu_f32_n16": ["lu_reg.cuh", "common.cuh"],
+    "lu_f32_n16": ["lu_rows2.cu", "common.cuh"],
     "lu_f64_n8": ["lu_reg.cuh", "common.cuh"],
     "lu_f64_n64": ["lu_cta.cu", "common.cuh"],
     "chol_f64_n32": ["chol_sys.cu", "common.cuh"],
     "bdsv_f64_32x8": ["bdsv.cu", "common.cuh"],
 }
 KERNEL_NAMES = {
-    "lu_f32_n16": "lu_reg_kernel", "lu_f64_n8": "lu_reg_kernel", "lu_f64_n64": "lu_cta_kernel",
+    "lu_f32_n16": "lu_rows2_kernel", "lu_f64_n8": "lu_reg_kernel", "lu_f64_n64": "lu_cta_kernel",
     "chol_f64_n32": "chol_sys_kernel", "bdsv_f64_32x8": "bdsv_kernel",
 }
 REASONS = ["clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
@@ -249,12 +249,12 @@ NEXT_ROWS = {
 # systems per block of the interleaved rows (None: the whole batch, SoA)
 IL_WIDTH = {"getrf_getrs_aosoa32_f32_n16": 32, "potrf_potrs_soa_f64_n32": None}
 KERNEL_SOURCES.update({
-    "getrf_f32_n16": ["lu_reg.cuh", "common.cuh"], "getrs_f32_n16": ["solve.cu", "common.cuh"],
+    "getrf_f32_n16": ["lu_rows2.cu", "common.cuh"], "getrs_f32_n16": ["solve.cu", "common.cuh"],
     "potrf_f64_n32": ["chol_sys.cu", "common.cuh"],
     "potrs_f64_n32": ["solve_lane.cu", "common.cuh"],
     "bdsv_factor_f64_32x8": ["bdsv.cu", "common.cuh"],
     "bdsv_solve_f64_32x8": ["bdsv.cu", "common.cuh"], "bdmv_f64_32x8": ["bdmv.cu", "common.cuh"],
-    "getrf_getrs_T_f32_n16": ["solve.cu", "lu_reg.cuh", "common.cuh"],
+    "getrf_getrs_T_f32_n16": ["solve.cu", "lu_rows2.cu", "common.cuh"],
     "getrf_getrs_aosoa32_f32_n16": ["lu_reg.cuh", "common.cuh"],
     "potrf_potrs_soa_f64_n32": ["chol_sys.cu", "common.cuh"],
     "potrf_potrs_f64_n256": ["chol_cluster.cu", "common.cuh"],

@@ -23,7 +23,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--fmad=false", "-Xcompiler", "-
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 LIB_SOURCES = ["api.cu", "lu_reg.cu", "lu_reg_f32_row.cu", "lu_reg_f32_col.cu", "lu_reg_f64_row.cu",
                "lu_reg_f64_col.cu", "lu_reg_il_f32_row.cu", "lu_reg_il_f32_col.cu", "lu_reg_il_f64_row.cu",
-               "lu_reg_il_f64_col.cu", "lu_cta.cu",
+               "lu_reg_il_f64_col.cu", "lu_rows2.cu", "lu_cta.cu",
                "smem_solvers.cu", "chol_sys.cu", "chol_cluster.cu", "bdsv.cu", "bdmv.cu", "solve.cu",
                "solve_lane.cu"]
 PROBE_SOURCES = ["fma_peak.cu"]
