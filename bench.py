@@ -255,7 +255,7 @@ KERNEL_SOURCES.update({
     "bdsv_factor_f64_32x8": ["bdsv.cu", "common.cuh"],
     "bdsv_solve_f64_32x8": ["bdsv.cu", "common.cuh"], "bdmv_f64_32x8": ["bdmv.cu", "common.cuh"],
     "getrf_getrs_T_f32_n16": ["solve.cu", "lu_rows2.cu", "common.cuh"],
-    "getrf_getrs_aosoa32_f32_n16": ["lu_reg.cuh", "common.cuh"],
+    "getrf_getrs_aosoa32_f32_n16": ["lu_rows2.cu", "common.cuh"],
     "potrf_potrs_soa_f64_n32": ["chol_sys.cu", "common.cuh"],
     "potrf_potrs_f64_n256": ["chol_cluster.cu", "common.cuh"],
 })

@@ -25,9 +25,9 @@ cudaError_t launch_lu_smem(int layout, int n, int nrhs, int64_t batch, T* A, T* 
 // The same with the options of the _ex calls: TDLS threshold tau in (0, 1], RUDA status
 // contract (ruda != 0); any 1 <= n <= 128.
 // LU + solve for FP32, 8 < n <= 16, nrhs <= 8 (0: factor only), two rows per lane and
-// four systems per warp; the plain batched layout.
+// four systems per warp; ilv: the element stride of an interleaved batched layout (1: plain).
 cudaError_t launch_lu_rows2(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
-                            int32_t* ipiv, int32_t* info, cudaStream_t stream);
+                            int32_t* ipiv, int32_t* info, cudaStream_t stream, int64_t ilv = 1);
 
 template <typename T>
 cudaError_t launch_lu_smem_ex(int layout, int n, int nrhs, int64_t batch, T* A, T* B,

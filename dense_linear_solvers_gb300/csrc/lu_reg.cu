@@ -17,6 +17,10 @@ cudaError_t launch_layout_il(int n, int nrhs, int64_t batch, int64_t ilv, T* A, 
 template <typename T>
 cudaError_t launch_lu_reg_il(int layout, int n, int nrhs, int64_t batch, int64_t ilv, T* A, T* B,
                              int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if constexpr (sizeof(T) == 4) {
+    if (n > 8 && n <= 16)
+      return launch_lu_rows2(layout, n, nrhs, batch, A, B, ipiv, info, stream, ilv);
+  }
   if (layout == kRowMajor)
     return lu_reg_detail::launch_layout_il<T, kRowMajor>(n, nrhs, batch, ilv, A, B, ipiv, info,
                                                          stream);

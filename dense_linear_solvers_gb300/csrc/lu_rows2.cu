@@ -1,5 +1,6 @@
 // LU with partial pivoting + solve for FP32 systems of order 8 < n <= 16: two rows per
-// lane, eight lanes per system, four systems per warp.
+// lane, eight lanes per system, four systems per warp; the plain and the interleaved
+// batched layouts.
 //
 // The register-row scheme of the TDLS CooperativeLUpp solver (TDLS API,
 // "solver_static.hpp File Reference", Detailed Description: rows held in registers,
@@ -150,15 +151,32 @@ __device__ __forceinline__ void store_rhs(float* p, const float (&b)[RT]) {
 
 // RT: right-hand-side tier (0: factor only). FULL: n == 16 and nrhs == RT (no guards).
 // W32: 32-byte row accesses of A (FULL row-major with a 32-byte aligned A).
-template <int RT, int LAYOUT, bool FULL, bool W32>
-__global__ void __launch_bounds__(kThreads, RT == 0 ? 8 : (RT <= 4 ? 7 : 6))
+// IL: the interleaved batched layout (TDLS API, "solver_static.hpp File Reference": element
+// e of system s at base_s[e * ilv], base_s = (s / ilv) * ilv * size + s % ilv, for A, B and
+// ipiv; info one entry per system). When the block's sixteen systems fill whole 16-byte
+// groups of one AoSoA block (ilv a multiple of 16, not the batch's ragged tail) they are
+// staged through shared memory with 16-byte accesses, each holding one element of four
+// systems; otherwise every element is read and written on its own.
+template <int RT, int LAYOUT, bool FULL, bool W32, bool IL>
+__global__ void __launch_bounds__(kThreads, RT == 0 ? 8 : (RT <= 4 && !IL ? 7 : 6))
 lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* __restrict__ B,
-                int32_t* __restrict__ ipiv, int32_t* __restrict__ info) {
+                int32_t* __restrict__ ipiv, int32_t* __restrict__ info, int64_t ilv) {
   constexpr bool kSolve = RT > 0;
   constexpr int RB = kSolve ? RT : 1;
   constexpr int WP = (NT + RB + 3) / 4 * 4;   // published row: A part, then B part
   __shared__ __align__(16) float prow[kWarps][GPW][2][WP];
   __shared__ __align__(16) float xbuf[kWarps][GPW][2][(RB + 3) / 4 * 4];
+  // staging of an interleaved block: row r of the block's system j at j*SA + r*PA (A) and
+  // j*SB + r*PB (B). Row pitches of 16-byte multiples let a lane move its row with 16-byte
+  // accesses (PA = 20 words: eight consecutive rows hit distinct banks); the system strides
+  // are 4 words off a multiple of 32 so that the element-wise transposition from and to the
+  // 16-byte global vectors (one element of four systems each) spreads over the banks.
+  constexpr int SPC = kWarps * GPW;          // systems of a thread block
+  constexpr int PA = NT + 4, PB = (RB + 3) / 4 * 4;
+  constexpr int SA = NT * PA + 4, SB = NT * PB + 4;
+  __shared__ __align__(16) float st_a[IL ? SPC * SA : 4];
+  __shared__ __align__(16) float st_b[IL ? SPC * SB : 4];
+  __shared__ int32_t st_p[IL ? SPC * NT : 1];
 
   const int n = FULL ? NT : n_;
   const int nrhs = FULL ? RT : nrhs_;
@@ -170,6 +188,46 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
   const bool valid = s < batch;
   const int64_t sA = s * n * n;
   const int64_t sB = s * n * nrhs;
+  // interleaved: the system's first element of A, B and ipiv (element stride ilv)
+  const int64_t blk = IL ? s / ilv : 0;
+  const int64_t sl = IL ? s - blk * ilv : 0;
+  const int64_t eA = IL ? blk * ilv * n * n + sl : 0;
+  const int64_t eB = IL ? blk * ilv * n * nrhs + sl : 0;
+  const int64_t s_first = static_cast<int64_t>(blockIdx.x) * SPC;
+  const bool staged = IL && ilv % SPC == 0 && s_first + SPC <= batch;   // uniform per block
+  const int jl = warp * GPW + g;              // this group's system in the block
+  const int64_t blk0 = IL ? s_first / ilv : 0;
+  const int64_t sl0 = IL ? s_first - blk0 * ilv : 0;
+  if (staged) {
+    constexpr int PER = SPC / 4;              // 16-byte vectors per element
+    const float* Ab = A + blk0 * ilv * n * n + sl0;
+    for (int idx = threadIdx.x; idx < n * n * PER; idx += kThreads) {
+      const int e = idx / PER, q = idx - e * PER;
+      const int r = LAYOUT == kRowMajor ? e / n : e % n;
+      const int c = LAYOUT == kRowMajor ? e % n : e / n;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(Ab + static_cast<int64_t>(e) * ilv + q * 4));
+      float* d = st_a + (q * 4) * SA + r * PA + c;
+      d[0] = v.x;
+      d[SA] = v.y;
+      d[2 * SA] = v.z;
+      d[3 * SA] = v.w;
+    }
+    if constexpr (kSolve) {
+      const float* Bb = B + blk0 * ilv * n * nrhs + sl0;
+      for (int idx = threadIdx.x; idx < n * nrhs * PER; idx += kThreads) {
+        const int e = idx / PER, q = idx - e * PER;
+        const int r = LAYOUT == kRowMajor ? e / nrhs : e % n;
+        const int c = LAYOUT == kRowMajor ? e % nrhs : e / n;
+        const float4 v = __ldg(reinterpret_cast<const float4*>(Bb + static_cast<int64_t>(e) * ilv + q * 4));
+        float* d = st_b + (q * 4) * SB + r * PB + c;
+        d[0] = v.x;
+        d[SB] = v.y;
+        d[2 * SB] = v.z;
+        d[3 * SB] = v.w;
+      }
+    }
+    __syncthreads();
+  }
 
   float a[R][NT];
   float b[R][RB];
@@ -184,8 +242,35 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
     const bool row_ok = valid && (FULL || pos[j] < n);
     okm[j] = row_ok ? 0xFFFFFFFFu : 0u;
     const int row = pos[j];
-    if (row_ok) {
-      if constexpr (LAYOUT == kRowMajor && FULL) {
+    if (row_ok && staged) {
+      const float* ra = st_a + jl * SA + row * PA;
+      const float* rb = st_b + jl * SB + row * PB;
+      if constexpr (FULL) {
+#pragma unroll
+        for (int c = 0; c < NT; c += 4) {
+          const float4 v = ld4(ra + c);
+          a[j][c] = v.x; a[j][c + 1] = v.y; a[j][c + 2] = v.z; a[j][c + 3] = v.w;
+        }
+        if constexpr (kSolve) ld_rhs_shared<RT>(rb, b[j]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NT; ++c) a[j][c] = c < n ? ra[c] : 0.f;
+#pragma unroll
+        for (int c = 0; c < RT; ++c) b[j][c] = c < nrhs ? rb[c] : 0.f;
+      }
+    } else if (row_ok && IL) {
+#pragma unroll
+      for (int c = 0; c < NT; ++c)
+        a[j][c] = (FULL || c < n)
+                      ? A[eA + (LAYOUT == kRowMajor ? row * n + c : c * n + row) * ilv]
+                      : 0.f;
+#pragma unroll
+      for (int c = 0; c < RT; ++c)
+        b[j][c] = (FULL || c < nrhs)
+                      ? B[eB + (LAYOUT == kRowMajor ? row * nrhs + c : c * n + row) * ilv]
+                      : 0.f;
+    } else if (row_ok) {
+      if constexpr (LAYOUT == kRowMajor && FULL && !IL) {
         const float* pa = A + sA + row * NT;
         if constexpr (W32) {
           ld8(pa, &a[j][0]);
@@ -348,18 +433,79 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
     }
   }
 
-  if (!valid) return;
   if (fm != 0) {   // the contract: X is zero where info != 0
 #pragma unroll
     for (int j = 0; j < R; ++j)
 #pragma unroll
       for (int c = 0; c < RB; ++c) b[j][c] = 0.f;
   }
+  if (staged) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (!okm[j]) continue;
+      const int row = pos[j];
+      float* ra = st_a + jl * SA + row * PA;
+      float* rb = st_b + jl * SB + row * PB;
+      if constexpr (FULL) {
+#pragma unroll
+        for (int c = 0; c < NT; c += 4) st4(ra + c, a[j][c], a[j][c + 1], a[j][c + 2], a[j][c + 3]);
+        if constexpr (kSolve) store_rhs<RT>(rb, b[j]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NT; ++c)
+          if (c < n) ra[c] = a[j][c];
+#pragma unroll
+        for (int c = 0; c < RT; ++c)
+          if (c < nrhs) rb[c] = b[j][c];
+      }
+      st_p[jl * NT + row] = ip[j];
+    }
+    if (t == 0) info[s] = fm ? __ffs(static_cast<int>(fm)) : 0;
+    __syncthreads();
+    constexpr int PER = SPC / 4;
+    float* Ab = A + blk0 * ilv * n * n + sl0;
+    for (int idx = threadIdx.x; idx < n * n * PER; idx += kThreads) {
+      const int e = idx / PER, q = idx - e * PER;
+      const int r = LAYOUT == kRowMajor ? e / n : e % n;
+      const int c = LAYOUT == kRowMajor ? e % n : e / n;
+      const float* d = st_a + (q * 4) * SA + r * PA + c;
+      st4(Ab + static_cast<int64_t>(e) * ilv + q * 4, d[0], d[SA], d[2 * SA], d[3 * SA]);
+    }
+    if constexpr (kSolve) {
+      float* Bb = B + blk0 * ilv * n * nrhs + sl0;
+      for (int idx = threadIdx.x; idx < n * nrhs * PER; idx += kThreads) {
+        const int e = idx / PER, q = idx - e * PER;
+        const int r = LAYOUT == kRowMajor ? e / nrhs : e % n;
+        const int c = LAYOUT == kRowMajor ? e % nrhs : e / n;
+        const float* d = st_b + (q * 4) * SB + r * PB + c;
+        st4(Bb + static_cast<int64_t>(e) * ilv + q * 4, d[0], d[SB], d[2 * SB], d[3 * SB]);
+      }
+    }
+    int32_t* Pb = ipiv + blk0 * ilv * n + sl0;
+    for (int idx = threadIdx.x; idx < n * PER; idx += kThreads) {
+      const int k = idx / PER, q = idx - k * PER;
+      *reinterpret_cast<int4*>(Pb + static_cast<int64_t>(k) * ilv + q * 4) =
+          make_int4(st_p[(q * 4) * NT + k], st_p[(q * 4 + 1) * NT + k],
+                    st_p[(q * 4 + 2) * NT + k], st_p[(q * 4 + 3) * NT + k]);
+    }
+    return;
+  }
+  if (!valid) return;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
     if (!okm[j]) continue;
     const int row = pos[j];   // the final position
-    if constexpr (LAYOUT == kRowMajor && FULL) {
+    if constexpr (IL) {
+#pragma unroll
+      for (int c = 0; c < NT; ++c)
+        if (FULL || c < n) A[eA + (LAYOUT == kRowMajor ? row * n + c : c * n + row) * ilv] = a[j][c];
+#pragma unroll
+      for (int c = 0; c < RT; ++c)
+        if (FULL || c < nrhs)
+          B[eB + (LAYOUT == kRowMajor ? row * nrhs + c : c * n + row) * ilv] = b[j][c];
+      ipiv[blk * ilv * n + sl + static_cast<int64_t>(row) * ilv] = ip[j];
+      continue;
+    } else if constexpr (LAYOUT == kRowMajor && FULL) {
       float* pa = A + sA + row * NT;
       if constexpr (W32) {
         st8(pa, &a[j][0]);
@@ -383,44 +529,52 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
 }
 
 template <int RT, int LAYOUT>
-cudaError_t launch_tier(int n, int nrhs, int64_t batch, float* A, float* B, int32_t* ipiv,
-                        int32_t* info, cudaStream_t stream) {
+cudaError_t launch_tier(int n, int nrhs, int64_t batch, int64_t ilv, float* A, float* B,
+                        int32_t* ipiv, int32_t* info, cudaStream_t stream) {
   constexpr int per_block = kWarps * GPW;
   const int64_t blocks = (batch + per_block - 1) / per_block;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const unsigned nb = static_cast<unsigned>(blocks);
-  if (n == NT && nrhs == RT) {
-    if (LAYOUT == kRowMajor && reinterpret_cast<uintptr_t>(A) % 32 == 0)
-      lu_rows2_kernel<RT, LAYOUT, true, true><<<nb, kThreads, 0, stream>>>(n, nrhs, batch, A, B,
-                                                                           ipiv, info);
+  const bool full = n == NT && nrhs == RT;
+  if (ilv > 1) {
+    if (full)
+      lu_rows2_kernel<RT, LAYOUT, true, false, true><<<nb, kThreads, 0, stream>>>(
+          n, nrhs, batch, A, B, ipiv, info, ilv);
     else
-      lu_rows2_kernel<RT, LAYOUT, true, false><<<nb, kThreads, 0, stream>>>(n, nrhs, batch, A, B,
-                                                                            ipiv, info);
+      lu_rows2_kernel<RT, LAYOUT, false, false, true><<<nb, kThreads, 0, stream>>>(
+          n, nrhs, batch, A, B, ipiv, info, ilv);
+  } else if (full) {
+    if (LAYOUT == kRowMajor && reinterpret_cast<uintptr_t>(A) % 32 == 0)
+      lu_rows2_kernel<RT, LAYOUT, true, true, false><<<nb, kThreads, 0, stream>>>(
+          n, nrhs, batch, A, B, ipiv, info, 1);
+    else
+      lu_rows2_kernel<RT, LAYOUT, true, false, false><<<nb, kThreads, 0, stream>>>(
+          n, nrhs, batch, A, B, ipiv, info, 1);
   } else {
-    lu_rows2_kernel<RT, LAYOUT, false, false><<<nb, kThreads, 0, stream>>>(n, nrhs, batch, A, B,
-                                                                           ipiv, info);
+    lu_rows2_kernel<RT, LAYOUT, false, false, false><<<nb, kThreads, 0, stream>>>(
+        n, nrhs, batch, A, B, ipiv, info, 1);
   }
   return cudaGetLastError();
 }
 
 template <int LAYOUT>
-cudaError_t launch_layout(int n, int nrhs, int64_t batch, float* A, float* B, int32_t* ipiv,
-                          int32_t* info, cudaStream_t stream) {
-  if (nrhs == 0) return launch_tier<0, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
-  if (nrhs <= 1) return launch_tier<1, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
-  if (nrhs <= 2) return launch_tier<2, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
-  if (nrhs <= 4) return launch_tier<4, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
-  return launch_tier<8, LAYOUT>(n, nrhs, batch, A, B, ipiv, info, stream);
+cudaError_t launch_layout(int n, int nrhs, int64_t batch, int64_t ilv, float* A, float* B,
+                          int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  if (nrhs == 0) return launch_tier<0, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (nrhs <= 1) return launch_tier<1, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (nrhs <= 2) return launch_tier<2, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  if (nrhs <= 4) return launch_tier<4, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  return launch_tier<8, LAYOUT>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_lu_rows2(int layout, int n, int nrhs, int64_t batch, float* A, float* B,
-                            int32_t* ipiv, int32_t* info, cudaStream_t stream) {
-  if (n <= G || n > NT || nrhs < 0 || nrhs > 8) return cudaErrorInvalidValue;
+                            int32_t* ipiv, int32_t* info, cudaStream_t stream, int64_t ilv) {
+  if (n <= G || n > NT || nrhs < 0 || nrhs > 8 || ilv < 1) return cudaErrorInvalidValue;
   if (layout == kRowMajor)
-    return launch_layout<kRowMajor>(n, nrhs, batch, A, B, ipiv, info, stream);
-  return launch_layout<kColMajor>(n, nrhs, batch, A, B, ipiv, info, stream);
+    return launch_layout<kRowMajor>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+  return launch_layout<kColMajor>(n, nrhs, batch, ilv, A, B, ipiv, info, stream);
 }
 
 }  // namespace bsolve
