@@ -29,11 +29,68 @@ struct Tri {
   __host__ __device__ static constexpr int at(int i, int j) { return i * (i + 1) / 2 + j; }
 };
 
+// n contiguous elements at p to d (or d to p): 32-byte pieces where whole when W32 (FP64,
+// strips and x 32-byte aligned), then 16-byte pieces when VEC (the address then 16-byte
+// aligned by construction), the rest element by element; nothing at or past p[n] is
+// touched.
+template <typename T, bool VEC, bool W32>
+__device__ __forceinline__ void ld_n(const T* p, T* d, int n) {
+  constexpr int VW = 16 / sizeof(T);
+  const int n32 = (W32 && sizeof(T) == 8) ? n / 4 : 0;   // 32-byte pieces (FP64)
+  const int nv = VEC ? (n - 4 * n32) / VW : 0;
+#pragma unroll
+  for (int q = 0; q < n32; ++q) {
+    double* o = reinterpret_cast<double*>(d) + 4 * q;
+    asm volatile("ld.global.v4.f64 {%0,%1,%2,%3}, [%4];"
+                 : "=d"(o[0]), "=d"(o[1]), "=d"(o[2]), "=d"(o[3])
+                 : "l"(reinterpret_cast<const double*>(p) + 4 * q));
+  }
+  const T* pv = p + 4 * n32;
+  T* dv = d + 4 * n32;
+#pragma unroll
+  for (int q = 0; q < nv; ++q) {
+    if constexpr (sizeof(T) == 8) {
+      const double2 v = *reinterpret_cast<const double2*>(pv + q * VW);
+      dv[q * VW] = v.x; dv[q * VW + 1] = v.y;
+    } else {
+      const float4 v = *reinterpret_cast<const float4*>(pv + q * VW);
+      dv[q * VW] = v.x; dv[q * VW + 1] = v.y; dv[q * VW + 2] = v.z; dv[q * VW + 3] = v.w;
+    }
+  }
+#pragma unroll
+  for (int j = 4 * n32 + nv * VW; j < n; ++j) d[j] = p[j];
+}
+template <typename T, bool VEC, bool W32>
+__device__ __forceinline__ void st_n(T* p, const T* d, int n) {
+  constexpr int VW = 16 / sizeof(T);
+  const int n32 = (W32 && sizeof(T) == 8) ? n / 4 : 0;
+  const int nv = VEC ? (n - 4 * n32) / VW : 0;
+#pragma unroll
+  for (int q = 0; q < n32; ++q) {
+    const double* o = reinterpret_cast<const double*>(d) + 4 * q;
+    asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(reinterpret_cast<double*>(p) + 4 * q),
+                 "d"(o[0]), "d"(o[1]), "d"(o[2]), "d"(o[3])
+                 : "memory");
+  }
+  T* pv = p + 4 * n32;
+  const T* dv = d + 4 * n32;
+#pragma unroll
+  for (int q = 0; q < nv; ++q) {
+    if constexpr (sizeof(T) == 8)
+      *reinterpret_cast<double2*>(pv + q * VW) = make_double2(dv[q * VW], dv[q * VW + 1]);
+    else
+      *reinterpret_cast<float4*>(pv + q * VW) =
+          make_float4(dv[q * VW], dv[q * VW + 1], dv[q * VW + 2], dv[q * VW + 3]);
+  }
+#pragma unroll
+  for (int j = 4 * n32 + nv * VW; j < n; ++j) p[j] = d[j];
+}
+
 // MODE: kFused (factor + solve, the forward solve riding on the factor sweep),
 // kFactor (strips only), kSolve (strips already factored, read only).
 enum Mode : int { kFused = 0, kFactor = 1, kSolve = 2 };
 
-template <typename T, int BS, int MODE>
+template <typename T, int BS, int MODE, bool W32>
 __global__ void __launch_bounds__(kThreads)
 bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad,
             int32_t* __restrict__ info) {
@@ -41,6 +98,10 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
   constexpr bool kFactors = MODE != kSolve;   // computes F_k, E_k
   constexpr bool kSolves = MODE != kFactor;   // computes y, x
   using Tr = Tri<BS>;
+  // every row of a strip, the diagonal block's columns and every block of x start on a
+  // 16-byte boundary when a block row is a whole number of 16-byte pieces (the bases are
+  // 16-byte aligned)
+  constexpr bool VEC = (BS * sizeof(T)) % 16 == 0;
   const int64_t s = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if (s >= batch) return;
   T* S = strips + s * static_cast<int64_t>(nbr) * BS * W;
@@ -57,15 +118,10 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
     T* strip = S + static_cast<int64_t>(k) * BS * W;
     T Sm[Tr::kSize];
     T z[BS];
-    if constexpr (kSolves) {
-#pragma unroll
-      for (int i = 0; i < BS; ++i) z[i] = x[k * BS + i];
-    }
+    if constexpr (kSolves) ld_n<T, VEC, W32>(x + k * BS, z, BS);
     if constexpr (kFactors) {
 #pragma unroll
-      for (int i = 0; i < BS; ++i)
-#pragma unroll
-        for (int j = 0; j <= i; ++j) Sm[Tr::at(i, j)] = strip[i * W + BS + j];
+      for (int i = 0; i < BS; ++i) ld_n<T, VEC, W32>(strip + i * W + BS, &Sm[Tr::at(i, 0)], i + 1);
     }
     if (k > 0) {
       T E[BS][BS];
@@ -73,18 +129,18 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
         // E_k = L_k F_{k-1}^{-T}, row by row
 #pragma unroll
         for (int a = 0; a < BS; ++a) {
+          T Lrow[BS];
+          ld_n<T, VEC, W32>(strip + a * W, Lrow, BS);
 #pragma unroll
           for (int j = 0; j < BS; ++j) {
-            T acc = strip[a * W + j];
+            T acc = Lrow[j];
 #pragma unroll
             for (int m = 0; m < j; ++m) acc = fma_rn<T>(-E[a][m], F[Tr::at(j, m)], acc);
             E[a][j] = acc * Fr[j];
           }
         }
 #pragma unroll
-        for (int a = 0; a < BS; ++a)
-#pragma unroll
-          for (int j = 0; j < BS; ++j) strip[a * W + j] = E[a][j];
+        for (int a = 0; a < BS; ++a) st_n<T, VEC, W32>(strip + a * W, E[a], BS);
         // S_k = D_k - E_k E_k^T (lower)
 #pragma unroll
         for (int i = 0; i < BS; ++i)
@@ -97,9 +153,7 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
           }
       } else {
 #pragma unroll
-        for (int a = 0; a < BS; ++a)
-#pragma unroll
-          for (int j = 0; j < BS; ++j) E[a][j] = strip[a * W + j];
+        for (int a = 0; a < BS; ++a) ld_n<T, VEC, W32>(strip + a * W, E[a], BS);
       }
       if constexpr (kSolves) {
 #pragma unroll
@@ -114,10 +168,12 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
 #pragma unroll
       for (int c = 0; c < BS; ++c) {
         const T d = Sm[Tr::at(c, c)];
-        if (!failed && !(d > T(0))) {
-          failed = true;
-          inf = k * BS + c + 1;
-        }
+        // branch-free, so that the whole knot stays one block of straight-line code and
+        // the compiler can overlap one column's square root and reciprocal with the
+        // previous column's independent updates
+        const bool bad = !(d > T(0));
+        inf = (!failed && bad) ? k * BS + c + 1 : inf;
+        failed = failed || bad;
         const T l = sqrt_rn<T>(d);
         const T r = rcp_rn<T>(l);
         Sm[Tr::at(c, c)] = l;
@@ -134,14 +190,10 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
       }
       if (failed) break;
 #pragma unroll
-      for (int i = 0; i < BS; ++i)
-#pragma unroll
-        for (int j = 0; j <= i; ++j) strip[i * W + BS + j] = Sm[Tr::at(i, j)];
+      for (int i = 0; i < BS; ++i) st_n<T, VEC, W32>(strip + i * W + BS, &Sm[Tr::at(i, 0)], i + 1);
     } else {
 #pragma unroll
-      for (int i = 0; i < BS; ++i)
-#pragma unroll
-        for (int j = 0; j <= i; ++j) Sm[Tr::at(i, j)] = strip[i * W + BS + j];
+      for (int i = 0; i < BS; ++i) ld_n<T, VEC, W32>(strip + i * W + BS, &Sm[Tr::at(i, 0)], i + 1);
 #pragma unroll
       for (int c = 0; c < BS; ++c) Fr[c] = rcp_rn<T>(Sm[Tr::at(c, c)]);
     }
@@ -154,8 +206,7 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
         for (int m = 0; m < j; ++m) acc = fma_rn<T>(-Sm[Tr::at(j, m)], y[m], acc);
         y[j] = acc * Fr[j];
       }
-#pragma unroll
-      for (int j = 0; j < BS; ++j) x[k * BS + j] = y[j];
+      st_n<T, VEC, W32>(x + k * BS, y, BS);
     }
     if constexpr (kFactors) {
 #pragma unroll
@@ -177,19 +228,20 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
     for (int k = nbr - 1; k >= 0; --k) {
       const T* strip = S + static_cast<int64_t>(k) * BS * W;
       T w[BS];
-#pragma unroll
-      for (int i = 0; i < BS; ++i) w[i] = x[k * BS + i];
+      ld_n<T, VEC, W32>(x + k * BS, w, BS);
       if (k < nbr - 1) {
+        // each w[m] takes its updates in increasing i, row i of E_{k+1} at a time
         const T* nstrip = strip + BS * W;
 #pragma unroll
-        for (int m = 0; m < BS; ++m)
+        for (int i = 0; i < BS; ++i) {
+          T er[BS];
+          ld_n<T, VEC, W32>(nstrip + i * W, er, BS);
 #pragma unroll
-          for (int i = 0; i < BS; ++i) w[m] = fma_rn<T>(-nstrip[i * W + m], xn[i], w[m]);
+          for (int m = 0; m < BS; ++m) w[m] = fma_rn<T>(-er[m], xn[i], w[m]);
+        }
       }
 #pragma unroll
-      for (int i = 0; i < BS; ++i)
-#pragma unroll
-        for (int j = 0; j <= i; ++j) F[Tr::at(i, j)] = strip[i * W + BS + j];
+      for (int i = 0; i < BS; ++i) ld_n<T, VEC, W32>(strip + i * W + BS, &F[Tr::at(i, 0)], i + 1);
       T xk[BS];
 #pragma unroll
       for (int j = BS - 1; j >= 0; --j) {
@@ -198,11 +250,9 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
         for (int m = j + 1; m < BS; ++m) acc = fma_rn<T>(-F[Tr::at(m, j)], xk[m], acc);
         xk[j] = acc * rcp_rn<T>(F[Tr::at(j, j)]);
       }
+      st_n<T, VEC, W32>(x + k * BS, xk, BS);
 #pragma unroll
-      for (int j = 0; j < BS; ++j) {
-        x[k * BS + j] = xk[j];
-        xn[j] = xk[j];
-      }
+      for (int j = 0; j < BS; ++j) xn[j] = xk[j];
     }
     if (MODE == kFused) info[s] = 0;
   }
@@ -213,8 +263,16 @@ cudaError_t launch_bs(int nbr, int64_t batch, T* strips, T* xpad, int32_t* info,
                       cudaStream_t stream) {
   const int64_t blocks = (batch + kThreads - 1) / kThreads;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  bdsv_kernel<T, BS, MODE><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      nbr, batch, strips, xpad, info);
+  // 32-byte accesses for FP64 block rows of whole 32-byte pieces when both bases allow
+  const bool w32 = sizeof(T) == 8 && (BS * sizeof(T)) % 32 == 0 &&
+                   reinterpret_cast<uintptr_t>(strips) % 32 == 0 &&
+                   (xpad == nullptr || reinterpret_cast<uintptr_t>(xpad) % 32 == 0);
+  if (w32)
+    bdsv_kernel<T, BS, MODE, true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        nbr, batch, strips, xpad, info);
+  else
+    bdsv_kernel<T, BS, MODE, false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        nbr, batch, strips, xpad, info);
   return cudaGetLastError();
 }
 
