@@ -33,6 +33,10 @@ struct Tri {
 // strips and x 32-byte aligned), then 16-byte pieces when VEC (the address then 16-byte
 // aligned by construction), the rest element by element; nothing at or past p[n] is
 // touched.
+struct __align__(32) D4 {
+  double v[4];
+};
+
 template <typename T, bool VEC, bool W32>
 __device__ __forceinline__ void ld_n(const T* p, T* d, int n) {
   constexpr int VW = 16 / sizeof(T);
@@ -40,10 +44,9 @@ __device__ __forceinline__ void ld_n(const T* p, T* d, int n) {
   const int nv = VEC ? (n - 4 * n32) / VW : 0;
 #pragma unroll
   for (int q = 0; q < n32; ++q) {
+    const D4 v = reinterpret_cast<const D4*>(p)[q];
     double* o = reinterpret_cast<double*>(d) + 4 * q;
-    asm volatile("ld.global.v4.f64 {%0,%1,%2,%3}, [%4];"
-                 : "=d"(o[0]), "=d"(o[1]), "=d"(o[2]), "=d"(o[3])
-                 : "l"(reinterpret_cast<const double*>(p) + 4 * q));
+    o[0] = v.v[0]; o[1] = v.v[1]; o[2] = v.v[2]; o[3] = v.v[3];
   }
   const T* pv = p + 4 * n32;
   T* dv = d + 4 * n32;
@@ -68,9 +71,9 @@ __device__ __forceinline__ void st_n(T* p, const T* d, int n) {
 #pragma unroll
   for (int q = 0; q < n32; ++q) {
     const double* o = reinterpret_cast<const double*>(d) + 4 * q;
-    asm volatile("st.global.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(reinterpret_cast<double*>(p) + 4 * q),
-                 "d"(o[0]), "d"(o[1]), "d"(o[2]), "d"(o[3])
-                 : "memory");
+    D4 v;
+    v.v[0] = o[0]; v.v[1] = o[1]; v.v[2] = o[2]; v.v[3] = o[3];
+    reinterpret_cast<D4*>(p)[q] = v;
   }
   T* pv = p + 4 * n32;
   const T* dv = d + 4 * n32;
@@ -264,7 +267,9 @@ cudaError_t launch_bs(int nbr, int64_t batch, T* strips, T* xpad, int32_t* info,
   const int64_t blocks = (batch + kThreads - 1) / kThreads;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   // 32-byte accesses for FP64 block rows of whole 32-byte pieces when both bases allow
-  const bool w32 = sizeof(T) == 8 && (BS * sizeof(T)) % 32 == 0 &&
+  // (not for the factor sweep alone: there they cost registers it has none left for, and
+  // measured slower)
+  const bool w32 = MODE != kFactor && sizeof(T) == 8 && (BS * sizeof(T)) % 32 == 0 &&
                    reinterpret_cast<uintptr_t>(strips) % 32 == 0 &&
                    (xpad == nullptr || reinterpret_cast<uintptr_t>(xpad) % 32 == 0);
   if (w32)
