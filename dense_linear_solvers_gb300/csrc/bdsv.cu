@@ -21,7 +21,7 @@
 namespace bsolve {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 32;
 
 template <int BS>
 struct Tri {
