@@ -110,3 +110,50 @@ def test_two_streams_at_once():
     torch.cuda.synchronize()
     for x, r in zip((A2, B2, ip2, in2, C2, D2, ci2), ref):
         assert _same_bits(x, r)
+
+
+def test_cluster_interleaved_and_split_calls_graph_replay():
+    """The cluster Cholesky (a launch with cluster dimensions), the interleaved two-rows LU
+    and the row-major reading's two launches capture and replay like the eager calls."""
+    rng = np.random.default_rng(5151)
+    G = rng.standard_normal((6, 160, 160))
+    C0 = _dev(G @ np.swapaxes(G, 1, 2) + 160 * np.eye(160))
+    D0 = _dev(rng.standard_normal((6, 3, 160)))                     # column-major B
+    w, A0, B0, _, _ = _lu_buffers("lu_f32_n16", 96)
+    Ai0 = _dev(W.interleave(A0.cpu().numpy(), 32))
+    Bi0 = _dev(W.interleave(B0.cpu().numpy(), 32))
+    R0 = _dev(rng.standard_normal((40, 16, 16)).astype(np.float32))
+    S0 = _dev(rng.standard_normal((40, 16, 9)).astype(np.float32))
+
+    def calls(bufs, stream=None):
+        C, D, ci, Ai, Bi, ipi, ini, R, S, ipr, inr = bufs
+        bs.bs_potrf_potrs_batched(C, D, ci, COL_MAJOR, bs.BS_LOWER, stream=stream)
+        bs.bs_getrf_getrs_batched_ex(Ai, Bi, ipi, ini, w.layout, interleave=32,
+                                     shape=(96, 16, 4), stream=stream)
+        bs.bs_getrf_getrs_batched_ex(R, S, ipr, inr, bs.BS_ROW_MAJOR, transposed_factor=1,
+                                     stream=stream)
+
+    def fresh():
+        return [C0.clone(), D0.clone(), torch.zeros(6, dtype=torch.int32, device="cuda"),
+                Ai0.clone(), Bi0.clone(), torch.zeros(96 * 16, dtype=torch.int32, device="cuda"),
+                torch.zeros(96, dtype=torch.int32, device="cuda"), R0.clone(), S0.clone(),
+                torch.zeros((40, 16), dtype=torch.int32, device="cuda"),
+                torch.zeros(40, dtype=torch.int32, device="cuda")]
+
+    ref = fresh()
+    calls(ref)
+    torch.cuda.synchronize()
+    gb = fresh()
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls(gb, stream=s)
+    src = fresh()
+    for _ in range(2):
+        for dst, x in zip(gb, src):
+            dst.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        for x, r in zip(gb, ref):
+            assert _same_bits(x, r)
