@@ -122,9 +122,13 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
     T Sm[Tr::kSize];
     T z[BS];
     if constexpr (kSolves) ld_n<T, VEC, W32>(x + k * BS, z, BS);
+    // D_k's lower triangle (at the knot's start for k = 0, after E_k otherwise: fewer live
+    // registers while E_k is formed)
     if constexpr (kFactors) {
+      if (k == 0) {
 #pragma unroll
-      for (int i = 0; i < BS; ++i) ld_n<T, VEC, W32>(strip + i * W + BS, &Sm[Tr::at(i, 0)], i + 1);
+        for (int i = 0; i < BS; ++i) ld_n<T, VEC, W32>(strip + i * W + BS, &Sm[Tr::at(i, 0)], i + 1);
+      }
     }
     if (k > 0) {
       T E[BS][BS];
@@ -144,6 +148,8 @@ bdsv_kernel(int nbr, int64_t batch, T* __restrict__ strips, T* __restrict__ xpad
         }
 #pragma unroll
         for (int a = 0; a < BS; ++a) st_n<T, VEC, W32>(strip + a * W, E[a], BS);
+#pragma unroll
+        for (int i = 0; i < BS; ++i) ld_n<T, VEC, W32>(strip + i * W + BS, &Sm[Tr::at(i, 0)], i + 1);
         // S_k = D_k - E_k E_k^T (lower)
 #pragma unroll
         for (int i = 0; i < BS; ++i)
@@ -267,9 +273,7 @@ cudaError_t launch_bs(int nbr, int64_t batch, T* strips, T* xpad, int32_t* info,
   const int64_t blocks = (batch + kThreads - 1) / kThreads;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   // 32-byte accesses for FP64 block rows of whole 32-byte pieces when both bases allow
-  // (not for the factor sweep alone: there they cost registers it has none left for, and
-  // measured slower)
-  const bool w32 = MODE != kFactor && sizeof(T) == 8 && (BS * sizeof(T)) % 32 == 0 &&
+  const bool w32 = sizeof(T) == 8 && (BS * sizeof(T)) % 32 == 0 &&
                    reinterpret_cast<uintptr_t>(strips) % 32 == 0 &&
                    (xpad == nullptr || reinterpret_cast<uintptr_t>(xpad) % 32 == 0);
   if (w32)
