@@ -94,15 +94,39 @@ __device__ __forceinline__ void ldg_row(const T* __restrict__ p, T (&r)[N]) {
   }
 }
 
+// A row of N elements in 32-byte pieces (sm_100 and later; p 32-byte aligned, the factor
+// read only).
+template <typename T, int N>
+__device__ __forceinline__ void ldg_row32(const T* __restrict__ p, T (&r)[N]) {
+  static_assert((N * sizeof(T)) % 32 == 0, "whole 32-byte pieces");
+#pragma unroll
+  for (int j = 0; j < N; j += 32 / sizeof(T)) {
+    if constexpr (sizeof(T) == 4) {
+      asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=f"(r[j]), "=f"(r[j + 1]), "=f"(r[j + 2]), "=f"(r[j + 3]), "=f"(r[j + 4]),
+            "=f"(r[j + 5]), "=f"(r[j + 6]), "=f"(r[j + 7])
+          : "l"(p + j));
+    } else {
+      asm("ld.global.nc.v4.f64 {%0,%1,%2,%3}, [%4];"
+          : "=d"(r[j]), "=d"(r[j + 1]), "=d"(r[j + 2]), "=d"(r[j + 3])
+          : "l"(p + j));
+    }
+  }
+}
+
+// layouts: bit 0 the factor's storage order, bit 1 B's, bit 2 (FULL instances) the factor
+// 32-byte aligned, its rows then read in 32-byte pieces
 template <typename T, int NT, int R, int RT, int KIND, bool FULL>
 __global__ void __launch_bounds__(kThreads)
-solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restrict__ M,
+solve_reg_kernel(int n_, int nrhs_, int layouts_, int64_t batch, const T* __restrict__ M,
                  const int32_t* __restrict__ ipiv, T* __restrict__ B,
                  const int32_t* __restrict__ zinfo) {
   constexpr int G = NT / R;
   constexpr int GPW = 32 / G;
   const int n = FULL ? NT : n_;
   const int nrhs = FULL ? RT : nrhs_;
+  const int layouts = layouts_ & 3;
+  const bool w32 = FULL && (layouts_ & 4) != 0;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane / G;
@@ -148,7 +172,12 @@ solve_reg_kernel(int n_, int nrhs_, int layouts, int64_t batch, const T* __restr
     if (ok[q]) {
       if (FULL && ((KIND == kSolveLu && (layouts & 1) == kRowMajor) ||
                    (KIND == kSolveLuT && (layouts & 1) == kColMajor))) {
-        ldg_row<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
+        if constexpr ((NT * sizeof(T)) % 32 == 0) {
+          if (w32) ldg_row32<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
+          else ldg_row<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
+        } else {
+          ldg_row<T, NT>(Ms + static_cast<int64_t>(pq) * NT, v[q]);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -271,7 +300,9 @@ cudaError_t launch_reg_tier(int layout, int n, int nrhs, int64_t batch, const T*
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const unsigned nb = static_cast<unsigned>(blocks);
   if (n == NT && nrhs == RT)
-    solve_reg_kernel<T, NT, R, RT, KIND, true><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo);
+    solve_reg_kernel<T, NT, R, RT, KIND, true><<<nb, kThreads, 0, stream>>>(
+        n, nrhs, layout | (reinterpret_cast<uintptr_t>(M) % 32 == 0 ? 4 : 0), batch, M, ipiv, B,
+        zinfo);
   else
     solve_reg_kernel<T, NT, R, RT, KIND, false><<<nb, kThreads, 0, stream>>>(n, nrhs, layout, batch, M, ipiv, B, zinfo);
   return cudaGetLastError();
