@@ -153,15 +153,20 @@ __device__ __forceinline__ void store_rhs(float* p, const float (&b)[RT]) {
 // W32: 32-byte row accesses of A (FULL row-major with a 32-byte aligned A).
 // IL: the interleaved batched layout (TDLS API, "solver_static.hpp File Reference": element
 // e of system s at base_s[e * ilv], base_s = (s / ilv) * ilv * size + s % ilv, for A, B and
-// ipiv; info one entry per system). When the block's sixteen systems fill whole 16-byte
-// groups of one AoSoA block (ilv a multiple of 16, not the batch's ragged tail) they are
-// staged through shared memory with 16-byte accesses, each holding one element of four
-// systems; otherwise every element is read and written on its own.
-template <int RT, int LAYOUT, bool FULL, bool W32, bool IL>
-__global__ void __launch_bounds__(kThreads, RT == 0 ? 8 : (RT <= 4 && !IL ? 7 : 6))
+// ipiv; info one entry per system). kIlStaged: every block's sixteen systems fill whole
+// 16-byte groups of one AoSoA block (ilv a multiple of 16, the batch's ragged tail left to
+// a kIlElem launch) and are staged through shared memory with 16-byte accesses, each
+// holding one element of four systems; kIlElem: every element is read and written on its
+// own. first_block: the index of the launch's first block in the batch (a tail launch
+// starts past the staged blocks).
+constexpr int kIlNone = 0, kIlElem = 1, kIlStaged = 2;
+template <int RT, int LAYOUT, bool FULL, bool W32, int IL>
+__global__ void __launch_bounds__(kThreads, RT == 0 ? 8 : (RT <= 4 && IL != kIlElem ? 7 : 6))
 lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* __restrict__ B,
-                int32_t* __restrict__ ipiv, int32_t* __restrict__ info, int64_t ilv) {
+                int32_t* __restrict__ ipiv, int32_t* __restrict__ info, int64_t ilv,
+                int64_t first_block) {
   constexpr bool kSolve = RT > 0;
+  constexpr bool staged = IL == kIlStaged;
   constexpr int RB = kSolve ? RT : 1;
   constexpr int WP = (NT + RB + 3) / 4 * 4;   // published row: A part, then B part
   __shared__ __align__(16) float prow[kWarps][GPW][2][WP];
@@ -174,9 +179,9 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
   constexpr int SPC = kWarps * GPW;          // systems of a thread block
   constexpr int PA = NT + 4, PB = (RB + 3) / 4 * 4;
   constexpr int SA = NT * PA + 4, SB = NT * PB + 4;
-  __shared__ __align__(16) float st_a[IL ? SPC * SA : 4];
-  __shared__ __align__(16) float st_b[IL ? SPC * SB : 4];
-  __shared__ int32_t st_p[IL ? SPC * NT : 1];
+  __shared__ __align__(16) float st_a[staged ? SPC * SA : 4];
+  __shared__ __align__(16) float st_b[staged ? SPC * SB : 4];
+  __shared__ int32_t st_p[staged ? SPC * NT : 1];
 
   const int n = FULL ? NT : n_;
   const int nrhs = FULL ? RT : nrhs_;
@@ -184,8 +189,9 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
   const int warp = threadIdx.x >> 5;
   const int g = lane / G;
   const int t = lane % G;
-  const int64_t s = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * GPW + g;
-  const bool valid = s < batch;
+  const int64_t bidx = first_block + blockIdx.x;
+  const int64_t s = (bidx * kWarps + warp) * GPW + g;
+  const bool valid = staged || s < batch;
   const int64_t sA = s * n * n;
   const int64_t sB = s * n * nrhs;
   // interleaved: the system's first element of A, B and ipiv (element stride ilv)
@@ -193,32 +199,53 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
   const int64_t sl = IL ? s - blk * ilv : 0;
   const int64_t eA = IL ? blk * ilv * n * n + sl : 0;
   const int64_t eB = IL ? blk * ilv * n * nrhs + sl : 0;
-  const int64_t s_first = static_cast<int64_t>(blockIdx.x) * SPC;
-  const bool staged = IL && ilv % SPC == 0 && s_first + SPC <= batch;   // uniform per block
+  const int64_t s_first = bidx * SPC;
   const int jl = warp * GPW + g;              // this group's system in the block
-  const int64_t blk0 = IL ? s_first / ilv : 0;
-  const int64_t sl0 = IL ? s_first - blk0 * ilv : 0;
-  if (staged) {
-    constexpr int PER = SPC / 4;              // 16-byte vectors per element
-    const float* Ab = A + blk0 * ilv * n * n + sl0;
-    for (int idx = threadIdx.x; idx < n * n * PER; idx += kThreads) {
-      const int e = idx / PER, q = idx - e * PER;
-      const int r = LAYOUT == kRowMajor ? e / n : e % n;
-      const int c = LAYOUT == kRowMajor ? e % n : e / n;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(Ab + static_cast<int64_t>(e) * ilv + q * 4));
-      float* d = st_a + (q * 4) * SA + r * PA + c;
-      d[0] = v.x;
-      d[SA] = v.y;
-      d[2 * SA] = v.z;
-      d[3 * SA] = v.w;
+  const int64_t blk0 = staged ? s_first / ilv : 0;
+  const int64_t sl0 = staged ? s_first - blk0 * ilv : 0;
+  // staging passes: thread i moves the 16-byte vector q = i % PER (systems 4q..4q+3 of the
+  // block) of elements i / PER + EPI * pass
+  constexpr int PER = SPC / 4;                // 16-byte vectors per element
+  constexpr int EPI = kThreads / PER;         // elements per pass
+  const int q = threadIdx.x % PER, e0 = threadIdx.x / PER;
+  if constexpr (staged) {
+    const float* Ab = A + blk0 * ilv * n * n + sl0 + q * 4 + e0 * ilv;
+    const int64_t step = EPI * ilv;
+    if constexpr (FULL) {
+      constexpr int kPassA = NT * NT / EPI;
+      float4 v[kPassA];
+#pragma unroll
+      for (int it = 0; it < kPassA; ++it) v[it] = __ldg(reinterpret_cast<const float4*>(Ab + it * step));
+#pragma unroll
+      for (int it = 0; it < kPassA; ++it) {
+        const int e = e0 + it * EPI;
+        const int r = LAYOUT == kRowMajor ? e / NT : e % NT;
+        const int c = LAYOUT == kRowMajor ? e % NT : e / NT;
+        float* d = st_a + (q * 4) * SA + r * PA + c;
+        d[0] = v[it].x;
+        d[SA] = v[it].y;
+        d[2 * SA] = v[it].z;
+        d[3 * SA] = v[it].w;
+      }
+    } else {
+      for (int e = e0, it = 0; e < n * n; e += EPI, ++it) {
+        const int r = LAYOUT == kRowMajor ? e / n : e % n;
+        const int c = LAYOUT == kRowMajor ? e % n : e / n;
+        const float4 v = __ldg(reinterpret_cast<const float4*>(Ab + it * step));
+        float* d = st_a + (q * 4) * SA + r * PA + c;
+        d[0] = v.x;
+        d[SA] = v.y;
+        d[2 * SA] = v.z;
+        d[3 * SA] = v.w;
+      }
     }
     if constexpr (kSolve) {
-      const float* Bb = B + blk0 * ilv * n * nrhs + sl0;
-      for (int idx = threadIdx.x; idx < n * nrhs * PER; idx += kThreads) {
-        const int e = idx / PER, q = idx - e * PER;
+      const float* Bb = B + blk0 * ilv * n * nrhs + sl0 + q * 4 + e0 * ilv;
+#pragma unroll
+      for (int e = e0, it = 0; e < n * nrhs; e += EPI, ++it) {
         const int r = LAYOUT == kRowMajor ? e / nrhs : e % n;
         const int c = LAYOUT == kRowMajor ? e % nrhs : e / n;
-        const float4 v = __ldg(reinterpret_cast<const float4*>(Bb + static_cast<int64_t>(e) * ilv + q * 4));
+        const float4 v = __ldg(reinterpret_cast<const float4*>(Bb + it * step));
         float* d = st_b + (q * 4) * SB + r * PB + c;
         d[0] = v.x;
         d[SB] = v.y;
@@ -258,7 +285,7 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
 #pragma unroll
         for (int c = 0; c < RT; ++c) b[j][c] = c < nrhs ? rb[c] : 0.f;
       }
-    } else if (row_ok && IL) {
+    } else if (row_ok && IL == kIlElem) {
 #pragma unroll
       for (int c = 0; c < NT; ++c)
         a[j][c] = (FULL || c < n)
@@ -270,7 +297,7 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
                       ? B[eB + (LAYOUT == kRowMajor ? row * nrhs + c : c * n + row) * ilv]
                       : 0.f;
     } else if (row_ok) {
-      if constexpr (LAYOUT == kRowMajor && FULL && !IL) {
+      if constexpr (LAYOUT == kRowMajor && FULL && IL == kIlNone) {
         const float* pa = A + sA + row * NT;
         if constexpr (W32) {
           ld8(pa, &a[j][0]);
@@ -439,7 +466,7 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
 #pragma unroll
       for (int c = 0; c < RB; ++c) b[j][c] = 0.f;
   }
-  if (staged) {
+  if constexpr (staged) {
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       if (!okm[j]) continue;
@@ -462,32 +489,40 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
     }
     if (t == 0) info[s] = fm ? __ffs(static_cast<int>(fm)) : 0;
     __syncthreads();
-    constexpr int PER = SPC / 4;
-    float* Ab = A + blk0 * ilv * n * n + sl0;
-    for (int idx = threadIdx.x; idx < n * n * PER; idx += kThreads) {
-      const int e = idx / PER, q = idx - e * PER;
-      const int r = LAYOUT == kRowMajor ? e / n : e % n;
-      const int c = LAYOUT == kRowMajor ? e % n : e / n;
-      const float* d = st_a + (q * 4) * SA + r * PA + c;
-      st4(Ab + static_cast<int64_t>(e) * ilv + q * 4, d[0], d[SA], d[2 * SA], d[3 * SA]);
+    float* Ab = A + blk0 * ilv * n * n + sl0 + q * 4 + e0 * ilv;
+    const int64_t step = EPI * ilv;
+    if constexpr (FULL) {
+#pragma unroll
+      for (int it = 0; it < NT * NT / EPI; ++it) {
+        const int e = e0 + it * EPI;
+        const int r = LAYOUT == kRowMajor ? e / NT : e % NT;
+        const int c = LAYOUT == kRowMajor ? e % NT : e / NT;
+        const float* d = st_a + (q * 4) * SA + r * PA + c;
+        st4(Ab + it * step, d[0], d[SA], d[2 * SA], d[3 * SA]);
+      }
+    } else {
+      for (int e = e0, it = 0; e < n * n; e += EPI, ++it) {
+        const int r = LAYOUT == kRowMajor ? e / n : e % n;
+        const int c = LAYOUT == kRowMajor ? e % n : e / n;
+        const float* d = st_a + (q * 4) * SA + r * PA + c;
+        st4(Ab + it * step, d[0], d[SA], d[2 * SA], d[3 * SA]);
+      }
     }
     if constexpr (kSolve) {
-      float* Bb = B + blk0 * ilv * n * nrhs + sl0;
-      for (int idx = threadIdx.x; idx < n * nrhs * PER; idx += kThreads) {
-        const int e = idx / PER, q = idx - e * PER;
+      float* Bb = B + blk0 * ilv * n * nrhs + sl0 + q * 4 + e0 * ilv;
+#pragma unroll
+      for (int e = e0, it = 0; e < n * nrhs; e += EPI, ++it) {
         const int r = LAYOUT == kRowMajor ? e / nrhs : e % n;
         const int c = LAYOUT == kRowMajor ? e % nrhs : e / n;
         const float* d = st_b + (q * 4) * SB + r * PB + c;
-        st4(Bb + static_cast<int64_t>(e) * ilv + q * 4, d[0], d[SB], d[2 * SB], d[3 * SB]);
+        st4(Bb + it * step, d[0], d[SB], d[2 * SB], d[3 * SB]);
       }
     }
-    int32_t* Pb = ipiv + blk0 * ilv * n + sl0;
-    for (int idx = threadIdx.x; idx < n * PER; idx += kThreads) {
-      const int k = idx / PER, q = idx - k * PER;
-      *reinterpret_cast<int4*>(Pb + static_cast<int64_t>(k) * ilv + q * 4) =
+    int32_t* Pb = ipiv + blk0 * ilv * n + sl0 + q * 4;
+    for (int k = e0; k < n; k += EPI)
+      *reinterpret_cast<int4*>(Pb + static_cast<int64_t>(k) * ilv) =
           make_int4(st_p[(q * 4) * NT + k], st_p[(q * 4 + 1) * NT + k],
                     st_p[(q * 4 + 2) * NT + k], st_p[(q * 4 + 3) * NT + k]);
-    }
     return;
   }
   if (!valid) return;
@@ -495,7 +530,7 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
   for (int j = 0; j < R; ++j) {
     if (!okm[j]) continue;
     const int row = pos[j];   // the final position
-    if constexpr (IL) {
+    if constexpr (IL == kIlElem) {
 #pragma unroll
       for (int c = 0; c < NT; ++c)
         if (FULL || c < n) A[eA + (LAYOUT == kRowMajor ? row * n + c : c * n + row) * ilv] = a[j][c];
@@ -528,6 +563,31 @@ lu_rows2_kernel(int n_, int nrhs_, int64_t batch, float* __restrict__ A, float* 
   if (t == 0) info[s] = fm ? __ffs(static_cast<int>(fm)) : 0;
 }
 
+// The staged instance takes whole interleaved blocks with the shared memory it needs for
+// seven blocks per SM; the element-wise one the ragged tail (or every block when ilv is
+// not a multiple of sixteen).
+template <int RT, int LAYOUT, bool FULL>
+cudaError_t launch_il(unsigned nb, int n, int nrhs, int64_t batch, int64_t ilv, float* A,
+                      float* B, int32_t* ipiv, int32_t* info, cudaStream_t stream) {
+  constexpr int per_block = kWarps * GPW;
+  const int64_t whole = ilv % per_block == 0 ? batch / per_block : 0;
+  if (whole > 0) {
+    auto kern = lu_rows2_kernel<RT, LAYOUT, FULL, false, kIlStaged>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(whole), kThreads, 0, stream>>>(n, nrhs, batch, A, B, ipiv,
+                                                                info, ilv, 0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (nb > whole)
+    lu_rows2_kernel<RT, LAYOUT, FULL, false, kIlElem>
+        <<<static_cast<unsigned>(nb - whole), kThreads, 0, stream>>>(n, nrhs, batch, A, B,
+                                                                    ipiv, info, ilv, whole);
+  return cudaGetLastError();
+}
+
 template <int RT, int LAYOUT>
 cudaError_t launch_tier(int n, int nrhs, int64_t batch, int64_t ilv, float* A, float* B,
                         int32_t* ipiv, int32_t* info, cudaStream_t stream) {
@@ -537,22 +597,18 @@ cudaError_t launch_tier(int n, int nrhs, int64_t batch, int64_t ilv, float* A, f
   const unsigned nb = static_cast<unsigned>(blocks);
   const bool full = n == NT && nrhs == RT;
   if (ilv > 1) {
-    if (full)
-      lu_rows2_kernel<RT, LAYOUT, true, false, true><<<nb, kThreads, 0, stream>>>(
-          n, nrhs, batch, A, B, ipiv, info, ilv);
-    else
-      lu_rows2_kernel<RT, LAYOUT, false, false, true><<<nb, kThreads, 0, stream>>>(
-          n, nrhs, batch, A, B, ipiv, info, ilv);
+    if (full) return launch_il<RT, LAYOUT, true>(nb, n, nrhs, batch, ilv, A, B, ipiv, info, stream);
+    return launch_il<RT, LAYOUT, false>(nb, n, nrhs, batch, ilv, A, B, ipiv, info, stream);
   } else if (full) {
     if (LAYOUT == kRowMajor && reinterpret_cast<uintptr_t>(A) % 32 == 0)
-      lu_rows2_kernel<RT, LAYOUT, true, true, false><<<nb, kThreads, 0, stream>>>(
-          n, nrhs, batch, A, B, ipiv, info, 1);
+      lu_rows2_kernel<RT, LAYOUT, true, true, kIlNone><<<nb, kThreads, 0, stream>>>(
+          n, nrhs, batch, A, B, ipiv, info, 1, 0);
     else
-      lu_rows2_kernel<RT, LAYOUT, true, false, false><<<nb, kThreads, 0, stream>>>(
-          n, nrhs, batch, A, B, ipiv, info, 1);
+      lu_rows2_kernel<RT, LAYOUT, true, false, kIlNone><<<nb, kThreads, 0, stream>>>(
+          n, nrhs, batch, A, B, ipiv, info, 1, 0);
   } else {
-    lu_rows2_kernel<RT, LAYOUT, false, false, false><<<nb, kThreads, 0, stream>>>(
-        n, nrhs, batch, A, B, ipiv, info, 1);
+    lu_rows2_kernel<RT, LAYOUT, false, false, kIlNone><<<nb, kThreads, 0, stream>>>(
+        n, nrhs, batch, A, B, ipiv, info, 1, 0);
   }
   return cudaGetLastError();
 }

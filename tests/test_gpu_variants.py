@@ -183,14 +183,16 @@ def _il_case(rng, dtype, batch, n, nrhs, layout, spd=False):
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 @pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
 def test_interleaved_lu(dtype, layout):
-    """AoSoA (blocks of 2, 3 and 32, the last block ragged), SoA (W = batch) and SoA
+    """AoSoA (blocks of 2, 3, 16 and 32, the last block ragged), SoA (W = batch) and SoA
     with spare capacity, every tier of the register kernel and the one-CTA kernel,
-    against the oracle bit for bit; the slots past the batch are never written."""
+    against the oracle bit for bit; the slots past the batch are never written. Blocks of
+    16 and 32 take the staged path for whole groups of sixteen systems and the
+    element-wise one for the ragged rest."""
     from gen.workloads import deinterleave, interleave
     rng = np.random.default_rng(1616 + layout)
     batch = 45
     for n in (1, 2, 3, 5, 8, 13, 16, 17, 31, 32, 33, 40, 64, 65, 128):
-        for w in (2, 3, 32, batch, batch + 5):
+        for w in (2, 3, 16, 32, batch, batch + 5):
             nrhs = int(rng.integers(1, 9))
             A, B = _il_case(rng, dtype, batch, n, nrhs, layout)
             Af, Bf = interleave(A, w), interleave(B, w)
@@ -214,6 +216,47 @@ def test_interleaved_lu(dtype, layout):
             pads = np.isnan(interleave(np.zeros((batch, n)), w))
             assert np.all(ipg[:pads.size][pads] == SENT)
             assert np.array_equal(infg[clean], info_o[clean]) and infg[batch // 2] > 0
+
+
+@pytest.mark.parametrize("layout", [ROW_MAJOR, COL_MAJOR])
+@pytest.mark.parametrize("nrhs", [0, 1, 2, 3, 4, 8])
+def test_interleaved_lu_staged_blocks(layout, nrhs):
+    """FP32 n = 16 on AoSoA blocks of 16, 32 and 48 and on SoA: whole groups of sixteen
+    systems go through shared memory (the staged launch), the ragged rest element by
+    element (a second launch); every right-hand-side tier and getrf alone, against the
+    oracle bit for bit."""
+    from gen.workloads import deinterleave, interleave
+    rng = np.random.default_rng(1717 + 10 * nrhs + layout)
+    n, batch = 16, 16 * 6 + 5
+    for w in (16, 32, 48, batch):
+        A, B = _il_case(rng, np.float32, batch, n, max(nrhs, 1), layout)
+        A[7] = rng.integers(-2, 3, (n, n)).astype(np.float32)     # exact ties
+        Af, Bf = interleave(A, w), interleave(B, w)
+        tA = _dev(Af)
+        ipiv = torch.full((Af.size // n,), SENT, dtype=torch.int32, device="cuda")
+        info = torch.full((batch,), SENT, dtype=torch.int32, device="cuda")
+        if nrhs == 0:
+            Fo, ipo, info_o, tie = oracle.getrf_il(Af, n, batch, w, layout, nthreads=NT)
+            bs.bs_getrf_batched_ex(tA, ipiv, info, layout, interleave=w, shape=(batch, n))
+        else:
+            Fo, Xo, ipo, info_o, tie = oracle.getrf_getrs_il(Af, Bf, n, nrhs, batch, w, layout,
+                                                             nthreads=NT)
+            tB = _dev(Bf)
+            bs.bs_getrf_getrs_batched_ex(tA, tB, ipiv, info, layout, interleave=w,
+                                         shape=(batch, n, nrhs))
+            Xg = _host(tB)
+            assert np.array_equal(deinterleave(Xg, batch, w, B.shape[1:])[tie < 0],
+                                  deinterleave(Xo, batch, w, B.shape[1:])[tie < 0]), w
+        clean = tie < 0
+        assert clean.sum() >= batch - 3, w
+        Fg, ipg, infg = _host(tA), _host(ipiv), _host(info)
+        assert np.array_equal(deinterleave(Fg, batch, w, (n, n))[clean],
+                              deinterleave(Fo, batch, w, (n, n))[clean]), w
+        assert np.array_equal(deinterleave(ipg, batch, w, (n,))[clean],
+                              deinterleave(ipo, batch, w, (n,))[clean]), w
+        assert np.array_equal(infg[clean], info_o[clean]) and infg[batch // 2] > 0
+        pads = np.isnan(interleave(np.zeros((batch, n)), w))
+        assert np.all(ipg[:pads.size][pads] == SENT)
 
 
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
