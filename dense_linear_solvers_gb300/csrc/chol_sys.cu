@@ -62,32 +62,85 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
   T* const Ms = M + s * D;                          // this lane's system
   T* const Ys = Ms + TRI;                           // its right-hand sides, [i][c]
 
-  // load: warp w copies systems w, w+kWarps, ...; lanes walk the rows of a column, with
-  // asynchronous element copies so that every load of the block is in flight at once
-  for (int q = warp; q < kSys; q += kWarps) {
+  // Element e of system sys at As[e * ilv]: ilv = 1, the systems one after another (each
+  // warp copies whole systems, its lanes walking the rows of a column); otherwise the
+  // interleaved batched layout, where the block's sixteen systems hold each element side by
+  // side, so each half-warp copies one element of all sixteen (128 contiguous bytes in
+  // FP64 when they lie in one block of ilv). Asynchronous element copies keep every load
+  // of the block in flight at once.
+  auto sys_base = [&](int64_t sys, T* P, int size) {
+    const int64_t blk = IL ? sys / ilv : sys, sl = IL ? sys - blk * ilv : 0;
+    return P + blk * ilv * size + sl;
+  };
+  if constexpr (IL) {
+    // thread -> system tid % 16 and element slot tid / 16 of each pass (kSlots per pass);
+    // the lower triangle walked row by row (row i: columns 0..i), then B by rows
+    const int q = tid % kSys, e0 = tid / kSys;
     const int64_t sys = s0 + q;
     T* const Mq = M + q * D;
     if (sys < batch) {
-      // element e of system sys at As[e * ilv] (ilv = 1: the systems one after another;
-      // otherwise the interleaved batched layout, systems in blocks of ilv), likewise B
-      const int64_t blk = IL ? sys / ilv : sys, sl = IL ? sys - blk * ilv : 0;
-      const T* As = A + blk * ilv * n * n + sl;
-      const T* Bs = B + blk * ilv * n * nrhs + sl;
-      for (int j = 0; j < n; ++j)
-        for (int i = j + lane; i < n; i += 32)
-          cp_async_elem<T>(Mq + tri(i) + j,
-                           As + (alay == kColMajor ? j * n + i : i * n + j) * ilv);
-      for (int c = 0; c < nrhs; ++c)
-        for (int i = lane; i < n; i += 32)
-          cp_async_elem<T>(Mq + TRI + i * nrhs + c,
-                           Bs + (blay == kColMajor ? c * n + i : i * nrhs + c) * ilv);
+      const T* As = sys_base(sys, A, n * n);
+      const T* Bs = sys_base(sys, B, n * nrhs);
+      int i = 0, j = e0;
+      while (j > i) {
+        j -= i + 1;
+        ++i;
+      }
+      for (int t = e0; t < TRI; t += kSlots) {
+        cp_async_elem<T>(Mq + t, As + (alay == kColMajor ? j * n + i : i * n + j) * ilv);
+        j += kSlots;
+        while (j > i) {
+          j -= i + 1;
+          ++i;
+        }
+      }
+      for (int f = e0; f < n * nrhs; f += kSlots) {
+        const int i2 = f / nrhs, c = f - i2 * nrhs;
+        cp_async_elem<T>(Mq + TRI + f,
+                         Bs + (blay == kColMajor ? c * n + i2 : i2 * nrhs + c) * ilv);
+      }
     } else {
-      // a system past the end of the batch: an identity keeps its lanes finite
-      for (int e = lane; e < D; e += 32) Mq[e] = T(0);
-      __syncwarp();
-      for (int i = lane; i < n; i += 32) Mq[tri(i) + i] = T(1);
+      // a system past the end of the batch: an identity keeps its lanes finite (each
+      // element written once, by the thread that owns it)
+      int i = 0, j = e0;
+      while (j > i) {
+        j -= i + 1;
+        ++i;
+      }
+      for (int t = e0; t < TRI; t += kSlots) {
+        Mq[t] = i == j ? T(1) : T(0);
+        j += kSlots;
+        while (j > i) {
+          j -= i + 1;
+          ++i;
+        }
+      }
+      for (int e = TRI + e0; e < D; e += kSlots) Mq[e] = T(0);
     }
-    if (lane == 0) sinfo[q] = 0;
+    if (e0 == 0) sinfo[q] = 0;
+  } else {
+    for (int q = warp; q < kSys; q += kWarps) {
+      const int64_t sys = s0 + q;
+      T* const Mq = M + q * D;
+      if (sys < batch) {
+        const T* As = sys_base(sys, A, n * n);
+        const T* Bs = sys_base(sys, B, n * nrhs);
+        for (int j = 0; j < n; ++j)
+          for (int i = j + lane; i < n; i += 32)
+            cp_async_elem<T>(Mq + tri(i) + j,
+                             As + (alay == kColMajor ? j * n + i : i * n + j) * ilv);
+        for (int c = 0; c < nrhs; ++c)
+          for (int i = lane; i < n; i += 32)
+            cp_async_elem<T>(Mq + TRI + i * nrhs + c,
+                             Bs + (blay == kColMajor ? c * n + i : i * nrhs + c) * ilv);
+      } else {
+        // a system past the end of the batch: an identity keeps its lanes finite
+        for (int e = lane; e < D; e += 32) Mq[e] = T(0);
+        __syncwarp();
+        for (int i = lane; i < n; i += 32) Mq[tri(i) + i] = T(1);
+      }
+      if (lane == 0) sinfo[q] = 0;
+    }
   }
   cp_async_wait_all();
   __syncthreads();
@@ -180,23 +233,52 @@ chol_sys_kernel(int n, int nrhs, int layouts, int64_t batch, T* __restrict__ A,
     __syncthreads();
   }
 
-  // store: the lower triangle, X (zero for a failed system), info
-  for (int q = warp; q < kSys; q += kWarps) {
+  // store: the lower triangle, X (zero for a failed system), info; the same thread to
+  // element maps as the load
+  if constexpr (IL) {
+    const int q = tid % kSys, e0 = tid / kSys;
     const int64_t sys = s0 + q;
-    if (sys >= batch) continue;
-    const T* const Mq = M + q * D;
-    const int64_t blk = IL ? sys / ilv : sys, sl = IL ? sys - blk * ilv : 0;
-    T* As = A + blk * ilv * n * n + sl;
-    T* Bs = B + blk * ilv * n * nrhs + sl;
-    const bool failed = sinfo[q] != 0;
-    for (int j = 0; j < n; ++j)
-      for (int i = j + lane; i < n; i += 32)
-        As[(alay == kColMajor ? j * n + i : i * n + j) * ilv] = Mq[tri(i) + j];
-    for (int c = 0; c < nrhs; ++c)
-      for (int i = lane; i < n; i += 32)
-        Bs[(blay == kColMajor ? c * n + i : i * nrhs + c) * ilv] =
-            failed ? T(0) : Mq[TRI + i * nrhs + c];
-    if (lane == 0) info[sys] = sinfo[q];
+    if (sys < batch) {
+      const T* const Mq = M + q * D;
+      T* As = sys_base(sys, A, n * n);
+      T* Bs = sys_base(sys, B, n * nrhs);
+      const bool failed = sinfo[q] != 0;
+      int i = 0, j = e0;
+      while (j > i) {
+        j -= i + 1;
+        ++i;
+      }
+      for (int t = e0; t < TRI; t += kSlots) {
+        As[(alay == kColMajor ? j * n + i : i * n + j) * ilv] = Mq[t];
+        j += kSlots;
+        while (j > i) {
+          j -= i + 1;
+          ++i;
+        }
+      }
+      for (int f = e0; f < n * nrhs; f += kSlots) {
+        const int i2 = f / nrhs, c = f - i2 * nrhs;
+        Bs[(blay == kColMajor ? c * n + i2 : i2 * nrhs + c) * ilv] = failed ? T(0) : Mq[TRI + f];
+      }
+      if (e0 == 0) info[sys] = sinfo[q];
+    }
+  } else {
+    for (int q = warp; q < kSys; q += kWarps) {
+      const int64_t sys = s0 + q;
+      if (sys >= batch) continue;
+      const T* const Mq = M + q * D;
+      T* As = sys_base(sys, A, n * n);
+      T* Bs = sys_base(sys, B, n * nrhs);
+      const bool failed = sinfo[q] != 0;
+      for (int j = 0; j < n; ++j)
+        for (int i = j + lane; i < n; i += 32)
+          As[(alay == kColMajor ? j * n + i : i * n + j) * ilv] = Mq[tri(i) + j];
+      for (int c = 0; c < nrhs; ++c)
+        for (int i = lane; i < n; i += 32)
+          Bs[(blay == kColMajor ? c * n + i : i * nrhs + c) * ilv] =
+              failed ? T(0) : Mq[TRI + i * nrhs + c];
+      if (lane == 0) info[sys] = sinfo[q];
+    }
   }
 }
 
