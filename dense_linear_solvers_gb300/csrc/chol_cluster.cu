@@ -4,21 +4,30 @@
 // CTA), and the solve with the stored factor, one CTA per system.
 //
 // Factor: the lower triangle in 32 x 32 tiles; tile t = i(i+1)/2 + j of tile row i and
-// tile column j <= i lives in CTA t % 4, slot t / 4. Right-looking by tile columns k:
-//   1. the owner of tile (k,k) factors it with one warp (lane r holds row r in registers;
-//      column c: l_cc = sqrt(a_cc), r_c = 1/l_cc, l_rc = a_rc r_c, then
-//      a_rj -= l_rc l_jc for c < j <= r, the multipliers broadcast by shuffles);
+// tile column j <= i lives in CTA t % 4, slot t / 4. Right-looking by tile columns k. The
+// FP64 pipe charges a warp instruction whatever its active lanes and each SM sub-partition
+// has its own, so the serial work of a step (the diagonal tile, the panel, the next tile
+// column) runs on teams of four warps, one per sub-partition, that split each tile's
+// columns (or rows) between them:
+//   1. the owner of tile (k,k) factors it with a team (lane r holds row r of the tile in
+//      shared memory, warp u the columns j = u mod 4; column c: its warp takes
+//      l_cc = sqrt(a_cc), r_c = 1/l_cc and scales the column, the team synchronizes, then
+//      each warp applies the column to its own columns, a_rj -= l_rc l_jc for c < j <= r;
+//      the warp of column c+1 applies column c to it first and takes its square root at
+//      once, so the chain overlaps the team's remaining updates);
 //   2. cluster barrier; every CTA copies L_kk and the reciprocals out of the owner's
-//      shared memory (distributed shared memory loads) and scales its own tiles (i,k),
-//      i > k, one thread per row, column by column (l_rc = a_rc r_c, then
-//      a_rj -= l_rc l_jc for the tile's later columns);
-//   3. cluster barrier; every CTA applies the 32 updates of the panel to each of its
-//      trailing tiles (i,j), k < j <= i, element (r, c) taking a_rc -= l_rK l_cK in
-//      increasing K, one warp a tile: first the tiles of column k+1, then (look-ahead)
-//      warp 0 of the owner of tile (k+1,k+1) factors it while every other warp updates
-//      the remaining tiles. FP64 reads the panel tiles where they live (the other CTAs'
-//      through distributed-shared-memory loads: an FP64 update costs the pipe far more
-//      than its loads, and no staging buffer keeps two CTAs per SM); FP32 stages them.
+//      shared memory (distributed shared memory loads) and solves its own panel tiles
+//      (i,k), i > k, one team a tile, in the same column-split order (l_rc = a_rc r_c,
+//      then a_rj -= l_rc l_jc for the tile's later columns);
+//   3. cluster barrier; the tiles (i,k+1) of the next tile column take the panel's 32
+//      updates first, one team a tile (each warp eight rows), then (look-ahead) a team of
+//      the owner of tile (k+1,k+1) factors it while every other warp applies the panel to
+//      the remaining trailing tiles (i,j), k+1 < j <= i, one warp a tile, taken from a
+//      shared counter (the factoring team joins when it is done). Element (r, c) takes
+//      a_rc -= l_rK l_cK in increasing K. FP64 reads the panel tiles where they live (the
+//      other CTAs' through distributed-shared-memory loads: an FP64 update costs the pipe
+//      far more than its loads, and no staging buffer keeps two CTAs per SM); FP32 stages
+//      them.
 // Every element thus takes the oracle's right-looking updates in increasing column order,
 // each one fused multiply-add, so the factor is the oracle's bit for bit. Orders that are
 // not a multiple of 32 are padded with identity rows and columns at the end: they come
@@ -51,6 +60,8 @@ constexpr int kMaxTiles = kMaxT * (kMaxT + 1) / 2;
 constexpr int kMaxSlots = (kMaxTiles + CL - 1) / CL;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kTeam = 4;                 // warps of a team: one per SM sub-partition
+constexpr int kTeams = kWarps / kTeam;
 constexpr int kTile = TS * TP;  // elements of one staged tile
 
 __host__ __device__ constexpr int tile_index(int i, int j) { return i * (i + 1) / 2 + j; }
@@ -73,7 +84,7 @@ constexpr bool kStagePanel = sizeof(T) == 4;
 template <typename T>
 size_t cluster_smem_bytes() {
   // owned tiles, a staged copy of L_kk, the staged panel (FP32), the diagonal
-  // reciprocals (own and staged), the first failure
+  // reciprocals (own and staged), the first failure and the trailing-tile counter
   return static_cast<size_t>(kMaxSlots + 1 + (kStagePanel<T> ? kMaxT : 0)) * kTile * sizeof(T) +
          2 * TS * sizeof(T) + 16;
 }
@@ -117,35 +128,114 @@ __device__ __forceinline__ void tile_coords(int t, int& i, int& j) {
   j = t - tile_index(i, 0);
 }
 
-// Factor the diagonal tile at `a` (pitch TP, in shared memory) with one warp; lane r
-// owns row r. k is the tile column (for the global index of a failing minor), n the
-// order. The tile stays in shared memory (the warp's rows would take 64 registers a
-// thread in FP64): column c is scaled by the lanes below it, then each lane applies the
-// column to the rest of its row; one __syncwarp orders each phase.
+// Barrier of the four warps of team `team` (named barriers 1 and 2, immediate ids; 0 is
+// __syncthreads).
+static_assert(kTeams == 2, "one named barrier per team");
+__device__ __forceinline__ void team_sync(int team) {
+  if (team == 0)
+    asm volatile("bar.sync 1, %0;" ::"n"(kTeam * 32) : "memory");
+  else
+    asm volatile("bar.sync 2, %0;" ::"n"(kTeam * 32) : "memory");
+}
+
+// The first column j > c that warp u of a team owns (j = u mod 4).
+__device__ __forceinline__ int first_col(int c, int u) { return c + 1 + ((u - c - 1) & (kTeam - 1)); }
+
+// Factor the diagonal tile at `a` (pitch TP, in shared memory) with a team of four warps
+// (this thread's warp is u of team `team`); lane r owns row r, warp u the columns j = u
+// mod 4. k is the tile column (for the global index of a failing minor), n the order.
+// Every element (r, j), j <= r, takes a_rj -= l_rc l_jc for c = 0, 1, ... in order, one
+// fused multiply-add each, and the diagonal and column steps of the CPU oracle.
 template <typename T>
-__device__ void potrf_tile(T* a, T* rc, int k, int n, int* fail) {
+__device__ void potrf_tile_team(T* a, T* rc, int k, int n, int* fail, int team, int u) {
   const int r = threadIdx.x & 31;
   int first = 0x7FFFFFFF;
-#pragma unroll 1
-  for (int c = 0; c < TS; ++c) {
+  // column c's pivot and scaling, by the warp that owns column c
+  auto pivot = [&](int c) {
     const T d = a[c * TP + c];
     if (!(d > T(0)) && k * TS + c < n && first == 0x7FFFFFFF) first = k * TS + c + 1;
     const T l = sqrt_rn<T>(d);
     const T rr = rcp_rn<T>(l);
-    __syncwarp();
+    __syncwarp();   // every lane has read a_cc
     if (r == c) a[c * TP + c] = l;
     if (r > c) a[r * TP + c] = a[r * TP + c] * rr;
     if (r == 0) rc[c] = rr;
-    __syncwarp();
-    if (r > c) {
-      const T lrc = a[r * TP + c];
+  };
+  if (u == 0) pivot(0);
+  team_sync(team);
 #pragma unroll 1
-      for (int j = c + 1; j <= r; ++j)
-        a[r * TP + j] = fma_rn<T>(-lrc, a[j * TP + c], a[r * TP + j]);
+  for (int c = 0; c < TS; ++c) {
+    const T lrc = a[r * TP + c];
+    const int cn = c + 1;
+    // look-ahead: the warp of column c+1 applies column c to it and takes its pivot first
+    if (cn < TS && (cn & (kTeam - 1)) == u) {
+      if (r >= cn) a[r * TP + cn] = fma_rn<T>(-lrc, a[cn * TP + c], a[r * TP + cn]);
+      __syncwarp();
+      pivot(cn);
     }
-    __syncwarp();
+#pragma unroll 1
+    for (int j = first_col(c, u); j < TS; j += kTeam) {
+      if (j == cn) continue;
+      if (r >= j) a[r * TP + j] = fma_rn<T>(-lrc, a[j * TP + c], a[r * TP + j]);
+    }
+    team_sync(team);   // column c+1 is scaled; column c applied everywhere
   }
-  if (r == 0 && first < *fail) *fail = first;
+  if (r == 0 && first != 0x7FFFFFFF) atomicMin(fail, first);
+}
+
+// Solve a panel tile in place with a team: row r of the tile (lane r) becomes
+// L_rk = A_rk L_kk^-T, column by column (l_rc = a_rc r_c, then a_rj -= l_rc (L_kk)_jc for
+// the later columns j of warp u's residue), the oracle's order for every element. `lkk` is
+// the factored diagonal tile (pitch TP), `rcs` its diagonal reciprocals.
+template <typename T>
+__device__ void panel_tile_team(T* a, const T* lkk, const T* rcs, int team, int u) {
+  const int r = threadIdx.x & 31;
+  T* const row = a + r * TP;
+  if (u == 0) row[0] = row[0] * rcs[0];
+  team_sync(team);
+#pragma unroll 1
+  for (int c = 0; c < TS; ++c) {
+    const T lrc = row[c];
+    const int cn = c + 1;
+    if (cn < TS && (cn & (kTeam - 1)) == u) {
+      row[cn] = fma_rn<T>(-lrc, lkk[cn * TP + c], row[cn]);
+      row[cn] = row[cn] * rcs[cn];
+    }
+#pragma unroll 1
+    for (int j = first_col(c, u); j < TS; j += kTeam) {
+      if (j == cn) continue;
+      row[j] = fma_rn<T>(-lrc, lkk[j * TP + c], row[j]);
+    }
+    team_sync(team);
+  }
+}
+
+// One warp of a team applies the 32 updates of a panel to rows 8u..8u+7 of a 32 x 32 tile
+// (a_rc -= l_iK l_jK for K = 0..31 in order); lane = a 2 x 4 block.
+template <typename T>
+__device__ __forceinline__ void update_rows_team(T* a, const T* li, const T* lj, int lane, int u) {
+  const int r0 = 8 * u + (lane >> 3) * 2, c0 = (lane & 7) * 4;
+  T acc[2][4];
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) acc[p][v] = a[(r0 + p) * TP + c0 + v];
+#pragma unroll 4
+  for (int K = 0; K < TS; ++K) {
+    T x[2], y[4];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) x[p] = li[(r0 + p) * TP + K];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) y[v] = lj[(c0 + v) * TP + K];
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) acc[p][v] = fma_rn<T>(-x[p], y[v], acc[p][v]);
+  }
+#pragma unroll
+  for (int p = 0; p < 2; ++p)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) a[(r0 + p) * TP + c0 + v] = acc[p][v];
 }
 
 template <typename T>
@@ -162,6 +252,7 @@ chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* 
                                                                 // this CTA factored
   T* const rcs = rc + TS;                  // staged reciprocals of L_kk
   int* const fail = reinterpret_cast<int*>(rcs + TS);
+  int* const next = fail + 1;              // the trailing-tile counter of a step
   const int tid = threadIdx.x;
   const int nt = (n + TS - 1) / TS;
   const int ntiles = nt * (nt + 1) / 2;
@@ -198,8 +289,9 @@ chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* 
       return cluster.map_shared_rank(tiles + (t / CL) * kTile, t % CL);
     }
   };
+  const int team = warp / kTeam, u = warp % kTeam;   // warp u of a team runs on sub-partition u
   // tile (0,0) lives in rank 0, slot 0
-  if (rank == 0 && warp == 0) potrf_tile<T>(tiles, rc, 0, n, fail);
+  if (rank == 0 && team == 0) potrf_tile_team<T>(tiles, rc, 0, n, fail, team, u);
   for (int k = 0; k < nt; ++k) {
     const int tkk = tile_index(k, k);
     cluster.sync();   // L_kk is factored
@@ -211,24 +303,13 @@ chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* 
       if (tid < TS) rcs[tid] = rsrc[tid];
     }
     __syncthreads();
-    // the owned panel tiles (i,k), i > k: one thread per row
+    // the owned panel tiles (i,k), i > k: one team a tile
     {
-      const T* Lkk = lkk;
       int q = 0;   // ordinal of the owned panel tile
       for (int i = k + 1; i < nt; ++i) {
         const int t = tile_index(i, k);
         if (t % CL != rank) continue;
-        if (q * TS <= tid && tid < (q + 1) * TS) {
-          // the row stays in shared memory (32 FP64 values would crowd the registers)
-          T* row = tiles + (t / CL) * kTile + (tid - q * TS) * TP;
-#pragma unroll 1
-          for (int c = 0; c < TS; ++c) {
-            const T l = row[c] * rcs[c];
-            row[c] = l;
-#pragma unroll 4
-            for (int j = c + 1; j < TS; ++j) row[j] = fma_rn<T>(-l, Lkk[j * TP + c], row[j]);
-          }
-        }
+        if (q % kTeams == team) panel_tile_team<T>(tiles + (t / CL) * kTile, lkk, rcs, team, u);
         ++q;
       }
     }
@@ -242,35 +323,40 @@ chol_cluster_kernel(int n, int alay, int64_t batch, T* __restrict__ A, int32_t* 
       }
       __syncthreads();
     }
-    // look-ahead: the next tile column first (one warp a tile) ...
+    // look-ahead: the next tile column first (one team a tile, eight rows a warp) ...
     if (k + 1 < nt) {
       int q = 0;
       for (int i = k + 1; i < nt; ++i) {
         const int t = tile_index(i, k + 1);
         if (t % CL != rank) continue;
-        if (q % kWarps == warp)
-          update_tile<T>(tiles + (t / CL) * kTile, panel_tile(i, k), panel_tile(k + 1, k), lane);
+        if (q % kTeams == team)
+          update_rows_team<T>(tiles + (t / CL) * kTile, panel_tile(i, k), panel_tile(k + 1, k),
+                              lane, u);
         ++q;
       }
     }
+    if (tid == 0) *next = 0;
     __syncthreads();
-    // ... then the next diagonal tile is factored by warp 0 of its owner while every other
-    // warp applies this panel to the rest of the trailing tiles
+    // ... then a team of the next diagonal tile's owner factors it while the other warps
+    // apply this panel to the remaining trailing tiles, one warp a tile from the counter
+    // (the team takes tiles too once it is done)
     const int tn = tile_index(k + 1, k + 1);
-    const bool diag_here = k + 1 < nt && tn % CL == rank;
-    if (diag_here && warp == 0) {
-      potrf_tile<T>(tiles + (tn / CL) * kTile, rc, k + 1, n, fail);
-    } else {
-      const int nw = diag_here ? kWarps - 1 : kWarps;
-      const int wi = diag_here ? warp - 1 : warp;
-      int q = 0;
-      for (int t = rank; t < ntiles; t += CL) {
-        int i, j;
-        tile_coords(t, i, j);
-        if (j <= k + 1) continue;
-        if (q % nw == wi)
-          update_tile<T>(tiles + (t / CL) * kTile, panel_tile(i, k), panel_tile(j, k), lane);
-        ++q;
+    if (k + 1 < nt && tn % CL == rank && team == 0)
+      potrf_tile_team<T>(tiles + (tn / CL) * kTile, rc, k + 1, n, fail, team, u);
+    {
+      // the owned trailing tiles, in slot order: t = rank + CL * slot with column j > k + 1
+#pragma unroll 1
+      for (;;) {
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(next, 1);
+        idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
+        int t = rank, i = 0, j = 0, seen = -1;
+        for (; t < ntiles; t += CL) {
+          tile_coords(t, i, j);
+          if (j > k + 1 && ++seen == idx) break;
+        }
+        if (t >= ntiles) break;
+        update_tile<T>(tiles + (t / CL) * kTile, panel_tile(i, k), panel_tile(j, k), lane);
       }
     }
     __syncthreads();
