@@ -143,6 +143,23 @@ solve_reg_kernel(int n_, int nrhs_, int layouts_, int64_t batch, const T* __rest
     ok[q] = valid && (FULL || t + q * G < n);
     src[q] = t + q * G;
   }
+  // LU with row-major B in one pass: every lane loads its own rows of B (rows t + qG) with
+  // the factor and the swap sequence, and takes the permuted rows from the group's lanes by
+  // shuffles once the swaps are known, instead of a second round trip to memory that would
+  // wait on the swap sequence
+  constexpr bool kEarlyB = KIND == kSolveLu && FULL;
+  const bool early_b = kEarlyB && (layouts >> 1) == kRowMajor;
+  T bown[R][RT];
+  if (kEarlyB && early_b) {
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      if (ok[q]) ldg_row<T, RT>(Bs + static_cast<int64_t>(t + q * G) * RT, bown[q]);
+      else {
+#pragma unroll
+        for (int c = 0; c < RT; ++c) bown[q][c] = T(0);
+      }
+    }
+  }
   if (KIND != kSolveChol && valid) {
     // the swaps undone from the last, on the group's copy of the swap sequence
     int iv[NT];
@@ -206,6 +223,22 @@ solve_reg_kernel(int n_, int nrhs_, int layouts_, int64_t batch, const T* __rest
   T b[R][RT];
 #pragma unroll
   for (int q = 0; q < R; ++q) {
+    if (kEarlyB && early_b) {
+      // row src[q] sits in lane src[q] % G of the group, slot src[q] / G (every lane of the
+      // group joins the shuffles; rows past a partial last system are zeros, never used)
+      const int sl = src[q] % G, sq = src[q] / G;
+#pragma unroll
+      for (int c = 0; c < RT; ++c) {
+        T got = T(0);
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+          const T v_u = __shfl_sync(0xFFFFFFFFu, bown[u][c], sl, G);
+          got = sq == u ? v_u : got;
+        }
+        b[q][c] = ok[q] ? got : T(0);
+      }
+      continue;
+    }
     if (ok[q]) {
       // LU: the row the swaps bring to position pq; LuT: row pq (swapped on the way out)
       const int lrow = KIND == kSolveLuT ? t + q * G : src[q];
