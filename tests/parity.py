@@ -56,7 +56,7 @@ def gpu_bdsv(strips, xpad):
 
 def condition_numbers(A_logical):
     s = np.linalg.svd(np.asarray(A_logical, np.float64), compute_uv=False)
-    with np.errstate(divide="ignore"):
+    with np.errstate(divide="ignore", invalid="ignore"):   # a zero matrix: 0 / 0
         return np.where(s[:, -1] > 0, s[:, 0] / s[:, -1], np.inf)
 
 
